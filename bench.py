@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 MoE expert layer (libmoe.so).
+
+Workloads (all inputs seeded and synthetic, shapes of the pages' model:
+H=2048, 256 routed experts, top-8, one shared expert, I=512, int4 g64):
+  decode40     (default) one token at a time through a stack of 40 MoE layers
+               with RMSNorm + residual between layers; metric: HBM GB/s of the
+               bytes a token must stream (router + 9 experts per layer).
+  layer256     one layer, T=256
+  layer512zipf one layer, T=512, Zipf(1.1)-skewed routing
+  layer2048    one layer, T=2048
+  layer4096    one layer, T=4096
+  prefill32k   a 32768-token prompt in 4096-token chunks through 40 layers
+The prefill workloads report tokens/s.
+
+One JSON line is printed by rank 0.  ``--impl reference`` times the CPU
+oracle (the only reference this project has) on a bounded sample of the
+same workload.  Multi-GPU runs are independent replicas (one process per
+GPU, no collective on the data path): value = units of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+H, E, K_TOP, I_DIM, G = 2048, 256, 8, 512, 64
+EXPERT_BYTES = 3 * (H * I_DIM // 2) + 3 * 2 * 2 * (H * I_DIM // G)   # 1,769,472
+GATEUP_BYTES = 2 * (H * I_DIM // 2) + 2 * 2 * 2 * (H * I_DIM // G)   # 1,179,648
+ROUTER_BYTES = E * H * 4                                              # 2,097,152
+METRIC = "MoE-layer prefill tokens/s & % of roofline (T=256–32K); T=1 HBM GB/s"
+
+WORKLOADS = {
+    "decode40": dict(T=1, layers=40, chunk=1, zipf=False, centred=False,
+                     desc="T=1 decode through 40 MoE layers (H=2048, E=256, top-8 + 1 shared, I=512, int4 g64), "
+                          "RMSNorm + residual between layers, 64 distinct tokens cycled"),
+    "layer256": dict(T=256, layers=1, chunk=256, zipf=False, centred=False, desc="one MoE layer, T=256"),
+    "layer512zipf": dict(T=512, layers=1, chunk=512, zipf=True, centred=False,
+                         desc="one MoE layer, T=512, Zipf(1.1) expert-bias skew"),
+    "layer2048": dict(T=2048, layers=1, chunk=2048, zipf=False, centred=False, desc="one MoE layer, T=2048"),
+    "layer4096": dict(T=4096, layers=1, chunk=4096, zipf=False, centred=False, desc="one MoE layer, T=4096"),
+    "prefill32k": dict(T=32768, layers=40, chunk=4096, zipf=False, centred=True,
+                       desc="32768-token prompt, 8 chunks of 4096 through 40 MoE layers (centred weights), "
+                            "one fixed workspace"),
+}
+DEFAULT_STEPS = {"decode40": 2000, "layer256": 200, "layer512zipf": 200, "layer2048": 100, "layer4096": 50,
+                 "prefill32k": 3}
+DEFAULT_WARMUP = {"decode40": 50, "layer256": 10, "layer512zipf": 10, "layer2048": 5, "layer4096": 5,
+                  "prefill32k": 3}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--workload", default="decode40", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--experts", default="tc", choices=["tc", "simt"], help="grouped GEMM kernels")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    a = ap.parse_args()
+    if a.steps is None:
+        a.steps = DEFAULT_STEPS[a.workload] if a.impl == "ours" else 5
+    if a.warmup is None:
+        a.warmup = DEFAULT_WARMUP[a.workload] if a.impl == "ours" else 1
+    a.warmup = max(a.warmup, 3) if a.impl == "ours" else a.warmup
+    return a
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id(device):
+    """nvidia-smi id of a torch device (its UUID when torch exposes it)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device.index or 0)
+
+
+# ------------------------------------------------------------------ inputs
+
+def layer_weights(seed, layer, centred, device):
+    """Host-generated packed weights of one layer, copied to the device."""
+    import torch
+    import synthetic as syn
+    W = syn.experts(seed, E + 1, H, I_DIM, layer=layer, centred=centred)
+    W["router"] = syn.router(seed, E, H, layer=layer)
+    out = {}
+    for n, a in W.items():
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        elif a.dtype == np.uint32:
+            a = a.view(np.int32)
+        out[n] = torch.from_numpy(a).to(device)
+    return out
+
+
+def as_dev(a, device):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(device)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, wl, rank, world, device):
+    import torch
+    import __graft_entry__
+    import bit_grouped_expert_gb300 as moe
+    import synthetic as syn
+
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(device)
+    T, L, chunk = wl["T"], wl["layers"], wl["chunk"]
+    flags = moe.MOE_FLAG_SIMT_EXPERTS if args.experts == "simt" else 0
+    plan = moe.moe_plan(moe.make_config(H, E, K_TOP, I_DIM, 1, G), chunk, flags)
+    ws = torch.zeros(moe.moe_workspace_bytes(plan), dtype=torch.uint8, device=device)
+    moe.moe_workspace_init(plan, ws)
+    seed = args.seed + 1000 * rank
+    weights = [layer_weights(seed, l, wl["centred"], device) for l in range(L)]
+    cws = [moe.make_weights(w) for w in weights]
+    bias = as_dev(syn.zipf_bias(seed, E), device) if wl["zipf"] else None
+
+    n_in = 64 if T == 1 else 1
+    x_host = syn.activations(seed, max(T, n_in), H)
+    if T == 1:
+        tokens = as_dev(x_host[:n_in], device).reshape(n_in, 1, H)
+        x_in = torch.empty((1, H), dtype=torch.int16, device=device)
+    else:
+        x_in = as_dev(x_host, device)
+    r = torch.empty((chunk, H), dtype=torch.int16, device=device)
+    xn = torch.empty((chunk, H), dtype=torch.int16, device=device)
+    out = torch.empty((T, H), dtype=torch.int16, device=device)
+
+    stream = torch.cuda.Stream(device=device)
+    launches = [0]
+
+    def body():
+        launches[0] = 0
+        s = stream
+        for c0 in range(0, T, chunk):
+            if L == 1:
+                moe.moe_forward(plan, x_in[c0:c0 + chunk], None, chunk, cws[0], bias, out[c0:c0 + chunk], ws,
+                                stream=s)
+                launches[0] += moe.moe_last_launch_count()
+                continue
+            r.copy_(x_in[c0:c0 + chunk])
+            for l in range(L):
+                moe.moe_rmsnorm(r, chunk, H, 1e-6, xn, stream=s)
+                launches[0] += 1
+                moe.moe_forward(plan, xn, r, chunk, cws[l], bias, r, ws, stream=s)
+                launches[0] += moe.moe_last_launch_count()
+            out[c0:c0 + chunk].copy_(r)
+
+    # dominant kernel: gate/up (decode: the gate/up GEMV)
+    dom = moe.MOE_KERNEL_DECODE_GATEUP if T == 1 else moe.MOE_KERNEL_GATEUP
+    n_dom = (T // chunk) * L
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
+
+    # warm the path once eagerly, then capture one step into a CUDA graph
+    with torch.cuda.stream(stream):
+        if T == 1:
+            x_in.copy_(tokens[0])
+        body()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    moe.moe_profile_events(dom, ev_a, ev_b)
+    with torch.cuda.graph(graph, stream=stream):
+        body()
+    moe.moe_profile_events(dom)
+    per_step_launches = launches[0]
+
+    def step(i):
+        if T == 1:
+            x_in.copy_(tokens[i % n_in])
+        graph.replay()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id(device)) as clk:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(args.steps):
+                step(i)
+            t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    try:
+        dom_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / n_dom
+    except Exception:
+        dom_ms = None
+    if world > 1:
+        tt = torch.tensor([ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # bytes / flops of the workload
+    h_out = out.cpu()
+    st = moe.moe_device_status(plan, ws)
+    touched = E + 1
+    if T > 1 and L == 1:
+        v = moe.moe_route_view(plan, ws, T)
+        counts = moe.workspace_tensor(ws, v.counts_d, E, torch.int32).cpu().numpy()
+        touched = int((counts > 0).sum()) + 1
+    tok_per_step = T
+    flops_tok = 9 * 3 * 2 * H * I_DIM + 2 * H * E
+    result = {}
+    if T == 1:
+        bytes_tok = L * (ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2)
+        gbs = bytes_tok * args.steps / (ms * 1e-3) / 1e9 * world
+        result.update(value=gbs, unit="GB/s", higher_is_better=True)
+        dom_bytes = 9 * GATEUP_BYTES + H * 2
+        dom_bound, dom_units = "hbm", dom_bytes
+    else:
+        tps = tok_per_step * args.steps / (ms * 1e-3) * world
+        result.update(value=tps, unit="tokens/s", higher_is_better=True)
+        rows = (K_TOP + 1) * chunk
+        dom_flops = 2 * 2 * rows * H * I_DIM
+        dom_bytes = touched * GATEUP_BYTES + chunk * H * 2
+        pk = peaks()
+        t_flops = dom_flops / (pk["bf16_tflops"] * 1e12)
+        t_bytes = dom_bytes / (pk["hbm_gbs"] * 1e9)
+        dom_bound, dom_units = ("tensor", dom_flops) if t_flops > t_bytes else ("hbm", dom_bytes)
+    pk = peaks()
+    if dom_ms:
+        if dom_bound == "hbm":
+            achieved = dom_units / (dom_ms * 1e-3) / 1e9
+            peak = pk["hbm_gbs"]
+            unit = "GB/s"
+        else:
+            achieved = dom_units / (dom_ms * 1e-3) / 1e12
+            peak = pk["bf16_tflops_sustained"] if L > 1 else pk["bf16_tflops"]
+            unit = "TFLOP/s"
+        roofline = {"bound": dom_bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                    "frac": round(achieved / peak, 4), "traffic": None,
+                    "kernel": "decode_gateup" if T == 1 else "grouped gate/up",
+                    "kernel_ms": round(dom_ms, 5), "peak_src": pk["src"]}
+    else:
+        roofline = None
+
+    # end to end: pinned host input -> device, the step, output -> pinned host
+    in_rows = 1 if T == 1 else T
+    host_in = torch.from_numpy(np.ascontiguousarray(x_host[:in_rows]).view(np.int16)).pin_memory()
+    host_out = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    e2e_steps = min(args.steps, 200 if T == 1 else max(3, args.steps))
+    torch.cuda.synchronize()
+    t_e = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            x_in[:in_rows].copy_(host_in, non_blocking=True)
+            graph.replay()
+            host_out.copy_(out, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t_e
+    if T == 1:
+        e2e_val = bytes_tok * e2e_steps / e2e_s / 1e9 * world
+    else:
+        e2e_val = tok_per_step * e2e_steps / e2e_s * world
+    e2e = {"value": e2e_val, "unit": result["unit"], "h2d_bytes_per_step": in_rows * H * 2,
+           "d2h_bytes_per_step": T * H * 2}
+
+    result.update(ms_per_step=ms / args.steps, roofline=roofline, e2e=e2e, clocks=clk.summary(),
+                  gpu_launches=per_step_launches * args.steps, device_status=st,
+                  touched_experts=touched if T > 1 else None,
+                  dtype="int4-g64 weights, bf16 activations, fp32 accumulate")
+    del h_out
+    return result
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+
+def oracle_sample(wl, seed, budget_tokens=None):
+    """Run the CPU oracle once on a bounded sample of the workload.  Returns
+    (seconds, units, unit, description)."""
+    import oracle as orc
+    import synthetic as syn
+    T = wl["T"]
+    d = orc.Dims()
+    if T == 1:
+        n_layers = 1
+        W = syn.experts(seed, E + 1, H, I_DIM, layer=0, centred=wl["centred"])
+        W["router"] = syn.router(seed, E, H, layer=0)
+        x = syn.activations(seed, 1, H)
+        t = time.perf_counter()
+        orc.moe_layer(d, x, W)
+        dt = time.perf_counter() - t
+        units = n_layers * (ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2) / 1e9
+        return dt, units, "GB/s", "1 token through 1 layer (GB of router + 9 experts streamed per second)"
+    n_tok = budget_tokens or (32 if wl["layers"] > 1 else 64)
+    W = syn.experts(seed, E + 1, H, I_DIM, layer=0, centred=wl["centred"])
+    W["router"] = syn.router(seed, E, H, layer=0)
+    x = syn.activations(seed, n_tok, H)
+    bias = syn.zipf_bias(seed, E) if wl["zipf"] else None
+    t = time.perf_counter()
+    orc.moe_layer(d, x, W, bias=bias)
+    dt = time.perf_counter() - t
+    # tokens/s of the workload: one layer of the sample, scaled to all layers
+    units = n_tok / wl["layers"]
+    return dt, units, "tokens/s", f"{n_tok} tokens through 1 of {wl['layers']} layer(s), scaled to the full stack"
+
+
+def cpu_baseline(wl, seed):
+    import oracle as orc
+    orc.build()
+    dt, units, unit, desc = oracle_sample(wl, seed)
+    return {"value": units / dt, "unit": unit, "cores": orc.num_threads(), "kind": "oracle", "sample": desc,
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args, wl):
+    import oracle as orc
+    import synthetic as syn
+    orc.build()
+    syn.build()
+    for i in range(args.warmup):
+        oracle_sample(wl, args.seed + i)
+    steps = args.steps
+    tot, units, unit, desc = 0.0, 0.0, None, None
+    for i in range(steps):
+        dt, u, unit, desc = oracle_sample(wl, args.seed + 100 + i)
+        tot += dt
+        units += u
+    val = units / tot
+    return {"value": val, "unit": unit, "higher_is_better": True, "ms_per_step": tot / steps * 1e3,
+            "cpu_baseline": {"value": val, "unit": unit, "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "dtype": "fp64 oracle (bf16 rounding points of the layer)"}
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    args = parse()
+    wl = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    base = {"metric": METRIC, "n_gpus": args.gpus if world == 1 else world, "steps": args.steps,
+            "warmup": args.warmup, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {wl['desc']}", "tokens_per_step": wl["T"],
+                       "layers": wl["layers"], "chunk": wl["chunk"], "parallelism": "replicas" if world > 1 else "1 GPU",
+                       "l2": "inputs larger than L2 (packed weights >= 455 MB per layer)",
+                       "experts": args.experts}}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        res = run_reference(args, wl)
+        line = {**base, **res, "impl": "reference"}
+        print(json.dumps(line))
+        return
+    import torch
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.cuda.set_device(device)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, wl, rank, world, device)
+    if rank == 0:
+        line = {**base, **res}
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(wl, args.seed)
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,123 @@
+// Weighted gather-combine, RMSNorm and the dequantisation test hook.
+//
+// combine:  out[t] = bf16(res[t] + y_shared[t] + sum_j w[t,j] * y[inv[t*k+j]])
+//           fp32, summed in that order (the layer's bf16 weighted gather-combine
+//           with the shared expert's output and a residual add).
+// rmsnorm:  x = bf16(r / sqrt(mean(r^2) + eps)), fp32 (between stacked layers).
+// dequant:  w = bf16_rne(scale * q + bias) ("Prefill": 64 weights share one bf16
+//           scale and bias; weights are rebuilt to bf16).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+__device__ __forceinline__ void unpack8(uint4 v, float f[8]) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(u[i] << 16);
+    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float f[8]) {
+  uint32_t u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) u[i] = f32_to_bf16(f[2 * i]) | ((uint32_t)f32_to_bf16(f[2 * i + 1]) << 16);
+  return make_uint4(u[0], u[1], u[2], u[3]);
+}
+
+// One block per token; each thread owns 8 consecutive columns.
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ res, const uint16_t *__restrict__ y,
+                                                      const int32_t *__restrict__ inv,
+                                                      const float *__restrict__ topk_w, int T, int H, int k, int S,
+                                                      uint16_t *__restrict__ out) {
+  const int t = blockIdx.x;
+  __shared__ int s_row[16];
+  __shared__ float s_w[16];
+  if (threadIdx.x < k) {
+    s_row[threadIdx.x] = inv[(size_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    float acc[8], v[8];
+    unpack8(*reinterpret_cast<const uint4 *>(res + (size_t)t * H + c), acc);
+    if (S) {
+      unpack8(*reinterpret_cast<const uint4 *>(y + ((size_t)k * T + t) * H + c), v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += v[i];
+    }
+    for (int j = 0; j < k; ++j) {
+      unpack8(*reinterpret_cast<const uint4 *>(y + (size_t)s_row[j] * H + c), v);
+      const float wj = s_w[j];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+    }
+    *reinterpret_cast<uint4 *>(out + (size_t)t * H + c) = pack8(acc);
+  }
+}
+
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t *__restrict__ r, int H, float eps,
+                                                      uint16_t *__restrict__ x) {
+  const int t = blockIdx.x;
+  __shared__ float s_part[8];
+  float ss = 0.f;
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    float v[8];
+    unpack8(*reinterpret_cast<const uint4 *>(r + (size_t)t * H + c), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_part[w];
+  const float scale = rsqrtf(tot / (float)H + eps);
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    float v[8];
+    unpack8(*reinterpret_cast<const uint4 *>(r + (size_t)t * H + c), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] *= scale;
+    *reinterpret_cast<uint4 *>(x + (size_t)t * H + c) = pack8(v);
+  }
+}
+
+// One thread per packed word (8 weights).
+__global__ void dequant_kernel(const uint32_t *__restrict__ q, const uint16_t *__restrict__ sc,
+                               const uint16_t *__restrict__ b, int rows, int K, int G, uint16_t *__restrict__ w) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t words = (size_t)rows * (K / 8);
+  if (i >= words) return;
+  const size_t n = i / (K / 8), kw = i % (K / 8);
+  const size_t g = n * (K / G) + (kw * 8) / G;
+  __nv_bfloat162 p[4];
+  dequant_word(q[i], bf16x2_splat(sc[g]), bf16x2_splat(b[g]), p);
+  *reinterpret_cast<uint4 *>(w + n * K + kw * 8) = *reinterpret_cast<uint4 *>(p);
+}
+
+cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w, int T,
+                           int H, int k, int S, uint16_t *out, cudaStream_t s) {
+  prof_before(MOE_KERNEL_COMBINE, s);
+  combine_kernel<<<T, 256, 0, s>>>(res, y, inv, topk_w, T, H, k, S, out);
+  prof_after(MOE_KERNEL_COMBINE, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const uint16_t *r, int T, int H, float eps, uint16_t *x, cudaStream_t s) {
+  prof_before(MOE_KERNEL_RMSNORM, s);
+  rmsnorm_kernel<<<T, 256, 0, s>>>(r, H, eps, x);
+  prof_after(MOE_KERNEL_RMSNORM, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint32_t *q, const uint16_t *sc, const uint16_t *b, int rows, int K, int G,
+                           uint16_t *w, cudaStream_t s) {
+  const size_t words = (size_t)rows * (K / 8);
+  const unsigned blocks = (unsigned)((words + 255) / 256);
+  dequant_kernel<<<blocks, 256, 0, s>>>(q, sc, b, rows, K, G, w);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,47 @@
+// Launchers of libmoe.so's kernels (host declarations, one place).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Profiling hook (moe_profile_events): record events around a kernel launch.
+void prof_before(int kernel, cudaStream_t s);
+void prof_after(int kernel, cudaStream_t s);
+
+struct ExpertPtrs {
+  const uint32_t *gate_q, *up_q, *down_q;
+  const uint16_t *gate_s, *gate_b, *up_s, *up_b, *down_s, *down_b;
+};
+
+// route.cu
+cudaError_t launch_router_logits(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
+                                 float *keys, cudaStream_t s);
+cudaError_t launch_topk(const float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
+                        int32_t *status, cudaStream_t s);
+cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, int S, const int32_t *counts,
+                           int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *blockmap, int32_t *n_tiles,
+                           int max_tiles, int32_t *status, int debug, cudaStream_t s);
+
+// experts_simt.cu (CUDA-core grouped GEMMs, tiles of SIMT_ROWS rows)
+constexpr int SIMT_ROWS = 32;
+cudaError_t launch_gateup_simt(const uint16_t *x, int T, int H, int I, int E, int k, const int32_t *perm,
+                               const int32_t *blockmap, const int32_t *n_tiles, int max_tiles, ExpertPtrs w,
+                               uint16_t *h, cudaStream_t s);
+cudaError_t launch_down_simt(const uint16_t *h, int T, int H, int I, int E, int k, const int32_t *blockmap,
+                             const int32_t *n_tiles, int max_tiles, ExpertPtrs w, uint16_t *y, cudaStream_t s);
+
+// combine.cu
+cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w, int T,
+                           int H, int k, int S, uint16_t *out, cudaStream_t s);
+cudaError_t launch_rmsnorm(const uint16_t *r, int T, int H, float eps, uint16_t *x, cudaStream_t s);
+cudaError_t launch_dequant(const uint32_t *q, const uint16_t *sc, const uint16_t *b, int rows, int K, int G,
+                           uint16_t *w, cudaStream_t s);
+
+// decode.cu (T == 1)
+cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, int k, int I, int S,
+                          const float *router, const float *bias, ExpertPtrs w, float *keys, int32_t *topk_id,
+                          float *topk_w, int32_t *counter, uint16_t *hbuf, uint16_t *out, int32_t *status,
+                          int *launches, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,400 @@
+// The C ABI (include/moe.h): plan, workspace layout, argument checks and the
+// enqueue order of the layer's kernels.  Host code only; nothing here
+// allocates device memory or synchronises (moe_device_status excepted).
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.h"
+
+namespace {
+
+thread_local int32_t g_last_launches = 0;
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+struct ProfState {
+  int kernel = 0;
+  int n = 0;
+  unsigned long long next = 0;
+  cudaEvent_t start[4096];
+  cudaEvent_t stop[4096];
+  bool open = false;
+};
+thread_local ProfState *g_prof = nullptr;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int tiles_bound(int T, int k, int E, int S, int BN) {
+  // sum_e ceil(c_e / BN) <= k*T/BN + E, plus the shared expert's tiles
+  return (k * T + BN - 1) / BN + E + (S ? (T + BN - 1) / BN : 0);
+}
+
+moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles) {
+  moe::Layout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  const size_t E = c.n_experts, k = c.top_k, S = c.n_shared, H = c.hidden, I = c.inter, T = Tmax;
+  L.status = take(64);
+  L.counter = take(64);
+  L.keys = take(T * E * 4);
+  L.topk_id = take(T * k * 4);
+  L.topk_w = take(T * k * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.perm = take(k * T * 4);
+  L.inv = take(k * T * 4);
+  L.blockmap = take((size_t)max_tiles * 16);
+  L.n_tiles = take(16);
+  L.h = take((k + S) * T * I * 2);
+  L.y = take((k + S) * T * H * 2);
+  L.total = o;
+  return L;
+}
+
+bool weights_aligned(const moe_weights *w) {
+  using moe::aligned16;
+  return aligned16(w->router_d) && aligned16(w->gate_q_d) && aligned16(w->up_q_d) && aligned16(w->gate_s_d) &&
+         aligned16(w->gate_b_d) && aligned16(w->up_s_d) && aligned16(w->up_b_d) && aligned16(w->down_q_d) &&
+         aligned16(w->down_s_d) && aligned16(w->down_b_d);
+}
+
+bool weights_present(const moe_weights *w) {
+  return w->router_d && w->gate_q_d && w->up_q_d && w->gate_s_d && w->gate_b_d && w->up_s_d && w->up_b_d &&
+         w->down_q_d && w->down_s_d && w->down_b_d;
+}
+
+moe_status check_call(const moe_plan_t *p, int32_t T, const void *ws, size_t ws_bytes) {
+  if (!p) return MOE_ERR_INVALID_ARGUMENT;
+  if (T < 1) return MOE_ERR_INVALID_ARGUMENT;
+  if (T > p->max_tokens) return MOE_ERR_TOO_MANY_TOKENS;
+  if (!ws) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(ws)) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < p->lay.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+// Checked after every argument check: no device means nothing can be enqueued.
+moe_status device_ready(const moe_plan_t *p) { return p->num_sms > 0 ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  g_last_cuda = e;
+  return MOE_ERR_CUDA;
+}
+
+// Routing kernels for T tokens; keys already in ws when from_keys.
+moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const float *router, const float *bias,
+                         void *ws, bool from_keys, cudaStream_t s, int *launches) {
+  const moe_config &c = p->cfg;
+  const moe::Layout &L = p->lay;
+  float *keys = moe::ws_ptr<float>(ws, L.keys);
+  int32_t *status = moe::ws_ptr<int32_t>(ws, L.status);
+  int32_t *counts = moe::ws_ptr<int32_t>(ws, L.counts);
+  cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts, s);
+  if (err != cudaSuccess) return cuda_status(err);
+  if (!from_keys) {
+    if ((err = moe::launch_router_logits(x, T, c.hidden, router, c.n_experts, bias, keys, s)) != cudaSuccess)
+      return cuda_status(err);
+    ++*launches;
+  }
+  if ((err = moe::launch_topk(keys, T, c.n_experts, c.top_k, moe::ws_ptr<int32_t>(ws, L.topk_id),
+                              moe::ws_ptr<float>(ws, L.topk_w), counts, status, s)) != cudaSuccess)
+    return cuda_status(err);
+  ++*launches;
+  const int max_tiles = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, p->block_rows);
+  if ((err = moe::launch_scatter(moe::ws_ptr<int32_t>(ws, L.topk_id), T, c.n_experts, c.top_k, p->block_rows,
+                                 c.n_shared, counts, moe::ws_ptr<int32_t>(ws, L.offsets),
+                                 moe::ws_ptr<int32_t>(ws, L.perm), moe::ws_ptr<int32_t>(ws, L.inv),
+                                 moe::ws_ptr<int32_t>(ws, L.blockmap), moe::ws_ptr<int32_t>(ws, L.n_tiles), max_tiles,
+                                 status, (p->flags & MOE_FLAG_DEBUG_CHECKS) ? 1 : 0, s)) != cudaSuccess)
+    return cuda_status(err);
+  ++*launches;
+  return MOE_OK;
+}
+
+moe::ExpertPtrs expert_ptrs(const moe_weights *w) {
+  moe::ExpertPtrs e;
+  e.gate_q = w->gate_q_d;
+  e.up_q = w->up_q_d;
+  e.down_q = w->down_q_d;
+  e.gate_s = w->gate_s_d;
+  e.gate_b = w->gate_b_d;
+  e.up_s = w->up_s_d;
+  e.up_b = w->up_b_d;
+  e.down_s = w->down_s_d;
+  e.down_b = w->down_b_d;
+  return e;
+}
+
+}  // namespace
+
+namespace moe {
+void prof_before(int kernel, cudaStream_t s) {
+  ProfState *p = g_prof;
+  if (!p || p->n == 0 || p->kernel != kernel) return;
+  cudaEventRecord(p->start[p->next % p->n], s);
+  p->open = true;
+}
+void prof_after(int kernel, cudaStream_t s) {
+  ProfState *p = g_prof;
+  if (!p || p->n == 0 || p->kernel != kernel || !p->open) return;
+  cudaEventRecord(p->stop[p->next % p->n], s);
+  p->open = false;
+  ++p->next;
+}
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *const *stop_events, int32_t n) {
+  if (kernel < MOE_KERNEL_ROUTER || kernel > MOE_KERNEL_RMSNORM || n < 0 || n > 4096) return MOE_ERR_INVALID_ARGUMENT;
+  if (n > 0 && (!start_events || !stop_events)) return MOE_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < n; ++i)
+    if (!start_events[i] || !stop_events[i]) return MOE_ERR_INVALID_ARGUMENT;
+  if (n == 0) {
+    delete g_prof;
+    g_prof = nullptr;
+    return MOE_OK;
+  }
+  if (!g_prof) g_prof = new (std::nothrow) ProfState;
+  if (!g_prof) return MOE_ERR_INVALID_ARGUMENT;
+  g_prof->kernel = kernel;
+  g_prof->n = n;
+  g_prof->next = 0;
+  g_prof->open = false;
+  for (int i = 0; i < n; ++i) {
+    g_prof->start[i] = static_cast<cudaEvent_t>(start_events[i]);
+    g_prof->stop[i] = static_cast<cudaEvent_t>(stop_events[i]);
+  }
+  return MOE_OK;
+}
+
+const char *moe_status_str(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dimensions";
+    case MOE_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_TOO_MANY_TOKENS: return "T exceeds the plan's max_tokens";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_NONFINITE: return "non-finite router key";
+    case MOE_ERR_DEVICE_BOUNDS: return "device bounds check failed";
+  }
+  return "unknown status";
+}
+
+moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, moe_plan_t **out) {
+  if (!cfg || !out) return MOE_ERR_INVALID_ARGUMENT;
+  *out = nullptr;
+  const uint32_t known = MOE_FLAG_DEBUG_CHECKS | MOE_FLAG_FORCE_GROUPED | MOE_FLAG_SIMT_EXPERTS |
+                         MOE_FLAG_TILE_ROWS_64;
+  if (flags & ~known) return MOE_ERR_INVALID_ARGUMENT;
+  if (max_tokens < 1 || max_tokens > 65536) return MOE_ERR_INVALID_ARGUMENT;
+  const moe_config &c = *cfg;
+  if (c.hidden <= 0 || c.n_experts <= 0 || c.top_k <= 0 || c.inter <= 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (c.hidden % 128 || c.inter % 64 || c.group_size != 64 || c.n_experts > 1024 || c.top_k > 16 ||
+      c.top_k > c.n_experts || (c.n_shared != 0 && c.n_shared != 1) || c.hidden > 12288 || c.inter > 8192)
+    return MOE_ERR_UNSUPPORTED;
+  // the decode path stages h of every slot in 48 KB of shared memory
+  if ((size_t)(c.top_k + c.n_shared) * ((c.inter + 511) / 512) * 512 * 4 > 48 * 1024) return MOE_ERR_UNSUPPORTED;
+  moe_plan_t *p = new (std::nothrow) moe_plan_t;
+  if (!p) return MOE_ERR_INVALID_ARGUMENT;
+  p->cfg = c;
+  p->max_tokens = max_tokens;
+  p->flags = flags;
+  const bool simt = (flags & MOE_FLAG_SIMT_EXPERTS) != 0 || !moe::TC_READY;
+  p->use_tc = !simt;
+  p->block_rows = simt ? moe::SIMT_ROWS : ((flags & MOE_FLAG_TILE_ROWS_64) ? 64 : moe::TC_ROWS);
+  p->max_tiles = tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows);
+  p->lay = make_layout(c, max_tokens, p->max_tiles);
+  p->num_sms = 0;
+  int dev = 0, count = 0;
+  if (cudaGetDeviceCount(&count) == cudaSuccess && count > 0 && cudaGetDevice(&dev) == cudaSuccess) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) p->num_sms = prop.multiProcessorCount;
+  } else {
+    cudaGetLastError();  // no device: host-side checks still work, launches report MOE_ERR_CUDA
+  }
+  *out = p;
+  return MOE_OK;
+}
+
+void moe_plan_destroy(moe_plan_t *plan) { delete plan; }
+
+size_t moe_workspace_bytes(const moe_plan_t *plan) { return plan ? plan->lay.total : 0; }
+
+moe_status moe_workspace_init(const moe_plan_t *plan, void *ws_d, size_t ws_bytes, void *stream) {
+  if (!plan || !ws_d) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(ws_d)) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < plan->lay.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (device_ready(plan) != MOE_OK) return MOE_ERR_CUDA;
+  // status and counter words
+  return cuda_status(cudaMemsetAsync(ws_d, 0, plan->lay.keys, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_route(const moe_plan_t *plan, const void *x_d, int32_t T, const float *router_d,
+                     const float *logit_bias_d, void *ws_d, size_t ws_bytes, void *stream) {
+  g_last_launches = 0;
+  moe_status st = check_call(plan, T, ws_d, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!x_d || !router_d) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(x_d) || !moe::aligned16(router_d) || !moe::aligned16(logit_bias_d))
+    return MOE_ERR_MISALIGNED;
+  if ((st = device_ready(plan)) != MOE_OK) return st;
+  int launches = 0;
+  st = enqueue_route(plan, static_cast<const uint16_t *>(x_d), T, router_d, logit_bias_d, ws_d, false,
+                     static_cast<cudaStream_t>(stream), &launches);
+  g_last_launches = launches;
+  return st;
+}
+
+moe_status moe_route_from_logits(const moe_plan_t *plan, const float *keys_d, int32_t T, void *ws_d,
+                                 size_t ws_bytes, void *stream) {
+  g_last_launches = 0;
+  moe_status st = check_call(plan, T, ws_d, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!keys_d) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(keys_d)) return MOE_ERR_MISALIGNED;
+  if ((st = device_ready(plan)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float *keys = moe::ws_ptr<float>(ws_d, plan->lay.keys);
+  if (keys != keys_d) {
+    cudaError_t err =
+        cudaMemcpyAsync(keys, keys_d, sizeof(float) * (size_t)T * plan->cfg.n_experts, cudaMemcpyDeviceToDevice, s);
+    if (err != cudaSuccess) return cuda_status(err);
+  }
+  int launches = 0;
+  st = enqueue_route(plan, nullptr, T, nullptr, nullptr, ws_d, true, s, &launches);
+  g_last_launches = launches;
+  return st;
+}
+
+moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *residual_d, int32_t T,
+                       const moe_weights *w, const float *logit_bias_d, void *out_d, void *ws_d, size_t ws_bytes,
+                       void *stream) {
+  g_last_launches = 0;
+  moe_status st = check_call(plan, T, ws_d, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!x_d || !w || !out_d || !weights_present(w)) return MOE_ERR_INVALID_ARGUMENT;
+  if (out_d == x_d) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(x_d) || !moe::aligned16(residual_d) || !moe::aligned16(out_d) ||
+      !moe::aligned16(logit_bias_d) || !weights_aligned(w))
+    return MOE_ERR_MISALIGNED;
+  if ((st = device_ready(plan)) != MOE_OK) return st;
+  const moe_config &c = plan->cfg;
+  const moe::Layout &L = plan->lay;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t *x = static_cast<const uint16_t *>(x_d);
+  const uint16_t *res = residual_d ? static_cast<const uint16_t *>(residual_d) : x;
+  uint16_t *out = static_cast<uint16_t *>(out_d);
+  const moe::ExpertPtrs ep = expert_ptrs(w);
+  int32_t *status = moe::ws_ptr<int32_t>(ws_d, L.status);
+  int launches = 0;
+
+  if (T == 1 && !(plan->flags & MOE_FLAG_FORCE_GROUPED)) {
+    cudaError_t err = moe::launch_decode(
+        x, res, c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, w->router_d, logit_bias_d, ep,
+        moe::ws_ptr<float>(ws_d, L.keys), moe::ws_ptr<int32_t>(ws_d, L.topk_id), moe::ws_ptr<float>(ws_d, L.topk_w),
+        moe::ws_ptr<int32_t>(ws_d, L.counter), moe::ws_ptr<uint16_t>(ws_d, L.h), out, status, &launches, s);
+    g_last_launches = launches;
+    return cuda_status(err);
+  }
+
+  st = enqueue_route(plan, x, T, w->router_d, logit_bias_d, ws_d, false, s, &launches);
+  if (st != MOE_OK) return st;
+  const int max_tiles = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, plan->block_rows);
+  const int32_t *perm = moe::ws_ptr<int32_t>(ws_d, L.perm);
+  const int32_t *bm = moe::ws_ptr<int32_t>(ws_d, L.blockmap);
+  const int32_t *nt = moe::ws_ptr<int32_t>(ws_d, L.n_tiles);
+  uint16_t *h = moe::ws_ptr<uint16_t>(ws_d, L.h);
+  uint16_t *y = moe::ws_ptr<uint16_t>(ws_d, L.y);
+  cudaError_t err;
+  if (!plan->use_tc) {
+    err = moe::launch_gateup_simt(x, T, c.hidden, c.inter, c.n_experts, c.top_k, perm, bm, nt, max_tiles, ep, h, s);
+    if (err != cudaSuccess) return cuda_status(err);
+    err = moe::launch_down_simt(h, T, c.hidden, c.inter, c.n_experts, c.top_k, bm, nt, max_tiles, ep, y, s);
+    if (err != cudaSuccess) return cuda_status(err);
+    launches += 2;
+  } else {
+    err = moe::launch_experts_tc(plan, x, T, perm, bm, nt, max_tiles, ep, h, y, status, &launches, s);
+    if (err != cudaSuccess) return cuda_status(err);
+  }
+  err = moe::launch_combine(res, y, moe::ws_ptr<int32_t>(ws_d, L.inv), moe::ws_ptr<float>(ws_d, L.topk_w), T,
+                            c.hidden, c.top_k, c.n_shared, out, s);
+  if (err != cudaSuccess) return cuda_status(err);
+  ++launches;
+  g_last_launches = launches;
+  return MOE_OK;
+}
+
+moe_status moe_route_view(const moe_plan_t *plan, void *ws_d, int32_t T, moe_route_ptrs *out) {
+  if (!plan || !ws_d || !out) return MOE_ERR_INVALID_ARGUMENT;
+  if (T < 1) return MOE_ERR_INVALID_ARGUMENT;
+  if (T > plan->max_tokens) return MOE_ERR_TOO_MANY_TOKENS;
+  const moe::Layout &L = plan->lay;
+  out->keys_d = moe::ws_ptr<float>(ws_d, L.keys);
+  out->topk_id_d = moe::ws_ptr<int32_t>(ws_d, L.topk_id);
+  out->topk_w_d = moe::ws_ptr<float>(ws_d, L.topk_w);
+  out->counts_d = moe::ws_ptr<int32_t>(ws_d, L.counts);
+  out->offsets_d = moe::ws_ptr<int32_t>(ws_d, L.offsets);
+  out->perm_d = moe::ws_ptr<int32_t>(ws_d, L.perm);
+  out->inv_d = moe::ws_ptr<int32_t>(ws_d, L.inv);
+  out->blockmap_d = moe::ws_ptr<int32_t>(ws_d, L.blockmap);
+  out->n_tiles_d = moe::ws_ptr<int32_t>(ws_d, L.n_tiles);
+  out->h_d = moe::ws_ptr<uint16_t>(ws_d, L.h);
+  out->y_d = moe::ws_ptr<uint16_t>(ws_d, L.y);
+  out->status_d = moe::ws_ptr<int32_t>(ws_d, L.status);
+  out->max_tiles = tiles_bound(T, plan->cfg.top_k, plan->cfg.n_experts, plan->cfg.n_shared, plan->block_rows);
+  out->block_rows = plan->block_rows;
+  return MOE_OK;
+}
+
+moe_status moe_rmsnorm(const void *r_d, int32_t T, int32_t H, float eps, void *x_d, void *stream) {
+  g_last_launches = 0;
+  if (!r_d || !x_d || T < 1 || H < 8 || H % 8 || !(eps >= 0.f)) return MOE_ERR_INVALID_ARGUMENT;
+  if (r_d == x_d) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(r_d) || !moe::aligned16(x_d)) return MOE_ERR_MISALIGNED;
+  cudaError_t err = moe::launch_rmsnorm(static_cast<const uint16_t *>(r_d), T, H, eps, static_cast<uint16_t *>(x_d),
+                                        static_cast<cudaStream_t>(stream));
+  g_last_launches = 1;
+  return cuda_status(err);
+}
+
+moe_status moe_dequant(const uint32_t *q_d, const uint16_t *s_d, const uint16_t *b_d, int32_t rows, int32_t K,
+                       int32_t G, void *w_d, void *stream) {
+  g_last_launches = 0;
+  if (!q_d || !s_d || !b_d || !w_d || rows < 1 || K < 8) return MOE_ERR_INVALID_ARGUMENT;
+  if (G != 64 || K % G) return MOE_ERR_UNSUPPORTED;
+  if (!moe::aligned16(q_d) || !moe::aligned16(w_d)) return MOE_ERR_MISALIGNED;
+  cudaError_t err = moe::launch_dequant(q_d, s_d, b_d, rows, K, G, static_cast<uint16_t *>(w_d),
+                                        static_cast<cudaStream_t>(stream));
+  g_last_launches = 1;
+  return cuda_status(err);
+}
+
+moe_status moe_device_status(const moe_plan_t *plan, void *ws_d, void *stream, int32_t *host_status,
+                             int32_t reset) {
+  if (!plan || !ws_d || !host_status) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(ws_d)) return MOE_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t *status = moe::ws_ptr<int32_t>(ws_d, plan->lay.status);
+  cudaError_t err = cudaMemcpyAsync(host_status, status, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess && reset) err = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  return cuda_status(err);
+}
+
+int32_t moe_last_launch_count(void) { return g_last_launches; }
+
+const char *moe_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda); }
+
+}  // extern "C"

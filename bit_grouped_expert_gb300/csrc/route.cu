@@ -1,0 +1,230 @@
+// Routing on the device ("Prefill" section of the Lily pages: histogram,
+// prefix scan, scatter and block map stay in one GPU submission with no CPU
+// sync inside the layer; "three workload shapes": the router scores every
+// expert and picks k).
+//
+//   router_logits_kernel   keys[t][e] = fp32(x[t] . router[e]) (+ bias[e])
+//   topk_kernel            per token: k best keys, softmax weights, histogram
+//   scatter_kernel         per expert: offset (scan of the histogram), stable
+//                          scatter of its pairs (perm / inv) and its block-map
+//                          tiles; the last expert's block also appends the
+//                          shared expert's tiles.
+#include "common.cuh"
+#include "kernels.h"
+#include "topk.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------- router
+// fp32 CUDA-core GEMM: a block computes 32 tokens x 64 experts, K in steps
+// of 32; each thread owns 2 tokens x 4 experts.
+constexpr int RT_M = 32, RT_N = 64, RT_K = 32;
+
+__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t *__restrict__ x, int T, int H,
+                                                            const float *__restrict__ router, int E,
+                                                            const float *__restrict__ bias,
+                                                            float *__restrict__ keys) {
+  __shared__ float xs[RT_K][RT_M + 1];
+  __shared__ float ws[RT_K][RT_N + 1];
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * RT_M, e0 = blockIdx.y * RT_N;
+  const int tx = tid % 16, ty = tid / 16;
+  float acc[2][4] = {};
+  for (int k0 = 0; k0 < H; k0 += RT_K) {
+    // x tile: 32 tokens x 32 k  (1024 values, 4 per thread)
+    for (int i = tid; i < RT_M * RT_K; i += 256) {
+      int r = i / RT_K, c = i % RT_K;
+      int t = t0 + r;
+      xs[c][r] = (t < T) ? bf16_to_f32(x[(size_t)t * H + k0 + c]) : 0.f;
+    }
+    for (int i = tid; i < RT_N * RT_K; i += 256) {
+      int r = i / RT_K, c = i % RT_K;
+      int e = e0 + r;
+      ws[c][r] = (e < E) ? router[(size_t)e * H + k0 + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int c = 0; c < RT_K; ++c) {
+      float a0 = xs[c][2 * ty], a1 = xs[c][2 * ty + 1];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float b = ws[c][4 * tx + j];
+        acc[0][j] = fmaf(a0, b, acc[0][j]);
+        acc[1][j] = fmaf(a1, b, acc[1][j]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    int t = t0 + 2 * ty + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int e = e0 + 4 * tx + j;
+      if (e < E) keys[(size_t)t * E + e] = bias ? acc[i][j] + bias[e] : acc[i][j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- top-k
+// (per-token selection: topk.cuh)
+template <int KPL>
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ keys, int T, int E, int k,
+                                                   int32_t *__restrict__ topk_id, float *__restrict__ topk_w,
+                                                   int32_t *__restrict__ counts, int32_t *__restrict__ status) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+  if (warp >= T) return;
+  topk_token<KPL>(keys + (size_t)warp * E, E, k, lane, topk_id + (size_t)warp * k, topk_w + (size_t)warp * k,
+                  counts, status);
+}
+
+// ---------------------------------------------------------------- scatter
+// One block per expert e.  offsets[e] and the first tile index of e are
+// sums over counts[0..e-1] (each block recomputes them: E values).  The
+// scatter walks tokens in ascending order, so perm is stable.
+__global__ void __launch_bounds__(256) scatter_kernel(const int32_t *__restrict__ topk_id, int T, int E, int k,
+                                                      int BN, int S, const int32_t *__restrict__ counts,
+                                                      int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+                                                      int32_t *__restrict__ inv, int32_t *__restrict__ blockmap,
+                                                      int32_t *__restrict__ n_tiles, int max_tiles,
+                                                      int32_t *__restrict__ status, int debug) {
+  __shared__ int s_a[32], s_b[32];
+  __shared__ int s_warp[8];
+  __shared__ int s_off, s_tb;
+  const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int off = 0, tb = 0;
+  for (int i = tid; i < e; i += blockDim.x) {
+    int c = counts[i];
+    off += c;
+    tb += (c + BN - 1) / BN;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    off += __shfl_xor_sync(0xffffffffu, off, o);
+    tb += __shfl_xor_sync(0xffffffffu, tb, o);
+  }
+  if (lane == 0) {
+    s_a[wid] = off;
+    s_b[wid] = tb;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int a = 0, b = 0;
+    for (int w = 0; w < (int)(blockDim.x / 32); ++w) {
+      a += s_a[w];
+      b += s_b[w];
+    }
+    s_off = a;
+    s_tb = b;
+  }
+  __syncthreads();
+  off = s_off;
+  tb = s_tb;
+  const int ce = counts[e];
+  const int ntile_e = (ce + BN - 1) / BN;
+  if (tid == 0) offsets[e] = off;
+  if (e == E - 1) {
+    const int routed_tiles = tb + ntile_e;
+    const int shared_tiles = S ? (T + BN - 1) / BN : 0;
+    if (tid == 0) {
+      offsets[E] = off + ce;
+      *n_tiles = routed_tiles + shared_tiles;
+      if (debug && (off + ce != k * T || routed_tiles + shared_tiles > max_tiles))
+        set_status(status, MOE_ERR_DEVICE_BOUNDS);
+    }
+    for (int s = tid; s < shared_tiles; s += blockDim.x) {
+      int idx = routed_tiles + s;
+      if (idx < max_tiles) {
+        int4 ent = make_int4(E, k * T + s * BN, min(BN, T - s * BN), 0);
+        reinterpret_cast<int4 *>(blockmap)[idx] = ent;
+      }
+    }
+  }
+  for (int r = tid; r < ntile_e; r += blockDim.x) {
+    int idx = tb + r;
+    if (idx < max_tiles) {
+      int4 ent = make_int4(e, off + r * BN, min(BN, ce - r * BN), 0);
+      reinterpret_cast<int4 *>(blockmap)[idx] = ent;
+    }
+  }
+  if (ce == 0) return;
+  int running = 0;
+  for (int t0 = 0; t0 < T; t0 += blockDim.x) {
+    const int t = t0 + tid;
+    int jf = -1;
+    if (t < T) {
+      for (int j = 0; j < k; ++j)
+        if (topk_id[(size_t)t * k + j] == e) jf = j;
+    }
+    const bool flag = jf >= 0;
+    const uint32_t ballot = __ballot_sync(0xffffffffu, flag);
+    const int wrank = __popc(ballot & ((1u << lane) - 1u));
+    if (lane == 0) s_warp[wid] = __popc(ballot);
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      int c = s_warp[w];
+      before += (w < wid) ? c : 0;
+      total += c;
+    }
+    if (flag) {
+      const int pos = off + running + before + wrank;
+      const int p = t * k + jf;
+      if (pos < off + ce) {  // always checked: a stale histogram must not write out of bounds
+        perm[pos] = p;
+        inv[p] = pos;
+      } else {
+        set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      }
+    }
+    running += total;
+    __syncthreads();
+  }
+  if (debug && tid == 0 && running != ce) set_status(status, MOE_ERR_DEVICE_BOUNDS);
+}
+
+// ---------------------------------------------------------------- launchers
+
+cudaError_t launch_router_logits(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
+                                 float *keys, cudaStream_t s) {
+  dim3 grid((T + RT_M - 1) / RT_M, (E + RT_N - 1) / RT_N);
+  prof_before(MOE_KERNEL_ROUTER, s);
+  router_logits_kernel<<<grid, 256, 0, s>>>(x, T, H, router, E, bias, keys);
+  prof_after(MOE_KERNEL_ROUTER, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
+                        int32_t *status, cudaStream_t s) {
+  const int blocks = (T + 7) / 8;
+  const int kpl = (E + 31) / 32;
+  prof_before(MOE_KERNEL_TOPK, s);
+  if (kpl <= 1)
+    topk_kernel<1><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+  else if (kpl <= 2)
+    topk_kernel<2><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+  else if (kpl <= 4)
+    topk_kernel<4><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+  else if (kpl <= 8)
+    topk_kernel<8><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+  else if (kpl <= 16)
+    topk_kernel<16><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+  else
+    topk_kernel<32><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+  prof_after(MOE_KERNEL_TOPK, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, int S, const int32_t *counts,
+                           int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *blockmap, int32_t *n_tiles,
+                           int max_tiles, int32_t *status, int debug, cudaStream_t s) {
+  prof_before(MOE_KERNEL_SCATTER, s);
+  scatter_kernel<<<E, 256, 0, s>>>(topk_id, T, E, k, BN, S, counts, offsets, perm, inv, blockmap, n_tiles, max_tiles,
+                                   status, debug);
+  prof_after(MOE_KERNEL_SCATTER, s);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

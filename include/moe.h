@@ -1,0 +1,211 @@
+/* moe.h -- C ABI of libmoe.so, the GB300 (sm_103a) MoE expert layer.
+ *
+ * The layer (source: "Perplexity open-sources Lily, a Rust + Metal inference
+ * engine for Qwen3.6-35B-A3B on Apple Silicon"):
+ *   - "three workload shapes": a router scores 256 experts per token and picks
+ *     8; a shared expert processes every token;
+ *   - "Prefill": weights are groupwise-affine 4-bit, 64 weights sharing one
+ *     bf16 scale and one bf16 bias; they are rebuilt to bf16 tile by tile
+ *     inside the grouped GEMM with FP32 accumulation, so no unpacked weight
+ *     array reaches memory; routing (histogram, prefix scan, scatter, block
+ *     map) stays on the GPU with no CPU sync inside the layer;
+ *   - "Decode": at batch 1 there is almost no weight reuse, so bandwidth
+ *     bounds the step; only the selected experts' bytes are streamed.
+ *
+ * Arithmetic (where the pages are silent, the plainest reading):
+ *   w      = bf16_rne(scale * q + bias), q = (word[k/8] >> 4*(k%8)) & 15
+ *   key    = fp32(x . router_row) (+ logit_bias[e] in fp32)
+ *   top-k  = k largest keys, ties to the lower expert index, NaN lowest;
+ *            weights = softmax over the k picked keys (slot order = rank)
+ *   h      = bf16(silu(x.Wg^T) * (x.Wu^T)),  y = bf16(h.Wd^T)   (fp32 sums)
+ *   out    = bf16(residual + y_shared + sum_j w_j * y_j)         (fp32 sum)
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_d are DEVICE pointers; every other pointer is host.
+ *   - bf16 tensors are passed as raw 16-bit patterns (uint16_t / void*).
+ *   - Every device pointer must be 16-byte aligned (MOE_ERR_MISALIGNED).
+ *   - Argument checks run on the host before anything is enqueued; on any
+ *     error nothing is enqueued.  Launch failures return MOE_ERR_CUDA.
+ *   - No entry point allocates device memory, synchronises, or reads device
+ *     memory on the host, except moe_device_status (documented below).  The
+ *     caller owns every device buffer, including the workspace.
+ *   - A workspace may serve one call at a time; concurrent calls on different
+ *     streams need different workspaces.  A plan is immutable after creation
+ *     and may be shared across threads and streams.
+ */
+#ifndef MOE_H
+#define MOE_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARGUMENT = 1,   /* null pointer, bad size, bad flag        */
+  MOE_ERR_UNSUPPORTED = 2,        /* dims outside the supported set          */
+  MOE_ERR_MISALIGNED = 3,         /* a device pointer not 16-byte aligned    */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,
+  MOE_ERR_TOO_MANY_TOKENS = 5,    /* T > max_tokens: the caller chunks       */
+  MOE_ERR_CUDA = 6,               /* a CUDA call or launch failed            */
+  MOE_ERR_DEVICE_TIMEOUT = 7,     /* device status: a bounded wait gave up   */
+  MOE_ERR_NONFINITE = 8,          /* device status: NaN/Inf router key       */
+  MOE_ERR_DEVICE_BOUNDS = 9       /* device status: debug bounds check hit   */
+} moe_status;
+
+/* Layer dimensions.  Supported: hidden % 128 == 0, inter % 64 == 0,
+ * group_size == 64, 1 <= top_k <= min(16, n_experts), n_experts <= 1024,
+ * n_shared in {0, 1}.  The pages' model: {2048, 256, 8, 512, 1, 64}. */
+typedef struct {
+  int32_t hidden;      /* H */
+  int32_t n_experts;   /* E routed experts */
+  int32_t top_k;       /* k */
+  int32_t inter;       /* I, expert intermediate size */
+  int32_t n_shared;    /* S, 0 or 1; the shared expert is stored at index E */
+  int32_t group_size;  /* G = 64 */
+} moe_config;
+
+/* Packed expert weights, device pointers, experts stacked 0..E+S-1:
+ *   gate_q, up_q   uint32 [E+S][I][H/8]   8 codes per word, code k at bits 4*(k%8)
+ *   gate_s, gate_b, up_s, up_b  bf16 [E+S][I][H/G]  scale and bias per group
+ *   down_q         uint32 [E+S][H][I/8]
+ *   down_s, down_b bf16   [E+S][H][I/G]
+ *   router         fp32   [E][H]
+ * Rows are output features; groups run along the input (K) dimension.  The
+ * library only reads these buffers. */
+typedef struct {
+  const float *router_d;
+  const uint32_t *gate_q_d, *up_q_d;
+  const uint16_t *gate_s_d, *gate_b_d, *up_s_d, *up_b_d;
+  const uint32_t *down_q_d;
+  const uint16_t *down_s_d, *down_b_d;
+} moe_weights;
+
+/* Device pointers into a workspace, for tests and tools (moe_route_view). */
+typedef struct {
+  float *keys_d;       /* [T][E] fp32 selection keys (logits + bias)         */
+  int32_t *topk_id_d;  /* [T][k] picked experts in slot (rank) order          */
+  float *topk_w_d;     /* [T][k] softmax weights over the picked keys         */
+  int32_t *counts_d;   /* [E] pairs per expert (histogram)                    */
+  int32_t *offsets_d;  /* [E+1] exclusive scan of counts, offsets[E] = k*T    */
+  int32_t *perm_d;     /* [k*T] pair id t*k+j, experts in index order, tokens ascending */
+  int32_t *inv_d;      /* [k*T] position of pair t*k+j in perm                */
+  int32_t *blockmap_d; /* [max_tiles][4] (expert, first row, rows, 0)         */
+  int32_t *n_tiles_d;  /* [1] entries in use                                 */
+  uint16_t *h_d;       /* [(k+S)*T][I] bf16 SwiGLU rows (routed in perm order, then shared) */
+  uint16_t *y_d;       /* [(k+S)*T][H] bf16 expert outputs, same row order    */
+  int32_t *status_d;   /* [1] sticky device status (moe_status values)        */
+  int32_t max_tiles;   /* capacity of blockmap_d                             */
+  int32_t block_rows;  /* rows per block-map tile for this plan              */
+} moe_route_ptrs;
+
+/* Plan flags. */
+#define MOE_FLAG_DEBUG_CHECKS   0x1u  /* device bounds checks -> MOE_ERR_DEVICE_BOUNDS in the status */
+#define MOE_FLAG_FORCE_GROUPED  0x2u  /* T == 1 runs the grouped path instead of the decode path */
+#define MOE_FLAG_SIMT_EXPERTS   0x4u  /* CUDA-core grouped GEMMs instead of the tensor-core ones */
+#define MOE_FLAG_TILE_ROWS_64   0x8u  /* tensor-core path: 64-token tiles instead of 128 */
+
+typedef struct moe_plan moe_plan_t;
+
+/* Validate dims and build a host-only plan for up to max_tokens tokens per
+ * call (1 <= max_tokens <= 65536).  *out owns host memory only; free it with
+ * moe_plan_destroy.  Errors: MOE_ERR_INVALID_ARGUMENT (null pointers, bad
+ * max_tokens or unknown flags), MOE_ERR_UNSUPPORTED (dims), MOE_ERR_CUDA (no
+ * device or not sm_103). */
+moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, moe_plan_t **out);
+void moe_plan_destroy(moe_plan_t *plan);
+
+/* Bytes of device workspace a call of this plan needs (0 for a null plan). */
+size_t moe_workspace_bytes(const moe_plan_t *plan);
+
+/* Zero the workspace's status word and counters (enqueued on stream).  Call
+ * once after allocating a workspace. */
+moe_status moe_workspace_init(const moe_plan_t *plan, void *ws_d, size_t ws_bytes, void *stream);
+
+/* Routing only ("Prefill": histogram, prefix scan, scatter, block map, all on
+ * the GPU).  x_d: bf16 [T][H]; router_d: fp32 [E][H]; logit_bias_d: fp32 [E]
+ * or NULL.  Writes keys, top-k ids and weights, counts, offsets, perm, inv
+ * and the block map into ws (see moe_route_view).  1 <= T <= max_tokens. */
+moe_status moe_route(const moe_plan_t *plan, const void *x_d, int32_t T, const float *router_d,
+                     const float *logit_bias_d, void *ws_d, size_t ws_bytes, void *stream);
+
+/* Routing from given selection keys (test hook: lets the oracle and the GPU
+ * select from identical fp32 keys).  keys_d: fp32 [T][E]; it is copied into
+ * the workspace's key buffer first. */
+moe_status moe_route_from_logits(const moe_plan_t *plan, const float *keys_d, int32_t T, void *ws_d,
+                                 size_t ws_bytes, void *stream);
+
+/* The whole layer: routing, shared + routed SwiGLU experts over the packed
+ * weights, and the weighted combine with the residual.
+ *   x_d        bf16 [T][H] layer input (read only)
+ *   residual_d bf16 [T][H] or NULL (NULL: the residual is x)
+ *   out_d      bf16 [T][H]; may alias residual_d, must not alias x_d
+ * T == 1 takes the bandwidth-bound decode path unless the plan has
+ * MOE_FLAG_FORCE_GROUPED.  Never allocates or synchronises, so the call can
+ * be captured into a CUDA graph. */
+moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *residual_d, int32_t T,
+                       const moe_weights *w, const float *logit_bias_d, void *out_d, void *ws_d,
+                       size_t ws_bytes, void *stream);
+
+/* Device pointers of the workspace's routing buffers for T tokens (host-side
+ * arithmetic only; nothing is read or enqueued). */
+moe_status moe_route_view(const moe_plan_t *plan, void *ws_d, int32_t T, moe_route_ptrs *out);
+
+/* Unit-gain RMSNorm used between stacked layers (the pages' model is a stack
+ * of 40 such layers; the norm is not printed there):
+ *   x = bf16(r / sqrt(mean(r^2) + eps)), fp32 arithmetic.
+ * r_d, x_d: bf16 [T][H]; H % 8 == 0; r_d may not alias x_d. */
+moe_status moe_rmsnorm(const void *r_d, int32_t T, int32_t H, float eps, void *x_d, void *stream);
+
+/* Dequantise one packed matrix to bf16 (test hook for the rebuild step of
+ * "Prefill"):  w_d[n][k] = bf16_rne(s[n][k/G] * q + b[n][k/G]).
+ * q_d: uint32 [rows][K/8]; s_d, b_d: bf16 [rows][K/G]; w_d: bf16 [rows][K]. */
+moe_status moe_dequant(const uint32_t *q_d, const uint16_t *s_d, const uint16_t *b_d, int32_t rows,
+                       int32_t K, int32_t G, void *w_d, void *stream);
+
+/* Synchronises the stream, reads the workspace's sticky status word into
+ * *host_status, and (if reset != 0) zeroes it.  The only entry point that
+ * synchronises. */
+moe_status moe_device_status(const moe_plan_t *plan, void *ws_d, void *stream, int32_t *host_status,
+                             int32_t reset);
+
+/* Number of kernel launches the last moe_forward/moe_route call on this
+ * thread enqueued (for launch accounting in benchmarks). */
+int32_t moe_last_launch_count(void);
+
+/* Kernels of the library, for moe_profile_events. */
+typedef enum {
+  MOE_KERNEL_ROUTER = 1,         /* router keys, T > 1                        */
+  MOE_KERNEL_TOPK = 2,           /* top-k + histogram                          */
+  MOE_KERNEL_SCATTER = 3,        /* scan + stable scatter + block map          */
+  MOE_KERNEL_GATEUP = 4,         /* grouped gate/up dequant-GEMM + SwiGLU      */
+  MOE_KERNEL_DOWN = 5,           /* grouped down dequant-GEMM                  */
+  MOE_KERNEL_COMBINE = 6,        /* weighted gather-combine + residual         */
+  MOE_KERNEL_DECODE_ROUTER = 7,  /* T == 1: router GEMV + top-k                */
+  MOE_KERNEL_DECODE_GATEUP = 8,  /* T == 1: gate/up GEMV + SwiGLU              */
+  MOE_KERNEL_DECODE_DOWN = 9,    /* T == 1: down GEMV + combine + residual     */
+  MOE_KERNEL_RMSNORM = 10
+} moe_kernel;
+
+/* Profiling hook.  From now on, on the calling thread, the i-th launch of
+ * `kernel` is bracketed by cudaEventRecord(start_events[i % n]) and
+ * cudaEventRecord(stop_events[i % n]) on that launch's stream (also inside a
+ * stream capture, where the records become graph nodes).  start_events and
+ * stop_events are host arrays of n cudaEvent_t handles, copied by the call;
+ * the caller owns the events.  n == 0 (arrays may be NULL) turns the hook off.
+ * Errors: MOE_ERR_INVALID_ARGUMENT for an unknown kernel, n < 0, n > 4096,
+ * null arrays with n > 0, or a null event handle. */
+moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *const *stop_events, int32_t n);
+
+const char *moe_status_str(moe_status s);
+
+/* Text of the CUDA error behind the last MOE_ERR_CUDA returned on the
+ * calling thread ("no error" if there was none). */
+const char *moe_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

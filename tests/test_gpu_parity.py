@@ -1,0 +1,350 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Routing must be bit-exact given identical fp32 keys;
+dequantisation bit-exact; outputs within the layer's tolerance (see
+tests/tolerances.py)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle as orc
+import synthetic as syn
+from tests.tolerances import assert_outputs_close, bf16_value
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import bit_grouped_expert_gb300 as moe  # noqa: E402
+from tests.gpu_util import Layer, dev, dev_weights, host_u16  # noqa: E402
+
+TINY = dict(H=256, E=16, k=4, I=128)
+PATHS = {"tc": 0, "simt": moe.MOE_FLAG_SIMT_EXPERTS}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from bit_grouped_expert_gb300 import build
+    build.build()
+    orc.build()
+    syn.build()
+
+
+@pytest.fixture(scope="module")
+def real():
+    W = syn.experts(0, 257, 2048, 512)
+    W["router"] = syn.router(0, 256, 2048)
+    return W, dev_weights(W)
+
+
+def _tiny(seed, S=1, centred=False, **kw):
+    d = {**TINY, **kw}
+    W = syn.experts(seed, d["E"] + S, d["H"], d["I"], centred=centred)
+    W["router"] = syn.router(seed, d["E"], d["H"])
+    return d, W, dev_weights(W)
+
+
+def _forward(L: Layer, x, Wd, res=None, bias=None, T=None):
+    T = x.shape[0] if T is None else T
+    xd = dev(x)
+    resd = None if res is None else dev(res)
+    out = torch.empty_like(xd)
+    moe.moe_forward(L.plan, xd, resd, T, Wd, None if bias is None else dev(bias), out, L.ws)
+    torch.cuda.synchronize()
+    return host_u16(out)
+
+
+def _route_ref(keys, k, E, S, BN):
+    ids, w = orc.select(keys, k)
+    m = orc.route_maps(ids, E, n_shared=S, BN=BN)
+    return ids, w, m
+
+
+def _assert_routing_equal(got, keys, k, E, S):
+    ids, w, m = _route_ref(keys, k, E, S, got["block_rows"])
+    np.testing.assert_array_equal(got["ids"], ids)
+    np.testing.assert_allclose(got["w"], w, rtol=2e-6, atol=1e-7)
+    np.testing.assert_array_equal(got["counts"], m["counts"])
+    np.testing.assert_array_equal(got["offsets"], m["offsets"])
+    np.testing.assert_array_equal(got["perm"], m["perm"])
+    np.testing.assert_array_equal(got["inv"], m["inv"])
+    assert got["n_tiles"] == m["n_tiles"]
+    np.testing.assert_array_equal(got["blockmap"], m["blockmap"])
+
+
+# ---------------------------------------------------------------- dequant
+
+def test_dequant_bit_exact():
+    rows, K = 256, 2048
+    W = syn.experts(5, 1, K, rows)
+    q, s, b = W["gate_q"][0], W["gate_s"][0], W["gate_b"][0]
+    # add the worked example and edge values: zero scale/bias, ties, tiny bias
+    s = s.copy()
+    b = b.copy()
+    s[0, :] = 0x3C80
+    b[0, :] = 0xBE00
+    s[1, :] = 0
+    b[1, :] = 0
+    s[2, :] = 0x3F81
+    b[2, :] = 0
+    b[3, :] = 0x0001  # subnormal bias
+    wd = torch.empty((rows, K), dtype=torch.int16, device="cuda:0")
+    moe.moe_dequant(dev(q), dev(s), dev(b), rows, K, 64, wd)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host_u16(wd), orc.dequant(q, s, b))
+
+
+# ---------------------------------------------------------------- routing
+
+def test_router_keys_within_fp32_bound(real):
+    W, Wd = real
+    T = 256
+    x = syn.activations(0, T, 2048)
+    bias = syn.zipf_bias(0, 256)
+    L = Layer(max_tokens=T)
+    moe.moe_route(L.plan, dev(x), T, Wd["router"], dev(bias), L.ws)
+    torch.cuda.synchronize()
+    got = L.routing(T)["keys"].astype(np.float64)
+    ref = orc.logits(x, W["router"], bias).astype(np.float64)
+    mag = np.abs(bf16_value(x)) @ np.abs(W["router"].astype(np.float64)).T + np.abs(bias)[None, :]
+    bound = 2048 * 2.0 ** -24 * mag + np.abs(ref) * 2.0 ** -23
+    assert (np.abs(got - ref) <= bound).all()
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("T,zipf", [(256, False), (512, True), (77, False)])
+def test_routing_bit_exact_given_keys(real, path, T, zipf):
+    W, Wd = real
+    x = syn.activations(T, T, 2048)
+    bias = syn.zipf_bias(T, 256) if zipf else None
+    L = Layer(max_tokens=T, flags=PATHS[path])
+    moe.moe_route(L.plan, dev(x), T, Wd["router"], None if bias is None else dev(bias), L.ws)
+    torch.cuda.synchronize()
+    got = L.routing(T)
+    _assert_routing_equal(got, got["keys"], 8, 256, 1)
+    assert L.status() == 0
+
+
+def test_routing_edge_cases_from_keys():
+    E, k = 16, 4
+    L = Layer(H=256, E=E, k=k, I=128, max_tokens=300, flags=moe.MOE_FLAG_SIMT_EXPERTS)
+    BN = L.view(1).block_rows
+    rng = np.random.default_rng(3)
+    T = 2 * BN + 5
+    keys = rng.normal(size=(T, E)).astype(np.float32)
+    # about BN-1, BN, BN+1 rows on experts 1, 2, 3 (rows 5-7 below add a few);
+    # expert 15 is never picked
+    keys[:, 0] = -100
+    keys[:, 15] = -100
+    keys[: BN - 1, 1] = 50
+    keys[:BN, 2] = 49
+    keys[: BN + 1, 3] = 48
+    keys[5, :] = 0.0          # all-equal row -> experts 0..3
+    keys[6, 4:8] = 7.0        # ties -> lower index first
+    keys[7, 9] = -0.0
+    keys[7, 10] = 0.0
+    kd = dev(keys)
+    moe.moe_route_from_logits(L.plan, kd, T, L.ws)
+    torch.cuda.synchronize()
+    got = L.routing(T)
+    np.testing.assert_array_equal(got["keys"], keys)
+    _assert_routing_equal(got, keys, k, E, 1)
+    assert list(got["ids"][5]) == [0, 1, 2, 3] and np.all(got["w"][5] == 0.25)
+    assert L.status() == 0
+
+
+def test_routing_is_deterministic(real):
+    W, Wd = real
+    T = 512
+    x = syn.activations(9, T, 2048)
+    L = Layer(max_tokens=T)
+    outs = []
+    for _ in range(2):
+        moe.moe_route(L.plan, dev(x), T, Wd["router"], None, L.ws)
+        torch.cuda.synchronize()
+        r = L.routing(T)
+        outs.append(np.concatenate([r["perm"], r["inv"], r["ids"].ravel(), r["w"].view(np.int32).ravel()]))
+    np.testing.assert_array_equal(outs[0], outs[1])
+
+
+# ---------------------------------------------------------------- layer, tiny dims
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("T", [2, 3, 7, 33, 100, 300])
+def test_layer_tiny_dims(path, T):
+    d, W, Wd = _tiny(T)
+    x = syn.activations(T, T, d["H"])
+    res = syn.activations(T, T, d["H"], tensor=syn.T_RESID)
+    bias = syn.zipf_bias(T, d["E"])
+    L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=300, flags=PATHS[path])
+    out = _forward(L, x, Wd, res=res, bias=bias)
+    keys = L.routing(T)["keys"]
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, res=res, keys=keys, intermediates=True)
+    assert_outputs_close(out, ref, f"tiny T={T} {path}", k=d["k"])
+    assert L.status() == 0
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_layer_tiny_no_shared_centred(path):
+    T = 65
+    d, W, Wd = _tiny(11, S=0, centred=True)
+    x = syn.activations(11, T, d["H"])
+    L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], S=0, max_tokens=T, flags=PATHS[path])
+    out = _forward(L, x, Wd)
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=0), x, W, keys=L.routing(T)["keys"], intermediates=True)
+    assert_outputs_close(out, ref, k=d["k"], n_shared=0)
+
+
+# ---------------------------------------------------------------- layer, real dims
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_layer_t256_full(real, path):
+    W, Wd = real
+    T = 256
+    x = syn.activations(0, T, 2048)
+    L = Layer(max_tokens=T, flags=PATHS[path])
+    out = _forward(L, x, Wd)
+    ref = orc.moe_layer(orc.Dims(), x, W, keys=L.routing(T)["keys"], intermediates=True)
+    assert_outputs_close(out, ref, f"T=256 {path}")
+    assert L.status() == 0
+
+
+def test_layer_t256_centred_full():
+    W = syn.experts(1, 257, 2048, 512, centred=True)
+    W["router"] = syn.router(1, 256, 2048)
+    Wd = dev_weights(W)
+    T = 256
+    x = syn.activations(1, T, 2048)
+    L = Layer(max_tokens=T)
+    out = _forward(L, x, Wd)
+    ref = orc.moe_layer(orc.Dims(), x, W, keys=L.routing(T)["keys"], intermediates=True)
+    assert_outputs_close(out, ref, "T=256 centred")
+
+
+def test_layer_t512_zipf_sampled(real):
+    W, Wd = real
+    T = 512
+    x = syn.activations(2, T, 2048)
+    bias = syn.zipf_bias(2, 256)
+    L = Layer(max_tokens=T)
+    out = _forward(L, x, Wd, bias=bias)
+    r = L.routing(T)
+    assert (r["counts"] == 0).sum() > 50  # skewed: many experts get no token
+    rows = np.random.default_rng(0).choice(T, 40, replace=False)
+    ref = orc.moe_layer(orc.Dims(), x[rows], W, keys=r["keys"][rows], intermediates=True)
+    assert_outputs_close(out[rows], ref, "T=512 zipf sample")
+
+
+# ---------------------------------------------------------------- decode path
+
+def test_decode_t1_matches_oracle_and_grouped(real):
+    W, Wd = real
+    for seed in (0, 1, 2):
+        x = syn.activations(100 + seed, 1, 2048)
+        res = syn.activations(100 + seed, 1, 2048, tensor=syn.T_RESID)
+        Ld = Layer(max_tokens=1)
+        out_d = _forward(Ld, x, Wd, res=res)
+        keys = Ld.routing(1)["keys"]
+        ref = orc.moe_layer(orc.Dims(), x, W, res=res, keys=keys, intermediates=True)
+        assert_outputs_close(out_d, ref, "decode T=1")
+        ids, w = orc.select(keys, 8)
+        np.testing.assert_array_equal(Ld.routing(1)["ids"], ids)
+        Lg = Layer(max_tokens=1, flags=moe.MOE_FLAG_FORCE_GROUPED)
+        out_g = _forward(Lg, x, Wd, res=res)
+        assert_outputs_close(out_g, ref, "grouped T=1")
+        assert Ld.status() == 0 and Lg.status() == 0
+
+
+def test_decode_tiny_dims_in_place_residual():
+    d, W, Wd = _tiny(21)
+    x = syn.activations(21, 1, d["H"])
+    res = syn.activations(21, 1, d["H"], tensor=syn.T_RESID)
+    L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=4)
+    xd, rd = dev(x), dev(res)
+    moe.moe_forward(L.plan, xd, rd, 1, Wd, None, rd, L.ws)  # out aliases residual
+    torch.cuda.synchronize()
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, res=res, keys=L.routing(1)["keys"], intermediates=True)
+    assert_outputs_close(host_u16(rd), ref, k=d["k"])
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("T", [1, 40])
+def test_zero_expert_weights_return_residual(T):
+    d, W, _ = _tiny(3)
+    for n in ("gate_s", "gate_b", "up_s", "up_b", "down_s", "down_b"):
+        W[n][:] = 0
+    Wd = dev_weights(W)
+    x = syn.activations(4, T, d["H"])
+    res = syn.activations(4, T, d["H"], tensor=syn.T_RESID)
+    for flags in PATHS.values():
+        L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=64, flags=flags)
+        np.testing.assert_array_equal(_forward(L, x, Wd, res=res), res)
+
+
+def test_nonfinite_router_key_sets_status():
+    d, W, Wd = _tiny(5)
+    x = syn.activations(5, 9, d["H"])
+    x[4, 17] = 0x7FC0  # NaN
+    for T, xs in ((9, x), (1, x[4:5])):
+        L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=16)
+        _forward(L, xs, Wd)
+        assert L.status() == moe.MOE_ERR_NONFINITE
+        assert L.status() == 0  # reset by the previous read
+
+
+def test_max_tokens_and_ragged_tail():
+    d, W, Wd = _tiny(6)
+    T = 257
+    x = syn.activations(6, T, d["H"])
+    L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=T)
+    out = _forward(L, x, Wd)
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, keys=L.routing(T)["keys"], intermediates=True)
+    assert_outputs_close(out, ref, k=d["k"])
+    with pytest.raises(moe.MoeError) as ei:
+        _forward(L, syn.activations(6, T + 1, d["H"]), Wd)
+    assert ei.value.status == moe.MOE_ERR_TOO_MANY_TOKENS
+
+
+def test_layer_output_deterministic(real):
+    W, Wd = real
+    x = syn.activations(8, 300, 2048)
+    L = Layer(max_tokens=300)
+    a = _forward(L, x, Wd)
+    b = _forward(L, x, Wd)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_rmsnorm_matches_oracle():
+    r = syn.activations(12, 33, 2048)
+    xd = torch.empty((33, 2048), dtype=torch.int16, device="cuda:0")
+    moe.moe_rmsnorm(dev(r), 33, 2048, 1e-6, xd)
+    torch.cuda.synchronize()
+    got = bf16_value(host_u16(xd))
+    want = bf16_value(orc.rmsnorm(r, 1e-6))
+    # fp32 vs fp64 norm: at most one bf16 step apart
+    assert (np.abs(got - want) <= np.abs(want) * 2.0 ** -7 + 1e-30).all()
+    assert (got == want).mean() > 0.99
+
+
+def test_forward_captures_into_cuda_graph(real):
+    W, Wd = real
+    for T in (1, 64):
+        x = syn.activations(13, T, 2048)
+        L = Layer(max_tokens=64)
+        eager = _forward(L, x, Wd)
+        xd = dev(x)
+        out = torch.empty_like(xd)
+        cw = moe.make_weights(Wd)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                moe.moe_forward(L.plan, xd, None, T, cw, None, out, L.ws, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_u16(out), eager)

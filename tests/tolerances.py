@@ -2,11 +2,20 @@
 
 Outputs: rel-L2 <= 5e-3 and max|err| <= 1e-2 * rms(ref) (the layer's stated
 output tolerance).  ``ref`` is the oracle's fp64 value before its final bf16
-rounding.  The output is bf16, and on these workloads single elements reach
-~10x rms(ref), where half a bf16 ulp alone is ~2.5e-2 * rms(ref): even the
-oracle's own rounded output would fail a bare max-error bound.  The max-error
-bound is therefore applied to the error beyond the output format's own half
-ulp at each element: max(|out - ref| - ulp(ref)/2) <= 1e-2 * rms(ref).
+rounding.
+
+The max-error bound is applied to the error that the layer's own bf16
+rounding points cannot explain.  Two effects exceed it on their own:
+  - the output is bf16, and single elements reach ~10x rms(ref), where half
+    a bf16 ulp is ~2.5e-2 * rms(ref) (the oracle's own rounded output would
+    fail a bare bound);
+  - every expert output y is rounded to bf16 before the combine, in both
+    paths; fp32 (GPU) and fp64 (oracle) sums that land on either side of a
+    rounding boundary give y one ulp apart, and one ulp of a large y (the
+    shared expert enters with weight 1) can exceed 1e-2 * rms(ref).
+So, per element, allowance = ulp(out)/2 + ulp(y_shared) + sum_j w_j ulp(y_j)
+(the oracle's y and w), and the check is
+    max(|out - ref| - allowance) <= 1e-2 * rms(ref).
 """
 from __future__ import annotations
 
@@ -27,7 +36,25 @@ def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
     return 0.5 * np.exp2(e - 7)
 
 
-def output_errors(out_bits: np.ndarray, ref_exact: np.ndarray) -> dict:
+def intermediate_allowance(ref: dict, k: int, n_shared: int) -> np.ndarray:
+    """[T, H] allowance for one-ulp flips of the bf16 expert outputs y, from
+    the oracle's intermediates (ids, w, y in block-map row order)."""
+    ids, w, y = ref["ids"], ref["w"], ref["y"]
+    T = ids.shape[0]
+    yv = np.abs(bf16_value(y))
+    ulp = 2.0 * bf16_half_ulp(yv)
+    perm = np.argsort(ids.ravel(), kind="stable")
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size)
+    allow = np.zeros((T, y.shape[1]))
+    if n_shared:
+        allow += ulp[k * T:k * T + T]
+    for j in range(k):
+        allow += np.abs(w[:, j:j + 1]) * ulp[inv[np.arange(T) * k + j]]
+    return allow
+
+
+def output_errors(out_bits: np.ndarray, ref_exact: np.ndarray, allowance=None) -> dict:
     got = bf16_value(out_bits).ravel()
     ref = np.asarray(ref_exact, np.float64).ravel()
     diff = got - ref
@@ -35,14 +62,24 @@ def output_errors(out_bits: np.ndarray, ref_exact: np.ndarray) -> dict:
     den = float(np.sqrt(np.sum(ref ** 2)))
     rel_l2 = float(np.sqrt(np.sum(diff ** 2)) / den) if den > 0 else float(np.sqrt(np.sum(diff ** 2)))
     beyond = np.abs(diff) - bf16_half_ulp(ref)
+    if allowance is not None:
+        beyond = beyond - np.asarray(allowance, np.float64).ravel()
     max_beyond = float(beyond.max()) if ref.size else 0.0
     return {"rel_l2": rel_l2, "max_beyond_half_ulp": max_beyond, "rms": rms,
             "max_abs": float(np.abs(diff).max()) if ref.size else 0.0,
             "ok": bool(rel_l2 <= REL_L2 and max_beyond <= MAX_ERR_RMS * rms)}
 
 
-def assert_outputs_close(out_bits: np.ndarray, ref_exact: np.ndarray, what: str = "out") -> dict:
-    r = output_errors(out_bits, ref_exact)
+def assert_outputs_close(out_bits: np.ndarray, ref_exact, what: str = "out", k: int = 8,
+                         n_shared: int = 1) -> dict:
+    """``ref_exact``: the oracle's fp64 output, or the oracle's result dict
+    (with intermediates), which adds the allowance for flips of y."""
+    allowance = None
+    if isinstance(ref_exact, dict):
+        if "y" in ref_exact:
+            allowance = intermediate_allowance(ref_exact, k, n_shared)
+        ref_exact = ref_exact["out_exact"]
+    r = output_errors(out_bits, ref_exact, allowance)
     assert r["ok"], f"{what}: rel_l2={r['rel_l2']:.3e} (<= {REL_L2}), max err beyond half-ulp=" \
                     f"{r['max_beyond_half_ulp']:.3e} (<= {MAX_ERR_RMS} * rms {r['rms']:.3e})"
     return r
