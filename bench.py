@@ -281,10 +281,11 @@ def run_ours(args, wl, rank, world, device):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
+    dom_err = None
     try:
         dom_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / n_dom
-    except Exception:
-        dom_ms = None
+    except Exception as ex:  # noqa: BLE001 - reported in the JSON line
+        dom_ms, dom_err = None, f"{type(ex).__name__}: {ex}"[:300]
     if world > 1:
         tt = torch.tensor([ms], device=device, dtype=torch.float64)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
@@ -332,7 +333,7 @@ def run_ours(args, wl, rank, world, device):
                     "kernel": "decode_gateup" if T == 1 else "grouped gate/up",
                     "kernel_ms": round(dom_ms, 5), "peak_src": pk["src"]}
     else:
-        roofline = None
+        roofline = {"error": dom_err}
 
     # end to end: pinned host input -> device, the step, output -> pinned host
     in_rows = 1 if T == 1 else T

@@ -11,7 +11,7 @@ namespace moe {
 // ----------------------------------------------------------------- plan
 
 struct Layout {
-  size_t status, counter, keys, topk_id, topk_w, counts, offsets, perm, inv, blockmap, n_tiles, h, y,
+  size_t status, counter, keys, topk_id, topk_w, counts, offsets, perm, inv, blockmap, n_tiles, h, y, rsplit,
       total;
 };
 
@@ -24,7 +24,8 @@ struct moe_plan {
   int32_t block_rows;  // rows per block-map tile
   int32_t max_tiles;
   int32_t num_sms;
-  bool use_tc;  // tensor-core grouped GEMMs (else the CUDA-core ones)
+  bool use_tc;         // tensor-core grouped GEMMs (else the CUDA-core ones)
+  bool use_router_tc;  // tensor-core router for T >= ROUTER_TC_MIN_T
   moe::Layout lay;
 };
 

@@ -98,26 +98,48 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(const uint16_t *__re
   const uint4 *gq = reinterpret_cast<const uint4 *>(w.gate_q + rq);
   const uint4 *uq = reinterpret_cast<const uint4 *>(w.up_q + rq);
   float ag = 0.f, au = 0.f;
-  for (int u = lane; u < H / 32; u += 32) {
-    const uint4 wg4 = gq[u], wu4 = uq[u];
-    const int g = u >> 1;
-    const __nv_bfloat162 sg = bf16x2_splat(w.gate_s[rg + g]), bg = bf16x2_splat(w.gate_b[rg + g]);
-    const __nv_bfloat162 su = bf16x2_splat(w.up_s[rg + g]), bu = bf16x2_splat(w.up_b[rg + g]);
-    const float *xs = s_x + (u >> 5) * 1024 + (u & 31);
-    const uint32_t wgv[4] = {wg4.x, wg4.y, wg4.z, wg4.w}, wuv[4] = {wu4.x, wu4.y, wu4.z, wu4.w};
+  // every load of the row is issued before any arithmetic (up to 4 x 16 B per
+  // matrix per lane in flight), then the rows are dequantised and reduced
+  constexpr int MAXIT = 4;
+  const int nu = H / 32;
+  for (int u0 = 0; u0 < nu; u0 += 32 * MAXIT) {
+    uint4 wg4[MAXIT], wu4[MAXIT];
+    uint16_t sgv[MAXIT], bgv[MAXIT], suv[MAXIT], buv[MAXIT];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 pg[4], pu[4];
-      dequant_word(wgv[i], sg, bg, pg);
-      dequant_word(wuv[i], su, bu, pu);
+    for (int it = 0; it < MAXIT; ++it) {
+      const int u = u0 + lane + 32 * it;
+      if (u < nu) {
+        wg4[it] = __ldg(gq + u);
+        wu4[it] = __ldg(uq + u);
+        sgv[it] = __ldg(w.gate_s + rg + (u >> 1));
+        bgv[it] = __ldg(w.gate_b + rg + (u >> 1));
+        suv[it] = __ldg(w.up_s + rg + (u >> 1));
+        buv[it] = __ldg(w.up_b + rg + (u >> 1));
+      }
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float x0 = xs[(8 * i + 2 * j) * 32], x1 = xs[(8 * i + 2 * j + 1) * 32];
-        const float2 fg = __bfloat1622float2(pg[j]), fu = __bfloat1622float2(pu[j]);
-        ag = fmaf(x0, fg.x, ag);
-        ag = fmaf(x1, fg.y, ag);
-        au = fmaf(x0, fu.x, au);
-        au = fmaf(x1, fu.y, au);
+    for (int it = 0; it < MAXIT; ++it) {
+      const int u = u0 + lane + 32 * it;
+      if (u >= nu) break;
+      const __nv_bfloat162 sg = bf16x2_splat(sgv[it]), bg = bf16x2_splat(bgv[it]);
+      const __nv_bfloat162 su = bf16x2_splat(suv[it]), bu = bf16x2_splat(buv[it]);
+      const float *xs = s_x + (u >> 5) * 1024 + (u & 31);
+      const uint32_t wgv[4] = {wg4[it].x, wg4[it].y, wg4[it].z, wg4[it].w};
+      const uint32_t wuv[4] = {wu4[it].x, wu4[it].y, wu4[it].z, wu4[it].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 pg[4], pu[4];
+        dequant_word(wgv[i], sg, bg, pg);
+        dequant_word(wuv[i], su, bu, pu);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float x0 = xs[(8 * i + 2 * j) * 32], x1 = xs[(8 * i + 2 * j + 1) * 32];
+          const float2 fg = __bfloat1622float2(pg[j]), fu = __bfloat1622float2(pu[j]);
+          ag = fmaf(x0, fg.x, ag);
+          ag = fmaf(x1, fg.y, ag);
+          au = fmaf(x0, fu.x, au);
+          au = fmaf(x1, fu.y, au);
+        }
       }
     }
   }
@@ -151,40 +173,58 @@ __global__ void __launch_bounds__(256) decode_down_kernel(const uint16_t *__rest
   __syncthreads();
   const int n = blockIdx.x * 8 + warp;
   if (n >= H) return;
+  // all slots' code and scale loads are issued first (one 8-byte chunk of 16
+  // codes per lane per slot and pass), then dequantised and reduced
   float acc[17];
 #pragma unroll
   for (int sl = 0; sl < 17; ++sl) acc[sl] = 0.f;
+  const int nu = I / 16;
+  for (int u0 = 0; u0 < nu; u0 += 32) {
+    const int u = u0 + lane;
+    uint2 wv[17];
+    uint16_t sv[17], bv[17];
 #pragma unroll
-  for (int sl = 0; sl < 17; ++sl) {
-    if (sl >= nslot) break;
-    const int e = s_e[sl];
-    const size_t rq = ((size_t)e * H + n) * (I / 8), rg = ((size_t)e * H + n) * (I / 64);
-    const uint2 *dq = reinterpret_cast<const uint2 *>(w.down_q + rq);
-    float a = 0.f;
-    for (int u = lane; u < I / 16; u += 32) {
-      const uint2 wv = dq[u];
-      const int g = u >> 2;
-      const __nv_bfloat162 s2 = bf16x2_splat(w.down_s[rg + g]), b2 = bf16x2_splat(w.down_b[rg + g]);
-      const float *hs_ = s_h + sl * hs + (u >> 5) * 512 + (u & 31);
-      const uint32_t wvv[2] = {wv.x, wv.y};
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        __nv_bfloat162 p[4];
-        dequant_word(wvv[i], s2, b2, p);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __bfloat1622float2(p[j]);
-          a = fmaf(hs_[(8 * i + 2 * j) * 32], f.x, a);
-          a = fmaf(hs_[(8 * i + 2 * j + 1) * 32], f.y, a);
-        }
+    for (int sl = 0; sl < 17; ++sl) {
+      if (sl < nslot && u < nu) {
+        const size_t r = (size_t)s_e[sl] * H + n;
+        wv[sl] = __ldg(reinterpret_cast<const uint2 *>(w.down_q + r * (I / 8)) + u);
+        sv[sl] = __ldg(w.down_s + r * (I / 64) + (u >> 2));
+        bv[sl] = __ldg(w.down_b + r * (I / 64) + (u >> 2));
       }
     }
-    acc[sl] = warp_sum(a);
+#pragma unroll
+    for (int sl = 0; sl < 17; ++sl) {
+      if (sl < nslot && u < nu) {
+        const __nv_bfloat162 s2 = bf16x2_splat(sv[sl]), b2 = bf16x2_splat(bv[sl]);
+        const float *hs_ = s_h + sl * hs + (u >> 5) * 512 + (u & 31);
+        const uint32_t wvv[2] = {wv[sl].x, wv[sl].y};
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          __nv_bfloat162 p[4];
+          dequant_word(wvv[i], s2, b2, p);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(p[j]);
+            a = fmaf(hs_[(8 * i + 2 * j) * 32], f.x, a);
+            a = fmaf(hs_[(8 * i + 2 * j + 1) * 32], f.y, a);
+          }
+        }
+        acc[sl] += a;
+      }
+    }
   }
+#pragma unroll
+  for (int sl = 0; sl < 17; ++sl)
+    if (sl < nslot) acc[sl] = warp_sum(acc[sl]);
   if (lane == 0) {
     float o = bf16_to_f32(res[n]);
-    if (S) o += bf16_to_f32(f32_to_bf16(acc[k]));
-    for (int sl = 0; sl < k; ++sl) o = fmaf(s_w[sl], bf16_to_f32(f32_to_bf16(acc[sl])), o);
+#pragma unroll
+    for (int sl = 0; sl < 17; ++sl)
+      if (S && sl == k) o += bf16_to_f32(f32_to_bf16(acc[sl]));
+#pragma unroll
+    for (int sl = 0; sl < 16; ++sl)
+      if (sl < k) o = fmaf(s_w[sl], bf16_to_f32(f32_to_bf16(acc[sl])), o);
     out[n] = f32_to_bf16(o);
   }
 }

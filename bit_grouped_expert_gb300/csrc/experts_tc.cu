@@ -1,13 +1,475 @@
-// Tensor-core grouped expert GEMMs (tcgen05): not built yet.
+// Tensor-core grouped expert GEMMs (tcgen05, sm_103a).
+//
+// "Prefill" section of the Lily pages: the 4-bit groupwise-affine weights are
+// rebuilt to bf16 tile by tile inside the grouped GEMM and accumulated in
+// FP32, so no unpacked weight array reaches memory; the grouped GEMMs follow
+// a device-built block map (one tile = up to 128 rows of one expert).
+//
+// One persistent CTA per SM walks work items (block-map tile, 128 output
+// features).  The packed weights are the MMA's A operand (M = 128 rows of
+// output features) and the tile's token rows are B (N = rows rounded up to
+// 16), so a weight tile is rebuilt once for all of an expert's tokens:
+//   warp 0      TMA: packed 4-bit codes, 128 rows x 256 codes per box, 128B
+//               swizzle, one box per matrix per stage of 4 k-blocks
+//   warp 1      one thread issues tcgen05.mma (A from tensor memory, B from
+//               shared memory, D fp32 in tensor memory) and commits
+//   warp 2      cp.async loader of the token rows (gathered through perm for
+//               routed experts) into the 128B-swizzled K-major layout; each
+//               lane's copies arrive on the slot's mbarrier when they land
+//   warp 3      tensor-memory allocation
+//   warps 4-15  three warpgroups: dequantise a k-block of one matrix (64 codes
+//               of a row -> 32 bf16x2, w = bf16_rne(scale*q + bias)) straight
+//               into tensor memory with tcgen05.st, then run the epilogue:
+//               gate/up: h = bf16(silu(g) * u); down: y = bf16(acc)
+// Tensor memory (512 columns): D_gate [0,128), D_up [128,256), four A slots
+// of 64 columns at 256 (gate at +0, up at +32; 32 columns = 64 bf16 of K).
+// Every wait is bounded: after one second the kernel records
+// MOE_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees tensor memory
+// and exits.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "kernels.h"
 #include "tc.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
+namespace {
 
-cudaError_t launch_experts_tc(const moe_plan_t *, const uint16_t *, int, const int32_t *, const int32_t *,
-                              const int32_t *, int, ExpertPtrs, uint16_t *, uint16_t *, int32_t *, int *,
-                              cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int BM = 128;         // output features per work item (= TMEM lanes)
+constexpr int KBLK = 64;        // k-block = one quantisation group
+constexpr int STAGE_KB = 4;     // k-blocks per code stage (one TMA box per matrix)
+constexpr int BOX = BM * 128;   // one TMA box: 128 rows x 128 bytes (256 codes)
+constexpr int NSLOT = 4;        // A slots in TMEM == B slots in shared memory
+constexpr int MAXN = 128;       // token rows per work item
+constexpr int B_SLOT = MAXN * 128;
+constexpr int NWG = 3;                    // dequant/epilogue warpgroups
+constexpr int THREADS = 128 + NWG * 128;  // 4 role warps + the warpgroups
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int D_UP_COL = 128;
+constexpr int A_COL = 256;
+constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
+
+template <bool GATEUP>
+struct Cfg {
+  static constexpr int NMAT = GATEUP ? 2 : 1;
+  static constexpr int CSTAGES = GATEUP ? 4 : 8;
+  static constexpr int STAGE_BYTES = NMAT * BOX;
+  static constexpr int OFF_B = CSTAGES * STAGE_BYTES;
+  static constexpr int OFF_MISC = OFF_B + NSLOT * B_SLOT;
+  static constexpr int SMEM = OFF_MISC + 1024 /* misc */ + 1024 /* alignment slack */;
+};
+
+struct TcArgs {
+  const uint16_t *act;  // activation rows: x [T][K] (gate/up) or h [rows][K] (down)
+  const int32_t *perm, *blockmap, *n_tiles;
+  const uint16_t *sc[2], *bi[2];  // scale / bias arrays of the matrices
+  uint16_t *out;                  // h [rows][NOUT] or y [rows][NOUT]
+  int32_t *status;
+  int T, k, E, K, NOUT;           // K: reduction length; NOUT: output features per expert
+};
+
+struct Misc {
+  uint64_t code_full[8], code_empty[8];
+  uint64_t b_full[NSLOT], a_full[NSLOT], slot_free[NSLOT];
+  uint64_t acc_full, acc_empty, final_bar;
+  uint32_t tmem;
+  int abort_flag;
+  int src[MAXN];
+};
+
+struct Item {
+  int e, row0, nrows, n_mma, mt;
+};
+
+__device__ __forceinline__ Item get_item(const TcArgs &a, int item, int MT) {
+  const int tile = item / MT;
+  Item it;
+  it.mt = item - tile * MT;
+  const int4 ent = reinterpret_cast<const int4 *>(a.blockmap)[tile];
+  it.e = ent.x;
+  it.row0 = ent.y;
+  it.nrows = min(ent.z, MAXN);
+  it.n_mma = max(16, (it.nrows + 15) & ~15);
+  return it;
+}
+
+// Bounded wait on an mbarrier phase; false (and the CTA-wide abort flag) on
+// timeout or when another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Misc *m, int32_t *status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  uint32_t n = 0;
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if ((++n & 31u) == 0) {
+      if (*reinterpret_cast<volatile int *>(&m->abort_flag)) return false;
+      if (ptx::globaltimer() - t0 > TIMEOUT_NS) {
+        *reinterpret_cast<volatile int *>(&m->abort_flag) = 1;
+        set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Bounded wait used while draining after an abort (ignores the abort flag).
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (ptx::globaltimer() - t0 > TIMEOUT_NS) return;
+}
+
+// Scale/bias values of groups g0 .. g0+n-1 of one row (n <= 4).
+__device__ __forceinline__ void load_groups(const uint16_t *p, int n, bool vec, uint16_t (&v)[4]) {
+  if (vec && n == 4) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+    v[0] = u.x & 0xFFFF; v[1] = u.x >> 16; v[2] = u.y & 0xFFFF; v[3] = u.y >> 16;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (i < n) ? __ldg(p + i) : 0;
+  }
+}
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(THREADS, 1)
+    experts_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                      const TcArgs a) {
+  using C = Cfg<GATEUP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Misc *m = reinterpret_cast<Misc *>(smem + C::OFF_MISC);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 3) {
+    ptx::tmem_alloc(&m->tmem, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::CSTAGES; ++i) {
+      ptx::mbar_init(&m->code_full[i], 1);
+      ptx::mbar_init(&m->code_empty[i], NWG * 4);
+    }
+    for (int i = 0; i < NSLOT; ++i) {
+      ptx::mbar_init(&m->b_full[i], 32);  // one cp.async-tracked arrival per loader lane
+      ptx::mbar_init(&m->a_full[i], C::NMAT * 128);  // one warpgroup per (k-block, matrix)
+      ptx::mbar_init(&m->slot_free[i], 1);
+    }
+    ptx::mbar_init(&m->acc_full, 1);
+    ptx::mbar_init(&m->acc_empty, NWG * 128);
+    ptx::mbar_init(&m->final_bar, 1);
+    m->abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = m->tmem;
+
+  const int MT = a.NOUT / BM;
+  const int KB = a.K / KBLK;
+  const int NST = (KB + STAGE_KB - 1) / STAGE_KB;
+  const int n_items = (*a.n_tiles) * MT;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm0);
+      if (GATEUP) ptx::prefetch_tmap(&tm1);
+      uint32_t cs = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const Item it = get_item(a, item, MT);
+        const int row_base = it.e * a.NOUT + it.mt * BM;
+        for (int st = 0; st < NST; ++st, ++cs) {
+          const int slot = cs % C::CSTAGES;
+          const uint32_t ph = (cs / C::CSTAGES) & 1u;
+          if (!wait_bar(&m->code_empty[slot], ph ^ 1u, m, a.status)) {
+            ok = false;
+            break;
+          }
+          const int kb0 = st * STAGE_KB;
+          ptx::mbar_arrive_expect_tx(&m->code_full[slot], (uint32_t)(C::NMAT * BOX));
+          uint8_t *stage = smem + slot * C::STAGE_BYTES;
+          for (int mat = 0; mat < C::NMAT; ++mat)
+            ptx::tma_load_2d(stage + mat * BOX, mat ? &tm1 : &tm0, &m->code_full[slot], kb0 * (KBLK / 2), row_base);
+        }
+      }
+      if (!ok) {  // loads of the last stages may still be in flight
+        const uint32_t n = cs < (uint32_t)C::CSTAGES ? cs : (uint32_t)C::CSTAGES;
+        for (uint32_t i = 1; i <= n; ++i) {
+          const uint32_t c = cs - i;
+          drain_wait(&m->code_full[c % C::CSTAGES], (c / C::CSTAGES) & 1u);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kbc = 0, itc = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const Item it = get_item(a, item, MT);
+        const uint32_t idesc = ptx::idesc_bf16_f32((uint32_t)it.n_mma);
+        if (!wait_bar(&m->acc_empty, (itc & 1u) ^ 1u, m, a.status)) break;
+        ptx::tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb, ++kbc) {
+          const int slot = kbc % NSLOT;
+          const uint32_t ph = (kbc / NSLOT) & 1u;
+          if (!wait_bar(&m->b_full[slot], ph, m, a.status) || !wait_bar(&m->a_full[slot], ph, m, a.status)) {
+            ok = false;
+            break;
+          }
+          ptx::fence_proxy_async_smem();  // token rows were written by cp.async (generic proxy)
+          ptx::tc_fence_after();
+          const uint32_t baddr = ptx::smem_u32(smem + C::OFF_B + slot * B_SLOT);
+#pragma unroll
+          for (int mat = 0; mat < C::NMAT; ++mat)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              ptx::mma_ts(tmem + mat * D_UP_COL, tmem + A_COL + slot * 64 + mat * 32 + i * 8,
+                          ptx::sdesc_sw128(baddr + 32 * i), idesc, (uint32_t)(kb | i));
+          ptx::mma_commit(&m->slot_free[slot]);
+        }
+        if (!ok) break;
+        ptx::mma_commit(&m->acc_full);
+        ++itc;
+      }
+      // every MMA this CTA issued has completed before tensor memory is freed
+      ptx::mma_commit(&m->final_bar);
+      drain_wait(&m->final_bar, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ token-row loader
+    uint32_t kbc = 0;
+    bool ok = true;
+    const int c = lane & 7;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const Item it = get_item(a, item, MT);
+      __syncwarp();
+      for (int r = lane; r < MAXN; r += 32) {
+        int src = -1;
+        if (r < it.nrows) {
+          if (GATEUP)
+            src = (it.e < a.E) ? a.perm[it.row0 + r] / a.k : it.row0 + r - a.k * a.T;
+          else
+            src = it.row0 + r;
+        }
+        m->src[r] = src;
+      }
+      __syncwarp();
+      for (int kb = 0; kb < KB; ++kb, ++kbc) {
+        const int slot = kbc % NSLOT;
+        const uint32_t ph = (kbc / NSLOT) & 1u;
+        if (!__all_sync(0xffffffffu, wait_bar(&m->slot_free[slot], ph ^ 1u, m, a.status))) {
+          ok = false;
+          break;
+        }
+        uint8_t *bs = smem + C::OFF_B + slot * B_SLOT;
+        for (int r = lane >> 3; r < it.n_mma; r += 4) {
+          const int src = m->src[r];
+          const uint16_t *g = a.act + (size_t)(src < 0 ? 0 : src) * a.K + kb * KBLK + c * 8;
+          ptx::cp_async_16(bs + r * 128 + ((c ^ (r & 7)) << 4), g, src < 0 ? 0u : 16u);
+        }
+        ptx::cp_async_arrive_noinc(&m->b_full[slot]);  // fires when this lane's copies have landed
+      }
+    }
+    ptx::cp_async_wait_all();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ dequant + epilogue
+    // Work unit u = kb * NMAT + mat (one k-block of one matrix) goes to
+    // warpgroup u % NWG; epilogue chunks of 16 columns are dealt the same way.
+    const int wg = (warp - 4) >> 2, q = warp & 3;
+    const int row = q * 32 + lane;  // weight row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int groups = a.K / KBLK;
+    const bool vec = (groups % 4) == 0;
+    uint32_t cs = 0, kbc = 0, itc = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const Item it = get_item(a, item, MT);
+      const size_t grow = (size_t)it.e * a.NOUT + (size_t)it.mt * BM + row;
+      for (int st = 0; st < NST; ++st, ++cs) {
+        const int kb0 = st * STAGE_KB, nkb = min(STAGE_KB, KB - kb0);
+        uint16_t sv[C::NMAT][4], bv[C::NMAT][4];
+#pragma unroll
+        for (int mat = 0; mat < C::NMAT; ++mat) {
+          load_groups(a.sc[mat] + grow * groups + kb0, nkb, vec, sv[mat]);
+          load_groups(a.bi[mat] + grow * groups + kb0, nkb, vec, bv[mat]);
+        }
+        const int cslot = cs % C::CSTAGES;
+        if (!__all_sync(0xffffffffu, wait_bar(&m->code_full[cslot], (cs / C::CSTAGES) & 1u, m, a.status))) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int j = 0; j < STAGE_KB; ++j) {
+#pragma unroll
+          for (int mat = 0; mat < C::NMAT; ++mat) {
+            const int u = (kb0 + j) * C::NMAT + mat;
+            if (j >= nkb || u % NWG != wg || !ok) continue;
+            const uint32_t kbg = kbc + j;
+            const uint8_t *rb = smem + cslot * C::STAGE_BYTES + mat * BOX + row * 128;
+            const int c0 = j * 2;
+            const uint4 w0 = *reinterpret_cast<const uint4 *>(rb + ((c0 ^ (row & 7)) << 4));
+            const uint4 w1 = *reinterpret_cast<const uint4 *>(rb + (((c0 + 1) ^ (row & 7)) << 4));
+            const __nv_bfloat162 s2 = bf16x2_splat(sv[mat][j]), b2 = bf16x2_splat(bv[mat][j]);
+            uint32_t v[32];
+            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) {
+              __nv_bfloat162 p[4];
+              dequant_word(wv[wi], s2, b2, p);
+#pragma unroll
+              for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = *reinterpret_cast<uint32_t *>(&p[pi]);
+            }
+            const int aslot = kbg % NSLOT;
+            if (!__all_sync(0xffffffffu,
+                            wait_bar(&m->slot_free[aslot], ((kbg / NSLOT) & 1u) ^ 1u, m, a.status))) {
+              ok = false;
+              continue;
+            }
+            ptx::tc_fence_after();
+            ptx::tmem_st_x32(tmem + lane_base + A_COL + aslot * 64 + mat * 32, v);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&m->a_full[aslot]);
+          }
+        }
+        kbc += nkb;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&m->code_empty[cslot]);
+        if (!ok) break;
+      }
+      if (!ok) break;
+      // epilogue: chunks of 16 token columns dealt round-robin to the warpgroups
+      if (!__all_sync(0xffffffffu, wait_bar(&m->acc_full, itc & 1u, m, a.status))) break;
+      ptx::tc_fence_after();
+      uint16_t *orow = a.out + (size_t)it.row0 * a.NOUT + (size_t)it.mt * BM + row;
+      for (int ch = wg; ch < it.n_mma / 16; ch += NWG) {
+        uint32_t g[16], u[16];
+        ptx::tmem_ld_x16(tmem + lane_base + ch * 16, g);
+        if (GATEUP) ptx::tmem_ld_x16(tmem + lane_base + D_UP_COL + ch * 16, u);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int n = ch * 16 + i;
+          if (n < it.nrows) {
+            const float val = GATEUP ? silu(__uint_as_float(g[i])) * __uint_as_float(u[i]) : __uint_as_float(g[i]);
+            orow[(size_t)n * a.NOUT] = f32_to_bf16(val);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&m->acc_empty);
+      ++itc;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 3) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Packed codes as a 2D byte tensor [rows_total][K/2], boxes of 128 x 128 B.
+cudaError_t code_map(CUtensorMap *map, const uint32_t *codes, int rows_total, int K) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorInitializationError;
+  cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows_total};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(codes), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool tc_supported(const moe_config &c) { return c.hidden % 256 == 0 && c.inter % 256 == 0; }
+
+cudaError_t tc_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(experts_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<true>::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(experts_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<false>::SMEM);
+  return e;
+}
+
+cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
+                              const int32_t *blockmap, const int32_t *n_tiles, int max_tiles, ExpertPtrs w,
+                              uint16_t *h, uint16_t *y, int32_t *status, int *launches, cudaStream_t s) {
+  const moe_config &c = plan->cfg;
+  const int rows_gu = (c.n_experts + c.n_shared) * c.inter;
+  const int rows_dn = (c.n_experts + c.n_shared) * c.hidden;
+  CUtensorMap tg, tu, td;
+  cudaError_t e;
+  if ((e = code_map(&tg, w.gate_q, rows_gu, c.hidden)) != cudaSuccess) return e;
+  if ((e = code_map(&tu, w.up_q, rows_gu, c.hidden)) != cudaSuccess) return e;
+  if ((e = code_map(&td, w.down_q, rows_dn, c.inter)) != cudaSuccess) return e;
+
+  TcArgs a{};
+  a.perm = perm;
+  a.blockmap = blockmap;
+  a.n_tiles = n_tiles;
+  a.status = status;
+  a.T = T;
+  a.k = c.top_k;
+  a.E = c.n_experts;
+
+  // gate/up + SwiGLU: x rows (gathered) -> h
+  a.act = x;
+  a.sc[0] = w.gate_s;
+  a.bi[0] = w.gate_b;
+  a.sc[1] = w.up_s;
+  a.bi[1] = w.up_b;
+  a.out = h;
+  a.K = c.hidden;
+  a.NOUT = c.inter;
+  int items = max_tiles * (c.inter / BM);
+  int grid = items < plan->num_sms ? items : plan->num_sms;
+  prof_before(MOE_KERNEL_GATEUP, s);
+  experts_tc_kernel<true><<<grid, THREADS, Cfg<true>::SMEM, s>>>(tg, tu, a);
+  prof_after(MOE_KERNEL_GATEUP, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  // down: h rows -> y
+  a.act = h;
+  a.sc[0] = w.down_s;
+  a.bi[0] = w.down_b;
+  a.sc[1] = w.down_s;
+  a.bi[1] = w.down_b;
+  a.out = y;
+  a.K = c.inter;
+  a.NOUT = c.hidden;
+  items = max_tiles * (c.hidden / BM);
+  grid = items < plan->num_sms ? items : plan->num_sms;
+  prof_before(MOE_KERNEL_DOWN, s);
+  experts_tc_kernel<false><<<grid, THREADS, Cfg<false>::SMEM, s>>>(td, td, a);
+  prof_after(MOE_KERNEL_DOWN, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  *launches += 2;
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -54,6 +54,7 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles) {
   L.n_tiles = take(16);
   L.h = take((k + S) * T * I * 2);
   L.y = take((k + S) * T * H * 2);
+  L.rsplit = take(3 * E * H * 2);
   L.total = o;
   return L;
 }
@@ -100,9 +101,16 @@ moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const fl
   cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts, s);
   if (err != cudaSuccess) return cuda_status(err);
   if (!from_keys) {
-    if ((err = moe::launch_router_logits(x, T, c.hidden, router, c.n_experts, bias, keys, s)) != cudaSuccess)
-      return cuda_status(err);
-    ++*launches;
+    if (p->use_router_tc && T >= moe::ROUTER_TC_MIN_T) {
+      err = moe::launch_router_tc(x, T, c.hidden, router, c.n_experts, bias, moe::ws_ptr<uint16_t>(ws, L.rsplit), keys,
+                                  status, p->num_sms, s);
+      if (err != cudaSuccess) return cuda_status(err);
+      *launches += 2;
+    } else {
+      if ((err = moe::launch_router_logits(x, T, c.hidden, router, c.n_experts, bias, keys, s)) != cudaSuccess)
+        return cuda_status(err);
+      ++*launches;
+    }
   }
   if ((err = moe::launch_topk(keys, T, c.n_experts, c.top_k, moe::ws_ptr<int32_t>(ws, L.topk_id),
                               moe::ws_ptr<float>(ws, L.topk_w), counts, status, s)) != cudaSuccess)
@@ -136,16 +144,26 @@ moe::ExpertPtrs expert_ptrs(const moe_weights *w) {
 }  // namespace
 
 namespace moe {
+// Inside a stream capture the records become external event-record nodes,
+// which time like ordinary records when the graph runs.
+static void prof_record(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cap);
+  if (cap == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
+}
 void prof_before(int kernel, cudaStream_t s) {
   ProfState *p = g_prof;
   if (!p || p->n == 0 || p->kernel != kernel) return;
-  cudaEventRecord(p->start[p->next % p->n], s);
+  prof_record(p->start[p->next % p->n], s);
   p->open = true;
 }
 void prof_after(int kernel, cudaStream_t s) {
   ProfState *p = g_prof;
   if (!p || p->n == 0 || p->kernel != kernel || !p->open) return;
-  cudaEventRecord(p->stop[p->next % p->n], s);
+  prof_record(p->stop[p->next % p->n], s);
   p->open = false;
   ++p->next;
 }
@@ -211,16 +229,28 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
   p->cfg = c;
   p->max_tokens = max_tokens;
   p->flags = flags;
-  const bool simt = (flags & MOE_FLAG_SIMT_EXPERTS) != 0 || !moe::TC_READY;
+  const bool simt = (flags & MOE_FLAG_SIMT_EXPERTS) != 0 || !moe::tc_supported(c);
   p->use_tc = !simt;
   p->block_rows = simt ? moe::SIMT_ROWS : ((flags & MOE_FLAG_TILE_ROWS_64) ? 64 : moe::TC_ROWS);
   p->max_tiles = tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows);
   p->lay = make_layout(c, max_tokens, p->max_tiles);
   p->num_sms = 0;
+  p->use_router_tc = false;
   int dev = 0, count = 0;
   if (cudaGetDeviceCount(&count) == cudaSuccess && count > 0 && cudaGetDevice(&dev) == cudaSuccess) {
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) p->num_sms = prop.multiProcessorCount;
+    if (p->use_tc && p->num_sms > 0 && moe::tc_prepare() != cudaSuccess) {
+      cudaGetLastError();
+      p->use_tc = false;  // no tensor-core kernels on this device: CUDA-core path
+      p->block_rows = moe::SIMT_ROWS;
+      p->max_tiles = tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows);
+      p->lay = make_layout(c, max_tokens, p->max_tiles);
+    }
+    if (p->num_sms > 0 && moe::router_tc_supported(c.n_experts, c.hidden)) {
+      p->use_router_tc = moe::router_tc_prepare() == cudaSuccess;
+      if (!p->use_router_tc) cudaGetLastError();
+    }
   } else {
     cudaGetLastError();  // no device: host-side checks still work, launches report MOE_ERR_CUDA
   }

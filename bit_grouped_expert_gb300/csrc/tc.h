@@ -10,10 +10,23 @@
 namespace moe {
 
 constexpr int TC_ROWS = 128;     // default token rows per block-map tile
-constexpr bool TC_READY = false;  // the tcgen05 path is selected by default once built
+
+// Dims the tensor-core path handles (H and I multiples of 256); others use
+// the CUDA-core kernels.
+bool tc_supported(const moe_config &c);
+// One-time kernel attributes (dynamic shared memory size); needs a device.
+cudaError_t tc_prepare();
 
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
                               const int32_t *blockmap, const int32_t *n_tiles, int max_tiles, ExpertPtrs w,
                               uint16_t *h, uint16_t *y, int32_t *status, int *launches, cudaStream_t s);
+
+// Router keys on tensor cores (E % 128 == 0, H % 64 == 0).
+bool router_tc_supported(int E, int H);
+cudaError_t router_tc_prepare();
+// split: workspace for three bf16 copies of the router ([3][E][H]).
+cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
+                             uint16_t *split, float *keys, int32_t *status, int num_sms, cudaStream_t s);
+constexpr int ROUTER_TC_MIN_T = 32;  // below this the CUDA-core router is used
 
 }  // namespace moe

@@ -20,7 +20,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU container
 import bit_grouped_expert_gb300 as moe  # noqa: E402
 from tests.gpu_util import Layer, dev, dev_weights, host_u16  # noqa: E402
 
-TINY = dict(H=256, E=16, k=4, I=128)
+TINY = dict(H=256, E=16, k=4, I=256)  # H, I multiples of 256: both expert paths apply
 PATHS = {"tc": 0, "simt": moe.MOE_FLAG_SIMT_EXPERTS}
 
 
@@ -98,11 +98,12 @@ def test_dequant_bit_exact():
 
 # ---------------------------------------------------------------- routing
 
-def test_router_keys_within_fp32_bound(real):
+@pytest.mark.parametrize("T", [16, 256, 300, 2048])
+def test_router_keys_within_fp32_bound(real, T):
+    # T >= 32 runs the tensor-core router (3 x bf16 split), T = 16 the CUDA-core one
     W, Wd = real
-    T = 256
-    x = syn.activations(0, T, 2048)
-    bias = syn.zipf_bias(0, 256)
+    x = syn.activations(T, T, 2048)
+    bias = syn.zipf_bias(T, 256)
     L = Layer(max_tokens=T)
     moe.moe_route(L.plan, dev(x), T, Wd["router"], dev(bias), L.ws)
     torch.cuda.synchronize()
@@ -129,7 +130,7 @@ def test_routing_bit_exact_given_keys(real, path, T, zipf):
 
 def test_routing_edge_cases_from_keys():
     E, k = 16, 4
-    L = Layer(H=256, E=E, k=k, I=128, max_tokens=300, flags=moe.MOE_FLAG_SIMT_EXPERTS)
+    L = Layer(H=256, E=E, k=k, I=256, max_tokens=300, flags=moe.MOE_FLAG_SIMT_EXPERTS)
     BN = L.view(1).block_rows
     rng = np.random.default_rng(3)
     T = 2 * BN + 5
@@ -170,6 +171,24 @@ def test_routing_is_deterministic(real):
 
 
 # ---------------------------------------------------------------- layer, tiny dims
+
+def test_default_plan_uses_tensor_core_path():
+    assert Layer(max_tokens=8).view(1).block_rows == 128
+    assert Layer(max_tokens=8, flags=moe.MOE_FLAG_TILE_ROWS_64).view(1).block_rows == 64
+    assert Layer(max_tokens=8, flags=moe.MOE_FLAG_SIMT_EXPERTS).view(1).block_rows == 32
+
+
+@pytest.mark.parametrize("T", [1, 5, 64, 129, 300])
+def test_tc_tile_rows_64_tiny(T):
+    d, W, Wd = _tiny(40 + T)
+    x = syn.activations(40 + T, T, d["H"])
+    bias = syn.zipf_bias(40 + T, d["E"])
+    L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=300,
+              flags=moe.MOE_FLAG_TILE_ROWS_64 | moe.MOE_FLAG_FORCE_GROUPED)
+    out = _forward(L, x, Wd, bias=bias)
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, bias=bias, keys=L.routing(T)["keys"], intermediates=True)
+    assert_outputs_close(out, ref, f"tc64 T={T}", k=d["k"])
+    assert L.status() == 0
 
 @pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("T", [2, 3, 7, 33, 100, 300])
