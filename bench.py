@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--experts", default="tc", choices=["tc", "simt"], help="grouped GEMM kernels")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (profiling aid; the reported workloads use the default)")
     a = ap.parse_args()
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.workload] if a.impl == "ours" else 5
@@ -429,7 +431,10 @@ def run_reference(args, wl):
 
 def main():
     args = parse()
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    if args.layers is not None:
+        wl["layers"] = args.layers
+        wl["desc"] += f" [profiling override: {args.layers} layers]"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -100,8 +100,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Misc *m
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   uint32_t n = 0;
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if ((++n & 31u) == 0) {
+  while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u)) {
+    if ((++n & 7u) == 0) {
       if (*reinterpret_cast<volatile int *>(&m->abort_flag)) return false;
       if (ptx::globaltimer() - t0 > TIMEOUT_NS) {
         *reinterpret_cast<volatile int *>(&m->abort_flag) = 1;
@@ -120,15 +120,22 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     if (ptx::globaltimer() - t0 > TIMEOUT_NS) return;
 }
 
-// Scale/bias values of groups g0 .. g0+n-1 of one row (n <= 4).
-__device__ __forceinline__ void load_groups(const uint16_t *p, int n, bool vec, uint16_t (&v)[4]) {
-  if (vec && n == 4) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
-    v[0] = u.x & 0xFFFF; v[1] = u.x >> 16; v[2] = u.y & 0xFFFF; v[3] = u.y >> 16;
-  } else {
+// The bf16 values of groups g0 .. g0+n-1 of one row (n <= 4), packed two
+// per 32-bit word (group g0 in the low half of .x).
+__device__ __forceinline__ uint2 load_groups(const uint16_t *p, int n, bool vec) {
+  if (vec && n == 4) return __ldg(reinterpret_cast<const uint2 *>(p));
+  uint16_t v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = (i < n) ? __ldg(p + i) : 0;
-  }
+  for (int i = 0; i < 4; ++i) v[i] = (i < n) ? __ldg(p + i) : 0;
+  return make_uint2(v[0] | ((uint32_t)v[1] << 16), v[2] | ((uint32_t)v[3] << 16));
+}
+
+// bf16x2 with group j's value (of a load_groups word pair) in both halves.
+__device__ __forceinline__ __nv_bfloat162 pick_group(uint2 g, int j) {
+  const uint32_t w = (j & 2) ? g.y : g.x;
+  const uint32_t h = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+  const uint32_t u = h | (h << 16);
+  return *reinterpret_cast<const __nv_bfloat162 *>(&u);
 }
 
 template <bool GATEUP>
@@ -286,55 +293,75 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool vec = (groups % 4) == 0;
     uint32_t cs = 0, kbc = 0, itc = 0;
     bool ok = true;
+    // scales/biases of the next stage are loaded one stage ahead
+    int nitem = blockIdx.x;
+    Item nit = nitem < n_items ? get_item(a, nitem, MT) : Item{0, 0, 0, 16, 0};
+    int nst = 0;
+    uint2 nsv[C::NMAT], nbv[C::NMAT];
+    auto prefetch = [&](const Item &pi, int pst) {
+      const size_t grow = (size_t)pi.e * a.NOUT + (size_t)pi.mt * BM + row;
+      const int kb0 = pst * STAGE_KB, nkb = min(STAGE_KB, KB - kb0);
+#pragma unroll
+      for (int mat = 0; mat < C::NMAT; ++mat) {
+        nsv[mat] = load_groups(a.sc[mat] + grow * groups + kb0, nkb, vec);
+        nbv[mat] = load_groups(a.bi[mat] + grow * groups + kb0, nkb, vec);
+      }
+    };
+    if (nitem < n_items) prefetch(nit, 0);
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const Item it = get_item(a, item, MT);
-      const size_t grow = (size_t)it.e * a.NOUT + (size_t)it.mt * BM + row;
+      const Item it = nit;
       for (int st = 0; st < NST; ++st, ++cs) {
         const int kb0 = st * STAGE_KB, nkb = min(STAGE_KB, KB - kb0);
-        uint16_t sv[C::NMAT][4], bv[C::NMAT][4];
+        uint2 sv[C::NMAT], bv[C::NMAT];
 #pragma unroll
         for (int mat = 0; mat < C::NMAT; ++mat) {
-          load_groups(a.sc[mat] + grow * groups + kb0, nkb, vec, sv[mat]);
-          load_groups(a.bi[mat] + grow * groups + kb0, nkb, vec, bv[mat]);
+          sv[mat] = nsv[mat];
+          bv[mat] = nbv[mat];
         }
+        // advance the prefetch cursor (next stage of this item, or stage 0 of the next item)
+        if (++nst == NST) {
+          nst = 0;
+          nitem += gridDim.x;
+          if (nitem < n_items) nit = get_item(a, nitem, MT);
+        }
+        if (nitem < n_items) prefetch(nit, nst);
         const int cslot = cs % C::CSTAGES;
         if (!__all_sync(0xffffffffu, wait_bar(&m->code_full[cslot], (cs / C::CSTAGES) & 1u, m, a.status))) {
           ok = false;
           break;
         }
+        const int u0 = kb0 * C::NMAT, u1 = (kb0 + nkb) * C::NMAT;
+#pragma unroll 1
+        for (int u = u0 + ((wg - u0 % NWG) + NWG) % NWG; u < u1; u += NWG) {
+          const int j = u / C::NMAT - kb0, mat = u % C::NMAT;
+          const uint32_t kbg = kbc + j;
+          const uint8_t *rb = smem + cslot * C::STAGE_BYTES + mat * BOX + row * 128;
+          const int c0 = j * 2;
+          const uint4 w0 = *reinterpret_cast<const uint4 *>(rb + ((c0 ^ (row & 7)) << 4));
+          const uint4 w1 = *reinterpret_cast<const uint4 *>(rb + (((c0 + 1) ^ (row & 7)) << 4));
+          const uint2 sg = mat ? sv[C::NMAT - 1] : sv[0];
+          const uint2 bg = mat ? bv[C::NMAT - 1] : bv[0];
+          const __nv_bfloat162 s2 = pick_group(sg, j), b2 = pick_group(bg, j);
+          uint32_t v[32];
+          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int j = 0; j < STAGE_KB; ++j) {
+          for (int wi = 0; wi < 8; ++wi) {
+            __nv_bfloat162 p[4];
+            dequant_word(wv[wi], s2, b2, p);
 #pragma unroll
-          for (int mat = 0; mat < C::NMAT; ++mat) {
-            const int u = (kb0 + j) * C::NMAT + mat;
-            if (j >= nkb || u % NWG != wg || !ok) continue;
-            const uint32_t kbg = kbc + j;
-            const uint8_t *rb = smem + cslot * C::STAGE_BYTES + mat * BOX + row * 128;
-            const int c0 = j * 2;
-            const uint4 w0 = *reinterpret_cast<const uint4 *>(rb + ((c0 ^ (row & 7)) << 4));
-            const uint4 w1 = *reinterpret_cast<const uint4 *>(rb + (((c0 + 1) ^ (row & 7)) << 4));
-            const __nv_bfloat162 s2 = bf16x2_splat(sv[mat][j]), b2 = bf16x2_splat(bv[mat][j]);
-            uint32_t v[32];
-            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-            for (int wi = 0; wi < 8; ++wi) {
-              __nv_bfloat162 p[4];
-              dequant_word(wv[wi], s2, b2, p);
-#pragma unroll
-              for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = *reinterpret_cast<uint32_t *>(&p[pi]);
-            }
-            const int aslot = kbg % NSLOT;
-            if (!__all_sync(0xffffffffu,
-                            wait_bar(&m->slot_free[aslot], ((kbg / NSLOT) & 1u) ^ 1u, m, a.status))) {
-              ok = false;
-              continue;
-            }
-            ptx::tc_fence_after();
-            ptx::tmem_st_x32(tmem + lane_base + A_COL + aslot * 64 + mat * 32, v);
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&m->a_full[aslot]);
+            for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = *reinterpret_cast<uint32_t *>(&p[pi]);
           }
+          const int aslot = kbg % NSLOT;
+          if (!__all_sync(0xffffffffu,
+                          wait_bar(&m->slot_free[aslot], ((kbg / NSLOT) & 1u) ^ 1u, m, a.status))) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          ptx::tmem_st_x32(tmem + lane_base + A_COL + aslot * 64 + mat * 32, v);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&m->a_full[aslot]);
         }
         kbc += nkb;
         __syncwarp();
