@@ -31,6 +31,8 @@ MOE_FLAG_DEBUG_CHECKS = 0x1
 MOE_FLAG_FORCE_GROUPED = 0x2
 MOE_FLAG_SIMT_EXPERTS = 0x4
 MOE_FLAG_TILE_ROWS_64 = 0x8
+MOE_FLAG_PRENORM = 0x10
+MOE_FLAG_TRACE = 0x20
 
 EXPORTS = ("moe_plan", "moe_plan_destroy", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_route_from_logits", "moe_forward", "moe_route_view", "moe_rmsnorm", "moe_dequant",
@@ -42,9 +44,7 @@ MOE_KERNEL_SCATTER = 3
 MOE_KERNEL_GATEUP = 4
 MOE_KERNEL_DOWN = 5
 MOE_KERNEL_COMBINE = 6
-MOE_KERNEL_DECODE_ROUTER = 7
-MOE_KERNEL_DECODE_GATEUP = 8
-MOE_KERNEL_DECODE_DOWN = 9
+MOE_KERNEL_DECODE_LAYER = 7
 MOE_KERNEL_RMSNORM = 10
 
 
@@ -68,7 +68,8 @@ class moe_weights(ctypes.Structure):
 
 class moe_route_ptrs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("keys_d", "topk_id_d", "topk_w_d", "counts_d", "offsets_d", "perm_d",
-                                               "inv_d", "blockmap_d", "n_tiles_d", "h_d", "y_d", "status_d")] + \
+                                               "inv_d", "blockmap_d", "n_tiles_d", "h_d", "y_d", "status_d",
+                                               "trace_d")] + \
                [("max_tiles", ctypes.c_int32), ("block_rows", ctypes.c_int32)]
 
 

@@ -12,7 +12,7 @@ namespace moe {
 
 struct Layout {
   size_t status, counter, keys, topk_id, topk_w, counts, offsets, perm, inv, blockmap, n_tiles, h, y, rsplit,
-      total;
+      xn, trace, total;
 };
 
 }  // namespace moe
@@ -26,6 +26,7 @@ struct moe_plan {
   int32_t num_sms;
   bool use_tc;         // tensor-core grouped GEMMs (else the CUDA-core ones)
   bool use_router_tc;  // tensor-core router for T >= ROUTER_TC_MIN_T
+  bool use_decode;     // one-launch decode layer for T == 1
   moe::Layout lay;
 };
 

@@ -50,14 +50,25 @@ constexpr int D_UP_COL = 128;
 constexpr int A_COL = 256;
 constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
 
+constexpr int SBOX = BM * 16;  // one scale (or bias) box: 128 rows x 8 groups of bf16
+
 template <bool GATEUP>
 struct Cfg {
   static constexpr int NMAT = GATEUP ? 2 : 1;
   static constexpr int CSTAGES = GATEUP ? 4 : 8;
-  static constexpr int STAGE_BYTES = NMAT * BOX;
+  // per stage: codes of each matrix, then (scale, bias) boxes of each matrix
+  static constexpr int STAGE_BYTES = NMAT * BOX + NMAT * 2 * SBOX;
   static constexpr int OFF_B = CSTAGES * STAGE_BYTES;
   static constexpr int OFF_MISC = OFF_B + NSLOT * B_SLOT;
   static constexpr int SMEM = OFF_MISC + 1024 /* misc */ + 1024 /* alignment slack */;
+};
+
+// Tensor maps: codes of matrix 0/1, and (when tma_scales) scale/bias of
+// matrix 0/1 as [rows][K/64] bf16 with 128 x 8 boxes.
+struct TcMaps {
+  CUtensorMap code[2];
+  CUtensorMap sc[2];
+  CUtensorMap bi[2];
 };
 
 struct TcArgs {
@@ -67,6 +78,7 @@ struct TcArgs {
   uint16_t *out;                  // h [rows][NOUT] or y [rows][NOUT]
   int32_t *status;
   int T, k, E, K, NOUT;           // K: reduction length; NOUT: output features per expert
+  int tma_scales;                 // scales/biases staged by TMA (K % 512 == 0)
 };
 
 struct Misc {
@@ -140,11 +152,12 @@ __device__ __forceinline__ __nv_bfloat162 pick_group(uint2 g, int j) {
 
 template <bool GATEUP>
 __global__ void __launch_bounds__(THREADS, 1)
-    experts_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-                      const TcArgs a) {
+    experts_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   using C = Cfg<GATEUP>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // offset the shared pointer itself (not an integer cast), so accesses stay
+  // shared-memory loads rather than generic ones
+  uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   Misc *m = reinterpret_cast<Misc *>(smem + C::OFF_MISC);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -181,12 +194,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      ptx::prefetch_tmap(&tm0);
-      if (GATEUP) ptx::prefetch_tmap(&tm1);
+      for (int mat = 0; mat < C::NMAT; ++mat) {
+        ptx::prefetch_tmap(&maps.code[mat]);
+        if (a.tma_scales) {
+          ptx::prefetch_tmap(&maps.sc[mat]);
+          ptx::prefetch_tmap(&maps.bi[mat]);
+        }
+      }
       uint32_t cs = 0;
       bool ok = true;
+      Item nit = blockIdx.x < n_items ? get_item(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const Item it = get_item(a, item, MT);
+        const Item it = nit;  // the next item's block-map entry is loaded one item ahead
+        if (item + (int)gridDim.x < n_items) nit = get_item(a, item + gridDim.x, MT);
         const int row_base = it.e * a.NOUT + it.mt * BM;
         for (int st = 0; st < NST; ++st, ++cs) {
           const int slot = cs % C::CSTAGES;
@@ -196,10 +216,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           const int kb0 = st * STAGE_KB;
-          ptx::mbar_arrive_expect_tx(&m->code_full[slot], (uint32_t)(C::NMAT * BOX));
+          const uint32_t bytes = C::NMAT * (BOX + (a.tma_scales ? 2 * SBOX : 0));
+          ptx::mbar_arrive_expect_tx(&m->code_full[slot], bytes);
           uint8_t *stage = smem + slot * C::STAGE_BYTES;
-          for (int mat = 0; mat < C::NMAT; ++mat)
-            ptx::tma_load_2d(stage + mat * BOX, mat ? &tm1 : &tm0, &m->code_full[slot], kb0 * (KBLK / 2), row_base);
+          for (int mat = 0; mat < C::NMAT; ++mat) {
+            ptx::tma_load_2d(stage + mat * BOX, &maps.code[mat], &m->code_full[slot], kb0 * (KBLK / 2), row_base);
+            if (a.tma_scales) {  // the 8 groups around this stage's 4 (16-byte aligned boxes)
+              uint8_t *sb = stage + C::NMAT * BOX + mat * 2 * SBOX;
+              ptx::tma_load_2d(sb, &maps.sc[mat], &m->code_full[slot], kb0 & ~7, row_base);
+              ptx::tma_load_2d(sb + SBOX, &maps.bi[mat], &m->code_full[slot], kb0 & ~7, row_base);
+            }
+          }
         }
       }
       if (!ok) {  // loads of the last stages may still be in flight
@@ -215,8 +242,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       uint32_t kbc = 0, itc = 0;
       bool ok = true;
+      Item nit = blockIdx.x < n_items ? get_item(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const Item it = get_item(a, item, MT);
+        const Item it = nit;
+        if (item + (int)gridDim.x < n_items) nit = get_item(a, item + gridDim.x, MT);
         const uint32_t idesc = ptx::idesc_bf16_f32((uint32_t)it.n_mma);
         if (!wait_bar(&m->acc_empty, (itc & 1u) ^ 1u, m, a.status)) break;
         ptx::tc_fence_after();
@@ -251,8 +280,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t kbc = 0;
     bool ok = true;
     const int c = lane & 7;
+    Item nit = blockIdx.x < n_items ? get_item(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const Item it = get_item(a, item, MT);
+      const Item it = nit;
+      if (item + (int)gridDim.x < n_items) nit = get_item(a, item + gridDim.x, MT);
       __syncwarp();
       for (int r = lane; r < MAXN; r += 32) {
         int src = -1;
@@ -293,9 +324,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool vec = (groups % 4) == 0;
     uint32_t cs = 0, kbc = 0, itc = 0;
     bool ok = true;
-    // scales/biases of the next stage are loaded one stage ahead
+    // scales/biases of the next stage are loaded one stage ahead; block-map
+    // entries two items ahead
     int nitem = blockIdx.x;
     Item nit = nitem < n_items ? get_item(a, nitem, MT) : Item{0, 0, 0, 16, 0};
+    Item nit2 = nitem + (int)gridDim.x < n_items ? get_item(a, nitem + gridDim.x, MT) : Item{0, 0, 0, 16, 0};
     int nst = 0;
     uint2 nsv[C::NMAT], nbv[C::NMAT];
     auto prefetch = [&](const Item &pi, int pst) {
@@ -307,7 +340,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         nbv[mat] = load_groups(a.bi[mat] + grow * groups + kb0, nkb, vec);
       }
     };
-    if (nitem < n_items) prefetch(nit, 0);
+    if (nitem < n_items && !a.tma_scales) prefetch(nit, 0);
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const Item it = nit;
       for (int st = 0; st < NST; ++st, ++cs) {
@@ -322,13 +355,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (++nst == NST) {
           nst = 0;
           nitem += gridDim.x;
-          if (nitem < n_items) nit = get_item(a, nitem, MT);
+          nit = nit2;
+          if (nitem + (int)gridDim.x < n_items) nit2 = get_item(a, nitem + gridDim.x, MT);
         }
-        if (nitem < n_items) prefetch(nit, nst);
+        if (nitem < n_items && !a.tma_scales) prefetch(nit, nst);
         const int cslot = cs % C::CSTAGES;
         if (!__all_sync(0xffffffffu, wait_bar(&m->code_full[cslot], (cs / C::CSTAGES) & 1u, m, a.status))) {
           ok = false;
           break;
+        }
+        if (a.tma_scales) {  // this row's 8 groups of the box; the stage uses 4 of them
+          const uint8_t *sb = smem + cslot * C::STAGE_BYTES + C::NMAT * BOX + row * 16 + (kb0 & 4) * 2;
+#pragma unroll
+          for (int mat = 0; mat < C::NMAT; ++mat) {
+            sv[mat] = *reinterpret_cast<const uint2 *>(sb + mat * 2 * SBOX);
+            bv[mat] = *reinterpret_cast<const uint2 *>(sb + mat * 2 * SBOX + SBOX);
+          }
         }
         const int u0 = kb0 * C::NMAT, u1 = (kb0 + nkb) * C::NMAT;
 #pragma unroll 1
@@ -416,6 +458,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Scales or biases as a 2D bf16 tensor [rows_total][K/64], boxes of 128 rows x
+// 8 groups (16 bytes), no swizzle.
+cudaError_t group_map(CUtensorMap *map, const uint16_t *p, int rows_total, int K) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorInitializationError;
+  cuuint64_t dims[2] = {(cuuint64_t)(K / KBLK), (cuuint64_t)rows_total};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / KBLK) * 2};
+  cuuint32_t box[2] = {8, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(p), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Packed codes as a 2D byte tensor [rows_total][K/2], boxes of 128 x 128 B.
 cudaError_t code_map(CUtensorMap *map, const uint32_t *codes, int rows_total, int K) {
   auto enc = encode_fn();
@@ -449,11 +506,22 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   const moe_config &c = plan->cfg;
   const int rows_gu = (c.n_experts + c.n_shared) * c.inter;
   const int rows_dn = (c.n_experts + c.n_shared) * c.hidden;
-  CUtensorMap tg, tu, td;
+  TcMaps mg{}, md{};
   cudaError_t e;
-  if ((e = code_map(&tg, w.gate_q, rows_gu, c.hidden)) != cudaSuccess) return e;
-  if ((e = code_map(&tu, w.up_q, rows_gu, c.hidden)) != cudaSuccess) return e;
-  if ((e = code_map(&td, w.down_q, rows_dn, c.inter)) != cudaSuccess) return e;
+  const bool ts_gu = c.hidden % 512 == 0, ts_dn = c.inter % 512 == 0;
+  if ((e = code_map(&mg.code[0], w.gate_q, rows_gu, c.hidden)) != cudaSuccess) return e;
+  if ((e = code_map(&mg.code[1], w.up_q, rows_gu, c.hidden)) != cudaSuccess) return e;
+  if ((e = code_map(&md.code[0], w.down_q, rows_dn, c.inter)) != cudaSuccess) return e;
+  if (ts_gu) {
+    if ((e = group_map(&mg.sc[0], w.gate_s, rows_gu, c.hidden)) != cudaSuccess) return e;
+    if ((e = group_map(&mg.bi[0], w.gate_b, rows_gu, c.hidden)) != cudaSuccess) return e;
+    if ((e = group_map(&mg.sc[1], w.up_s, rows_gu, c.hidden)) != cudaSuccess) return e;
+    if ((e = group_map(&mg.bi[1], w.up_b, rows_gu, c.hidden)) != cudaSuccess) return e;
+  }
+  if (ts_dn) {
+    if ((e = group_map(&md.sc[0], w.down_s, rows_dn, c.inter)) != cudaSuccess) return e;
+    if ((e = group_map(&md.bi[0], w.down_b, rows_dn, c.inter)) != cudaSuccess) return e;
+  }
 
   TcArgs a{};
   a.perm = perm;
@@ -473,10 +541,11 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.out = h;
   a.K = c.hidden;
   a.NOUT = c.inter;
+  a.tma_scales = ts_gu;
   int items = max_tiles * (c.inter / BM);
   int grid = items < plan->num_sms ? items : plan->num_sms;
   prof_before(MOE_KERNEL_GATEUP, s);
-  experts_tc_kernel<true><<<grid, THREADS, Cfg<true>::SMEM, s>>>(tg, tu, a);
+  experts_tc_kernel<true><<<grid, THREADS, Cfg<true>::SMEM, s>>>(mg, a);
   prof_after(MOE_KERNEL_GATEUP, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -489,10 +558,11 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.out = y;
   a.K = c.inter;
   a.NOUT = c.hidden;
+  a.tma_scales = ts_dn;
   items = max_tiles * (c.hidden / BM);
   grid = items < plan->num_sms ? items : plan->num_sms;
   prof_before(MOE_KERNEL_DOWN, s);
-  experts_tc_kernel<false><<<grid, THREADS, Cfg<false>::SMEM, s>>>(td, td, a);
+  experts_tc_kernel<false><<<grid, THREADS, Cfg<false>::SMEM, s>>>(md, a);
   prof_after(MOE_KERNEL_DOWN, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   *launches += 2;

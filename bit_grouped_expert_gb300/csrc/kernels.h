@@ -38,10 +38,12 @@ cudaError_t launch_rmsnorm(const uint16_t *r, int T, int H, float eps, uint16_t 
 cudaError_t launch_dequant(const uint32_t *q, const uint16_t *sc, const uint16_t *b, int rows, int K, int G,
                            uint16_t *w, cudaStream_t s);
 
-// decode.cu (T == 1)
-cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, int k, int I, int S,
-                          const float *router, const float *bias, ExpertPtrs w, float *keys, int32_t *topk_id,
-                          float *topk_w, int32_t *counter, uint16_t *hbuf, uint16_t *out, int32_t *status,
-                          int *launches, cudaStream_t s);
+// decode.cu (T == 1: the whole layer as one cooperative launch)
+bool decode_supported(int H, int E, int k, int I, int S, int num_sms);
+cudaError_t decode_prepare(int H, int E, int k, int I, int S, int num_sms);
+cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, int k, int I, int S, int prenorm,
+                          float eps, const float *router, const float *bias, ExpertPtrs w, float *keys,
+                          int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf, uint16_t *out,
+                          int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s);
 
 }  // namespace moe

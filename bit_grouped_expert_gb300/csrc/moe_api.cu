@@ -55,6 +55,8 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles) {
   L.h = take((k + S) * T * I * 2);
   L.y = take((k + S) * T * H * 2);
   L.rsplit = take(3 * E * H * 2);
+  L.xn = take(T * H * 2);  // normalised x of pre-norm plans
+  L.trace = take(3 * 16 * 8);
   L.total = o;
   return L;
 }
@@ -214,7 +216,7 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
   if (!cfg || !out) return MOE_ERR_INVALID_ARGUMENT;
   *out = nullptr;
   const uint32_t known = MOE_FLAG_DEBUG_CHECKS | MOE_FLAG_FORCE_GROUPED | MOE_FLAG_SIMT_EXPERTS |
-                         MOE_FLAG_TILE_ROWS_64;
+                         MOE_FLAG_TILE_ROWS_64 | MOE_FLAG_PRENORM | MOE_FLAG_TRACE;
   if (flags & ~known) return MOE_ERR_INVALID_ARGUMENT;
   if (max_tokens < 1 || max_tokens > 65536) return MOE_ERR_INVALID_ARGUMENT;
   const moe_config &c = *cfg;
@@ -222,8 +224,6 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
   if (c.hidden % 128 || c.inter % 64 || c.group_size != 64 || c.n_experts > 1024 || c.top_k > 16 ||
       c.top_k > c.n_experts || (c.n_shared != 0 && c.n_shared != 1) || c.hidden > 12288 || c.inter > 8192)
     return MOE_ERR_UNSUPPORTED;
-  // the decode path stages h of every slot in 48 KB of shared memory
-  if ((size_t)(c.top_k + c.n_shared) * ((c.inter + 511) / 512) * 512 * 4 > 48 * 1024) return MOE_ERR_UNSUPPORTED;
   moe_plan_t *p = new (std::nothrow) moe_plan_t;
   if (!p) return MOE_ERR_INVALID_ARGUMENT;
   p->cfg = c;
@@ -236,6 +236,7 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
   p->lay = make_layout(c, max_tokens, p->max_tiles);
   p->num_sms = 0;
   p->use_router_tc = false;
+  p->use_decode = false;
   int dev = 0, count = 0;
   if (cudaGetDeviceCount(&count) == cudaSuccess && count > 0 && cudaGetDevice(&dev) == cudaSuccess) {
     cudaDeviceProp prop;
@@ -246,6 +247,12 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
       p->block_rows = moe::SIMT_ROWS;
       p->max_tiles = tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows);
       p->lay = make_layout(c, max_tokens, p->max_tiles);
+    }
+    if (p->num_sms > 0 &&
+        moe::decode_supported(c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, p->num_sms)) {
+      p->use_decode =
+          moe::decode_prepare(c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, p->num_sms) == cudaSuccess;
+      if (!p->use_decode) cudaGetLastError();
     }
     if (p->num_sms > 0 && moe::router_tc_supported(c.n_experts, c.hidden)) {
       p->use_router_tc = moe::router_tc_prepare() == cudaSuccess;
@@ -314,8 +321,10 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
   g_last_launches = 0;
   moe_status st = check_call(plan, T, ws_d, ws_bytes);
   if (st != MOE_OK) return st;
+  const bool prenorm = (plan->flags & MOE_FLAG_PRENORM) != 0;
   if (!x_d || !w || !out_d || !weights_present(w)) return MOE_ERR_INVALID_ARGUMENT;
-  if (out_d == x_d) return MOE_ERR_INVALID_ARGUMENT;
+  if (out_d == x_d && !prenorm) return MOE_ERR_INVALID_ARGUMENT;
+  if (prenorm && residual_d) return MOE_ERR_INVALID_ARGUMENT;
   if (!moe::aligned16(x_d) || !moe::aligned16(residual_d) || !moe::aligned16(out_d) ||
       !moe::aligned16(logit_bias_d) || !weights_aligned(w))
     return MOE_ERR_MISALIGNED;
@@ -330,15 +339,24 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
   int32_t *status = moe::ws_ptr<int32_t>(ws_d, L.status);
   int launches = 0;
 
-  if (T == 1 && !(plan->flags & MOE_FLAG_FORCE_GROUPED)) {
+  if (T == 1 && plan->use_decode && !(plan->flags & MOE_FLAG_FORCE_GROUPED)) {
     cudaError_t err = moe::launch_decode(
-        x, res, c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, w->router_d, logit_bias_d, ep,
-        moe::ws_ptr<float>(ws_d, L.keys), moe::ws_ptr<int32_t>(ws_d, L.topk_id), moe::ws_ptr<float>(ws_d, L.topk_w),
-        moe::ws_ptr<int32_t>(ws_d, L.counter), moe::ws_ptr<uint16_t>(ws_d, L.h), out, status, &launches, s);
+        x, res, c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, prenorm ? 1 : 0, 1e-6f, w->router_d,
+        logit_bias_d, ep, moe::ws_ptr<float>(ws_d, L.keys), moe::ws_ptr<int32_t>(ws_d, L.topk_id),
+        moe::ws_ptr<float>(ws_d, L.topk_w), moe::ws_ptr<unsigned long long>(ws_d, L.counter),
+        moe::ws_ptr<uint16_t>(ws_d, L.h), out, status,
+        (plan->flags & MOE_FLAG_TRACE) ? moe::ws_ptr<uint64_t>(ws_d, L.trace) : nullptr, plan->num_sms, &launches, s);
     g_last_launches = launches;
     return cuda_status(err);
   }
 
+  if (prenorm) {  // x = RMSNorm(r) into the workspace; the residual is r
+    uint16_t *xn = moe::ws_ptr<uint16_t>(ws_d, L.xn);
+    cudaError_t err = moe::launch_rmsnorm(x, T, c.hidden, 1e-6f, xn, s);
+    if (err != cudaSuccess) return cuda_status(err);
+    ++launches;
+    x = xn;
+  }
   st = enqueue_route(plan, x, T, w->router_d, logit_bias_d, ws_d, false, s, &launches);
   if (st != MOE_OK) return st;
   const int max_tiles = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, plan->block_rows);
@@ -383,6 +401,7 @@ moe_status moe_route_view(const moe_plan_t *plan, void *ws_d, int32_t T, moe_rou
   out->h_d = moe::ws_ptr<uint16_t>(ws_d, L.h);
   out->y_d = moe::ws_ptr<uint16_t>(ws_d, L.y);
   out->status_d = moe::ws_ptr<int32_t>(ws_d, L.status);
+  out->trace_d = moe::ws_ptr<uint64_t>(ws_d, L.trace);
   out->max_tiles = tiles_bound(T, plan->cfg.top_k, plan->cfg.n_experts, plan->cfg.n_shared, plan->block_rows);
   out->block_rows = plan->block_rows;
   return MOE_OK;

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t *__re
 // ---------------------------------------------------------------- top-k
 // (per-token selection: topk.cuh)
 template <int KPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ keys, int T, int E, int k,
+__global__ void __launch_bounds__(64) topk_kernel(const float *__restrict__ keys, int T, int E, int k,
                                                    int32_t *__restrict__ topk_id, float *__restrict__ topk_w,
                                                    int32_t *__restrict__ counts, int32_t *__restrict__ status) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
@@ -198,21 +198,22 @@ cudaError_t launch_router_logits(const uint16_t *x, int T, int H, const float *r
 
 cudaError_t launch_topk(const float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
                         int32_t *status, cudaStream_t s) {
-  const int blocks = (T + 7) / 8;
+  // two tokens (warps) per block, so small T still spreads over many SMs
+  const int blocks = (T + 1) / 2;
   const int kpl = (E + 31) / 32;
   prof_before(MOE_KERNEL_TOPK, s);
   if (kpl <= 1)
-    topk_kernel<1><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    topk_kernel<1><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
   else if (kpl <= 2)
-    topk_kernel<2><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    topk_kernel<2><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
   else if (kpl <= 4)
-    topk_kernel<4><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    topk_kernel<4><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
   else if (kpl <= 8)
-    topk_kernel<8><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    topk_kernel<8><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
   else if (kpl <= 16)
-    topk_kernel<16><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    topk_kernel<16><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
   else
-    topk_kernel<32><<<blocks, 256, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    topk_kernel<32><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
   prof_after(MOE_KERNEL_TOPK, s);
   return cudaGetLastError();
 }

@@ -110,7 +110,9 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                      const RArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // offset the shared pointer itself (not an integer cast), so accesses stay
+  // shared-memory loads rather than generic ones
+  uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   RMisc *m = reinterpret_cast<RMisc *>(smem + RSTAGES * R_STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 3) {

@@ -1,76 +1,82 @@
 // Per-token top-k selection shared by the grouped and the decode routing.
 // Selection ("three workload shapes": the router scores every expert and
-// picks k): the k best keys under `precedes` (larger first, ties to the lower
-// index, NaN last), weights = softmax over the k picked keys.
+// picks k): the k best keys under this order -- larger key first, equal keys
+// by the lower expert index, NaN below every number, -0 == +0 -- and the
+// weights are a softmax over the k picked keys.
+//
+// A (key, expert) pair is encoded as one 64-bit integer whose unsigned order
+// is exactly that order, so selection is plain integer max / compare:
+//   high word: the fp32 key mapped to an order-preserving unsigned integer
+//              (NaN -> 0, below every number; -0 mapped to +0)
+//   low word : 0xFFFFFFFF - expert (lower index -> larger)
 #pragma once
 #include "common.cuh"
 
 namespace moe {
 
-// One warp per token.  Lane l holds keys l, l+32, ...; k rounds of a warp
-// arg-best under `precedes`; lane j keeps the j-th pick.
-template <int KPL>
-__device__ __forceinline__ void topk_row(const float *__restrict__ row, int E, int k, int lane,
-                                         int &my_id, float &my_key) {
-  float key[KPL];
-  uint32_t taken = 0;
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    int e = lane + 32 * i;
-    if (e < E)
-      key[i] = row[e];
-    else {
-      key[i] = 0.f;
-      taken |= 1u << i;
-    }
-  }
-  my_id = -1;
-  my_key = 0.f;
-  for (int r = 0; r < k; ++r) {
-    float bk = 0.f;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      if (taken & (1u << i)) continue;
-      int e = lane + 32 * i;
-      if (bi == 0x7fffffff || precedes(key[i], e, bk, bi)) {
-        bk = key[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || precedes(ok, oi, bk, bi))) {
-        bk = ok;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (r == lane) {
-      my_id = bi;
-      my_key = bk;
-    }
-  }
+__device__ __forceinline__ unsigned long long topk_code(float key, int e) {
+  uint32_t u = __float_as_uint(key);
+  if (u == 0x80000000u) u = 0u;  // -0 == +0
+  uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  if (isnan(key)) o = 0u;
+  return ((unsigned long long)o << 32) | (0xFFFFFFFFu - (uint32_t)e);
 }
 
-template <int KPL>
-__device__ void topk_token(const float *__restrict__ row, int E, int k, int lane, int32_t *__restrict__ ids_out,
-                           float *__restrict__ w_out, int32_t *__restrict__ counts, int32_t *__restrict__ status) {
-  int my_id;
-  float my_key;
-  topk_row<KPL>(row, E, k, lane, my_id, my_key);
+__device__ __forceinline__ int topk_code_expert(unsigned long long c) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(c & 0xFFFFFFFFull));
+}
+
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int o) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, o);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), o);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+// Weights of the picked keys: softmax over the k picked keys (max = slot 0),
+// written with the ids; lane j < k owns slot j.  NaN/Inf keys set the status.
+__device__ __forceinline__ void topk_finish(int lane, int k, int my_id, float my_key, int32_t *__restrict__ ids_out,
+                                            float *__restrict__ w_out, int32_t *__restrict__ counts,
+                                            int32_t *__restrict__ status) {
   const float l0 = __shfl_sync(0xffffffffu, my_key, 0);
-  float ex = (lane < k) ? expf(my_key - l0) : 0.f;
-  float den = warp_sum(ex);
-  bool bad = (lane < k) && !isfinite(my_key);
+  const float ex = (lane < k) ? expf(my_key - l0) : 0.f;
+  const float den = warp_sum(ex);
+  const bool bad = (lane < k) && !isfinite(my_key);
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
   if (lane < k) {
     ids_out[lane] = my_id;
     w_out[lane] = ex / den;
     if (counts) atomicAdd(&counts[my_id], 1);
   }
+}
+
+// One warp selects a token's top k (k <= 32) from E <= 32*KPL keys.  Lane l
+// holds experts l, l+32, ...; each round takes the warp-wide largest code.
+template <int KPL>
+__device__ void topk_token(const float *__restrict__ row, int E, int k, int lane, int32_t *__restrict__ ids_out,
+                           float *__restrict__ w_out, int32_t *__restrict__ counts, int32_t *__restrict__ status) {
+  unsigned long long c[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int e = lane + 32 * i;
+    c[i] = (e < E) ? topk_code(row[e], e) : 0ull;  // 0: below every real code
+  }
+  int my_id = -1;
+  float my_key = 0.f;
+  for (int r = 0; r < k; ++r) {
+    unsigned long long best = c[0];
+#pragma unroll
+    for (int i = 1; i < KPL; ++i) best = c[i] > best ? c[i] : best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = shfl_xor_u64(best, o);
+      best = other > best ? other : best;
+    }
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) c[i] = (c[i] == best) ? 0ull : c[i];  // the owner drops it
+    if (r == lane) my_id = topk_code_expert(best);
+  }
+  if (lane < k) my_key = row[my_id];
+  topk_finish(lane, k, my_id, my_key, ids_out, w_out, counts, status);
 }
 
 }  // namespace moe

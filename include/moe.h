@@ -97,6 +97,7 @@ typedef struct {
   uint16_t *h_d;       /* [(k+S)*T][I] bf16 SwiGLU rows (routed in perm order, then shared) */
   uint16_t *y_d;       /* [(k+S)*T][H] bf16 expert outputs, same row order    */
   int32_t *status_d;   /* [1] sticky device status (moe_status values)        */
+  uint64_t *trace_d;   /* [3][16] phase timestamps (ns) of MOE_FLAG_TRACE plans */
   int32_t max_tiles;   /* capacity of blockmap_d                             */
   int32_t block_rows;  /* rows per block-map tile for this plan              */
 } moe_route_ptrs;
@@ -106,6 +107,12 @@ typedef struct {
 #define MOE_FLAG_FORCE_GROUPED  0x2u  /* T == 1 runs the grouped path instead of the decode path */
 #define MOE_FLAG_SIMT_EXPERTS   0x4u  /* CUDA-core grouped GEMMs instead of the tensor-core ones */
 #define MOE_FLAG_TILE_ROWS_64   0x8u  /* tensor-core path: 64-token tiles instead of 128 */
+#define MOE_FLAG_TRACE          0x20u /* decode layer: record %globaltimer at each phase of CTAs 0,
+                                         G/2 and G-1 into moe_route_ptrs.trace_d (tracing aid) */
+#define MOE_FLAG_PRENORM        0x10u /* pre-norm block: x_d is the residual stream r, the layer
+                                         computes x = RMSNorm(r) (unit gain, eps 1e-6) and
+                                         out = r + MoE(x); residual_d must be NULL and out_d
+                                         may alias x_d (in-place residual update) */
 
 typedef struct moe_plan moe_plan_t;
 
@@ -139,12 +146,13 @@ moe_status moe_route_from_logits(const moe_plan_t *plan, const float *keys_d, in
 
 /* The whole layer: routing, shared + routed SwiGLU experts over the packed
  * weights, and the weighted combine with the residual.
- *   x_d        bf16 [T][H] layer input (read only)
- *   residual_d bf16 [T][H] or NULL (NULL: the residual is x)
- *   out_d      bf16 [T][H]; may alias residual_d, must not alias x_d
- * T == 1 takes the bandwidth-bound decode path unless the plan has
- * MOE_FLAG_FORCE_GROUPED.  Never allocates or synchronises, so the call can
- * be captured into a CUDA graph. */
+ *   x_d        bf16 [T][H] layer input (read only), or with MOE_FLAG_PRENORM
+ *              the residual stream r (the layer normalises it itself)
+ *   residual_d bf16 [T][H] or NULL (NULL: the residual is x); NULL with PRENORM
+ *   out_d      bf16 [T][H]; may alias residual_d; may alias x_d only with PRENORM
+ * T == 1 takes the bandwidth-bound decode path (one cooperative launch per
+ * layer, "Decode" section) unless the plan has MOE_FLAG_FORCE_GROUPED.  Never
+ * allocates or synchronises, so the call can be captured into a CUDA graph. */
 moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *residual_d, int32_t T,
                        const moe_weights *w, const float *logit_bias_d, void *out_d, void *ws_d,
                        size_t ws_bytes, void *stream);
@@ -183,9 +191,7 @@ typedef enum {
   MOE_KERNEL_GATEUP = 4,         /* grouped gate/up dequant-GEMM + SwiGLU      */
   MOE_KERNEL_DOWN = 5,           /* grouped down dequant-GEMM                  */
   MOE_KERNEL_COMBINE = 6,        /* weighted gather-combine + residual         */
-  MOE_KERNEL_DECODE_ROUTER = 7,  /* T == 1: router GEMV + top-k                */
-  MOE_KERNEL_DECODE_GATEUP = 8,  /* T == 1: gate/up GEMV + SwiGLU              */
-  MOE_KERNEL_DECODE_DOWN = 9,    /* T == 1: down GEMV + combine + residual     */
+  MOE_KERNEL_DECODE_LAYER = 7,   /* T == 1: the whole layer in one launch      */
   MOE_KERNEL_RMSNORM = 10
 } moe_kernel;
 

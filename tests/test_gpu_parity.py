@@ -288,6 +288,38 @@ def test_decode_tiny_dims_in_place_residual():
     assert_outputs_close(host_u16(rd), ref, k=d["k"])
 
 
+@pytest.mark.parametrize("T", [1, 37])
+def test_prenorm_in_place_matches_oracle(T):
+    # pre-norm block: out = r + MoE(RMSNorm(r)), written over r
+    d, W, Wd = _tiny(60 + T)
+    r = syn.activations(60 + T, T, d["H"], tensor=syn.T_RESID)
+    L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=64, flags=moe.MOE_FLAG_PRENORM)
+    rd = dev(r)
+    moe.moe_forward(L.plan, rd, None, T, Wd, None, rd, L.ws)
+    torch.cuda.synchronize()
+    x = orc.rmsnorm(r, 1e-6)
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, res=r, keys=L.routing(T)["keys"], intermediates=True)
+    assert_outputs_close(host_u16(rd), ref, f"prenorm T={T}", k=d["k"])
+    assert L.status() == 0
+
+
+def test_decode_real_dims_prenorm_and_deterministic(real):
+    W, Wd = real
+    r = syn.activations(77, 1, 2048, tensor=syn.T_RESID)
+    L = Layer(max_tokens=1, flags=moe.MOE_FLAG_PRENORM)
+    outs = []
+    for _ in range(3):
+        rd = dev(r)
+        moe.moe_forward(L.plan, rd, None, 1, Wd, None, rd, L.ws)
+        torch.cuda.synchronize()
+        outs.append(host_u16(rd))
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
+    ref = orc.moe_layer(orc.Dims(), orc.rmsnorm(r, 1e-6), W, res=r, keys=L.routing(1)["keys"], intermediates=True)
+    assert_outputs_close(outs[0], ref, "decode prenorm")
+    assert L.status() == 0
+
+
 # ---------------------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("T", [1, 40])
