@@ -36,7 +36,10 @@ MOE_FLAG_TRACE = 0x20
 
 EXPORTS = ("moe_plan", "moe_plan_destroy", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_route_from_logits", "moe_forward", "moe_route_view", "moe_rmsnorm", "moe_dequant",
-           "moe_device_status", "moe_last_launch_count", "moe_status_str", "moe_profile_events", "moe_last_cuda_error")
+           "moe_device_status", "moe_last_launch_count", "moe_status_str", "moe_profile_events", "moe_last_cuda_error",
+           "moe_decode_static")
+
+MOE_DECODE_STATIC_SCRATCH_BYTES = 65536
 
 MOE_KERNEL_ROUTER = 1
 MOE_KERNEL_TOPK = 2
@@ -114,6 +117,9 @@ def lib():
         L.moe_last_cuda_error.argtypes = []
         L.moe_status_str.restype = ctypes.c_char_p
         L.moe_status_str.argtypes = [i32]
+        L.moe_decode_static.restype = i32
+        L.moe_decode_static.argtypes = [ctypes.POINTER(moe_config), vp, vp, ctypes.POINTER(moe_weights), vp, vp, vp,
+                                        u32, vp]
         _lib = L
     return _lib
 
@@ -202,6 +208,16 @@ def moe_forward(plan: Plan, x, residual, T: int, weights, logit_bias, out, ws, s
     cw = weights if isinstance(weights, moe_weights) else make_weights(weights)
     _check("moe_forward", lib().moe_forward(plan.handle, _ptr(x), _ptr(residual), int(T), ctypes.byref(cw),
                                             _ptr(logit_bias), _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_decode_static(cfg: moe_config, x, residual, weights, logit_bias, out, status=None, flags: int = 0,
+                      stream=None):
+    """One token through the layer with no device allocation (library-owned
+    static scratch; see the header).  ``status``: optional device int32."""
+    cw = weights if isinstance(weights, moe_weights) else make_weights(weights)
+    _check("moe_decode_static", lib().moe_decode_static(ctypes.byref(cfg), _ptr(x), _ptr(residual), ctypes.byref(cw),
+                                                        _ptr(logit_bias), _ptr(out), _ptr(status), int(flags),
+                                                        _stream(stream)))
 
 
 def moe_route_view(plan: Plan, ws, T: int) -> moe_route_ptrs:

@@ -3,7 +3,13 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "moe.h"
+
 namespace moe {
+
+// Records e as the calling thread's last CUDA error (moe_last_cuda_error)
+// and returns MOE_ERR_CUDA, or MOE_OK for cudaSuccess.
+moe_status note_cuda_error(cudaError_t e);
 
 // Profiling hook (moe_profile_events): record events around a kernel launch.
 void prof_before(int kernel, cudaStream_t s);

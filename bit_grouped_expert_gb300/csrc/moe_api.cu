@@ -146,6 +146,8 @@ moe::ExpertPtrs expert_ptrs(const moe_weights *w) {
 }  // namespace
 
 namespace moe {
+moe_status note_cuda_error(cudaError_t e) { return cuda_status(e); }
+
 // Inside a stream capture the records become external event-record nodes,
 // which time like ordinary records when the graph runs.
 static void prof_record(cudaEvent_t ev, cudaStream_t s) {

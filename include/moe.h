@@ -205,6 +205,47 @@ typedef enum {
  * null arrays with n > 0, or a null event handle. */
 moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *const *stop_events, int32_t n);
 
+/* Allocation-free single-token layer.  The paper has no counterpart to this
+ * entry point: it serves callers that cannot call cudaMalloc -- code running
+ * inside another runtime that owns all of the device's memory (a serving
+ * engine or framework whose allocator has reserved it, or a process held to
+ * a fixed memory cap), and code that must not risk the implicit device-wide
+ * synchronisation an allocation can bring.  It computes what moe_forward
+ * computes for T == 1 on its decode path (one cooperative launch), with the
+ * scratch that path keeps in the workspace -- router keys, top-k ids and
+ * weights, the k + n_shared h vectors, the grid-barrier counter and the
+ * status word -- held instead in one static device array of
+ * MOE_DECODE_STATIC_SCRATCH_BYTES that every device loading the library keeps
+ * until the process exits.  It needs no plan and calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *   cfg          the layer's dimensions (checked as moe_plan checks them)
+ *   x_d          bf16 [H] input token, or with MOE_FLAG_PRENORM the residual
+ *                stream r (the call normalises it itself)
+ *   residual_d   bf16 [H] or NULL (NULL: the residual is x); NULL with PRENORM
+ *   w            packed weights, as for moe_forward; logit_bias_d fp32 [E] or NULL
+ *   out_d        bf16 [H]; may alias residual_d; may alias x_d only with PRENORM
+ *   status_d     device int32 or NULL: zeroed, then set to a moe_status code if
+ *                the kernel meets a device-side error (NULL: not reported)
+ *   flags        0 or MOE_FLAG_PRENORM
+ * The first call on a device (with that device current) resolves the array's
+ * address with cudaGetSymbolAddress and raises the decode kernel's
+ * shared-memory limit; make that first call before any stream capture.
+ * Every call clears the status word and the barrier counter on the stream
+ * before its launch; keys, top-k and h are rewritten before they are read, so
+ * the array otherwise keeps the previous call's contents.  All calls on a
+ * device share the one array: calls that can overlap on the GPU (other
+ * streams, other threads) race and must be serialised by the caller.
+ * Errors: MOE_ERR_WORKSPACE_TOO_SMALL when the layer's scratch (about
+ * 4E + 8k + 2(k + n_shared)I bytes plus 256-byte alignment: 11,008 bytes for
+ * H=2048, E=256, k=8, n_shared=1, I=512) exceeds the array; MOE_ERR_UNSUPPORTED for dimensions the decode path does not take
+ * (H and I powers of two, the kernel's shared memory within the device's
+ * limit); MOE_ERR_INVALID_ARGUMENT / MOE_ERR_MISALIGNED as for moe_forward;
+ * MOE_ERR_CUDA when a CUDA call fails (moe_last_cuda_error). */
+#define MOE_DECODE_STATIC_SCRATCH_BYTES 65536
+moe_status moe_decode_static(const moe_config *cfg, const void *x_d, const void *residual_d,
+                             const moe_weights *w, const float *logit_bias_d, void *out_d, int32_t *status_d,
+                             uint32_t flags, void *stream);
+
 const char *moe_status_str(moe_status s);
 
 /* Text of the CUDA error behind the last MOE_ERR_CUDA returned on the
