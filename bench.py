@@ -223,26 +223,36 @@ def run_ours(args, wl, rank, world, device):
     stream = torch.cuda.Stream(device=device)
     launches = [0]
 
+    # dominant kernel: gate/up (decode: the one-launch decode layer).  Only a
+    # few of its launches per step are bracketed by events, so the event nodes
+    # in the captured step barely perturb the step time.
+    dom = moe.MOE_KERNEL_DECODE_LAYER if T == 1 else moe.MOE_KERNEL_GATEUP
+    prof_layers = sorted({(2 * j + 1) * L // 8 for j in range(4)}) if L >= 4 else [0]
+    n_dom = len(prof_layers)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
+    profiling = [False]
+
+    def forward(l, c0, x_arg, out_arg):
+        on = profiling[0] and c0 == 0 and l in prof_layers
+        if on:
+            j = prof_layers.index(l)
+            moe.moe_profile_events(dom, ev_a[j:j + 1], ev_b[j:j + 1])
+        moe.moe_forward(plan, x_arg, None, chunk, cws[l], bias, out_arg, ws, stream=stream)
+        launches[0] += moe.moe_last_launch_count()
+        if on:
+            moe.moe_profile_events(dom)
+
     def body():
         launches[0] = 0
-        s = stream
         for c0 in range(0, T, chunk):
             if L == 1:
-                moe.moe_forward(plan, x_in[c0:c0 + chunk], None, chunk, cws[0], bias, out[c0:c0 + chunk], ws,
-                                stream=s)
-                launches[0] += moe.moe_last_launch_count()
+                forward(0, c0, x_in[c0:c0 + chunk], out[c0:c0 + chunk])
                 continue
             r.copy_(x_in[c0:c0 + chunk])
             for l in range(L):
-                moe.moe_forward(plan, r, None, chunk, cws[l], bias, r, ws, stream=s)
-                launches[0] += moe.moe_last_launch_count()
+                forward(l, c0, r, r)
             out[c0:c0 + chunk].copy_(r)
-
-    # dominant kernel: gate/up (decode: the one-launch decode layer)
-    dom = moe.MOE_KERNEL_DECODE_LAYER if T == 1 else moe.MOE_KERNEL_GATEUP
-    n_dom = (T // chunk) * L
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
 
     # warm the path once eagerly, then capture one step into a CUDA graph
     with torch.cuda.stream(stream):
@@ -250,11 +260,14 @@ def run_ours(args, wl, rank, world, device):
             x_in.copy_(tokens[0])
         body()
     torch.cuda.synchronize()
+    for e in ev_a + ev_b:  # create the CUDA events now, outside the capture
+        e.record(stream)
+    torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
-    moe.moe_profile_events(dom, ev_a, ev_b)
+    profiling[0] = True
     with torch.cuda.graph(graph, stream=stream):
         body()
-    moe.moe_profile_events(dom)
+    profiling[0] = False
     per_step_launches = launches[0]
 
     def step(i):

@@ -14,16 +14,31 @@
 //   --- grid barrier ---
 //   P3  the down rows of every slot for this CTA's output features, y_j =
 //       bf16(h_j . Wd_j), out = bf16(res + y_shared + sum_j w_j * y_j)
-// Weight rows reach shared memory by 16-byte cp.async issued by all threads
-// as soon as their addresses are known: P1 and the shared expert's down rows
-// at launch, the routed experts' gate/up and down rows right after the top-k,
-// so the down rows arrive while P2 computes.  The GEMVs run on mma.sync
-// m16n8k16: A = the activation vector broadcast to 16 rows, B = 8 weight rows
-// dequantised in registers (w = bf16_rne(scale*q + bias)), fp32 accumulate.
-// The grid barrier is a monotonic 64-bit arrival counter in the workspace;
-// every wait is bounded (MOE_ERR_DEVICE_TIMEOUT).
+//
+// Weights reach shared memory through the tensor-memory accelerator as soon
+// as their addresses are known -- P1 and the shared expert's down rows at
+// launch, the routed experts' rows right after the top-k -- and each routed
+// gate/up unit has its own mbarrier, so its GEMV starts when its bytes land
+// while later units are still in flight.  Packed codes arrive in the 128-byte
+// swizzled layout: for 8 rows and one K-chunk of 256 codes, [row][128 B] with
+// the 16-byte pieces of row r permuted by XOR r, which makes the GEMV's
+// 16-byte reads of eight rows conflict-free.
+//
+// The GEMVs run on mma.sync m16n8k16 with the activation vector broadcast
+// over the 16 A rows and 8 weight rows as B, dequantised in registers
+// (w = bf16_rne(scale * q + bias), fp32 accumulate).  The k index of the MMA
+// may map onto any 16 positions of K as long as A and B agree, so lane
+// (g, q) owns one whole quantisation group of row g -- 64 codes, one scale,
+// one bias -- and keeps that group's 64 x values in registers across all the
+// rows it visits.
+//
+// The grid barrier is a monotonic 64-bit arrival counter; every wait is
+// bounded (MOE_ERR_DEVICE_TIMEOUT).
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.h"
 #include "tc_ptx.cuh"
 #include "topk.cuh"
 
@@ -32,7 +47,14 @@ namespace {
 
 constexpr int DTHREADS = 512;
 constexpr int DWARPS = DTHREADS / 32;
+constexpr int KCH = 256;   // codes per K-chunk: 4 groups, 128 bytes of a code row
+constexpr int XPAD = 72;   // bf16 slots per 64-value group of x / h in shared memory
+constexpr int MAX_RU = 8;  // routed gate/up units (mbarriers) per CTA
 constexpr unsigned long long DTIMEOUT_NS = 1000000000ull;
+
+struct DecMaps {
+  CUtensorMap gate, up, down;  // packed codes, [rows][K/2] bytes, 128B-swizzled 8-row boxes
+};
 
 struct DecArgs {
   const uint16_t *xin;  // x, or the residual stream r for pre-norm plans
@@ -43,17 +65,18 @@ struct DecArgs {
   float *keys;
   int32_t *topk_id;
   float *topk_w;
-  uint16_t *hbuf;  // [k+S][I]
+  uint16_t *hbuf;           // [k+S][I]
   unsigned long long *bar;  // monotonic arrival counter of the grid barrier
   int32_t *status;
   uint64_t *trace;  // [3][16] phase timestamps or null
   int H, E, k, I, S, prenorm;
   float eps;
+  int map3d;  // 1: one TMA op per matrix (3-D map over the K-chunks), 0: one per K-chunk
   // schedule
   int n_su, rp_cta0, rp_ctas, n_ru, n_ou;
-  // shared-memory layout (bytes)
-  int off_x, off_h, off_red, off_keys, off_p1, off_p2, off_p3;
-  int ug, ud;  // bytes of one gate/up unit (8 rows, 2 matrices) and one down slot block (8 rows)
+  // shared-memory layout (bytes from the 1024-aligned base)
+  int off_dc, off_ru, off_su, off_rr, off_x, off_h, off_ds, off_rus, off_sus, off_red, off_keys, off_cand,
+      off_gmax, off_bar, off_ys;
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p) {
@@ -62,23 +85,22 @@ __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long l
   return v;
 }
 
-__device__ __forceinline__ unsigned long long atom_add_release64(unsigned long long *p, unsigned long long v) {
-  unsigned long long old;
-  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-  return old;
+// Grid barrier on a monotonic arrival counter.  Every launch adds exactly
+// two arrivals per CTA, so at launch the counter is a multiple of the grid
+// size G; a CTA rounds the value it first reads down to that multiple (no CTA
+// can have completed the first round before it arrives) and barrier b of the
+// launch ends when the counter reaches base + b * G.  Arrival is a release
+// reduction that needs no reply; the wait is bounded.
+__device__ __forceinline__ void red_add_release64(unsigned long long *p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Grid barrier on a monotonic arrival counter: a CTA's arrival number `old`
-// belongs to the round ending at the next multiple of the grid size, so no
-// reset is needed between barriers or launches (bounded wait).
-__device__ bool grid_sync(unsigned long long *bar, int32_t *status) {
+__device__ bool grid_sync(unsigned long long *bar, unsigned long long target, int32_t *status) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const unsigned long long G = gridDim.x;
-    const unsigned long long old = atom_add_release64(bar, 1ull);
-    const unsigned long long target = (old / G + 1ull) * G;
+    red_add_release64(bar, 1ull);
     if (ld_acquire64(bar) < target) {
       const uint64_t t0 = ptx::globaltimer();
       while (ld_acquire64(bar) < target) {
@@ -95,180 +117,233 @@ __device__ bool grid_sync(unsigned long long *bar, int32_t *status) {
   return s_ok != 0;
 }
 
+// Bounded wait for phase 0 of a one-shot mbarrier.
+__device__ bool wait_bar(uint64_t *bar, int32_t *status) {
+  if (ptx::mbar_try_wait(bar, 0)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait_sleep(bar, 0, 20000)) {
+    if (ptx::globaltimer() - t0 > DTIMEOUT_NS) {
+      set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(ptx::smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%4,%5,%5}, {%6,%7}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%4,%5,%5}, {%6,%7}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(b0), "r"(b1));
 }
 
-// Codes 2q and 2q+1 of a word (its byte q) as w = bf16_rne(s*q + b), packed.
-__device__ __forceinline__ uint32_t dq_pair(uint32_t word, int q, __nv_bfloat162 s2, __nv_bfloat162 b2) {
-  uint32_t t = __byte_perm(word, word >> 4, (uint32_t)(q | ((4 + q) << 8)));
+// Codes 2b and 2b+1 of a word (its byte b) as bf16_rne(s*q + bias), packed;
+// w4 = w >> 4.  0x4300 | q is the bf16 value 128 + q, so one subtraction and
+// one fused multiply-add (a single rounding) rebuild the weight.
+__device__ __forceinline__ uint32_t dq(uint32_t w, uint32_t w4, int b, __nv_bfloat162 s2, __nv_bfloat162 b2) {
+  uint32_t t = __byte_perm(w, w4, (uint32_t)(b | ((4 + b) << 8)));
   t = (t & 0x000F000Fu) | 0x43004300u;
   const __nv_bfloat162 m = *reinterpret_cast<__nv_bfloat162 *>(&t);
   const __nv_bfloat162 r = __hfma2(s2, __hsub2(m, __floats2bfloat162_rn(128.f, 128.f)), b2);
   return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-// One 32-K step of an 8-row GEMV: lane (g = lane/4, q = lane%4) dequantises
-// row g's codes 2q,2q+1 and 2q+8,2q+9 of both 16-K halves.
-__device__ __forceinline__ void gemv_step(float (&d)[4], const uint8_t *crow, const uint16_t *srow,
-                                          const uint16_t *brow, const uint16_t *xs, int kk, int q) {
-  const uint4 w = *reinterpret_cast<const uint4 *>(crow + kk / 2);
-  const __nv_bfloat162 s2 = bf16x2_splat(srow[kk >> 6]), b2 = bf16x2_splat(brow[kk >> 6]);
-  const uint32_t xa0 = *reinterpret_cast<const uint32_t *>(xs + kk + 2 * q);
-  const uint32_t xb0 = *reinterpret_cast<const uint32_t *>(xs + kk + 8 + 2 * q);
-  const uint32_t xa1 = *reinterpret_cast<const uint32_t *>(xs + kk + 16 + 2 * q);
-  const uint32_t xb1 = *reinterpret_cast<const uint32_t *>(xs + kk + 24 + 2 * q);
-  mma16816(d, xa0, xb0, dq_pair(w.x, q, s2, b2), dq_pair(w.y, q, s2, b2));
-  mma16816(d, xa1, xb1, dq_pair(w.z, q, s2, b2), dq_pair(w.w, q, s2, b2));
+// The 64 values of quantisation group `grp` (bf16 pairs) of a padded shared
+// vector (XPAD slots per group).
+__device__ __forceinline__ void load_group(const uint16_t *v, int grp, uint32_t (&xr)[32]) {
+  const uint4 *p = reinterpret_cast<const uint4 *>(v + grp * XPAD);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 t = p[i];
+    xr[4 * i] = t.x;
+    xr[4 * i + 1] = t.y;
+    xr[4 * i + 2] = t.z;
+    xr[4 * i + 3] = t.w;
+  }
 }
 
-// d += x[k0:k1] . W[8 rows][k0:k1] (k0, k1 multiples of 64).  Two
-// accumulators alternate over the 32-K steps so consecutive MMAs are
-// independent; after the call lane q holds rows 2q (d[0]) and 2q+1 (d[1]).
-__device__ __forceinline__ void gemv8(const uint8_t *codes, int rs, const uint16_t *sc, const uint16_t *bi, int gs,
-                                      const uint16_t *xs, int k0, int k1, int lane, float (&d)[4]) {
-  const int g = lane >> 2, q = lane & 3;
-  const uint8_t *crow = codes + g * rs;
-  const uint16_t *srow = sc + g * gs, *brow = bi + g * gs;
-  float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-  for (int kk = k0; kk < k1; kk += 64) {
-    gemv_step(d, crow, srow, brow, xs, kk, q);
-    gemv_step(e, crow, srow, brow, xs, kk + 32, q);
+// d += x . W over one K-chunk of 8 rows.  chunk: the swizzled [8][128 B] code
+// image of the chunk; s, b: the rows' scales and biases ([8][gpr] bf16);
+// lane (g, q) handles group grp = 4 * chunk + q of row g.  After the call
+// lane q holds rows 2q (d[0]) and 2q+1 (d[1]).
+__device__ __forceinline__ void gemv_chunk(const uint8_t *chunk, const uint16_t *s, const uint16_t *b, int gpr,
+                                           int grp, const uint32_t (&xr)[32], int g, int q, float (&d)[4]) {
+  const uint8_t *row = chunk + g * 128;
+  const uint4 c0 = *reinterpret_cast<const uint4 *>(row + (((2 * q) ^ g) << 4));
+  const uint4 c1 = *reinterpret_cast<const uint4 *>(row + (((2 * q + 1) ^ g) << 4));
+  const __nv_bfloat162 s2 = bf16x2_splat(s[g * gpr + grp]), b2 = bf16x2_splat(b[g * gpr + grp]);
+  const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  // four accumulators: chains of four dependent MMAs instead of sixteen
+  float e[4][4] = {};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {  // word i holds codes 8i..8i+7: MMAs 2i and 2i+1
+    const uint32_t w = wv[i], w4 = w >> 4;
+    mma16816(e[(2 * i) & 3], xr[4 * i], xr[4 * i + 1], dq(w, w4, 0, s2, b2), dq(w, w4, 1, s2, b2));
+    mma16816(e[(2 * i + 1) & 3], xr[4 * i + 2], xr[4 * i + 3], dq(w, w4, 2, s2, b2), dq(w, w4, 3, s2, b2));
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] += e[i];
+  for (int r = 0; r < 4; ++r) d[r] += (e[0][r] + e[1][r]) + (e[2][r] + e[3][r]);
 }
 
-// Gate and up rows of one unit over the same K range, interleaved so the four
-// accumulator chains overlap.
-__device__ __forceinline__ void gemv8x2(const uint8_t *cg, const uint8_t *cu, int rs, const uint16_t *sg,
-                                        const uint16_t *bg, const uint16_t *su, const uint16_t *bu, int gs,
-                                        const uint16_t *xs, int k0, int k1, int lane, float (&dg)[4],
-                                        float (&du)[4]) {
-  const int g = lane >> 2, q = lane & 3;
-  float eg[4] = {0.f, 0.f, 0.f, 0.f}, eu[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-  for (int kk = k0; kk < k1; kk += 64) {
-    gemv_step(dg, cg + g * rs, sg + g * gs, bg + g * gs, xs, kk, q);
-    gemv_step(du, cu + g * rs, su + g * gs, bu + g * gs, xs, kk, q);
-    gemv_step(eg, cg + g * rs, sg + g * gs, bg + g * gs, xs, kk + 32, q);
-    gemv_step(eu, cu + g * rs, su + g * gs, bu + g * gs, xs, kk + 32, q);
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    dg[i] += eg[i];
-    du[i] += eu[i];
-  }
-}
+__device__ __forceinline__ int gu_ops(const DecArgs &a) { return 2 * (a.map3d ? 1 : a.H / KCH) + 4; }
+__device__ __forceinline__ int dn_ops(const DecArgs &a) { return (a.map3d ? 1 : a.I / KCH) + 2; }
 
-// Shared-memory image of one gate/up unit: for each matrix, 8 code rows
-// (stride H/2 + 16 to spread banks), then 8 scale rows and 8 bias rows.
-__device__ __forceinline__ int gu_rs(int H) { return H / 2 + 16; }
-__device__ __forceinline__ int gu_mat_bytes(int H) { return 8 * gu_rs(H) + 2 * (H / 4); }
-__device__ __forceinline__ int dn_rs(int I) { return I / 2 + 16; }
-
-__device__ __forceinline__ int ilog2(int v) { return 31 - __clz(v); }
-
-// Stage one gate/up unit (expert e, rows r0..r0+7, both matrices) with
-// 16-byte cp.async copies spread over all threads of the CTA (H is a power
-// of two, so chunk indices split with shifts).
-__device__ void stage_gu(const DecArgs &a, uint8_t *dst, int e, int r0) {
-  const int H = a.H, rs = gu_rs(H), mb = gu_mat_bytes(H);
-  const int lc = ilog2(H / 32);  // log2 of the 16-byte chunks per code row
-  const size_t row = (size_t)e * a.I + r0;
-  const uint8_t *q0 = reinterpret_cast<const uint8_t *>(a.w.gate_q) + row * (H / 2);
-  const uint8_t *q1 = reinterpret_cast<const uint8_t *>(a.w.up_q) + row * (H / 2);
-  for (int c = threadIdx.x; c < (16 << lc); c += DTHREADS) {
-    const int mat = c >> (lc + 3), r = (c >> lc) & 7, j = c & ((1 << lc) - 1);
-    ptx::cp_async_16(dst + mat * mb + r * rs + j * 16, (mat ? q1 : q0) + r * (H / 2) + j * 16, 16);
-  }
-  const int ls = ilog2(H / 64);  // chunks per 8-row scale (or bias) block: 8 * H/64 * 2 / 16
-  for (int c = threadIdx.x; c < (4 << ls); c += DTHREADS) {
-    const int which = c >> ls, j = c & ((1 << ls) - 1);  // 0 gate s, 1 gate b, 2 up s, 3 up b
+// Gate/up image of one unit: codes [2 matrices][H/256 chunks][8 rows][128 B]
+// (8H bytes) and scales [gate_s, gate_b, up_s, up_b][8 rows][H/64] (H bytes).
+// Issues copy o of the unit (code boxes of both matrices, then 4 scale rows).
+__device__ void gu_op(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cdst, uint8_t *sdst, int e, int r0,
+                      uint64_t *bar) {
+  const int H = a.H, nco = a.map3d ? 1 : H / KCH;
+  const int row = e * a.I + r0;
+  if (o < 2 * nco) {
+    const int mat = o / nco, c = o % nco;
+    uint8_t *dst = cdst + mat * 4 * H + c * 1024;
+    const CUtensorMap *map = mat ? &mp.up : &mp.gate;
+    if (a.map3d)
+      ptx::tma_load_3d(dst, map, bar, 0, row, 0);
+    else
+      ptx::tma_load_2d(dst, map, bar, c * 128, row);
+  } else {
+    const int which = o - 2 * nco;  // 0 gate_s, 1 gate_b, 2 up_s, 3 up_b
     const uint16_t *src = which == 0 ? a.w.gate_s : which == 1 ? a.w.gate_b : which == 2 ? a.w.up_s : a.w.up_b;
-    ptx::cp_async_16(dst + (which >> 1) * mb + 8 * rs + (which & 1) * (H / 4) + j * 16,
-                     reinterpret_cast<const uint8_t *>(src + row * (H / 64)) + j * 16, 16);
+    ptx::bulk_g2s(sdst + which * (H / 4), src + (size_t)row * (H / 64), H / 4, bar);
   }
 }
 
-// Stage one down block: expert e, output rows n0..n0+7.
-__device__ void stage_dn(const DecArgs &a, uint8_t *dst, int e, int n0) {
-  const int I = a.I, rs = dn_rs(I);
-  const int lc = ilog2(I / 32), ls = ilog2(I / 64);
-  const size_t row = (size_t)e * a.H + n0;
-  const uint8_t *q = reinterpret_cast<const uint8_t *>(a.w.down_q) + row * (I / 2);
-  for (int c = threadIdx.x; c < (8 << lc); c += DTHREADS) {
-    const int r = c >> lc, j = c & ((1 << lc) - 1);
-    ptx::cp_async_16(dst + r * rs + j * 16, q + r * (I / 2) + j * 16, 16);
-  }
-  for (int c = threadIdx.x; c < (2 << ls); c += DTHREADS) {
-    const int which = c >> ls, j = c & ((1 << ls) - 1);
-    const uint16_t *src = which ? a.w.down_b : a.w.down_s;
-    ptx::cp_async_16(dst + 8 * rs + which * (I / 4) + j * 16,
-                     reinterpret_cast<const uint8_t *>(src + row * (I / 64)) + j * 16, 16);
-  }
-}
-
-// Stage router rows e0, e0+stride, ... (n rows, fp32, H values each).
-__device__ void stage_router(const DecArgs &a, float *dst, int e0, int stride, int n) {
-  const int lc = ilog2(a.H / 4);
-  for (int c = threadIdx.x; c < (n << lc); c += DTHREADS) {
-    const int r = c >> lc, j = c & ((1 << lc) - 1);
-    ptx::cp_async_16(dst + r * a.H + j * 4, a.router + (size_t)(e0 + r * stride) * a.H + j * 4, 16);
+// Down image of one (output unit, slot): codes [I/256 chunks][8 rows][128 B]
+// (4I bytes) and scales [down_s, down_b][8 rows][I/64] (I/2 bytes).
+__device__ void dn_op(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cdst, uint8_t *sdst, int e, int n0,
+                      uint64_t *bar) {
+  const int I = a.I, nco = a.map3d ? 1 : I / KCH;
+  const int row = e * a.H + n0;
+  if (o < nco) {
+    if (a.map3d)
+      ptx::tma_load_3d(cdst, &mp.down, bar, 0, row, 0);
+    else
+      ptx::tma_load_2d(cdst + o * 1024, &mp.down, bar, o * 128, row);
+  } else {
+    const int which = o - nco;  // 0 down_s, 1 down_b
+    ptx::bulk_g2s(sdst + which * (I / 4), (which ? a.w.down_b : a.w.down_s) + (size_t)row * (I / 64), I / 4, bar);
   }
 }
 
-// Top-k of one token by all threads of the CTA: each key's rank is the number
-// of keys whose order code is larger (codes are distinct), so the picked
-// experts land in slot order directly; warp 0 then computes the weights.
-__device__ void topk_block(const float *keys, int E, int k, unsigned long long *codes, int32_t *ids, float *w,
-                           int32_t *status) {
-  const int tid = threadIdx.x;
-  for (int e = tid; e < E; e += DTHREADS) codes[e] = topk_code(keys[e], e);
+// Partial gate/up dot products of `nu` unit images against x (padded, in
+// shared memory) into red[(u * nkc + kc) * 16 + r] (r < 8 gate rows, 8 + r up
+// rows).  Warps split the K-chunks first, then the row sets (unit, matrix);
+// with `bars`, unit u is read once bars[u] completes.  Returns false on a
+// timeout.
+__device__ bool gu_compute(const DecArgs &a, const uint8_t *codes, const uint8_t *scales, int nu, uint64_t *bars,
+                           const uint16_t *xs, float *red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int H = a.H, nkc = H / KCH, WK = nkc < DWARPS ? nkc : DWARPS, WR = DWARPS / WK;
+  const int kg = warp % WK, rg = warp / WK, gpr = H / 64;
+  if (rg >= 2 * nu) return true;
+  for (int kc = kg; kc < nkc; kc += WK) {
+    uint32_t xr[32];
+    load_group(xs, 4 * kc + q, xr);
+    for (int rs = rg; rs < 2 * nu; rs += WR) {
+      const int u = rs >> 1, mat = rs & 1;  // gate (0) or up (1) rows of unit u
+      if (bars && !wait_bar(&bars[u], a.status)) return false;
+      const uint16_t *su = reinterpret_cast<const uint16_t *>(scales + (size_t)u * H) + mat * 16 * gpr;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      gemv_chunk(codes + (size_t)u * 8 * H + mat * 4 * H + kc * 1024, su, su + 8 * gpr, gpr, 4 * kc + q, xr, g, q,
+                 d);
+      if (g == 0) {
+        float *r = red + (u * nkc + kc) * 16 + mat * 8;
+        r[2 * q] = d[0];
+        r[2 * q + 1] = d[1];
+      }
+    }
+  }
+  return true;
+}
+
+// h = bf16(silu(gate) * up) of `nu` units from the partials; unit u's 8 rows
+// go to hbuf from element row_of(u).
+template <typename RowOf>
+__device__ void gu_finish(const DecArgs &a, int nu, const float *red, RowOf row_of) {
+  const int nkc = a.H / KCH;
+  for (int t = threadIdx.x; t < nu * 8; t += DTHREADS) {
+    const int u = t >> 3, r = t & 7;
+    float gs = 0.f, us = 0.f;
+    for (int kc = 0; kc < nkc; ++kc) {
+      gs += red[(u * nkc + kc) * 16 + r];
+      us += red[(u * nkc + kc) * 16 + 8 + r];
+    }
+    a.hbuf[row_of(u) + r] = f32_to_bf16(silu(gs) * us);
+  }
+}
+
+// Top-k of one token by all threads of the CTA.  Codes (topk_code) order the
+// keys exactly as the selection does and are distinct.  The k-th largest of
+// the maxima of 16-key groups is a lower bound for the k-th largest key (k
+// distinct keys reach it), so only keys at or above it can be selected; their
+// rank among themselves is their slot.
+__device__ void topk_block(const float *keys, int E, int k, unsigned long long *cand, unsigned long long *gmax,
+                           int32_t *ids, float *w, int32_t *status) {
+  __shared__ int s_n;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int NG = (E + 15) / 16;
+  for (int base = 0; base < E; base += DTHREADS) {
+    const int e = base + tid;
+    unsigned long long c = e < E ? topk_code(keys[e], e) : 0ull;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {  // maximum over the 16 lanes of the half-warp
+      const unsigned long long other = shfl_xor_u64(c, o);
+      c = other > c ? other : c;
+    }
+    if ((tid & 15) == 0 && e < E) gmax[e >> 4] = c;
+  }
+  if (tid == 0) s_n = 0;
   __syncthreads();
-  for (int e = tid; e < E; e += DTHREADS) {
-    const unsigned long long c = codes[e];
+  // every warp finds the threshold itself (NG <= 64): no block barrier
+  unsigned long long tau = 0ull;
+  if (NG >= k) {
+    const unsigned long long m0 = lane < NG ? gmax[lane] : 0ull, m1 = lane + 32 < NG ? gmax[lane + 32] : 0ull;
+    int r0 = 0, r1 = 0;
+#pragma unroll 4
+    for (int j = 0; j < NG; ++j) {
+      const unsigned long long gj = gmax[j];
+      r0 += gj > m0;
+      r1 += gj > m1;
+    }
+    unsigned long long t = (lane < NG && r0 == k - 1) ? m0 : ((lane + 32 < NG && r1 == k - 1) ? m1 : 0ull);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = shfl_xor_u64(t, o);
+      t = other > t ? other : t;
+    }
+    tau = t;
+  }
+  for (int base = 0; base < E; base += DTHREADS) {
+    const int e = base + tid;
+    const unsigned long long c = e < E ? topk_code(keys[e], e) : 0ull;
+    const bool take = e < E && c >= tau;
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    int pos = 0;
+    if (lane == 0 && m) pos = atomicAdd(&s_n, __popc(m));
+    pos = __shfl_sync(0xffffffffu, pos, 0);
+    if (take) cand[pos + __popc(m & ((1u << lane) - 1u))] = c;
+  }
+  __syncthreads();
+  const int n = s_n;
+  for (int t = tid; t < n; t += DTHREADS) {
+    const unsigned long long c = cand[t];
     int rank = 0;
-#pragma unroll 8
-    for (int j = 0; j < E; ++j) rank += codes[j] > c;
-    if (rank < k) ids[rank] = e;
+    for (int j = 0; j < n; ++j) rank += cand[j] > c;
+    if (rank < k) ids[rank] = topk_code_expert(c);
   }
   __syncthreads();
   if (tid < 32) {
-    const int lane = tid;
     const int my_id = lane < k ? ids[lane] : -1;
     const float my_key = lane < k ? keys[my_id] : 0.f;
     topk_finish(lane, k, my_id, my_key, ids, w, nullptr, status);
   }
-}
-
-// One gate/up unit slice: a warp reduces K range [c*len, (c+1)*len) of the
-// unit at `base` and leaves 8 gate and 8 up partial sums in red[0..15].
-__device__ __forceinline__ void gu_slice(const uint8_t *base, int H, int mb, const uint16_t *xs, int c, int len,
-                                         int lane, float *red) {
-  float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
-  const uint16_t *sg = reinterpret_cast<const uint16_t *>(base + 8 * gu_rs(H));
-  const uint16_t *su = reinterpret_cast<const uint16_t *>(base + mb + 8 * gu_rs(H));
-  gemv8x2(base, base + mb, gu_rs(H), sg, sg + 8 * (H / 64), su, su + 8 * (H / 64), H / 64, xs, c * len,
-          (c + 1) * len, lane, dg, du);
-  if (lane < 4) {
-    red[2 * lane] = dg[0];
-    red[2 * lane + 1] = dg[1];
-    red[8 + 2 * lane] = du[0];
-    red[8 + 2 * lane + 1] = du[1];
-  }
-}
-
-__device__ __forceinline__ int k_chunks(int units, int H) {
-  int kc = units > 0 ? DWARPS / units : 1;
-  if (kc < 1) kc = 1;
-  while (kc > 1 && (H / 64) % kc) kc >>= 1;
-  return kc;
 }
 
 // Phase timestamp for the trace of CTAs 0, G/2 and G-1 (thread 0).
@@ -279,36 +354,83 @@ __device__ __forceinline__ void trace_at(const DecArgs &a, int slot) {
   if (row >= 0) a.trace[row * 16 + slot] = ptx::globaltimer();
 }
 
-__global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const DecArgs a) {
-  extern __shared__ __align__(1024) uint8_t sm[];
-  __shared__ int s_ids[17];
-  __shared__ float s_w[17];
+__global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_constant__ DecMaps mp,
+                                                                   const DecArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_ids[16];
+  __shared__ float s_w[16];
   __shared__ float s_part[DWARPS];
+  // 1024-byte aligned base for the swizzled code images (keeps the shared space)
+  uint8_t *sm = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x, G = gridDim.x;
   const int H = a.H, I = a.I, E = a.E, k = a.k, S = a.S, NS = k + S;
+  uint8_t *dc = sm + a.off_dc, *ru = sm + a.off_ru, *su = sm + a.off_su, *ds = sm + a.off_ds,
+          *rus = sm + a.off_rus, *sus = sm + a.off_sus;
+  float *rr = reinterpret_cast<float *>(sm + a.off_rr);
   uint16_t *xs = reinterpret_cast<uint16_t *>(sm + a.off_x);
   uint16_t *hs = reinterpret_cast<uint16_t *>(sm + a.off_h);
   float *red = reinterpret_cast<float *>(sm + a.off_red);
   float *keys = reinterpret_cast<float *>(sm + a.off_keys);
-  uint8_t *p1 = sm + a.off_p1, *p2 = sm + a.off_p2, *p3 = sm + a.off_p3;
-  const int mb = gu_mat_bytes(H);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + a.off_bar);
+  uint64_t *bar_p1 = bars, *bar_dsh = bars + 1, *bar_drt = bars + 2, *bar_ru = bars + 3;
   const int nsu = (cta < a.n_su) ? (a.n_su - 1 - cta) / G + 1 : 0;  // shared gate/up units of this CTA
   const int rc = cta - a.rp_cta0;                                    // index among the router CTAs
   const int nre = (rc >= 0 && rc < a.rp_ctas && rc < E) ? (E - 1 - rc) / a.rp_ctas + 1 : 0;  // router rows
-  const int nou = (cta < a.n_ou) ? (a.n_ou - 1 - cta) / G + 1 : 0;  // output units of this CTA
-  float *rrows = reinterpret_cast<float *>(p1 + nsu * a.ug);
+  const int nru = (cta < a.n_ru) ? (a.n_ru - 1 - cta) / G + 1 : 0;  // routed gate/up units
+  const int nou = (cta < a.n_ou) ? (a.n_ou - 1 - cta) / G + 1 : 0;  // output units
+  const int upr = I / 8;
   trace_at(a, 0);
 
-  // ---------------------------------------------------------------- copies known at launch (group 0)
-  for (int i = 0; i < nsu; ++i) stage_gu(a, p1 + i * a.ug, E, (cta + i * G) * 8);
-  if (nre) stage_router(a, rrows, rc, a.rp_ctas, nre);
-  if (S)
-    for (int i = 0; i < nou; ++i) stage_dn(a, p3 + (i * NS + k) * a.ud, E, (cta + i * G) * 8);
-  ptx::cp_async_commit();
+  if (tid == 0) {
+    for (int i = 0; i < 3 + MAX_RU; ++i) ptx::mbar_init(&bars[i], 1);
+    ptx::fence_mbar_init();
+    if (a.map3d) {
+      ptx::prefetch_tmap(&mp.gate);
+      ptx::prefetch_tmap(&mp.up);
+      ptx::prefetch_tmap(&mp.down);
+    }
+    expect_tx(bar_p1, (uint32_t)(nsu * 9 * H + nre * 4 * H));
+    expect_tx(bar_dsh, S ? (uint32_t)(nou * (4 * I + I / 2)) : 0u);
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- copies known at launch
+  // (issued by the first two lanes of every warp: one warp alone issues slowly)
+  const int issuer = lane < 2 ? warp * 2 + lane : -1;
+  if (issuer >= 0) {
+    const int ngu = gu_ops(a), ndn = dn_ops(a);
+    const int n1 = nsu * ngu, n2 = n1 + nre, n3 = n2 + (S ? nou * ndn : 0);
+    for (int o = issuer; o < n3; o += 2 * DWARPS) {
+      if (o < n1) {
+        const int i = o / ngu;
+        gu_op(a, mp, o % ngu, su + i * 8 * H, sus + i * H, E, (cta + i * G) * 8, bar_p1);
+      } else if (o < n2) {
+        const int i = o - n1;
+        ptx::bulk_g2s(rr + i * H, a.router + (size_t)(rc + i * a.rp_ctas) * H, 4 * H, bar_p1);
+      } else {
+        const int ol = (o - n2) / ndn;
+        dn_op(a, mp, (o - n2) % ndn, dc + (ol * NS + k) * 4 * I, ds + (ol * NS + k) * (I / 2), E,
+              (cta + ol * G) * 8, bar_dsh);
+      }
+    }
+  }
   trace_at(a, 1);
 
-  // ---------------------------------------------------------------- P0: x
+  // ---------------------------------------------------------------- P0: x (padded groups)
+  // The input (and the workspace) may still be written by the previous layer's
+  // launch when this one starts early: wait for it here, after the weight
+  // copies are on their way.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ unsigned long long s_base;
+  if (tid == 0) {  // a relaxed read: only the value matters, not ordering
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.bar) : "memory");
+    s_base = v / (unsigned long long)G * (unsigned long long)G;
+  }
+  // the residual of this CTA's output rows, read now rather than at the end
+  float res_v = 0.f;
+  if (tid < nou * 8) res_v = bf16_to_f32(a.res[(cta + (tid >> 3) * G) * 8 + (tid & 7)]);
   if (a.prenorm) {
     float ss = 0.f;
     for (int i = tid; i < H; i += DTHREADS) {
@@ -322,132 +444,142 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const DecArgs
 #pragma unroll
     for (int w = 0; w < DWARPS; ++w) tot += s_part[w];
     const float scale = rsqrtf(tot / (float)H + a.eps);
-    for (int i = tid; i < H; i += DTHREADS) xs[i] = f32_to_bf16(bf16_to_f32(a.xin[i]) * scale);
+    for (int i = tid; i < H; i += DTHREADS)
+      xs[(i >> 6) * XPAD + (i & 63)] = f32_to_bf16(bf16_to_f32(a.xin[i]) * scale);
   } else {
-    for (int i = tid; i < H; i += DTHREADS) xs[i] = a.xin[i];
+    for (int i = tid; i < H / 8; i += DTHREADS)
+      *reinterpret_cast<uint4 *>(xs + (i >> 3) * XPAD + (i & 7) * 8) = reinterpret_cast<const uint4 *>(a.xin)[i];
   }
-  trace_at(a, 2);
-  ptx::cp_async_wait_all();
   __syncthreads();
-  trace_at(a, 3);
+  trace_at(a, 2);
 
   // ---------------------------------------------------------------- P1: shared gate/up, router rows
-  if (nsu > 0) {
-    const int kc = k_chunks(nsu, H), len = H / kc;
-    if (warp < nsu * kc) gu_slice(p1 + (warp / kc) * a.ug, H, mb, xs, warp % kc, len, lane, red + warp * 16);
-    __syncthreads();
-    if (tid < nsu * 8) {
-      const int u = tid / 8, r = tid % 8;
-      float g = 0.f, uu = 0.f;
-      for (int c = 0; c < kc; ++c) {
-        g += red[(u * kc + c) * 16 + r];
-        uu += red[(u * kc + c) * 16 + 8 + r];
+  bool ok = wait_bar(bar_p1, a.status);
+  trace_at(a, 3);
+  if (ok && nsu > 0) ok = gu_compute(a, su, sus, nsu, nullptr, xs, red);
+  if (ok)
+    for (int i = warp; i < nre; i += DWARPS) {  // one warp per router row, fp32 FMA
+      const float *row = rr + i * H;
+      float acc = 0.f;
+      for (int kk = 4 * lane; kk < H; kk += 128) {
+        const float4 wv = *reinterpret_cast<const float4 *>(row + kk);
+        const uint2 xv = *reinterpret_cast<const uint2 *>(xs + (kk >> 6) * XPAD + (kk & 63));
+        acc = fmaf(__uint_as_float(xv.x << 16), wv.x, acc);
+        acc = fmaf(__uint_as_float(xv.x & 0xFFFF0000u), wv.y, acc);
+        acc = fmaf(__uint_as_float(xv.y << 16), wv.z, acc);
+        acc = fmaf(__uint_as_float(xv.y & 0xFFFF0000u), wv.w, acc);
       }
-      a.hbuf[(size_t)k * I + (cta + u * G) * 8 + r] = f32_to_bf16(silu(g) * uu);
+      acc = warp_sum(acc);
+      const int e = rc + i * a.rp_ctas;
+      if (lane == 0) a.keys[e] = a.bias ? acc + a.bias[e] : acc;
     }
-  }
-  for (int i = warp; i < nre; i += DWARPS) {  // one warp per router row, fp32 FMA
-    const float *row = rrows + i * H;
-    float acc = 0.f;
-    for (int kk = 4 * lane; kk < H; kk += 128) {
-      const float4 wv = *reinterpret_cast<const float4 *>(row + kk);
-      const uint2 xv = *reinterpret_cast<const uint2 *>(xs + kk);
-      acc = fmaf(__uint_as_float(xv.x << 16), wv.x, acc);
-      acc = fmaf(__uint_as_float(xv.x & 0xFFFF0000u), wv.y, acc);
-      acc = fmaf(__uint_as_float(xv.y << 16), wv.z, acc);
-      acc = fmaf(__uint_as_float(xv.y & 0xFFFF0000u), wv.w, acc);
-    }
-    acc = warp_sum(acc);
-    const int e = rc + i * a.rp_ctas;
-    if (lane == 0) a.keys[e] = a.bias ? acc + a.bias[e] : acc;
-  }
+  ok = __syncthreads_and(ok) != 0;  // every flag below stays uniform across the CTA
+  if (ok && nsu > 0) gu_finish(a, nsu, red, [&](int u) { return (size_t)k * I + (size_t)(cta + u * G) * 8; });
   trace_at(a, 4);
-  bool ok = grid_sync(a.bar, a.status);
+  ok = grid_sync(a.bar, s_base + (unsigned long long)G, a.status) && ok;
   trace_at(a, 5);
 
   // ---------------------------------------------------------------- P2: routing, routed gate/up
-  const int upr = I / 8;
-  const int nru = (cta < a.n_ru) ? (a.n_ru - 1 - cta) / G + 1 : 0;
+  bool issued2 = false;
   if (ok) {
     for (int e = tid; e < E; e += DTHREADS) keys[e] = __ldcg(a.keys + e);
     __syncthreads();
     trace_at(a, 6);
-    topk_block(keys, E, k, reinterpret_cast<unsigned long long *>(p2), s_ids, s_w, a.status);
+    topk_block(keys, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand),
+               reinterpret_cast<unsigned long long *>(sm + a.off_gmax), s_ids, s_w, a.status);
     __syncthreads();
     trace_at(a, 14);
     if (cta == 0 && tid < k) {
       a.topk_id[tid] = s_ids[tid];
       a.topk_w[tid] = s_w[tid];
     }
-    // group 1: routed gate/up units u = slot * (I/8) + rowblock with u % G == cta
-    for (int i = 0; i < nru; ++i) {
-      const int u = cta + i * G;
-      stage_gu(a, p2 + i * a.ug, s_ids[u / upr], (u % upr) * 8);
+    if (tid == 0) {
+      for (int i = 0; i < nru; ++i) expect_tx(&bar_ru[i], (uint32_t)(9 * H));
+      expect_tx(bar_drt, (uint32_t)(nou * k * (4 * I + I / 2)));
     }
-    ptx::cp_async_commit();
-    // group 2: the routed experts' down rows of this CTA's output units
-    for (int i = 0; i < nou; ++i)
-      for (int j = 0; j < k; ++j) stage_dn(a, p3 + (i * NS + j) * a.ud, s_ids[j], (cta + i * G) * 8);
-    ptx::cp_async_commit();
-    trace_at(a, 7);
-    ptx::cp_async_wait_1();
     __syncthreads();
-    trace_at(a, 8);
-    if (nru > 0) {
-      const int kc = k_chunks(nru, H), len = H / kc;
-      if (warp < nru * kc) gu_slice(p2 + (warp / kc) * a.ug, H, mb, xs, warp % kc, len, lane, red + warp * 16);
-      __syncthreads();
-      if (tid < nru * 8) {
-        const int ul = tid / 8, r = tid % 8, u = cta + ul * G;
-        float g = 0.f, uu = 0.f;
-        for (int c = 0; c < kc; ++c) {
-          g += red[(ul * kc + c) * 16 + r];
-          uu += red[(ul * kc + c) * 16 + 8 + r];
+    if (issuer >= 0) {
+      const int ngu = gu_ops(a), ndn = dn_ops(a);
+      const int n1 = nru * ngu, n2 = n1 + nou * k * ndn;
+      for (int o = issuer; o < n2; o += 2 * DWARPS) {
+        if (o < n1) {
+          const int i = o / ngu, u = cta + i * G;
+          gu_op(a, mp, o % ngu, ru + i * 8 * H, rus + i * H, s_ids[u / upr], (u % upr) * 8, &bar_ru[i]);
+        } else {
+          const int b = (o - n1) / ndn, ol = b / k, j = b % k;
+          dn_op(a, mp, (o - n1) % ndn, dc + (ol * NS + j) * 4 * I, ds + (ol * NS + j) * (I / 2), s_ids[j],
+                (cta + ol * G) * 8, bar_drt);
         }
-        a.hbuf[(size_t)(u / upr) * I + (u % upr) * 8 + r] = f32_to_bf16(silu(g) * uu);
       }
     }
+    issued2 = true;
+    trace_at(a, 7);
+    const bool ok2 = __syncthreads_and(gu_compute(a, ru, rus, nru, bar_ru, xs, red)) != 0;
+    trace_at(a, 8);
+    if (ok2 && nru > 0)
+      gu_finish(a, nru, red, [&](int u) {
+        const int uu = cta + u * G;
+        return (size_t)(uu / upr) * I + (size_t)(uu % upr) * 8;
+      });
+    ok = ok && ok2;
   }
   trace_at(a, 9);
-  ok = grid_sync(a.bar, a.status) && ok;
+  ok = grid_sync(a.bar, s_base + 2ull * (unsigned long long)G, a.status) && ok;
   trace_at(a, 10);
 
   // ---------------------------------------------------------------- P3: down + combine
-  ptx::cp_async_wait_all();  // also drains every copy of a CTA that gave up
+  // let the next launch in the stream start its prologue and weight copies
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (ok) ok = __syncthreads_and(wait_bar(bar_dsh, a.status) && wait_bar(bar_drt, a.status)) != 0;
   if (ok) {
-    // h of every slot, 16 bytes per load, all loads in flight together
-    const int nvec = NS * I / 8;
-    for (int i = tid; i < nvec; i += DTHREADS)
-      reinterpret_cast<uint4 *>(hs)[i] = __ldcg(reinterpret_cast<const uint4 *>(a.hbuf) + i);
+    const int nv = NS * I / 8;  // h of every slot, 16 bytes per load, into padded groups
+    for (int i = tid; i < nv; i += DTHREADS) {
+      const int j = i / (I / 8), c8 = i % (I / 8);
+      *reinterpret_cast<uint4 *>(hs + (j * (I / 64) + (c8 >> 3)) * XPAD + (c8 & 7) * 8) =
+          __ldcg(reinterpret_cast<const uint4 *>(a.hbuf) + i);
+    }
     __syncthreads();
     trace_at(a, 11);
-    // tasks (output unit, slot, K half): partial sums, then bf16(y) per slot
-    float *yp = red;  // [nou][NS][2][8] partials
-    const int ntask = nou * NS * 2;
-    for (int t = warp; t < ntask; t += DWARPS) {
-      const int half = t & 1, ol = (t >> 1) / NS, j = (t >> 1) % NS;
-      const uint8_t *base = p3 + (ol * NS + j) * a.ud;
-      const uint16_t *sd = reinterpret_cast<const uint16_t *>(base + 8 * dn_rs(I));
+    const int nkcd = I / KCH, gpr = I / 64, g = lane >> 2, q = lane & 3;
+    const int nitem = nou * NS * nkcd;
+    for (int t = warp; t < nitem; t += DWARPS) {
+      const int kc = t % nkcd, j = (t / nkcd) % NS, ol = t / (nkcd * NS);
+      uint32_t xr[32];
+      load_group(hs + j * (I / 64) * XPAD, 4 * kc + q, xr);
+      const uint16_t *sc = reinterpret_cast<const uint16_t *>(ds + (ol * NS + j) * (I / 2));
       float d[4] = {0.f, 0.f, 0.f, 0.f};
-      gemv8(base, dn_rs(I), sd, sd + 8 * (I / 64), I / 64, hs + j * I, half * (I / 2), (half + 1) * (I / 2), lane, d);
-      if (lane < 4) {
-        yp[t * 8 + 2 * lane] = d[0];
-        yp[t * 8 + 2 * lane + 1] = d[1];
+      gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, sc, sc + 8 * gpr, gpr, 4 * kc + q, xr, g, q, d);
+      if (g == 0) {
+        red[t * 8 + 2 * q] = d[0];
+        red[t * 8 + 2 * q + 1] = d[1];
       }
     }
     __syncthreads();
     trace_at(a, 12);
+    // y_j = bf16(h_j . Wd_j) of every (row, slot) in parallel, then the combine
+    float *ys = reinterpret_cast<float *>(sm + a.off_ys);  // [nou * 8][NS]
+    for (int t = tid; t < nou * 8 * NS; t += DTHREADS) {
+      const int ol = t / (8 * NS), r = (t / NS) & 7, j = t % NS;
+      float v = 0.f;
+      for (int kc = 0; kc < nkcd; ++kc) v += red[((ol * NS + j) * nkcd + kc) * 8 + r];
+      ys[t] = bf16_to_f32(f32_to_bf16(v));
+    }
+    __syncthreads();
     if (tid < nou * 8) {
-      const int ol = tid / 8, r = tid % 8;
-      const int n = (cta + ol * G) * 8 + r;
-      auto y = [&](int j) {
-        const int t = (ol * NS + j) * 2;
-        return bf16_to_f32(f32_to_bf16(yp[t * 8 + r] + yp[(t + 1) * 8 + r]));
-      };
-      float o = bf16_to_f32(a.res[n]);
-      if (S) o += y(k);
-      for (int j = 0; j < k; ++j) o = fmaf(s_w[j], y(j), o);
-      a.out[n] = f32_to_bf16(o);
+      const float *yr = ys + tid * NS;
+      float o = res_v;
+      if (S) o += yr[k];
+      for (int j = 0; j < k; ++j) o = fmaf(s_w[j], yr[j], o);
+      a.out[(cta + (tid >> 3) * G) * 8 + (tid & 7)] = f32_to_bf16(o);
+    }
+  }
+  // never leave with copies in flight into this CTA's shared memory
+  if (tid == 0 && !ok) {
+    wait_bar(bar_p1, a.status);
+    wait_bar(bar_dsh, a.status);
+    if (issued2) {
+      wait_bar(bar_drt, a.status);
+      for (int i = 0; i < nru; ++i) wait_bar(&bar_ru[i], a.status);
     }
   }
   trace_at(a, 13);
@@ -455,7 +587,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const DecArgs
 
 struct DecPlan {
   DecArgs a;
-  int grid, smem;
+  int grid, smem, max_ru;
 };
 
 DecPlan make_plan(int H, int E, int k, int I, int S, int num_sms) {
@@ -466,46 +598,60 @@ DecPlan make_plan(int H, int E, int k, int I, int S, int num_sms) {
   a.k = k;
   a.I = I;
   a.S = S;
-  const int G = num_sms;
+  const int G = num_sms, NS = k + S;
   a.n_su = S ? I / 8 : 0;
   a.rp_cta0 = a.n_su < G ? a.n_su : 0;
   a.rp_ctas = a.n_su < G ? G - a.n_su : G;
   a.n_ru = k * (I / 8);
   a.n_ou = H / 8;
-  a.ug = 2 * (8 * (H / 2 + 16) + 2 * (H / 4));
-  a.ud = 8 * (I / 2 + 16) + 2 * (I / 4);
   const int max_su = (a.n_su + G - 1) / G;
   const int max_re = (E + a.rp_ctas - 1) / a.rp_ctas;
   const int max_ru = (a.n_ru + G - 1) / G;
   const int max_ou = (a.n_ou + G - 1) / G;
-  auto al = [](int v) { return (v + 127) & ~127; };
+  const int nkc = H / KCH, nkcd = I / KCH;
+  auto al = [](int v, int m) { return (v + m - 1) / m * m; };
   int o = 0;
+  a.off_dc = o;
+  o = al(o + max_ou * NS * 4 * I, 1024);
+  a.off_ru = o;
+  o = al(o + max_ru * 8 * H, 1024);
+  a.off_su = o;
+  o = al(o + max_su * 8 * H, 1024);
+  a.off_rr = o;
+  o = al(o + max_re * 4 * H, 128);
   a.off_x = o;
-  o = al(o + H * 2);
+  o = al(o + (H / 64) * XPAD * 2, 128);
   a.off_h = o;
-  o = al(o + (k + S) * I * 2);
+  o = al(o + NS * (I / 64) * XPAD * 2, 128);
+  a.off_ds = o;
+  o = al(o + max_ou * NS * (I / 2), 128);
+  a.off_rus = o;
+  o = al(o + max_ru * H, 128);
+  a.off_sus = o;
+  o = al(o + max_su * H, 128);
   a.off_red = o;
-  o = al(o + 4096);
+  const int red_gu = (max_ru > max_su ? max_ru : max_su) * nkc * 16 * 4;
+  const int red_dn = max_ou * NS * nkcd * 8 * 4;
+  o = al(o + (red_gu > red_dn ? red_gu : red_dn), 128);
   a.off_keys = o;
-  o = al(o + E * 4);
-  a.off_p1 = o;
-  o = al(o + max_su * a.ug + max_re * H * 4);
-  a.off_p2 = o;
-  o = al(o + max_ru * a.ug);
-  a.off_p3 = o;
-  o = al(o + max_ou * (k + S) * a.ud);
-  p.smem = o;
+  o = al(o + E * 4, 128);
+  a.off_cand = o;
+  o = al(o + E * 8, 128);
+  a.off_gmax = o;
+  o = al(o + ((E + 15) / 16) * 8, 128);
+  a.off_bar = o;
+  o = al(o + (3 + MAX_RU) * 8, 128);
+  a.off_ys = o;
+  o = al(o + max_ou * 8 * NS * 4, 128);
+  p.smem = o + 1024;  // slack for aligning the base
   p.grid = G;
-  // reduction scratch: 16 floats per warp task, 16 per (output unit, slot)
-  if (max_ou * (k + S) * 16 * 4 > 4096) p.smem = -1;
+  p.max_ru = max_ru;
   return p;
 }
 
-}  // namespace
-
 // Dynamic shared memory the decode kernel may use on the current device: the
 // per-block opt-in maximum less the kernel's static shared memory.
-static int decode_smem_limit() {
+int decode_smem_limit() {
   int dev = 0, optin = 0;
   cudaFuncAttributes fa;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -517,13 +663,48 @@ static int decode_smem_limit() {
   return optin - (int)fa.sharedSizeBytes;
 }
 
+// Codes as bytes [rows][K/2]: either one 3-D box per 8 rows (dims 128 B x
+// rows x K/256 chunks, the chunk stride 128 B) or 2-D boxes of 8 rows x 128 B
+// taken one K-chunk at a time.  Both land as [chunk][row][128 B], swizzled.
+cudaError_t codes_map(CUtensorMap *m, const uint32_t *codes, int rows, int K, bool three_d) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorInitializationError;
+  CUresult r;
+  if (three_d) {
+    cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)(K / KCH)};
+    cuuint64_t strides[2] = {(cuuint64_t)(K / 2), 128};
+    cuuint32_t box[3] = {128, 8, (cuuint32_t)(K / KCH)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint32_t *>(codes), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+    cuuint32_t box[2] = {128, 8};
+    cuuint32_t estr[2] = {1, 1};
+    r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(codes), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_maps(DecMaps *m, const ExpertPtrs &w, int H, int E, int I, int S, bool three_d) {
+  const int E_tot = E + S;
+  cudaError_t e = codes_map(&m->gate, w.gate_q, E_tot * I, H, three_d);
+  if (e == cudaSuccess) e = codes_map(&m->up, w.up_q, E_tot * I, H, three_d);
+  if (e == cudaSuccess) e = codes_map(&m->down, w.down_q, E_tot * H, I, three_d);
+  return e;
+}
+
+}  // namespace
+
 bool decode_supported(int H, int E, int k, int I, int S, int num_sms) {
   auto pow2 = [](int v) { return v > 0 && (v & (v - 1)) == 0; };
-  if (!pow2(H) || !pow2(I) || H < 128 || I < 128 || num_sms <= 0 || k > 16) return false;
-  if ((size_t)E * 8 > (size_t)((k * (I / 8) + num_sms - 1) / num_sms) * (2 * (8 * (H / 2 + 16) + 2 * (H / 4))))
-    return false;  // the top-k codes borrow the P2 staging area
+  if (!pow2(H) || !pow2(I) || H < KCH || I < KCH || num_sms <= 0 || k > 16 || E > 1024) return false;
   DecPlan p = make_plan(H, E, k, I, S, num_sms);
-  return p.smem > 0 && p.smem <= decode_smem_limit();
+  return p.max_ru <= MAX_RU && p.smem <= decode_smem_limit();
 }
 
 cudaError_t decode_prepare(int H, int E, int k, int I, int S, int num_sms) {
@@ -557,19 +738,37 @@ cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, 
   a.trace = trace;
   a.prenorm = prenorm;
   a.eps = eps;
+  DecMaps maps;
+  a.map3d = 1;
+  cudaError_t e = make_maps(&maps, w, H, E, I, S, true);
+  if (e != cudaSuccess) {  // the driver refused the 3-D view: one 2-D box per K-chunk
+    a.map3d = 0;
+    if ((e = make_maps(&maps, w, H, E, I, S, false)) != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(DTHREADS);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  // The grid barrier needs every CTA resident at once: launch cooperatively
+  // or not at all.  Programmatic serialisation lets the launch begin while
+  // the previous kernel in the stream drains (the kernel waits for it before
+  // it reads its input); drivers that refuse the pair get a plain cooperative
+  // launch.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   prof_before(MOE_KERNEL_DECODE_LAYER, s);
-  // the grid barrier needs every CTA resident at once: launch cooperatively or not at all
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
+  e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, maps, a);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, maps, a);
+  }
   prof_after(MOE_KERNEL_DECODE_LAYER, s);
   if (e != cudaSuccess) return e;
   *launches += 1;

@@ -1,5 +1,6 @@
 // Tensor-core (tcgen05) grouped expert GEMMs: host-side declarations.
 #pragma once
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -10,6 +11,9 @@
 namespace moe {
 
 constexpr int TC_ROWS = 128;     // default token rows per block-map tile
+
+// The driver's cuTensorMapEncodeTiled (null when the driver lacks it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Dims the tensor-core path handles (H and I multiples of 256); others use
 // the CUDA-core kernels.
