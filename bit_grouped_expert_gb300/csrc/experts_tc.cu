@@ -13,10 +13,10 @@
 //               swizzle, one box per matrix per stage of 4 k-blocks
 //   warp 1      one thread issues tcgen05.mma (A from tensor memory, B from
 //               shared memory, D fp32 in tensor memory) and commits
-//   warp 2      cp.async loader of the token rows (gathered through perm for
+//   warps 2, 3  cp.async loaders of the token rows (gathered through perm for
 //               routed experts) into the 128B-swizzled K-major layout; each
 //               lane's copies arrive on the slot's mbarrier when they land
-//   warp 3      tensor-memory allocation
+//               (warp 3 also allocates and frees the tensor memory)
 //   warps 4-15  three warpgroups: dequantise a k-block of one matrix (64 codes
 //               of a row -> 32 bf16x2, w = bf16_rne(scale*q + bias)) straight
 //               into tensor memory with tcgen05.st, then run the epilogue:
@@ -40,7 +40,7 @@ constexpr int BM = 128;         // output features per work item (= TMEM lanes)
 constexpr int KBLK = 64;        // k-block = one quantisation group
 constexpr int STAGE_KB = 4;     // k-blocks per code stage (one TMA box per matrix)
 constexpr int BOX = BM * 128;   // one TMA box: 128 rows x 128 bytes (256 codes)
-constexpr int NSLOT = 4;        // A slots in TMEM == B slots in shared memory
+constexpr int NSLOT = 4;        // A slots in tensor memory (64 columns each)
 constexpr int MAXN = 128;       // token rows per work item
 constexpr int B_SLOT = MAXN * 128;
 constexpr int NWG = 3;                    // dequant/epilogue warpgroups
@@ -55,12 +55,18 @@ constexpr int SBOX = BM * 16;  // one scale (or bias) box: 128 rows x 8 groups o
 template <bool GATEUP>
 struct Cfg {
   static constexpr int NMAT = GATEUP ? 2 : 1;
-  static constexpr int CSTAGES = GATEUP ? 4 : 8;
+  // Code stages (4 k-blocks each, from HBM) and token-row slots (1 k-block
+  // each, mostly from L2) share the shared memory; the token rows get the
+  // deeper ring, since every k-block's MMA waits on them.
+  static constexpr int CSTAGES = GATEUP ? 3 : 4;
+  static constexpr int NBSLOT = GATEUP ? 6 : 8;
   // per stage: codes of each matrix, then (scale, bias) boxes of each matrix
   static constexpr int STAGE_BYTES = NMAT * BOX + NMAT * 2 * SBOX;
   static constexpr int OFF_B = CSTAGES * STAGE_BYTES;
-  static constexpr int OFF_MISC = OFF_B + NSLOT * B_SLOT;
+  static constexpr int OFF_MISC = OFF_B + NBSLOT * B_SLOT;
   static constexpr int SMEM = OFF_MISC + 1024 /* misc */ + 1024 /* alignment slack */;
+  static_assert(NBSLOT <= 8, "b_full / b_free arrays");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 // Tensor maps: codes of matrix 0/1, and (when tma_scales) scale/bias of
@@ -83,11 +89,10 @@ struct TcArgs {
 
 struct Misc {
   uint64_t code_full[8], code_empty[8];
-  uint64_t b_full[NSLOT], a_full[NSLOT], slot_free[NSLOT];
+  uint64_t b_full[8], b_free[8], a_full[NSLOT], a_free[NSLOT];
   uint64_t acc_full, acc_empty, final_bar;
   uint32_t tmem;
   int abort_flag;
-  int src[MAXN];
 };
 
 struct Item {
@@ -170,10 +175,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(&m->code_full[i], 1);
       ptx::mbar_init(&m->code_empty[i], NWG * 4);
     }
+    for (int i = 0; i < C::NBSLOT; ++i) {
+      ptx::mbar_init(&m->b_full[i], 64);  // one cp.async-tracked arrival per loader lane (2 warps)
+      ptx::mbar_init(&m->b_free[i], 1);
+    }
     for (int i = 0; i < NSLOT; ++i) {
-      ptx::mbar_init(&m->b_full[i], 32);  // one cp.async-tracked arrival per loader lane
       ptx::mbar_init(&m->a_full[i], C::NMAT * 128);  // one warpgroup per (k-block, matrix)
-      ptx::mbar_init(&m->slot_free[i], 1);
+      ptx::mbar_init(&m->a_free[i], 1);
     }
     ptx::mbar_init(&m->acc_full, 1);
     ptx::mbar_init(&m->acc_empty, NWG * 128);
@@ -250,22 +258,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!wait_bar(&m->acc_empty, (itc & 1u) ^ 1u, m, a.status)) break;
         ptx::tc_fence_after();
         for (int kb = 0; kb < KB; ++kb, ++kbc) {
-          const int slot = kbc % NSLOT;
-          const uint32_t ph = (kbc / NSLOT) & 1u;
-          if (!wait_bar(&m->b_full[slot], ph, m, a.status) || !wait_bar(&m->a_full[slot], ph, m, a.status)) {
+          const int slot = kbc % NSLOT, bslot = kbc % C::NBSLOT;
+          if (!wait_bar(&m->b_full[bslot], (kbc / C::NBSLOT) & 1u, m, a.status) ||
+              !wait_bar(&m->a_full[slot], (kbc / NSLOT) & 1u, m, a.status)) {
             ok = false;
             break;
           }
           ptx::fence_proxy_async_smem();  // token rows were written by cp.async (generic proxy)
           ptx::tc_fence_after();
-          const uint32_t baddr = ptx::smem_u32(smem + C::OFF_B + slot * B_SLOT);
+          const uint32_t baddr = ptx::smem_u32(smem + C::OFF_B + bslot * B_SLOT);
 #pragma unroll
           for (int mat = 0; mat < C::NMAT; ++mat)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               ptx::mma_ts(tmem + mat * D_UP_COL, tmem + A_COL + slot * 64 + mat * 32 + i * 8,
                           ptx::sdesc_sw128(baddr + 32 * i), idesc, (uint32_t)(kb | i));
-          ptx::mma_commit(&m->slot_free[slot]);
+          ptx::mma_commit(&m->a_free[slot]);
+          ptx::mma_commit(&m->b_free[bslot]);
         }
         if (!ok) break;
         ptx::mma_commit(&m->acc_full);
@@ -275,17 +284,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mma_commit(&m->final_bar);
       drain_wait(&m->final_bar, 0);
     }
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ token-row loader
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ token-row loaders
+    // Warps 2 and 3 each copy half of the tile's rows: lane l of loader w owns
+    // rows w*4 + l/8 + 8i (i < 16) and 16-byte chunk l%8 of each, so its
+    // destinations share one swizzle and its sources are kept as 32-bit byte
+    // offsets for the whole item.
+    const int lw = warp - 2, c = lane & 7, r0 = lw * 4 + (lane >> 3);
+    const uint8_t *act = reinterpret_cast<const uint8_t *>(a.act);
+    const uint32_t sw = (uint32_t)((c ^ (r0 & 7)) << 4);
     uint32_t kbc = 0;
     bool ok = true;
-    const int c = lane & 7;
     Item nit = blockIdx.x < n_items ? get_item(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const Item it = nit;
       if (item + (int)gridDim.x < n_items) nit = get_item(a, item + gridDim.x, MT);
-      __syncwarp();
-      for (int r = lane; r < MAXN; r += 32) {
+      uint32_t off[MAXN / 8];
+      uint32_t valid = 0;  // bit i: row r0 + 8i holds a token
+#pragma unroll
+      for (int i = 0; i < MAXN / 8; ++i) {
+        const int r = r0 + 8 * i;
+        if (r >= it.n_mma) break;  // rows past the MMA's N are never copied
         int src = -1;
         if (r < it.nrows) {
           if (GATEUP)
@@ -293,21 +312,23 @@ __global__ void __launch_bounds__(THREADS, 1)
           else
             src = it.row0 + r;
         }
-        m->src[r] = src;
+        off[i] = src < 0 ? 0u : (uint32_t)src * (uint32_t)a.K * 2u + (uint32_t)c * 16u;
+        if (src >= 0) valid |= 1u << i;
       }
-      __syncwarp();
+      const int nr = it.n_mma;
       for (int kb = 0; kb < KB; ++kb, ++kbc) {
-        const int slot = kbc % NSLOT;
-        const uint32_t ph = (kbc / NSLOT) & 1u;
-        if (!__all_sync(0xffffffffu, wait_bar(&m->slot_free[slot], ph ^ 1u, m, a.status))) {
+        const int slot = kbc % C::NBSLOT;
+        const uint32_t ph = (kbc / C::NBSLOT) & 1u;
+        if (!__all_sync(0xffffffffu, wait_bar(&m->b_free[slot], ph ^ 1u, m, a.status))) {
           ok = false;
           break;
         }
-        uint8_t *bs = smem + C::OFF_B + slot * B_SLOT;
-        for (int r = lane >> 3; r < it.n_mma; r += 4) {
-          const int src = m->src[r];
-          const uint16_t *g = a.act + (size_t)(src < 0 ? 0 : src) * a.K + kb * KBLK + c * 8;
-          ptx::cp_async_16(bs + r * 128 + ((c ^ (r & 7)) << 4), g, src < 0 ? 0u : 16u);
+        uint8_t *bs = smem + C::OFF_B + slot * B_SLOT + r0 * 128 + sw;
+        const uint32_t kofs = (uint32_t)kb * (KBLK * 2);
+#pragma unroll
+        for (int i = 0; i < MAXN / 8; ++i) {
+          if (r0 + 8 * i >= nr) break;  // small tiles: a few iterations, not sixteen
+          ptx::cp_async_16(bs + i * 1024, act + off[i] + kofs, ((valid >> i) & 1u) ? 16u : 0u);
         }
         ptx::cp_async_arrive_noinc(&m->b_full[slot]);  // fires when this lane's copies have landed
       }
@@ -395,7 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const int aslot = kbg % NSLOT;
           if (!__all_sync(0xffffffffu,
-                          wait_bar(&m->slot_free[aslot], ((kbg / NSLOT) & 1u) ^ 1u, m, a.status))) {
+                          wait_bar(&m->a_free[aslot], ((kbg / NSLOT) & 1u) ^ 1u, m, a.status))) {
             ok = false;
             break;
           }
