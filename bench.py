@@ -38,6 +38,15 @@ H, E, K_TOP, I_DIM, G = 2048, 256, 8, 512, 64
 EXPERT_BYTES = 3 * (H * I_DIM // 2) + 3 * 2 * 2 * (H * I_DIM // G)   # 1,769,472
 GATEUP_BYTES = 2 * (H * I_DIM // 2) + 2 * 2 * 2 * (H * I_DIM // G)   # 1,179,648
 ROUTER_BYTES = E * H * 4                                              # 2,097,152
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture of the current kernels (profiles/*.md give the commands); None
+# where no capture of that workload exists.  Update with every kernel change.
+TRAFFIC = {
+    "decode40": 18_112_256,       # decode_layer_kernel, profiles/decode_layer_decode40.md
+    "layer256": 310_078_464,      # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer256.md
+    "layer4096": 375_236_608,     # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer4096.md
+}
 METRIC = "MoE-layer prefill tokens/s & % of roofline (T=256–32K); T=1 HBM GB/s"
 
 WORKLOADS = {
@@ -343,7 +352,7 @@ def run_ours(args, wl, rank, world, device):
             peak = pk["bf16_tflops_sustained"] if L > 1 else pk["bf16_tflops"]
             unit = "TFLOP/s"
         roofline = {"bound": dom_bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                    "frac": round(achieved / peak, 4), "traffic": None,
+                    "frac": round(achieved / peak, 4), "traffic": TRAFFIC.get(args.workload),
                     "kernel": "decode layer (router+top-k+9 experts+combine)" if T == 1 else "grouped gate/up",
                     "kernel_ms": round(dom_ms, 5), "peak_src": pk["src"]}
     else:
