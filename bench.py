@@ -43,11 +43,13 @@ ROUTER_BYTES = E * H * 4                                              # 2,097,15
 # capture of the current kernels (profiles/*.md give the commands); None
 # where no capture of that workload exists.  Update with every kernel change.
 TRAFFIC = {
-    "decode40": 18_112_256,       # decode_layer_kernel, profiles/decode_layer_decode40.md
+    "decode40": None,             # decode_layer_kernel, 7 layers per launch: not yet captured
     "layer256": 310_078_464,      # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer256.md
     "layer4096": 375_236_608,     # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer4096.md
 }
 METRIC = "MoE-layer prefill tokens/s & % of roofline (T=256–32K); T=1 HBM GB/s"
+
+STACK = 7  # layers per launch of the stacked decode kernel
 
 WORKLOADS = {
     "decode40": dict(T=1, layers=40, chunk=1, zipf=False, centred=False,
@@ -232,12 +234,21 @@ def run_ours(args, wl, rank, world, device):
     stream = torch.cuda.Stream(device=device)
     launches = [0]
 
-    # dominant kernel: gate/up (decode: the one-launch decode layer).  Only a
-    # few of its launches per step are bracketed by events, so the event nodes
-    # in the captured step barely perturb the step time.
+    # dominant kernel: gate/up (decode: the decode kernel, which runs up to
+    # STACK layers per cooperative launch).  Only a few of its launches per
+    # step are bracketed by events, so the event nodes in the captured step
+    # barely perturb the step time.
     dom = moe.MOE_KERNEL_DECODE_LAYER if T == 1 else moe.MOE_KERNEL_GATEUP
-    prof_layers = sorted({(2 * j + 1) * L // 8 for j in range(4)}) if L >= 4 else [0]
-    n_dom = len(prof_layers)
+    if T == 1 and L > 1:
+        # layer groups of one launch each; the 2nd and 4th (full) ones are timed
+        groups = [(l0, min(L, l0 + STACK)) for l0 in range(0, L, STACK)]
+        prof_groups = [j for j in (1, 3) if j < len(groups) and groups[j][1] - groups[j][0] == STACK] or [0]
+        n_dom = len(prof_groups)
+        layers_per_launch = groups[prof_groups[0]][1] - groups[prof_groups[0]][0]
+    else:
+        prof_layers = sorted({(2 * j + 1) * L // 8 for j in range(4)}) if L >= 4 else [0]
+        n_dom = len(prof_layers)
+        layers_per_launch = 1
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
     profiling = [False]
@@ -252,8 +263,26 @@ def run_ours(args, wl, rank, world, device):
         if on:
             moe.moe_profile_events(dom)
 
+    def stack(j):
+        on = profiling[0] and j in prof_groups
+        if on:
+            i = prof_groups.index(j)
+            moe.moe_profile_events(dom, ev_a[i:i + 1], ev_b[i:i + 1])
+        l0, l1 = groups[j]
+        moe.moe_decode_stack(plan, r, cws[l0:l1], None, ws, stream=stream)
+        launches[0] += moe.moe_last_launch_count()
+        if on:
+            moe.moe_profile_events(dom)
+
     def body():
         launches[0] = 0
+        if T == 1 and L > 1:
+            # the residual stream through the whole stack, one call per group
+            r.copy_(x_in)
+            for j in range(len(groups)):
+                stack(j)
+            out.copy_(r)
+            return
         for c0 in range(0, T, chunk):
             if L == 1:
                 forward(0, c0, x_in[c0:c0 + chunk], out[c0:c0 + chunk])
@@ -329,7 +358,7 @@ def run_ours(args, wl, rank, world, device):
         bytes_tok = L * (ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2)
         gbs = bytes_tok * args.steps / (ms * 1e-3) / 1e9 * world
         result.update(value=gbs, unit="GB/s", higher_is_better=True)
-        dom_bytes = ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2
+        dom_bytes = layers_per_launch * (ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2)
         dom_bound, dom_units = "hbm", dom_bytes
     else:
         tps = tok_per_step * args.steps / (ms * 1e-3) * world
@@ -353,7 +382,8 @@ def run_ours(args, wl, rank, world, device):
             unit = "TFLOP/s"
         roofline = {"bound": dom_bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                     "frac": round(achieved / peak, 4), "traffic": TRAFFIC.get(args.workload),
-                    "kernel": "decode layer (router+top-k+9 experts+combine)" if T == 1 else "grouped gate/up",
+                    "kernel": (f"decode kernel, {layers_per_launch} layers per launch (RMSNorm+router+top-k+9 experts"
+                               "+combine each)") if T == 1 else "grouped gate/up",
                     "kernel_ms": round(dom_ms, 5), "peak_src": pk["src"]}
     else:
         roofline = {"error": dom_err}

@@ -33,11 +33,13 @@ MOE_FLAG_SIMT_EXPERTS = 0x4
 MOE_FLAG_TILE_ROWS_64 = 0x8
 MOE_FLAG_PRENORM = 0x10
 MOE_FLAG_TRACE = 0x20
+MOE_TRACE_CTAS = 256
+MOE_TRACE_SLOTS = 32
 
 EXPORTS = ("moe_plan", "moe_plan_destroy", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_route_from_logits", "moe_forward", "moe_route_view", "moe_rmsnorm", "moe_dequant",
            "moe_device_status", "moe_last_launch_count", "moe_status_str", "moe_profile_events", "moe_last_cuda_error",
-           "moe_decode_static")
+           "moe_decode_static", "moe_decode_stack")
 
 MOE_DECODE_STATIC_SCRATCH_BYTES = 65536
 
@@ -117,6 +119,8 @@ def lib():
         L.moe_last_cuda_error.argtypes = []
         L.moe_status_str.restype = ctypes.c_char_p
         L.moe_status_str.argtypes = [i32]
+        L.moe_decode_stack.restype = i32
+        L.moe_decode_stack.argtypes = [vp, vp, i32, ctypes.POINTER(moe_weights), ctypes.POINTER(vp), vp, sz, vp]
         L.moe_decode_static.restype = i32
         L.moe_decode_static.argtypes = [ctypes.POINTER(moe_config), vp, vp, ctypes.POINTER(moe_weights), vp, vp, vp,
                                         u32, vp]
@@ -208,6 +212,21 @@ def moe_forward(plan: Plan, x, residual, T: int, weights, logit_bias, out, ws, s
     cw = weights if isinstance(weights, moe_weights) else make_weights(weights)
     _check("moe_forward", lib().moe_forward(plan.handle, _ptr(x), _ptr(residual), int(T), ctypes.byref(cw),
                                             _ptr(logit_bias), _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_decode_stack(plan: Plan, r, weights, logit_bias=None, ws=None, stream=None):
+    """Single-token decode through len(weights) pre-norm layers, r updated in
+    place.  ``weights``: list of weight dicts (or moe_weights); ``logit_bias``:
+    None or a list of per-layer bias tensors (entries may be None)."""
+    n = len(weights)
+    arr = (moe_weights * max(n, 1))(*[w if isinstance(w, moe_weights) else make_weights(w) for w in weights])
+    bias = None
+    if logit_bias is not None:
+        if len(logit_bias) != n:
+            raise ValueError("one logit bias (or None) per layer")
+        bias = (ctypes.c_void_p * max(n, 1))(*[_ptr(b) for b in logit_bias])
+    _check("moe_decode_stack", lib().moe_decode_stack(plan.handle, _ptr(r), n, arr, bias, _ptr(ws), _nbytes(ws),
+                                                      _stream(stream)))
 
 
 def moe_decode_static(cfg: moe_config, x, residual, weights, logit_bias, out, status=None, flags: int = 0,

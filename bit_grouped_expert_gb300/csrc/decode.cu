@@ -50,34 +50,45 @@ constexpr int DWARPS = DTHREADS / 32;
 constexpr int KCH = 256;   // codes per K-chunk: 4 groups, 128 bytes of a code row
 constexpr int XPAD = 72;   // bf16 slots per 64-value group of x / h in shared memory
 constexpr int MAX_RU = 8;  // routed gate/up units (mbarriers) per CTA
+constexpr int MAXL = 7;    // layers per launch (the parameters stay under 4 KB)
+constexpr int XREG = 4;    // uint2 of r a thread holds in the RMSNorm: H <= 4 * XREG * DTHREADS
 constexpr unsigned long long DTIMEOUT_NS = 1000000000ull;
 
 struct DecMaps {
   CUtensorMap gate, up, down;  // packed codes, [rows][K/2] bytes, 128B-swizzled 8-row boxes
 };
 
-struct DecArgs {
-  const uint16_t *xin;  // x, or the residual stream r for pre-norm plans
-  const uint16_t *res;  // residual added by the combine
-  uint16_t *out;
+// One layer's weights: router fp32 [E][H], logit bias [E] or null, experts.
+struct LayerW {
   const float *router, *bias;
   ExpertPtrs w;
+};
+
+struct DecArgs {
+  DecMaps maps[MAXL];   // per layer (the tensor maps must live in the parameters)
+  LayerW lw[MAXL];
+  int nl;               // layers of this launch
+  const uint16_t *xin;  // x, or the residual stream r for pre-norm plans (layers > 0: r)
+  const uint16_t *res;  // residual added by the first layer's combine (later layers: r)
+  uint16_t *out;        // output (stacks: r, updated in place layer by layer)
   float *keys;
   int32_t *topk_id;
   float *topk_w;
   uint16_t *hbuf;           // [k+S][I]
   unsigned long long *bar;  // monotonic arrival counter of the grid barrier
   int32_t *status;
-  uint64_t *trace;  // [3][16] phase timestamps or null
+  uint64_t *trace;  // [MOE_TRACE_CTAS][MOE_TRACE_SLOTS] phase timestamps or null
   int H, E, k, I, S, prenorm;
   float eps;
   int map3d;  // 1: one TMA op per matrix (3-D map over the K-chunks), 0: one per K-chunk
   // schedule
   int n_su, rp_cta0, rp_ctas, n_ru, n_ou;
   // shared-memory layout (bytes from the 1024-aligned base)
-  int off_dc, off_ru, off_su, off_rr, off_x, off_h, off_ds, off_rus, off_sus, off_red, off_keys, off_cand,
+  int off_dc, off_ru, off_su, off_rr, off_x, off_xn, off_h, off_ds, off_rus, off_sus, off_red, off_keys, off_cand,
       off_gmax, off_bar, off_ys;
 };
+static_assert(sizeof(DecArgs) <= 4000, "kernel parameters stay under 4 KB");
+
 
 __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p) {
   unsigned long long v;
@@ -95,12 +106,18 @@ __device__ __forceinline__ void red_add_release64(unsigned long long *p, unsigne
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ bool grid_sync(unsigned long long *bar, unsigned long long target, int32_t *status) {
-  __shared__ int s_ok;
+// Split phases: grid_arrive publishes this CTA's writes (every thread's, via
+// the block barrier and the release) and grid_wait returns once every CTA
+// has arrived; work between the two overlaps the barrier's latency.
+__device__ __forceinline__ void grid_arrive(unsigned long long *bar) {
   __syncthreads();
+  if (threadIdx.x == 0) red_add_release64(bar, 1ull);
+}
+
+__device__ bool grid_wait(unsigned long long *bar, unsigned long long target, int32_t *status) {
+  __shared__ int s_ok;
   if (threadIdx.x == 0) {
     int ok = 1;
-    red_add_release64(bar, 1ull);
     if (ld_acquire64(bar) < target) {
       const uint64_t t0 = ptx::globaltimer();
       while (ld_acquire64(bar) < target) {
@@ -117,11 +134,16 @@ __device__ bool grid_sync(unsigned long long *bar, unsigned long long target, in
   return s_ok != 0;
 }
 
-// Bounded wait for phase 0 of a one-shot mbarrier.
-__device__ bool wait_bar(uint64_t *bar, int32_t *status) {
-  if (ptx::mbar_try_wait(bar, 0)) return true;
+__device__ bool grid_sync(unsigned long long *bar, unsigned long long target, int32_t *status) {
+  grid_arrive(bar);
+  return grid_wait(bar, target, status);
+}
+
+// Bounded wait for the phase of an mbarrier with the given parity.
+__device__ bool wait_bar(uint64_t *bar, uint32_t parity, int32_t *status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait_sleep(bar, 0, 20000)) {
+  while (!ptx::mbar_try_wait_sleep(bar, parity, 20000)) {
     if (ptx::globaltimer() - t0 > DTIMEOUT_NS) {
       set_status(status, MOE_ERR_DEVICE_TIMEOUT);
       return false;
@@ -135,59 +157,59 @@ __device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
                : "memory");
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%4,%5,%5}, {%6,%7}, "
+// D += A.B on bf16 fragments, fp32 accumulators (m16n8k16).
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(b0), "r"(b1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Codes 2b and 2b+1 of a word (its byte b) as bf16_rne(s*q + bias), packed;
-// w4 = w >> 4.  0x4300 | q is the bf16 value 128 + q, so one subtraction and
-// one fused multiply-add (a single rounding) rebuild the weight.
-__device__ __forceinline__ uint32_t dq(uint32_t w, uint32_t w4, int b, __nv_bfloat162 s2, __nv_bfloat162 b2) {
-  uint32_t t = __byte_perm(w, w4, (uint32_t)(b | ((4 + b) << 8)));
+// Codes j and j+4 of a word (nibbles j and j+4, after a shift of 4j bits) as
+// bf16_rne(s*q + bias), packed.  0x4300 | q is the bf16 value 128 + q, so one
+// subtraction and one fused multiply-add (a single rounding) rebuild the weight.
+__device__ __forceinline__ uint32_t dq(uint32_t t, __nv_bfloat162 s2, __nv_bfloat162 b2) {
   t = (t & 0x000F000Fu) | 0x43004300u;
   const __nv_bfloat162 m = *reinterpret_cast<__nv_bfloat162 *>(&t);
   const __nv_bfloat162 r = __hfma2(s2, __hsub2(m, __floats2bfloat162_rn(128.f, 128.f)), b2);
   return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-// The 64 values of quantisation group `grp` (bf16 pairs) of a padded shared
-// vector (XPAD slots per group).
-__device__ __forceinline__ void load_group(const uint16_t *v, int grp, uint32_t (&xr)[32]) {
-  const uint4 *p = reinterpret_cast<const uint4 *>(v + grp * XPAD);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 t = p[i];
-    xr[4 * i] = t.x;
-    xr[4 * i + 1] = t.y;
-    xr[4 * i + 2] = t.z;
-    xr[4 * i + 3] = t.w;
-  }
+// Vectors the GEMV reads (x, h) sit in shared memory in groups of 64 values,
+// XPAD slots apart, each 8-value run (one code word) stored in the order
+// p0 p4 p1 p5 | p2 p6 p3 p7: the pairs dq() yields.  perm8 takes a run in
+// natural order (v0 = p0 p1, v1 = p2 p3, v2 = p4 p5, v3 = p6 p7) to that order.
+__device__ __forceinline__ uint4 perm8(uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  return make_uint4(__byte_perm(v0, v2, 0x5410), __byte_perm(v0, v2, 0x7632), __byte_perm(v1, v3, 0x5410),
+                    __byte_perm(v1, v3, 0x7632));
 }
 
-// d += x . W over one K-chunk of 8 rows.  chunk: the swizzled [8][128 B] code
+// x . W over one K-chunk of 8 rows.  chunk: the swizzled [8][128 B] code
 // image of the chunk; s, b: the rows' scales and biases ([8][gpr] bf16);
-// lane (g, q) handles group grp = 4 * chunk + q of row g.  After the call
-// lane q holds rows 2q (d[0]) and 2q+1 (d[1]).
-__device__ __forceinline__ void gemv_chunk(const uint8_t *chunk, const uint16_t *s, const uint16_t *b, int gpr,
-                                           int grp, const uint32_t (&xr)[32], int g, int q, float (&d)[4]) {
+// xg: the chunk's first group of the permuted vector.  Lane (g, q) takes
+// group q of the chunk in row g; the weights are the A operand: rows g and
+// g+8 of A are codes {j, j+4 : j = 0, 1} and {j, j+4 : j = 2, 3} of a word of
+// row g, and B columns 0 and 1 (lanes g = 0 and 1) carry the matching x
+// values, so D[g][0] + D[g+8][1] sums row g over the 32 values of the word
+// and its three quad partners.  Returns row g's sum in the lanes with q == 0.
+__device__ __forceinline__ float gemv_chunk(const uint8_t *chunk, const uint16_t *s, const uint16_t *b, int gpr,
+                                            int grp, const uint16_t *xg, int g, int q) {
   const uint8_t *row = chunk + g * 128;
   const uint4 c0 = *reinterpret_cast<const uint4 *>(row + (((2 * q) ^ g) << 4));
   const uint4 c1 = *reinterpret_cast<const uint4 *>(row + (((2 * q + 1) ^ g) << 4));
   const __nv_bfloat162 s2 = bf16x2_splat(s[g * gpr + grp]), b2 = bf16x2_splat(b[g * gpr + grp]);
   const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  // four accumulators: chains of four dependent MMAs instead of sixteen
+  const uint2 *xp = reinterpret_cast<const uint2 *>(xg + q * XPAD) + (g & 1);
+  // four accumulators: chains of two dependent MMAs
   float e[4][4] = {};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {  // word i holds codes 8i..8i+7: MMAs 2i and 2i+1
-    const uint32_t w = wv[i], w4 = w >> 4;
-    mma16816(e[(2 * i) & 3], xr[4 * i], xr[4 * i + 1], dq(w, w4, 0, s2, b2), dq(w, w4, 1, s2, b2));
-    mma16816(e[(2 * i + 1) & 3], xr[4 * i + 2], xr[4 * i + 3], dq(w, w4, 2, s2, b2), dq(w, w4, 3, s2, b2));
+  for (int i = 0; i < 8; ++i) {  // word i: codes 8i..8i+7 of the group
+    const uint32_t w = wv[i];
+    const uint2 xv = xp[2 * i];
+    mma16816(e[i & 3], dq(w, s2, b2), dq(w >> 8, s2, b2), dq(w >> 4, s2, b2), dq(w >> 12, s2, b2), xv.x, xv.y);
   }
-#pragma unroll
-  for (int r = 0; r < 4; ++r) d[r] += (e[0][r] + e[1][r]) + (e[2][r] + e[3][r]);
+  return ((e[0][0] + e[1][0]) + (e[2][0] + e[3][0])) + ((e[0][3] + e[1][3]) + (e[2][3] + e[3][3]));
 }
 
 __device__ __forceinline__ int gu_ops(const DecArgs &a) { return 2 * (a.map3d ? 1 : a.H / KCH) + 4; }
@@ -196,8 +218,8 @@ __device__ __forceinline__ int dn_ops(const DecArgs &a) { return (a.map3d ? 1 : 
 // Gate/up image of one unit: codes [2 matrices][H/256 chunks][8 rows][128 B]
 // (8H bytes) and scales [gate_s, gate_b, up_s, up_b][8 rows][H/64] (H bytes).
 // Issues copy o of the unit (code boxes of both matrices, then 4 scale rows).
-__device__ void gu_op(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cdst, uint8_t *sdst, int e, int r0,
-                      uint64_t *bar) {
+__device__ void gu_op(const DecArgs &a, const LayerW &L, const DecMaps &mp, int o, uint8_t *cdst, uint8_t *sdst,
+                      int e, int r0, uint64_t *bar) {
   const int H = a.H, nco = a.map3d ? 1 : H / KCH;
   const int row = e * a.I + r0;
   if (o < 2 * nco) {
@@ -210,15 +232,15 @@ __device__ void gu_op(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cdst,
       ptx::tma_load_2d(dst, map, bar, c * 128, row);
   } else {
     const int which = o - 2 * nco;  // 0 gate_s, 1 gate_b, 2 up_s, 3 up_b
-    const uint16_t *src = which == 0 ? a.w.gate_s : which == 1 ? a.w.gate_b : which == 2 ? a.w.up_s : a.w.up_b;
+    const uint16_t *src = which == 0 ? L.w.gate_s : which == 1 ? L.w.gate_b : which == 2 ? L.w.up_s : L.w.up_b;
     ptx::bulk_g2s(sdst + which * (H / 4), src + (size_t)row * (H / 64), H / 4, bar);
   }
 }
 
 // Down image of one (output unit, slot): codes [I/256 chunks][8 rows][128 B]
 // (4I bytes) and scales [down_s, down_b][8 rows][I/64] (I/2 bytes).
-__device__ void dn_op(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cdst, uint8_t *sdst, int e, int n0,
-                      uint64_t *bar) {
+__device__ void dn_op(const DecArgs &a, const LayerW &L, const DecMaps &mp, int o, uint8_t *cdst, uint8_t *sdst,
+                      int e, int n0, uint64_t *bar) {
   const int I = a.I, nco = a.map3d ? 1 : I / KCH;
   const int row = e * a.H + n0;
   if (o < nco) {
@@ -228,7 +250,7 @@ __device__ void dn_op(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cdst,
       ptx::tma_load_2d(cdst + o * 1024, &mp.down, bar, o * 128, row);
   } else {
     const int which = o - nco;  // 0 down_s, 1 down_b
-    ptx::bulk_g2s(sdst + which * (I / 4), (which ? a.w.down_b : a.w.down_s) + (size_t)row * (I / 64), I / 4, bar);
+    ptx::bulk_g2s(sdst + which * (I / 4), (which ? L.w.down_b : L.w.down_s) + (size_t)row * (I / 64), I / 4, bar);
   }
 }
 
@@ -238,26 +260,20 @@ __device__ void dn_op(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cdst,
 // with `bars`, unit u is read once bars[u] completes.  Returns false on a
 // timeout.
 __device__ bool gu_compute(const DecArgs &a, const uint8_t *codes, const uint8_t *scales, int nu, uint64_t *bars,
+                           uint32_t parity,
                            const uint16_t *xs, float *red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   const int H = a.H, nkc = H / KCH, WK = nkc < DWARPS ? nkc : DWARPS, WR = DWARPS / WK;
   const int kg = warp % WK, rg = warp / WK, gpr = H / 64;
   if (rg >= 2 * nu) return true;
   for (int kc = kg; kc < nkc; kc += WK) {
-    uint32_t xr[32];
-    load_group(xs, 4 * kc + q, xr);
     for (int rs = rg; rs < 2 * nu; rs += WR) {
       const int u = rs >> 1, mat = rs & 1;  // gate (0) or up (1) rows of unit u
-      if (bars && !wait_bar(&bars[u], a.status)) return false;
+      if (bars && !wait_bar(&bars[u], parity, a.status)) return false;
       const uint16_t *su = reinterpret_cast<const uint16_t *>(scales + (size_t)u * H) + mat * 16 * gpr;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      gemv_chunk(codes + (size_t)u * 8 * H + mat * 4 * H + kc * 1024, su, su + 8 * gpr, gpr, 4 * kc + q, xr, g, q,
-                 d);
-      if (g == 0) {
-        float *r = red + (u * nkc + kc) * 16 + mat * 8;
-        r[2 * q] = d[0];
-        r[2 * q + 1] = d[1];
-      }
+      const float d = gemv_chunk(codes + (size_t)u * 8 * H + mat * 4 * H + kc * 1024, su, su + 8 * gpr, gpr,
+                                 4 * kc + q, xs + 4 * kc * XPAD, g, q);
+      if (q == 0) red[(u * nkc + kc) * 16 + mat * 8 + g] = d;
     }
   }
   return true;
@@ -277,6 +293,66 @@ __device__ void gu_finish(const DecArgs &a, int nu, const float *red, RowOf row_
     }
     a.hbuf[row_of(u) + r] = f32_to_bf16(silu(gs) * us);
   }
+}
+
+// Top-k of one token by one warp, for E <= 256 keys read from global memory:
+// lane l holds the codes of experts l, l+32, ...  The k-th largest of the 32
+// lane maxima bounds the k-th largest key from below (k distinct keys reach
+// it), so only the keys at or above it -- at most 8k -- are ranked, each
+// against the others.  Same order and tie rule as topk_block.
+__device__ void topk_warp(const float *keys_g, int E, int k, unsigned long long *cand, int32_t *ids, float *w,
+                          int32_t *status) {
+  const int lane = threadIdx.x & 31;
+  float kv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) kv[i] = lane + 32 * i < E ? __ldcg(keys_g + lane + 32 * i) : 0.f;
+  unsigned long long c[8], m = 0ull;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    c[i] = lane + 32 * i < E ? topk_code(kv[i], lane + 32 * i) : 0ull;
+    m = c[i] > m ? c[i] : m;
+  }
+  // rank of this lane's maximum among the lane maxima (the nonzero ones are distinct)
+  int r = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)m, j), hi = __shfl_sync(0xffffffffu, (uint32_t)(m >> 32), j);
+    r += (((unsigned long long)hi << 32) | lo) > m;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, m != 0ull && r == k - 1);
+  unsigned long long tau = 0ull;  // no such lane: E < k cannot occur, rank everything
+  if (hit) {
+    const int src = __ffs(hit) - 1;
+    const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)m, src), hi = __shfl_sync(0xffffffffu, (uint32_t)(m >> 32), src);
+    tau = ((unsigned long long)hi << 32) | lo;
+  }
+  int n = 0;
+  const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool take = c[i] != 0ull && c[i] >= tau;
+    const unsigned b = __ballot_sync(0xffffffffu, take);
+    if (take) cand[n + __popc(b & below)] = c[i];
+    n += __popc(b);
+  }
+  __syncwarp();
+  for (int t = lane; t < n; t += 32) {
+    const unsigned long long ct = cand[t];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += cand[j] > ct;
+    if (rank < k) {
+      ids[rank] = topk_code_expert(ct);
+      // the key back from its code (a NaN stays a NaN, -0 becomes +0: same weights)
+      const uint32_t o = (uint32_t)(ct >> 32);
+      w[rank] = __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+    }
+  }
+  __syncwarp();
+  const int my_id = lane < k ? ids[lane] : -1;
+  const float my_key = lane < k ? w[lane] : 0.f;
+  __syncwarp();
+  topk_finish(lane, k, my_id, my_key, ids, w, nullptr, status);
+  __syncwarp();
 }
 
 // Top-k of one token by all threads of the CTA.  Codes (topk_code) order the
@@ -348,18 +424,16 @@ __device__ void topk_block(const float *keys, int E, int k, unsigned long long *
 
 // Phase timestamp for the trace of CTAs 0, G/2 and G-1 (thread 0).
 __device__ __forceinline__ void trace_at(const DecArgs &a, int slot) {
-  if (!a.trace || threadIdx.x != 0) return;
-  const int c = blockIdx.x, G = gridDim.x;
-  const int row = c == 0 ? 0 : (c == G / 2 ? 1 : (c == G - 1 ? 2 : -1));
-  if (row >= 0) a.trace[row * 16 + slot] = ptx::globaltimer();
+  if (!a.trace || threadIdx.x != 0 || blockIdx.x >= MOE_TRACE_CTAS) return;
+  a.trace[blockIdx.x * MOE_TRACE_SLOTS + slot] = ptx::globaltimer();
 }
 
-__global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_constant__ DecMaps mp,
-                                                                   const DecArgs a) {
+__global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_constant__ DecArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_ids[16];
   __shared__ float s_w[16];
   __shared__ float s_part[DWARPS];
+  __shared__ unsigned long long s_base;
   // 1024-byte aligned base for the swizzled code images (keeps the shared space)
   uint8_t *sm = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -368,7 +442,8 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   uint8_t *dc = sm + a.off_dc, *ru = sm + a.off_ru, *su = sm + a.off_su, *ds = sm + a.off_ds,
           *rus = sm + a.off_rus, *sus = sm + a.off_sus;
   float *rr = reinterpret_cast<float *>(sm + a.off_rr);
-  uint16_t *xs = reinterpret_cast<uint16_t *>(sm + a.off_x);
+  uint16_t *xs = reinterpret_cast<uint16_t *>(sm + a.off_x);   // x, permuted groups (GEMV operand)
+  uint16_t *xn = reinterpret_cast<uint16_t *>(sm + a.off_xn);  // x in natural order (router)
   uint16_t *hs = reinterpret_cast<uint16_t *>(sm + a.off_h);
   float *red = reinterpret_cast<float *>(sm + a.off_red);
   float *keys = reinterpret_cast<float *>(sm + a.off_keys);
@@ -380,209 +455,300 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   const int nru = (cta < a.n_ru) ? (a.n_ru - 1 - cta) / G + 1 : 0;  // routed gate/up units
   const int nou = (cta < a.n_ou) ? (a.n_ou - 1 - cta) / G + 1 : 0;  // output units
   const int upr = I / 8;
+  // copies are issued by the first two lanes of every warp: one warp alone issues slowly
+  const int issuer = lane < 2 ? warp * 2 + lane : -1;
+  const bool trace0 = a.trace != nullptr;
+  // phases of the launch's last layer (its first one has the prologue's copies)
+  auto trace = [&](int slot, int l) {
+    if (trace0 && l == a.nl - 1) trace_at(a, slot);
+  };
   trace_at(a, 0);
+
+  // Layer l's router rows and shared gate/up unit (bar_p1) and its shared
+  // expert's down rows (bar_dsh); each mbarrier completes once per layer, so
+  // layer l waits on parity l & 1.
+  auto issue_p1 = [&](int l) {
+    const LayerW &L = a.lw[l];
+    if (issuer >= 0) {
+      const int ngu = gu_ops(a), n1 = nsu * ngu, n2 = n1 + nre;
+      for (int o = issuer; o < n2; o += 2 * DWARPS) {
+        if (o < n1) {
+          const int i = o / ngu;
+          gu_op(a, L, a.maps[l], o % ngu, su + i * 8 * H, sus + i * H, E, (cta + i * G) * 8, bar_p1);
+        } else {
+          const int i = o - n1;
+          ptx::bulk_g2s(rr + i * H, L.router + (size_t)(rc + i * a.rp_ctas) * H, 4 * H, bar_p1);
+        }
+      }
+    }
+  };
+  auto issue_dsh = [&](int l) {
+    if (issuer >= 0 && S) {
+      const int ndn = dn_ops(a);
+      for (int o = issuer; o < nou * ndn; o += 2 * DWARPS) {
+        const int ol = o / ndn;
+        dn_op(a, a.lw[l], a.maps[l], o % ndn, dc + (ol * NS + k) * 4 * I, ds + (ol * NS + k) * (I / 2), E,
+              (cta + ol * G) * 8, bar_dsh);
+      }
+    }
+  };
+  const uint32_t p1_bytes = (uint32_t)(nsu * 9 * H + nre * 4 * H);
+  const uint32_t dsh_bytes = S ? (uint32_t)(nou * (4 * I + I / 2)) : 0u;
 
   if (tid == 0) {
     for (int i = 0; i < 3 + MAX_RU; ++i) ptx::mbar_init(&bars[i], 1);
     ptx::fence_mbar_init();
-    if (a.map3d) {
-      ptx::prefetch_tmap(&mp.gate);
-      ptx::prefetch_tmap(&mp.up);
-      ptx::prefetch_tmap(&mp.down);
-    }
-    expect_tx(bar_p1, (uint32_t)(nsu * 9 * H + nre * 4 * H));
-    expect_tx(bar_dsh, S ? (uint32_t)(nou * (4 * I + I / 2)) : 0u);
+    if (a.map3d)
+      for (int l = 0; l < a.nl; ++l) {
+        ptx::prefetch_tmap(&a.maps[l].gate);
+        ptx::prefetch_tmap(&a.maps[l].up);
+        ptx::prefetch_tmap(&a.maps[l].down);
+      }
+    expect_tx(bar_p1, p1_bytes);
+    expect_tx(bar_dsh, dsh_bytes);
   }
   __syncthreads();
-
   // ---------------------------------------------------------------- copies known at launch
-  // (issued by the first two lanes of every warp: one warp alone issues slowly)
-  const int issuer = lane < 2 ? warp * 2 + lane : -1;
-  if (issuer >= 0) {
-    const int ngu = gu_ops(a), ndn = dn_ops(a);
-    const int n1 = nsu * ngu, n2 = n1 + nre, n3 = n2 + (S ? nou * ndn : 0);
-    for (int o = issuer; o < n3; o += 2 * DWARPS) {
-      if (o < n1) {
-        const int i = o / ngu;
-        gu_op(a, mp, o % ngu, su + i * 8 * H, sus + i * H, E, (cta + i * G) * 8, bar_p1);
-      } else if (o < n2) {
-        const int i = o - n1;
-        ptx::bulk_g2s(rr + i * H, a.router + (size_t)(rc + i * a.rp_ctas) * H, 4 * H, bar_p1);
-      } else {
-        const int ol = (o - n2) / ndn;
-        dn_op(a, mp, (o - n2) % ndn, dc + (ol * NS + k) * 4 * I, ds + (ol * NS + k) * (I / 2), E,
-              (cta + ol * G) * 8, bar_dsh);
-      }
-    }
-  }
+  issue_p1(0);
+  issue_dsh(0);
   trace_at(a, 1);
-
-  // ---------------------------------------------------------------- P0: x (padded groups)
-  // The input (and the workspace) may still be written by the previous layer's
-  // launch when this one starts early: wait for it here, after the weight
-  // copies are on their way.
+  // The input (and the workspace) may still be written by the previous
+  // launch in the stream when this one starts early: wait for it here, after
+  // the weight copies are on their way.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ unsigned long long s_base;
   if (tid == 0) {  // a relaxed read: only the value matters, not ordering
     unsigned long long v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.bar) : "memory");
     s_base = v / (unsigned long long)G * (unsigned long long)G;
   }
-  // the residual of this CTA's output rows, read now rather than at the end
+  // the residual of this CTA's output rows: read once; later layers keep
+  // their own output, which is the next layer's residual
   float res_v = 0.f;
   if (tid < nou * 8) res_v = bf16_to_f32(a.res[(cta + (tid >> 3) * G) * 8 + (tid & 7)]);
-  if (a.prenorm) {
-    float ss = 0.f;
-    for (int i = tid; i < H; i += DTHREADS) {
-      const float v = bf16_to_f32(a.xin[i]);
-      ss = fmaf(v, v, ss);
+  bool ok = true;
+  uint32_t n_p1 = 1, n_dsh = 1, n_drt = 0;  // phases armed so far, for the drain on failure
+  int l = 0;
+  for (; l < a.nl; ++l) {
+    const LayerW &L = a.lw[l];
+    const uint32_t ph = (uint32_t)l & 1u;
+    const unsigned long long b0 = s_base + 3ull * (unsigned long long)l * (unsigned long long)G;
+    trace(2, l);
+    // this layer's tensor maps, for the copies issued after the routing
+    if (tid == 0 && a.map3d && l > 0) {
+      ptx::prefetch_tmap(&a.maps[l].gate);
+      ptx::prefetch_tmap(&a.maps[l].up);
+      ptx::prefetch_tmap(&a.maps[l].down);
     }
-    ss = warp_sum(ss);
-    if (lane == 0) s_part[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
+    // -------------------------------------------------------------- P0: x (padded groups)
+    if (a.prenorm) {
+      // r read once into registers (4 values a thread a round), RMS, scale
+      uint2 rv[XREG];
+      float ss = 0.f;
 #pragma unroll
-    for (int w = 0; w < DWARPS; ++w) tot += s_part[w];
-    const float scale = rsqrtf(tot / (float)H + a.eps);
-    for (int i = tid; i < H; i += DTHREADS)
-      xs[(i >> 6) * XPAD + (i & 63)] = f32_to_bf16(bf16_to_f32(a.xin[i]) * scale);
-  } else {
-    for (int i = tid; i < H / 8; i += DTHREADS)
-      *reinterpret_cast<uint4 *>(xs + (i >> 3) * XPAD + (i & 7) * 8) = reinterpret_cast<const uint4 *>(a.xin)[i];
-  }
-  __syncthreads();
-  trace_at(a, 2);
-
-  // ---------------------------------------------------------------- P1: shared gate/up, router rows
-  bool ok = wait_bar(bar_p1, a.status);
-  trace_at(a, 3);
-  if (ok && nsu > 0) ok = gu_compute(a, su, sus, nsu, nullptr, xs, red);
-  if (ok)
-    for (int i = warp; i < nre; i += DWARPS) {  // one warp per router row, fp32 FMA
-      const float *row = rr + i * H;
-      float acc = 0.f;
-      for (int kk = 4 * lane; kk < H; kk += 128) {
-        const float4 wv = *reinterpret_cast<const float4 *>(row + kk);
-        const uint2 xv = *reinterpret_cast<const uint2 *>(xs + (kk >> 6) * XPAD + (kk & 63));
-        acc = fmaf(__uint_as_float(xv.x << 16), wv.x, acc);
-        acc = fmaf(__uint_as_float(xv.x & 0xFFFF0000u), wv.y, acc);
-        acc = fmaf(__uint_as_float(xv.y << 16), wv.z, acc);
-        acc = fmaf(__uint_as_float(xv.y & 0xFFFF0000u), wv.w, acc);
+      for (int j = 0; j < XREG; ++j) {
+        const int i = tid + j * DTHREADS;
+        rv[j] = i < H / 4 ? __ldcg(reinterpret_cast<const uint2 *>(a.xin) + i) : make_uint2(0u, 0u);
+        const float v0 = __uint_as_float(rv[j].x << 16), v1 = __uint_as_float(rv[j].x & 0xFFFF0000u);
+        const float v2 = __uint_as_float(rv[j].y << 16), v3 = __uint_as_float(rv[j].y & 0xFFFF0000u);
+        ss = fmaf(v0, v0, ss);
+        ss = fmaf(v1, v1, ss);
+        ss = fmaf(v2, v2, ss);
+        ss = fmaf(v3, v3, ss);
       }
-      acc = warp_sum(acc);
-      const int e = rc + i * a.rp_ctas;
-      if (lane == 0) a.keys[e] = a.bias ? acc + a.bias[e] : acc;
-    }
-  ok = __syncthreads_and(ok) != 0;  // every flag below stays uniform across the CTA
-  if (ok && nsu > 0) gu_finish(a, nsu, red, [&](int u) { return (size_t)k * I + (size_t)(cta + u * G) * 8; });
-  trace_at(a, 4);
-  ok = grid_sync(a.bar, s_base + (unsigned long long)G, a.status) && ok;
-  trace_at(a, 5);
-
-  // ---------------------------------------------------------------- P2: routing, routed gate/up
-  bool issued2 = false;
-  if (ok) {
-    for (int e = tid; e < E; e += DTHREADS) keys[e] = __ldcg(a.keys + e);
-    __syncthreads();
-    trace_at(a, 6);
-    topk_block(keys, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand),
-               reinterpret_cast<unsigned long long *>(sm + a.off_gmax), s_ids, s_w, a.status);
-    __syncthreads();
-    trace_at(a, 14);
-    if (cta == 0 && tid < k) {
-      a.topk_id[tid] = s_ids[tid];
-      a.topk_w[tid] = s_w[tid];
-    }
-    if (tid == 0) {
-      for (int i = 0; i < nru; ++i) expect_tx(&bar_ru[i], (uint32_t)(9 * H));
-      expect_tx(bar_drt, (uint32_t)(nou * k * (4 * I + I / 2)));
-    }
-    __syncthreads();
-    if (issuer >= 0) {
-      const int ngu = gu_ops(a), ndn = dn_ops(a);
-      const int n1 = nru * ngu, n2 = n1 + nou * k * ndn;
-      for (int o = issuer; o < n2; o += 2 * DWARPS) {
-        if (o < n1) {
-          const int i = o / ngu, u = cta + i * G;
-          gu_op(a, mp, o % ngu, ru + i * 8 * H, rus + i * H, s_ids[u / upr], (u % upr) * 8, &bar_ru[i]);
-        } else {
-          const int b = (o - n1) / ndn, ol = b / k, j = b % k;
-          dn_op(a, mp, (o - n1) % ndn, dc + (ol * NS + j) * 4 * I, ds + (ol * NS + j) * (I / 2), s_ids[j],
-                (cta + ol * G) * 8, bar_drt);
+      ss = warp_sum(ss);
+      if (lane == 0) s_part[warp] = ss;
+      __syncthreads();
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < DWARPS; ++w) tot += s_part[w];
+      const float scale = rsqrtf(tot / (float)H + a.eps);
+#pragma unroll
+      for (int j = 0; j < XREG; ++j) {
+        const int i = tid + j * DTHREADS;  // H / 4 is a multiple of 32: whole warps take this branch
+        if (i < H / 4) {
+          const uint32_t y0 = f32_to_bf16(__uint_as_float(rv[j].x << 16) * scale);
+          const uint32_t y1 = f32_to_bf16(__uint_as_float(rv[j].x & 0xFFFF0000u) * scale);
+          const uint32_t y2 = f32_to_bf16(__uint_as_float(rv[j].y << 16) * scale);
+          const uint32_t y3 = f32_to_bf16(__uint_as_float(rv[j].y & 0xFFFF0000u) * scale);
+          const uint32_t lo = y0 | (y1 << 16), hi = y2 | (y3 << 16);
+          reinterpret_cast<uint2 *>(xn)[i] = make_uint2(lo, hi);
+          // lanes 2c and 2c+1 hold the halves of word c: swap one register
+          const bool odd = (lane & 1) != 0;
+          const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+          const uint4 pw = odd ? perm8(got, got, lo, hi) : perm8(lo, hi, got, got);
+          *reinterpret_cast<uint2 *>(xs + (i >> 4) * XPAD + (i & 15) * 4) =
+              odd ? make_uint2(pw.z, pw.w) : make_uint2(pw.x, pw.y);
         }
       }
-    }
-    issued2 = true;
-    trace_at(a, 7);
-    const bool ok2 = __syncthreads_and(gu_compute(a, ru, rus, nru, bar_ru, xs, red)) != 0;
-    trace_at(a, 8);
-    if (ok2 && nru > 0)
-      gu_finish(a, nru, red, [&](int u) {
-        const int uu = cta + u * G;
-        return (size_t)(uu / upr) * I + (size_t)(uu % upr) * 8;
-      });
-    ok = ok && ok2;
-  }
-  trace_at(a, 9);
-  ok = grid_sync(a.bar, s_base + 2ull * (unsigned long long)G, a.status) && ok;
-  trace_at(a, 10);
-
-  // ---------------------------------------------------------------- P3: down + combine
-  // let the next launch in the stream start its prologue and weight copies
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (ok) ok = __syncthreads_and(wait_bar(bar_dsh, a.status) && wait_bar(bar_drt, a.status)) != 0;
-  if (ok) {
-    const int nv = NS * I / 8;  // h of every slot, 16 bytes per load, into padded groups
-    for (int i = tid; i < nv; i += DTHREADS) {
-      const int j = i / (I / 8), c8 = i % (I / 8);
-      *reinterpret_cast<uint4 *>(hs + (j * (I / 64) + (c8 >> 3)) * XPAD + (c8 & 7) * 8) =
-          __ldcg(reinterpret_cast<const uint4 *>(a.hbuf) + i);
-    }
-    __syncthreads();
-    trace_at(a, 11);
-    const int nkcd = I / KCH, gpr = I / 64, g = lane >> 2, q = lane & 3;
-    const int nitem = nou * NS * nkcd;
-    for (int t = warp; t < nitem; t += DWARPS) {
-      const int kc = t % nkcd, j = (t / nkcd) % NS, ol = t / (nkcd * NS);
-      uint32_t xr[32];
-      load_group(hs + j * (I / 64) * XPAD, 4 * kc + q, xr);
-      const uint16_t *sc = reinterpret_cast<const uint16_t *>(ds + (ol * NS + j) * (I / 2));
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, sc, sc + 8 * gpr, gpr, 4 * kc + q, xr, g, q, d);
-      if (g == 0) {
-        red[t * 8 + 2 * q] = d[0];
-        red[t * 8 + 2 * q + 1] = d[1];
+    } else {
+      for (int i = tid; i < H / 8; i += DTHREADS) {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.xin) + i);
+        reinterpret_cast<uint4 *>(xn)[i] = v;
+        *reinterpret_cast<uint4 *>(xs + (i >> 3) * XPAD + (i & 7) * 8) = perm8(v.x, v.y, v.z, v.w);
       }
     }
     __syncthreads();
-    trace_at(a, 12);
-    // y_j = bf16(h_j . Wd_j) of every (row, slot) in parallel, then the combine
-    float *ys = reinterpret_cast<float *>(sm + a.off_ys);  // [nou * 8][NS]
-    for (int t = tid; t < nou * 8 * NS; t += DTHREADS) {
-      const int ol = t / (8 * NS), r = (t / NS) & 7, j = t % NS;
-      float v = 0.f;
-      for (int kc = 0; kc < nkcd; ++kc) v += red[((ol * NS + j) * nkcd + kc) * 8 + r];
-      ys[t] = bf16_to_f32(f32_to_bf16(v));
+    trace(3, l);
+
+    // -------------------------------------------------------------- P1: router rows, shared gate/up
+    if (ok) ok = wait_bar(bar_p1, ph, a.status);
+    trace(4, l);
+    if (ok)
+      for (int i = warp; i < nre; i += DWARPS) {  // one warp per router row, fp32 FMA
+        const float *row = rr + i * H;
+        float acc = 0.f;
+        for (int kk = 4 * lane; kk < H; kk += 128) {
+          const float4 wv = *reinterpret_cast<const float4 *>(row + kk);
+          const uint2 xv = *reinterpret_cast<const uint2 *>(xn + kk);
+          acc = fmaf(__uint_as_float(xv.x << 16), wv.x, acc);
+          acc = fmaf(__uint_as_float(xv.x & 0xFFFF0000u), wv.y, acc);
+          acc = fmaf(__uint_as_float(xv.y << 16), wv.z, acc);
+          acc = fmaf(__uint_as_float(xv.y & 0xFFFF0000u), wv.w, acc);
+        }
+        acc = warp_sum(acc);
+        const int e = rc + i * a.rp_ctas;
+        if (lane == 0) a.keys[e] = L.bias ? acc + L.bias[e] : acc;
+      }
+    // The keys are all the barrier publishes; the shared expert's h goes out
+    // with the next barrier, so its units are computed while this one settles.
+    grid_arrive(a.bar);
+    trace(5, l);
+    if (ok && nsu > 0) ok = gu_compute(a, su, sus, nsu, nullptr, 0u, xs, red);
+    ok = __syncthreads_and(ok) != 0;  // every flag below stays uniform across the CTA
+    if (ok && nsu > 0) gu_finish(a, nsu, red, [&](int u) { return (size_t)k * I + (size_t)(cta + u * G) * 8; });
+    trace(6, l);
+    ok = grid_wait(a.bar, b0 + (unsigned long long)G, a.status) && ok;
+    trace(7, l);
+    // the next layer's router rows and shared unit, into the buffers P1 has
+    // finished with (read by this CTA's generic loads, written by TMA next)
+    if (ok && l + 1 < a.nl) {
+      ptx::fence_proxy_async_smem();
+      if (tid == 0) expect_tx(bar_p1, p1_bytes);
+      __syncthreads();
+      issue_p1(l + 1);
+      n_p1 = l + 2;
     }
-    __syncthreads();
-    if (tid < nou * 8) {
-      const float *yr = ys + tid * NS;
-      float o = res_v;
-      if (S) o += yr[k];
-      for (int j = 0; j < k; ++j) o = fmaf(s_w[j], yr[j], o);
-      a.out[(cta + (tid >> 3) * G) * 8 + (tid & 7)] = f32_to_bf16(o);
+
+    // -------------------------------------------------------------- P2: routing, routed gate/up
+    if (ok) {
+      if (E <= 256) {
+        if (warp == 0) topk_warp(a.keys, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand), s_ids, s_w,
+                                 a.status);
+      } else {
+        for (int e = tid; e < E; e += DTHREADS) keys[e] = __ldcg(a.keys + e);
+        __syncthreads();
+        topk_block(keys, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand),
+                   reinterpret_cast<unsigned long long *>(sm + a.off_gmax), s_ids, s_w, a.status);
+      }
+      ptx::fence_proxy_async_smem();  // the routed buffers were last read by generic loads
+      if (tid == 0) {
+        for (int i = 0; i < nru; ++i) expect_tx(&bar_ru[i], (uint32_t)(9 * H));
+        expect_tx(bar_drt, (uint32_t)(nou * k * (4 * I + I / 2)));
+      }
+      __syncthreads();
+      trace(8, l);
+      if (cta == 0 && tid < k) {
+        a.topk_id[tid] = s_ids[tid];
+        a.topk_w[tid] = s_w[tid];
+      }
+      n_drt = l + 1;
+      if (issuer >= 0) {
+        const int ngu = gu_ops(a), ndn = dn_ops(a);
+        const int n1 = nru * ngu, n2 = n1 + nou * k * ndn;
+        for (int o = issuer; o < n2; o += 2 * DWARPS) {
+          if (o < n1) {
+            const int i = o / ngu, u = cta + i * G;
+            gu_op(a, L, a.maps[l], o % ngu, ru + i * 8 * H, rus + i * H, s_ids[u / upr], (u % upr) * 8,
+                  &bar_ru[i]);
+          } else {
+            const int b = (o - n1) / ndn, ol = b / k, j = b % k;
+            dn_op(a, L, a.maps[l], (o - n1) % ndn, dc + (ol * NS + j) * 4 * I, ds + (ol * NS + j) * (I / 2),
+                  s_ids[j], (cta + ol * G) * 8, bar_drt);
+          }
+        }
+      }
+      trace(9, l);
+      const bool ok2 = __syncthreads_and(gu_compute(a, ru, rus, nru, bar_ru, ph, xs, red)) != 0;
+      trace(10, l);
+      if (ok2 && nru > 0)
+        gu_finish(a, nru, red, [&](int u) {
+          const int uu = cta + u * G;
+          return (size_t)(uu / upr) * I + (size_t)(uu % upr) * 8;
+        });
+      ok = ok && ok2;
     }
+    trace(11, l);
+    ok = grid_sync(a.bar, b0 + 2ull * (unsigned long long)G, a.status) && ok;
+    trace(12, l);
+
+    // -------------------------------------------------------------- P3: down + combine
+    // let the next launch in the stream start its prologue and weight copies
+    if (l + 1 == a.nl) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (ok) {
+      const int nv = NS * I / 8;  // h of every slot, 16 bytes per load, into padded groups
+      for (int i = tid; i < nv; i += DTHREADS) {
+        const int j = i / (I / 8), c8 = i % (I / 8);
+        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.hbuf) + i);
+        *reinterpret_cast<uint4 *>(hs + (j * (I / 64) + (c8 >> 3)) * XPAD + (c8 & 7) * 8) = perm8(v.x, v.y, v.z, v.w);
+      }
+      trace(13, l);
+      ok = __syncthreads_and(wait_bar(bar_dsh, ph, a.status) && wait_bar(bar_drt, ph, a.status)) != 0;
+      trace(14, l);
+    }
+    if (ok) {
+      const int nkcd = I / KCH, gpr = I / 64, g = lane >> 2, q = lane & 3;
+      const int nitem = nou * NS * nkcd;
+      for (int t = warp; t < nitem; t += DWARPS) {
+        const int kc = t % nkcd, j = (t / nkcd) % NS, ol = t / (nkcd * NS);
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(ds + (ol * NS + j) * (I / 2));
+        const float d = gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, sc, sc + 8 * gpr, gpr, 4 * kc + q,
+                                   hs + (j * (I / 64) + 4 * kc) * XPAD, g, q);
+        if (q == 0) red[t * 8 + g] = d;
+      }
+      __syncthreads();
+      trace(15, l);
+      // the next layer's shared down rows, into the slots just read
+      if (l + 1 < a.nl) {
+        ptx::fence_proxy_async_smem();
+        if (tid == 0) expect_tx(bar_dsh, dsh_bytes);
+        __syncthreads();
+        issue_dsh(l + 1);
+        n_dsh = l + 2;
+      }
+      // y_j = bf16(h_j . Wd_j) of every (row, slot) in parallel, then the combine
+      float *ys = reinterpret_cast<float *>(sm + a.off_ys);  // [nou * 8][NS]
+      for (int t = tid; t < nou * 8 * NS; t += DTHREADS) {
+        const int ol = t / (8 * NS), r = (t / NS) & 7, j = t % NS;
+        float v = 0.f;
+        for (int kc = 0; kc < nkcd; ++kc) v += red[((ol * NS + j) * nkcd + kc) * 8 + r];
+        ys[t] = bf16_to_f32(f32_to_bf16(v));
+      }
+      __syncthreads();
+      if (tid < nou * 8) {
+        const float *yr = ys + tid * NS;
+        float o = res_v;
+        if (S) o += yr[k];
+        for (int j = 0; j < k; ++j) o = fmaf(s_w[j], yr[j], o);
+        const uint16_t ob = f32_to_bf16(o);
+        a.out[(cta + (tid >> 3) * G) * 8 + (tid & 7)] = ob;
+        res_v = bf16_to_f32(ob);  // the next layer's residual for this row
+      }
+      trace(16, l);
+    }
+    if (l + 1 < a.nl) ok = grid_sync(a.bar, b0 + 3ull * (unsigned long long)G, a.status) && ok;
+    trace(17, l);
   }
   // never leave with copies in flight into this CTA's shared memory
+  // (a phase that has completed passes at once)
   if (tid == 0 && !ok) {
-    wait_bar(bar_p1, a.status);
-    wait_bar(bar_dsh, a.status);
-    if (issued2) {
-      wait_bar(bar_drt, a.status);
-      for (int i = 0; i < nru; ++i) wait_bar(&bar_ru[i], a.status);
+    wait_bar(bar_p1, (n_p1 - 1) & 1u, a.status);
+    wait_bar(bar_dsh, (n_dsh - 1) & 1u, a.status);
+    if (n_drt > 0) {
+      wait_bar(bar_drt, (n_drt - 1) & 1u, a.status);
+      for (int i = 0; i < nru; ++i) wait_bar(&bar_ru[i], (n_drt - 1) & 1u, a.status);
     }
   }
-  trace_at(a, 13);
+  trace_at(a, MOE_TRACE_SLOTS - 1);
 }
 
 struct DecPlan {
@@ -621,6 +787,8 @@ DecPlan make_plan(int H, int E, int k, int I, int S, int num_sms) {
   o = al(o + max_re * 4 * H, 128);
   a.off_x = o;
   o = al(o + (H / 64) * XPAD * 2, 128);
+  a.off_xn = o;
+  o = al(o + H * 2, 128);
   a.off_h = o;
   o = al(o + NS * (I / 64) * XPAD * 2, 128);
   a.off_ds = o;
@@ -702,7 +870,9 @@ cudaError_t make_maps(DecMaps *m, const ExpertPtrs &w, int H, int E, int I, int 
 
 bool decode_supported(int H, int E, int k, int I, int S, int num_sms) {
   auto pow2 = [](int v) { return v > 0 && (v & (v - 1)) == 0; };
-  if (!pow2(H) || !pow2(I) || H < KCH || I < KCH || num_sms <= 0 || k > 16 || E > 1024) return false;
+  if (!pow2(H) || !pow2(I) || H < KCH || I < KCH || H > 4 * XREG * DTHREADS || num_sms <= 0 || k > 16 ||
+      E > 1024)
+    return false;
   DecPlan p = make_plan(H, E, k, I, S, num_sms);
   return p.max_ru <= MAX_RU && p.smem <= decode_smem_limit();
 }
@@ -717,18 +887,19 @@ cudaError_t decode_prepare(int H, int E, int k, int I, int S, int num_sms) {
   return cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
 }
 
-cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, int k, int I, int S, int prenorm,
-                          float eps, const float *router, const float *bias, ExpertPtrs w, float *keys,
-                          int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf, uint16_t *out,
-                          int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s) {
+namespace {
+
+// One cooperative launch of layers [0, nl) of lw (nl <= MAXL).
+cudaError_t launch_layers(const uint16_t *x, const uint16_t *res, uint16_t *out, int H, int E, int k, int I, int S,
+                          int prenorm, float eps, const LayerW *lw, int nl, float *keys, int32_t *topk_id,
+                          float *topk_w, unsigned long long *bar, uint16_t *hbuf, int32_t *status, uint64_t *trace,
+                          int num_sms, cudaStream_t s) {
   DecPlan p = make_plan(H, E, k, I, S, num_sms);
   DecArgs &a = p.a;
+  a.nl = nl;
   a.xin = x;
   a.res = res;
   a.out = out;
-  a.router = router;
-  a.bias = bias;
-  a.w = w;
   a.keys = keys;
   a.topk_id = topk_id;
   a.topk_w = topk_w;
@@ -738,12 +909,15 @@ cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, 
   a.trace = trace;
   a.prenorm = prenorm;
   a.eps = eps;
-  DecMaps maps;
   a.map3d = 1;
-  cudaError_t e = make_maps(&maps, w, H, E, I, S, true);
-  if (e != cudaSuccess) {  // the driver refused the 3-D view: one 2-D box per K-chunk
-    a.map3d = 0;
-    if ((e = make_maps(&maps, w, H, E, I, S, false)) != cudaSuccess) return e;
+  for (int l = 0; l < nl; ++l) {
+    a.lw[l] = lw[l];
+    cudaError_t e = make_maps(&a.maps[l], lw[l].w, H, E, I, S, a.map3d != 0);
+    if (e != cudaSuccess && l == 0) {  // the driver refused the 3-D view: one 2-D box per K-chunk
+      a.map3d = 0;
+      e = make_maps(&a.maps[l], lw[l].w, H, E, I, S, false);
+    }
+    if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
@@ -763,15 +937,43 @@ cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   prof_before(MOE_KERNEL_DECODE_LAYER, s);
-  e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, maps, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, maps, a);
+    e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
   }
   prof_after(MOE_KERNEL_DECODE_LAYER, s);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, int k, int I, int S, int prenorm,
+                          float eps, const float *router, const float *bias, ExpertPtrs w, float *keys,
+                          int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf, uint16_t *out,
+                          int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s) {
+  const LayerW lw{router, bias, w};
+  const cudaError_t e = launch_layers(x, res, out, H, E, k, I, S, prenorm, eps, &lw, 1, keys, topk_id, topk_w, bar,
+                                      hbuf, status, trace, num_sms, s);
   if (e != cudaSuccess) return e;
   *launches += 1;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_stack(uint16_t *r, int n_layers, int H, int E, int k, int I, int S, float eps,
+                                const float *const *router, const float *const *bias, const ExpertPtrs *w,
+                                float *keys, int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf,
+                                int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s) {
+  for (int l0 = 0; l0 < n_layers; l0 += MAXL) {
+    const int nl = n_layers - l0 < MAXL ? n_layers - l0 : MAXL;
+    LayerW lw[MAXL];
+    for (int l = 0; l < nl; ++l) lw[l] = LayerW{router[l0 + l], bias ? bias[l0 + l] : nullptr, w[l0 + l]};
+    const cudaError_t e = launch_layers(r, r, r, H, E, k, I, S, 1, eps, lw, nl, keys, topk_id, topk_w, bar, hbuf,
+                                        status, l0 == 0 ? trace : nullptr, num_sms, s);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+  }
   return cudaSuccess;
 }
 

@@ -51,5 +51,11 @@ cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, 
                           float eps, const float *router, const float *bias, ExpertPtrs w, float *keys,
                           int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf, uint16_t *out,
                           int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s);
+// n_layers pre-norm layers on one token, r updated in place: r += MoE_l(RMSNorm(r));
+// router/bias/w: host arrays of n_layers (bias may be null, or hold nulls).
+cudaError_t launch_decode_stack(uint16_t *r, int n_layers, int H, int E, int k, int I, int S, float eps,
+                                const float *const *router, const float *const *bias, const ExpertPtrs *w,
+                                float *keys, int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf,
+                                int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s);
 
 }  // namespace moe

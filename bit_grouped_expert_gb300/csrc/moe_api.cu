@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <new>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -56,7 +57,7 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles) {
   L.y = take((k + S) * T * H * 2);
   L.rsplit = take(3 * E * H * 2);
   L.xn = take(T * H * 2);  // normalised x of pre-norm plans
-  L.trace = take(3 * 16 * 8);
+  L.trace = take(MOE_TRACE_CTAS * MOE_TRACE_SLOTS * 8);
   L.total = o;
   return L;
 }
@@ -384,6 +385,39 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
   ++launches;
   g_last_launches = launches;
   return MOE_OK;
+}
+
+moe_status moe_decode_stack(const moe_plan_t *plan, void *r_d, int32_t n_layers, const moe_weights *w,
+                            const float *const *logit_bias_d, void *ws_d, size_t ws_bytes, void *stream) {
+  g_last_launches = 0;
+  moe_status st = check_call(plan, 1, ws_d, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!r_d || !w || n_layers < 1) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(r_d)) return MOE_ERR_MISALIGNED;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!weights_present(&w[l])) return MOE_ERR_INVALID_ARGUMENT;
+    if (!weights_aligned(&w[l]) || (logit_bias_d && !moe::aligned16(logit_bias_d[l]))) return MOE_ERR_MISALIGNED;
+  }
+  if ((st = device_ready(plan)) != MOE_OK) return st;
+  if (!plan->use_decode) return MOE_ERR_UNSUPPORTED;
+  const moe_config &c = plan->cfg;
+  const moe::Layout &L = plan->lay;
+  std::vector<const float *> router(n_layers);
+  std::vector<moe::ExpertPtrs> ep(n_layers);
+  for (int l = 0; l < n_layers; ++l) {
+    router[l] = w[l].router_d;
+    ep[l] = expert_ptrs(&w[l]);
+  }
+  int launches = 0;
+  const cudaError_t err = moe::launch_decode_stack(
+      static_cast<uint16_t *>(r_d), n_layers, c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, 1e-6f,
+      router.data(), logit_bias_d, ep.data(), moe::ws_ptr<float>(ws_d, L.keys), moe::ws_ptr<int32_t>(ws_d, L.topk_id),
+      moe::ws_ptr<float>(ws_d, L.topk_w), moe::ws_ptr<unsigned long long>(ws_d, L.counter),
+      moe::ws_ptr<uint16_t>(ws_d, L.h), moe::ws_ptr<int32_t>(ws_d, L.status),
+      (plan->flags & MOE_FLAG_TRACE) ? moe::ws_ptr<uint64_t>(ws_d, L.trace) : nullptr, plan->num_sms, &launches,
+      static_cast<cudaStream_t>(stream));
+  g_last_launches = launches;
+  return cuda_status(err);
 }
 
 moe_status moe_route_view(const moe_plan_t *plan, void *ws_d, int32_t T, moe_route_ptrs *out) {

@@ -97,7 +97,7 @@ typedef struct {
   uint16_t *h_d;       /* [(k+S)*T][I] bf16 SwiGLU rows (routed in perm order, then shared) */
   uint16_t *y_d;       /* [(k+S)*T][H] bf16 expert outputs, same row order    */
   int32_t *status_d;   /* [1] sticky device status (moe_status values)        */
-  uint64_t *trace_d;   /* [3][16] phase timestamps (ns) of MOE_FLAG_TRACE plans */
+  uint64_t *trace_d;   /* [MOE_TRACE_CTAS][MOE_TRACE_SLOTS] phase timestamps (ns), MOE_FLAG_TRACE */
   int32_t max_tiles;   /* capacity of blockmap_d                             */
   int32_t block_rows;  /* rows per block-map tile for this plan              */
 } moe_route_ptrs;
@@ -107,8 +107,11 @@ typedef struct {
 #define MOE_FLAG_FORCE_GROUPED  0x2u  /* T == 1 runs the grouped path instead of the decode path */
 #define MOE_FLAG_SIMT_EXPERTS   0x4u  /* CUDA-core grouped GEMMs instead of the tensor-core ones */
 #define MOE_FLAG_TILE_ROWS_64   0x8u  /* tensor-core path: 64-token tiles instead of 128 */
-#define MOE_FLAG_TRACE          0x20u /* decode layer: record %globaltimer at each phase of CTAs 0,
-                                         G/2 and G-1 into moe_route_ptrs.trace_d (tracing aid) */
+#define MOE_FLAG_TRACE          0x20u /* decode kernel: record %globaltimer at each phase of the
+                                         last layer of a launch, per CTA, into moe_route_ptrs.trace_d
+                                         (tracing aid) */
+#define MOE_TRACE_CTAS 256             /* CTAs with a row in the trace buffer */
+#define MOE_TRACE_SLOTS 32             /* timestamps in a row */
 #define MOE_FLAG_PRENORM        0x10u /* pre-norm block: x_d is the residual stream r, the layer
                                          computes x = RMSNorm(r) (unit gain, eps 1e-6) and
                                          out = r + MoE(x); residual_d must be NULL and out_d
@@ -156,6 +159,22 @@ moe_status moe_route_from_logits(const moe_plan_t *plan, const float *keys_d, in
 moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *residual_d, int32_t T,
                        const moe_weights *w, const float *logit_bias_d, void *out_d, void *ws_d,
                        size_t ws_bytes, void *stream);
+
+/* Single-token decode through a stack of n_layers pre-norm MoE layers (the
+ * pages' model stacks 40 of them; "Decode" section: at batch 1 bandwidth
+ * bounds the step):  for l = 0 .. n_layers-1,  r = r + MoE_l(RMSNorm(r)),
+ * each layer routed on its own fp32 keys, RMSNorm as in moe_rmsnorm.  The same
+ * arithmetic as n_layers moe_forward calls of a MOE_FLAG_PRENORM plan at
+ * T == 1, run as ceil(n_layers / 7) cooperative launches that fetch each
+ * layer's router and shared-expert weights during the previous layer.
+ *   r_d           bf16 [H] residual stream, updated in place (device)
+ *   w             host array of n_layers moe_weights (device pointers)
+ *   logit_bias_d  host array of n_layers device pointers (entries may be
+ *                 NULL), or NULL
+ * The workspace keeps the last layer's keys and top-k.  Errors: as
+ * moe_forward; MOE_ERR_UNSUPPORTED when the plan's shape has no decode path. */
+moe_status moe_decode_stack(const moe_plan_t *plan, void *r_d, int32_t n_layers, const moe_weights *w,
+                            const float *const *logit_bias_d, void *ws_d, size_t ws_bytes, void *stream);
 
 /* Device pointers of the workspace's routing buffers for T tokens (host-side
  * arithmetic only; nothing is read or enqueued). */

@@ -118,6 +118,32 @@ def test_forward_argument_errors_enqueue_nothing(lib):
     assert moe.moe_last_launch_count() == 0
 
 
+def test_decode_stack_argument_errors(lib):
+    plan = moe.moe_plan(moe.make_config(), 1)
+    need = moe.moe_workspace_bytes(plan)
+    ws = _FakeTensor(0x10000000, need)
+    W = {n: 0x30000000 + i * 0x100000 for i, n in enumerate(
+        ("router", "gate_q", "up_q", "gate_s", "gate_b", "up_s", "up_b", "down_q", "down_s", "down_b"))}
+
+    def status_of(r=0x20000000, Ws=(W, W), bias=None, w=ws):
+        try:
+            moe.moe_decode_stack(plan, r, list(Ws), bias, w, stream=0)
+        except moe.MoeError as e:
+            return e.status
+        return moe.MOE_OK
+
+    assert status_of(Ws=()) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert status_of(r=None) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert status_of(r=0x20000008) == moe.MOE_ERR_MISALIGNED
+    assert status_of(Ws=(W, {**W, "gate_b": None})) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert status_of(Ws=({**W, "down_s": W["down_s"] + 4}, W)) == moe.MOE_ERR_MISALIGNED
+    assert status_of(bias=[None, 0x50000004]) == moe.MOE_ERR_MISALIGNED
+    assert status_of(w=_FakeTensor(0x10000000, need - 1)) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(ValueError):
+        moe.moe_decode_stack(plan, 0x20000000, [W, W], [None], ws, stream=0)
+    assert moe.moe_last_launch_count() == 0
+
+
 def test_route_and_view_argument_errors(lib):
     plan = moe.moe_plan(moe.make_config(), 64)
     need = moe.moe_workspace_bytes(plan)

@@ -320,6 +320,107 @@ def test_decode_real_dims_prenorm_and_deterministic(real):
     assert L.status() == 0
 
 
+@pytest.mark.parametrize("E,k", [(512, 8), (40, 16)])
+def test_decode_expert_counts(E, k):
+    # E > 256: the CTA-wide selection; E=40, k=16: half of the warp's lanes
+    # hold two keys and the k-th lane maximum sits among them
+    d, W, Wd = _tiny(30 + E, E=E, k=k)
+    x = syn.activations(30 + E, 1, d["H"])
+    res = syn.activations(30 + E, 1, d["H"], tensor=syn.T_RESID)
+    L = Layer(H=d["H"], E=E, k=k, I=d["I"], max_tokens=1)
+    out = _forward(L, x, Wd, res=res)
+    r = L.routing(1)
+    ids, w = orc.select(r["keys"], k)
+    np.testing.assert_array_equal(r["ids"], ids)
+    np.testing.assert_allclose(r["w"], w, rtol=2e-6, atol=1e-7)
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, res=res, keys=r["keys"], intermediates=True)
+    assert_outputs_close(out, ref, f"decode E={E} k={k}", k=k)
+    assert L.status() == 0
+
+
+def test_decode_tied_keys_take_the_lower_expert(real):
+    # router rows repeated in pairs: every key ties with its neighbour's
+    W, _ = real
+    W2 = dict(W)
+    W2["router"] = np.repeat(W["router"][::2], 2, axis=0)
+    Wd = dev_weights(W2)
+    x = syn.activations(123, 1, 2048)
+    L = Layer(max_tokens=1)
+    out = _forward(L, x, Wd)
+    r = L.routing(1)
+    assert np.all(r["keys"][0, ::2] == r["keys"][0, 1::2])
+    ids, w = orc.select(r["keys"], 8)
+    np.testing.assert_array_equal(r["ids"], ids)
+    assert set(ids[0, 0::2] % 2) == {0} and set(ids[0, 1::2] % 2) == {1}  # pairs, lower index first
+    ref = orc.moe_layer(orc.Dims(), x, W2, keys=r["keys"], intermediates=True)
+    assert_outputs_close(out, ref, "decode tied keys")
+
+
+def _stack_vs_layers(d, Ws, biases, r):
+    """moe_decode_stack over the layers against one PRENORM moe_forward per
+    layer; returns (stack result, per-layer inputs of the sequential run, the
+    plan used by the stack)."""
+    L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=1, flags=moe.MOE_FLAG_PRENORM)
+    Wds = [dev_weights(W) for W in Ws]
+    bds = [None if b is None else dev(b) for b in biases]
+    seq = dev(r)
+    inputs = []
+    for Wd, b in zip(Wds, bds):
+        inputs.append(host_u16(seq))
+        moe.moe_forward(L.plan, seq, None, 1, Wd, b, seq, L.ws)
+    torch.cuda.synchronize()
+    Ls = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=1)
+    rs = dev(r)
+    moe.moe_decode_stack(Ls.plan, rs, Wds, bds if any(b is not None for b in biases) else None, Ls.ws)
+    launches = moe.moe_last_launch_count()
+    torch.cuda.synchronize()
+    assert L.status() == 0 and Ls.status() == 0
+    np.testing.assert_array_equal(host_u16(rs), host_u16(seq))
+    return host_u16(rs), inputs, Ls, launches
+
+
+def test_decode_stack_real_dims_matches_layer_by_layer(real):
+    # three distinct layers at the model's dims: one launch, bit-identical to
+    # three single-layer calls; the last layer also against the oracle
+    W0, _ = real
+    Ws = [W0]
+    for seed in (1, 2):
+        W = syn.experts(seed, 257, 2048, 512)
+        W["router"] = syn.router(seed, 256, 2048)
+        Ws.append(W)
+    biases = [None, syn.zipf_bias(5, 256), None]
+    r = syn.activations(88, 1, 2048, tensor=syn.T_RESID)
+    out, inputs, Ls, launches = _stack_vs_layers(dict(H=2048, E=256, k=8, I=512), Ws, biases, r)
+    assert launches == 1
+    r_last = inputs[-1]
+    keys = Ls.routing(1)["keys"]
+    ref = orc.moe_layer(orc.Dims(), orc.rmsnorm(r_last, 1e-6), Ws[-1], res=r_last, keys=keys, intermediates=True)
+    assert_outputs_close(out, ref, "stack layer 3")
+
+
+def test_decode_stack_tiny_dims_spans_launches():
+    # nine layers at tiny dims: more layers than one launch carries
+    Ws, biases = [], []
+    for l in range(9):
+        d, W, _ = _tiny(200 + l)
+        Ws.append(W)
+        biases.append(syn.zipf_bias(200 + l, d["E"]) if l % 3 == 1 else None)
+    r = syn.activations(90, 1, d["H"], tensor=syn.T_RESID)
+    out, inputs, Ls, launches = _stack_vs_layers(d, Ws, biases, r)
+    assert launches == 2
+    keys = Ls.routing(1)["keys"]
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), orc.rmsnorm(inputs[-1], 1e-6), Ws[-1], res=inputs[-1],
+                        keys=keys, intermediates=True)
+    assert_outputs_close(out, ref, "stack layer 9", k=d["k"])
+
+
+def test_decode_stack_single_layer(real):
+    W, _ = real
+    r = syn.activations(91, 1, 2048, tensor=syn.T_RESID)
+    _, _, _, launches = _stack_vs_layers(dict(H=2048, E=256, k=8, I=512), [W], [None], r)
+    assert launches == 1
+
+
 # ---------------------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("T", [1, 40])
