@@ -11,7 +11,9 @@ namespace moe {
 // ----------------------------------------------------------------- plan
 
 struct Layout {
-  size_t status, counter, keys, topk_id, topk_w, counts, offsets, perm, inv, blockmap, n_tiles, h, y, rsplit,
+  // status, counter (the decode epoch) and dtags (the decode kernel's tagged
+  // exchange words) lie below keys: moe_workspace_init zeroes [0, keys)
+  size_t status, counter, dtags, keys, topk_id, topk_w, counts, offsets, perm, inv, blockmap, n_tiles, h, y, rsplit,
       xn, trace, total;
 };
 

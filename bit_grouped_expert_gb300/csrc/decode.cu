@@ -74,8 +74,11 @@ struct DecArgs {
   float *keys;
   int32_t *topk_id;
   float *topk_w;
-  uint16_t *hbuf;           // [k+S][I]
-  unsigned long long *bar;  // monotonic arrival counter of the grid barrier
+  // tagged exchange buffers (see ld_relaxed64) and the epoch counter
+  unsigned long long *tkeys;  // [2][E]           fp32 router keys
+  unsigned long long *th;     // [2][(k+S)*I/2]   h, bf16 pairs
+  unsigned long long *tr;     // [2][H/2]         residual stream between layers, bf16 pairs
+  unsigned long long *epoch;  // epochs used so far (low 32 bits)
   int32_t *status;
   uint64_t *trace;  // [MOE_TRACE_CTAS][MOE_TRACE_SLOTS] phase timestamps or null
   int H, E, k, I, S, prenorm;
@@ -90,53 +93,59 @@ struct DecArgs {
 static_assert(sizeof(DecArgs) <= 4000, "kernel parameters stay under 4 KB");
 
 
-__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p) {
+// CTAs hand values to one another without grid barriers: every value that
+// crosses CTAs (router keys, h, the residual stream between layers) travels
+// in a 64-bit word whose high half is its layer's epoch and whose low half is
+// the payload (an fp32 key or two bf16).  An aligned 64-bit store is seen
+// whole, so a reader that finds the current epoch in a word has its payload.
+// Each layer of each launch has its own epoch -- a counter read at launch and
+// advanced by the launch's layer count -- and the buffers alternate with the
+// epoch's parity.  Every layer rewrites all words of its parity, so a buffer
+// never holds a tag more than two epochs old and the 32-bit epoch may wrap.
+// A buffer is rewritten two layers later only by a CTA that has waited for
+// values every CTA produced after it had read that buffer.
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long *p) {
   unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-// Grid barrier on a monotonic arrival counter.  Every launch adds exactly
-// two arrivals per CTA, so at launch the counter is a multiple of the grid
-// size G; a CTA rounds the value it first reads down to that multiple (no CTA
-// can have completed the first round before it arrives) and barrier b of the
-// launch ends when the counter reaches base + b * G.  Arrival is a release
-// reduction that needs no reply; the wait is bounded.
-__device__ __forceinline__ void red_add_release64(unsigned long long *p, unsigned long long v) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ void st_relaxed64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Split phases: grid_arrive publishes this CTA's writes (every thread's, via
-// the block barrier and the release) and grid_wait returns once every CTA
-// has arrived; work between the two overlaps the barrier's latency.
-__device__ __forceinline__ void grid_arrive(unsigned long long *bar) {
-  __syncthreads();
-  if (threadIdx.x == 0) red_add_release64(bar, 1ull);
+__device__ __forceinline__ unsigned long long tagged(uint32_t ep, uint32_t payload) {
+  return ((unsigned long long)ep << 32) | payload;
 }
 
-__device__ bool grid_wait(unsigned long long *bar, unsigned long long target, int32_t *status) {
-  __shared__ int s_ok;
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    if (ld_acquire64(bar) < target) {
-      const uint64_t t0 = ptx::globaltimer();
-      while (ld_acquire64(bar) < target) {
-        if (ptx::globaltimer() - t0 > DTIMEOUT_NS) {
-          set_status(status, MOE_ERR_DEVICE_TIMEOUT);
-          ok = 0;
-          break;
-        }
+__device__ __forceinline__ bool has_tag(unsigned long long w, uint32_t ep) { return (uint32_t)(w >> 32) == ep; }
+
+// w[i] = src[idx[i]] once that word carries epoch ep (idx[i] < 0: no word);
+// false, with the status set, when the wait times out.
+template <int N>
+__device__ bool poll_tagged(const unsigned long long *src, const int (&idx)[N], unsigned long long (&w)[N],
+                            uint32_t ep, int32_t *status) {
+  bool done = true;
+#pragma unroll
+  for (int i = 0; i < N; ++i) w[i] = idx[i] >= 0 ? ld_relaxed64(src + idx[i]) : tagged(ep, 0u);
+#pragma unroll
+  for (int i = 0; i < N; ++i) done = done && has_tag(w[i], ep);
+  if (done) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    done = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (!has_tag(w[i], ep)) {
+        w[i] = ld_relaxed64(src + idx[i]);
+        done = done && has_tag(w[i], ep);
       }
+    if (done) return true;
+    if (ptx::globaltimer() - t0 > DTIMEOUT_NS) {
+      set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+      return false;
     }
-    s_ok = ok;
   }
-  __syncthreads();
-  return s_ok != 0;
-}
-
-__device__ bool grid_sync(unsigned long long *bar, unsigned long long target, int32_t *status) {
-  grid_arrive(bar);
-  return grid_wait(bar, target, status);
 }
 
 // Bounded wait for the phase of an mbarrier with the given parity.
@@ -280,18 +289,25 @@ __device__ bool gu_compute(const DecArgs &a, const uint8_t *codes, const uint8_t
 }
 
 // h = bf16(silu(gate) * up) of `nu` units from the partials; unit u's 8 rows
-// go to hbuf from element row_of(u).
+// are elements row_of(u) .. +7 of the h vectors [k+S][I], written as tagged
+// bf16 pairs into th (this epoch's half).
 template <typename RowOf>
-__device__ void gu_finish(const DecArgs &a, int nu, const float *red, RowOf row_of) {
+__device__ void gu_finish(const DecArgs &a, int nu, const float *red, unsigned long long *th, uint32_t ep,
+                          RowOf row_of) {
   const int nkc = a.H / KCH;
-  for (int t = threadIdx.x; t < nu * 8; t += DTHREADS) {
-    const int u = t >> 3, r = t & 7;
-    float gs = 0.f, us = 0.f;
-    for (int kc = 0; kc < nkc; ++kc) {
-      gs += red[(u * nkc + kc) * 16 + r];
-      us += red[(u * nkc + kc) * 16 + 8 + r];
+  for (int t = threadIdx.x; t < nu * 4; t += DTHREADS) {
+    const int u = t >> 2, r = (t & 3) * 2;
+    uint32_t hv[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float gs = 0.f, us = 0.f;
+      for (int kc = 0; kc < nkc; ++kc) {
+        gs += red[(u * nkc + kc) * 16 + r + i];
+        us += red[(u * nkc + kc) * 16 + 8 + r + i];
+      }
+      hv[i] = f32_to_bf16(silu(gs) * us);
     }
-    a.hbuf[row_of(u) + r] = f32_to_bf16(silu(gs) * us);
+    st_relaxed64(th + (row_of(u) + r) / 2, tagged(ep, hv[0] | (hv[1] << 16)));
   }
 }
 
@@ -300,13 +316,23 @@ __device__ void gu_finish(const DecArgs &a, int nu, const float *red, RowOf row_
 // lane maxima bounds the k-th largest key from below (k distinct keys reach
 // it), so only the keys at or above it -- at most 8k -- are ranked, each
 // against the others.  Same order and tie rule as topk_block.
-__device__ void topk_warp(const float *keys_g, int E, int k, unsigned long long *cand, int32_t *ids, float *w,
-                          int32_t *status) {
+__device__ bool topk_warp(const unsigned long long *tkeys, uint32_t ep, int E, int k, unsigned long long *cand,
+                          int32_t *ids, float *w, int32_t *status, uint64_t *tr) {
   const int lane = threadIdx.x & 31;
+  auto mark = [&](int slot) {
+    if (tr && lane == 0) tr[slot] = ptx::globaltimer();
+  };
+  int idx[8];
+  unsigned long long kw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) idx[i] = lane + 32 * i < E ? lane + 32 * i : -1;
+  const bool got = __all_sync(0xffffffffu, poll_tagged(tkeys, idx, kw, ep, status));
+  if (!got) return false;
   float kv[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) kv[i] = lane + 32 * i < E ? __ldcg(keys_g + lane + 32 * i) : 0.f;
+  for (int i = 0; i < 8; ++i) kv[i] = __uint_as_float((uint32_t)kw[i]);
   unsigned long long c[8], m = 0ull;
+  mark(18);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     c[i] = lane + 32 * i < E ? topk_code(kv[i], lane + 32 * i) : 0ull;
@@ -326,6 +352,7 @@ __device__ void topk_warp(const float *keys_g, int E, int k, unsigned long long 
     const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)m, src), hi = __shfl_sync(0xffffffffu, (uint32_t)(m >> 32), src);
     tau = ((unsigned long long)hi << 32) | lo;
   }
+  mark(19);
   int n = 0;
   const unsigned below = (1u << lane) - 1u;
 #pragma unroll
@@ -348,11 +375,14 @@ __device__ void topk_warp(const float *keys_g, int E, int k, unsigned long long 
     }
   }
   __syncwarp();
+  mark(20);
   const int my_id = lane < k ? ids[lane] : -1;
   const float my_key = lane < k ? w[lane] : 0.f;
   __syncwarp();
   topk_finish(lane, k, my_id, my_key, ids, w, nullptr, status);
   __syncwarp();
+  mark(21);
+  return true;
 }
 
 // Top-k of one token by all threads of the CTA.  Codes (topk_code) order the
@@ -433,7 +463,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   __shared__ int s_ids[16];
   __shared__ float s_w[16];
   __shared__ float s_part[DWARPS];
-  __shared__ unsigned long long s_base;
+  __shared__ uint32_t s_ep0;
   // 1024-byte aligned base for the swizzled code images (keeps the shared space)
   uint8_t *sm = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -516,22 +546,23 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   // launch in the stream when this one starts early: wait for it here, after
   // the weight copies are on their way.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0) {  // a relaxed read: only the value matters, not ordering
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.bar) : "memory");
-    s_base = v / (unsigned long long)G * (unsigned long long)G;
-  }
+  // This launch's layers take epochs ep0 + 1 .. ep0 + nl (CTA 0 advances the
+  // counter when it is done, by which time every CTA has read it).
+  if (tid == 0) s_ep0 = (uint32_t)ld_relaxed64(a.epoch);
   // the residual of this CTA's output rows: read once; later layers keep
   // their own output, which is the next layer's residual
   float res_v = 0.f;
   if (tid < nou * 8) res_v = bf16_to_f32(a.res[(cta + (tid >> 3) * G) * 8 + (tid & 7)]);
+  __syncthreads();
+  const uint32_t ep0 = s_ep0;
   bool ok = true;
   uint32_t n_p1 = 1, n_dsh = 1, n_drt = 0;  // phases armed so far, for the drain on failure
+  const int hw = NS * I / 2;                // words of one h buffer
   int l = 0;
-  for (; l < a.nl; ++l) {
+  for (; l < a.nl && ok; ++l) {
     const LayerW &L = a.lw[l];
-    const uint32_t ph = (uint32_t)l & 1u;
-    const unsigned long long b0 = s_base + 3ull * (unsigned long long)l * (unsigned long long)G;
+    const uint32_t ph = (uint32_t)l & 1u, ep = ep0 + (uint32_t)l + 1u, pb = ep & 1u;
+    unsigned long long *tk = a.tkeys + pb * E, *thb = a.th + (size_t)pb * hw;
     trace(2, l);
     // this layer's tensor maps, for the copies issued after the routing
     if (tid == 0 && a.map3d && l > 0) {
@@ -541,13 +572,32 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     }
     // -------------------------------------------------------------- P0: x (padded groups)
     if (a.prenorm) {
-      // r read once into registers (4 values a thread a round), RMS, scale
+      // r into registers (4 values a thread a round): layer 0 from the
+      // input, later layers from the previous layer's tagged words; RMS, scale
       uint2 rv[XREG];
+      bool got = true;
+      if (l == 0) {
+#pragma unroll
+        for (int j = 0; j < XREG; ++j) {
+          const int i = tid + j * DTHREADS;
+          rv[j] = i < H / 4 ? __ldcg(reinterpret_cast<const uint2 *>(a.xin) + i) : make_uint2(0u, 0u);
+        }
+      } else {
+        int idx[2 * XREG];
+        unsigned long long w[2 * XREG];
+#pragma unroll
+        for (int j = 0; j < XREG; ++j) {
+          const int i = tid + j * DTHREADS;
+          idx[2 * j] = i < H / 4 ? 2 * i : -1;
+          idx[2 * j + 1] = i < H / 4 ? 2 * i + 1 : -1;
+        }
+        got = poll_tagged(a.tr + (size_t)pb * (H / 2), idx, w, ep, a.status);
+#pragma unroll
+        for (int j = 0; j < XREG; ++j) rv[j] = make_uint2((uint32_t)w[2 * j], (uint32_t)w[2 * j + 1]);
+      }
       float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < XREG; ++j) {
-        const int i = tid + j * DTHREADS;
-        rv[j] = i < H / 4 ? __ldcg(reinterpret_cast<const uint2 *>(a.xin) + i) : make_uint2(0u, 0u);
         const float v0 = __uint_as_float(rv[j].x << 16), v1 = __uint_as_float(rv[j].x & 0xFFFF0000u);
         const float v2 = __uint_as_float(rv[j].y << 16), v3 = __uint_as_float(rv[j].y & 0xFFFF0000u);
         ss = fmaf(v0, v0, ss);
@@ -557,7 +607,8 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       }
       ss = warp_sum(ss);
       if (lane == 0) s_part[warp] = ss;
-      __syncthreads();
+      ok = __syncthreads_and(got) != 0;
+      if (!ok) break;
       float tot = 0.f;
 #pragma unroll
       for (int w = 0; w < DWARPS; ++w) tot += s_part[w];
@@ -574,13 +625,13 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
           reinterpret_cast<uint2 *>(xn)[i] = make_uint2(lo, hi);
           // lanes 2c and 2c+1 hold the halves of word c: swap one register
           const bool odd = (lane & 1) != 0;
-          const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
-          const uint4 pw = odd ? perm8(got, got, lo, hi) : perm8(lo, hi, got, got);
+          const uint32_t got2 = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+          const uint4 pw = odd ? perm8(got2, got2, lo, hi) : perm8(lo, hi, got2, got2);
           *reinterpret_cast<uint2 *>(xs + (i >> 4) * XPAD + (i & 15) * 4) =
               odd ? make_uint2(pw.z, pw.w) : make_uint2(pw.x, pw.y);
         }
       }
-    } else {
+    } else {  // one layer (launches of several layers are pre-norm)
       for (int i = tid; i < H / 8; i += DTHREADS) {
         const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.xin) + i);
         reinterpret_cast<uint4 *>(xn)[i] = v;
@@ -591,7 +642,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     trace(3, l);
 
     // -------------------------------------------------------------- P1: router rows, shared gate/up
-    if (ok) ok = wait_bar(bar_p1, ph, a.status);
+    ok = wait_bar(bar_p1, ph, a.status);
     trace(4, l);
     if (ok)
       for (int i = warp; i < nre; i += DWARPS) {  // one warp per router row, fp32 FMA
@@ -607,95 +658,115 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         }
         acc = warp_sum(acc);
         const int e = rc + i * a.rp_ctas;
-        if (lane == 0) a.keys[e] = L.bias ? acc + L.bias[e] : acc;
+        if (lane == 0) {
+          const float key = L.bias ? acc + L.bias[e] : acc;
+          a.keys[e] = key;
+          st_relaxed64(tk + e, tagged(ep, __float_as_uint(key)));
+        }
       }
-    // The keys are all the barrier publishes; the shared expert's h goes out
-    // with the next barrier, so its units are computed while this one settles.
-    grid_arrive(a.bar);
     trace(5, l);
     if (ok && nsu > 0) ok = gu_compute(a, su, sus, nsu, nullptr, 0u, xs, red);
     ok = __syncthreads_and(ok) != 0;  // every flag below stays uniform across the CTA
-    if (ok && nsu > 0) gu_finish(a, nsu, red, [&](int u) { return (size_t)k * I + (size_t)(cta + u * G) * 8; });
+    if (!ok) break;
+    if (nsu > 0)
+      gu_finish(a, nsu, red, thb, ep, [&](int u) { return (size_t)k * I + (size_t)(cta + u * G) * 8; });
     trace(6, l);
-    ok = grid_wait(a.bar, b0 + (unsigned long long)G, a.status) && ok;
-    trace(7, l);
     // the next layer's router rows and shared unit, into the buffers P1 has
     // finished with (read by this CTA's generic loads, written by TMA next)
-    if (ok && l + 1 < a.nl) {
+    if (l + 1 < a.nl) {
       ptx::fence_proxy_async_smem();
       if (tid == 0) expect_tx(bar_p1, p1_bytes);
       __syncthreads();
       issue_p1(l + 1);
       n_p1 = l + 2;
     }
+    trace(7, l);
 
     // -------------------------------------------------------------- P2: routing, routed gate/up
-    if (ok) {
-      if (E <= 256) {
-        if (warp == 0) topk_warp(a.keys, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand), s_ids, s_w,
-                                 a.status);
-      } else {
-        for (int e = tid; e < E; e += DTHREADS) keys[e] = __ldcg(a.keys + e);
-        __syncthreads();
+    bool got = true;
+    if (E <= 256) {
+      if (warp == 0)
+        got = topk_warp(tk, ep, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand), s_ids, s_w, a.status,
+                        trace0 && l == a.nl - 1 && cta < MOE_TRACE_CTAS ? a.trace + cta * MOE_TRACE_SLOTS : nullptr);
+    } else {
+      for (int e = tid; e < E; e += DTHREADS) {
+        const int idx[1] = {e};
+        unsigned long long w[1];
+        got = poll_tagged(tk, idx, w, ep, a.status) && got;
+        keys[e] = __uint_as_float((uint32_t)w[0]);
+      }
+      if (__syncthreads_and(got))
         topk_block(keys, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand),
                    reinterpret_cast<unsigned long long *>(sm + a.off_gmax), s_ids, s_w, a.status);
-      }
-      ptx::fence_proxy_async_smem();  // the routed buffers were last read by generic loads
-      if (tid == 0) {
-        for (int i = 0; i < nru; ++i) expect_tx(&bar_ru[i], (uint32_t)(9 * H));
-        expect_tx(bar_drt, (uint32_t)(nou * k * (4 * I + I / 2)));
-      }
-      __syncthreads();
-      trace(8, l);
-      if (cta == 0 && tid < k) {
-        a.topk_id[tid] = s_ids[tid];
-        a.topk_w[tid] = s_w[tid];
-      }
-      n_drt = l + 1;
-      if (issuer >= 0) {
-        const int ngu = gu_ops(a), ndn = dn_ops(a);
-        const int n1 = nru * ngu, n2 = n1 + nou * k * ndn;
-        for (int o = issuer; o < n2; o += 2 * DWARPS) {
-          if (o < n1) {
-            const int i = o / ngu, u = cta + i * G;
-            gu_op(a, L, a.maps[l], o % ngu, ru + i * 8 * H, rus + i * H, s_ids[u / upr], (u % upr) * 8,
-                  &bar_ru[i]);
-          } else {
-            const int b = (o - n1) / ndn, ol = b / k, j = b % k;
-            dn_op(a, L, a.maps[l], (o - n1) % ndn, dc + (ol * NS + j) * 4 * I, ds + (ol * NS + j) * (I / 2),
-                  s_ids[j], (cta + ol * G) * 8, bar_drt);
-          }
+    }
+    ok = __syncthreads_and(got) != 0;
+    if (!ok) break;
+    ptx::fence_proxy_async_smem();  // the routed buffers were last read by generic loads
+    if (tid == 0) {
+      for (int i = 0; i < nru; ++i) expect_tx(&bar_ru[i], (uint32_t)(9 * H));
+      expect_tx(bar_drt, (uint32_t)(nou * k * (4 * I + I / 2)));
+    }
+    __syncthreads();
+    trace(8, l);
+    if (cta == 0 && tid < k) {
+      a.topk_id[tid] = s_ids[tid];
+      a.topk_w[tid] = s_w[tid];
+    }
+    n_drt = l + 1;
+    if (issuer >= 0) {
+      const int ngu = gu_ops(a), ndn = dn_ops(a);
+      const int n1 = nru * ngu, n2 = n1 + nou * k * ndn;
+      for (int o = issuer; o < n2; o += 2 * DWARPS) {
+        if (o < n1) {
+          const int i = o / ngu, u = cta + i * G;
+          gu_op(a, L, a.maps[l], o % ngu, ru + i * 8 * H, rus + i * H, s_ids[u / upr], (u % upr) * 8, &bar_ru[i]);
+        } else {
+          const int b = (o - n1) / ndn, ol = b / k, j = b % k;
+          dn_op(a, L, a.maps[l], (o - n1) % ndn, dc + (ol * NS + j) * 4 * I, ds + (ol * NS + j) * (I / 2), s_ids[j],
+                (cta + ol * G) * 8, bar_drt);
         }
       }
-      trace(9, l);
-      const bool ok2 = __syncthreads_and(gu_compute(a, ru, rus, nru, bar_ru, ph, xs, red)) != 0;
-      trace(10, l);
-      if (ok2 && nru > 0)
-        gu_finish(a, nru, red, [&](int u) {
-          const int uu = cta + u * G;
-          return (size_t)(uu / upr) * I + (size_t)(uu % upr) * 8;
-        });
-      ok = ok && ok2;
     }
+    trace(9, l);
+    ok = __syncthreads_and(gu_compute(a, ru, rus, nru, bar_ru, ph, xs, red)) != 0;
+    trace(10, l);
+    if (!ok) break;
+    if (nru > 0)
+      gu_finish(a, nru, red, thb, ep, [&](int u) {
+        const int uu = cta + u * G;
+        return (size_t)(uu / upr) * I + (size_t)(uu % upr) * 8;
+      });
     trace(11, l);
-    ok = grid_sync(a.bar, b0 + 2ull * (unsigned long long)G, a.status) && ok;
-    trace(12, l);
 
     // -------------------------------------------------------------- P3: down + combine
     // let the next launch in the stream start its prologue and weight copies
     if (l + 1 == a.nl) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (ok) {
-      const int nv = NS * I / 8;  // h of every slot, 16 bytes per load, into padded groups
-      for (int i = tid; i < nv; i += DTHREADS) {
-        const int j = i / (I / 8), c8 = i % (I / 8);
-        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.hbuf) + i);
-        *reinterpret_cast<uint4 *>(hs + (j * (I / 64) + (c8 >> 3)) * XPAD + (c8 & 7) * 8) = perm8(v.x, v.y, v.z, v.w);
+    {
+      // h of every slot (tagged pairs, 4 words per 8 values) into padded groups
+      const int nv = NS * I / 8;
+      got = true;
+      for (int i0 = tid; i0 < nv; i0 += 2 * DTHREADS) {
+        const int i1 = i0 + DTHREADS;
+        const int idx[8] = {4 * i0, 4 * i0 + 1, 4 * i0 + 2, 4 * i0 + 3, i1 < nv ? 4 * i1 : -1,
+                            i1 < nv ? 4 * i1 + 1 : -1, i1 < nv ? 4 * i1 + 2 : -1, i1 < nv ? 4 * i1 + 3 : -1};
+        unsigned long long w[8];
+        got = poll_tagged(thb, idx, w, ep, a.status) && got;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int i = r ? i1 : i0;
+          if (i < nv) {
+            const int j = i / (I / 8), c8 = i % (I / 8);
+            *reinterpret_cast<uint4 *>(hs + (j * (I / 64) + (c8 >> 3)) * XPAD + (c8 & 7) * 8) =
+                perm8((uint32_t)w[4 * r], (uint32_t)w[4 * r + 1], (uint32_t)w[4 * r + 2], (uint32_t)w[4 * r + 3]);
+          }
+        }
       }
-      trace(13, l);
-      ok = __syncthreads_and(wait_bar(bar_dsh, ph, a.status) && wait_bar(bar_drt, ph, a.status)) != 0;
+      trace(12, l);
+      ok = __syncthreads_and(got && wait_bar(bar_dsh, ph, a.status) && wait_bar(bar_drt, ph, a.status)) != 0;
       trace(14, l);
+      if (!ok) break;
     }
-    if (ok) {
+    {
       const int nkcd = I / KCH, gpr = I / 64, g = lane >> 2, q = lane & 3;
       const int nitem = nou * NS * nkcd;
       for (int t = warp; t < nitem; t += DWARPS) {
@@ -724,20 +795,29 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         ys[t] = bf16_to_f32(f32_to_bf16(v));
       }
       __syncthreads();
-      if (tid < nou * 8) {
-        const float *yr = ys + tid * NS;
-        float o = res_v;
-        if (S) o += yr[k];
-        for (int j = 0; j < k; ++j) o = fmaf(s_w[j], yr[j], o);
-        const uint16_t ob = f32_to_bf16(o);
-        a.out[(cta + (tid >> 3) * G) * 8 + (tid & 7)] = ob;
-        res_v = bf16_to_f32(ob);  // the next layer's residual for this row
+      // rows of this CTA (nou * 8 <= 16 of them, all in warp 0): out, and the
+      // next epoch's tagged words (row pairs)
+      if (warp == 0) {
+        uint32_t ob = 0u;
+        const int n = (cta + (tid >> 3) * G) * 8 + (tid & 7);
+        if (tid < nou * 8) {
+          const float *yr = ys + tid * NS;
+          float o = res_v;
+          if (S) o += yr[k];
+          for (int j = 0; j < k; ++j) o = fmaf(s_w[j], yr[j], o);
+          ob = f32_to_bf16(o);
+          if (l + 1 == a.nl) a.out[n] = (uint16_t)ob;
+          res_v = bf16_to_f32((uint16_t)ob);  // the next layer's residual for this row
+        }
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, ob, 1);
+        if (tid < nou * 8 && !(tid & 1))
+          st_relaxed64(a.tr + (size_t)((ep + 1u) & 1u) * (H / 2) + n / 2, tagged(ep + 1u, ob | (other << 16)));
       }
       trace(16, l);
     }
-    if (l + 1 < a.nl) ok = grid_sync(a.bar, b0 + 3ull * (unsigned long long)G, a.status) && ok;
     trace(17, l);
   }
+  if (cta == 0 && tid == 0) st_relaxed64(a.epoch, (unsigned long long)(uint32_t)(ep0 + (uint32_t)a.nl));
   // never leave with copies in flight into this CTA's shared memory
   // (a phase that has completed passes at once)
   if (tid == 0 && !ok) {
@@ -891,22 +971,24 @@ namespace {
 
 // One cooperative launch of layers [0, nl) of lw (nl <= MAXL).
 cudaError_t launch_layers(const uint16_t *x, const uint16_t *res, uint16_t *out, int H, int E, int k, int I, int S,
-                          int prenorm, float eps, const LayerW *lw, int nl, float *keys, int32_t *topk_id,
-                          float *topk_w, unsigned long long *bar, uint16_t *hbuf, int32_t *status, uint64_t *trace,
+                          int prenorm, float eps, const LayerW *lw, int nl, const DecodeScratch &sc, bool trace,
                           int num_sms, cudaStream_t s) {
+  if (nl < 1 || nl > MAXL || (nl > 1 && !prenorm)) return cudaErrorInvalidValue;
   DecPlan p = make_plan(H, E, k, I, S, num_sms);
   DecArgs &a = p.a;
   a.nl = nl;
   a.xin = x;
   a.res = res;
   a.out = out;
-  a.keys = keys;
-  a.topk_id = topk_id;
-  a.topk_w = topk_w;
-  a.hbuf = hbuf;
-  a.bar = bar;
-  a.status = status;
-  a.trace = trace;
+  a.keys = sc.keys;
+  a.topk_id = sc.topk_id;
+  a.topk_w = sc.topk_w;
+  a.tkeys = sc.tags;
+  a.th = sc.tags + 2 * (size_t)E;
+  a.tr = a.th + (size_t)(k + S) * I;
+  a.epoch = sc.epoch;
+  a.status = sc.status;
+  a.trace = trace ? sc.trace : nullptr;
   a.prenorm = prenorm;
   a.eps = eps;
   a.map3d = 1;
@@ -924,8 +1006,8 @@ cudaError_t launch_layers(const uint16_t *x, const uint16_t *res, uint16_t *out,
   cfg.blockDim = dim3(DTHREADS);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = s;
-  // The grid barrier needs every CTA resident at once: launch cooperatively
-  // or not at all.  Programmatic serialisation lets the launch begin while
+  // CTAs wait for values other CTAs produce, so every CTA must be resident at
+  // once: launch cooperatively or not at all.  Programmatic serialisation lets the launch begin while
   // the previous kernel in the stream drains (the kernel waits for it before
   // it reads its input); drivers that refuse the pair get a plain cooperative
   // launch.
@@ -949,13 +1031,16 @@ cudaError_t launch_layers(const uint16_t *x, const uint16_t *res, uint16_t *out,
 
 }  // namespace
 
+size_t decode_tag_words(int H, int E, int k, int I, int S) {
+  // keys [2][E], h [2][(k+S) I / 2], residual [2][H / 2]
+  return 2 * (size_t)E + (size_t)(k + S) * I + (size_t)H;
+}
+
 cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, int k, int I, int S, int prenorm,
-                          float eps, const float *router, const float *bias, ExpertPtrs w, float *keys,
-                          int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf, uint16_t *out,
-                          int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s) {
+                          float eps, const float *router, const float *bias, ExpertPtrs w, uint16_t *out,
+                          const DecodeScratch &sc, int num_sms, int *launches, cudaStream_t s) {
   const LayerW lw{router, bias, w};
-  const cudaError_t e = launch_layers(x, res, out, H, E, k, I, S, prenorm, eps, &lw, 1, keys, topk_id, topk_w, bar,
-                                      hbuf, status, trace, num_sms, s);
+  const cudaError_t e = launch_layers(x, res, out, H, E, k, I, S, prenorm, eps, &lw, 1, sc, true, num_sms, s);
   if (e != cudaSuccess) return e;
   *launches += 1;
   return cudaSuccess;
@@ -963,14 +1048,12 @@ cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, 
 
 cudaError_t launch_decode_stack(uint16_t *r, int n_layers, int H, int E, int k, int I, int S, float eps,
                                 const float *const *router, const float *const *bias, const ExpertPtrs *w,
-                                float *keys, int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf,
-                                int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s) {
+                                const DecodeScratch &sc, int num_sms, int *launches, cudaStream_t s) {
   for (int l0 = 0; l0 < n_layers; l0 += MAXL) {
     const int nl = n_layers - l0 < MAXL ? n_layers - l0 : MAXL;
     LayerW lw[MAXL];
     for (int l = 0; l < nl; ++l) lw[l] = LayerW{router[l0 + l], bias ? bias[l0 + l] : nullptr, w[l0 + l]};
-    const cudaError_t e = launch_layers(r, r, r, H, E, k, I, S, 1, eps, lw, nl, keys, topk_id, topk_w, bar, hbuf,
-                                        status, l0 == 0 ? trace : nullptr, num_sms, s);
+    const cudaError_t e = launch_layers(r, r, r, H, E, k, I, S, 1, eps, lw, nl, sc, l0 == 0, num_sms, s);
     if (e != cudaSuccess) return e;
     *launches += 1;
   }

@@ -1,8 +1,9 @@
 // moe_decode_static: the single-token layer of moe_forward's decode path for
-// callers that cannot allocate device memory.  Its scratch -- the router keys,
-// the top-k ids and weights, the per-slot h vectors, the grid-barrier counter
-// and the status word -- lives in one file-scope __device__ array instead of a
-// caller-allocated workspace.
+// callers that cannot allocate device memory.  Its scratch -- the status
+// word, the decode epoch counter, the tagged exchange words, the router keys
+// and the top-k ids and weights -- lives in one file-scope __device__ array
+// instead of a caller-allocated workspace.
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -18,19 +19,20 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) uint8_t g_decode_scratch[MOE_DECODE_STATIC_SCRATCH_BYTES];
 
 // Byte offsets inside the array (256-byte aligned).
-constexpr size_t kStatus = 0, kCounter = 64, kKeys = 256;
+constexpr size_t kStatus = 0, kCounter = 64, kTags = 256;
 constexpr size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct Scratch {
-  size_t topk_id, topk_w, h, total;
+  size_t tag_bytes, keys, topk_id, topk_w, total;
 };
 
 Scratch scratch_layout(const moe_config &c) {
   Scratch s;
-  s.topk_id = al256(kKeys + (size_t)c.n_experts * 4);
+  s.tag_bytes = moe::decode_tag_words(c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared) * 8;
+  s.keys = al256(kTags + s.tag_bytes);
+  s.topk_id = al256(s.keys + (size_t)c.n_experts * 4);
   s.topk_w = al256(s.topk_id + (size_t)c.top_k * 4);
-  s.h = al256(s.topk_w + (size_t)c.top_k * 4);
-  s.total = s.h + (size_t)(c.top_k + c.n_shared) * c.inter * 2;
+  s.total = s.topk_w + (size_t)c.top_k * 4;
   return s;
 }
 
@@ -38,6 +40,7 @@ struct DeviceState {
   bool ready = false;
   uint8_t *scratch = nullptr;  // device address of g_decode_scratch on this device
   int num_sms = 0;
+  moe_config last{};  // dimensions of the previous call: its tagged words lie in another layout
 };
 
 std::mutex g_mu;
@@ -108,10 +111,19 @@ extern "C" moe_status moe_decode_static(const moe_config *cfg, const void *x_d, 
     return MOE_ERR_UNSUPPORTED;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents.  The status word and the
-  // grid-barrier counter must start at zero; keys, top-k and h are rewritten
-  // in full before they are read.
-  cudaError_t e = cudaMemsetAsync(d->scratch, 0, kKeys, s);
+  // The array keeps the previous call's contents (zero before the first).
+  // The status word starts at zero; the epoch counter and the tagged words
+  // carry over from call to call, except that the words are cleared when the
+  // dimensions change (a word of the old layout must not pass for the new);
+  // keys and top-k are rewritten in full.
+  bool same;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    same = std::memcmp(&d->last, &c, sizeof c) == 0;
+    d->last = c;
+  }
+  cudaError_t e = cudaMemsetAsync(d->scratch + kStatus, 0, 64, s);
+  if (e == cudaSuccess && !same) e = cudaMemsetAsync(d->scratch + kTags, 0, L.tag_bytes, s);
   if (e == cudaSuccess && status_d) e = cudaMemsetAsync(status_d, 0, sizeof(int32_t), s);
   if (e != cudaSuccess) return moe::note_cuda_error(e);
 
@@ -129,12 +141,17 @@ extern "C" moe_status moe_decode_static(const moe_config *cfg, const void *x_d, 
   const uint16_t *res = residual_d ? static_cast<const uint16_t *>(residual_d) : x;
   uint8_t *sc = d->scratch;
   int32_t *status = status_d ? status_d : reinterpret_cast<int32_t *>(sc + kStatus);
+  moe::DecodeScratch ds;
+  ds.keys = reinterpret_cast<float *>(sc + L.keys);
+  ds.topk_id = reinterpret_cast<int32_t *>(sc + L.topk_id);
+  ds.topk_w = reinterpret_cast<float *>(sc + L.topk_w);
+  ds.epoch = reinterpret_cast<unsigned long long *>(sc + kCounter);
+  ds.tags = reinterpret_cast<unsigned long long *>(sc + kTags);
+  ds.status = status;
+  ds.trace = nullptr;
   int launches = 0;
   e = moe::launch_decode(x, res, c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, prenorm ? 1 : 0, 1e-6f,
-                         w->router_d, logit_bias_d, ep, reinterpret_cast<float *>(sc + kKeys),
-                         reinterpret_cast<int32_t *>(sc + L.topk_id), reinterpret_cast<float *>(sc + L.topk_w),
-                         reinterpret_cast<unsigned long long *>(sc + kCounter),
-                         reinterpret_cast<uint16_t *>(sc + L.h), static_cast<uint16_t *>(out_d), status, nullptr,
-                         d->num_sms, &launches, s);
+                         w->router_d, logit_bias_d, ep, static_cast<uint16_t *>(out_d), ds, d->num_sms, &launches,
+                         s);
   return e == cudaSuccess ? MOE_OK : moe::note_cuda_error(e);
 }

@@ -44,18 +44,30 @@ cudaError_t launch_rmsnorm(const uint16_t *r, int T, int H, float eps, uint16_t 
 cudaError_t launch_dequant(const uint32_t *q, const uint16_t *sc, const uint16_t *b, int rows, int K, int G,
                            uint16_t *w, cudaStream_t s);
 
-// decode.cu (T == 1: the whole layer as one cooperative launch)
+// decode.cu (T == 1: one cooperative launch runs whole layers)
+// The decode kernel's scratch: the fp32 router keys and the top-k of the last
+// layer run (for inspection), the epoch counter and the tagged exchange
+// buffers (decode_tag_words 64-bit words; both zero before the first launch,
+// kept between launches), the status word and the optional trace.
+struct DecodeScratch {
+  float *keys;
+  int32_t *topk_id;
+  float *topk_w;
+  unsigned long long *epoch;
+  unsigned long long *tags;
+  int32_t *status;
+  uint64_t *trace;
+};
+size_t decode_tag_words(int H, int E, int k, int I, int S);
 bool decode_supported(int H, int E, int k, int I, int S, int num_sms);
 cudaError_t decode_prepare(int H, int E, int k, int I, int S, int num_sms);
 cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, int k, int I, int S, int prenorm,
-                          float eps, const float *router, const float *bias, ExpertPtrs w, float *keys,
-                          int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf, uint16_t *out,
-                          int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s);
+                          float eps, const float *router, const float *bias, ExpertPtrs w, uint16_t *out,
+                          const DecodeScratch &sc, int num_sms, int *launches, cudaStream_t s);
 // n_layers pre-norm layers on one token, r updated in place: r += MoE_l(RMSNorm(r));
 // router/bias/w: host arrays of n_layers (bias may be null, or hold nulls).
 cudaError_t launch_decode_stack(uint16_t *r, int n_layers, int H, int E, int k, int I, int S, float eps,
                                 const float *const *router, const float *const *bias, const ExpertPtrs *w,
-                                float *keys, int32_t *topk_id, float *topk_w, unsigned long long *bar, uint16_t *hbuf,
-                                int32_t *status, uint64_t *trace, int num_sms, int *launches, cudaStream_t s);
+                                const DecodeScratch &sc, int num_sms, int *launches, cudaStream_t s);
 
 }  // namespace moe

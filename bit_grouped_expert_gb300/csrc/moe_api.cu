@@ -44,6 +44,7 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles) {
   const size_t E = c.n_experts, k = c.top_k, S = c.n_shared, H = c.hidden, I = c.inter, T = Tmax;
   L.status = take(64);
   L.counter = take(64);
+  L.dtags = take(moe::decode_tag_words(c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared) * 8);
   L.keys = take(T * E * 4);
   L.topk_id = take(T * k * 4);
   L.topk_w = take(T * k * 4);
@@ -60,6 +61,19 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles) {
   L.trace = take(MOE_TRACE_CTAS * MOE_TRACE_SLOTS * 8);
   L.total = o;
   return L;
+}
+
+moe::DecodeScratch decode_scratch(const moe_plan_t *plan, void *ws_d) {
+  const moe::Layout &L = plan->lay;
+  moe::DecodeScratch sc;
+  sc.keys = moe::ws_ptr<float>(ws_d, L.keys);
+  sc.topk_id = moe::ws_ptr<int32_t>(ws_d, L.topk_id);
+  sc.topk_w = moe::ws_ptr<float>(ws_d, L.topk_w);
+  sc.epoch = moe::ws_ptr<unsigned long long>(ws_d, L.counter);
+  sc.tags = moe::ws_ptr<unsigned long long>(ws_d, L.dtags);
+  sc.status = moe::ws_ptr<int32_t>(ws_d, L.status);
+  sc.trace = (plan->flags & MOE_FLAG_TRACE) ? moe::ws_ptr<uint64_t>(ws_d, L.trace) : nullptr;
+  return sc;
 }
 
 bool weights_aligned(const moe_weights *w) {
@@ -277,7 +291,7 @@ moe_status moe_workspace_init(const moe_plan_t *plan, void *ws_d, size_t ws_byte
   if (!moe::aligned16(ws_d)) return MOE_ERR_MISALIGNED;
   if (ws_bytes < plan->lay.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (device_ready(plan) != MOE_OK) return MOE_ERR_CUDA;
-  // status and counter words
+  // status, the decode epoch counter and its tagged words
   return cuda_status(cudaMemsetAsync(ws_d, 0, plan->lay.keys, static_cast<cudaStream_t>(stream)));
 }
 
@@ -343,12 +357,9 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
   int launches = 0;
 
   if (T == 1 && plan->use_decode && !(plan->flags & MOE_FLAG_FORCE_GROUPED)) {
-    cudaError_t err = moe::launch_decode(
-        x, res, c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, prenorm ? 1 : 0, 1e-6f, w->router_d,
-        logit_bias_d, ep, moe::ws_ptr<float>(ws_d, L.keys), moe::ws_ptr<int32_t>(ws_d, L.topk_id),
-        moe::ws_ptr<float>(ws_d, L.topk_w), moe::ws_ptr<unsigned long long>(ws_d, L.counter),
-        moe::ws_ptr<uint16_t>(ws_d, L.h), out, status,
-        (plan->flags & MOE_FLAG_TRACE) ? moe::ws_ptr<uint64_t>(ws_d, L.trace) : nullptr, plan->num_sms, &launches, s);
+    cudaError_t err = moe::launch_decode(x, res, c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared,
+                                         prenorm ? 1 : 0, 1e-6f, w->router_d, logit_bias_d, ep, out,
+                                         decode_scratch(plan, ws_d), plan->num_sms, &launches, s);
     g_last_launches = launches;
     return cuda_status(err);
   }
@@ -411,10 +422,7 @@ moe_status moe_decode_stack(const moe_plan_t *plan, void *r_d, int32_t n_layers,
   int launches = 0;
   const cudaError_t err = moe::launch_decode_stack(
       static_cast<uint16_t *>(r_d), n_layers, c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, 1e-6f,
-      router.data(), logit_bias_d, ep.data(), moe::ws_ptr<float>(ws_d, L.keys), moe::ws_ptr<int32_t>(ws_d, L.topk_id),
-      moe::ws_ptr<float>(ws_d, L.topk_w), moe::ws_ptr<unsigned long long>(ws_d, L.counter),
-      moe::ws_ptr<uint16_t>(ws_d, L.h), moe::ws_ptr<int32_t>(ws_d, L.status),
-      (plan->flags & MOE_FLAG_TRACE) ? moe::ws_ptr<uint64_t>(ws_d, L.trace) : nullptr, plan->num_sms, &launches,
+      router.data(), logit_bias_d, ep.data(), decode_scratch(plan, ws_d), plan->num_sms, &launches,
       static_cast<cudaStream_t>(stream));
   g_last_launches = launches;
   return cuda_status(err);

@@ -130,8 +130,11 @@ void moe_plan_destroy(moe_plan_t *plan);
 /* Bytes of device workspace a call of this plan needs (0 for a null plan). */
 size_t moe_workspace_bytes(const moe_plan_t *plan);
 
-/* Zero the workspace's status word and counters (enqueued on stream).  Call
- * once after allocating a workspace. */
+/* Zero the workspace's status word, counters and the decode kernel's tagged
+ * exchange words (enqueued on stream).  Call once after allocating a
+ * workspace, and again after a call has left an error in the device status
+ * (a decode launch cut short by a timeout can leave words that a later launch
+ * would take for its own).  A workspace serves one stream at a time. */
 moe_status moe_workspace_init(const moe_plan_t *plan, void *ws_d, size_t ws_bytes, void *stream);
 
 /* Routing only ("Prefill": histogram, prefix scan, scatter, block map, all on
@@ -232,8 +235,9 @@ moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *c
  * synchronisation an allocation can bring.  It computes what moe_forward
  * computes for T == 1 on its decode path (one cooperative launch), with the
  * scratch that path keeps in the workspace -- router keys, top-k ids and
- * weights, the k + n_shared h vectors, the grid-barrier counter and the
- * status word -- held instead in one static device array of
+ * weights, the decode epoch counter, the tagged words the kernel's CTAs
+ * exchange (keys, h, residual) and the status word -- held instead in one
+ * static device array of
  * MOE_DECODE_STATIC_SCRATCH_BYTES that every device loading the library keeps
  * until the process exits.  It needs no plan and calls no cudaMalloc,
  * cudaFree or allocating library routine.
@@ -249,14 +253,16 @@ moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *c
  * The first call on a device (with that device current) resolves the array's
  * address with cudaGetSymbolAddress and raises the decode kernel's
  * shared-memory limit; make that first call before any stream capture.
- * Every call clears the status word and the barrier counter on the stream
- * before its launch; keys, top-k and h are rewritten before they are read, so
- * the array otherwise keeps the previous call's contents.  All calls on a
- * device share the one array: calls that can overlap on the GPU (other
- * streams, other threads) race and must be serialised by the caller.
+ * Every call clears the status word on the stream before its launch, and
+ * the tagged words too when the dimensions differ from the previous call's;
+ * the epoch counter carries over, and keys and top-k are rewritten, so the
+ * array otherwise keeps the previous call's contents.  All calls on a device
+ * share the one array: calls that can overlap on the GPU (other streams,
+ * other threads) race and must be serialised by the caller.
  * Errors: MOE_ERR_WORKSPACE_TOO_SMALL when the layer's scratch (about
- * 4E + 8k + 2(k + n_shared)I bytes plus 256-byte alignment: 11,008 bytes for
- * H=2048, E=256, k=8, n_shared=1, I=512) exceeds the array; MOE_ERR_UNSUPPORTED for dimensions the decode path does not take
+ * 16E + 8(k + n_shared)I + 8H + 4E + 8k bytes plus 256-byte alignment: 58,912
+ * bytes for H=2048, E=256, k=8, n_shared=1, I=512) exceeds the array;
+ * MOE_ERR_UNSUPPORTED for dimensions the decode path does not take
  * (H and I powers of two, the kernel's shared memory within the device's
  * limit); MOE_ERR_INVALID_ARGUMENT / MOE_ERR_MISALIGNED as for moe_forward;
  * MOE_ERR_CUDA when a CUDA call fails (moe_last_cuda_error). */
