@@ -3,37 +3,39 @@
 // selected experts are streamed, and the step's kernels overlap instead of
 // running as hundreds of sequential launches).
 //
-// One cooperative launch per layer: every CTA (one per SM) runs
+// One cooperative launch runs up to MAXL layers; for each layer every CTA
+// (one per SM) runs
 //   P0  x = bf16(r / sqrt(mean(r^2) + eps)) (pre-norm plans) or x = input,
 //       computed redundantly into shared memory
-//   P1  router keys (fp32, one warp per expert row) and the shared expert's
-//       gate/up rows (h = bf16(silu(g) * u))
-//   --- grid barrier ---
+//   P1  router keys (fp32, one warp per expert row) or, on the CTAs without
+//       router rows, the shared expert's gate/up rows (h = bf16(silu(g) * u))
 //   P2  top-k over the keys (every CTA, same order, same result); the routed
 //       experts' gate/up rows
-//   --- grid barrier ---
-//   P3  the down rows of every slot for this CTA's output features, y_j =
+//   P3  the down rows of every slot for this CTA's output rows, y_j =
 //       bf16(h_j . Wd_j), out = bf16(res + y_shared + sum_j w_j * y_j)
+// The keys, h and the next layer's residual cross CTAs as epoch-tagged words
+// (see ld_relaxed64): a CTA waits for exactly the values it reads, with no
+// grid barrier.
 //
 // Weights reach shared memory through the tensor-memory accelerator as soon
-// as their addresses are known -- P1 and the shared expert's down rows at
-// launch, the routed experts' rows right after the top-k -- and each routed
-// gate/up unit has its own mbarrier, so its GEMV starts when its bytes land
-// while later units are still in flight.  Packed codes arrive in the 128-byte
-// swizzled layout: for 8 rows and one K-chunk of 256 codes, [row][128 B] with
-// the 16-byte pieces of row r permuted by XOR r, which makes the GEMV's
-// 16-byte reads of eight rows conflict-free.
+// as their addresses are known -- the next layer's router rows, shared rows
+// and shared down rows during this layer, the routed experts' rows right
+// after the top-k -- and each routed gate/up unit has its own mbarrier, so
+// its GEMV starts when its bytes land while later units are still in flight.
+// Packed codes arrive in the 128-byte swizzled layout: for 8 rows and one
+// K-chunk of 256 codes, [row][128 B] with the 16-byte pieces of row r
+// permuted by XOR r, which makes the GEMV's 16-byte reads of eight rows
+// conflict-free.
 //
-// The GEMVs run on mma.sync m16n8k16 with the activation vector broadcast
-// over the 16 A rows and 8 weight rows as B, dequantised in registers
-// (w = bf16_rne(scale * q + bias), fp32 accumulate).  The k index of the MMA
-// may map onto any 16 positions of K as long as A and B agree, so lane
-// (g, q) owns one whole quantisation group of row g -- 64 codes, one scale,
-// one bias -- and keeps that group's 64 x values in registers across all the
-// rows it visits.
+// The GEMVs run on mma.sync m16n8k16 with the weights as the A operand,
+// dequantised in registers (w = bf16_rne(scale * q + bias), fp32
+// accumulate) and the activation vector in B's first two columns.  The k
+// index of the MMA may map onto any 16 positions of K as long as A and B
+// agree, so lane (g, q) owns one whole quantisation group of row g -- 64
+// codes, one scale, one bias -- and the vector is kept in shared memory in
+// the order in which the codes unpack (see perm8).
 //
-// The grid barrier is a monotonic 64-bit arrival counter; every wait is
-// bounded (MOE_ERR_DEVICE_TIMEOUT).
+// Every wait is bounded (MOE_ERR_DEVICE_TIMEOUT).
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -86,6 +88,7 @@ struct DecArgs {
   int map3d;  // 1: one TMA op per matrix (3-D map over the K-chunks), 0: one per K-chunk
   // schedule
   int n_su, rp_cta0, rp_ctas, n_ru, n_ou;
+  int max_su, max_ru, max_ou;  // per-CTA maxima (strides of the scale images)
   // shared-memory layout (bytes from the 1024-aligned base)
   int off_dc, off_ru, off_su, off_rr, off_x, off_xn, off_h, off_ds, off_rus, off_sus, off_red, off_keys, off_cand,
       off_gmax, off_bar, off_ys;
@@ -221,56 +224,60 @@ __device__ __forceinline__ float gemv_chunk(const uint8_t *chunk, const uint16_t
   return ((e[0][0] + e[1][0]) + (e[2][0] + e[3][0])) + ((e[0][3] + e[1][3]) + (e[2][3] + e[3][3]));
 }
 
-__device__ __forceinline__ int gu_ops(const DecArgs &a) { return 2 * (a.map3d ? 1 : a.H / KCH) + 4; }
-__device__ __forceinline__ int dn_ops(const DecArgs &a) { return (a.map3d ? 1 : a.I / KCH) + 2; }
+// Copies.  Code images: one 3-D TMA box per 8 rows and matrix (or one 2-D box
+// per K-chunk where the driver refused the 3-D view), landing as
+// [chunk][8 rows][128 B], swizzled.  Scales and biases: one bulk copy per
+// array for a run of consecutive 8-row units of one expert.
+__device__ __forceinline__ int code_ops(const DecArgs &a, int K) { return a.map3d ? 1 : K / KCH; }
 
-// Gate/up image of one unit: codes [2 matrices][H/256 chunks][8 rows][128 B]
-// (8H bytes) and scales [gate_s, gate_b, up_s, up_b][8 rows][H/64] (H bytes).
-// Issues copy o of the unit (code boxes of both matrices, then 4 scale rows).
-__device__ void gu_op(const DecArgs &a, const LayerW &L, const DecMaps &mp, int o, uint8_t *cdst, uint8_t *sdst,
-                      int e, int r0, uint64_t *bar) {
-  const int H = a.H, nco = a.map3d ? 1 : H / KCH;
-  const int row = e * a.I + r0;
-  if (o < 2 * nco) {
-    const int mat = o / nco, c = o % nco;
-    uint8_t *dst = cdst + mat * 4 * H + c * 1024;
-    const CUtensorMap *map = mat ? &mp.up : &mp.gate;
-    if (a.map3d)
-      ptx::tma_load_3d(dst, map, bar, 0, row, 0);
-    else
-      ptx::tma_load_2d(dst, map, bar, c * 128, row);
-  } else {
-    const int which = o - 2 * nco;  // 0 gate_s, 1 gate_b, 2 up_s, 3 up_b
-    const uint16_t *src = which == 0 ? L.w.gate_s : which == 1 ? L.w.gate_b : which == 2 ? L.w.up_s : L.w.up_b;
-    ptx::bulk_g2s(sdst + which * (H / 4), src + (size_t)row * (H / 64), H / 4, bar);
-  }
+// Gate/up codes of one unit (rows r0 .. r0+7 of expert e): copy o of
+// 2 * code_ops, gate then up; cdst = [2 matrices][K/256 chunks][8][128 B] (8H bytes).
+__device__ void gu_codes(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cdst, int e, int r0, uint64_t *bar) {
+  const int H = a.H, nco = code_ops(a, H), row = e * a.I + r0;
+  const int mat = o / nco, c = o % nco;
+  uint8_t *dst = cdst + mat * 4 * H + c * 1024;
+  const CUtensorMap *map = mat ? &mp.up : &mp.gate;
+  if (a.map3d)
+    ptx::tma_load_3d(dst, map, bar, 0, row, 0);
+  else
+    ptx::tma_load_2d(dst, map, bar, c * 128, row);
 }
 
-// Down image of one (output unit, slot): codes [I/256 chunks][8 rows][128 B]
-// (4I bytes) and scales [down_s, down_b][8 rows][I/64] (I/2 bytes).
-__device__ void dn_op(const DecArgs &a, const LayerW &L, const DecMaps &mp, int o, uint8_t *cdst, uint8_t *sdst,
-                      int e, int n0, uint64_t *bar) {
-  const int I = a.I, nco = a.map3d ? 1 : I / KCH;
+// Array `which` (0 gate_s, 1 gate_b, 2 up_s, 3 up_b) of n units from rows r0
+// of expert e: n * H/4 bytes, [n][8 rows][H/64] bf16.
+__device__ void gu_scales(const DecArgs &a, const LayerW &L, int which, uint8_t *sdst, int e, int r0, int n,
+                          uint64_t *bar) {
+  const int H = a.H;
+  const uint16_t *src = which == 0 ? L.w.gate_s : which == 1 ? L.w.gate_b : which == 2 ? L.w.up_s : L.w.up_b;
+  ptx::bulk_g2s(sdst, src + ((size_t)e * a.I + r0) * (H / 64), n * (H / 4), bar);
+}
+
+// Down codes of one (output unit, slot): rows n0 .. n0+7 of expert e, copy o
+// of code_ops; cdst = [I/256 chunks][8][128 B] (4I bytes).
+__device__ void dn_codes(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cdst, int e, int n0, uint64_t *bar) {
   const int row = e * a.H + n0;
-  if (o < nco) {
-    if (a.map3d)
-      ptx::tma_load_3d(cdst, &mp.down, bar, 0, row, 0);
-    else
-      ptx::tma_load_2d(cdst + o * 1024, &mp.down, bar, o * 128, row);
-  } else {
-    const int which = o - nco;  // 0 down_s, 1 down_b
-    ptx::bulk_g2s(sdst + which * (I / 4), (which ? L.w.down_b : L.w.down_s) + (size_t)row * (I / 64), I / 4, bar);
-  }
+  if (a.map3d)
+    ptx::tma_load_3d(cdst, &mp.down, bar, 0, row, 0);
+  else
+    ptx::tma_load_2d(cdst + o * 1024, &mp.down, bar, o * 128, row);
+}
+
+// Down array `which` (0 down_s, 1 down_b) of n output units from row n0 of
+// expert e: n * I/4 bytes, [n][8 rows][I/64] bf16.
+__device__ void dn_scales(const DecArgs &a, const LayerW &L, int which, uint8_t *sdst, int e, int n0, int n,
+                          uint64_t *bar) {
+  const int I = a.I;
+  ptx::bulk_g2s(sdst, (which ? L.w.down_b : L.w.down_s) + ((size_t)e * a.H + n0) * (I / 64), n * (I / 4), bar);
 }
 
 // Partial gate/up dot products of `nu` unit images against x (padded, in
 // shared memory) into red[(u * nkc + kc) * 16 + r] (r < 8 gate rows, 8 + r up
-// rows).  Warps split the K-chunks first, then the row sets (unit, matrix);
-// with `bars`, unit u is read once bars[u] completes.  Returns false on a
-// timeout.
-__device__ bool gu_compute(const DecArgs &a, const uint8_t *codes, const uint8_t *scales, int nu, uint64_t *bars,
-                           uint32_t parity,
-                           const uint16_t *xs, float *red) {
+// rows).  scales: [4 arrays][ustride units][8 rows][H/64] bf16.  Warps split
+// the K-chunks first, then the row sets (unit, matrix); with `bars`, unit u is
+// read once bars[u] (its codes) and bars[0] (every unit's scales) complete.
+// Returns false on a timeout.
+__device__ bool gu_compute(const DecArgs &a, const uint8_t *codes, const uint8_t *scales, int ustride, int nu,
+                           uint64_t *bars, uint32_t parity, const uint16_t *xs, float *red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   const int H = a.H, nkc = H / KCH, WK = nkc < DWARPS ? nkc : DWARPS, WR = DWARPS / WK;
   const int kg = warp % WK, rg = warp / WK, gpr = H / 64;
@@ -278,10 +285,11 @@ __device__ bool gu_compute(const DecArgs &a, const uint8_t *codes, const uint8_t
   for (int kc = kg; kc < nkc; kc += WK) {
     for (int rs = rg; rs < 2 * nu; rs += WR) {
       const int u = rs >> 1, mat = rs & 1;  // gate (0) or up (1) rows of unit u
-      if (bars && !wait_bar(&bars[u], parity, a.status)) return false;
-      const uint16_t *su = reinterpret_cast<const uint16_t *>(scales + (size_t)u * H) + mat * 16 * gpr;
-      const float d = gemv_chunk(codes + (size_t)u * 8 * H + mat * 4 * H + kc * 1024, su, su + 8 * gpr, gpr,
-                                 4 * kc + q, xs + 4 * kc * XPAD, g, q);
+      if (bars && !(wait_bar(&bars[0], parity, a.status) && wait_bar(&bars[u], parity, a.status))) return false;
+      const uint16_t *sc = reinterpret_cast<const uint16_t *>(scales + (size_t)(2 * mat * ustride + u) * (H / 4));
+      const uint16_t *bi = reinterpret_cast<const uint16_t *>(scales + (size_t)((2 * mat + 1) * ustride + u) * (H / 4));
+      const float d = gemv_chunk(codes + (size_t)u * 8 * H + mat * 4 * H + kc * 1024, sc, bi, gpr, 4 * kc + q,
+                                 xs + 4 * kc * XPAD, g, q);
       if (q == 0) red[(u * nkc + kc) * 16 + mat * 8 + g] = d;
     }
   }
@@ -311,26 +319,20 @@ __device__ void gu_finish(const DecArgs &a, int nu, const float *red, unsigned l
   }
 }
 
-// Top-k of one token by one warp, for E <= 256 keys read from global memory:
+// Top-k of one token by one warp, for E <= 256 keys in shared memory:
 // lane l holds the codes of experts l, l+32, ...  The k-th largest of the 32
 // lane maxima bounds the k-th largest key from below (k distinct keys reach
 // it), so only the keys at or above it -- at most 8k -- are ranked, each
 // against the others.  Same order and tie rule as topk_block.
-__device__ bool topk_warp(const unsigned long long *tkeys, uint32_t ep, int E, int k, unsigned long long *cand,
-                          int32_t *ids, float *w, int32_t *status, uint64_t *tr) {
+__device__ void topk_warp(const float *keys, int E, int k, unsigned long long *cand, int32_t *ids, float *w,
+                          int32_t *status, uint64_t *tr) {
   const int lane = threadIdx.x & 31;
   auto mark = [&](int slot) {
     if (tr && lane == 0) tr[slot] = ptx::globaltimer();
   };
-  int idx[8];
-  unsigned long long kw[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) idx[i] = lane + 32 * i < E ? lane + 32 * i : -1;
-  const bool got = __all_sync(0xffffffffu, poll_tagged(tkeys, idx, kw, ep, status));
-  if (!got) return false;
   float kv[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) kv[i] = __uint_as_float((uint32_t)kw[i]);
+  for (int i = 0; i < 8; ++i) kv[i] = lane + 32 * i < E ? keys[lane + 32 * i] : 0.f;
   unsigned long long c[8], m = 0ull;
   mark(18);
 #pragma unroll
@@ -382,7 +384,6 @@ __device__ bool topk_warp(const unsigned long long *tkeys, uint32_t ep, int E, i
   topk_finish(lane, k, my_id, my_key, ids, w, nullptr, status);
   __syncwarp();
   mark(21);
-  return true;
 }
 
 // Top-k of one token by all threads of the CTA.  Codes (topk_code) order the
@@ -482,8 +483,14 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   const int nsu = (cta < a.n_su) ? (a.n_su - 1 - cta) / G + 1 : 0;  // shared gate/up units of this CTA
   const int rc = cta - a.rp_cta0;                                    // index among the router CTAs
   const int nre = (rc >= 0 && rc < a.rp_ctas && rc < E) ? (E - 1 - rc) / a.rp_ctas + 1 : 0;  // router rows
-  const int nru = (cta < a.n_ru) ? (a.n_ru - 1 - cta) / G + 1 : 0;  // routed gate/up units
-  const int nou = (cta < a.n_ou) ? (a.n_ou - 1 - cta) / G + 1 : 0;  // output units
+  // Routed gate/up units: a run of consecutive units per CTA (so that one
+  // copy per array brings a run's scales), the CTAs counted from the first one
+  // without a shared unit, so that those take the extra units.
+  const int rcta = (cta + G - a.n_su % G) % G;
+  const int nru = a.n_ru / G + (rcta < a.n_ru % G), u0 = rcta * (a.n_ru / G) + min(rcta, a.n_ru % G);
+  // output units: a run of consecutive 8-row units, rows o0 ..
+  const int nou = a.n_ou / G + (cta < a.n_ou % G);
+  const int o0 = 8 * (cta * (a.n_ou / G) + min(cta, a.n_ou % G));
   const int upr = I / 8;
   // copies are issued by the first two lanes of every warp: one warp alone issues slowly
   const int issuer = lane < 2 ? warp * 2 + lane : -1;
@@ -500,11 +507,15 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   auto issue_p1 = [&](int l) {
     const LayerW &L = a.lw[l];
     if (issuer >= 0) {
-      const int ngu = gu_ops(a), n1 = nsu * ngu, n2 = n1 + nre;
+      const int ngu = 2 * code_ops(a, H) + 4, n1 = nsu * ngu, n2 = n1 + nre;
       for (int o = issuer; o < n2; o += 2 * DWARPS) {
         if (o < n1) {
-          const int i = o / ngu;
-          gu_op(a, L, a.maps[l], o % ngu, su + i * 8 * H, sus + i * H, E, (cta + i * G) * 8, bar_p1);
+          const int i = o / ngu, c = o % ngu;
+          if (c < ngu - 4)
+            gu_codes(a, a.maps[l], c, su + i * 8 * H, E, (cta + i * G) * 8, bar_p1);
+          else
+            gu_scales(a, L, c - (ngu - 4), sus + ((c - (ngu - 4)) * a.max_su + i) * (H / 4), E, (cta + i * G) * 8, 1,
+                      bar_p1);
         } else {
           const int i = o - n1;
           ptx::bulk_g2s(rr + i * H, L.router + (size_t)(rc + i * a.rp_ctas) * H, 4 * H, bar_p1);
@@ -512,13 +523,19 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       }
     }
   };
+  // down scales: [NS slots][2 arrays][max_ou units][8 rows][I/64] bf16
+  auto dn_sc = [&](int j, int which) { return ds + ((j * 2 + which) * a.max_ou) * (I / 4); };
   auto issue_dsh = [&](int l) {
     if (issuer >= 0 && S) {
-      const int ndn = dn_ops(a);
-      for (int o = issuer; o < nou * ndn; o += 2 * DWARPS) {
-        const int ol = o / ndn;
-        dn_op(a, a.lw[l], a.maps[l], o % ndn, dc + (ol * NS + k) * 4 * I, ds + (ol * NS + k) * (I / 2), E,
-              (cta + ol * G) * 8, bar_dsh);
+      const int ndn = code_ops(a, I);
+      for (int o = issuer; o < nou * ndn + 2; o += 2 * DWARPS) {
+        if (o < nou * ndn) {
+          const int ol = o / ndn;
+          dn_codes(a, a.maps[l], o % ndn, dc + (ol * NS + k) * 4 * I, E, o0 + ol * 8, bar_dsh);
+        } else {
+          const int which = o - nou * ndn;
+          dn_scales(a, a.lw[l], which, dn_sc(k, which), E, o0, nou, bar_dsh);
+        }
       }
     }
   };
@@ -552,7 +569,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   // the residual of this CTA's output rows: read once; later layers keep
   // their own output, which is the next layer's residual
   float res_v = 0.f;
-  if (tid < nou * 8) res_v = bf16_to_f32(a.res[(cta + (tid >> 3) * G) * 8 + (tid & 7)]);
+  if (tid < nou * 8) res_v = bf16_to_f32(a.res[o0 + tid]);
   __syncthreads();
   const uint32_t ep0 = s_ep0;
   bool ok = true;
@@ -665,7 +682,8 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         }
       }
     trace(5, l);
-    if (ok && nsu > 0) ok = gu_compute(a, su, sus, nsu, nullptr, 0u, xs, red);
+    // the shared expert's units (CTAs without router rows)
+    if (ok && nsu > 0) ok = gu_compute(a, su, sus, a.max_su, nsu, nullptr, 0u, xs, red);
     ok = __syncthreads_and(ok) != 0;  // every flag below stays uniform across the CTA
     if (!ok) break;
     if (nsu > 0)
@@ -683,27 +701,30 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     trace(7, l);
 
     // -------------------------------------------------------------- P2: routing, routed gate/up
-    bool got = true;
-    if (E <= 256) {
-      if (warp == 0)
-        got = topk_warp(tk, ep, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand), s_ids, s_w, a.status,
-                        trace0 && l == a.nl - 1 && cta < MOE_TRACE_CTAS ? a.trace + cta * MOE_TRACE_SLOTS : nullptr);
-    } else {
-      for (int e = tid; e < E; e += DTHREADS) {
-        const int idx[1] = {e};
-        unsigned long long w[1];
-        got = poll_tagged(tk, idx, w, ep, a.status) && got;
-        keys[e] = __uint_as_float((uint32_t)w[0]);
-      }
-      if (__syncthreads_and(got))
-        topk_block(keys, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand),
-                   reinterpret_cast<unsigned long long *>(sm + a.off_gmax), s_ids, s_w, a.status);
+    // the keys: every thread polls a word or two (many pollers with few words
+    // each see the last store sooner than a few pollers with many)
+    bool got;
+    {
+      const int idx[2] = {tid < E ? tid : -1, tid + DTHREADS < E ? tid + DTHREADS : -1};
+      unsigned long long w[2];
+      got = poll_tagged(tk, idx, w, ep, a.status);
+      if (tid < E) keys[tid] = __uint_as_float((uint32_t)w[0]);
+      if (tid + DTHREADS < E) keys[tid + DTHREADS] = __uint_as_float((uint32_t)w[1]);
     }
     ok = __syncthreads_and(got) != 0;
     if (!ok) break;
+    if (E <= 256) {
+      if (warp == 0)
+        topk_warp(keys, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand), s_ids, s_w, a.status,
+                  trace0 && l == a.nl - 1 && cta < MOE_TRACE_CTAS ? a.trace + cta * MOE_TRACE_SLOTS : nullptr);
+    } else {
+      topk_block(keys, E, k, reinterpret_cast<unsigned long long *>(sm + a.off_cand),
+                 reinterpret_cast<unsigned long long *>(sm + a.off_gmax), s_ids, s_w, a.status);
+    }
     ptx::fence_proxy_async_smem();  // the routed buffers were last read by generic loads
     if (tid == 0) {
-      for (int i = 0; i < nru; ++i) expect_tx(&bar_ru[i], (uint32_t)(9 * H));
+      // unit 0's barrier also takes every unit's scales
+      for (int i = 0; i < nru; ++i) expect_tx(&bar_ru[i], (uint32_t)(8 * H + (i ? 0 : nru * H)));
       expect_tx(bar_drt, (uint32_t)(nou * k * (4 * I + I / 2)));
     }
     __syncthreads();
@@ -713,27 +734,43 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       a.topk_w[tid] = s_w[tid];
     }
     n_drt = l + 1;
-    if (issuer >= 0) {
-      const int ngu = gu_ops(a), ndn = dn_ops(a);
-      const int n1 = nru * ngu, n2 = n1 + nou * k * ndn;
-      for (int o = issuer; o < n2; o += 2 * DWARPS) {
-        if (o < n1) {
-          const int i = o / ngu, u = cta + i * G;
-          gu_op(a, L, a.maps[l], o % ngu, ru + i * 8 * H, rus + i * H, s_ids[u / upr], (u % upr) * 8, &bar_ru[i]);
+    // the gate/up rows first (a block barrier keeps the down rows behind them
+    // in the copy engine's queue): the scales of the unit run (one or two runs
+    // of one slot each), then the code images unit by unit
+    if (issuer >= 0 && nru > 0) {
+      const int ua = u0, ub = min(u0 + nru, (u0 / upr + 1) * upr), uc = u0 + nru;  // runs [ua,ub) [ub,uc)
+      const int nseg = ub < uc ? 2 : 1, ngc = 2 * code_ops(a, H);
+      for (int o = issuer; o < 4 * nseg + nru * ngc; o += 2 * DWARPS) {
+        if (o < 4 * nseg) {
+          const int sg = o >> 2, which = o & 3, f = sg ? ub : ua, n = sg ? uc - ub : ub - ua;
+          gu_scales(a, L, which, rus + (which * a.max_ru + (f - u0)) * (H / 4), s_ids[f / upr], (f % upr) * 8, n,
+                    &bar_ru[0]);
         } else {
-          const int b = (o - n1) / ndn, ol = b / k, j = b % k;
-          dn_op(a, L, a.maps[l], (o - n1) % ndn, dc + (ol * NS + j) * 4 * I, ds + (ol * NS + j) * (I / 2), s_ids[j],
-                (cta + ol * G) * 8, bar_drt);
+          const int i = (o - 4 * nseg) / ngc, u = u0 + i;
+          gu_codes(a, a.maps[l], (o - 4 * nseg) % ngc, ru + i * 8 * H, s_ids[u / upr], (u % upr) * 8, &bar_ru[i]);
+        }
+      }
+    }
+    __syncthreads();
+    if (issuer >= 0) {  // routed down rows: code images per (unit, slot), scales per (slot, array)
+      const int ndn = code_ops(a, I), nc = nou * k * ndn;
+      for (int o = issuer; o < nc + 2 * k; o += 2 * DWARPS) {
+        if (o < nc) {
+          const int b = o / ndn, ol = b / k, j = b % k;
+          dn_codes(a, a.maps[l], o % ndn, dc + (ol * NS + j) * 4 * I, s_ids[j], o0 + ol * 8, bar_drt);
+        } else {
+          const int j = (o - nc) >> 1, which = (o - nc) & 1;
+          dn_scales(a, L, which, dn_sc(j, which), s_ids[j], o0, nou, bar_drt);
         }
       }
     }
     trace(9, l);
-    ok = __syncthreads_and(gu_compute(a, ru, rus, nru, bar_ru, ph, xs, red)) != 0;
+    ok = __syncthreads_and(gu_compute(a, ru, rus, a.max_ru, nru, bar_ru, ph, xs, red)) != 0;
     trace(10, l);
     if (!ok) break;
     if (nru > 0)
       gu_finish(a, nru, red, thb, ep, [&](int u) {
-        const int uu = cta + u * G;
+        const int uu = u0 + u;
         return (size_t)(uu / upr) * I + (size_t)(uu % upr) * 8;
       });
     trace(11, l);
@@ -762,7 +799,9 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         }
       }
       trace(12, l);
-      ok = __syncthreads_and(got && wait_bar(bar_dsh, ph, a.status) && wait_bar(bar_drt, ph, a.status)) != 0;
+      got = got && wait_bar(bar_drt, ph, a.status);
+      trace(13, l);
+      ok = __syncthreads_and(got && wait_bar(bar_dsh, ph, a.status)) != 0;
       trace(14, l);
       if (!ok) break;
     }
@@ -771,8 +810,9 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       const int nitem = nou * NS * nkcd;
       for (int t = warp; t < nitem; t += DWARPS) {
         const int kc = t % nkcd, j = (t / nkcd) % NS, ol = t / (nkcd * NS);
-        const uint16_t *sc = reinterpret_cast<const uint16_t *>(ds + (ol * NS + j) * (I / 2));
-        const float d = gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, sc, sc + 8 * gpr, gpr, 4 * kc + q,
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(dn_sc(j, 0) + ol * (I / 4));
+        const uint16_t *bi = reinterpret_cast<const uint16_t *>(dn_sc(j, 1) + ol * (I / 4));
+        const float d = gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, sc, bi, gpr, 4 * kc + q,
                                    hs + (j * (I / 64) + 4 * kc) * XPAD, g, q);
         if (q == 0) red[t * 8 + g] = d;
       }
@@ -799,7 +839,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       // next epoch's tagged words (row pairs)
       if (warp == 0) {
         uint32_t ob = 0u;
-        const int n = (cta + (tid >> 3) * G) * 8 + (tid & 7);
+        const int n = o0 + tid;
         if (tid < nou * 8) {
           const float *yr = ys + tid * NS;
           float o = res_v;
@@ -854,6 +894,9 @@ DecPlan make_plan(int H, int E, int k, int I, int S, int num_sms) {
   const int max_re = (E + a.rp_ctas - 1) / a.rp_ctas;
   const int max_ru = (a.n_ru + G - 1) / G;
   const int max_ou = (a.n_ou + G - 1) / G;
+  a.max_su = max_su > 0 ? max_su : 1;
+  a.max_ru = max_ru;
+  a.max_ou = max_ou;
   const int nkc = H / KCH, nkcd = I / KCH;
   auto al = [](int v, int m) { return (v + m - 1) / m * m; };
   int o = 0;

@@ -414,6 +414,29 @@ def test_decode_stack_tiny_dims_spans_launches():
     assert_outputs_close(out, ref, "stack layer 9", k=d["k"])
 
 
+def test_decode_stack_repeated_tokens_seven_layers(real):
+    # one full launch (7 layers) per token, several tokens in a row on one
+    # workspace: the tagged exchange must hand every launch its own values
+    W0, _ = real
+    Ws = [W0]
+    for seed in range(1, 7):
+        W = syn.experts(seed, 257, 2048, 512)
+        W["router"] = syn.router(seed, 256, 2048)
+        Ws.append(W)
+    Wds = [dev_weights(W) for W in Ws]
+    L = Layer(max_tokens=1, flags=moe.MOE_FLAG_PRENORM)
+    Ls = Layer(max_tokens=1)
+    for t in range(6):
+        r = syn.activations(500 + t, 1, 2048, tensor=syn.T_RESID)
+        seq, rs = dev(r), dev(r)
+        for Wd in Wds:
+            moe.moe_forward(L.plan, seq, None, 1, Wd, None, seq, L.ws)
+        moe.moe_decode_stack(Ls.plan, rs, Wds, None, Ls.ws)
+        torch.cuda.synchronize()
+        assert L.status() == 0 and Ls.status() == 0, f"token {t}"
+        np.testing.assert_array_equal(host_u16(rs), host_u16(seq), err_msg=f"token {t}")
+
+
 def test_decode_stack_single_layer(real):
     W, _ = real
     r = syn.activations(91, 1, 2048, tensor=syn.T_RESID)
