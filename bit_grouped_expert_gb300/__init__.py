@@ -75,7 +75,8 @@ class moe_route_ptrs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("keys_d", "topk_id_d", "topk_w_d", "counts_d", "offsets_d", "perm_d",
                                                "inv_d", "blockmap_d", "n_tiles_d", "h_d", "y_d", "status_d",
                                                "trace_d")] + \
-               [("max_tiles", ctypes.c_int32), ("block_rows", ctypes.c_int32)]
+               [("max_tiles", ctypes.c_int32), ("block_rows", ctypes.c_int32), ("blockmap2_d", ctypes.c_void_p),
+                ("n_tiles2_d", ctypes.c_void_p), ("max_tiles2", ctypes.c_int32), ("block_rows2", ctypes.c_int32)]
 
 
 _lib = None

@@ -13,8 +13,8 @@ namespace moe {
 struct Layout {
   // status, counter (the decode epoch) and dtags (the decode kernel's tagged
   // exchange words) lie below keys: moe_workspace_init zeroes [0, keys)
-  size_t status, counter, dtags, keys, topk_id, topk_w, counts, offsets, perm, inv, blockmap, n_tiles, h, y, rsplit,
-      xn, trace, total;
+  size_t status, counter, dtags, keys, topk_id, topk_w, counts, offsets, perm, inv, blockmap, n_tiles, blockmap2,
+      n_tiles2, h, y, rsplit, xn, trace, total;
 };
 
 }  // namespace moe
@@ -25,6 +25,8 @@ struct moe_plan {
   uint32_t flags;
   int32_t block_rows;  // rows per block-map tile
   int32_t max_tiles;
+  int32_t block_rows2;  // rows per tile of the second block map (tensor-core down GEMM); 0: none
+  int32_t max_tiles2;
   int32_t num_sms;
   bool use_tc;         // tensor-core grouped GEMMs (else the CUDA-core ones)
   bool use_router_tc;  // tensor-core router for T >= ROUTER_TC_MIN_T

@@ -779,44 +779,34 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     // let the next launch in the stream start its prologue and weight copies
     if (l + 1 == a.nl) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     {
-      // h of every slot (tagged pairs, 4 words per 8 values) into padded groups
-      const int nv = NS * I / 8;
-      got = true;
-      for (int i0 = tid; i0 < nv; i0 += 2 * DTHREADS) {
-        const int i1 = i0 + DTHREADS;
-        const int idx[8] = {4 * i0, 4 * i0 + 1, 4 * i0 + 2, 4 * i0 + 3, i1 < nv ? 4 * i1 : -1,
-                            i1 < nv ? 4 * i1 + 1 : -1, i1 < nv ? 4 * i1 + 2 : -1, i1 < nv ? 4 * i1 + 3 : -1};
-        unsigned long long w[8];
-        got = poll_tagged(thb, idx, w, ep, a.status) && got;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int i = r ? i1 : i0;
-          if (i < nv) {
-            const int j = i / (I / 8), c8 = i % (I / 8);
-            *reinterpret_cast<uint4 *>(hs + (j * (I / 64) + (c8 >> 3)) * XPAD + (c8 & 7) * 8) =
-                perm8((uint32_t)w[4 * r], (uint32_t)w[4 * r + 1], (uint32_t)w[4 * r + 2], (uint32_t)w[4 * r + 3]);
-          }
-        }
-      }
-      trace(12, l);
-      got = got && wait_bar(bar_drt, ph, a.status);
-      trace(13, l);
-      ok = __syncthreads_and(got && wait_bar(bar_dsh, ph, a.status)) != 0;
-      trace(14, l);
-      if (!ok) break;
-    }
-    {
+      // Down items (output unit ol, slot j, K-chunk kc) warp by warp: a warp
+      // polls just the 256 h values of its item (tagged pairs, 4 words per
+      // lane) into its own padded buffer and runs the item as soon as they
+      // are there, so slots whose experts finished early do not wait for the
+      // last ones.
       const int nkcd = I / KCH, gpr = I / 64, g = lane >> 2, q = lane & 3;
       const int nitem = nou * NS * nkcd;
-      for (int t = warp; t < nitem; t += DWARPS) {
+      uint16_t *hwb = hs + warp * 4 * XPAD;  // this warp's 4 padded groups
+      bool gotw = wait_bar(bar_drt, ph, a.status) && wait_bar(bar_dsh, ph, a.status);
+      trace(12, l);
+      for (int t = warp; t < nitem && __all_sync(0xffffffffu, gotw); t += DWARPS) {
         const int kc = t % nkcd, j = (t / nkcd) % NS, ol = t / (nkcd * NS);
+        const int w0 = (j * I + kc * KCH) / 2 + 4 * lane;  // words of values 8*lane .. +7 of the chunk
+        const int idx[4] = {w0, w0 + 1, w0 + 2, w0 + 3};
+        unsigned long long w[4];
+        gotw = poll_tagged(thb, idx, w, ep, a.status);
+        if (!__all_sync(0xffffffffu, gotw)) break;
+        *reinterpret_cast<uint4 *>(hwb + (lane >> 3) * XPAD + (lane & 7) * 8) =
+            perm8((uint32_t)w[0], (uint32_t)w[1], (uint32_t)w[2], (uint32_t)w[3]);
+        __syncwarp();
         const uint16_t *sc = reinterpret_cast<const uint16_t *>(dn_sc(j, 0) + ol * (I / 4));
         const uint16_t *bi = reinterpret_cast<const uint16_t *>(dn_sc(j, 1) + ol * (I / 4));
-        const float d = gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, sc, bi, gpr, 4 * kc + q,
-                                   hs + (j * (I / 64) + 4 * kc) * XPAD, g, q);
+        const float d = gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, sc, bi, gpr, 4 * kc + q, hwb, g, q);
         if (q == 0) red[t * 8 + g] = d;
+        __syncwarp();  // every lane has read the buffer before the next item overwrites it
       }
-      __syncthreads();
+      ok = __syncthreads_and(gotw) != 0;
+      if (!ok) break;
       trace(15, l);
       // the next layer's shared down rows, into the slots just read
       if (l + 1 < a.nl) {
@@ -912,8 +902,8 @@ DecPlan make_plan(int H, int E, int k, int I, int S, int num_sms) {
   o = al(o + (H / 64) * XPAD * 2, 128);
   a.off_xn = o;
   o = al(o + H * 2, 128);
-  a.off_h = o;
-  o = al(o + NS * (I / 64) * XPAD * 2, 128);
+  a.off_h = o;  // per-warp down buffers: 4 padded groups (one K-chunk of h) each
+  o = al(o + DWARPS * 4 * XPAD * 2, 128);
   a.off_ds = o;
   o = al(o + max_ou * NS * (I / 2), 128);
   a.off_rus = o;

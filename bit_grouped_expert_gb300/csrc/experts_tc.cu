@@ -41,8 +41,6 @@ constexpr int KBLK = 64;        // k-block = one quantisation group
 constexpr int STAGE_KB = 4;     // k-blocks per code stage (one TMA box per matrix)
 constexpr int BOX = BM * 128;   // one TMA box: 128 rows x 128 bytes (256 codes)
 constexpr int NSLOT = 4;        // A slots in tensor memory (64 columns each)
-constexpr int MAXN = 128;       // token rows per work item
-constexpr int B_SLOT = MAXN * 128;
 constexpr int NWG = 3;                    // dequant/epilogue warpgroups
 constexpr int THREADS = 128 + NWG * 128;  // 4 role warps + the warpgroups
 constexpr uint32_t TMEM_COLS = 512;
@@ -55,11 +53,16 @@ constexpr int SBOX = BM * 16;  // one scale (or bias) box: 128 rows x 8 groups o
 template <bool GATEUP>
 struct Cfg {
   static constexpr int NMAT = GATEUP ? 2 : 1;
+  // Token rows per work item (the MMA's N).  Gate and up keep two fp32
+  // accumulators of N columns next to the A slots in tensor memory, so N <=
+  // 128; the down GEMM has one accumulator and takes N <= 256.
+  static constexpr int MAXN = GATEUP ? 128 : 256;
+  static constexpr int B_SLOT = MAXN * 128;  // one k-block of MAXN token rows
   // Code stages (4 k-blocks each, from HBM) and token-row slots (1 k-block
   // each, mostly from L2) share the shared memory; the token rows get the
   // deeper ring, since every k-block's MMA waits on them.
-  static constexpr int CSTAGES = GATEUP ? 3 : 4;
-  static constexpr int NBSLOT = GATEUP ? 6 : 8;
+  static constexpr int CSTAGES = 3;
+  static constexpr int NBSLOT = GATEUP ? 6 : 5;
   // per stage: codes of each matrix, then (scale, bias) boxes of each matrix
   static constexpr int STAGE_BYTES = NMAT * BOX + NMAT * 2 * SBOX;
   static constexpr int OFF_B = CSTAGES * STAGE_BYTES;
@@ -75,6 +78,9 @@ struct TcMaps {
   CUtensorMap code[2];
   CUtensorMap sc[2];
   CUtensorMap bi[2];
+  // down GEMM: h as a bf16 tensor [rows][K], 128B-swizzled boxes of one
+  // k-block (64 values) x 128 / 64 / 32 / 16 rows
+  CUtensorMap act[4];
 };
 
 struct TcArgs {
@@ -99,6 +105,7 @@ struct Item {
   int e, row0, nrows, n_mma, mt;
 };
 
+template <int MAXN>
 __device__ __forceinline__ Item get_item(const TcArgs &a, int item, int MT) {
   const int tile = item / MT;
   Item it;
@@ -176,7 +183,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(&m->code_empty[i], NWG * 4);
     }
     for (int i = 0; i < C::NBSLOT; ++i) {
-      ptx::mbar_init(&m->b_full[i], 64);  // one cp.async-tracked arrival per loader lane (2 warps)
+      // gate/up: one cp.async-tracked arrival per loader lane (2 warps);
+      // down: one arrival with the slot's TMA byte count
+      ptx::mbar_init(&m->b_full[i], GATEUP ? 64 : 1);
       ptx::mbar_init(&m->b_free[i], 1);
     }
     for (int i = 0; i < NSLOT; ++i) {
@@ -211,10 +220,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       uint32_t cs = 0;
       bool ok = true;
-      Item nit = blockIdx.x < n_items ? get_item(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
+      Item nit = blockIdx.x < n_items ? get_item<C::MAXN>(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const Item it = nit;  // the next item's block-map entry is loaded one item ahead
-        if (item + (int)gridDim.x < n_items) nit = get_item(a, item + gridDim.x, MT);
+        if (item + (int)gridDim.x < n_items) nit = get_item<C::MAXN>(a, item + gridDim.x, MT);
         const int row_base = it.e * a.NOUT + it.mt * BM;
         for (int st = 0; st < NST; ++st, ++cs) {
           const int slot = cs % C::CSTAGES;
@@ -250,10 +259,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       uint32_t kbc = 0, itc = 0;
       bool ok = true;
-      Item nit = blockIdx.x < n_items ? get_item(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
+      Item nit = blockIdx.x < n_items ? get_item<C::MAXN>(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const Item it = nit;
-        if (item + (int)gridDim.x < n_items) nit = get_item(a, item + gridDim.x, MT);
+        if (item + (int)gridDim.x < n_items) nit = get_item<C::MAXN>(a, item + gridDim.x, MT);
         const uint32_t idesc = ptx::idesc_bf16_f32((uint32_t)it.n_mma);
         if (!wait_bar(&m->acc_empty, (itc & 1u) ^ 1u, m, a.status)) break;
         ptx::tc_fence_after();
@@ -266,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           ptx::fence_proxy_async_smem();  // token rows were written by cp.async (generic proxy)
           ptx::tc_fence_after();
-          const uint32_t baddr = ptx::smem_u32(smem + C::OFF_B + bslot * B_SLOT);
+          const uint32_t baddr = ptx::smem_u32(smem + C::OFF_B + bslot * C::B_SLOT);
 #pragma unroll
           for (int mat = 0; mat < C::NMAT; ++mat)
 #pragma unroll
@@ -284,7 +293,50 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mma_commit(&m->final_bar);
       drain_wait(&m->final_bar, 0);
     }
-  } else if (warp == 2 || warp == 3) {
+  } else if (!GATEUP && warp == 2) {
+    // ------------------------------------------------------------ token-row TMA (down)
+    // h rows of a tile are contiguous (routed rows in perm order, then the
+    // shared expert's), so each k-block of the tile's n_mma rows arrives in
+    // a few TMA boxes (128 rows at a time, then 64 / 32 / 16), already in the
+    // MMA's 128B-swizzled K-major layout.  Rows past the tile belong to the next
+    // tile (or lie past the tensor and read as zero): they only feed MMA
+    // columns the epilogue never stores.
+    if (lane == 0) {
+      for (int i = 0; i < 4; ++i) ptx::prefetch_tmap(&maps.act[i]);
+      uint32_t kbc = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const Item it = get_item<C::MAXN>(a, item, MT);
+        for (int kb = 0; kb < KB; ++kb, ++kbc) {
+          const int slot = kbc % C::NBSLOT;
+          if (!wait_bar(&m->b_free[slot], ((kbc / C::NBSLOT) & 1u) ^ 1u, m, a.status)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&m->b_full[slot], (uint32_t)it.n_mma * 128u);
+          uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT;
+          int r = 0;
+          for (; it.n_mma - r >= 128; r += 128)
+            ptx::tma_load_2d(bs + r * 128, &maps.act[0], &m->b_full[slot], kb * KBLK, it.row0 + r);
+#pragma unroll
+          for (int i = 1; i < 4; ++i) {
+            const int h = 128 >> i;
+            if (it.n_mma - r >= h) {
+              ptx::tma_load_2d(bs + r * 128, &maps.act[i], &m->b_full[slot], kb * KBLK, it.row0 + r);
+              r += h;
+            }
+          }
+        }
+      }
+      if (!ok) {  // the last slots' loads may still be in flight
+        const uint32_t n = kbc < (uint32_t)C::NBSLOT ? kbc : (uint32_t)C::NBSLOT;
+        for (uint32_t i = 1; i <= n; ++i) {
+          const uint32_t c = kbc - i;
+          drain_wait(&m->b_full[c % C::NBSLOT], (c / C::NBSLOT) & 1u);
+        }
+      }
+    }
+  } else if (GATEUP && (warp == 2 || warp == 3)) {
     // ------------------------------------------------------------ token-row loaders
     // Warps 2 and 3 each copy half of the tile's rows: lane l of loader w owns
     // rows w*4 + l/8 + 8i (i < 16) and 16-byte chunk l%8 of each, so its
@@ -295,14 +347,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t sw = (uint32_t)((c ^ (r0 & 7)) << 4);
     uint32_t kbc = 0;
     bool ok = true;
-    Item nit = blockIdx.x < n_items ? get_item(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
+    Item nit = blockIdx.x < n_items ? get_item<C::MAXN>(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const Item it = nit;
-      if (item + (int)gridDim.x < n_items) nit = get_item(a, item + gridDim.x, MT);
-      uint32_t off[MAXN / 8];
+      if (item + (int)gridDim.x < n_items) nit = get_item<C::MAXN>(a, item + gridDim.x, MT);
+      uint32_t off[C::MAXN / 8];
       uint32_t valid = 0;  // bit i: row r0 + 8i holds a token
 #pragma unroll
-      for (int i = 0; i < MAXN / 8; ++i) {
+      for (int i = 0; i < C::MAXN / 8; ++i) {
         const int r = r0 + 8 * i;
         if (r >= it.n_mma) break;  // rows past the MMA's N are never copied
         int src = -1;
@@ -323,10 +375,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = false;
           break;
         }
-        uint8_t *bs = smem + C::OFF_B + slot * B_SLOT + r0 * 128 + sw;
+        uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT + r0 * 128 + sw;
         const uint32_t kofs = (uint32_t)kb * (KBLK * 2);
 #pragma unroll
-        for (int i = 0; i < MAXN / 8; ++i) {
+        for (int i = 0; i < C::MAXN / 8; ++i) {
           if (r0 + 8 * i >= nr) break;  // small tiles: a few iterations, not sixteen
           ptx::cp_async_16(bs + i * 1024, act + off[i] + kofs, ((valid >> i) & 1u) ? 16u : 0u);
         }
@@ -348,8 +400,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // scales/biases of the next stage are loaded one stage ahead; block-map
     // entries two items ahead
     int nitem = blockIdx.x;
-    Item nit = nitem < n_items ? get_item(a, nitem, MT) : Item{0, 0, 0, 16, 0};
-    Item nit2 = nitem + (int)gridDim.x < n_items ? get_item(a, nitem + gridDim.x, MT) : Item{0, 0, 0, 16, 0};
+    Item nit = nitem < n_items ? get_item<C::MAXN>(a, nitem, MT) : Item{0, 0, 0, 16, 0};
+    Item nit2 = nitem + (int)gridDim.x < n_items ? get_item<C::MAXN>(a, nitem + gridDim.x, MT) : Item{0, 0, 0, 16, 0};
     int nst = 0;
     uint2 nsv[C::NMAT], nbv[C::NMAT];
     auto prefetch = [&](const Item &pi, int pst) {
@@ -377,7 +429,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           nst = 0;
           nitem += gridDim.x;
           nit = nit2;
-          if (nitem + (int)gridDim.x < n_items) nit2 = get_item(a, nitem + gridDim.x, MT);
+          if (nitem + (int)gridDim.x < n_items) nit2 = get_item<C::MAXN>(a, nitem + gridDim.x, MT);
         }
         if (nitem < n_items && !a.tma_scales) prefetch(nit, nst);
         const int cslot = cs % C::CSTAGES;
@@ -497,6 +549,21 @@ cudaError_t code_map(CUtensorMap *map, const uint32_t *codes, int rows_total, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Activation rows as a 2D bf16 tensor [rows_total][K], boxes of one k-block
+// (64 values, 128 B) x box_rows rows, 128B swizzle (the MMA's K-major layout).
+cudaError_t act_map(CUtensorMap *map, const uint16_t *p, int rows_total, int K, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorInitializationError;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_total};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)KBLK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(p), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -524,7 +591,8 @@ cudaError_t tc_prepare() {
 }
 
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
-                              const int32_t *blockmap, const int32_t *n_tiles, int max_tiles, ExpertPtrs w,
+                              const int32_t *blockmap, const int32_t *n_tiles, int max_tiles,
+                              const int32_t *blockmap2, const int32_t *n_tiles2, int max_tiles2, ExpertPtrs w,
                               uint16_t *h, uint16_t *y, int32_t *status, int *launches, cudaStream_t s) {
   const moe_config &c = plan->cfg;
   const int rows_gu = (c.n_experts + c.n_shared) * c.inter;
@@ -545,6 +613,10 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
     if ((e = group_map(&md.sc[0], w.down_s, rows_dn, c.inter)) != cudaSuccess) return e;
     if ((e = group_map(&md.bi[0], w.down_b, rows_dn, c.inter)) != cudaSuccess) return e;
   }
+  // h: the routed rows (k per token) then the shared expert's (n_shared per token)
+  const int rows_h = (c.top_k + c.n_shared) * T;
+  for (int i = 0; i < 4; ++i)
+    if ((e = act_map(&md.act[i], h, rows_h, c.inter, BM >> i)) != cudaSuccess) return e;
 
   TcArgs a{};
   a.perm = perm;
@@ -572,8 +644,10 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   prof_after(MOE_KERNEL_GATEUP, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  // down: h rows -> y
+  // down: h rows -> y, over the block map of taller tiles
   a.act = h;
+  a.blockmap = blockmap2;
+  a.n_tiles = n_tiles2;
   a.sc[0] = w.down_s;
   a.bi[0] = w.down_b;
   a.sc[1] = w.down_s;
@@ -582,7 +656,7 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.K = c.inter;
   a.NOUT = c.hidden;
   a.tma_scales = ts_dn;
-  items = max_tiles * (c.hidden / BM);
+  items = max_tiles2 * (c.hidden / BM);
   grid = items < plan->num_sms ? items : plan->num_sms;
   prof_before(MOE_KERNEL_DOWN, s);
   experts_tc_kernel<false><<<grid, THREADS, Cfg<false>::SMEM, s>>>(md, a);

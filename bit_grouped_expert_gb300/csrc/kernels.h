@@ -27,7 +27,8 @@ cudaError_t launch_topk(const float *keys, int T, int E, int k, int32_t *topk_id
                         int32_t *status, cudaStream_t s);
 cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, int S, const int32_t *counts,
                            int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *blockmap, int32_t *n_tiles,
-                           int max_tiles, int32_t *status, int debug, cudaStream_t s);
+                           int max_tiles, int BN2, int32_t *blockmap2, int32_t *n_tiles2, int max_tiles2,
+                           int32_t *status, int debug, cudaStream_t s);
 
 // experts_simt.cu (CUDA-core grouped GEMMs, tiles of SIMT_ROWS rows)
 constexpr int SIMT_ROWS = 32;

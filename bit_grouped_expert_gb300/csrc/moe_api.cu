@@ -33,7 +33,7 @@ int tiles_bound(int T, int k, int E, int S, int BN) {
   return (k * T + BN - 1) / BN + E + (S ? (T + BN - 1) / BN : 0);
 }
 
-moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles) {
+moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_tiles2) {
   moe::Layout L;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -54,6 +54,8 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles) {
   L.inv = take(k * T * 4);
   L.blockmap = take((size_t)max_tiles * 16);
   L.n_tiles = take(16);
+  L.blockmap2 = take((size_t)max_tiles2 * 16);
+  L.n_tiles2 = take(16);
   L.h = take((k + S) * T * I * 2);
   L.y = take((k + S) * T * H * 2);
   L.rsplit = take(3 * E * H * 2);
@@ -134,11 +136,14 @@ moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const fl
     return cuda_status(err);
   ++*launches;
   const int max_tiles = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, p->block_rows);
+  const int max_tiles2 = p->block_rows2 ? tiles_bound(T, c.top_k, c.n_experts, c.n_shared, p->block_rows2) : 0;
   if ((err = moe::launch_scatter(moe::ws_ptr<int32_t>(ws, L.topk_id), T, c.n_experts, c.top_k, p->block_rows,
                                  c.n_shared, counts, moe::ws_ptr<int32_t>(ws, L.offsets),
                                  moe::ws_ptr<int32_t>(ws, L.perm), moe::ws_ptr<int32_t>(ws, L.inv),
                                  moe::ws_ptr<int32_t>(ws, L.blockmap), moe::ws_ptr<int32_t>(ws, L.n_tiles), max_tiles,
-                                 status, (p->flags & MOE_FLAG_DEBUG_CHECKS) ? 1 : 0, s)) != cudaSuccess)
+                                 p->block_rows2, p->block_rows2 ? moe::ws_ptr<int32_t>(ws, L.blockmap2) : nullptr,
+                                 moe::ws_ptr<int32_t>(ws, L.n_tiles2), max_tiles2, status,
+                                 (p->flags & MOE_FLAG_DEBUG_CHECKS) ? 1 : 0, s)) != cudaSuccess)
     return cuda_status(err);
   ++*launches;
   return MOE_OK;
@@ -250,7 +255,10 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
   p->use_tc = !simt;
   p->block_rows = simt ? moe::SIMT_ROWS : ((flags & MOE_FLAG_TILE_ROWS_64) ? 64 : moe::TC_ROWS);
   p->max_tiles = tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows);
-  p->lay = make_layout(c, max_tokens, p->max_tiles);
+  // the tensor-core down GEMM takes tiles of up to TC_DOWN_ROWS rows
+  p->block_rows2 = simt ? 0 : ((flags & MOE_FLAG_TILE_ROWS_64) ? 64 : moe::TC_DOWN_ROWS);
+  p->max_tiles2 = p->block_rows2 ? tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows2) : 0;
+  p->lay = make_layout(c, max_tokens, p->max_tiles, p->max_tiles2);
   p->num_sms = 0;
   p->use_router_tc = false;
   p->use_decode = false;
@@ -263,7 +271,9 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
       p->use_tc = false;  // no tensor-core kernels on this device: CUDA-core path
       p->block_rows = moe::SIMT_ROWS;
       p->max_tiles = tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows);
-      p->lay = make_layout(c, max_tokens, p->max_tiles);
+      p->block_rows2 = 0;
+      p->max_tiles2 = 0;
+      p->lay = make_layout(c, max_tokens, p->max_tiles, p->max_tiles2);
     }
     if (p->num_sms > 0 &&
         moe::decode_supported(c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, p->num_sms)) {
@@ -387,7 +397,9 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
     if (err != cudaSuccess) return cuda_status(err);
     launches += 2;
   } else {
-    err = moe::launch_experts_tc(plan, x, T, perm, bm, nt, max_tiles, ep, h, y, status, &launches, s);
+    const int max_tiles2 = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, plan->block_rows2);
+    err = moe::launch_experts_tc(plan, x, T, perm, bm, nt, max_tiles, moe::ws_ptr<int32_t>(ws_d, L.blockmap2),
+                                 moe::ws_ptr<int32_t>(ws_d, L.n_tiles2), max_tiles2, ep, h, y, status, &launches, s);
     if (err != cudaSuccess) return cuda_status(err);
   }
   err = moe::launch_combine(res, y, moe::ws_ptr<int32_t>(ws_d, L.inv), moe::ws_ptr<float>(ws_d, L.topk_w), T,
@@ -448,6 +460,12 @@ moe_status moe_route_view(const moe_plan_t *plan, void *ws_d, int32_t T, moe_rou
   out->trace_d = moe::ws_ptr<uint64_t>(ws_d, L.trace);
   out->max_tiles = tiles_bound(T, plan->cfg.top_k, plan->cfg.n_experts, plan->cfg.n_shared, plan->block_rows);
   out->block_rows = plan->block_rows;
+  out->blockmap2_d = moe::ws_ptr<int32_t>(ws_d, L.blockmap2);
+  out->n_tiles2_d = moe::ws_ptr<int32_t>(ws_d, L.n_tiles2);
+  out->max_tiles2 =
+      plan->block_rows2 ? tiles_bound(T, plan->cfg.top_k, plan->cfg.n_experts, plan->cfg.n_shared, plan->block_rows2)
+                        : 0;
+  out->block_rows2 = plan->block_rows2;
   return MOE_OK;
 }
 

@@ -87,67 +87,78 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t *__restrict_
                                                       int BN, int S, const int32_t *__restrict__ counts,
                                                       int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
                                                       int32_t *__restrict__ inv, int32_t *__restrict__ blockmap,
-                                                      int32_t *__restrict__ n_tiles, int max_tiles,
-                                                      int32_t *__restrict__ status, int debug) {
-  __shared__ int s_a[32], s_b[32];
+                                                      int32_t *__restrict__ n_tiles, int max_tiles, int BN2,
+                                                      int32_t *__restrict__ blockmap2, int32_t *__restrict__ n_tiles2,
+                                                      int max_tiles2, int32_t *__restrict__ status, int debug) {
+  __shared__ int s_a[32], s_b[32], s_c[32];
   __shared__ int s_warp[8];
-  __shared__ int s_off, s_tb;
+  __shared__ int s_off, s_tb, s_tb2;
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  int off = 0, tb = 0;
+  int off = 0, tb = 0, tb2 = 0;
   for (int i = tid; i < e; i += blockDim.x) {
     int c = counts[i];
     off += c;
     tb += (c + BN - 1) / BN;
+    tb2 += (c + BN2 - 1) / BN2;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     off += __shfl_xor_sync(0xffffffffu, off, o);
     tb += __shfl_xor_sync(0xffffffffu, tb, o);
+    tb2 += __shfl_xor_sync(0xffffffffu, tb2, o);
   }
   if (lane == 0) {
     s_a[wid] = off;
     s_b[wid] = tb;
+    s_c[wid] = tb2;
   }
   __syncthreads();
   if (tid == 0) {
-    int a = 0, b = 0;
+    int a = 0, b = 0, c = 0;
     for (int w = 0; w < (int)(blockDim.x / 32); ++w) {
       a += s_a[w];
       b += s_b[w];
+      c += s_c[w];
     }
     s_off = a;
     s_tb = b;
+    s_tb2 = c;
   }
   __syncthreads();
   off = s_off;
   tb = s_tb;
+  tb2 = s_tb2;
   const int ce = counts[e];
-  const int ntile_e = (ce + BN - 1) / BN;
-  if (tid == 0) offsets[e] = off;
-  if (e == E - 1) {
-    const int routed_tiles = tb + ntile_e;
-    const int shared_tiles = S ? (T + BN - 1) / BN : 0;
-    if (tid == 0) {
-      offsets[E] = off + ce;
-      *n_tiles = routed_tiles + shared_tiles;
-      if (debug && (off + ce != k * T || routed_tiles + shared_tiles > max_tiles))
-        set_status(status, MOE_ERR_DEVICE_BOUNDS);
-    }
-    for (int s = tid; s < shared_tiles; s += blockDim.x) {
-      int idx = routed_tiles + s;
-      if (idx < max_tiles) {
-        int4 ent = make_int4(E, k * T + s * BN, min(BN, T - s * BN), 0);
-        reinterpret_cast<int4 *>(blockmap)[idx] = ent;
+  // one block map per tile height: rows of BN (and, when blockmap2 is given, of BN2)
+  auto write_map = [&](int32_t *map, int32_t *nt, int mt, int bn, int tbase) {
+    const int ntile_e = (ce + bn - 1) / bn;
+    if (e == E - 1) {
+      const int routed_tiles = tbase + ntile_e;
+      const int shared_tiles = S ? (T + bn - 1) / bn : 0;
+      if (tid == 0) {
+        *nt = routed_tiles + shared_tiles;
+        if (debug && (off + ce != k * T || routed_tiles + shared_tiles > mt)) set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      }
+      for (int s = tid; s < shared_tiles; s += blockDim.x) {
+        int idx = routed_tiles + s;
+        if (idx < mt) {
+          int4 ent = make_int4(E, k * T + s * bn, min(bn, T - s * bn), 0);
+          reinterpret_cast<int4 *>(map)[idx] = ent;
+        }
       }
     }
-  }
-  for (int r = tid; r < ntile_e; r += blockDim.x) {
-    int idx = tb + r;
-    if (idx < max_tiles) {
-      int4 ent = make_int4(e, off + r * BN, min(BN, ce - r * BN), 0);
-      reinterpret_cast<int4 *>(blockmap)[idx] = ent;
+    for (int r = tid; r < ntile_e; r += blockDim.x) {
+      int idx = tbase + r;
+      if (idx < mt) {
+        int4 ent = make_int4(e, off + r * bn, min(bn, ce - r * bn), 0);
+        reinterpret_cast<int4 *>(map)[idx] = ent;
+      }
     }
-  }
+  };
+  if (tid == 0) offsets[e] = off;
+  if (e == E - 1 && tid == 0) offsets[E] = off + ce;
+  write_map(blockmap, n_tiles, max_tiles, BN, tb);
+  if (blockmap2) write_map(blockmap2, n_tiles2, max_tiles2, BN2, tb2);
   if (ce == 0) return;
   int running = 0;
   for (int t0 = 0; t0 < T; t0 += blockDim.x) {
@@ -220,10 +231,12 @@ cudaError_t launch_topk(const float *keys, int T, int E, int k, int32_t *topk_id
 
 cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, int S, const int32_t *counts,
                            int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *blockmap, int32_t *n_tiles,
-                           int max_tiles, int32_t *status, int debug, cudaStream_t s) {
+                           int max_tiles, int BN2, int32_t *blockmap2, int32_t *n_tiles2, int max_tiles2,
+                           int32_t *status, int debug, cudaStream_t s) {
+  if (!blockmap2) BN2 = BN;
   prof_before(MOE_KERNEL_SCATTER, s);
   scatter_kernel<<<E, 256, 0, s>>>(topk_id, T, E, k, BN, S, counts, offsets, perm, inv, blockmap, n_tiles, max_tiles,
-                                   status, debug);
+                                   BN2, blockmap2, n_tiles2, max_tiles2, status, debug);
   prof_after(MOE_KERNEL_SCATTER, s);
   return cudaGetLastError();
 }

@@ -10,7 +10,8 @@
 
 namespace moe {
 
-constexpr int TC_ROWS = 128;     // default token rows per block-map tile
+constexpr int TC_ROWS = 128;       // default token rows per block-map tile (gate/up GEMM)
+constexpr int TC_DOWN_ROWS = 256;  // token rows per tile of the down GEMM's block map
 
 // The driver's cuTensorMapEncodeTiled (null when the driver lacks it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
@@ -22,7 +23,8 @@ bool tc_supported(const moe_config &c);
 cudaError_t tc_prepare();
 
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
-                              const int32_t *blockmap, const int32_t *n_tiles, int max_tiles, ExpertPtrs w,
+                              const int32_t *blockmap, const int32_t *n_tiles, int max_tiles,
+                              const int32_t *blockmap2, const int32_t *n_tiles2, int max_tiles2, ExpertPtrs w,
                               uint16_t *h, uint16_t *y, int32_t *status, int *launches, cudaStream_t s);
 
 // Router keys on tensor cores (E % 128 == 0, H % 64 == 0).

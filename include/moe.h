@@ -100,6 +100,11 @@ typedef struct {
   uint64_t *trace_d;   /* [MOE_TRACE_CTAS][MOE_TRACE_SLOTS] phase timestamps (ns), MOE_FLAG_TRACE */
   int32_t max_tiles;   /* capacity of blockmap_d                             */
   int32_t block_rows;  /* rows per block-map tile for this plan              */
+  int32_t *blockmap2_d; /* [max_tiles2][4] the same map with tiles of block_rows2 rows
+                           (tensor-core plans: the down GEMM's tiles); unused otherwise */
+  int32_t *n_tiles2_d;  /* [1] entries in use in blockmap2_d                 */
+  int32_t max_tiles2;   /* capacity of blockmap2_d (0: no second map)         */
+  int32_t block_rows2;  /* rows per tile of blockmap2_d                       */
 } moe_route_ptrs;
 
 /* Plan flags. */

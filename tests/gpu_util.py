@@ -53,6 +53,7 @@ class Layer:
         v = self.view(T)
         E, k = self.E, self.k
         n_tiles = int(self.ws_array(v.n_tiles_d, (1,), torch.int32)[0])
+        n_tiles2 = int(self.ws_array(v.n_tiles2_d, (1,), torch.int32)[0]) if v.block_rows2 else 0
         return {
             "keys": self.ws_array(v.keys_d, (T, E), torch.float32),
             "ids": self.ws_array(v.topk_id_d, (T, k), torch.int32),
@@ -64,6 +65,9 @@ class Layer:
             "n_tiles": n_tiles,
             "blockmap": self.ws_array(v.blockmap_d, (max(n_tiles, 1), 4), torch.int32)[:n_tiles],
             "block_rows": v.block_rows,
+            "n_tiles2": n_tiles2,
+            "blockmap2": self.ws_array(v.blockmap2_d, (max(n_tiles2, 1), 4), torch.int32)[:n_tiles2],
+            "block_rows2": v.block_rows2,
         }
 
     def status(self, reset=True):

@@ -72,6 +72,10 @@ def _assert_routing_equal(got, keys, k, E, S):
     np.testing.assert_array_equal(got["inv"], m["inv"])
     assert got["n_tiles"] == m["n_tiles"]
     np.testing.assert_array_equal(got["blockmap"], m["blockmap"])
+    if got["block_rows2"]:  # the down GEMM's map of taller tiles
+        m2 = orc.route_maps(ids, E, n_shared=S, BN=got["block_rows2"])
+        assert got["n_tiles2"] == m2["n_tiles"]
+        np.testing.assert_array_equal(got["blockmap2"], m2["blockmap"])
 
 
 # ---------------------------------------------------------------- dequant
@@ -128,10 +132,12 @@ def test_routing_bit_exact_given_keys(real, path, T, zipf):
     assert L.status() == 0
 
 
-def test_routing_edge_cases_from_keys():
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_routing_edge_cases_from_keys(path):
     E, k = 16, 4
-    L = Layer(H=256, E=E, k=k, I=256, max_tokens=300, flags=moe.MOE_FLAG_SIMT_EXPERTS)
-    BN = L.view(1).block_rows
+    L = Layer(H=256, E=E, k=k, I=256, max_tokens=520, flags=PATHS[path])
+    v = L.view(1)
+    BN = max(v.block_rows, v.block_rows2)  # groups of BN-1, BN, BN+1 rows in the taller tiles
     rng = np.random.default_rng(3)
     T = 2 * BN + 5
     keys = rng.normal(size=(T, E)).astype(np.float32)
@@ -173,9 +179,12 @@ def test_routing_is_deterministic(real):
 # ---------------------------------------------------------------- layer, tiny dims
 
 def test_default_plan_uses_tensor_core_path():
-    assert Layer(max_tokens=8).view(1).block_rows == 128
-    assert Layer(max_tokens=8, flags=moe.MOE_FLAG_TILE_ROWS_64).view(1).block_rows == 64
-    assert Layer(max_tokens=8, flags=moe.MOE_FLAG_SIMT_EXPERTS).view(1).block_rows == 32
+    v = Layer(max_tokens=8).view(1)
+    assert (v.block_rows, v.block_rows2) == (128, 256)
+    v = Layer(max_tokens=8, flags=moe.MOE_FLAG_TILE_ROWS_64).view(1)
+    assert (v.block_rows, v.block_rows2) == (64, 64)
+    v = Layer(max_tokens=8, flags=moe.MOE_FLAG_SIMT_EXPERTS).view(1)
+    assert (v.block_rows, v.block_rows2) == (32, 0)
 
 
 @pytest.mark.parametrize("T", [1, 5, 64, 129, 300])
@@ -199,7 +208,10 @@ def test_layer_tiny_dims(path, T):
     bias = syn.zipf_bias(T, d["E"])
     L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=300, flags=PATHS[path])
     out = _forward(L, x, Wd, res=res, bias=bias)
-    keys = L.routing(T)["keys"]
+    r = L.routing(T)
+    keys = r["keys"]
+    if T == 300 and path == "tc":  # the skew puts > 128 rows in one down tile (N up to 256)
+        assert (r["blockmap2"][:, 2] > 128).any()
     ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, res=res, keys=keys, intermediates=True)
     assert_outputs_close(out, ref, f"tiny T={T} {path}", k=d["k"])
     assert L.status() == 0
