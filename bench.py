@@ -419,31 +419,40 @@ def run_ours(args, wl, rank, world, device):
 
 # ------------------------------------------------------------------ oracle (CPU)
 
-def oracle_sample(wl, seed, budget_tokens=None):
-    """Run the CPU oracle once on a bounded sample of the workload.  Returns
-    (seconds, units, unit, description)."""
+def oracle_sample(wl, seed, target_s=None):
+    """Run the CPU oracle on a bounded sample of the workload: one token (T=1)
+    or 64 tokens (32 for stacks) through one layer, or, with target_s, as many
+    tokens as take about target_s seconds (at most 256 single tokens, or the
+    workload's T).  Returns (seconds, units, unit, description)."""
     import oracle as orc
     import synthetic as syn
     T = wl["T"]
     d = orc.Dims()
-    if T == 1:
-        n_layers = 1
-        W = syn.experts(seed, E + 1, H, I_DIM, layer=0, centred=wl["centred"])
-        W["router"] = syn.router(seed, E, H, layer=0)
-        x = syn.activations(seed, 1, H)
-        t = time.perf_counter()
-        orc.moe_layer(d, x, W)
-        dt = time.perf_counter() - t
-        units = n_layers * (ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2) / 1e9
-        return dt, units, "GB/s", "1 token through 1 layer (GB of router + 9 experts streamed per second)"
-    n_tok = budget_tokens or (32 if wl["layers"] > 1 else 64)
     W = syn.experts(seed, E + 1, H, I_DIM, layer=0, centred=wl["centred"])
     W["router"] = syn.router(seed, E, H, layer=0)
-    x = syn.activations(seed, n_tok, H)
+    if T == 1:
+        xs = syn.activations(seed, 256, H)
+        n, dt = 0, 0.0
+        while n < 256:
+            t = time.perf_counter()
+            orc.moe_layer(d, xs[n:n + 1], W)
+            dt += time.perf_counter() - t
+            n += 1
+            if target_s is None or dt >= target_s:
+                break
+        units = n * (ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2) / 1e9
+        return dt, units, "GB/s", (f"{n} token(s) one at a time through 1 layer "
+                                   "(GB of router + 9 experts streamed per second)")
     bias = syn.zipf_bias(seed, E) if wl["zipf"] else None
-    t = time.perf_counter()
-    orc.moe_layer(d, x, W, bias=bias)
-    dt = time.perf_counter() - t
+    n_tok = 32 if wl["layers"] > 1 else 64
+    while True:
+        x = syn.activations(seed, n_tok, H)
+        t = time.perf_counter()
+        orc.moe_layer(d, x, W, bias=bias)
+        dt = time.perf_counter() - t
+        if target_s is None or dt >= 0.5 * target_s or n_tok >= T:
+            break
+        n_tok = min(T, max(2 * n_tok, int(n_tok * target_s / max(dt, 1e-3))))
     # tokens/s of the workload: one layer of the sample, scaled to all layers
     units = n_tok / wl["layers"]
     return dt, units, "tokens/s", f"{n_tok} tokens through 1 of {wl['layers']} layer(s), scaled to the full stack"
@@ -452,7 +461,7 @@ def oracle_sample(wl, seed, budget_tokens=None):
 def cpu_baseline(wl, seed):
     import oracle as orc
     orc.build()
-    dt, units, unit, desc = oracle_sample(wl, seed)
+    dt, units, unit, desc = oracle_sample(wl, seed, target_s=10.0)
     return {"value": units / dt, "unit": unit, "cores": orc.num_threads(), "kind": "oracle", "sample": desc,
             "seconds": round(dt, 3)}
 

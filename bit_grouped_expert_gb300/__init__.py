@@ -51,6 +51,7 @@ MOE_KERNEL_DOWN = 5
 MOE_KERNEL_COMBINE = 6
 MOE_KERNEL_DECODE_LAYER = 7
 MOE_KERNEL_RMSNORM = 10
+MOE_KERNEL_GATHER = 11
 
 
 class MoeError(RuntimeError):

@@ -3,7 +3,8 @@
 // "Prefill" section of the Lily pages: the 4-bit groupwise-affine weights are
 // rebuilt to bf16 tile by tile inside the grouped GEMM and accumulated in
 // FP32, so no unpacked weight array reaches memory; the grouped GEMMs follow
-// a device-built block map (one tile = up to 128 rows of one expert).
+// a device-built block map (one tile = up to 128 (gate/up) or 256 (down)
+// rows of one expert).
 //
 // One persistent CTA per SM walks work items (block-map tile, 128 output
 // features).  The packed weights are the MMA's A operand (M = 128 rows of
@@ -11,18 +12,20 @@
 // 16), so a weight tile is rebuilt once for all of an expert's tokens:
 //   warp 0      TMA: packed 4-bit codes, 128 rows x 256 codes per box, 128B
 //               swizzle, one box per matrix per stage of 4 k-blocks
-//   warp 1      one thread issues tcgen05.mma (A from tensor memory, B from
-//               shared memory, D fp32 in tensor memory) and commits
-//   warps 2, 3  cp.async loaders of the token rows (gathered through perm for
-//               routed experts) into the 128B-swizzled K-major layout; each
-//               lane's copies arrive on the slot's mbarrier when they land
-//               (warp 3 also allocates and frees the tensor memory)
+//   warps 1, 3  one thread each issues tcgen05.mma (A from tensor memory, B
+//               from shared memory, D fp32 in tensor memory) and commits;
+//               warp 3 also allocates and frees the tensor memory
+//   warp 2      TMA: the tile's token rows, contiguous in the source (x rows
+//               gathered in perm order for the routed experts, x itself for
+//               the shared expert, h for the down GEMM), 128B-swizzled
 //   warps 4-15  three warpgroups: dequantise a k-block of one matrix (64 codes
 //               of a row -> 32 bf16x2, w = bf16_rne(scale*q + bias)) straight
 //               into tensor memory with tcgen05.st, then run the epilogue:
 //               gate/up: h = bf16(silu(g) * u); down: y = bf16(acc)
-// Tensor memory (512 columns): D_gate [0,128), D_up [128,256), four A slots
-// of 64 columns at 256 (gate at +0, up at +32; 32 columns = 64 bf16 of K).
+// Tensor memory (512 columns): D_gate [0,128), D_up [128,256) (down: D
+// [0,256)), four A slots of 64 columns at 256 (gate at +0, up at +32; 32
+// columns = 64 bf16 of K).  A k-block's token rows and its A slot form one
+// slot of a four-slot ring.
 // Every wait is bounded: after one second the kernel records
 // MOE_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees tensor memory
 // and exits.
@@ -40,7 +43,8 @@ constexpr int BM = 128;         // output features per work item (= TMEM lanes)
 constexpr int KBLK = 64;        // k-block = one quantisation group
 constexpr int STAGE_KB = 4;     // k-blocks per code stage (one TMA box per matrix)
 constexpr int BOX = BM * 128;   // one TMA box: 128 rows x 128 bytes (256 codes)
-constexpr int NSLOT = 4;        // A slots in tensor memory (64 columns each)
+constexpr int NSLOT = 4;        // k-block ring: A slots in tensor memory (64 columns each) + token-row slots
+constexpr int NISS = 2;         // MMA-issuing threads (warps 1 and 3)
 constexpr int NWG = 3;                    // dequant/epilogue warpgroups
 constexpr int THREADS = 128 + NWG * 128;  // 4 role warps + the warpgroups
 constexpr uint32_t TMEM_COLS = 512;
@@ -58,17 +62,16 @@ struct Cfg {
   // 128; the down GEMM has one accumulator and takes N <= 256.
   static constexpr int MAXN = GATEUP ? 128 : 256;
   static constexpr int B_SLOT = MAXN * 128;  // one k-block of MAXN token rows
-  // Code stages (4 k-blocks each, from HBM) and token-row slots (1 k-block
-  // each, mostly from L2) share the shared memory; the token rows get the
-  // deeper ring, since every k-block's MMA waits on them.
-  static constexpr int CSTAGES = 3;
-  static constexpr int NBSLOT = GATEUP ? 6 : 5;
+  // Code stages (4 k-blocks each, from HBM) and the k-block ring (token rows
+  // in shared memory + dequantised weights in tensor memory) share the
+  // shared memory.
+  static constexpr int CSTAGES = 4;
   // per stage: codes of each matrix, then (scale, bias) boxes of each matrix
   static constexpr int STAGE_BYTES = NMAT * BOX + NMAT * 2 * SBOX;
   static constexpr int OFF_B = CSTAGES * STAGE_BYTES;
-  static constexpr int OFF_MISC = OFF_B + NBSLOT * B_SLOT;
+  static constexpr int OFF_MISC = OFF_B + NSLOT * B_SLOT;
   static constexpr int SMEM = OFF_MISC + 1024 /* misc */ + 1024 /* alignment slack */;
-  static_assert(NBSLOT <= 8, "b_full / b_free arrays");
+  static_assert(CSTAGES <= 8, "code_full / code_empty arrays");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -78,24 +81,52 @@ struct TcMaps {
   CUtensorMap code[2];
   CUtensorMap sc[2];
   CUtensorMap bi[2];
-  // down GEMM: h as a bf16 tensor [rows][K], 128B-swizzled boxes of one
-  // k-block (64 values) x 128 / 64 / 32 / 16 rows
+  // token rows: a bf16 tensor [rows][K] with 128B-swizzled boxes of one
+  // k-block (64 values) x 128 / 64 / 32 / 16 rows.  act: h (down) or the
+  // routed x rows gathered in perm order (gate/up); act_sh: x itself, for the
+  // shared expert's tiles (gate/up)
   CUtensorMap act[4];
+  CUtensorMap act_sh[4];
 };
 
 struct TcArgs {
-  const uint16_t *act;  // activation rows: x [T][K] (gate/up) or h [rows][K] (down)
-  const int32_t *perm, *blockmap, *n_tiles;
+  const int32_t *blockmap, *n_tiles;
   const uint16_t *sc[2], *bi[2];  // scale / bias arrays of the matrices
   uint16_t *out;                  // h [rows][NOUT] or y [rows][NOUT]
   int32_t *status;
   int T, k, E, K, NOUT;           // K: reduction length; NOUT: output features per expert
   int tma_scales;                 // scales/biases staged by TMA (K % 512 == 0)
+  // Optional wait accounting (tracing aid): per CTA, cycles each role spent
+  // in its barrier waits and in total, at trace[cta * 32 + trace_base + i].
+  uint64_t *trace;
+  int trace_base;
 };
 
+// Slots of the wait accounting (see TcArgs::trace).
+enum {
+  TW_TMA_EMPTY, TW_MMA_ACC, TW_MMA_READY, TW_UNUSED3, TW_LOAD_FREE, TW_DQ_CODE, TW_DQ_FREE, TW_DQ_ACC,
+  TW_TMA_TOTAL, TW_MMA_TOTAL, TW_LOAD_TOTAL, TW_DQ_TOTAL, TW_ITEMS, TW_N
+};
+
+// f() (a wait), with its clock64 cycles added to acc when on.
+template <typename F>
+__device__ __forceinline__ bool timed(bool on, unsigned long long &acc, F f) {
+  if (!on) return f();
+  const long long t0 = clock64();
+  const bool r = f();
+  acc += (unsigned long long)(clock64() - t0);
+  return r;
+}
+
+// The k-block ring: slot s holds k-block kb (s = kb % NSLOT of the CTA's
+// running k-block count) -- its token rows in shared memory and its
+// dequantised weights in tensor memory.  ready[s] completes when both have
+// landed (the TMA bytes plus one arrival per dequant thread of each matrix);
+// free[s] when every MMA that read the slot has completed (one commit per
+// issuer).
 struct Misc {
   uint64_t code_full[8], code_empty[8];
-  uint64_t b_full[8], b_free[8], a_full[NSLOT], a_free[NSLOT];
+  uint64_t ready[NSLOT], free[NSLOT];
   uint64_t acc_full, acc_empty, final_bar;
   uint32_t tmem;
   int abort_flag;
@@ -162,6 +193,10 @@ __device__ __forceinline__ __nv_bfloat162 pick_group(uint2 g, int j) {
   return *reinterpret_cast<const __nv_bfloat162 *>(&u);
 }
 
+__device__ __forceinline__ void trace_put(const TcArgs &a, int slot, unsigned long long v) {
+  if (a.trace && blockIdx.x < MOE_TRACE_CTAS) a.trace[blockIdx.x * MOE_TRACE_SLOTS + a.trace_base + slot] = v;
+}
+
 template <bool GATEUP>
 __global__ void __launch_bounds__(THREADS, 1)
     experts_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
@@ -182,19 +217,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(&m->code_full[i], 1);
       ptx::mbar_init(&m->code_empty[i], NWG * 4);
     }
-    for (int i = 0; i < C::NBSLOT; ++i) {
-      // gate/up: one cp.async-tracked arrival per loader lane (2 warps);
-      // down: one arrival with the slot's TMA byte count
-      ptx::mbar_init(&m->b_full[i], GATEUP ? 64 : 1);
-      ptx::mbar_init(&m->b_free[i], 1);
-    }
     for (int i = 0; i < NSLOT; ++i) {
-      ptx::mbar_init(&m->a_full[i], C::NMAT * 128);  // one warpgroup per (k-block, matrix)
-      ptx::mbar_init(&m->a_free[i], 1);
+      ptx::mbar_init(&m->ready[i], 1 + C::NMAT * 128);  // token-row TMA + one warpgroup per matrix
+      ptx::mbar_init(&m->free[i], NISS);
     }
-    ptx::mbar_init(&m->acc_full, 1);
+    ptx::mbar_init(&m->acc_full, NISS);
     ptx::mbar_init(&m->acc_empty, NWG * 128);
-    ptx::mbar_init(&m->final_bar, 1);
+    ptx::mbar_init(&m->final_bar, NISS);
     m->abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -204,13 +233,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = m->tmem;
 
   const int MT = a.NOUT / BM;
-  const int KB = a.K / KBLK;
+  const int KB = a.K / KBLK;  // a multiple of NSLOT (K % 256 == 0)
   const int NST = (KB + STAGE_KB - 1) / STAGE_KB;
   const int n_items = (*a.n_tiles) * MT;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (codes, scales)
     if (lane == 0) {
+      const bool tr = a.trace != nullptr;
+      const long long t_start = clock64();
+      unsigned long long w_empty = 0;
       for (int mat = 0; mat < C::NMAT; ++mat) {
         ptx::prefetch_tmap(&maps.code[mat]);
         if (a.tma_scales) {
@@ -228,7 +260,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int st = 0; st < NST; ++st, ++cs) {
           const int slot = cs % C::CSTAGES;
           const uint32_t ph = (cs / C::CSTAGES) & 1u;
-          if (!wait_bar(&m->code_empty[slot], ph ^ 1u, m, a.status)) {
+          if (!timed(tr, w_empty, [&] { return wait_bar(&m->code_empty[slot], ph ^ 1u, m, a.status); })) {
             ok = false;
             break;
           }
@@ -253,139 +285,128 @@ __global__ void __launch_bounds__(THREADS, 1)
           drain_wait(&m->code_full[c % C::CSTAGES], (c / C::CSTAGES) & 1u);
         }
       }
+      trace_put(a, TW_TMA_EMPTY, w_empty);
+      trace_put(a, TW_TMA_TOTAL, (unsigned long long)(clock64() - t_start));
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // A thread issues at most one tcgen05.mma every ~50 cycles and every
+    // instruction between them adds to that, so two threads issue, from a
+    // loop unrolled over the ring's slots (constant addresses).  Each
+    // accumulator column stays with one issuer, in K order, so the result
+    // does not depend on how the two interleave: gate/up split by matrix,
+    // down by halves of the tile's N.
     if (lane == 0) {
+      const int iss = warp == 3 ? 1 : 0;
+      const bool tr = a.trace != nullptr && iss == 0;
+      const long long t_start = clock64();
+      unsigned long long w_acc = 0, w_ready = 0;
+      // descriptor of B slot 0 (128B-swizzled K-major); other slots and K
+      // steps only move the address field in its low word
+      const uint64_t bdesc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + C::OFF_B));
+      const uint32_t b_lo0 = (uint32_t)bdesc0, b_hi = (uint32_t)(bdesc0 >> 32);
+      const int mat = GATEUP ? iss : 0;
+      const uint32_t a_col = tmem + A_COL + (uint32_t)(mat * 32);
       uint32_t kbc = 0, itc = 0;
       bool ok = true;
       Item nit = blockIdx.x < n_items ? get_item<C::MAXN>(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const Item it = nit;
         if (item + (int)gridDim.x < n_items) nit = get_item<C::MAXN>(a, item + gridDim.x, MT);
-        const uint32_t idesc = ptx::idesc_bf16_f32((uint32_t)it.n_mma);
-        if (!wait_bar(&m->acc_empty, (itc & 1u) ^ 1u, m, a.status)) break;
+        // this issuer's token columns [c0, c0 + nc)
+        int c0 = 0, nc = it.n_mma;
+        if (!GATEUP) {
+          const int half = ((it.n_mma >> 1) + 15) & ~15;
+          c0 = iss ? half : 0;
+          nc = iss ? it.n_mma - half : half;
+        }
+        const uint32_t idesc = ptx::idesc_bf16_f32((uint32_t)(nc > 0 ? nc : 16));
+        const uint32_t d = tmem + (uint32_t)(mat * D_UP_COL + c0);
+        const uint32_t b_lo = b_lo0 + (uint32_t)c0 * 8u;  // c0 rows of 128 B, in 16-byte units
+        if (!timed(tr, w_acc, [&] { return wait_bar(&m->acc_empty, (itc & 1u) ^ 1u, m, a.status); })) break;
         ptx::tc_fence_after();
-        for (int kb = 0; kb < KB; ++kb, ++kbc) {
-          const int slot = kbc % NSLOT, bslot = kbc % C::NBSLOT;
-          if (!wait_bar(&m->b_full[bslot], (kbc / C::NBSLOT) & 1u, m, a.status) ||
-              !wait_bar(&m->a_full[slot], (kbc / NSLOT) & 1u, m, a.status)) {
-            ok = false;
-            break;
+        for (int kb = 0; kb < KB && ok; kb += NSLOT, kbc += NSLOT) {
+          const uint32_t ph = (kbc / NSLOT) & 1u;
+#pragma unroll
+          for (int j = 0; j < NSLOT; ++j) {
+            if (!timed(tr, w_ready, [&] { return wait_bar(&m->ready[j], ph, m, a.status); })) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            if (nc > 0)
+              ptx::mma_ts_kblock(d, a_col + j * 64, b_lo + (uint32_t)(j * (C::B_SLOT >> 4)), b_hi, idesc,
+                                 (uint32_t)(kb + j));
+            ptx::mma_commit(&m->free[j]);
           }
-          ptx::fence_proxy_async_smem();  // token rows were written by cp.async (generic proxy)
-          ptx::tc_fence_after();
-          const uint32_t baddr = ptx::smem_u32(smem + C::OFF_B + bslot * C::B_SLOT);
-#pragma unroll
-          for (int mat = 0; mat < C::NMAT; ++mat)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              ptx::mma_ts(tmem + mat * D_UP_COL, tmem + A_COL + slot * 64 + mat * 32 + i * 8,
-                          ptx::sdesc_sw128(baddr + 32 * i), idesc, (uint32_t)(kb | i));
-          ptx::mma_commit(&m->a_free[slot]);
-          ptx::mma_commit(&m->b_free[bslot]);
         }
         if (!ok) break;
         ptx::mma_commit(&m->acc_full);
         ++itc;
       }
-      // every MMA this CTA issued has completed before tensor memory is freed
+      // every MMA this thread issued has completed before tensor memory is freed
       ptx::mma_commit(&m->final_bar);
       drain_wait(&m->final_bar, 0);
+      trace_put(a, TW_MMA_ACC, w_acc);
+      trace_put(a, TW_MMA_READY, w_ready);
+      trace_put(a, TW_MMA_TOTAL, (unsigned long long)(clock64() - t_start));
+      trace_put(a, TW_ITEMS, itc);
     }
-  } else if (!GATEUP && warp == 2) {
-    // ------------------------------------------------------------ token-row TMA (down)
-    // h rows of a tile are contiguous (routed rows in perm order, then the
-    // shared expert's), so each k-block of the tile's n_mma rows arrives in
-    // a few TMA boxes (128 rows at a time, then 64 / 32 / 16), already in the
-    // MMA's 128B-swizzled K-major layout.  Rows past the tile belong to the next
-    // tile (or lie past the tensor and read as zero): they only feed MMA
-    // columns the epilogue never stores.
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ token-row TMA
+    // The rows of a tile are contiguous (down: routed rows of h in perm order,
+    // then the shared expert's; gate/up: the routed x rows gathered in perm
+    // order, or x itself for the shared expert), so each k-block of the
+    // tile's n_mma rows arrives in a few TMA boxes (128 rows at a time, then
+    // 64 / 32 / 16), already in the MMA's 128B-swizzled K-major layout.  Rows
+    // past the tile belong to the next tile (or lie past the tensor and read
+    // as zero): they only feed MMA columns the epilogue never stores.
     if (lane == 0) {
-      for (int i = 0; i < 4; ++i) ptx::prefetch_tmap(&maps.act[i]);
+      const bool tr = a.trace != nullptr;
+      const long long t_start = clock64();
+      unsigned long long w_free = 0;
+      for (int i = 0; i < 4; ++i) {
+        ptx::prefetch_tmap(&maps.act[i]);
+        if (GATEUP) ptx::prefetch_tmap(&maps.act_sh[i]);
+      }
       uint32_t kbc = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const Item it = get_item<C::MAXN>(a, item, MT);
+        const bool sh = GATEUP && it.e >= a.E;
+        const CUtensorMap *mp = sh ? maps.act_sh : maps.act;
+        const int rb = sh ? it.row0 - a.k * a.T : it.row0;
         for (int kb = 0; kb < KB; ++kb, ++kbc) {
-          const int slot = kbc % C::NBSLOT;
-          if (!wait_bar(&m->b_free[slot], ((kbc / C::NBSLOT) & 1u) ^ 1u, m, a.status)) {
+          const int slot = kbc % NSLOT;
+          if (!timed(tr, w_free, [&] { return wait_bar(&m->free[slot], ((kbc / NSLOT) & 1u) ^ 1u, m, a.status); })) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&m->b_full[slot], (uint32_t)it.n_mma * 128u);
+          ptx::mbar_arrive_expect_tx(&m->ready[slot], (uint32_t)it.n_mma * 128u);
           uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT;
           int r = 0;
           for (; it.n_mma - r >= 128; r += 128)
-            ptx::tma_load_2d(bs + r * 128, &maps.act[0], &m->b_full[slot], kb * KBLK, it.row0 + r);
+            ptx::tma_load_2d(bs + r * 128, &mp[0], &m->ready[slot], kb * KBLK, rb + r);
 #pragma unroll
           for (int i = 1; i < 4; ++i) {
             const int h = 128 >> i;
             if (it.n_mma - r >= h) {
-              ptx::tma_load_2d(bs + r * 128, &maps.act[i], &m->b_full[slot], kb * KBLK, it.row0 + r);
+              ptx::tma_load_2d(bs + r * 128, &mp[i], &m->ready[slot], kb * KBLK, rb + r);
               r += h;
             }
           }
         }
       }
       if (!ok) {  // the last slots' loads may still be in flight
-        const uint32_t n = kbc < (uint32_t)C::NBSLOT ? kbc : (uint32_t)C::NBSLOT;
+        const uint32_t n = kbc < (uint32_t)NSLOT ? kbc : (uint32_t)NSLOT;
         for (uint32_t i = 1; i <= n; ++i) {
           const uint32_t c = kbc - i;
-          drain_wait(&m->b_full[c % C::NBSLOT], (c / C::NBSLOT) & 1u);
+          drain_wait(&m->ready[c % NSLOT], (c / NSLOT) & 1u);
         }
       }
+      trace_put(a, TW_LOAD_FREE, w_free);
+      trace_put(a, TW_LOAD_TOTAL, (unsigned long long)(clock64() - t_start));
     }
-  } else if (GATEUP && (warp == 2 || warp == 3)) {
-    // ------------------------------------------------------------ token-row loaders
-    // Warps 2 and 3 each copy half of the tile's rows: lane l of loader w owns
-    // rows w*4 + l/8 + 8i (i < 16) and 16-byte chunk l%8 of each, so its
-    // destinations share one swizzle and its sources are kept as 32-bit byte
-    // offsets for the whole item.
-    const int lw = warp - 2, c = lane & 7, r0 = lw * 4 + (lane >> 3);
-    const uint8_t *act = reinterpret_cast<const uint8_t *>(a.act);
-    const uint32_t sw = (uint32_t)((c ^ (r0 & 7)) << 4);
-    uint32_t kbc = 0;
-    bool ok = true;
-    Item nit = blockIdx.x < n_items ? get_item<C::MAXN>(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const Item it = nit;
-      if (item + (int)gridDim.x < n_items) nit = get_item<C::MAXN>(a, item + gridDim.x, MT);
-      uint32_t off[C::MAXN / 8];
-      uint32_t valid = 0;  // bit i: row r0 + 8i holds a token
-#pragma unroll
-      for (int i = 0; i < C::MAXN / 8; ++i) {
-        const int r = r0 + 8 * i;
-        if (r >= it.n_mma) break;  // rows past the MMA's N are never copied
-        int src = -1;
-        if (r < it.nrows) {
-          if (GATEUP)
-            src = (it.e < a.E) ? a.perm[it.row0 + r] / a.k : it.row0 + r - a.k * a.T;
-          else
-            src = it.row0 + r;
-        }
-        off[i] = src < 0 ? 0u : (uint32_t)src * (uint32_t)a.K * 2u + (uint32_t)c * 16u;
-        if (src >= 0) valid |= 1u << i;
-      }
-      const int nr = it.n_mma;
-      for (int kb = 0; kb < KB; ++kb, ++kbc) {
-        const int slot = kbc % C::NBSLOT;
-        const uint32_t ph = (kbc / C::NBSLOT) & 1u;
-        if (!__all_sync(0xffffffffu, wait_bar(&m->b_free[slot], ph ^ 1u, m, a.status))) {
-          ok = false;
-          break;
-        }
-        uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT + r0 * 128 + sw;
-        const uint32_t kofs = (uint32_t)kb * (KBLK * 2);
-#pragma unroll
-        for (int i = 0; i < C::MAXN / 8; ++i) {
-          if (r0 + 8 * i >= nr) break;  // small tiles: a few iterations, not sixteen
-          ptx::cp_async_16(bs + i * 1024, act + off[i] + kofs, ((valid >> i) & 1u) ? 16u : 0u);
-        }
-        ptx::cp_async_arrive_noinc(&m->b_full[slot]);  // fires when this lane's copies have landed
-      }
-    }
-    ptx::cp_async_wait_all();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ dequant + epilogue
     // Work unit u = kb * NMAT + mat (one k-block of one matrix) goes to
@@ -395,6 +416,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int groups = a.K / KBLK;
     const bool vec = (groups % 4) == 0;
+    const bool tr = a.trace != nullptr && warp == 4 && lane == 0;
+    const long long t_start = clock64();
+    unsigned long long w_code = 0, w_free = 0, w_acc = 0;
     uint32_t cs = 0, kbc = 0, itc = 0;
     bool ok = true;
     // scales/biases of the next stage are loaded one stage ahead; block-map
@@ -408,9 +432,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const size_t grow = (size_t)pi.e * a.NOUT + (size_t)pi.mt * BM + row;
       const int kb0 = pst * STAGE_KB, nkb = min(STAGE_KB, KB - kb0);
 #pragma unroll
-      for (int mat = 0; mat < C::NMAT; ++mat) {
-        nsv[mat] = load_groups(a.sc[mat] + grow * groups + kb0, nkb, vec);
-        nbv[mat] = load_groups(a.bi[mat] + grow * groups + kb0, nkb, vec);
+      for (int mt = 0; mt < C::NMAT; ++mt) {
+        nsv[mt] = load_groups(a.sc[mt] + grow * groups + kb0, nkb, vec);
+        nbv[mt] = load_groups(a.bi[mt] + grow * groups + kb0, nkb, vec);
       }
     };
     if (nitem < n_items && !a.tma_scales) prefetch(nit, 0);
@@ -420,9 +444,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int kb0 = st * STAGE_KB, nkb = min(STAGE_KB, KB - kb0);
         uint2 sv[C::NMAT], bv[C::NMAT];
 #pragma unroll
-        for (int mat = 0; mat < C::NMAT; ++mat) {
-          sv[mat] = nsv[mat];
-          bv[mat] = nbv[mat];
+        for (int mt = 0; mt < C::NMAT; ++mt) {
+          sv[mt] = nsv[mt];
+          bv[mt] = nbv[mt];
         }
         // advance the prefetch cursor (next stage of this item, or stage 0 of the next item)
         if (++nst == NST) {
@@ -433,16 +457,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (nitem < n_items && !a.tma_scales) prefetch(nit, nst);
         const int cslot = cs % C::CSTAGES;
-        if (!__all_sync(0xffffffffu, wait_bar(&m->code_full[cslot], (cs / C::CSTAGES) & 1u, m, a.status))) {
+        if (!__all_sync(0xffffffffu, timed(tr, w_code, [&] {
+              return wait_bar(&m->code_full[cslot], (cs / C::CSTAGES) & 1u, m, a.status);
+            }))) {
           ok = false;
           break;
         }
         if (a.tma_scales) {  // this row's 8 groups of the box; the stage uses 4 of them
           const uint8_t *sb = smem + cslot * C::STAGE_BYTES + C::NMAT * BOX + row * 16 + (kb0 & 4) * 2;
 #pragma unroll
-          for (int mat = 0; mat < C::NMAT; ++mat) {
-            sv[mat] = *reinterpret_cast<const uint2 *>(sb + mat * 2 * SBOX);
-            bv[mat] = *reinterpret_cast<const uint2 *>(sb + mat * 2 * SBOX + SBOX);
+          for (int mt = 0; mt < C::NMAT; ++mt) {
+            sv[mt] = *reinterpret_cast<const uint2 *>(sb + mt * 2 * SBOX);
+            bv[mt] = *reinterpret_cast<const uint2 *>(sb + mt * 2 * SBOX + SBOX);
           }
         }
         const int u0 = kb0 * C::NMAT, u1 = (kb0 + nkb) * C::NMAT;
@@ -467,8 +493,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = *reinterpret_cast<uint32_t *>(&p[pi]);
           }
           const int aslot = kbg % NSLOT;
-          if (!__all_sync(0xffffffffu,
-                          wait_bar(&m->a_free[aslot], ((kbg / NSLOT) & 1u) ^ 1u, m, a.status))) {
+          if (!__all_sync(0xffffffffu, timed(tr, w_free, [&] {
+                return wait_bar(&m->free[aslot], ((kbg / NSLOT) & 1u) ^ 1u, m, a.status);
+              }))) {
             ok = false;
             break;
           }
@@ -476,7 +503,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::tmem_st_x32(tmem + lane_base + A_COL + aslot * 64 + mat * 32, v);
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
-          ptx::mbar_arrive(&m->a_full[aslot]);
+          ptx::mbar_arrive(&m->ready[aslot]);
         }
         kbc += nkb;
         __syncwarp();
@@ -485,7 +512,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
       // epilogue: chunks of 16 token columns dealt round-robin to the warpgroups
-      if (!__all_sync(0xffffffffu, wait_bar(&m->acc_full, itc & 1u, m, a.status))) break;
+      if (!__all_sync(0xffffffffu,
+                      timed(tr, w_acc, [&] { return wait_bar(&m->acc_full, itc & 1u, m, a.status); })))
+        break;
       ptx::tc_fence_after();
       uint16_t *orow = a.out + (size_t)it.row0 * a.NOUT + (size_t)it.mt * BM + row;
       for (int ch = wg; ch < it.n_mma / 16; ch += NWG) {
@@ -506,6 +535,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_arrive(&m->acc_empty);
       ++itc;
     }
+    if (tr) {
+      trace_put(a, TW_DQ_CODE, w_code);
+      trace_put(a, TW_DQ_FREE, w_free);
+      trace_put(a, TW_DQ_ACC, w_acc);
+      trace_put(a, TW_DQ_TOTAL, (unsigned long long)(clock64() - t_start));
+    }
   }
 
   ptx::tc_fence_before();
@@ -514,6 +549,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+// Routed token rows in perm order: xg[p] = x[perm[p] / k], one warp per row
+// (16-byte loads and stores), so that the gate/up GEMM can stage its token
+// rows with TMA boxes instead of per-row copies.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *__restrict__ x,
+                                                          const int32_t *__restrict__ perm, int rows, int k, int K,
+                                                          uint16_t *__restrict__ xg) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(perm[r] / k) * K);
+  uint4 *dst = reinterpret_cast<uint4 *>(xg + (size_t)r * K);
+  for (int i = lane; i < K / 8; i += 32) dst[i] = __ldg(src + i);
 }
 
 // ---------------------------------------------------------------- host
@@ -593,7 +641,8 @@ cudaError_t tc_prepare() {
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
                               const int32_t *blockmap, const int32_t *n_tiles, int max_tiles,
                               const int32_t *blockmap2, const int32_t *n_tiles2, int max_tiles2, ExpertPtrs w,
-                              uint16_t *h, uint16_t *y, int32_t *status, int *launches, cudaStream_t s) {
+                              uint16_t *h, uint16_t *y, uint16_t *xg, int32_t *status, uint64_t *trace,
+                              int *launches, cudaStream_t s) {
   const moe_config &c = plan->cfg;
   const int rows_gu = (c.n_experts + c.n_shared) * c.inter;
   const int rows_dn = (c.n_experts + c.n_shared) * c.hidden;
@@ -617,18 +666,29 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   const int rows_h = (c.top_k + c.n_shared) * T;
   for (int i = 0; i < 4; ++i)
     if ((e = act_map(&md.act[i], h, rows_h, c.inter, BM >> i)) != cudaSuccess) return e;
+  {  // gate/up token rows by TMA: routed rows gathered into xg, shared rows from x
+    for (int i = 0; i < 4; ++i) {
+      if ((e = act_map(&mg.act[i], xg, c.top_k * T, c.hidden, BM >> i)) != cudaSuccess) return e;
+      if ((e = act_map(&mg.act_sh[i], x, T, c.hidden, BM >> i)) != cudaSuccess) return e;
+    }
+    prof_before(MOE_KERNEL_GATHER, s);
+    gather_rows_kernel<<<(c.top_k * T + 7) / 8, 256, 0, s>>>(x, perm, c.top_k * T, c.top_k, c.hidden, xg);
+    prof_after(MOE_KERNEL_GATHER, s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    *launches += 1;
+  }
 
   TcArgs a{};
-  a.perm = perm;
   a.blockmap = blockmap;
   a.n_tiles = n_tiles;
   a.status = status;
   a.T = T;
   a.k = c.top_k;
   a.E = c.n_experts;
+  a.trace = trace;
+  a.trace_base = 0;
 
   // gate/up + SwiGLU: x rows (gathered) -> h
-  a.act = x;
   a.sc[0] = w.gate_s;
   a.bi[0] = w.gate_b;
   a.sc[1] = w.up_s;
@@ -645,7 +705,7 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // down: h rows -> y, over the block map of taller tiles
-  a.act = h;
+  a.trace_base = 16;
   a.blockmap = blockmap2;
   a.n_tiles = n_tiles2;
   a.sc[0] = w.down_s;

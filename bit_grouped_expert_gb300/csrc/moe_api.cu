@@ -33,7 +33,7 @@ int tiles_bound(int T, int k, int E, int S, int BN) {
   return (k * T + BN - 1) / BN + E + (S ? (T + BN - 1) / BN : 0);
 }
 
-moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_tiles2) {
+moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_tiles2, bool tc) {
   moe::Layout L;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -58,6 +58,7 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_ti
   L.n_tiles2 = take(16);
   L.h = take((k + S) * T * I * 2);
   L.y = take((k + S) * T * H * 2);
+  L.xg = take(tc ? k * T * H * 2 : 0);  // routed x rows in perm order (tensor-core gate/up)
   L.rsplit = take(3 * E * H * 2);
   L.xn = take(T * H * 2);  // normalised x of pre-norm plans
   L.trace = take(MOE_TRACE_CTAS * MOE_TRACE_SLOTS * 8);
@@ -196,7 +197,7 @@ void prof_after(int kernel, cudaStream_t s) {
 extern "C" {
 
 moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *const *stop_events, int32_t n) {
-  if (kernel < MOE_KERNEL_ROUTER || kernel > MOE_KERNEL_RMSNORM || n < 0 || n > 4096) return MOE_ERR_INVALID_ARGUMENT;
+  if (kernel < MOE_KERNEL_ROUTER || kernel > MOE_KERNEL_GATHER || n < 0 || n > 4096) return MOE_ERR_INVALID_ARGUMENT;
   if (n > 0 && (!start_events || !stop_events)) return MOE_ERR_INVALID_ARGUMENT;
   for (int i = 0; i < n; ++i)
     if (!start_events[i] || !stop_events[i]) return MOE_ERR_INVALID_ARGUMENT;
@@ -258,7 +259,7 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
   // the tensor-core down GEMM takes tiles of up to TC_DOWN_ROWS rows
   p->block_rows2 = simt ? 0 : ((flags & MOE_FLAG_TILE_ROWS_64) ? 64 : moe::TC_DOWN_ROWS);
   p->max_tiles2 = p->block_rows2 ? tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows2) : 0;
-  p->lay = make_layout(c, max_tokens, p->max_tiles, p->max_tiles2);
+  p->lay = make_layout(c, max_tokens, p->max_tiles, p->max_tiles2, !simt);
   p->num_sms = 0;
   p->use_router_tc = false;
   p->use_decode = false;
@@ -273,7 +274,7 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
       p->max_tiles = tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows);
       p->block_rows2 = 0;
       p->max_tiles2 = 0;
-      p->lay = make_layout(c, max_tokens, p->max_tiles, p->max_tiles2);
+      p->lay = make_layout(c, max_tokens, p->max_tiles, p->max_tiles2, false);
     }
     if (p->num_sms > 0 &&
         moe::decode_supported(c.hidden, c.n_experts, c.top_k, c.inter, c.n_shared, p->num_sms)) {
@@ -399,7 +400,11 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
   } else {
     const int max_tiles2 = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, plan->block_rows2);
     err = moe::launch_experts_tc(plan, x, T, perm, bm, nt, max_tiles, moe::ws_ptr<int32_t>(ws_d, L.blockmap2),
-                                 moe::ws_ptr<int32_t>(ws_d, L.n_tiles2), max_tiles2, ep, h, y, status, &launches, s);
+                                 moe::ws_ptr<int32_t>(ws_d, L.n_tiles2), max_tiles2, ep, h, y,
+                                 moe::ws_ptr<uint16_t>(ws_d, L.xg),
+                                 status,
+                                 (plan->flags & MOE_FLAG_TRACE) ? moe::ws_ptr<uint64_t>(ws_d, L.trace) : nullptr,
+                                 &launches, s);
     if (err != cudaSuccess) return cuda_status(err);
   }
   err = moe::launch_combine(res, y, moe::ws_ptr<int32_t>(ws_d, L.inv), moe::ws_ptr<float>(ws_d, L.topk_w), T,

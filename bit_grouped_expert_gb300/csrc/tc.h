@@ -25,7 +25,8 @@ cudaError_t tc_prepare();
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
                               const int32_t *blockmap, const int32_t *n_tiles, int max_tiles,
                               const int32_t *blockmap2, const int32_t *n_tiles2, int max_tiles2, ExpertPtrs w,
-                              uint16_t *h, uint16_t *y, int32_t *status, int *launches, cudaStream_t s);
+                              uint16_t *h, uint16_t *y, uint16_t *xg, int32_t *status, uint64_t *trace,
+                              int *launches, cudaStream_t s);
 
 // Router keys on tensor cores (E % 128 == 0, H % 64 == 0).
 bool router_tc_supported(int E, int H);

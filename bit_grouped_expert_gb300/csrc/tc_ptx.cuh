@@ -141,6 +141,27 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// The four MMAs of one 64-wide k-block: D[d] (+)= A[a + 8i] * B[i], i = 0..3,
+// where B[i] is the shared-memory descriptor whose low word is b_lo + 2i (32 B
+// further along K in the 128B-swizzled atom) and high word b_hi; the first
+// MMA accumulates only when acc != 0.  One asm block, no per-MMA arithmetic
+// outside it: a thread issues a tcgen05.mma every ~50 cycles at best, and
+// instructions between the MMAs add to that.
+__device__ __forceinline__ void mma_ts_kblock(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                              uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 b0, b1, b2, b3;\n\t.reg .b32 l1, l2, l3, a1, a2, a3;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 q, 1, 0;\n\t"
+      "add.u32 l1, %2, 2;\n\tadd.u32 l2, %2, 4;\n\tadd.u32 l3, %2, 6;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "mov.b64 b0, {%2, %3};\n\tmov.b64 b1, {l1, %3};\n\tmov.b64 b2, {l2, %3};\n\tmov.b64 b3, {l3, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b0, %4, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, q;\n\t}" ::"r"(d),
+      "r"(a), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc));
+}
+
 // Arrive on an mbarrier when every prior tcgen05 op of this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

@@ -112,9 +112,11 @@ typedef struct {
 #define MOE_FLAG_FORCE_GROUPED  0x2u  /* T == 1 runs the grouped path instead of the decode path */
 #define MOE_FLAG_SIMT_EXPERTS   0x4u  /* CUDA-core grouped GEMMs instead of the tensor-core ones */
 #define MOE_FLAG_TILE_ROWS_64   0x8u  /* tensor-core path: 64-token tiles instead of 128 */
-#define MOE_FLAG_TRACE          0x20u /* decode kernel: record %globaltimer at each phase of the
-                                         last layer of a launch, per CTA, into moe_route_ptrs.trace_d
-                                         (tracing aid) */
+#define MOE_FLAG_TRACE          0x20u /* tracing aid, into moe_route_ptrs.trace_d, per CTA:
+                                         decode kernel: %globaltimer at each phase of the last layer
+                                         of a launch; grouped tensor-core GEMMs: clock64 cycles each
+                                         role spent waiting on its barriers and in total (gate/up in
+                                         slots 0-12, down in slots 16-28) */
 #define MOE_TRACE_CTAS 256             /* CTAs with a row in the trace buffer */
 #define MOE_TRACE_SLOTS 32             /* timestamps in a row */
 #define MOE_FLAG_PRENORM        0x10u /* pre-norm block: x_d is the residual stream r, the layer
@@ -219,7 +221,8 @@ typedef enum {
   MOE_KERNEL_DOWN = 5,           /* grouped down dequant-GEMM                  */
   MOE_KERNEL_COMBINE = 6,        /* weighted gather-combine + residual         */
   MOE_KERNEL_DECODE_LAYER = 7,   /* T == 1: the whole layer in one launch      */
-  MOE_KERNEL_RMSNORM = 10
+  MOE_KERNEL_RMSNORM = 10,
+  MOE_KERNEL_GATHER = 11         /* routed x rows copied into perm order (tensor-core path) */
 } moe_kernel;
 
 /* Profiling hook.  From now on, on the calling thread, the i-th launch of
