@@ -82,11 +82,9 @@ struct TcMaps {
   CUtensorMap sc[2];
   CUtensorMap bi[2];
   // token rows: a bf16 tensor [rows][K] with 128B-swizzled boxes of one
-  // k-block (64 values) x 128 / 64 / 32 / 16 rows.  act: h (down) or the
-  // routed x rows gathered in perm order (gate/up); act_sh: x itself, for the
-  // shared expert's tiles (gate/up)
+  // k-block (64 values) x 128 / 64 / 32 / 16 rows: h (down) or the x rows
+  // gathered in block-map row order (gate/up), both in the interleaved K order
   CUtensorMap act[4];
-  CUtensorMap act_sh[4];
 };
 
 struct TcArgs {
@@ -173,6 +171,30 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait(bar, parity))
     if (ptx::globaltimer() - t0 > TIMEOUT_NS) return;
+}
+
+// K order inside the tensor-core GEMMs.  Within every run of 8 values along
+// K the operands are stored as (0,4), (1,5), (2,6), (3,7) pairs: a packed code
+// word holds code i at bits 4i, so the pair (j, j+4) sits at bits 4j and
+// 4j+16 and comes out with one shift and one and-or, and the token rows (x
+// gathered, h written by the gate/up epilogue) are stored in the same order,
+// so the MMA sums exactly the same products.
+//   ilv_pos(f): storage position of value f of a run.
+__device__ __forceinline__ int ilv_pos(int f) { return (f & ~7) | ((f & 3) << 1) | ((f >> 2) & 1); }
+
+// Codes (j, j+4), j = 0..3, of a word as bf16_rne(scale * q + bias) pairs
+// (one rounding: 0x4300 | q is 128 + q exactly, the subtraction is exact and
+// the fused multiply-add rounds once).
+__device__ __forceinline__ void dequant_word_ilv(uint32_t word, __nv_bfloat162 s2, __nv_bfloat162 b2,
+                                                 uint32_t out[4]) {
+  const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t t = ((word >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+    const __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&t), k128);
+    const __nv_bfloat162 r = __hfma2(s2, q, b2);
+    out[j] = *reinterpret_cast<const uint32_t *>(&r);
+  }
 }
 
 // The bf16 values of groups g0 .. g0+n-1 of one row (n <= 4), packed two
@@ -355,8 +377,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ token-row TMA
     // The rows of a tile are contiguous (down: routed rows of h in perm order,
-    // then the shared expert's; gate/up: the routed x rows gathered in perm
-    // order, or x itself for the shared expert), so each k-block of the
+    // then the shared expert's; gate/up: the x rows gathered in the same
+    // order), so each k-block of the
     // tile's n_mma rows arrives in a few TMA boxes (128 rows at a time, then
     // 64 / 32 / 16), already in the MMA's 128B-swizzled K-major layout.  Rows
     // past the tile belong to the next tile (or lie past the tensor and read
@@ -365,17 +387,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool tr = a.trace != nullptr;
       const long long t_start = clock64();
       unsigned long long w_free = 0;
-      for (int i = 0; i < 4; ++i) {
-        ptx::prefetch_tmap(&maps.act[i]);
-        if (GATEUP) ptx::prefetch_tmap(&maps.act_sh[i]);
-      }
+      for (int i = 0; i < 4; ++i) ptx::prefetch_tmap(&maps.act[i]);
       uint32_t kbc = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const Item it = get_item<C::MAXN>(a, item, MT);
-        const bool sh = GATEUP && it.e >= a.E;
-        const CUtensorMap *mp = sh ? maps.act_sh : maps.act;
-        const int rb = sh ? it.row0 - a.k * a.T : it.row0;
+        const CUtensorMap *mp = maps.act;
+        const int rb = it.row0;
         for (int kb = 0; kb < KB; ++kb, ++kbc) {
           const int slot = kbc % NSLOT;
           if (!timed(tr, w_free, [&] { return wait_bar(&m->free[slot], ((kbc / NSLOT) & 1u) ^ 1u, m, a.status); })) {
@@ -487,10 +505,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int wi = 0; wi < 8; ++wi) {
-            __nv_bfloat162 p[4];
-            dequant_word(wv[wi], s2, b2, p);
+            uint32_t p[4];
+            dequant_word_ilv(wv[wi], s2, b2, p);
 #pragma unroll
-            for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = *reinterpret_cast<uint32_t *>(&p[pi]);
+            for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = p[pi];
           }
           const int aslot = kbg % NSLOT;
           if (!__all_sync(0xffffffffu, timed(tr, w_free, [&] {
@@ -516,7 +534,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                       timed(tr, w_acc, [&] { return wait_bar(&m->acc_full, itc & 1u, m, a.status); })))
         break;
       ptx::tc_fence_after();
-      uint16_t *orow = a.out + (size_t)it.row0 * a.NOUT + (size_t)it.mt * BM + row;
+      // gate/up writes h in the interleaved K order of the down GEMM
+      uint16_t *orow = a.out + (size_t)it.row0 * a.NOUT + (size_t)it.mt * BM + (GATEUP ? ilv_pos(row) : row);
       for (int ch = wg; ch < it.n_mma / 16; ch += NWG) {
         uint32_t g[16], u[16];
         ptx::tmem_ld_x16(tmem + lane_base + ch * 16, g);
@@ -551,17 +570,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// Routed token rows in perm order: xg[p] = x[perm[p] / k], one warp per row
-// (16-byte loads and stores), so that the gate/up GEMM can stage its token
-// rows with TMA boxes instead of per-row copies.
+// Token rows of the gate/up GEMM in block-map row order, interleaved along K
+// (see ilv_pos): row p < k*T is x[perm[p] / k] (the routed pairs in perm
+// order), row k*T + t is x[t] (the shared expert).  One warp per row, 16-byte
+// loads and stores; each 8-value run (v0 .. v7) is stored as v0 v4 v1 v5 v2
+// v6 v3 v7.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *__restrict__ x,
-                                                          const int32_t *__restrict__ perm, int rows, int k, int K,
-                                                          uint16_t *__restrict__ xg) {
+                                                          const int32_t *__restrict__ perm, int routed, int rows,
+                                                          int k, int K, uint16_t *__restrict__ xg) {
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= rows) return;
-  const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(perm[r] / k) * K);
+  const int t = r < routed ? perm[r] / k : r - routed;
+  const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * K);
   uint4 *dst = reinterpret_cast<uint4 *>(xg + (size_t)r * K);
-  for (int i = lane; i < K / 8; i += 32) dst[i] = __ldg(src + i);
+  for (int i = lane; i < K / 8; i += 32) {
+    const uint4 v = __ldg(src + i);
+    dst[i] = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632), __byte_perm(v.y, v.w, 0x5410),
+                        __byte_perm(v.y, v.w, 0x7632));
+  }
 }
 
 // ---------------------------------------------------------------- host
@@ -666,13 +692,11 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   const int rows_h = (c.top_k + c.n_shared) * T;
   for (int i = 0; i < 4; ++i)
     if ((e = act_map(&md.act[i], h, rows_h, c.inter, BM >> i)) != cudaSuccess) return e;
-  {  // gate/up token rows by TMA: routed rows gathered into xg, shared rows from x
-    for (int i = 0; i < 4; ++i) {
-      if ((e = act_map(&mg.act[i], xg, c.top_k * T, c.hidden, BM >> i)) != cudaSuccess) return e;
-      if ((e = act_map(&mg.act_sh[i], x, T, c.hidden, BM >> i)) != cudaSuccess) return e;
-    }
+  {  // gate/up token rows by TMA from a gathered, interleaved copy of x
+    for (int i = 0; i < 4; ++i)
+      if ((e = act_map(&mg.act[i], xg, rows_h, c.hidden, BM >> i)) != cudaSuccess) return e;
     prof_before(MOE_KERNEL_GATHER, s);
-    gather_rows_kernel<<<(c.top_k * T + 7) / 8, 256, 0, s>>>(x, perm, c.top_k * T, c.top_k, c.hidden, xg);
+    gather_rows_kernel<<<(rows_h + 7) / 8, 256, 0, s>>>(x, perm, c.top_k * T, rows_h, c.top_k, c.hidden, xg);
     prof_after(MOE_KERNEL_GATHER, s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     *launches += 1;

@@ -58,7 +58,7 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_ti
   L.n_tiles2 = take(16);
   L.h = take((k + S) * T * I * 2);
   L.y = take((k + S) * T * H * 2);
-  L.xg = take(tc ? k * T * H * 2 : 0);  // routed x rows in perm order (tensor-core gate/up)
+  L.xg = take(tc ? (k + S) * T * H * 2 : 0);  // x rows gathered in block-map row order (tensor-core gate/up)
   L.rsplit = take(3 * E * H * 2);
   L.xn = take(T * H * 2);  // normalised x of pre-norm plans
   L.trace = take(MOE_TRACE_CTAS * MOE_TRACE_SLOTS * 8);

@@ -94,7 +94,8 @@ typedef struct {
   int32_t *inv_d;      /* [k*T] position of pair t*k+j in perm                */
   int32_t *blockmap_d; /* [max_tiles][4] (expert, first row, rows, 0)         */
   int32_t *n_tiles_d;  /* [1] entries in use                                 */
-  uint16_t *h_d;       /* [(k+S)*T][I] bf16 SwiGLU rows (routed in perm order, then shared) */
+  uint16_t *h_d;       /* [(k+S)*T][I] bf16 SwiGLU rows (routed in perm order, then shared);
+                          tensor-core plans store each run of 8 columns as 0,4,1,5,2,6,3,7 */
   uint16_t *y_d;       /* [(k+S)*T][H] bf16 expert outputs, same row order    */
   int32_t *status_d;   /* [1] sticky device status (moe_status values)        */
   uint64_t *trace_d;   /* [MOE_TRACE_CTAS][MOE_TRACE_SLOTS] phase timestamps (ns), MOE_FLAG_TRACE */

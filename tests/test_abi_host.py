@@ -67,9 +67,9 @@ def test_workspace_size_covers_buffers(lib):
     need = moe.moe_workspace_bytes(plan)
     T, E, k, H, I = 4096, 256, 8, 2048, 512
     # keys, top-k, perm/inv, h and y, the router's bf16 split, normalised x, and
-    # the routed x rows gathered in perm order for the tensor-core gate/up GEMM
+    # the x rows gathered in block-map row order for the tensor-core gate/up GEMM
     floor = (T * E * 4 + 2 * T * k * 4 + 2 * k * T * 4 + (k + 1) * T * (I + H) * 2 + 3 * E * H * 2 + T * H * 2
-             + k * T * H * 2)
+             + (k + 1) * T * H * 2)
     assert floor <= need <= floor * 1.01 + (1 << 20)
     assert lib.moe_workspace_bytes(None) == 0
 
