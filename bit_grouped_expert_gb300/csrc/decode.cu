@@ -808,14 +808,6 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       ok = __syncthreads_and(gotw) != 0;
       if (!ok) break;
       trace(15, l);
-      // the next layer's shared down rows, into the slots just read
-      if (l + 1 < a.nl) {
-        ptx::fence_proxy_async_smem();
-        if (tid == 0) expect_tx(bar_dsh, dsh_bytes);
-        __syncthreads();
-        issue_dsh(l + 1);
-        n_dsh = l + 2;
-      }
       // y_j = bf16(h_j . Wd_j) of every (row, slot) in parallel, then the combine
       float *ys = reinterpret_cast<float *>(sm + a.off_ys);  // [nou * 8][NS]
       for (int t = tid; t < nou * 8 * NS; t += DTHREADS) {
@@ -842,6 +834,15 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         const uint32_t other = __shfl_xor_sync(0xffffffffu, ob, 1);
         if (tid < nou * 8 && !(tid & 1))
           st_relaxed64(a.tr + (size_t)((ep + 1u) & 1u) * (H / 2) + n / 2, tagged(ep + 1u, ob | (other << 16)));
+      }
+      // the next layer's shared down rows, into the slots the down items have
+      // finished with (after the residual words, which every CTA waits for)
+      if (l + 1 < a.nl) {
+        ptx::fence_proxy_async_smem();
+        if (tid == 0) expect_tx(bar_dsh, dsh_bytes);
+        __syncthreads();
+        issue_dsh(l + 1);
+        n_dsh = l + 2;
       }
       trace(16, l);
     }

@@ -160,35 +160,63 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t *__restrict_
   write_map(blockmap, n_tiles, max_tiles, BN, tb);
   if (blockmap2) write_map(blockmap2, n_tiles2, max_tiles2, BN2, tb2);
   if (ce == 0) return;
+  // Tokens in rounds of blockDim.x * TPT: thread tid takes TPT consecutive
+  // tokens, so (thread, token) order is token order and a block-wide scan of
+  // the per-thread match counts gives every match its rank.
+  constexpr int TPT = 4;
+  const bool vec = (k % 4) == 0;  // a token's k ids as int4 loads (rows are 16-byte aligned)
   int running = 0;
-  for (int t0 = 0; t0 < T; t0 += blockDim.x) {
-    const int t = t0 + tid;
-    int jf = -1;
-    if (t < T) {
-      for (int j = 0; j < k; ++j)
-        if (topk_id[(size_t)t * k + j] == e) jf = j;
+  for (int t0 = 0; t0 < T; t0 += blockDim.x * TPT) {
+    int jf[TPT];
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < TPT; ++i) {
+      const int t = t0 + tid * TPT + i;
+      jf[i] = -1;
+      if (t < T) {
+        const int32_t *row = topk_id + (size_t)t * k;
+        if (vec) {
+          for (int j4 = 0; j4 < k; j4 += 4) {
+            const int4 v = *reinterpret_cast<const int4 *>(row + j4);
+            if (v.x == e) jf[i] = j4;
+            if (v.y == e) jf[i] = j4 + 1;
+            if (v.z == e) jf[i] = j4 + 2;
+            if (v.w == e) jf[i] = j4 + 3;
+          }
+        } else {
+          for (int j = 0; j < k; ++j)
+            if (row[j] == e) jf[i] = j;
+        }
+      }
+      c += jf[i] >= 0;
     }
-    const bool flag = jf >= 0;
-    const uint32_t ballot = __ballot_sync(0xffffffffu, flag);
-    const int wrank = __popc(ballot & ((1u << lane) - 1u));
-    if (lane == 0) s_warp[wid] = __popc(ballot);
+    int incl = c;  // inclusive scan of the counts over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp[wid] = incl;
     __syncthreads();
     int before = 0, total = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      int c = s_warp[w];
-      before += (w < wid) ? c : 0;
-      total += c;
+      const int cw = s_warp[w];
+      before += (w < wid) ? cw : 0;
+      total += cw;
     }
-    if (flag) {
-      const int pos = off + running + before + wrank;
-      const int p = t * k + jf;
+    int pos = off + running + before + incl - c;
+#pragma unroll
+    for (int i = 0; i < TPT; ++i) {
+      if (jf[i] < 0) continue;
+      const int p = (t0 + tid * TPT + i) * k + jf[i];
       if (pos < off + ce) {  // always checked: a stale histogram must not write out of bounds
         perm[pos] = p;
         inv[p] = pos;
       } else {
         set_status(status, MOE_ERR_DEVICE_BOUNDS);
       }
+      ++pos;
     }
     running += total;
     __syncthreads();
