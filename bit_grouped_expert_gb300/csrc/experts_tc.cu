@@ -429,6 +429,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ dequant + epilogue
     // Work unit u = kb * NMAT + mat (one k-block of one matrix) goes to
     // warpgroup u % NWG; epilogue chunks of 16 columns are dealt the same way.
+    // A slot's free barrier is waited on by phase parity, which is exact only
+    // while the waiter is at most one phase ahead of the slot.  That holds
+    // here: a warpgroup's consecutive units are at most 2 (gate/up) or 3
+    // (down) k-blocks apart, so its previous wait already saw the MMA past
+    // k-block kb - 8, and every warp meets the MMA at the end of each item
+    // (acc_full) before it starts the next.  A different unit order, or an
+    // epilogue moved past the next item's first units, must keep this.
     const int wg = (warp - 4) >> 2, q = warp & 3;
     const int row = q * 32 + lane;  // weight row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
