@@ -53,6 +53,7 @@ constexpr int KCH = 256;   // codes per K-chunk: 4 groups, 128 bytes of a code r
 constexpr int XPAD = 72;   // bf16 slots per 64-value group of x / h in shared memory
 constexpr int MAX_RU = 8;  // routed gate/up units (mbarriers) per CTA
 constexpr int MAXL = 7;    // layers per launch (the parameters stay under 4 KB)
+constexpr int DN_ITEMS = 4;  // down items (output unit, slot, K-chunk) per warp at most
 constexpr int XREG = 4;    // uint2 of r a thread holds in the RMSNorm: H <= 4 * XREG * DTHREADS
 constexpr unsigned long long DTIMEOUT_NS = 1000000000ull;
 
@@ -90,7 +91,7 @@ struct DecArgs {
   int n_su, rp_cta0, rp_ctas, n_ru, n_ou;
   int max_su, max_ru, max_ou;  // per-CTA maxima (strides of the scale images)
   // shared-memory layout (bytes from the 1024-aligned base)
-  int off_dc, off_ru, off_su, off_rr, off_x, off_xn, off_h, off_ds, off_rus, off_sus, off_red, off_keys, off_cand,
+  int off_dc, off_ru, off_su, off_rr, off_x, off_xn, off_h, off_rus, off_sus, off_red, off_keys, off_cand,
       off_gmax, off_bar, off_ys;
 };
 static_assert(sizeof(DecArgs) <= 4000, "kernel parameters stay under 4 KB");
@@ -198,19 +199,19 @@ __device__ __forceinline__ uint4 perm8(uint32_t v0, uint32_t v1, uint32_t v2, ui
 }
 
 // x . W over one K-chunk of 8 rows.  chunk: the swizzled [8][128 B] code
-// image of the chunk; s, b: the rows' scales and biases ([8][gpr] bf16);
-// xg: the chunk's first group of the permuted vector.  Lane (g, q) takes
+// image of the chunk; sv, bv: the scale and bias of this lane's group (row g,
+// group q of the chunk); xg: the chunk's first group of the permuted vector.  Lane (g, q) takes
 // group q of the chunk in row g; the weights are the A operand: rows g and
 // g+8 of A are codes {j, j+4 : j = 0, 1} and {j, j+4 : j = 2, 3} of a word of
 // row g, and B columns 0 and 1 (lanes g = 0 and 1) carry the matching x
 // values, so D[g][0] + D[g+8][1] sums row g over the 32 values of the word
 // and its three quad partners.  Returns row g's sum in the lanes with q == 0.
-__device__ __forceinline__ float gemv_chunk(const uint8_t *chunk, const uint16_t *s, const uint16_t *b, int gpr,
-                                            int grp, const uint16_t *xg, int g, int q) {
+__device__ __forceinline__ float gemv_chunk(const uint8_t *chunk, uint16_t sv, uint16_t bv, const uint16_t *xg, int g,
+                                            int q) {
   const uint8_t *row = chunk + g * 128;
   const uint4 c0 = *reinterpret_cast<const uint4 *>(row + (((2 * q) ^ g) << 4));
   const uint4 c1 = *reinterpret_cast<const uint4 *>(row + (((2 * q + 1) ^ g) << 4));
-  const __nv_bfloat162 s2 = bf16x2_splat(s[g * gpr + grp]), b2 = bf16x2_splat(b[g * gpr + grp]);
+  const __nv_bfloat162 s2 = bf16x2_splat(sv), b2 = bf16x2_splat(bv);
   const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
   const uint2 *xp = reinterpret_cast<const uint2 *>(xg + q * XPAD) + (g & 1);
   // four accumulators: chains of two dependent MMAs
@@ -262,14 +263,6 @@ __device__ void dn_codes(const DecArgs &a, const DecMaps &mp, int o, uint8_t *cd
     ptx::tma_load_2d(cdst + o * 1024, &mp.down, bar, o * 128, row);
 }
 
-// Down array `which` (0 down_s, 1 down_b) of n output units from row n0 of
-// expert e: n * I/4 bytes, [n][8 rows][I/64] bf16.
-__device__ void dn_scales(const DecArgs &a, const LayerW &L, int which, uint8_t *sdst, int e, int n0, int n,
-                          uint64_t *bar) {
-  const int I = a.I;
-  ptx::bulk_g2s(sdst, (which ? L.w.down_b : L.w.down_s) + ((size_t)e * a.H + n0) * (I / 64), n * (I / 4), bar);
-}
-
 // Partial gate/up dot products of `nu` unit images against x (padded, in
 // shared memory) into red[(u * nkc + kc) * 16 + r] (r < 8 gate rows, 8 + r up
 // rows).  scales: [4 arrays][ustride units][8 rows][H/64] bf16.  Warps split
@@ -288,8 +281,8 @@ __device__ bool gu_compute(const DecArgs &a, const uint8_t *codes, const uint8_t
       if (bars && !(wait_bar(&bars[0], parity, a.status) && wait_bar(&bars[u], parity, a.status))) return false;
       const uint16_t *sc = reinterpret_cast<const uint16_t *>(scales + (size_t)(2 * mat * ustride + u) * (H / 4));
       const uint16_t *bi = reinterpret_cast<const uint16_t *>(scales + (size_t)((2 * mat + 1) * ustride + u) * (H / 4));
-      const float d = gemv_chunk(codes + (size_t)u * 8 * H + mat * 4 * H + kc * 1024, sc, bi, gpr, 4 * kc + q,
-                                 xs + 4 * kc * XPAD, g, q);
+      const float d = gemv_chunk(codes + (size_t)u * 8 * H + mat * 4 * H + kc * 1024, sc[g * gpr + 4 * kc + q],
+                                 bi[g * gpr + 4 * kc + q], xs + 4 * kc * XPAD, g, q);
       if (q == 0) red[(u * nkc + kc) * 16 + mat * 8 + g] = d;
     }
   }
@@ -323,7 +316,9 @@ __device__ void gu_finish(const DecArgs &a, int nu, const float *red, unsigned l
 // lane l holds the codes of experts l, l+32, ...  The k-th largest of the 32
 // lane maxima bounds the k-th largest key from below (k distinct keys reach
 // it), so only the keys at or above it -- at most 8k -- are ranked, each
-// against the others.  Same order and tie rule as topk_block.
+// against the others.  Same order and tie rule as topk_block.  Leaves the
+// ids and their keys by rank in ids and w; topk_weights turns the keys into
+// weights.
 __device__ void topk_warp(const float *keys, int E, int k, unsigned long long *cand, int32_t *ids, float *w,
                           int32_t *status, uint64_t *tr) {
   const int lane = threadIdx.x & 31;
@@ -378,12 +373,18 @@ __device__ void topk_warp(const float *keys, int E, int k, unsigned long long *c
   }
   __syncwarp();
   mark(20);
+}
+
+// The softmax weights of the picked keys (in w, by rank) replace the keys:
+// run by one warp after topk_warp, once the copies the ids decide are on
+// their way.
+__device__ void topk_weights(int k, int32_t *ids, float *w, int32_t *status) {
+  const int lane = threadIdx.x & 31;
   const int my_id = lane < k ? ids[lane] : -1;
   const float my_key = lane < k ? w[lane] : 0.f;
   __syncwarp();
   topk_finish(lane, k, my_id, my_key, ids, w, nullptr, status);
   __syncwarp();
-  mark(21);
 }
 
 // Top-k of one token by all threads of the CTA.  Codes (topk_code) order the
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x, G = gridDim.x;
   const int H = a.H, I = a.I, E = a.E, k = a.k, S = a.S, NS = k + S;
-  uint8_t *dc = sm + a.off_dc, *ru = sm + a.off_ru, *su = sm + a.off_su, *ds = sm + a.off_ds,
+  uint8_t *dc = sm + a.off_dc, *ru = sm + a.off_ru, *su = sm + a.off_su,
           *rus = sm + a.off_rus, *sus = sm + a.off_sus;
   float *rr = reinterpret_cast<float *>(sm + a.off_rr);
   uint16_t *xs = reinterpret_cast<uint16_t *>(sm + a.off_x);   // x, permuted groups (GEMV operand)
@@ -523,24 +524,19 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       }
     }
   };
-  // down scales: [NS slots][2 arrays][max_ou units][8 rows][I/64] bf16
-  auto dn_sc = [&](int j, int which) { return ds + ((j * 2 + which) * a.max_ou) * (I / 4); };
+  // the shared expert's down rows (its scales and biases are loaded into
+  // registers by the down items themselves)
   auto issue_dsh = [&](int l) {
     if (issuer >= 0 && S) {
       const int ndn = code_ops(a, I);
-      for (int o = issuer; o < nou * ndn + 2; o += 2 * DWARPS) {
-        if (o < nou * ndn) {
-          const int ol = o / ndn;
-          dn_codes(a, a.maps[l], o % ndn, dc + (ol * NS + k) * 4 * I, E, o0 + ol * 8, bar_dsh);
-        } else {
-          const int which = o - nou * ndn;
-          dn_scales(a, a.lw[l], which, dn_sc(k, which), E, o0, nou, bar_dsh);
-        }
+      for (int o = issuer; o < nou * ndn; o += 2 * DWARPS) {
+        const int ol = o / ndn;
+        dn_codes(a, a.maps[l], o % ndn, dc + (ol * NS + k) * 4 * I, E, o0 + ol * 8, bar_dsh);
       }
     }
   };
   const uint32_t p1_bytes = (uint32_t)(nsu * 9 * H + nre * 4 * H);
-  const uint32_t dsh_bytes = S ? (uint32_t)(nou * (4 * I + I / 2)) : 0u;
+  const uint32_t dsh_bytes = S ? (uint32_t)(nou * 4 * I) : 0u;
 
   if (tid == 0) {
     for (int i = 0; i < 3 + MAX_RU; ++i) ptx::mbar_init(&bars[i], 1);
@@ -725,14 +721,10 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     if (tid == 0) {
       // unit 0's barrier also takes every unit's scales
       for (int i = 0; i < nru; ++i) expect_tx(&bar_ru[i], (uint32_t)(8 * H + (i ? 0 : nru * H)));
-      expect_tx(bar_drt, (uint32_t)(nou * k * (4 * I + I / 2)));
+      expect_tx(bar_drt, (uint32_t)(nou * k * 4 * I));
     }
     __syncthreads();
     trace(8, l);
-    if (cta == 0 && tid < k) {
-      a.topk_id[tid] = s_ids[tid];
-      a.topk_w[tid] = s_w[tid];
-    }
     n_drt = l + 1;
     // the gate/up rows first (a block barrier keeps the down rows behind them
     // in the copy engine's queue): the scales of the unit run (one or two runs
@@ -752,16 +744,19 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       }
     }
     __syncthreads();
-    if (issuer >= 0) {  // routed down rows: code images per (unit, slot), scales per (slot, array)
+    if (issuer >= 0) {  // routed down rows: code images per (unit, slot)
       const int ndn = code_ops(a, I), nc = nou * k * ndn;
-      for (int o = issuer; o < nc + 2 * k; o += 2 * DWARPS) {
-        if (o < nc) {
-          const int b = o / ndn, ol = b / k, j = b % k;
-          dn_codes(a, a.maps[l], o % ndn, dc + (ol * NS + j) * 4 * I, s_ids[j], o0 + ol * 8, bar_drt);
-        } else {
-          const int j = (o - nc) >> 1, which = (o - nc) & 1;
-          dn_scales(a, L, which, dn_sc(j, which), s_ids[j], o0, nou, bar_drt);
-        }
+      for (int o = issuer; o < nc; o += 2 * DWARPS) {
+        const int b = o / ndn, ol = b / k, j = b % k;
+        dn_codes(a, a.maps[l], o % ndn, dc + (ol * NS + j) * 4 * I, s_ids[j], o0 + ol * 8, bar_drt);
+      }
+    }
+    // the weights (only the combine needs them) while the copies are in flight
+    if (warp == 0) {
+      if (E <= 256) topk_weights(k, s_ids, s_w, a.status);
+      if (cta == 0 && tid < k) {
+        a.topk_id[tid] = s_ids[tid];
+        a.topk_w[tid] = s_w[tid];
       }
     }
     trace(9, l);
@@ -787,9 +782,26 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       const int nkcd = I / KCH, gpr = I / 64, g = lane >> 2, q = lane & 3;
       const int nitem = nou * NS * nkcd;
       uint16_t *hwb = hs + warp * 4 * XPAD;  // this warp's 4 padded groups
+      // this lane's scale and bias for each of the warp's items (row g, group
+      // q of the chunk), loaded while h is on its way
+      uint16_t dsv[DN_ITEMS], dbv[DN_ITEMS];
+#pragma unroll
+      for (int i = 0; i < DN_ITEMS; ++i) {
+        const int t = warp + i * DWARPS;
+        dsv[i] = dbv[i] = 0;
+        if (t < nitem) {
+          const int kc = t % nkcd, j = (t / nkcd) % NS, ol = t / (nkcd * NS);
+          const size_t at = ((size_t)(j < k ? s_ids[j] : E) * H + o0 + ol * 8 + g) * gpr + 4 * kc + q;
+          dsv[i] = __ldg(L.w.down_s + at);
+          dbv[i] = __ldg(L.w.down_b + at);
+        }
+      }
       bool gotw = wait_bar(bar_drt, ph, a.status) && wait_bar(bar_dsh, ph, a.status);
       trace(12, l);
-      for (int t = warp; t < nitem && __all_sync(0xffffffffu, gotw); t += DWARPS) {
+#pragma unroll
+      for (int i = 0; i < DN_ITEMS; ++i) {
+        const int t = warp + i * DWARPS;
+        if (t >= nitem || !__all_sync(0xffffffffu, gotw)) break;
         const int kc = t % nkcd, j = (t / nkcd) % NS, ol = t / (nkcd * NS);
         const int w0 = (j * I + kc * KCH) / 2 + 4 * lane;  // words of values 8*lane .. +7 of the chunk
         const int idx[4] = {w0, w0 + 1, w0 + 2, w0 + 3};
@@ -799,9 +811,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         *reinterpret_cast<uint4 *>(hwb + (lane >> 3) * XPAD + (lane & 7) * 8) =
             perm8((uint32_t)w[0], (uint32_t)w[1], (uint32_t)w[2], (uint32_t)w[3]);
         __syncwarp();
-        const uint16_t *sc = reinterpret_cast<const uint16_t *>(dn_sc(j, 0) + ol * (I / 4));
-        const uint16_t *bi = reinterpret_cast<const uint16_t *>(dn_sc(j, 1) + ol * (I / 4));
-        const float d = gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, sc, bi, gpr, 4 * kc + q, hwb, g, q);
+        const float d = gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, dsv[i], dbv[i], hwb, g, q);
         if (q == 0) red[t * 8 + g] = d;
         __syncwarp();  // every lane has read the buffer before the next item overwrites it
       }
@@ -905,8 +915,6 @@ DecPlan make_plan(int H, int E, int k, int I, int S, int num_sms) {
   o = al(o + H * 2, 128);
   a.off_h = o;  // per-warp down buffers: 4 padded groups (one K-chunk of h) each
   o = al(o + DWARPS * 4 * XPAD * 2, 128);
-  a.off_ds = o;
-  o = al(o + max_ou * NS * (I / 2), 128);
   a.off_rus = o;
   o = al(o + max_ru * H, 128);
   a.off_sus = o;
@@ -988,7 +996,8 @@ bool decode_supported(int H, int E, int k, int I, int S, int num_sms) {
       E > 1024)
     return false;
   DecPlan p = make_plan(H, E, k, I, S, num_sms);
-  return p.max_ru <= MAX_RU && p.smem <= decode_smem_limit();
+  const int dn_items = p.a.max_ou * (k + S) * (I / KCH);  // down items of the busiest CTA
+  return p.max_ru <= MAX_RU && dn_items <= DN_ITEMS * DWARPS && p.smem <= decode_smem_limit();
 }
 
 cudaError_t decode_prepare(int H, int E, int k, int I, int S, int num_sms) {
