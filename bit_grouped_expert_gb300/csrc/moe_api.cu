@@ -33,7 +33,8 @@ int tiles_bound(int T, int k, int E, int S, int BN) {
   return (k * T + BN - 1) / BN + E + (S ? (T + BN - 1) / BN : 0);
 }
 
-moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_tiles2, bool tc) {
+moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_tiles2, bool tc,
+                        size_t rpart_floats = 0) {
   moe::Layout L;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -60,6 +61,7 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_ti
   L.y = take((k + S) * T * H * 2);
   L.xg = take(tc ? (k + S) * T * H * 2 : 0);  // x rows gathered in block-map row order (tensor-core gate/up)
   L.rsplit = take(3 * E * H * 2);
+  L.rpart = take(rpart_floats * 4);  // the tensor-core router's K-slice partial sums
   L.xn = take(T * H * 2);  // normalised x of pre-norm plans
   L.trace = take(MOE_TRACE_CTAS * MOE_TRACE_SLOTS * 8);
   L.total = o;
@@ -122,10 +124,10 @@ moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const fl
   if (err != cudaSuccess) return cuda_status(err);
   if (!from_keys) {
     if (p->use_router_tc && T >= moe::ROUTER_TC_MIN_T) {
-      err = moe::launch_router_tc(x, T, c.hidden, router, c.n_experts, bias, moe::ws_ptr<uint16_t>(ws, L.rsplit), keys,
-                                  status, p->num_sms, s);
+      err = moe::launch_router_tc(x, T, c.hidden, router, c.n_experts, bias, moe::ws_ptr<uint16_t>(ws, L.rsplit),
+                                  moe::ws_ptr<float>(ws, L.rpart), keys, status, p->num_sms, s);
       if (err != cudaSuccess) return cuda_status(err);
-      *launches += 2;
+      *launches += moe::router_tc_slices(T, c.n_experts, c.hidden, p->num_sms) > 1 ? 3 : 2;
     } else {
       if ((err = moe::launch_router_logits(x, T, c.hidden, router, c.n_experts, bias, keys, s)) != cudaSuccess)
         return cuda_status(err);
@@ -285,6 +287,9 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
     if (p->num_sms > 0 && moe::router_tc_supported(c.n_experts, c.hidden)) {
       p->use_router_tc = moe::router_tc_prepare() == cudaSuccess;
       if (!p->use_router_tc) cudaGetLastError();
+      if (p->use_router_tc)  // room for its K-slice partial sums
+        p->lay = make_layout(c, max_tokens, p->max_tiles, p->max_tiles2, p->use_tc,
+                             moe::router_tc_partial_floats(max_tokens, c.n_experts, c.hidden, p->num_sms));
     }
   } else {
     cudaGetLastError();  // no device: host-side checks still work, launches report MOE_ERR_CUDA

@@ -13,7 +13,10 @@
 //   router_tc_kernel     D[e][t] = sum over parts of A_p[e] . x[t] (tcgen05,
 //                        A and B from shared memory, fp32 accumulate in
 //                        tensor memory), keys[t][e] = D + bias[e]
-// One work item = 128 experts x N tokens (N = 32/64/128 by T); warp 0 issues
+// One work item = 128 experts x N tokens (N = 32/64/128 by T) x one of KS
+// slices of K (KS chosen so that the items fill the SMs; with KS > 1 each
+// item writes fp32 partial sums and router_reduce_kernel adds the KS slices
+// in order, so the keys do not depend on timing); warp 0 issues
 // TMA (three 128x64 A boxes + one N x 64 B box per k-block, 128B swizzle),
 // warp 1 issues the MMAs, warps 4-7 drain the accumulator.  Waits are bounded
 // as in the expert kernels.
@@ -38,10 +41,10 @@ constexpr int R_SMEM = RSTAGES * R_STAGE + 1024 + 1024;
 constexpr unsigned long long R_TIMEOUT_NS = 1000000000ull;
 
 struct RArgs {
-  float *keys;
-  const float *bias;
+  float *keys;     // [T][E] keys, or with KS > 1 the partial sums [KS][T][E]
+  const float *bias;  // added when KS == 1 (else by the reduction)
   int32_t *status;
-  int T, E, H, N;
+  int T, E, H, N, KS;
 };
 
 struct RMisc {
@@ -135,8 +138,8 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = m->tmem;
   const int MT = a.E / RM;
-  const int n_items = ((a.T + a.N - 1) / a.N) * MT;
-  const int KB = a.H / RKB;
+  const int n_items = ((a.T + a.N - 1) / a.N) * MT * a.KS;
+  const int KB = a.H / RKB / a.KS;  // k-blocks of one slice
   const uint32_t b_bytes = (uint32_t)a.N * 128u;
 
   if (warp == 0) {
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       uint32_t c = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int tt = item / MT, et = item - tt * MT;
+        const int ks = item % a.KS, ti = item / a.KS, tt = ti / MT, et = ti - tt * MT;
         for (int kb = 0; kb < KB; ++kb, ++c) {
           const int s = c % RSTAGES;
           if (!rwait(&m->empty[s], ((c / RSTAGES) & 1u) ^ 1u, m, a.status)) {
@@ -154,10 +157,11 @@ __global__ void __launch_bounds__(RTHREADS, 1)
             break;
           }
           uint8_t *st = smem + s * R_STAGE;
+          const int k0 = (ks * KB + kb) * RKB;
           ptx::mbar_arrive_expect_tx(&m->full[s], 3u * A_PART + b_bytes);
           for (int p = 0; p < 3; ++p)
-            ptx::tma_load_2d(st + p * A_PART, &tma, &m->full[s], kb * RKB, p * a.E + et * RM);
-          ptx::tma_load_2d(st + 3 * A_PART, &tmb, &m->full[s], kb * RKB, tt * a.N);
+            ptx::tma_load_2d(st + p * A_PART, &tma, &m->full[s], k0, p * a.E + et * RM);
+          ptx::tma_load_2d(st + 3 * A_PART, &tmb, &m->full[s], k0, tt * a.N);
         }
       }
       if (!ok) {
@@ -202,11 +206,12 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t itc = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const int tt = item / MT, et = item - tt * MT;
+      const int ks = item % a.KS, ti = item / a.KS, tt = ti / MT, et = ti - tt * MT;
       if (!__all_sync(0xffffffffu, rwait(&m->acc_full, itc & 1u, m, a.status))) break;
       ptx::tc_fence_after();
       const int e = et * RM + e_local;
-      const float b = a.bias ? a.bias[e] : 0.f;
+      const float b = (a.bias && a.KS == 1) ? a.bias[e] : 0.f;
+      float *out = a.keys + (size_t)ks * a.T * a.E;
       for (int ch = 0; ch < a.N / 16; ++ch) {
         uint32_t v[16];
         ptx::tmem_ld_x16(tmem + lane_base + ch * 16, v);
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int t = tt * a.N + ch * 16 + i;
-          if (t < a.T) a.keys[(size_t)t * a.E + e] = a.bias ? __uint_as_float(v[i]) + b : __uint_as_float(v[i]);
+          if (t < a.T) out[(size_t)t * a.E + e] = __uint_as_float(v[i]) + b;
         }
       }
       ptx::tc_fence_before();
@@ -228,6 +233,30 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 128);
   }
+}
+
+// keys = sum of the KS partial slices in slice order (+ bias), 4 keys a thread.
+__global__ void __launch_bounds__(256) router_reduce_kernel(const float4 *__restrict__ part, size_t n4, int KS,
+                                                            int E4, const float4 *__restrict__ bias,
+                                                            float4 *__restrict__ keys) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  float4 acc = part[i];
+  for (int s = 1; s < KS; ++s) {
+    const float4 v = part[(size_t)s * n4 + i];
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  if (bias) {
+    const float4 b = bias[i % E4];
+    acc.x += b.x;
+    acc.y += b.y;
+    acc.z += b.z;
+    acc.w += b.w;
+  }
+  keys[i] = acc;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
@@ -250,12 +279,33 @@ cudaError_t bf16_map(CUtensorMap *map, const void *base, int rows, int cols, int
 
 bool router_tc_supported(int E, int H) { return E % RM == 0 && H % RKB == 0; }
 
+namespace {
+int router_n(int T) { return T >= 2048 ? 128 : (T >= 512 ? 64 : 32); }
+}  // namespace
+
+int router_tc_slices(int T, int E, int H, int num_sms) {
+  const int items = ((T + router_n(T) - 1) / router_n(T)) * (E / RM), kb = H / RKB;
+  int ks = 1;
+  while (ks < 8 && items * ks * 2 <= num_sms && kb % (ks * 2) == 0 && kb / (ks * 2) >= 4) ks *= 2;
+  return ks;
+}
+
+size_t router_tc_partial_floats(int Tmax, int E, int H, int num_sms) {
+  size_t most = 0;
+  for (int T = 1; T <= Tmax; ++T) {
+    const int ks = router_tc_slices(T, E, H, num_sms);
+    if (ks > 1 && (size_t)ks * T > most) most = (size_t)ks * T;
+  }
+  return most * (size_t)E;
+}
+
 cudaError_t router_tc_prepare() {
   return cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, R_SMEM);
 }
 
 cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
-                             uint16_t *split, float *keys, int32_t *status, int num_sms, cudaStream_t s) {
+                             uint16_t *split, float *partial, float *keys, int32_t *status, int num_sms,
+                             cudaStream_t s) {
   const size_t n = (size_t)E * H;
   prof_before(MOE_KERNEL_ROUTER, s);
   router_split_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(
@@ -263,13 +313,19 @@ cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *route
       reinterpret_cast<uint2 *>(split + n), reinterpret_cast<uint2 *>(split + 2 * n));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int N = T >= 2048 ? 128 : (T >= 512 ? 64 : 32);
+  const int N = router_n(T), KS = router_tc_slices(T, E, H, num_sms);
   CUtensorMap ta, tb;
   if ((e = bf16_map(&ta, split, 3 * E, H, RM)) != cudaSuccess) return e;
   if ((e = bf16_map(&tb, x, T, H, N)) != cudaSuccess) return e;
-  RArgs a{keys, bias, status, T, E, H, N};
-  const int items = ((T + N - 1) / N) * (E / RM);
+  RArgs a{KS > 1 ? partial : keys, bias, status, T, E, H, N, KS};
+  const int items = ((T + N - 1) / N) * (E / RM) * KS;
   router_tc_kernel<<<items < num_sms ? items : num_sms, RTHREADS, R_SMEM, s>>>(ta, tb, a);
+  if (KS > 1 && (e = cudaGetLastError()) == cudaSuccess) {
+    const size_t n4 = (size_t)T * E / 4;
+    router_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
+        reinterpret_cast<const float4 *>(partial), n4, KS, E / 4, reinterpret_cast<const float4 *>(bias),
+        reinterpret_cast<float4 *>(keys));
+  }
   prof_after(MOE_KERNEL_ROUTER, s);
   return cudaGetLastError();
 }

@@ -32,8 +32,14 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
 bool router_tc_supported(int E, int H);
 cudaError_t router_tc_prepare();
 // split: workspace for three bf16 copies of the router ([3][E][H]).
+// K slices of the router GEMM at T tokens (1, 2, 4 or 8: enough items for
+// the SMs), and the fp32 partial-sum buffer a plan for up to Tmax tokens needs.
+int router_tc_slices(int T, int E, int H, int num_sms);
+size_t router_tc_partial_floats(int Tmax, int E, int H, int num_sms);
+// partial: workspace of router_tc_partial_floats floats (16-byte aligned).
 cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
-                             uint16_t *split, float *keys, int32_t *status, int num_sms, cudaStream_t s);
+                             uint16_t *split, float *partial, float *keys, int32_t *status, int num_sms,
+                             cudaStream_t s);
 constexpr int ROUTER_TC_MIN_T = 32;  // below this the CUDA-core router is used
 
 }  // namespace moe
