@@ -53,7 +53,7 @@ class _Dims(ctypes.Structure):
 
 class _Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
-        "router", "gate_q", "up_q", "gate_s", "gate_b", "up_s", "up_b", "down_q", "down_s", "down_b")]
+        "router", "gate_q", "up_q", "gate_s", "gate_b", "up_s", "up_b", "down_q", "down_s", "down_b", "shared_gate")]
 
 
 def _load():
@@ -170,7 +170,8 @@ def moe_layer(dims: Dims, x: np.ndarray, W: dict, res: np.ndarray | None = None,
     """Run the whole layer on the CPU.  ``W`` holds the packed arrays (see
     ``synthetic.experts``) stacked over E + n_shared experts plus ``router``.
     ``keys`` (optional) replaces the oracle's own router output with given
-    fp32 selection keys.  Returns out (bf16 bits), out_exact (fp64 before the
+    fp32 selection keys.  ``W["shared_gate"]`` (optional, fp32 [H]) scales the
+    shared expert's output by sigmoid(x . gate).  Returns out (bf16 bits), out_exact (fp64 before the
     final rounding) and, with ``intermediates``, keys/ids/w/h/y."""
     T = x.shape[0]
     H, E, k, I, S = dims.H, dims.E, dims.k, dims.I, dims.n_shared
@@ -180,6 +181,8 @@ def moe_layer(dims: Dims, x: np.ndarray, W: dict, res: np.ndarray | None = None,
     keep = {}
     arrs = {n: np.ascontiguousarray(W[n]) for n in
             ("router", "gate_q", "up_q", "gate_s", "gate_b", "up_s", "up_b", "down_q", "down_s", "down_b")}
+    sg = W.get("shared_gate")
+    arrs["shared_gate"] = None if sg is None else np.ascontiguousarray(sg, np.float32)
     cw = _Weights(*[_p(arrs[f[0]]) for f in _Weights._fields_])
     cd = _Dims(H, E, k, I, S, dims.G)
     if intermediates:

@@ -115,7 +115,10 @@ def moe_layer(x, W: dict, E: int, k: int, n_shared: int, res=None, bias=None, ke
         y[pairs // k, pairs % k] = yt
     acc = bf16_value(x if res is None else res).copy()
     if n_shared:
-        acc = acc + ffn(E, xd)
+        g = 1.0  # optional shared-expert gate: sigmoid of the expert input's dot with it
+        if W.get("shared_gate") is not None:
+            g = (1.0 / (1.0 + np.exp(-(xd @ np.asarray(W["shared_gate"], np.float64)))))[:, None]
+        acc = acc + g * ffn(E, xd)
     for j in range(k):
         acc = acc + w[:, j:j + 1] * y[:, j]
     return round_bf16_bits(acc), acc, keys, ids, w

@@ -312,9 +312,16 @@ int orc_moe_layer(const orc_dims *d, const uint16_t *x, const uint16_t *res, int
 
 #pragma omp parallel for schedule(static)
   for (int t = 0; t < T; ++t) {
+    /* optional shared-expert gate: g = 1 / (1 + exp(-x . gate)), x the expert input */
+    double g = 1.0;
+    if (S && W->shared_gate) {
+      double z = 0.0;
+      for (int h = 0; h < H; ++h) z += xd[(size_t)t * H + h] * (double)W->shared_gate[h];
+      g = 1.0 / (1.0 + exp(-z));
+    }
     for (int n = 0; n < H; ++n) {
       double acc = orc_bf16_to_double((res ? res : x)[(size_t)t * H + n]);
-      if (S) acc += orc_bf16_to_double(yrows[(P + (size_t)t) * H + n]);
+      if (S) acc += g * orc_bf16_to_double(yrows[(P + (size_t)t) * H + n]);
       for (int j = 0; j < k; ++j) {
         size_t row = (size_t)inv[(size_t)t * k + j];
         acc += w[(size_t)t * k + j] * orc_bf16_to_double(yrows[row * H + n]);

@@ -43,6 +43,8 @@ typedef struct {
   const uint16_t *up_s, *up_b;            /* [E+S][I][H/G] bf16                */
   const uint32_t *down_q;                 /* [E+S][H][I/8]                     */
   const uint16_t *down_s, *down_b;        /* [E+S][H][I/G] bf16                */
+  const float *shared_gate;               /* [H] fp32 or NULL: the shared expert's
+                                             output is scaled by sigmoid(x . gate) */
 } orc_weights;
 
 double orc_bf16_to_double(uint16_t h);

@@ -21,7 +21,7 @@ _SRC = [os.path.join(_HERE, "gen.c")]
 _lock = threading.Lock()
 _lib = None
 
-T_X, T_ROUTER, T_RESID = 1, 2, 13
+T_X, T_ROUTER, T_RESID, T_SHGATE = 1, 2, 13, 14
 
 
 def build(force: bool = False) -> str:
@@ -85,6 +85,13 @@ def router(seed: int, E: int, H: int, layer: int = 0, std: float = 0.02) -> np.n
     """Router weight [E, H] fp32 ~ N(0, std)."""
     out = np.empty((E, H), dtype=np.float32)
     _load().syn_fill_normal_f32(key(seed, T_ROUTER, layer), 0.0, std, _p(out), out.size)
+    return out
+
+
+def shared_gate(seed: int, H: int, layer: int = 0, std: float = 0.02) -> np.ndarray:
+    """Shared-expert gate vector [H] fp32 ~ N(0, std)."""
+    out = np.empty(H, dtype=np.float32)
+    _load().syn_fill_normal_f32(key(seed, T_SHGATE, layer), 0.0, std, _p(out), out.size)
     return out
 
 

@@ -34,7 +34,8 @@ enum {
   SYN_T_UP_Q = 6, SYN_T_UP_S = 7, SYN_T_UP_B = 8,
   SYN_T_DOWN_Q = 9, SYN_T_DOWN_S = 10, SYN_T_DOWN_B = 11,
   SYN_T_ZIPF = 12,   /* permutation behind the Zipf expert ranking   */
-  SYN_T_RESID = 13   /* a separate residual stream [T][H] bf16        */
+  SYN_T_RESID = 13,  /* a separate residual stream [T][H] bf16        */
+  SYN_T_SHGATE = 14  /* shared-expert gate vector [H] fp32 ~ N(0, 0.02) */
 };
 
 uint64_t syn_key(uint64_t seed, uint32_t tensor, uint32_t layer, uint32_t expert);

@@ -284,6 +284,35 @@ def test_layer_matches_brute_force(T, n_shared, centred, with_bias):
     np.testing.assert_allclose(r["keys"], lib, rtol=0, atol=np.abs(lib).max() * 2 ** -22)
 
 
+@pytest.mark.parametrize("T", [1, 7, 33])
+def test_layer_shared_gate_matches_brute_force(T):
+    """The optional shared-expert gate, sigmoid(x . gate) on the shared
+    expert's output, against the numpy statement (separate residual: the gate
+    reads the expert input x, not the residual)."""
+    d, W = _tiny_weights(50 + T)
+    W["shared_gate"] = syn.shared_gate(50 + T, d.H)
+    x = syn.activations(50 + T, T, d.H)
+    res = syn.activations(50 + T, T, d.H, tensor=syn.T_RESID)
+    r = orc.moe_layer(d, x, W, res=res, intermediates=True)
+    bo, bx, keys, ids, w = brute.moe_layer(x, W, d.E, d.k, 1, res=res, keys=r["keys"])
+    np.testing.assert_array_equal(ids, r["ids"])
+    np.testing.assert_allclose(bx, r["out_exact"], rtol=0, atol=1e-10 * max(1.0, np.abs(bx).max()))
+
+
+def test_layer_zero_shared_gate_halves_the_shared_expert():
+    """gate = 0 gives sigmoid(0) = 1/2: the output moves by exactly half the
+    shared expert's (bf16) output against the ungated layer."""
+    d, W = _tiny_weights(61)
+    x = syn.activations(61, 20, d.H)
+    plain = orc.moe_layer(d, x, W, intermediates=True)
+    W["shared_gate"] = np.zeros(d.H, np.float32)
+    gated = orc.moe_layer(d, x, W, intermediates=True)
+    y_sh = bf16_value(plain["y"][d.k * 20:])
+    np.testing.assert_array_equal(plain["y"], gated["y"])
+    np.testing.assert_allclose(gated["out_exact"], plain["out_exact"] - 0.5 * y_sh, rtol=0,
+                               atol=1e-12 * np.abs(plain["out_exact"]).max())
+
+
 def test_layer_zero_expert_weights_return_residual():
     d, W = _tiny_weights(1)
     for n in ("gate_s", "gate_b", "up_s", "up_b", "down_s", "down_b"):
