@@ -69,7 +69,7 @@ class moe_config(ctypes.Structure):
 
 class moe_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("router_d", "gate_q_d", "up_q_d", "gate_s_d", "gate_b_d", "up_s_d",
-                                               "up_b_d", "down_q_d", "down_s_d", "down_b_d")]
+                                               "up_b_d", "down_q_d", "down_s_d", "down_b_d", "shared_gate_d")]
 
 
 class moe_route_ptrs(ctypes.Structure):
@@ -195,9 +195,9 @@ def moe_workspace_init(plan: Plan, ws, stream=None):
 
 
 def make_weights(w: dict) -> moe_weights:
-    """moe_weights from a dict of device tensors (keys: router, gate_q, ...).
-    The caller keeps the tensors alive."""
-    return moe_weights(*[_ptr(w[n[:-2]]) for n, _ in moe_weights._fields_])
+    """moe_weights from a dict of device tensors (keys: router, gate_q, ...;
+    shared_gate optional).  The caller keeps the tensors alive."""
+    return moe_weights(*[_ptr(w.get(n[:-2])) for n, _ in moe_weights._fields_])
 
 
 def moe_route(plan: Plan, x, T: int, router, logit_bias, ws, stream=None):

@@ -1,8 +1,9 @@
 // Weighted gather-combine, RMSNorm and the dequantisation test hook.
 //
-// combine:  out[t] = bf16(res[t] + y_shared[t] + sum_j w[t,j] * y[inv[t*k+j]])
+// combine:  out[t] = bf16(res[t] + g[t] * y_shared[t] + sum_j w[t,j] * y[inv[t*k+j]])
 //           fp32, summed in that order (the layer's bf16 weighted gather-combine
-//           with the shared expert's output and a residual add).
+//           with the shared expert's output and a residual add); g[t] = 1, or
+//           with a shared-expert gate vector, sigmoid(x[t] . gate) in fp32.
 // rmsnorm:  x = bf16(r / sqrt(mean(r^2) + eps)), fp32 (between stacked layers).
 // dequant:  w = bf16_rne(scale * q + bias) ("Prefill": 64 weights share one bf16
 //           scale and bias; weights are rebuilt to bf16).
@@ -30,14 +31,40 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
 // One block per token; each thread owns 8 consecutive columns.
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ res, const uint16_t *__restrict__ y,
                                                       const int32_t *__restrict__ inv,
-                                                      const float *__restrict__ topk_w, int T, int H, int k, int S,
+                                                      const float *__restrict__ topk_w, const uint16_t *__restrict__ x,
+                                                      const float *__restrict__ sh_gate, int T, int H, int k, int S,
                                                       uint16_t *__restrict__ out) {
   const int t = blockIdx.x;
   __shared__ int s_row[16];
   __shared__ float s_w[16];
+  __shared__ float s_part[8];
   if (threadIdx.x < k) {
     s_row[threadIdx.x] = inv[(size_t)t * k + threadIdx.x];
     s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+  }
+  float gsh = 1.f;  // the shared expert's gate
+  if (S && sh_gate) {
+    float z = 0.f;
+    for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+      float v[8];
+      unpack8(*reinterpret_cast<const uint4 *>(x + (size_t)t * H + c), v);
+      const float4 g0 = *reinterpret_cast<const float4 *>(sh_gate + c);
+      const float4 g1 = *reinterpret_cast<const float4 *>(sh_gate + c + 4);
+      z = fmaf(v[0], g0.x, z);
+      z = fmaf(v[1], g0.y, z);
+      z = fmaf(v[2], g0.z, z);
+      z = fmaf(v[3], g0.w, z);
+      z = fmaf(v[4], g1.x, z);
+      z = fmaf(v[5], g1.y, z);
+      z = fmaf(v[6], g1.z, z);
+      z = fmaf(v[7], g1.w, z);
+    }
+    z = warp_sum(z);
+    if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = z;
+    __syncthreads();
+    z = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) z += s_part[w];
+    gsh = 1.f / (1.f + expf(-z));
   }
   __syncthreads();
   for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
@@ -46,7 +73,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     if (S) {
       unpack8(*reinterpret_cast<const uint4 *>(y + ((size_t)k * T + t) * H + c), v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += v[i];
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(gsh, v[i], acc[i]);
     }
     for (int j = 0; j < k; ++j) {
       unpack8(*reinterpret_cast<const uint4 *>(y + (size_t)s_row[j] * H + c), v);
@@ -97,10 +124,11 @@ __global__ void dequant_kernel(const uint32_t *__restrict__ q, const uint16_t *_
   *reinterpret_cast<uint4 *>(w + n * K + kw * 8) = *reinterpret_cast<uint4 *>(p);
 }
 
-cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w, int T,
-                           int H, int k, int S, uint16_t *out, cudaStream_t s) {
+cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w,
+                           const uint16_t *x, const float *shared_gate, int T, int H, int k, int S, uint16_t *out,
+                           cudaStream_t s) {
   prof_before(MOE_KERNEL_COMBINE, s);
-  combine_kernel<<<T, 256, 0, s>>>(res, y, inv, topk_w, T, H, k, S, out);
+  combine_kernel<<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out);
   prof_after(MOE_KERNEL_COMBINE, s);
   return cudaGetLastError();
 }

@@ -78,7 +78,7 @@ struct DecArgs {
   int32_t *topk_id;
   float *topk_w;
   // tagged exchange buffers (see ld_relaxed64) and the epoch counter
-  unsigned long long *tkeys;  // [2][E]           fp32 router keys
+  unsigned long long *tkeys;  // [2][key_words(E)] fp32 router keys, then the shared-expert gate's x . gate
   unsigned long long *th;     // [2][(k+S)*I/2]   h, bf16 pairs
   unsigned long long *tr;     // [2][H/2]         residual stream between layers, bf16 pairs
   unsigned long long *epoch;  // epochs used so far (low 32 bits)
@@ -117,6 +117,11 @@ __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long l
 __device__ __forceinline__ void st_relaxed64(unsigned long long *p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+
+// Tagged words per parity for the router keys and the shared-expert gate's
+// dot product (E + 1), rounded up to 16 so that the h and residual words
+// after them start on a 128-byte line: the down items poll h 32 bytes per lane.
+__host__ __device__ constexpr int key_words(int E) { return (E + 1 + 15) / 16 * 16; }
 
 __device__ __forceinline__ unsigned long long tagged(uint32_t ep, uint32_t payload) {
   return ((unsigned long long)ep << 32) | payload;
@@ -460,10 +465,14 @@ __device__ __forceinline__ void trace_at(const DecArgs &a, int slot) {
   a.trace[blockIdx.x * MOE_TRACE_SLOTS + slot] = ptx::globaltimer();
 }
 
+// GATE: some layer of the launch has a shared-expert gate vector (the
+// variant without one carries none of its code).
+template <bool GATE>
 __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_constant__ DecArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_ids[16];
   __shared__ float s_w[16];
+  __shared__ float s_gz;  // x . gate of the shared expert's sigmoid gate
   __shared__ float s_part[DWARPS];
   __shared__ uint32_t s_ep0;
   // 1024-byte aligned base for the swizzled code images (keeps the shared space)
@@ -483,7 +492,11 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   uint64_t *bar_p1 = bars, *bar_dsh = bars + 1, *bar_drt = bars + 2, *bar_ru = bars + 3;
   const int nsu = (cta < a.n_su) ? (a.n_su - 1 - cta) / G + 1 : 0;  // shared gate/up units of this CTA
   const int rc = cta - a.rp_cta0;                                    // index among the router CTAs
-  const int nre = (rc >= 0 && rc < a.rp_ctas && rc < E) ? (E - 1 - rc) / a.rp_ctas + 1 : 0;  // router rows
+  // router rows of this CTA: experts rc, rc + rp_ctas, ... < E, and row E,
+  // the shared-expert gate vector, in layers that have one
+  auto rows_below = [&](int n) { return (rc >= 0 && rc < a.rp_ctas && rc < n) ? (n - 1 - rc) / a.rp_ctas + 1 : 0; };
+  const int nre0 = rows_below(E), nre1 = rows_below(E + 1);
+  auto nre_of = [&](int l) { return (GATE && S && a.lw[l].w.shared_gate) ? nre1 : nre0; };
   // Routed gate/up units: a run of consecutive units per CTA (so that one
   // copy per array brings a run's scales), the CTAs counted from the first one
   // without a shared unit, so that those take the extra units.
@@ -508,7 +521,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   auto issue_p1 = [&](int l) {
     const LayerW &L = a.lw[l];
     if (issuer >= 0) {
-      const int ngu = 2 * code_ops(a, H) + 4, n1 = nsu * ngu, n2 = n1 + nre;
+      const int ngu = 2 * code_ops(a, H) + 4, n1 = nsu * ngu, n2 = n1 + nre_of(l);
       for (int o = issuer; o < n2; o += 2 * DWARPS) {
         if (o < n1) {
           const int i = o / ngu, c = o % ngu;
@@ -518,8 +531,8 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
             gu_scales(a, L, c - (ngu - 4), sus + ((c - (ngu - 4)) * a.max_su + i) * (H / 4), E, (cta + i * G) * 8, 1,
                       bar_p1);
         } else {
-          const int i = o - n1;
-          ptx::bulk_g2s(rr + i * H, L.router + (size_t)(rc + i * a.rp_ctas) * H, 4 * H, bar_p1);
+          const int i = o - n1, e = rc + i * a.rp_ctas;
+          ptx::bulk_g2s(rr + i * H, e < E ? L.router + (size_t)e * H : L.w.shared_gate, 4 * H, bar_p1);
         }
       }
     }
@@ -535,7 +548,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       }
     }
   };
-  const uint32_t p1_bytes = (uint32_t)(nsu * 9 * H + nre * 4 * H);
+  auto p1_bytes = [&](int l) { return (uint32_t)(nsu * 9 * H + nre_of(l) * 4 * H); };
   const uint32_t dsh_bytes = S ? (uint32_t)(nou * 4 * I) : 0u;
 
   if (tid == 0) {
@@ -547,7 +560,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         ptx::prefetch_tmap(&a.maps[l].up);
         ptx::prefetch_tmap(&a.maps[l].down);
       }
-    expect_tx(bar_p1, p1_bytes);
+    expect_tx(bar_p1, p1_bytes(0));
     expect_tx(bar_dsh, dsh_bytes);
   }
   __syncthreads();
@@ -575,7 +588,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   for (; l < a.nl && ok; ++l) {
     const LayerW &L = a.lw[l];
     const uint32_t ph = (uint32_t)l & 1u, ep = ep0 + (uint32_t)l + 1u, pb = ep & 1u;
-    unsigned long long *tk = a.tkeys + pb * E, *thb = a.th + (size_t)pb * hw;
+    unsigned long long *tk = a.tkeys + pb * key_words(E), *thb = a.th + (size_t)pb * hw;
     trace(2, l);
     // this layer's tensor maps, for the copies issued after the routing
     if (tid == 0 && a.map3d && l > 0) {
@@ -658,7 +671,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     ok = wait_bar(bar_p1, ph, a.status);
     trace(4, l);
     if (ok)
-      for (int i = warp; i < nre; i += DWARPS) {  // one warp per router row, fp32 FMA
+      for (int i = warp; i < nre_of(l); i += DWARPS) {  // one warp per router row, fp32 FMA
         const float *row = rr + i * H;
         float acc = 0.f;
         for (int kk = 4 * lane; kk < H; kk += 128) {
@@ -672,8 +685,8 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         acc = warp_sum(acc);
         const int e = rc + i * a.rp_ctas;
         if (lane == 0) {
-          const float key = L.bias ? acc + L.bias[e] : acc;
-          a.keys[e] = key;
+          const float key = (L.bias && e < E) ? acc + L.bias[e] : acc;
+          if (e < E) a.keys[e] = key;
           st_relaxed64(tk + e, tagged(ep, __float_as_uint(key)));
         }
       }
@@ -689,7 +702,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     // finished with (read by this CTA's generic loads, written by TMA next)
     if (l + 1 < a.nl) {
       ptx::fence_proxy_async_smem();
-      if (tid == 0) expect_tx(bar_p1, p1_bytes);
+      if (tid == 0) expect_tx(bar_p1, p1_bytes(l + 1));
       __syncthreads();
       issue_p1(l + 1);
       n_p1 = l + 2;
@@ -796,7 +809,14 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
           dbv[i] = __ldg(L.w.down_b + at);
         }
       }
-      bool gotw = wait_bar(bar_drt, ph, a.status) && wait_bar(bar_dsh, ph, a.status);
+      bool gotw = true;
+      if (GATE && S && L.w.shared_gate && tid == 0) {  // x . gate, published with the keys
+        const int gi[1] = {E};
+        unsigned long long gw[1];
+        gotw = poll_tagged(tk, gi, gw, ep, a.status);
+        s_gz = __uint_as_float((uint32_t)gw[0]);
+      }
+      gotw = gotw && wait_bar(bar_drt, ph, a.status) && wait_bar(bar_dsh, ph, a.status);
       trace(12, l);
 #pragma unroll
       for (int i = 0; i < DN_ITEMS; ++i) {
@@ -835,7 +855,8 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         if (tid < nou * 8) {
           const float *yr = ys + tid * NS;
           float o = res_v;
-          if (S) o += yr[k];
+          if (GATE && S && L.w.shared_gate) o = fmaf(1.f / (1.f + expf(-s_gz)), yr[k], o);
+          else if (S) o += yr[k];
           for (int j = 0; j < k; ++j) o = fmaf(s_w[j], yr[j], o);
           ob = f32_to_bf16(o);
           if (l + 1 == a.nl) a.out[n] = (uint16_t)ob;
@@ -892,7 +913,7 @@ DecPlan make_plan(int H, int E, int k, int I, int S, int num_sms) {
   a.n_ru = k * (I / 8);
   a.n_ou = H / 8;
   const int max_su = (a.n_su + G - 1) / G;
-  const int max_re = (E + a.rp_ctas - 1) / a.rp_ctas;
+  const int max_re = (E + 1 + a.rp_ctas - 1) / a.rp_ctas;  // experts and the shared-expert gate row
   const int max_ru = (a.n_ru + G - 1) / G;
   const int max_ou = (a.n_ou + G - 1) / G;
   a.max_su = max_su > 0 ? max_su : 1;
@@ -943,14 +964,15 @@ DecPlan make_plan(int H, int E, int k, int I, int S, int num_sms) {
 // per-block opt-in maximum less the kernel's static shared memory.
 int decode_smem_limit() {
   int dev = 0, optin = 0;
-  cudaFuncAttributes fa;
+  cudaFuncAttributes fa, fg;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-      cudaFuncGetAttributes(&fa, decode_layer_kernel) != cudaSuccess) {
+      cudaFuncGetAttributes(&fa, decode_layer_kernel<false>) != cudaSuccess ||
+      cudaFuncGetAttributes(&fg, decode_layer_kernel<true>) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  return optin - (int)fa.sharedSizeBytes;
+  return optin - (int)(fa.sharedSizeBytes > fg.sharedSizeBytes ? fa.sharedSizeBytes : fg.sharedSizeBytes);
 }
 
 // Codes as bytes [rows][K/2]: either one 3-D box per 8 rows (dims 128 B x
@@ -1007,7 +1029,9 @@ cudaError_t decode_prepare(int H, int E, int k, int I, int S, int num_sms) {
   (void)H, (void)E, (void)k, (void)I, (void)S, (void)num_sms;
   const int lim = decode_smem_limit();
   if (lim <= 0) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
 }
 
 namespace {
@@ -1027,7 +1051,7 @@ cudaError_t launch_layers(const uint16_t *x, const uint16_t *res, uint16_t *out,
   a.topk_id = sc.topk_id;
   a.topk_w = sc.topk_w;
   a.tkeys = sc.tags;
-  a.th = sc.tags + 2 * (size_t)E;
+  a.th = sc.tags + 2 * (size_t)key_words(E);
   a.tr = a.th + (size_t)(k + S) * I;
   a.epoch = sc.epoch;
   a.status = sc.status;
@@ -1061,12 +1085,15 @@ cudaError_t launch_layers(const uint16_t *x, const uint16_t *res, uint16_t *out,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  bool gate = false;
+  for (int l = 0; l < nl; ++l) gate = gate || (S && lw[l].w.shared_gate);
+  void (*kern)(DecArgs) = gate ? decode_layer_kernel<true> : decode_layer_kernel<false>;
   prof_before(MOE_KERNEL_DECODE_LAYER, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
+    e = cudaLaunchKernelEx(&cfg, kern, a);
   }
   prof_after(MOE_KERNEL_DECODE_LAYER, s);
   return e;
@@ -1075,8 +1102,8 @@ cudaError_t launch_layers(const uint16_t *x, const uint16_t *res, uint16_t *out,
 }  // namespace
 
 size_t decode_tag_words(int H, int E, int k, int I, int S) {
-  // keys [2][E], h [2][(k+S) I / 2], residual [2][H / 2]
-  return 2 * (size_t)E + (size_t)(k + S) * I + (size_t)H;
+  // keys and the shared-expert gate [2][key_words(E)], h [2][(k+S) I / 2], residual [2][H / 2]
+  return 2 * (size_t)key_words(E) + (size_t)(k + S) * I + (size_t)H;
 }
 
 cudaError_t launch_decode(const uint16_t *x, const uint16_t *res, int H, int E, int k, int I, int S, int prenorm,

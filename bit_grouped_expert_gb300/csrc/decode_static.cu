@@ -80,7 +80,7 @@ bool aligned(const moe_weights *w) {
   using moe::aligned16;
   return aligned16(w->router_d) && aligned16(w->gate_q_d) && aligned16(w->up_q_d) && aligned16(w->gate_s_d) &&
          aligned16(w->gate_b_d) && aligned16(w->up_s_d) && aligned16(w->up_b_d) && aligned16(w->down_q_d) &&
-         aligned16(w->down_s_d) && aligned16(w->down_b_d);
+         aligned16(w->down_s_d) && aligned16(w->down_b_d) && aligned16(w->shared_gate_d);
 }
 
 }  // namespace
@@ -137,6 +137,7 @@ extern "C" moe_status moe_decode_static(const moe_config *cfg, const void *x_d, 
   ep.up_b = w->up_b_d;
   ep.down_s = w->down_s_d;
   ep.down_b = w->down_b_d;
+  ep.shared_gate = w->shared_gate_d;
   const uint16_t *x = static_cast<const uint16_t *>(x_d);
   const uint16_t *res = residual_d ? static_cast<const uint16_t *>(residual_d) : x;
   uint8_t *sc = d->scratch;

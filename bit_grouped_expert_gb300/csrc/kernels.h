@@ -15,9 +15,12 @@ moe_status note_cuda_error(cudaError_t e);
 void prof_before(int kernel, cudaStream_t s);
 void prof_after(int kernel, cudaStream_t s);
 
+// Every member starts null: a pointer a caller leaves unset reads as absent.
 struct ExpertPtrs {
-  const uint32_t *gate_q, *up_q, *down_q;
-  const uint16_t *gate_s, *gate_b, *up_s, *up_b, *down_s, *down_b;
+  const uint32_t *gate_q = nullptr, *up_q = nullptr, *down_q = nullptr;
+  const uint16_t *gate_s = nullptr, *gate_b = nullptr, *up_s = nullptr, *up_b = nullptr, *down_s = nullptr,
+                 *down_b = nullptr;
+  const float *shared_gate = nullptr;  // [H] fp32 or null: the shared expert's output is scaled by sigmoid(x . gate)
 };
 
 // route.cu
@@ -39,8 +42,10 @@ cudaError_t launch_down_simt(const uint16_t *h, int T, int H, int I, int E, int 
                              const int32_t *n_tiles, int max_tiles, ExpertPtrs w, uint16_t *y, cudaStream_t s);
 
 // combine.cu
-cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w, int T,
-                           int H, int k, int S, uint16_t *out, cudaStream_t s);
+// shared_gate: [H] fp32 or null; x: the layer's expert input (read only with a gate)
+cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w,
+                           const uint16_t *x, const float *shared_gate, int T, int H, int k, int S, uint16_t *out,
+                           cudaStream_t s);
 cudaError_t launch_rmsnorm(const uint16_t *r, int T, int H, float eps, uint16_t *x, cudaStream_t s);
 cudaError_t launch_dequant(const uint32_t *q, const uint16_t *sc, const uint16_t *b, int rows, int K, int G,
                            uint16_t *w, cudaStream_t s);

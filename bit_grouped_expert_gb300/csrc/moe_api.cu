@@ -85,7 +85,7 @@ bool weights_aligned(const moe_weights *w) {
   using moe::aligned16;
   return aligned16(w->router_d) && aligned16(w->gate_q_d) && aligned16(w->up_q_d) && aligned16(w->gate_s_d) &&
          aligned16(w->gate_b_d) && aligned16(w->up_s_d) && aligned16(w->up_b_d) && aligned16(w->down_q_d) &&
-         aligned16(w->down_s_d) && aligned16(w->down_b_d);
+         aligned16(w->down_s_d) && aligned16(w->down_b_d) && aligned16(w->shared_gate_d);
 }
 
 bool weights_present(const moe_weights *w) {
@@ -163,6 +163,7 @@ moe::ExpertPtrs expert_ptrs(const moe_weights *w) {
   e.up_b = w->up_b_d;
   e.down_s = w->down_s_d;
   e.down_b = w->down_b_d;
+  e.shared_gate = w->shared_gate_d;
   return e;
 }
 
@@ -412,8 +413,8 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
                                  &launches, s);
     if (err != cudaSuccess) return cuda_status(err);
   }
-  err = moe::launch_combine(res, y, moe::ws_ptr<int32_t>(ws_d, L.inv), moe::ws_ptr<float>(ws_d, L.topk_w), T,
-                            c.hidden, c.top_k, c.n_shared, out, s);
+  err = moe::launch_combine(res, y, moe::ws_ptr<int32_t>(ws_d, L.inv), moe::ws_ptr<float>(ws_d, L.topk_w), x,
+                            ep.shared_gate, T, c.hidden, c.top_k, c.n_shared, out, s);
   if (err != cudaSuccess) return cuda_status(err);
   ++launches;
   g_last_launches = launches;

@@ -73,14 +73,20 @@ typedef struct {
  *   down_q         uint32 [E+S][H][I/8]
  *   down_s, down_b bf16   [E+S][H][I/G]
  *   router         fp32   [E][H]
+ *   shared_gate    fp32   [H], or NULL
  * Rows are output features; groups run along the input (K) dimension.  The
- * library only reads these buffers. */
+ * library only reads these buffers.
+ * shared_gate (optional, a variant the pages do not print): the shared
+ * expert's output is scaled by g = sigmoid(x . shared_gate) per token, x the
+ * layer's expert input (after the pre-norm of stacked layers), the dot
+ * product in fp32: out = bf16(res + g * y_shared + sum_j w_j y_j).  NULL: g = 1. */
 typedef struct {
   const float *router_d;
   const uint32_t *gate_q_d, *up_q_d;
   const uint16_t *gate_s_d, *gate_b_d, *up_s_d, *up_b_d;
   const uint32_t *down_q_d;
   const uint16_t *down_s_d, *down_b_d;
+  const float *shared_gate_d;
 } moe_weights;
 
 /* Device pointers into a workspace, for tests and tools (moe_route_view). */

@@ -9,7 +9,7 @@ import pytest
 
 import oracle as orc
 import synthetic as syn
-from tests.tolerances import assert_outputs_close, bf16_value
+from tests.tolerances import assert_outputs_close, bf16_value, output_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -228,6 +228,57 @@ def test_layer_tiny_no_shared_centred(path):
     assert_outputs_close(out, ref, k=d["k"], n_shared=0)
 
 
+# ---------------------------------------------------------------- shared-expert sigmoid gate
+
+def _gated(W, seed, H, std=0.1):
+    """W with a shared-expert gate vector, and the same weights without one."""
+    Wg = dict(W)
+    Wg["shared_gate"] = syn.shared_gate(seed, H, std=std)
+    return Wg
+
+
+def _gate_matters(out, d, x, W, keys, res=None):
+    # the ungated layer is not within tolerance of the result: the test above
+    # would catch a path that ignores the gate
+    ref0 = orc.moe_layer(orc.Dims(**d, n_shared=1) if d else orc.Dims(), x, W, res=res, keys=keys)
+    assert not output_errors(out, ref0["out_exact"])["ok"]
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("T", [1, 7, 300])
+def test_layer_tiny_shared_gate(path, T):
+    d, W, _ = _tiny(40 + T)
+    Wg = _gated(W, 40 + T, d["H"])
+    x = syn.activations(40 + T, T, d["H"])
+    res = syn.activations(40 + T, T, d["H"], tensor=syn.T_RESID)
+    L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=300, flags=PATHS[path])
+    out = _forward(L, x, dev_weights(Wg), res=res)
+    keys = L.routing(T)["keys"]
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, Wg, res=res, keys=keys, intermediates=True)
+    assert_outputs_close(out, ref, f"gated tiny T={T} {path}", k=d["k"])
+    _gate_matters(out, d, x, W, keys, res=res)
+    assert L.status() == 0
+
+
+@pytest.mark.parametrize("T", [1, 256])
+def test_layer_real_dims_shared_gate(real, T):
+    # T=1: the decode kernel (gate row on the router CTAs); T=256: the grouped
+    # path's combine kernel
+    W, Wd = real
+    Wg = _gated(W, 7, 2048, std=0.02)
+    Wgd = dict(Wd)
+    Wgd["shared_gate"] = dev(Wg["shared_gate"])
+    x = syn.activations(60 + T, T, 2048)
+    res = syn.activations(60 + T, T, 2048, tensor=syn.T_RESID)
+    L = Layer(max_tokens=T)
+    out = _forward(L, x, Wgd, res=res)
+    keys = L.routing(T)["keys"]
+    ref = orc.moe_layer(orc.Dims(), x, Wg, res=res, keys=keys, intermediates=True)
+    assert_outputs_close(out, ref, f"gated T={T}")
+    _gate_matters(out, None, x, W, keys, res=res)
+    assert L.status() == 0
+
+
 # ---------------------------------------------------------------- layer, real dims
 
 @pytest.mark.parametrize("path", sorted(PATHS))
@@ -424,6 +475,22 @@ def test_decode_stack_tiny_dims_spans_launches():
     ref = orc.moe_layer(orc.Dims(**d, n_shared=1), orc.rmsnorm(inputs[-1], 1e-6), Ws[-1], res=inputs[-1],
                         keys=keys, intermediates=True)
     assert_outputs_close(out, ref, "stack layer 9", k=d["k"])
+
+
+def test_decode_stack_mixed_shared_gates():
+    # eight tiny layers, a gate vector on every other one: the gate row's
+    # copy size and tagged word change from layer to layer within a launch
+    Ws = []
+    for l in range(8):
+        d, W, _ = _tiny(300 + l)
+        Ws.append(_gated(W, 300 + l, d["H"]) if l % 2 == 0 else W)
+    r = syn.activations(92, 1, d["H"], tensor=syn.T_RESID)
+    out, inputs, Ls, launches = _stack_vs_layers(d, Ws, [None] * 8, r)
+    assert launches == 2
+    keys = Ls.routing(1)["keys"]
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), orc.rmsnorm(inputs[-1], 1e-6), Ws[-1], res=inputs[-1],
+                        keys=keys, intermediates=True)
+    assert_outputs_close(out, ref, "gated stack layer 8", k=d["k"])
 
 
 def test_decode_stack_repeated_tokens_seven_layers(real):

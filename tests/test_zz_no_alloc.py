@@ -40,13 +40,15 @@ def gpu():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("prenorm", [False, True])
-def test_static_decode_matches_forward_on_consecutive_calls(gpu, prenorm):
+@pytest.mark.parametrize("prenorm,gate", [(False, False), (True, False), (True, True)])
+def test_static_decode_matches_forward_on_consecutive_calls(gpu, prenorm, gate):
     torch = gpu
     from tests.gpu_util import Layer, dev, dev_weights, host_u16
 
     W = syn.experts(0, 257, 2048, 512)
     W["router"] = syn.router(0, 256, 2048)
+    if gate:  # the shared expert scaled by its sigmoid gate
+        W["shared_gate"] = syn.shared_gate(0, 2048)
     Wd = dev_weights(W)
     bias = dev(syn.zipf_bias(0, 256))
     cfg = moe.make_config()
