@@ -318,10 +318,11 @@ __device__ void gu_finish(const DecArgs &a, int nu, const float *red, unsigned l
 }
 
 // Top-k of one token by one warp, for E <= 256 keys in shared memory:
-// lane l holds the codes of experts l, l+32, ...  The k-th largest of the 32
-// lane maxima bounds the k-th largest key from below (k distinct keys reach
-// it), so only the keys at or above it -- at most 8k -- are ranked, each
-// against the others.  Same order and tie rule as topk_block.  Leaves the
+// lane l holds the codes of experts l, l+32, ...  A bound taken from the 32
+// lane maxima bounds the k-th largest key from below, so only the keys at or
+// above it -- at most 8k unless lane maxima tie, all E at worst (cand holds
+// E codes) -- are ranked, each against the others.  Same order and tie rule
+// as topk_block.  Leaves the
 // ids and their keys by rank in ids and w; topk_weights turns the keys into
 // weights.
 __device__ void topk_warp(const float *keys, int E, int k, unsigned long long *cand, int32_t *ids, float *w,
@@ -340,20 +341,18 @@ __device__ void topk_warp(const float *keys, int E, int k, unsigned long long *c
     c[i] = lane + 32 * i < E ? topk_code(kv[i], lane + 32 * i) : 0ull;
     m = c[i] > m ? c[i] : m;
   }
-  // rank of this lane's maximum among the lane maxima (the nonzero ones are distinct)
-  int r = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)m, j), hi = __shfl_sync(0xffffffffu, (uint32_t)(m >> 32), j);
-    r += (((unsigned long long)hi << 32) | lo) > m;
+  // A lower bound on the k-th largest key: k rounds of a warp maximum over
+  // the key bits (upper word) of the lane maxima, each round dropping the
+  // lanes that hold it.  Every round drops at least one of the largest
+  // lanes, so the k-th round's maximum is at most the k-th largest lane
+  // maximum, itself at most the k-th largest key (k lanes hold distinct keys
+  // that reach it); tied lanes dropping together only lower the bound.
+  uint32_t v = (uint32_t)(m >> 32), tau_hi = 0u;
+  for (int i = 0; i < k; ++i) {
+    tau_hi = __reduce_max_sync(0xffffffffu, v);
+    if (v == tau_hi) v = 0u;
   }
-  const unsigned hit = __ballot_sync(0xffffffffu, m != 0ull && r == k - 1);
-  unsigned long long tau = 0ull;  // no such lane: E < k cannot occur, rank everything
-  if (hit) {
-    const int src = __ffs(hit) - 1;
-    const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)m, src), hi = __shfl_sync(0xffffffffu, (uint32_t)(m >> 32), src);
-    tau = ((unsigned long long)hi << 32) | lo;
-  }
+  const unsigned long long tau = (unsigned long long)tau_hi << 32;  // 0: every key is a candidate
   mark(19);
   int n = 0;
   const unsigned below = (1u << lane) - 1u;
