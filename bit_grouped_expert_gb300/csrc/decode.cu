@@ -786,14 +786,13 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     // let the next launch in the stream start its prologue and weight copies
     if (l + 1 == a.nl) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     {
-      // Down items (output unit ol, slot j, K-chunk kc) warp by warp: a warp
-      // polls just the 256 h values of its item (tagged pairs, 4 words per
-      // lane) into its own padded buffer and runs the item as soon as they
-      // are there, so slots whose experts finished early do not wait for the
-      // last ones.
+      // h of every slot comes into shared memory first (padded 64-value
+      // groups in the MMA operand order), all threads polling at once and
+      // before the down rows are waited for; the down items (output unit ol,
+      // slot j, K-chunk kc), warp by warp, then read it there.  (Items that
+      // polled their own h paid one L2 round trip each, in sequence.)
       const int nkcd = I / KCH, gpr = I / 64, g = lane >> 2, q = lane & 3;
       const int nitem = nou * NS * nkcd;
-      uint16_t *hwb = hs + warp * 4 * XPAD;  // this warp's 4 padded groups
       // this lane's scale and bias for each of the warp's items (row g, group
       // q of the chunk), loaded while h is on its way
       uint16_t dsv[DN_ITEMS], dbv[DN_ITEMS];
@@ -809,30 +808,40 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         }
       }
       bool gotw = true;
+      {
+        const int n8 = NS * I / 8;  // runs of 8 values (4 tagged words), two per thread and round
+        for (int u = tid; u < n8; u += 2 * DTHREADS) {
+          const int v = u + DTHREADS < n8 ? 4 * (u + DTHREADS) : -4;
+          const int idx[8] = {4 * u, 4 * u + 1, 4 * u + 2, 4 * u + 3, v, v + 1, v + 2, v + 3};
+          unsigned long long w[8];
+          gotw = poll_tagged(thb, idx, w, ep, a.status);
+          if (!gotw) break;
+          *reinterpret_cast<uint4 *>(hs + (u >> 3) * XPAD + (u & 7) * 8) =
+              perm8((uint32_t)w[0], (uint32_t)w[1], (uint32_t)w[2], (uint32_t)w[3]);
+          if (v >= 0) {
+            const int u2 = u + DTHREADS;
+            *reinterpret_cast<uint4 *>(hs + (u2 >> 3) * XPAD + (u2 & 7) * 8) =
+                perm8((uint32_t)w[4], (uint32_t)w[5], (uint32_t)w[6], (uint32_t)w[7]);
+          }
+        }
+      }
       if (GATE && S && L.w.shared_gate && tid == 0) {  // x . gate, published with the keys
         const int gi[1] = {E};
         unsigned long long gw[1];
-        gotw = poll_tagged(tk, gi, gw, ep, a.status);
+        gotw = gotw && poll_tagged(tk, gi, gw, ep, a.status);
         s_gz = __uint_as_float((uint32_t)gw[0]);
       }
       gotw = gotw && wait_bar(bar_drt, ph, a.status) && wait_bar(bar_dsh, ph, a.status);
+      gotw = __syncthreads_and(gotw) != 0;  // h is in shared memory
       trace(12, l);
 #pragma unroll
       for (int i = 0; i < DN_ITEMS; ++i) {
         const int t = warp + i * DWARPS;
-        if (t >= nitem || !__all_sync(0xffffffffu, gotw)) break;
+        if (t >= nitem || !gotw) break;  // gotw is uniform across the CTA here
         const int kc = t % nkcd, j = (t / nkcd) % NS, ol = t / (nkcd * NS);
-        const int w0 = (j * I + kc * KCH) / 2 + 4 * lane;  // words of values 8*lane .. +7 of the chunk
-        const int idx[4] = {w0, w0 + 1, w0 + 2, w0 + 3};
-        unsigned long long w[4];
-        gotw = poll_tagged(thb, idx, w, ep, a.status);
-        if (!__all_sync(0xffffffffu, gotw)) break;
-        *reinterpret_cast<uint4 *>(hwb + (lane >> 3) * XPAD + (lane & 7) * 8) =
-            perm8((uint32_t)w[0], (uint32_t)w[1], (uint32_t)w[2], (uint32_t)w[3]);
-        __syncwarp();
-        const float d = gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, dsv[i], dbv[i], hwb, g, q);
+        const float d = gemv_chunk(dc + (ol * NS + j) * 4 * I + kc * 1024, dsv[i], dbv[i],
+                                   hs + ((j * I + kc * KCH) / 64) * XPAD, g, q);
         if (q == 0) red[t * 8 + g] = d;
-        __syncwarp();  // every lane has read the buffer before the next item overwrites it
       }
       ok = __syncthreads_and(gotw) != 0;
       if (!ok) break;
@@ -933,8 +942,8 @@ DecPlan make_plan(int H, int E, int k, int I, int S, int num_sms) {
   o = al(o + (H / 64) * XPAD * 2, 128);
   a.off_xn = o;
   o = al(o + H * 2, 128);
-  a.off_h = o;  // per-warp down buffers: 4 padded groups (one K-chunk of h) each
-  o = al(o + DWARPS * 4 * XPAD * 2, 128);
+  a.off_h = o;  // h of every slot, padded 64-value groups
+  o = al(o + (NS * I / 64) * XPAD * 2, 128);
   a.off_rus = o;
   o = al(o + max_ru * H, 128);
   a.off_sus = o;
