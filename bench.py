@@ -43,8 +43,8 @@ ROUTER_BYTES = E * H * 4                                              # 2,097,15
 # capture of the current kernels (profiles/*.md give the commands); None
 # where no capture of that workload exists.  Update with every kernel change.
 TRAFFIC = {
-    "decode40": 126_741_248,      # decode_layer_kernel, one 7-layer launch, profiles/decode_layer_decode40.md
-    "layer256": 317_130_240,      # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer256.md
+    "decode40": 126_374_656,      # decode_layer_kernel, one 7-layer launch, profiles/decode_layer_decode40.md
+    "layer256": 316_907_520,      # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer256.md
     "layer4096": 484_388_608,     # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer4096.md
 }
 METRIC = "MoE-layer prefill tokens/s & % of roofline (T=256–32K); T=1 HBM GB/s"

@@ -755,6 +755,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         }
       }
     }
+    trace(21, l);
     __syncthreads();
     if (issuer >= 0) {  // routed down rows: code images per (unit, slot)
       const int ndn = code_ops(a, I), nc = nou * k * ndn;
@@ -763,6 +764,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         dn_codes(a, a.maps[l], o % ndn, dc + (ol * NS + j) * 4 * I, s_ids[j], o0 + ol * 8, bar_drt);
       }
     }
+    trace(22, l);
     // the weights (only the combine needs them) while the copies are in flight
     if (warp == 0) {
       if (E <= 256) topk_weights(k, s_ids, s_w, a.status);
@@ -825,6 +827,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
           }
         }
       }
+      trace(13, l);
       if (GATE && S && L.w.shared_gate && tid == 0) {  // x . gate, published with the keys
         const int gi[1] = {E};
         unsigned long long gw[1];
@@ -843,6 +846,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
                                    hs + ((j * I + kc * KCH) / 64) * XPAD, g, q);
         if (q == 0) red[t * 8 + g] = d;
       }
+      trace(14, l);
       ok = __syncthreads_and(gotw) != 0;
       if (!ok) break;
       trace(15, l);
