@@ -22,6 +22,7 @@ _lock = threading.Lock()
 _lib = None
 
 T_X, T_ROUTER, T_RESID, T_SHGATE = 1, 2, 13, 14
+T_GDN_Q, T_GDN_K, T_GDN_V, T_GDN_ALPHA, T_GDN_BETA, T_GDN_STATE = 15, 16, 17, 18, 19, 20
 
 
 def build(force: bool = False) -> str:
@@ -55,6 +56,7 @@ def _load():
         lib.syn_fill_normal_bf16.argtypes = [u64, dbl, dbl, vp, sz]
         lib.syn_fill_normal_f32.argtypes = [u64, dbl, dbl, vp, sz]
         lib.syn_fill_uniform_bf16.argtypes = [u64, dbl, dbl, vp, sz]
+        lib.syn_fill_uniform_f32.argtypes = [u64, dbl, dbl, vp, sz]
         lib.syn_fill_words.argtypes = [u64, vp, sz]
         lib.syn_expert.argtypes = [u64, u32, u32, i32, i32, i32] + [vp] * 9
         lib.syn_layer_experts.argtypes = [u64, u32, i32, i32, i32, i32] + [vp] * 9
@@ -92,6 +94,30 @@ def shared_gate(seed: int, H: int, layer: int = 0, std: float = 0.02) -> np.ndar
     """Shared-expert gate vector [H] fp32 ~ N(0, std)."""
     out = np.empty(H, dtype=np.float32)
     _load().syn_fill_normal_f32(key(seed, T_SHGATE, layer), 0.0, std, _p(out), out.size)
+    return out
+
+
+def gdn_inputs(seed: int, T: int, Hk: int, Hv: int, dk: int = 128, dv: int = 128, layer: int = 0,
+               state_std: float = 0.0, alpha=(0.85, 1.0), beta=(0.05, 0.95)) -> dict:
+    """Inputs of one Gated DeltaNet scan (one sequence):
+    q, k [T, Hk, dk] bf16 ~ N(0, 1/dk) (so |k| is near 1, as after the
+    model's L2 normalisation), v [T, Hv, dv] bf16 ~ N(0, 1), decay alpha
+    [T, Hv] fp32 ~ U(alpha), write strength beta [T, Hv] fp32 ~ U(beta), and
+    an initial state [Hv, dk, dv] fp32 ~ N(0, state_std) (zeros when 0)."""
+    lib = _load()
+    out = {"q": np.empty((T, Hk, dk), np.uint16), "k": np.empty((T, Hk, dk), np.uint16),
+           "v": np.empty((T, Hv, dv), np.uint16), "alpha": np.empty((T, Hv), np.float32),
+           "beta": np.empty((T, Hv), np.float32), "state": np.zeros((Hv, dk, dv), np.float32)}
+    sd = 1.0 / np.sqrt(dk)
+    if T:
+        lib.syn_fill_normal_bf16(key(seed, T_GDN_Q, layer), 0.0, sd, _p(out["q"]), out["q"].size)
+        lib.syn_fill_normal_bf16(key(seed, T_GDN_K, layer), 0.0, sd, _p(out["k"]), out["k"].size)
+        lib.syn_fill_normal_bf16(key(seed, T_GDN_V, layer), 0.0, 1.0, _p(out["v"]), out["v"].size)
+        lib.syn_fill_uniform_f32(key(seed, T_GDN_ALPHA, layer), alpha[0], alpha[1], _p(out["alpha"]),
+                                 out["alpha"].size)
+        lib.syn_fill_uniform_f32(key(seed, T_GDN_BETA, layer), beta[0], beta[1], _p(out["beta"]), out["beta"].size)
+    if state_std > 0:
+        lib.syn_fill_normal_f32(key(seed, T_GDN_STATE, layer), 0.0, state_std, _p(out["state"]), out["state"].size)
     return out
 
 

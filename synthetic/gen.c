@@ -56,6 +56,10 @@ void syn_fill_uniform_bf16(uint64_t key, double lo, double hi, uint16_t *out, si
   for (size_t i = 0; i < n; ++i) out[i] = syn_bf16_from_double(lo + (hi - lo) * syn_uniform(key, i));
 }
 
+void syn_fill_uniform_f32(uint64_t key, double lo, double hi, float *out, size_t n) {
+  for (size_t i = 0; i < n; ++i) out[i] = (float)(lo + (hi - lo) * syn_uniform(key, i));
+}
+
 void syn_fill_words(uint64_t key, uint32_t *out, size_t n) {
   for (size_t i = 0; i < n; ++i) out[i] = (uint32_t)syn_draw(key, i);
 }

@@ -35,7 +35,11 @@ enum {
   SYN_T_DOWN_Q = 9, SYN_T_DOWN_S = 10, SYN_T_DOWN_B = 11,
   SYN_T_ZIPF = 12,   /* permutation behind the Zipf expert ranking   */
   SYN_T_RESID = 13,  /* a separate residual stream [T][H] bf16        */
-  SYN_T_SHGATE = 14  /* shared-expert gate vector [H] fp32 ~ N(0, 0.02) */
+  SYN_T_SHGATE = 14, /* shared-expert gate vector [H] fp32 ~ N(0, 0.02) */
+  /* Gated DeltaNet scan inputs */
+  SYN_T_GDN_Q = 15, SYN_T_GDN_K = 16, SYN_T_GDN_V = 17, /* bf16                     */
+  SYN_T_GDN_ALPHA = 18, SYN_T_GDN_BETA = 19,          /* fp32 ~ U(lo, hi)         */
+  SYN_T_GDN_STATE = 20                                 /* fp32 initial state        */
 };
 
 uint64_t syn_key(uint64_t seed, uint32_t tensor, uint32_t layer, uint32_t expert);
@@ -47,6 +51,7 @@ uint16_t syn_bf16_from_double(double v);
 void syn_fill_normal_bf16(uint64_t key, double mean, double std, uint16_t *out, size_t n);
 void syn_fill_normal_f32(uint64_t key, double mean, double std, float *out, size_t n);
 void syn_fill_uniform_bf16(uint64_t key, double lo, double hi, uint16_t *out, size_t n);
+void syn_fill_uniform_f32(uint64_t key, double lo, double hi, float *out, size_t n);
 void syn_fill_words(uint64_t key, uint32_t *out, size_t n);
 
 /* One expert's packed weights (gate, up: [I][H/8] words + [I][H/64] scale,
