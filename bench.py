@@ -63,11 +63,17 @@ WORKLOADS = {
     "prefill32k": dict(T=32768, layers=40, chunk=4096, zipf=False, centred=True,
                        desc="32768-token prompt, 8 chunks of 4096 through 40 MoE layers (centred weights), "
                             "one fixed workspace"),
+    "gdn2k": dict(T=2048, layers=1, chunk=2048, zipf=False, centred=False, Hk=16, Hv=32, dk=128, dv=128,
+                  desc="Gated DeltaNet scan of one 2048-token sequence from an empty state (16 key heads, "
+                       "32 value heads, dk = dv = 128), 6 distinct input sets cycled"),
 }
+GDN_SETS = 6
+GDN_METRIC = "Gated DeltaNet scan tokens/s (one sequence, T=2048, 32 value heads); % of FP32 FMA peak"
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 flops (FMA) x max SM clock
 DEFAULT_STEPS = {"decode40": 2000, "layer256": 200, "layer512zipf": 200, "layer2048": 100, "layer4096": 50,
-                 "prefill32k": 3}
+                 "prefill32k": 3, "gdn2k": 30}
 DEFAULT_WARMUP = {"decode40": 50, "layer256": 10, "layer512zipf": 10, "layer2048": 5, "layer4096": 5,
-                  "prefill32k": 3}
+                  "prefill32k": 3, "gdn2k": 3}
 
 
 def parse():
@@ -444,6 +450,117 @@ def run_ours(args, wl, rank, world, device):
     return result
 
 
+def run_gdn(args, wl, rank, world, device):
+    """The Gated DeltaNet scan: each step scans one 2048-token sequence from
+    an empty state (state reset + scan, one captured graph per input set)."""
+    import torch
+    import __graft_entry__
+    import bit_grouped_expert_gb300 as moe
+    import synthetic as syn
+
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(device)
+    T, Hk, Hv, dk, dv = wl["T"], wl["Hk"], wl["Hv"], wl["dk"], wl["dv"]
+    seed = args.seed + 1000 * rank
+    host = [syn.gdn_inputs(seed + i, T, Hk, Hv, dk, dv) for i in range(GDN_SETS)]
+    sets = [{n: as_dev(a, device) for n, a in h.items()} for h in host]
+    outs = [torch.empty((T, Hv, dv), dtype=torch.int16, device=device) for _ in range(GDN_SETS)]
+    stream = torch.cuda.Stream(device=device)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def body(i, prof=None):
+        d = sets[i]
+        d["state"].zero_()
+        if prof is not None:
+            moe.moe_profile_events(moe.MOE_KERNEL_GDN_SCAN, ev_a[prof:prof + 1], ev_b[prof:prof + 1])
+        moe.gdn_scan(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["state"], outs[i], T, Hk, Hv, dk, dv,
+                     stream=stream)
+        if prof is not None:
+            moe.moe_profile_events(moe.MOE_KERNEL_GDN_SCAN)
+
+    with torch.cuda.stream(stream):
+        body(0)
+    torch.cuda.synchronize()
+    for e in ev_a + ev_b:
+        e.record(stream)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(GDN_SETS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body(i, prof=(i - 1) // 2 if i in (1, 3) else None)  # sets 1 and 3 time the scan kernel
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % GDN_SETS].replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id(device)) as clk:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(args.steps):
+                graphs[i % GDN_SETS].replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    dom_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / 2
+    tps = T * args.steps / (ms * 1e-3) * world
+    flops = 7.0 * Hv * dk * dv * T  # per sequence: u (2), state update (3), output (2) per state element per token
+    achieved = flops / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(FP32_PEAK_TFLOPS, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / FP32_PEAK_TFLOPS, 4),
+                "traffic": TRAFFIC.get(args.workload), "kernel": "gdn_scan_kernel (state in registers)",
+                "kernel_ms": round(dom_ms, 5),
+                "peak_src": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2070 MHz"}
+    # end to end: each step copies its inputs from pinned host memory, scans,
+    # and copies the outputs back
+    pinned = [{n: torch.from_numpy(np.ascontiguousarray(a).view(np.int16 if a.dtype == np.uint16 else a.dtype))
+               .pin_memory() for n, a in h.items() if n != "state"} for h in host[:2]]
+    host_o = torch.empty((T, Hv, dv), dtype=torch.int16).pin_memory()
+    h2d = sum(a.numel() * a.element_size() for a in pinned[0].values())
+    e2e_steps = min(args.steps, 10)
+    torch.cuda.synchronize()
+    te = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            b = i % 2
+            for n, a in pinned[b].items():
+                sets[b][n].copy_(a, non_blocking=True)
+            graphs[b].replay()
+            host_o.copy_(outs[b], non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - te
+    e2e = {"value": T * e2e_steps / e2e_s * world, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": T * Hv * dv * 2}
+    return {"metric": GDN_METRIC, "value": tps, "unit": "tokens/s", "higher_is_better": True,
+            "ms_per_step": ms / args.steps, "roofline": roofline, "e2e": e2e, "clocks": clk.summary(),
+            "gpu_launches": args.steps, "dtype": "bf16 q/k/v/o, fp32 alpha/beta/state and sums",
+            "config_extra": {"l2": f"{GDN_SETS} distinct input sets of {h2d / 1e6:.0f} MB cycled (larger than L2 "
+                                   "together)", "experts": None}}
+
+
+def gdn_oracle_sample(wl, seed, target_s=None):
+    """The oracle scan over the first tokens of one sequence (all heads):
+    64 tokens, or as many as take about target_s seconds."""
+    from oracle.gdn import gdn_scan as oracle_scan
+    import synthetic as syn
+    T = wl["T"]
+    d = syn.gdn_inputs(seed, T, wl["Hk"], wl["Hv"], wl["dk"], wl["dv"])
+    n = 64
+    while True:
+        t = time.perf_counter()
+        oracle_scan(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["state"], t_end=n)
+        dt = time.perf_counter() - t
+        if target_s is None or dt >= 0.5 * target_s or n >= T:
+            break
+        n = min(T, max(2 * n, int(n * target_s / max(dt, 1e-3))))
+    return dt, float(n), "tokens/s", f"the first {n} tokens of one sequence through the scan (all 32 heads)"
+
+
 # ------------------------------------------------------------------ oracle (CPU)
 
 def oracle_sample(wl, seed, target_s=None):
@@ -488,8 +605,10 @@ def oracle_sample(wl, seed, target_s=None):
 def cpu_baseline(wl, seed):
     import oracle as orc
     orc.build()
-    dt, units, unit, desc = oracle_sample(wl, seed, target_s=10.0)
-    return {"value": units / dt, "unit": unit, "cores": orc.num_threads(), "kind": "oracle", "sample": desc,
+    sample = gdn_oracle_sample if "Hv" in wl else oracle_sample
+    dt, units, unit, desc = sample(wl, seed, target_s=10.0)
+    cores = 1 if "Hv" in wl else orc.num_threads()  # the scan oracle is single-threaded numpy
+    return {"value": units / dt, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc,
             "seconds": round(dt, 3)}
 
 
@@ -498,17 +617,19 @@ def run_reference(args, wl):
     import synthetic as syn
     orc.build()
     syn.build()
+    sample = gdn_oracle_sample if "Hv" in wl else oracle_sample
     for i in range(args.warmup):
-        oracle_sample(wl, args.seed + i)
+        sample(wl, args.seed + i)
     steps = args.steps
     tot, units, unit, desc = 0.0, 0.0, None, None
     for i in range(steps):
-        dt, u, unit, desc = oracle_sample(wl, args.seed + 100 + i)
+        dt, u, unit, desc = sample(wl, args.seed + 100 + i)
         tot += dt
         units += u
     val = units / tot
     return {"value": val, "unit": unit, "higher_is_better": True, "ms_per_step": tot / steps * 1e3,
-            "cpu_baseline": {"value": val, "unit": unit, "cores": orc.num_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": val, "unit": unit, "cores": 1 if "Hv" in wl else orc.num_threads(),
+                             "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "dtype": "fp64 oracle (bf16 rounding points of the layer)"}
@@ -525,11 +646,12 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    base = {"metric": METRIC, "n_gpus": args.gpus if world == 1 else world, "steps": args.steps,
+    base = {"metric": GDN_METRIC if "Hv" in wl else METRIC, "n_gpus": args.gpus if world == 1 else world, "steps": args.steps,
             "warmup": args.warmup, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
             "config": {"workload": f"{args.workload}: {wl['desc']}", "tokens_per_step": wl["T"],
                        "layers": wl["layers"], "chunk": wl["chunk"], "parallelism": "replicas" if world > 1 else "1 GPU",
-                       "l2": "inputs larger than L2 (packed weights >= 455 MB per layer)",
+                       "l2": (f"{GDN_SETS} distinct input sets cycled (~50 MB each, larger than L2 together)"
+                              if "Hv" in wl else "inputs larger than L2 (packed weights >= 455 MB per layer)"),
                        "experts": args.experts}}
     if args.impl == "reference":
         if rank != 0:
@@ -543,9 +665,11 @@ def main():
     if world > 1:
         torch.cuda.set_device(device)
         torch.distributed.init_process_group("nccl")
-    res = run_ours(args, wl, rank, world, device)
+    res = (run_gdn if "Hv" in wl else run_ours)(args, wl, rank, world, device)
     if rank == 0:
+        extra = res.pop("config_extra", {})
         line = {**base, **res}
+        line["config"] = {**line["config"], **extra}
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(wl, args.seed)
         print(json.dumps(line))

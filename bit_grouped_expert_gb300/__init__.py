@@ -39,7 +39,7 @@ MOE_TRACE_SLOTS = 32
 EXPORTS = ("moe_plan", "moe_plan_destroy", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_route_from_logits", "moe_forward", "moe_route_view", "moe_rmsnorm", "moe_dequant",
            "moe_device_status", "moe_last_launch_count", "moe_status_str", "moe_profile_events", "moe_last_cuda_error",
-           "moe_decode_static", "moe_decode_stack")
+           "moe_decode_static", "moe_decode_stack", "gdn_scan")
 
 MOE_DECODE_STATIC_SCRATCH_BYTES = 65536
 
@@ -52,6 +52,7 @@ MOE_KERNEL_COMBINE = 6
 MOE_KERNEL_DECODE_LAYER = 7
 MOE_KERNEL_RMSNORM = 10
 MOE_KERNEL_GATHER = 11
+MOE_KERNEL_GDN_SCAN = 12
 
 
 class MoeError(RuntimeError):
@@ -126,6 +127,8 @@ def lib():
         L.moe_decode_static.restype = i32
         L.moe_decode_static.argtypes = [ctypes.POINTER(moe_config), vp, vp, ctypes.POINTER(moe_weights), vp, vp, vp,
                                         u32, vp]
+        L.gdn_scan.restype = i32
+        L.gdn_scan.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
         _lib = L
     return _lib
 
@@ -239,6 +242,14 @@ def moe_decode_static(cfg: moe_config, x, residual, weights, logit_bias, out, st
     _check("moe_decode_static", lib().moe_decode_static(ctypes.byref(cfg), _ptr(x), _ptr(residual), ctypes.byref(cw),
                                                         _ptr(logit_bias), _ptr(out), _ptr(status), int(flags),
                                                         _stream(stream)))
+
+
+def gdn_scan(q, k, v, alpha, beta, state, o, T: int, Hk: int, Hv: int, dk: int = 128, dv: int = 128, stream=None):
+    """Gated DeltaNet scan of one sequence (gdn.h): q, k [T, Hk, dk] and v
+    [T, Hv, dv] bf16, alpha, beta [T, Hv] fp32, state [Hv, dk, dv] fp32
+    (updated in place), o [T, Hv, dv] bf16 (written)."""
+    _check("gdn_scan", lib().gdn_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(state), _ptr(o),
+                                      int(T), int(Hk), int(Hv), int(dk), int(dv), _stream(stream)))
 
 
 def moe_route_view(plan: Plan, ws, T: int) -> moe_route_ptrs:

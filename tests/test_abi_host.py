@@ -5,6 +5,7 @@ is enqueued.  Every call here fails validation, so no kernel is launched
 from __future__ import annotations
 
 import ctypes
+import glob
 import os
 import re
 
@@ -23,9 +24,11 @@ def lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "moe.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+    names = set()
+    for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:moe|gdn)_[a-z_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_entry_points_exported(lib):
@@ -184,3 +187,26 @@ def test_other_entry_point_errors(lib):
         moe.moe_dequant(0x1004, 0x2000, 0x3000, 4, 128, 64, 0x4000, stream=0)
     assert ei.value.status == moe.MOE_ERR_MISALIGNED
     assert moe.status_str(moe.MOE_ERR_NONFINITE) == "non-finite router key"
+
+
+def test_gdn_scan_host_checks(lib):
+    # fake, aligned device addresses: every case below is refused on the host
+    q, k, v, al, be, st, o = (0x10000000 + i * 0x1000000 for i in range(7))
+    ok = dict(T=64, Hk=2, Hv=4, dk=128, dv=128)
+
+    def call(**kw):
+        a = {**dict(q=q, k=k, v=v, alpha=al, beta=be, state=st, o=o), **ok, **kw}
+        return lib.gdn_scan(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["state"], a["o"], a["T"], a["Hk"],
+                            a["Hv"], a["dk"], a["dv"], 0)
+
+    assert call(T=0, q=None, k=None) == moe.MOE_OK  # nothing to do, nothing enqueued
+    assert call(T=-1) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert call(Hk=0) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert call(Hv=3) == moe.MOE_ERR_INVALID_ARGUMENT  # not a multiple of Hk
+    assert call(dk=64) == moe.MOE_ERR_UNSUPPORTED
+    assert call(dv=48) == moe.MOE_ERR_UNSUPPORTED
+    assert call(beta=None) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert call(v=v + 8) == moe.MOE_ERR_MISALIGNED
+    assert call(alpha=al + 4) == moe.MOE_ERR_MISALIGNED
+    assert call(o=q + 4096) == moe.MOE_ERR_INVALID_ARGUMENT  # o overlaps q
+    assert call(o=st) == moe.MOE_ERR_INVALID_ARGUMENT  # o overlaps the state
