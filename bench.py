@@ -46,6 +46,7 @@ TRAFFIC = {
     "decode40": 126_374_656,      # decode_layer_kernel, one 7-layer launch, profiles/decode_layer_decode40.md
     "layer256": 316_907_520,      # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer256.md
     "layer4096": 484_388_608,     # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer4096.md
+    "gdn2k": 36_325_888,          # gdn_scan_kernel, profiles/gdn_scan_gdn2k.md
 }
 METRIC = "MoE-layer prefill tokens/s & % of roofline (T=256–32K); T=1 HBM GB/s"
 

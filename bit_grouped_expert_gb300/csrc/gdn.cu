@@ -138,8 +138,12 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_scan_kernel(const __grid_cons
     cp_async_wait<1>();  // block j+1 has landed (block j+2 may still be in flight)
     convert(j + 1);
     const int b = j & 1, n = min(GDN_BLK, T - j * GDN_BLK);
-    for (int tt2 = 0; tt2 < n; ++tt2) {
-      const int t = j * GDN_BLK + tt2;
+    // each token's output partial; the column sums wait for the block's end,
+    // off the chain from one token's state to the next
+    float op[GDN_BLK] = {};
+#pragma unroll
+    for (int tt2 = 0; tt2 < GDN_BLK; ++tt2) {
+      if (tt2 >= n) break;
       const float *kb = kf[b][tt2] + r * GDN_KPAD, *qb = qf[b][tt2] + r * GDN_KPAD;
       const float al = ab[b][tt2][0], be = ab[b][tt2][1];
       float u4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -169,11 +173,16 @@ __global__ void __launch_bounds__(GDN_THREADS) gdn_scan_kernel(const __grid_cons
         o4[2] = fmaf(S[i + 2], qv.z, o4[2]);
         o4[3] = fmaf(S[i + 3], qv.w, o4[3]);
       }
-      float o = (o4[0] + o4[1]) + (o4[2] + o4[3]);
-#pragma unroll
-      for (int m = 1; m < GDN_RQ; m <<= 1) o += __shfl_xor_sync(0xffffffffu, o, m);
-      if (r == 0) a.o[((size_t)t * a.Hv + h) * a.dv + c] = f32_to_bf16(o);
+      op[tt2] = (o4[0] + o4[1]) + (o4[2] + o4[3]);
     }
+#pragma unroll
+    for (int m = 1; m < GDN_RQ; m <<= 1)
+#pragma unroll
+      for (int tt2 = 0; tt2 < GDN_BLK; ++tt2) op[tt2] += __shfl_xor_sync(0xffffffffu, op[tt2], m);
+    if (r == 0)
+#pragma unroll
+      for (int tt2 = 0; tt2 < GDN_BLK; ++tt2)
+        if (tt2 < n) a.o[((size_t)(j * GDN_BLK + tt2) * a.Hv + h) * a.dv + c] = f32_to_bf16(op[tt2]);
     __syncthreads();  // buffer j & 1 and raw block j are free; buffer (j + 1) & 1 is published
     issue(j + 3);     // into raw block j's slots
   }
