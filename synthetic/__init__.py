@@ -23,6 +23,7 @@ _lib = None
 
 T_X, T_ROUTER, T_RESID, T_SHGATE = 1, 2, 13, 14
 T_GDN_Q, T_GDN_K, T_GDN_V, T_GDN_ALPHA, T_GDN_BETA, T_GDN_STATE = 15, 16, 17, 18, 19, 20
+T_ATT_Q, T_ATT_K, T_ATT_V = 21, 22, 23
 
 
 def build(force: bool = False) -> str:
@@ -118,6 +119,18 @@ def gdn_inputs(seed: int, T: int, Hk: int, Hv: int, dk: int = 128, dv: int = 128
         lib.syn_fill_uniform_f32(key(seed, T_GDN_BETA, layer), beta[0], beta[1], _p(out["beta"]), out["beta"].size)
     if state_std > 0:
         lib.syn_fill_normal_f32(key(seed, T_GDN_STATE, layer), 0.0, state_std, _p(out["state"]), out["state"].size)
+    return out
+
+
+def attn_inputs(seed: int, L: int, Hq: int = 16, Hkv: int = 2, D: int = 256, layer: int = 0) -> dict:
+    """One decode-attention call: query q [Hq, D] and the cache k, v [L, Hkv, D],
+    all bf16 ~ N(0, 1)."""
+    lib = _load()
+    out = {"q": np.empty((Hq, D), np.uint16), "k": np.empty((L, Hkv, D), np.uint16),
+           "v": np.empty((L, Hkv, D), np.uint16)}
+    for name, t in (("q", T_ATT_Q), ("k", T_ATT_K), ("v", T_ATT_V)):
+        if out[name].size:
+            lib.syn_fill_normal_bf16(key(seed, t, layer), 0.0, 1.0, _p(out[name]), out[name].size)
     return out
 
 

@@ -39,7 +39,9 @@ enum {
   /* Gated DeltaNet scan inputs */
   SYN_T_GDN_Q = 15, SYN_T_GDN_K = 16, SYN_T_GDN_V = 17, /* bf16                     */
   SYN_T_GDN_ALPHA = 18, SYN_T_GDN_BETA = 19,          /* fp32 ~ U(lo, hi)         */
-  SYN_T_GDN_STATE = 20                                 /* fp32 initial state        */
+  SYN_T_GDN_STATE = 20,                                /* fp32 initial state        */
+  /* decode attention inputs: query, key cache, value cache, bf16 ~ N(0, 1) */
+  SYN_T_ATT_Q = 21, SYN_T_ATT_K = 22, SYN_T_ATT_V = 23
 };
 
 uint64_t syn_key(uint64_t seed, uint32_t tensor, uint32_t layer, uint32_t expert);
