@@ -67,14 +67,21 @@ WORKLOADS = {
     "gdn2k": dict(T=2048, layers=1, chunk=2048, zipf=False, centred=False, Hk=16, Hv=32, dk=128, dv=128,
                   desc="Gated DeltaNet scan of one 2048-token sequence from an empty state (16 key heads, "
                        "32 value heads, dk = dv = 128), 6 distinct input sets cycled"),
+    "attn32k": dict(T=1, L=32768, layers=1, chunk=1, zipf=False, centred=False, Hq=16, Hkv=2, D=256, sets=4,
+                    desc="decode attention, one query token over a 32768-position KV cache (16 query heads, "
+                         "2 KV heads, head dim 256, bf16), 4 distinct caches cycled"),
+    "attn128k": dict(T=1, L=131072, layers=1, chunk=1, zipf=False, centred=False, Hq=16, Hkv=2, D=256, sets=2,
+                     desc="decode attention, one query token over a 131072-position KV cache (16 query heads, "
+                          "2 KV heads, head dim 256, bf16), 2 distinct caches cycled"),
 }
+ATTN_METRIC = "decode attention GB/s of KV cache streamed (T=1, 16 query / 2 KV heads, D=256); % of HBM"
 GDN_SETS = 6
 GDN_METRIC = "Gated DeltaNet scan tokens/s (one sequence, T=2048, 32 value heads); % of FP32 FMA peak"
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 flops (FMA) x max SM clock
 DEFAULT_STEPS = {"decode40": 2000, "layer256": 200, "layer512zipf": 200, "layer2048": 100, "layer4096": 50,
-                 "prefill32k": 3, "gdn2k": 30}
+                 "prefill32k": 3, "gdn2k": 30, "attn32k": 300, "attn128k": 100}
 DEFAULT_WARMUP = {"decode40": 50, "layer256": 10, "layer512zipf": 10, "layer2048": 5, "layer4096": 5,
-                  "prefill32k": 3, "gdn2k": 3}
+                  "prefill32k": 3, "gdn2k": 3, "attn32k": 10, "attn128k": 5}
 
 
 def parse():
@@ -544,6 +551,113 @@ def run_gdn(args, wl, rank, world, device):
                                    "together)", "experts": None}}
 
 
+def run_attn(args, wl, rank, world, device):
+    """Decode attention: each step is one query token against a KV cache of
+    wl["L"] positions (the caches cycle so that each step reads its cache from
+    HBM)."""
+    import torch
+    import __graft_entry__
+    import bit_grouped_expert_gb300 as moe
+    import synthetic as syn
+
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(device)
+    L, Hq, Hkv, D, n_sets = wl["L"], wl["Hq"], wl["Hkv"], wl["D"], wl["sets"]
+    seed = args.seed + 1000 * rank
+    host = [syn.attn_inputs(seed + i, L, Hq, Hkv, D) for i in range(n_sets)]
+    sets = [{n: as_dev(a, device) for n, a in h.items()} for h in host]
+    ws = torch.empty(moe.attn_decode_workspace_bytes(L, Hq, D), dtype=torch.uint8, device=device)
+    outs = [torch.empty((Hq, D), dtype=torch.int16, device=device) for _ in range(n_sets)]
+    stream = torch.cuda.Stream(device=device)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def body(i, prof=None):
+        d = sets[i]
+        if prof is not None:
+            moe.moe_profile_events(moe.MOE_KERNEL_ATTN_DECODE, ev_a[prof:prof + 1], ev_b[prof:prof + 1])
+        moe.attn_decode(d["q"], d["k"], d["v"], L, Hq, Hkv, D, ws, outs[i], stream=stream)
+        if prof is not None:
+            moe.moe_profile_events(moe.MOE_KERNEL_ATTN_DECODE)
+
+    with torch.cuda.stream(stream):
+        body(0)
+    torch.cuda.synchronize()
+    for e in ev_a + ev_b:
+        e.record(stream)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(n_sets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body(i, prof=min(i, 1) if i < 2 else None)  # the first two caches time the block pass
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % n_sets].replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id(device)) as clk:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(args.steps):
+                graphs[i % n_sets].replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    dom_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / 2
+    kv_bytes = 2 * L * Hkv * D * 2
+    gbs = kv_bytes * args.steps / (ms * 1e-3) / 1e9 * world
+    pk = peaks()
+    achieved = kv_bytes / (dom_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": TRAFFIC.get(args.workload),
+                "kernel": "attn_block_kernel (one block of positions per SM, 8 query heads per KV row read)",
+                "kernel_ms": round(dom_ms, 5), "peak_src": pk["src"]}
+    # end to end: the query in from pinned host memory, the output back
+    host_q = torch.from_numpy(np.ascontiguousarray(host[0]["q"]).view(np.int16)).pin_memory()
+    host_o = torch.empty((Hq, D), dtype=torch.int16).pin_memory()
+    e2e_steps = min(args.steps, 100)
+    torch.cuda.synchronize()
+    te = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            b = i % n_sets
+            sets[b]["q"].copy_(host_q, non_blocking=True)
+            graphs[b].replay()
+            host_o.copy_(outs[b], non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - te
+    e2e = {"value": kv_bytes * e2e_steps / e2e_s / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": Hq * D * 2,
+           "d2h_bytes_per_step": Hq * D * 2}
+    return {"metric": ATTN_METRIC, "value": gbs, "unit": "GB/s", "higher_is_better": True,
+            "ms_per_step": ms / args.steps, "roofline": roofline, "e2e": e2e, "clocks": clk.summary(),
+            "gpu_launches": 2 * args.steps, "dtype": "bf16 q/K/V/o, fp32 scores and sums, bf16 weights for P.V",
+            "config_extra": {"l2": f"{n_sets} distinct caches of {kv_bytes / 1e6:.0f} MB cycled (larger than L2 "
+                                   "together)", "experts": None, "kv_positions": L}}
+
+
+def attn_oracle_sample(wl, seed, target_s=None):
+    """The oracle on a prefix of the cache: as many positions as take about
+    target_s seconds (all of them at most); GB/s of K and V read."""
+    from oracle.attn import decode_attention
+    import synthetic as syn
+    L, Hq, Hkv, D = wl["L"], wl["Hq"], wl["Hkv"], wl["D"]
+    n = min(L, 4096)
+    while True:
+        d = syn.attn_inputs(seed, n, Hq, Hkv, D)
+        t = time.perf_counter()
+        decode_attention(d["q"], d["k"], d["v"])
+        dt = time.perf_counter() - t
+        if target_s is None or dt >= 0.5 * target_s or n >= L:
+            break
+        n = min(L, max(2 * n, int(n * target_s / max(dt, 1e-3))))
+    return dt, 2 * n * Hkv * D * 2 / 1e9, "GB/s", f"one query over the first {n} cache positions (GB of K and V read)"
+
+
 def gdn_oracle_sample(wl, seed, target_s=None):
     """The oracle scan over the first tokens of one sequence (all heads):
     64 tokens, or as many as take about target_s seconds."""
@@ -606,9 +720,10 @@ def oracle_sample(wl, seed, target_s=None):
 def cpu_baseline(wl, seed):
     import oracle as orc
     orc.build()
-    sample = gdn_oracle_sample if "Hv" in wl else oracle_sample
+    sample = gdn_oracle_sample if "Hv" in wl else attn_oracle_sample if "Hkv" in wl else oracle_sample
     dt, units, unit, desc = sample(wl, seed, target_s=10.0)
-    cores = 1 if "Hv" in wl else orc.num_threads()  # the scan oracle is single-threaded numpy
+    # the scan and attention oracles are numpy (the attention's matrix products may use BLAS threads)
+    cores = 1 if "Hv" in wl else (os.cpu_count() or 1) if "Hkv" in wl else orc.num_threads()
     return {"value": units / dt, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc,
             "seconds": round(dt, 3)}
 
@@ -618,7 +733,7 @@ def run_reference(args, wl):
     import synthetic as syn
     orc.build()
     syn.build()
-    sample = gdn_oracle_sample if "Hv" in wl else oracle_sample
+    sample = gdn_oracle_sample if "Hv" in wl else attn_oracle_sample if "Hkv" in wl else oracle_sample
     for i in range(args.warmup):
         sample(wl, args.seed + i)
     steps = args.steps
@@ -629,7 +744,8 @@ def run_reference(args, wl):
         units += u
     val = units / tot
     return {"value": val, "unit": unit, "higher_is_better": True, "ms_per_step": tot / steps * 1e3,
-            "cpu_baseline": {"value": val, "unit": unit, "cores": 1 if "Hv" in wl else orc.num_threads(),
+            "cpu_baseline": {"value": val, "unit": unit,
+                             "cores": 1 if "Hv" in wl else (os.cpu_count() or 1) if "Hkv" in wl else orc.num_threads(),
                              "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -647,12 +763,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    base = {"metric": GDN_METRIC if "Hv" in wl else METRIC, "n_gpus": args.gpus if world == 1 else world, "steps": args.steps,
+    base = {"metric": GDN_METRIC if "Hv" in wl else ATTN_METRIC if "Hkv" in wl else METRIC, "n_gpus": args.gpus if world == 1 else world, "steps": args.steps,
             "warmup": args.warmup, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
             "config": {"workload": f"{args.workload}: {wl['desc']}", "tokens_per_step": wl["T"],
                        "layers": wl["layers"], "chunk": wl["chunk"], "parallelism": "replicas" if world > 1 else "1 GPU",
                        "l2": (f"{GDN_SETS} distinct input sets cycled (~50 MB each, larger than L2 together)"
-                              if "Hv" in wl else "inputs larger than L2 (packed weights >= 455 MB per layer)"),
+                              if "Hv" in wl else f"{wl.get('sets')} distinct KV caches cycled" if "Hkv" in wl
+                              else "inputs larger than L2 (packed weights >= 455 MB per layer)"),
                        "experts": args.experts}}
     if args.impl == "reference":
         if rank != 0:
@@ -666,7 +783,7 @@ def main():
     if world > 1:
         torch.cuda.set_device(device)
         torch.distributed.init_process_group("nccl")
-    res = (run_gdn if "Hv" in wl else run_ours)(args, wl, rank, world, device)
+    res = (run_gdn if "Hv" in wl else run_attn if "Hkv" in wl else run_ours)(args, wl, rank, world, device)
     if rank == 0:
         extra = res.pop("config_extra", {})
         line = {**base, **res}

@@ -39,7 +39,7 @@ MOE_TRACE_SLOTS = 32
 EXPORTS = ("moe_plan", "moe_plan_destroy", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_route_from_logits", "moe_forward", "moe_route_view", "moe_rmsnorm", "moe_dequant",
            "moe_device_status", "moe_last_launch_count", "moe_status_str", "moe_profile_events", "moe_last_cuda_error",
-           "moe_decode_static", "moe_decode_stack", "gdn_scan")
+           "moe_decode_static", "moe_decode_stack", "gdn_scan", "attn_decode_workspace_bytes", "attn_decode")
 
 MOE_DECODE_STATIC_SCRATCH_BYTES = 65536
 
@@ -53,6 +53,7 @@ MOE_KERNEL_DECODE_LAYER = 7
 MOE_KERNEL_RMSNORM = 10
 MOE_KERNEL_GATHER = 11
 MOE_KERNEL_GDN_SCAN = 12
+MOE_KERNEL_ATTN_DECODE = 13
 
 
 class MoeError(RuntimeError):
@@ -129,6 +130,10 @@ def lib():
                                         u32, vp]
         L.gdn_scan.restype = i32
         L.gdn_scan.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        L.attn_decode_workspace_bytes.restype = sz
+        L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32]
+        L.attn_decode.restype = i32
+        L.attn_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, vp, sz, vp, vp]
         _lib = L
     return _lib
 
@@ -250,6 +255,19 @@ def gdn_scan(q, k, v, alpha, beta, state, o, T: int, Hk: int, Hv: int, dk: int =
     (updated in place), o [T, Hv, dv] bf16 (written)."""
     _check("gdn_scan", lib().gdn_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(state), _ptr(o),
                                       int(T), int(Hk), int(Hv), int(dk), int(dv), _stream(stream)))
+
+
+def attn_decode_workspace_bytes(L: int, Hq: int = 16, D: int = 256) -> int:
+    return int(lib().attn_decode_workspace_bytes(int(L), int(Hq), int(D)))
+
+
+def attn_decode(q, k, v, L: int, Hq: int, Hkv: int, D: int, ws, o, scale: float = 0.0, stream=None):
+    """One query token against a KV cache (attn.h): q [Hq, D], k, v [L, Hkv, D]
+    bf16, ws a uint8 device tensor of attn_decode_workspace_bytes(L, Hq, D)
+    bytes or more, o [Hq, D] bf16 (written)."""
+    _check("attn_decode", lib().attn_decode(_ptr(q), _ptr(k), _ptr(v), int(L), int(Hq), int(Hkv), int(D),
+                                            float(scale), _ptr(ws), _nbytes(ws) if not isinstance(ws, int) else 0,
+                                            _ptr(o), _stream(stream)))
 
 
 def moe_route_view(plan: Plan, ws, T: int) -> moe_route_ptrs:

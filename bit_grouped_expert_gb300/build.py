@@ -29,7 +29,7 @@ def sources():
 
 def headers():
     hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    return hs + [os.path.join(INCLUDE, "moe.h"), os.path.join(INCLUDE, "gdn.h")]
+    return hs + [os.path.join(INCLUDE, h) for h in ("moe.h", "gdn.h", "attn.h")]
 
 
 def _stale(target, deps):

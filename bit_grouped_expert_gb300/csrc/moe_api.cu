@@ -200,7 +200,7 @@ void prof_after(int kernel, cudaStream_t s) {
 extern "C" {
 
 moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *const *stop_events, int32_t n) {
-  if (kernel < MOE_KERNEL_ROUTER || kernel > MOE_KERNEL_GDN_SCAN || n < 0 || n > 4096) return MOE_ERR_INVALID_ARGUMENT;
+  if (kernel < MOE_KERNEL_ROUTER || kernel > MOE_KERNEL_ATTN_DECODE || n < 0 || n > 4096) return MOE_ERR_INVALID_ARGUMENT;
   if (n > 0 && (!start_events || !stop_events)) return MOE_ERR_INVALID_ARGUMENT;
   for (int i = 0; i < n; ++i)
     if (!start_events[i] || !stop_events[i]) return MOE_ERR_INVALID_ARGUMENT;

@@ -230,7 +230,8 @@ typedef enum {
   MOE_KERNEL_DECODE_LAYER = 7,   /* T == 1: the whole layer in one launch      */
   MOE_KERNEL_RMSNORM = 10,
   MOE_KERNEL_GATHER = 11,        /* routed x rows copied into perm order (tensor-core path) */
-  MOE_KERNEL_GDN_SCAN = 12       /* Gated DeltaNet scan (gdn.h)                */
+  MOE_KERNEL_GDN_SCAN = 12,      /* Gated DeltaNet scan (gdn.h)                */
+  MOE_KERNEL_ATTN_DECODE = 13    /* decode attention, per-block pass (attn.h)  */
 } moe_kernel;
 
 /* Profiling hook.  From now on, on the calling thread, the i-th launch of

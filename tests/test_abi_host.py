@@ -27,7 +27,7 @@ def _declared():
     names = set()
     for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))):
         src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b((?:moe|gdn)_[a-z_]+)\s*\(", src))
+        names |= set(re.findall(r"\b((?:moe|gdn|attn)_[a-z_]+)\s*\(", src))
     return sorted(names)
 
 
@@ -210,3 +210,28 @@ def test_gdn_scan_host_checks(lib):
     assert call(alpha=al + 4) == moe.MOE_ERR_MISALIGNED
     assert call(o=q + 4096) == moe.MOE_ERR_INVALID_ARGUMENT  # o overlaps q
     assert call(o=st) == moe.MOE_ERR_INVALID_ARGUMENT  # o overlaps the state
+
+
+def test_attn_decode_host_checks(lib):
+    import ctypes
+    q, k, v, ws, o = (0x10000000 + i * 0x1000000 for i in range(5))
+    need = lib.attn_decode_workspace_bytes(1000, 16, 256)
+    # up to one block per 64 positions (16 here): partial outputs 16*16*256 fp32, then the max and sum rows
+    assert need == 16 * 16 * 256 * 4 + 1024 + 16 * 16 * 4
+    assert lib.attn_decode_workspace_bytes(1 << 20, 16, 256) == 512 * 16 * 256 * 4 + 512 * 16 * 4 * 2  # 512 blocks at most
+    assert lib.attn_decode_workspace_bytes(0, 16, 256) == 0
+    assert lib.attn_decode_workspace_bytes(10, 16, 128) == 0
+
+    def call(L=1000, Hq=16, Hkv=2, D=256, scale=0.0, ws_bytes=need, **kw):
+        a = {**dict(q=q, k=k, v=v, ws=ws, o=o), **kw}
+        return lib.attn_decode(a["q"], a["k"], a["v"], L, Hq, Hkv, D, ctypes.c_float(scale), a["ws"], ws_bytes,
+                               a["o"], 0)
+
+    assert call(L=0) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert call(k=None) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert call(scale=-1.0) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert call(scale=float("nan")) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert call(D=128) == moe.MOE_ERR_UNSUPPORTED
+    assert call(Hq=8) == moe.MOE_ERR_UNSUPPORTED  # 4 query heads per KV head
+    assert call(v=v + 2) == moe.MOE_ERR_MISALIGNED
+    assert call(ws_bytes=need - 1) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
