@@ -569,7 +569,7 @@ def run_attn(args, wl, rank, world, device):
     seed = args.seed + 1000 * rank
     host = [syn.attn_inputs(seed + i, L, Hq, Hkv, D) for i in range(n_sets)]
     sets = [{n: as_dev(a, device) for n, a in h.items()} for h in host]
-    ws = torch.empty(moe.attn_decode_workspace_bytes(L, Hq, D), dtype=torch.uint8, device=device)
+    ws = torch.zeros(moe.attn_decode_workspace_bytes(L, Hq, D), dtype=torch.uint8, device=device)
     outs = [torch.empty((Hq, D), dtype=torch.int16, device=device) for _ in range(n_sets)]
     stream = torch.cuda.Stream(device=device)
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(2)]

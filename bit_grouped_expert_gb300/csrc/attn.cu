@@ -15,9 +15,11 @@
 //   softmax running maximum and sum per head (base-2 exponentials);
 //   output  O[8 heads x 256] += P . V   P rounded to bf16 and taken straight
 //           from the score fragments, V fragments by ldmatrix.trans.
-// K and V sub-tiles arrive by cp.async, two sub-tiles ahead, into each warp's
-// own buffers (rows padded to 528 bytes: the fragment reads hit 32 distinct
-// banks).  The warps' (max, sum, O) merge in shared memory into the block's
+// K and V sub-tiles arrive by bulk copies (TMA, one 512-byte row each, on a
+// per-stage mbarrier), three sub-tiles ahead, into each warp's own buffers
+// (rows padded to 528 bytes: the fragment reads hit 32 distinct banks).  The
+// waits are bounded: a wait that gives up sets MOE_ERR_DEVICE_TIMEOUT in the
+// workspace's status word.  The warps' (max, sum, O) merge in shared memory into the block's
 // partial result; a second kernel combines the blocks.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -27,6 +29,7 @@
 #include "attn.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -39,8 +42,9 @@ constexpr int AT_SUB = 16;                  // positions per sub-tile
 constexpr int AT_ROW = AT_D * 2 + 16;       // padded smem row (528 bytes)
 constexpr int AT_TILE = AT_SUB * AT_ROW;    // one K or V sub-tile
 constexpr int AT_STAGE = 2 * AT_TILE;       // K and V
-constexpr int AT_WARP_SMEM = 2 * AT_STAGE;  // two stages per warp
-constexpr int AT_SMEM = AT_WARPS * AT_WARP_SMEM;  // 135,168 bytes
+constexpr int AT_NSTAGE = 3;               // sub-tiles in flight per warp
+constexpr int AT_WARP_SMEM = AT_NSTAGE * AT_STAGE;
+constexpr int AT_SMEM = AT_WARPS * AT_WARP_SMEM;  // 202,752 bytes
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
   // rows 8-15 of A are zero: only the eight query heads of rows 0-7 are real
@@ -57,22 +61,25 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
                : "r"(addr));
 }
 
-// 16 bytes from global to shared; src_bytes 0 writes zeros and reads nothing
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)f32_to_bf16(lo) | ((uint32_t)f32_to_bf16(hi) << 16);
 }
 
+constexpr unsigned long long AT_TIMEOUT_NS = 1000000000ull;  // a copy wait gives up after 1 s
+
+// Bounded wait on an mbarrier phase; false once AT_TIMEOUT_NS has passed.
+__device__ bool at_wait(uint64_t *bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u))
+    if (ptx::globaltimer() - t0 > AT_TIMEOUT_NS) return false;
+  return true;
+}
+
 struct AttnArgs {
   const uint16_t *q, *k, *v;
+  int32_t *status;                  // sticky MOE_ERR_DEVICE_TIMEOUT
   float *part_o, *part_m, *part_l;  // [nblk][Hq][D], [nblk][Hq], [nblk][Hq]
   int L, Hq, Hkv;
   int blk_len, nsub;                // positions per block, sub-tiles per warp (blk_len / 64)
@@ -81,31 +88,36 @@ struct AttnArgs {
 
 __global__ void __launch_bounds__(AT_THREADS) attn_block_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ uint64_t bars[AT_WARPS][AT_NSTAGE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int blk = blockIdx.x, g = blockIdx.y;
   const int r = lane >> 2, c = lane & 3;  // fragment row (head / position) and column pair
   const int L = a.L, Hkv = a.Hkv;
   const int nsub = a.nsub, p_warp = blk * a.blk_len + warp * (a.blk_len / AT_WARPS);
   uint8_t *ws = smem + warp * AT_WARP_SMEM;
-  const uint32_t ws_u32 = static_cast<uint32_t>(__cvta_generic_to_shared(ws));
 
-  // this warp's sub-tile st into stage st & 1: 16 rows of K then of V, 512
-  // bytes each, 32 pieces of 16 bytes per row; rows past L are zero-filled
+  // this warp's sub-tile st into stage st % AT_NSTAGE: 16 rows of K and of V
+  // (512 bytes each, one bulk copy per row: lane i copies row i % 16 of K for
+  // i < 16, of V otherwise).  Rows past L are not copied.
+  uint64_t *wbar = bars[warp];
+  if (lane == 0) {
+    for (int s = 0; s < AT_NSTAGE; ++s) ptx::mbar_init(&wbar[s], 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
   auto issue = [&](int st) {
-    if (st < nsub) {
-      const uint32_t stage = ws_u32 + (st & 1) * AT_STAGE;
-      const int p0 = p_warp + st * AT_SUB;
-#pragma unroll
-      for (int i = 0; i < 2 * AT_SUB * 32 / 32; ++i) {  // 32 pieces per lane
-        const int idx = i * 32 + lane, kv = idx / (AT_SUB * 32), row = (idx / 32) % AT_SUB, piece = idx % 32;
-        const int pos = p0 + row;
-        const uint16_t *base = kv ? a.v : a.k;
-        const bool ok = pos < L;
-        const uint16_t *src = base + ((size_t)(ok ? pos : 0) * Hkv + g) * AT_D + piece * 8;
-        cp_async16_zfill(stage + kv * AT_TILE + row * AT_ROW + piece * 16, src, ok ? 16u : 0u);
-      }
-    }
-    cp_async_commit();
+    if (st >= nsub) return;
+    const int stg = st % AT_NSTAGE, p0 = p_warp + st * AT_SUB;
+    const int nvalid = min(AT_SUB, L - p0);
+    if (nvalid <= 0) return;
+    ptx::fence_proxy_async_smem();  // this stage's earlier reads come before the copies
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive_expect_tx(&wbar[stg], (uint32_t)(2 * nvalid * AT_D * 2));
+    __syncwarp();
+    const int row = lane & (AT_SUB - 1), kv = lane >> 4;
+    if (row < nvalid)
+      ptx::bulk_g2s(ws + stg * AT_STAGE + kv * AT_TILE + row * AT_ROW,
+                    (kv ? a.v : a.k) + ((size_t)(p0 + row) * Hkv + g) * AT_D, AT_D * 2, &wbar[stg]);
   };
 
   // the query rows of the group, as the A fragments of the 16 k-steps
@@ -123,21 +135,36 @@ __global__ void __launch_bounds__(AT_THREADS) attn_block_kernel(const __grid_con
   for (int t = 0; t < 32; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
   float m = -INFINITY, l = 0.f;  // running maximum (base-2 units) and this lane's part of the sum
 
-  issue(0);
-  issue(1);
+  for (int st = 0; st < AT_NSTAGE - 1; ++st) issue(st);
+  bool ok = true;
+  int st_fail = 0;
   for (int st = 0; st < nsub; ++st) {
     const int p0 = p_warp + st * AT_SUB;
-    cp_async_wait<1>();
-    __syncwarp();
-    if (p0 < L) {  // warp-uniform
-      const uint8_t *ks = ws + (st & 1) * AT_STAGE, *vs = ks + AT_TILE;
-      // scores of n-tiles 0 and 1 (positions p0 .. p0+7, p0+8 .. p0+15)
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    issue(st + AT_NSTAGE - 1);  // into the stage sub-tile st-1 used (every lane has finished it)
+    if (p0 < L && ok) {  // warp-uniform
+      ok = __all_sync(0xffffffffu, at_wait(&wbar[st % AT_NSTAGE], (uint32_t)(st / AT_NSTAGE) & 1u));
+      if (!ok) {
+        if (lane == 0) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
+        st_fail = st;
+        break;
+      }
+      uint8_t *ks = ws + (st % AT_NSTAGE) * AT_STAGE, *vs = ks + AT_TILE;
+      if (p0 + AT_SUB > L) {  // the cache's last sub-tile: V rows past L read as zeros
+        for (int row = L - p0; row < AT_SUB; ++row)
+          *reinterpret_cast<uint4 *>(vs + row * AT_ROW + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+      }
+      // scores of n-tiles 0 and 1 (positions p0 .. p0+7, p0+8 .. p0+15), each
+      // summed in four independent chains of four k-steps, then added
+      float sc[2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const uint32_t *krow = reinterpret_cast<const uint32_t *>(ks + (8 * j + r) * AT_ROW);
+        float part[4][4] = {};
 #pragma unroll
-        for (int s = 0; s < 16; ++s) mma16816(sc[j], qa[s], qb[s], krow[8 * s + c], krow[8 * s + 4 + c]);
+        for (int s = 0; s < 16; ++s) mma16816(part[s & 3], qa[s], qb[s], krow[8 * s + c], krow[8 * s + 4 + c]);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) sc[j][e] = (part[0][e] + part[1][e]) + (part[2][e] + part[3][e]);
       }
       // row r = head; this lane's positions p0 + 8j + 2c + {0, 1}
       float x[4];
@@ -160,10 +187,12 @@ __global__ void __launch_bounds__(AT_THREADS) attn_block_kernel(const __grid_con
 #pragma unroll
       for (int e = 0; e < 4; ++e) pr[e] = exp2f(x[e] - mn);
       l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {  // a head's maximum moved: rescale its sums
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        o[t][0] *= alpha;
-        o[t][1] *= alpha;
+        for (int t = 0; t < 32; ++t) {
+          o[t][0] *= alpha;
+          o[t][1] *= alpha;
+        }
       }
       const uint32_t pa0 = pack_bf16x2(pr[0], pr[1]), pa2 = pack_bf16x2(pr[2], pr[3]);
       // O += P . V, 16 output dimensions per ldmatrix
@@ -178,9 +207,11 @@ __global__ void __launch_bounds__(AT_THREADS) attn_block_kernel(const __grid_con
       }
     }
     __syncwarp();  // every lane is done with this stage before it is refilled
-    issue(st + 2);
   }
-  cp_async_wait<0>();
+  if (!ok) {  // let the copies still in flight land (bounded) before the buffers are reused
+    for (int st = st_fail; st < min(nsub, st_fail + AT_NSTAGE); ++st)
+      if (p_warp + st * AT_SUB < L) at_wait(&wbar[st % AT_NSTAGE], (uint32_t)(st / AT_NSTAGE) & 1u);
+  }
   __syncthreads();  // the staging buffers become the merge area
 
   // merge the four warps: per warp m[8], l[8], O[8][256]
@@ -229,14 +260,17 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restri
                                                            uint16_t *__restrict__ out) {
   __shared__ float sm_m[8][32], sm_n[8][32], sm_d[8][32];
   const int h = blockIdx.x, wg = threadIdx.x >> 5, lane = threadIdx.x & 31, d = blockIdx.y * 32 + lane;
-  float M = -INFINITY, num = 0.f, den = 0.f;
+  // the maximum first (independent loads), then the weighted sums
+  float M = -INFINITY;
+#pragma unroll 4
+  for (int b = wg; b < nblk; b += 8) M = fmaxf(M, part_m[(size_t)b * Hq + h]);
+  float num = 0.f, den = 0.f;
+#pragma unroll 4
   for (int b = wg; b < nblk; b += 8) {
     const size_t row = (size_t)b * Hq + h;
-    const float mb = part_m[row], ob = part_o[row * AT_D + d], lb = part_l[row];
-    const float mn = fmaxf(M, mb), fo = exp2f(M - mn), fb = exp2f(mb - mn);
-    num = num * fo + fb * ob;
-    den = den * fo + fb * lb;
-    M = mn;
+    const float f = exp2f(part_m[row] - M);
+    num = fmaf(f, part_o[row * AT_D + d], num);
+    den = fmaf(f, part_l[row], den);
   }
   sm_m[wg][lane] = M;
   sm_n[wg][lane] = num;
@@ -268,8 +302,9 @@ void block_split(int L, int Hkv, int num_sms, int *nblk, int *blk_len) {
   *nblk = (L + len - 1) / len;
 }
 
+// Workspace: the status word (256 bytes reserved), partial outputs, maxima, sums.
 size_t ws_layout(int nblk, int Hq, size_t *off_m, size_t *off_l) {
-  const size_t o = (size_t)nblk * Hq * AT_D * 4;
+  const size_t o = 256 + (size_t)nblk * Hq * AT_D * 4;
   *off_m = o;
   *off_l = o + (((size_t)nblk * Hq * 4 + 255) / 256) * 256;
   return *off_l + (size_t)nblk * Hq * 4;
@@ -313,7 +348,8 @@ extern "C" moe_status attn_decode(const void *q_d, const void *k_d, const void *
   a.q = static_cast<const uint16_t *>(q_d);
   a.k = static_cast<const uint16_t *>(k_d);
   a.v = static_cast<const uint16_t *>(v_d);
-  a.part_o = reinterpret_cast<float *>(ws);
+  a.status = reinterpret_cast<int32_t *>(ws);
+  a.part_o = reinterpret_cast<float *>(ws + 256);
   a.part_m = reinterpret_cast<float *>(ws + off_m);
   a.part_l = reinterpret_cast<float *>(ws + off_l);
   a.L = L;

@@ -39,8 +39,10 @@ size_t attn_decode_workspace_bytes(int L, int Hq, int D);
  *   k_d     bf16 [L][Hkv][D]      key cache, position-major (read)
  *   v_d     bf16 [L][Hkv][D]      value cache, same layout (read)
  *   scale   fp32                  score scale; 0 means 1 / sqrt(D)
- *   ws_d    device workspace of ws_bytes >= attn_decode_workspace_bytes(L, Hq, D)
- *           (scratch, contents need no initialisation)
+ *   ws_d    device workspace of ws_bytes >= attn_decode_workspace_bytes(L, Hq, D):
+ *           scratch, except its first int32, a status word that the call only
+ *           sets, to MOE_ERR_DEVICE_TIMEOUT, if a wait for cache rows gave up
+ *           (after 1 s; the output is then invalid).  Zero it to use it.
  *   o_d     bf16 [Hq][D]          output (written)
  * Supported: D == 256, Hq == 8 * Hkv, 1 <= L <= 2^24.
  * Errors: MOE_ERR_INVALID_ARGUMENT (null pointer, L < 1, Hkv < 1, scale < 0 or

@@ -217,8 +217,8 @@ def test_attn_decode_host_checks(lib):
     q, k, v, ws, o = (0x10000000 + i * 0x1000000 for i in range(5))
     need = lib.attn_decode_workspace_bytes(1000, 16, 256)
     # up to one block per 64 positions (16 here): partial outputs 16*16*256 fp32, then the max and sum rows
-    assert need == 16 * 16 * 256 * 4 + 1024 + 16 * 16 * 4
-    assert lib.attn_decode_workspace_bytes(1 << 20, 16, 256) == 512 * 16 * 256 * 4 + 512 * 16 * 4 * 2  # 512 blocks at most
+    assert need == 256 + 16 * 16 * 256 * 4 + 1024 + 16 * 16 * 4  # status word, then the partials
+    assert lib.attn_decode_workspace_bytes(1 << 20, 16, 256) == 256 + 512 * 16 * 256 * 4 + 512 * 16 * 4 * 2
     assert lib.attn_decode_workspace_bytes(0, 16, 256) == 0
     assert lib.attn_decode_workspace_bytes(10, 16, 128) == 0
 

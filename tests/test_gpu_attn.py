@@ -34,10 +34,11 @@ def _built():
 
 
 def _run(d, L, Hq=16, Hkv=2, scale=0.0):
-    ws = torch.empty(moe.attn_decode_workspace_bytes(L, Hq, 256), dtype=torch.uint8, device="cuda:0")
+    ws = torch.zeros(moe.attn_decode_workspace_bytes(L, Hq, 256), dtype=torch.uint8, device="cuda:0")
     o = torch.full((Hq, 256), 0x7FC0, dtype=torch.int16, device="cuda:0")
     moe.attn_decode(dev(d["q"]), dev(d["k"]), dev(d["v"]), L, Hq, Hkv, 256, ws, o, scale=scale)
     torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0  # the status word: no wait gave up
     return host_u16(o)
 
 
