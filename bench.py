@@ -47,6 +47,8 @@ TRAFFIC = {
     "layer256": 316_907_520,      # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer256.md
     "layer4096": 484_388_608,     # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer4096.md
     "gdn2k": 36_325_888,          # gdn_scan_kernel, profiles/gdn_scan_gdn2k.md
+    "attn32k": 67_307_776,        # attn_block_kernel, profiles/attn_block_attn128k.md
+    "attn128k": 268_621_926,      # attn_block_kernel, profiles/attn_block_attn128k.md
 }
 METRIC = "MoE-layer prefill tokens/s & % of roofline (T=256–32K); T=1 HBM GB/s"
 
@@ -79,7 +81,7 @@ GDN_SETS = 6
 GDN_METRIC = "Gated DeltaNet scan tokens/s (one sequence, T=2048, 32 value heads); % of FP32 FMA peak"
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 flops (FMA) x max SM clock
 DEFAULT_STEPS = {"decode40": 2000, "layer256": 200, "layer512zipf": 200, "layer2048": 100, "layer4096": 50,
-                 "prefill32k": 3, "gdn2k": 30, "attn32k": 300, "attn128k": 100}
+                 "prefill32k": 3, "gdn2k": 1500, "attn32k": 40000, "attn128k": 16000}  # >= ~1 s timed: clock samples
 DEFAULT_WARMUP = {"decode40": 50, "layer256": 10, "layer512zipf": 10, "layer2048": 5, "layer4096": 5,
                   "prefill32k": 3, "gdn2k": 3, "attn32k": 10, "attn128k": 5}
 
@@ -135,6 +137,9 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0:  # sampling is running before the timed region starts
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self

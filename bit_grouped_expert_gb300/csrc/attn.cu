@@ -260,17 +260,32 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restri
                                                            uint16_t *__restrict__ out) {
   __shared__ float sm_m[8][32], sm_n[8][32], sm_d[8][32];
   const int h = blockIdx.x, wg = threadIdx.x >> 5, lane = threadIdx.x & 31, d = blockIdx.y * 32 + lane;
-  // the maximum first (independent loads), then the weighted sums
-  float M = -INFINITY;
-#pragma unroll 4
-  for (int b = wg; b < nblk; b += 8) M = fmaxf(M, part_m[(size_t)b * Hq + h]);
-  float num = 0.f, den = 0.f;
-#pragma unroll 4
-  for (int b = wg; b < nblk; b += 8) {
-    const size_t row = (size_t)b * Hq + h;
-    const float f = exp2f(part_m[row] - M);
-    num = fmaf(f, part_o[row * AT_D + d], num);
-    den = fmaf(f, part_l[row], den);
+  // blocks wg, wg + 8, ... in groups of eight, each group's loads issued
+  // together, merged into a running maximum
+  float M = -INFINITY, num = 0.f, den = 0.f;
+  for (int b0 = wg; b0 < nblk; b0 += 64) {
+    float mb[8], ob[8], lb[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int b = b0 + 8 * i;
+      const size_t row = (size_t)(b < nblk ? b : b0) * Hq + h;
+      mb[i] = b < nblk ? part_m[row] : -INFINITY;
+      ob[i] = part_o[row * AT_D + d];
+      lb[i] = part_l[row];
+    }
+    float mx = M;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx = fmaxf(mx, mb[i]);
+    const float fo = exp2f(M - mx);  // 0 while M is still -inf
+    num *= fo;
+    den *= fo;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float f = exp2f(mb[i] - mx);  // 0 for the slots past nblk
+      num = fmaf(f, ob[i], num);
+      den = fmaf(f, lb[i], den);
+    }
+    M = mx;
   }
   sm_m[wg][lane] = M;
   sm_n[wg][lane] = num;
