@@ -511,6 +511,9 @@ def run_gdn(args, wl, rank, world, device):
         for i in range(args.warmup):
             graphs[i % GDN_SETS].replay()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_id(device)) as clk:
         with torch.cuda.stream(stream):
@@ -519,7 +522,14 @@ def run_gdn(args, wl, rank, world, device):
                 graphs[i % GDN_SETS].replay()
             t1.record(stream)
         torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
+    if world > 1:  # the slowest rank's time
+        tt = torch.tensor([ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
     dom_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / 2
     tps = T * args.steps / (ms * 1e-3) * world
     flops = 7.0 * Hv * dk * dv * T  # per sequence: u (2), state update (3), output (2) per state element per token
@@ -604,6 +614,9 @@ def run_attn(args, wl, rank, world, device):
         for i in range(args.warmup):
             graphs[i % n_sets].replay()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_id(device)) as clk:
         with torch.cuda.stream(stream):
@@ -612,7 +625,14 @@ def run_attn(args, wl, rank, world, device):
                 graphs[i % n_sets].replay()
             t1.record(stream)
         torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
+    if world > 1:  # the slowest rank's time
+        tt = torch.tensor([ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
     dom_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / 2
     kv_bytes = 2 * L * Hkv * D * 2
     gbs = kv_bytes * args.steps / (ms * 1e-3) / 1e9 * world

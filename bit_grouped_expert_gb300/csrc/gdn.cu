@@ -5,10 +5,12 @@
 // taken per token as: u = S^T k (what the state holds for k), delta =
 // beta (v - alpha u), S = alpha S + k delta^T, o = S^T q.
 //
-// Work split: one CTA per (value head, 32 value columns), 256 threads.  Thread
-// (column c, row part r of 8) keeps S[16 r .. 16 r + 15][c] in 16 registers
-// for the whole sequence; the eight parts of a column are neighbouring lanes,
-// so the column sums u and o take three xor-shuffles.  Per token the CTA needs
+// Work split: one CTA per (value head, 32 value columns), 512 threads.  Thread
+// (column c, row part r of 16) keeps S[8 r .. 8 r + 7][c] in 8 registers for
+// the whole sequence; the sixteen parts of a column are neighbouring lanes, so
+// the column sums u and o take four xor-shuffles.  (Four warps per scheduler
+// give it independent work while each token's chain waits; with eight row
+// parts the scan took 7 % longer.)  Per token the CTA needs
 // k_t and q_t of its key head, its 32 values of v_t, alpha_t and beta_t (600
 // bytes).  Tokens move in blocks of GDN_BLK: cp.async brings block j+2 into a
 // ring of three raw blocks in shared memory while the threads that copied
@@ -27,7 +29,7 @@ namespace {
 
 constexpr int GDN_DK = 128;
 constexpr int GDN_COLS = 32;                // value columns per CTA
-constexpr int GDN_RQ = 8;                   // row parts per column
+constexpr int GDN_RQ = 16;                  // row parts per column
 constexpr int GDN_ROWS = GDN_DK / GDN_RQ;   // state rows per thread
 constexpr int GDN_THREADS = GDN_COLS * GDN_RQ;
 constexpr int GDN_BLK = 8;                  // tokens per block
