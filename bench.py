@@ -46,7 +46,7 @@ TRAFFIC = {
     "decode40": 126_374_656,      # decode_layer_kernel, one 7-layer launch, profiles/decode_layer_decode40.md
     "layer256": 316_907_520,      # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer256.md
     "layer4096": 484_388_608,     # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer4096.md
-    "gdn2k": 36_325_888,          # gdn_scan_kernel, profiles/gdn_scan_gdn2k.md
+    "gdn2k": 36_231_706,          # gdn_scan_kernel, profiles/gdn_scan_gdn2k.md
     "attn32k": 67_307_776,        # attn_block_kernel, profiles/attn_block_attn128k.md
     "attn128k": 268_621_926,      # attn_block_kernel, profiles/attn_block_attn128k.md
 }
