@@ -178,6 +178,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def gpu_id(device):
     """nvidia-smi id of a torch device (its UUID when torch exposes it)."""
     import torch
@@ -364,9 +372,7 @@ def run_ours(args, wl, rank, world, device):
     except Exception as ex:  # noqa: BLE001 - reported in the JSON line
         dom_ms, dom_err = None, f"{type(ex).__name__}: {ex}"[:300]
     if world > 1:
-        tt = torch.tensor([ms], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, device)
 
     # bytes / flops of the workload
     h_out = out.cpu()
@@ -527,9 +533,7 @@ def run_gdn(args, wl, rank, world, device):
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
     if world > 1:  # the slowest rank's time
-        tt = torch.tensor([ms], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, device)
     dom_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / 2
     tps = T * args.steps / (ms * 1e-3) * world
     flops = 7.0 * Hv * dk * dv * T  # per sequence: u (2), state update (3), output (2) per state element per token
@@ -630,9 +634,7 @@ def run_attn(args, wl, rank, world, device):
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
     if world > 1:  # the slowest rank's time
-        tt = torch.tensor([ms], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, device)
     dom_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / 2
     kv_bytes = 2 * L * Hkv * D * 2
     gbs = kv_bytes * args.steps / (ms * 1e-3) / 1e9 * world
