@@ -20,7 +20,8 @@
 // (rows padded to 528 bytes: the fragment reads hit 32 distinct banks).  The
 // waits are bounded: a wait that gives up sets MOE_ERR_DEVICE_TIMEOUT in the
 // workspace's status word.  The warps' (max, sum, O) merge in shared memory into the block's
-// partial result; a second kernel combines the blocks.
+// partial result; a second kernel, launched as its programmatic dependent so
+// that it is resident when the pass ends, combines the blocks.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -89,6 +90,8 @@ struct AttnArgs {
 __global__ void __launch_bounds__(AT_THREADS) attn_block_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ uint64_t bars[AT_WARPS][AT_NSTAGE];
+  // the combine kernel may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int blk = blockIdx.x, g = blockIdx.y;
   const int r = lane >> 2, c = lane & 3;  // fragment row (head / position) and column pair
@@ -259,6 +262,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restri
                                                            const float *__restrict__ part_l, int nblk, int Hq,
                                                            uint16_t *__restrict__ out) {
   __shared__ float sm_m[8][32], sm_n[8][32], sm_d[8][32];
+  // launched as a programmatic dependent of the block pass: resident early,
+  // it reads the partials only once that grid has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int h = blockIdx.x, wg = threadIdx.x >> 5, lane = threadIdx.x & 31, d = blockIdx.y * 32 + lane;
   // blocks wg, wg + 8, ... in groups of eight, each group's loads issued
   // together, merged into a running maximum
@@ -379,7 +385,23 @@ extern "C" moe_status attn_decode(const void *q_d, const void *k_d, const void *
   moe::prof_after(MOE_KERNEL_ATTN_DECODE, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return moe::note_cuda_error(e);
-  moe::attn_combine_kernel<<<dim3(Hq, moe::AT_D / 32), 256, 0, s>>>(a.part_o, a.part_m, a.part_l, nblk, Hq,
-                                                                    static_cast<uint16_t *>(o_d));
-  return moe::note_cuda_error(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Hq, moe::AT_D / 32);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  uint16_t *out = static_cast<uint16_t *>(o_d);
+  e = cudaLaunchKernelEx(&cfg, moe::attn_combine_kernel, (const float *)a.part_o, (const float *)a.part_m,
+                         (const float *)a.part_l, nblk, Hq, out);
+  if (e != cudaSuccess) {  // a driver that refuses the attribute: a plain launch after the block pass
+    cudaGetLastError();
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, moe::attn_combine_kernel, (const float *)a.part_o, (const float *)a.part_m,
+                           (const float *)a.part_l, nblk, Hq, out);
+  }
+  return moe::note_cuda_error(e);
 }
