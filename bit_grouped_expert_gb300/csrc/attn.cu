@@ -6,7 +6,7 @@
 // is read once for all eight query heads that share it (their eight rows fill
 // the useful half of the tensor-core tiles below).  The block length is a
 // multiple of 64 chosen per call so that the CTAs fill the SMs once (one CTA
-// per SM: the staging buffers take 135 KB), which spreads the cache evenly and
+// per SM: the staging buffers take 198 KB), which spreads the cache evenly and
 // pays each CTA's prologue and merge once per SM.  The CTA's four warps take a
 // quarter of the block each and run a flash-decoding pass over it in sub-tiles
 // of 16 positions:
@@ -19,9 +19,10 @@
 // per-stage mbarrier), three sub-tiles ahead, into each warp's own buffers
 // (rows padded to 528 bytes: the fragment reads hit 32 distinct banks).  The
 // waits are bounded: a wait that gives up sets MOE_ERR_DEVICE_TIMEOUT in the
-// workspace's status word.  The warps' (max, sum, O) merge in shared memory into the block's
-// partial result; a second kernel, launched as its programmatic dependent so
-// that it is resident when the pass ends, combines the blocks.
+// workspace's status word.  The warps' (max, sum, O) merge in shared memory
+// into the block's partial result; a second kernel, launched as its
+// programmatic dependent so that it is resident when the pass ends, combines
+// the blocks.
 #include <cuda_bf16.h>
 #include <math.h>
 
