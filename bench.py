@@ -3,15 +3,22 @@
 
 Workloads (all inputs seeded and synthetic, shapes of the pages' model:
 H=2048, 256 routed experts, top-8, one shared expert, I=512, int4 g64):
-  decode40     (default) one token at a time through a stack of 40 MoE layers
-               with RMSNorm + residual between layers; metric: HBM GB/s of the
+  prefill32k   (default) a 32768-token prompt in 4096-token chunks through 40
+               pre-norm MoE layers (the library's chunk loop,
+               moe_prefill_stack), centred weight generator; tokens/s.  The
+               default run adds, from the same process, the same prompt with
+               the literal generator, decode40, layer4096 and layer2048
+               ("extras" in the JSON line; --no-extras leaves them out).
+  decode40     one token at a time through a stack of 40 MoE layers with
+               RMSNorm + residual between layers; metric: HBM GB/s of the
                bytes a token must stream (router + 9 experts per layer).
   layer256     one layer, T=256
   layer512zipf one layer, T=512, Zipf(1.1)-skewed routing
   layer2048    one layer, T=2048
   layer4096    one layer, T=4096
-  prefill32k   a 32768-token prompt in 4096-token chunks through 40 layers
-The prefill workloads report tokens/s.
+The prefill workloads report tokens/s and R_gemm, the grouped gate/up and
+down GEMMs' time against the slower of their FLOPs at the bf16 peak and their
+packed bytes at the HBM bandwidth.
 
 One JSON line is printed by rank 0.  ``--impl reference`` times the CPU
 oracle (the only reference this project has) on a bounded sample of the
@@ -43,9 +50,6 @@ ROUTER_BYTES = E * H * 4                                              # 2,097,15
 # capture of the current kernels (profiles/*.md give the commands); None
 # where no capture of that workload exists.  Update with every kernel change.
 TRAFFIC = {
-    "decode40": 126_374_656,      # decode_layer_kernel, one 7-layer launch, profiles/decode_layer_decode40.md
-    "layer256": 316_907_520,      # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer256.md
-    "layer4096": 484_388_608,     # experts_tc_kernel<gate/up>, profiles/grouped_experts_tc_layer4096.md
     "gdn2k": 36_231_706,          # gdn_scan_kernel, profiles/gdn_scan_gdn2k.md
     "attn32k": 67_307_776,        # attn_block_kernel, profiles/attn_block_attn128k.md
     "attn128k": 268_621_926,      # attn_block_kernel, profiles/attn_block_attn128k.md
@@ -81,7 +85,7 @@ GDN_SETS = 6
 GDN_METRIC = "Gated DeltaNet scan tokens/s (one sequence, T=2048, 32 value heads); % of FP32 FMA peak"
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 flops (FMA) x max SM clock
 DEFAULT_STEPS = {"decode40": 2000, "layer256": 200, "layer512zipf": 200, "layer2048": 100, "layer4096": 50,
-                 "prefill32k": 3, "gdn2k": 1500, "attn32k": 40000, "attn128k": 16000}  # >= ~1 s timed: clock samples
+                 "prefill32k": 8, "gdn2k": 1500, "attn32k": 40000, "attn128k": 16000}  # >= ~1 s timed: clock samples
 DEFAULT_WARMUP = {"decode40": 50, "layer256": 10, "layer512zipf": 10, "layer2048": 5, "layer4096": 5,
                   "prefill32k": 3, "gdn2k": 3, "attn32k": 10, "attn128k": 5}
 
@@ -91,7 +95,13 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="decode40", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="prefill32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--tile-rows", type=int, default=128, choices=[128, 64],
+                    help="token rows per grouped-GEMM tile (64: MOE_FLAG_TILE_ROWS_64)")
+    ap.add_argument("--generator", default=None, choices=["centred", "literal"],
+                    help="weight generator of a prefill workload (default: the workload's own)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="prefill32k: leave out the literal-generator, decode and single-layer lines")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--experts", default="tc", choices=["tc", "simt"], help="grouped GEMM kernels")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -198,21 +208,35 @@ def gpu_id(device):
 
 # ------------------------------------------------------------------ inputs
 
-def layer_weights(seed, layer, centred, device):
-    """Host-generated packed weights of one layer, copied to the device."""
-    import torch
-    import synthetic as syn
-    W = syn.experts(seed, E + 1, H, I_DIM, layer=layer, centred=centred)
-    W["router"] = syn.router(seed, E, H, layer=layer)
-    out = {}
-    for n, a in W.items():
-        a = np.ascontiguousarray(a)
-        if a.dtype == np.uint16:
-            a = a.view(np.int16)
-        elif a.dtype == np.uint32:
-            a = a.view(np.int32)
-        out[n] = torch.from_numpy(a).to(device)
-    return out
+class WeightCache:
+    """Packed weights of the stack's layers on the device, generated on the
+    host once per (seed, layer, generator) and shared by the workloads of one
+    run; each layer also gets the router's bf16 parts (moe_router_split) once."""
+
+    def __init__(self, device):
+        self.device = device
+        self.layers = {}
+
+    def get(self, seed, layer, centred):
+        import torch
+        import bit_grouped_expert_gb300 as moe
+        import synthetic as syn
+        key = (seed, layer, bool(centred))
+        if key not in self.layers:
+            W = syn.experts(seed, E + 1, H, I_DIM, layer=layer, centred=centred)
+            W["router"] = syn.router(seed, E, H, layer=layer)
+            out = {}
+            for n, a in W.items():
+                a = np.ascontiguousarray(a)
+                if a.dtype == np.uint16:
+                    a = a.view(np.int16)
+                elif a.dtype == np.uint32:
+                    a = a.view(np.int32)
+                out[n] = torch.from_numpy(a).to(self.device)
+            out["router_split"] = torch.empty(moe.moe_router_split_bytes(E, H), dtype=torch.uint8, device=self.device)
+            moe.moe_router_split(out["router"], E, H, out["router_split"])
+            self.layers[key] = out
+        return self.layers[key]
 
 
 def as_dev(a, device):
@@ -225,26 +249,33 @@ def as_dev(a, device):
 
 # ------------------------------------------------------------------ our arm
 
-def run_ours(args, wl, rank, world, device):
+def gemm_flops(rows):
+    """Expert FLOPs of the grouped gate/up and down GEMMs for `rows` token
+    rows (pairs + shared rows): 2 matrices x 2 flops x H x I, and 2 x H x I."""
+    return 4 * rows * H * I_DIM, 2 * rows * H * I_DIM
+
+
+def run_ours(args, wl, rank, world, device, cache=None, steps=None, warmup=None, e2e_on=True, name=None):
     import torch
-    import __graft_entry__
     import bit_grouped_expert_gb300 as moe
     import synthetic as syn
 
-    if rank == 0:
-        __graft_entry__.build()
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.set_device(device)
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
+    name = args.workload if name is None else name
+    cache = cache or WeightCache(device)
     T, L, chunk = wl["T"], wl["layers"], wl["chunk"]
     flags = moe.MOE_FLAG_SIMT_EXPERTS if args.experts == "simt" else 0
+    if args.tile_rows == 64:
+        flags |= moe.MOE_FLAG_TILE_ROWS_64
     if L > 1:
         flags |= moe.MOE_FLAG_PRENORM  # stacks: out = r + MoE(RMSNorm(r)), in place
     plan = moe.moe_plan(moe.make_config(H, E, K_TOP, I_DIM, 1, G), chunk, flags)
     ws = torch.zeros(moe.moe_workspace_bytes(plan), dtype=torch.uint8, device=device)
     moe.moe_workspace_init(plan, ws)
     seed = args.seed + 1000 * rank
-    weights = [layer_weights(seed, l, wl["centred"], device) for l in range(L)]
+    weights = [cache.get(seed, l, wl["centred"]) for l in range(L)]
     cws = [moe.make_weights(w) for w in weights]
     bias = as_dev(syn.zipf_bias(seed, E), device) if wl["zipf"] else None
 
@@ -255,51 +286,42 @@ def run_ours(args, wl, rank, world, device):
         x_in = torch.empty((1, H), dtype=torch.int16, device=device)
     else:
         x_in = as_dev(x_host, device)
-    r = torch.empty((chunk, H), dtype=torch.int16, device=device)
+    r = torch.empty((T if T > 1 else 1, H), dtype=torch.int16, device=device)
     out = torch.empty((T, H), dtype=torch.int16, device=device)
 
     stream = torch.cuda.Stream(device=device)
     launches = [0]
 
-    # dominant kernel: gate/up (decode: the decode kernel, which runs up to
-    # STACK layers per cooperative launch).  Only a few of its launches per
-    # step are bracketed by events, so the event nodes in the captured step
-    # barely perturb the step time.
-    dom = moe.MOE_KERNEL_DECODE_LAYER if T == 1 else moe.MOE_KERNEL_GATEUP
+    # Timed kernels.  Decode: the decode kernel, which runs up to STACK layers
+    # per cooperative launch (the 2nd and 4th launches of a step are
+    # bracketed).  Prefill: the grouped gate/up and down GEMMs, N_EV launches
+    # of each per step (the stacks: spread over the chunks and layers).
+    N_EV = 4
     if T == 1 and L > 1:
-        # layer groups of one launch each; the 2nd and 4th (full) ones are timed
         groups = [(l0, min(L, l0 + STACK)) for l0 in range(0, L, STACK)]
         prof_groups = [j for j in (1, 3) if j < len(groups) and groups[j][1] - groups[j][0] == STACK] or [0]
-        n_dom = len(prof_groups)
         layers_per_launch = groups[prof_groups[0]][1] - groups[prof_groups[0]][0]
+        kerns = [moe.MOE_KERNEL_DECODE_LAYER]
+        n_ev = len(prof_groups)
     else:
-        prof_layers = sorted({(2 * j + 1) * L // 8 for j in range(4)}) if L >= 4 else [0]
-        n_dom = len(prof_layers)
         layers_per_launch = 1
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_dom)]
+        kerns = [moe.MOE_KERNEL_GATEUP, moe.MOE_KERNEL_DOWN]
+        n_ev = N_EV
+    ev = {kn: ([torch.cuda.Event(enable_timing=True) for _ in range(n_ev)],
+               [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]) for kn in kerns}
     profiling = [False]
-
-    def forward(l, c0, x_arg, out_arg):
-        on = profiling[0] and c0 == 0 and l in prof_layers
-        if on:
-            j = prof_layers.index(l)
-            moe.moe_profile_events(dom, ev_a[j:j + 1], ev_b[j:j + 1])
-        moe.moe_forward(plan, x_arg, None, chunk, cws[l], bias, out_arg, ws, stream=stream)
-        launches[0] += moe.moe_last_launch_count()
-        if on:
-            moe.moe_profile_events(dom)
 
     def stack(j):
         on = profiling[0] and j in prof_groups
+        kn = kerns[0]
         if on:
             i = prof_groups.index(j)
-            moe.moe_profile_events(dom, ev_a[i:i + 1], ev_b[i:i + 1])
+            moe.moe_profile_events(kn, ev[kn][0][i:i + 1], ev[kn][1][i:i + 1])
         l0, l1 = groups[j]
         moe.moe_decode_stack(plan, r, cws[l0:l1], None, ws, stream=stream)
         launches[0] += moe.moe_last_launch_count()
         if on:
-            moe.moe_profile_events(dom)
+            moe.moe_profile_events(kn)
 
     def body(xb=x_in, ob=out):
         launches[0] = 0
@@ -310,14 +332,22 @@ def run_ours(args, wl, rank, world, device):
                 stack(j)
             ob.copy_(r)
             return
-        for c0 in range(0, T, chunk):
-            if L == 1:
-                forward(0, c0, xb[c0:c0 + chunk], ob[c0:c0 + chunk])
-                continue
-            r.copy_(xb[c0:c0 + chunk])
-            for l in range(L):
-                forward(l, c0, r, r)
-            ob[c0:c0 + chunk].copy_(r)
+        if profiling[0]:
+            for kn in kerns:
+                moe.moe_profile_events(kn, ev[kn][0], ev[kn][1])
+                if L > 1:  # 4 of the step's chunk-layers: (0, 0), (2, 1), (4, 2), (6, 3)
+                    moe.moe_profile_stride(kn, (T // chunk) * L // n_ev + 1)
+        if L == 1:
+            moe.moe_forward(plan, xb, None, T, cws[0], bias, ob, ws, stream=stream)
+            launches[0] += moe.moe_last_launch_count()
+        else:  # the library's chunk loop over the whole prompt
+            r.copy_(xb)
+            moe.moe_prefill_stack(plan, r, T, cws, None, ws, stream=stream)
+            launches[0] += moe.moe_last_launch_count()
+            ob.copy_(r)
+        if profiling[0]:
+            for kn in kerns:
+                moe.moe_profile_events(kn)
 
     # warm the path once eagerly, then capture one step into a CUDA graph
     with torch.cuda.stream(stream):
@@ -325,8 +355,9 @@ def run_ours(args, wl, rank, world, device):
             x_in.copy_(tokens[0])
         body()
     torch.cuda.synchronize()
-    for e in ev_a + ev_b:  # create the CUDA events now, outside the capture
-        e.record(stream)
+    for a, b in ev.values():  # create the CUDA events now, outside the capture
+        for e in a + b:
+            e.record(stream)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     profiling[0] = True
@@ -337,9 +368,11 @@ def run_ours(args, wl, rank, world, device):
     # a second copy of the step on its own input and output buffers, for the
     # double-buffered end-to-end loop
     x_in2, out2 = torch.empty_like(x_in), torch.empty_like(out)
-    graph2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph2, stream=stream):
-        body(x_in2, out2)
+    graph2 = None
+    if e2e_on:
+        graph2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph2, stream=stream):
+            body(x_in2, out2)
 
     def step(i):
         if T == 1:
@@ -347,7 +380,7 @@ def run_ours(args, wl, rank, world, device):
         graph.replay()
 
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
+        for i in range(warmup):
             step(i)
     torch.cuda.synchronize()
     if world > 1:
@@ -358,7 +391,7 @@ def run_ours(args, wl, rank, world, device):
     with ClockSampler(gpu_id(device)) as clk:
         with torch.cuda.stream(stream):
             t0.record(stream)
-            for i in range(args.steps):
+            for i in range(steps):
                 step(i)
             t1.record(stream)
         torch.cuda.synchronize()
@@ -366,58 +399,74 @@ def run_ours(args, wl, rank, world, device):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    dom_err = None
+    kern_ms, dom_err = {}, None
     try:
-        dom_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / n_dom
+        for kn, (a, b) in ev.items():
+            kern_ms[kn] = sum(x.elapsed_time(y) for x, y in zip(a, b)) / len(a)
     except Exception as ex:  # noqa: BLE001 - reported in the JSON line
-        dom_ms, dom_err = None, f"{type(ex).__name__}: {ex}"[:300]
+        kern_ms, dom_err = {}, f"{type(ex).__name__}: {ex}"[:300]
     if world > 1:
         ms = max_over_ranks(ms, device)
 
     # bytes / flops of the workload
-    h_out = out.cpu()
     st = moe.moe_device_status(plan, ws)
     touched = E + 1
-    if T > 1 and L == 1:
-        v = moe.moe_route_view(plan, ws, T)
+    if T > 1:
+        v = moe.moe_route_view(plan, ws, min(T, chunk))
         counts = moe.workspace_tensor(ws, v.counts_d, E, torch.int32).cpu().numpy()
-        touched = int((counts > 0).sum()) + 1
-    tok_per_step = T
-    flops_tok = 9 * 3 * 2 * H * I_DIM + 2 * H * E
+        touched = int((counts > 0).sum()) + 1  # of the last chunk the step routed
     result = {}
+    pk = peaks()
     if T == 1:
         bytes_tok = L * (ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2)
-        gbs = bytes_tok * args.steps / (ms * 1e-3) / 1e9 * world
+        gbs = bytes_tok * steps / (ms * 1e-3) / 1e9 * world
         result.update(value=gbs, unit="GB/s", higher_is_better=True)
-        dom_bytes = layers_per_launch * (ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2)
-        dom_bound, dom_units = "hbm", dom_bytes
+        dk = kerns[0]
+        if dk in kern_ms:
+            dom_bytes = layers_per_launch * (ROUTER_BYTES + 9 * EXPERT_BYTES + 3 * H * 2)
+            achieved = dom_bytes / (kern_ms[dk] * 1e-3) / 1e9
+            roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": TRAFFIC.get(name),
+                        "kernel": (f"decode kernel, {layers_per_launch} layers per launch (RMSNorm+router+top-k+9 "
+                                   "experts+combine each)"),
+                        "kernel_ms": round(kern_ms[dk], 5), "peak_src": pk["src"]}
+        else:
+            roofline = {"error": dom_err}
     else:
-        tps = tok_per_step * args.steps / (ms * 1e-3) * world
+        tps = T * steps / (ms * 1e-3) * world
         result.update(value=tps, unit="tokens/s", higher_is_better=True)
         rows = (K_TOP + 1) * chunk
-        dom_flops = 2 * 2 * rows * H * I_DIM
-        dom_bytes = touched * GATEUP_BYTES + chunk * H * 2
-        pk = peaks()
-        t_flops = dom_flops / (pk["bf16_tflops"] * 1e12)
-        t_bytes = dom_bytes / (pk["hbm_gbs"] * 1e9)
-        dom_bound, dom_units = ("tensor", dom_flops) if t_flops > t_bytes else ("hbm", dom_bytes)
-    pk = peaks()
-    if dom_ms:
-        if dom_bound == "hbm":
-            achieved = dom_units / (dom_ms * 1e-3) / 1e9
-            peak = pk["hbm_gbs"]
-            unit = "GB/s"
+        f_gu, f_dn = gemm_flops(rows)
+        b_gu = touched * GATEUP_BYTES + chunk * H * 2
+        b_dn = touched * (EXPERT_BYTES - GATEUP_BYTES)
+        if moe.MOE_KERNEL_GATEUP in kern_ms and moe.MOE_KERNEL_DOWN in kern_ms:
+            t_gu, t_dn = kern_ms[moe.MOE_KERNEL_GATEUP] * 1e-3, kern_ms[moe.MOE_KERNEL_DOWN] * 1e-3
+            tflops = pk["bf16_tflops_sustained"] if L > 1 else pk["bf16_tflops"]
+            # R_gemm: the two grouped GEMMs against the slower of their FLOPs at
+            # the bf16 peak and their packed bytes at the HBM bandwidth
+            t_flops = (f_gu + f_dn) / (tflops * 1e12)
+            t_bytes = (b_gu + b_dn) / (pk["hbm_gbs"] * 1e9)
+            if t_flops >= t_bytes:
+                achieved, peak, unit, bound = (f_gu + f_dn) / (t_gu + t_dn) / 1e12, tflops, "TFLOP/s", "tensor"
+            else:
+                achieved, peak, unit, bound = (b_gu + b_dn) / (t_gu + t_dn) / 1e9, pk["hbm_gbs"], "GB/s", "hbm"
+            roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                        "frac": round(achieved / peak, 4), "traffic": TRAFFIC.get(name),
+                        "kernel": "grouped gate/up + SwiGLU and grouped down (tcgen05), per chunk-layer",
+                        "kernel_ms": round((t_gu + t_dn) * 1e3, 5),
+                        "gateup_ms": round(t_gu * 1e3, 5), "down_ms": round(t_dn * 1e3, 5),
+                        "gateup_frac": round(max(f_gu / (tflops * 1e12), b_gu / (pk["hbm_gbs"] * 1e9)) / t_gu, 4),
+                        "down_frac": round(max(f_dn / (tflops * 1e12), b_dn / (pk["hbm_gbs"] * 1e9)) / t_dn, 4),
+                        "peak_src": pk["src"],
+                        "peak_kind": "sustained (kernel timed inside a long step)" if L > 1 else "burst"}
         else:
-            achieved = dom_units / (dom_ms * 1e-3) / 1e12
-            peak = pk["bf16_tflops_sustained"] if L > 1 else pk["bf16_tflops"]
-            unit = "TFLOP/s"
-        roofline = {"bound": dom_bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                    "frac": round(achieved / peak, 4), "traffic": TRAFFIC.get(args.workload),
-                    "kernel": (f"decode kernel, {layers_per_launch} layers per launch (RMSNorm+router+top-k+9 experts"
-                               "+combine each)") if T == 1 else "grouped gate/up",
-                    "kernel_ms": round(dom_ms, 5), "peak_src": pk["src"]}
-    else:
-        roofline = {"error": dom_err}
+            roofline = {"error": dom_err}
+
+    result.update(ms_per_step=ms / steps, roofline=roofline, clocks=clk.summary(),
+                  gpu_launches=per_step_launches * steps, device_status=st,
+                  touched_experts=touched if T > 1 else None)
+    if not e2e_on:
+        return result
 
     # end to end: every step copies its input from pinned host memory to the
     # device, runs, and copies its output back to pinned host memory.  Two
@@ -432,7 +481,7 @@ def run_ours(args, wl, rank, world, device):
     in_ready = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
     out_read = [torch.cuda.Event() for _ in range(2)]
-    e2e_steps = min(args.steps, 200 if T == 1 else max(3, args.steps))
+    e2e_steps = min(steps, 200 if T == 1 else max(3, steps))
     torch.cuda.synchronize()
     t_e = time.perf_counter()
     for i in range(e2e_steps):
@@ -457,16 +506,37 @@ def run_ours(args, wl, rank, world, device):
     if T == 1:
         e2e_val = bytes_tok * e2e_steps / e2e_s / 1e9 * world
     else:
-        e2e_val = tok_per_step * e2e_steps / e2e_s * world
-    e2e = {"value": e2e_val, "unit": result["unit"], "h2d_bytes_per_step": in_rows * H * 2,
-           "d2h_bytes_per_step": T * H * 2}
-
-    result.update(ms_per_step=ms / args.steps, roofline=roofline, e2e=e2e, clocks=clk.summary(),
-                  gpu_launches=per_step_launches * args.steps, device_status=st,
-                  touched_experts=touched if T > 1 else None,
-                  dtype="int4-g64 weights, bf16 activations, fp32 accumulate")
-    del h_out
+        e2e_val = T * e2e_steps / e2e_s * world
+    result["e2e"] = {"value": e2e_val, "unit": result["unit"], "h2d_bytes_per_step": in_rows * H * 2,
+                     "d2h_bytes_per_step": T * H * 2}
+    result["dtype"] = "int4-g64 weights, bf16 activations, fp32 accumulate"
     return result
+
+
+def run_default_extras(args, rank, world, device, cache):
+    """The other halves of the metric, measured in the same process after the
+    headline prefill line: the 32K prompt with the literal weight generator,
+    T=1 decode through 40 layers, and one layer at T=4096 and T=2048."""
+    out = {}
+    for name, gen, steps, warmup in (("prefill32k_literal", False, 3, 3), ("decode40", None, 2000, 50),
+                                     ("layer4096", None, 50, 5), ("layer2048", None, 100, 5)):
+        wl = dict(WORKLOADS[name.split("_")[0]])
+        if gen is not None:
+            wl["centred"] = gen
+        res = run_ours(args, wl, rank, world, device, cache=cache, steps=steps, warmup=warmup, e2e_on=False,
+                       name=name)
+        keep = {k: res[k] for k in ("value", "unit", "ms_per_step", "roofline", "clocks", "touched_experts",
+                                    "device_status") if k in res}
+        keep["workload"] = (wl["desc"] + (" [literal weight generator]" if gen is False else ""))
+        keep["steps"], keep["warmup"] = steps, warmup
+        out[name] = keep
+        torch_sync()
+    return out
+
+
+def torch_sync():
+    import torch
+    torch.cuda.synchronize()
 
 
 def run_gdn(args, wl, rank, world, device):
@@ -744,7 +814,9 @@ def oracle_sample(wl, seed, target_s=None):
         n_tok = min(T, max(2 * n_tok, int(n_tok * target_s / max(dt, 1e-3))))
     # tokens/s of the workload: one layer of the sample, scaled to all layers
     units = n_tok / wl["layers"]
-    return dt, units, "tokens/s", f"{n_tok} tokens through 1 of {wl['layers']} layer(s), scaled to the full stack"
+    desc = f"{n_tok} tokens through one layer" if wl["layers"] == 1 else \
+        f"{n_tok} tokens through 1 of {wl['layers']} layers, extrapolated to the {wl['layers']}-layer stack"
+    return dt, units, "tokens/s", desc
 
 
 def cpu_baseline(wl, seed):
@@ -790,13 +862,21 @@ def main():
     if args.layers is not None:
         wl["layers"] = args.layers
         wl["desc"] += f" [profiling override: {args.layers} layers]"
+    if args.generator is not None:
+        wl["centred"] = args.generator == "centred"
+        wl["desc"] += f" [{args.generator} weight generator]"
+    if args.tile_rows != 128:
+        wl["desc"] += f" [{args.tile_rows}-row tiles]"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     base = {"metric": GDN_METRIC if "Hv" in wl else ATTN_METRIC if "Hkv" in wl else METRIC, "n_gpus": args.gpus if world == 1 else world, "steps": args.steps,
             "warmup": args.warmup, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
             "config": {"workload": f"{args.workload}: {wl['desc']}", "tokens_per_step": wl["T"],
-                       "layers": wl["layers"], "chunk": wl["chunk"], "parallelism": "replicas" if world > 1 else "1 GPU",
+                       "layers": wl["layers"], "chunk": wl["chunk"], "tile_rows": args.tile_rows,
+                       "generator": ("centred" if wl.get("centred") else "literal") if "Hv" not in wl and "Hkv" not in wl
+                       else None,
+                       "parallelism": "replicas" if world > 1 else "1 GPU",
                        "l2": (f"{GDN_SETS} distinct input sets cycled (~50 MB each, larger than L2 together)"
                               if "Hv" in wl else f"{wl.get('sets')} distinct KV caches cycled" if "Hkv" in wl
                               else "inputs larger than L2 (packed weights >= 455 MB per layer)"),
@@ -813,11 +893,27 @@ def main():
     if world > 1:
         torch.cuda.set_device(device)
         torch.distributed.init_process_group("nccl")
-    res = (run_gdn if "Hv" in wl else run_attn if "Hkv" in wl else run_ours)(args, wl, rank, world, device)
+    if "Hv" in wl or "Hkv" in wl:
+        res = (run_gdn if "Hv" in wl else run_attn)(args, wl, rank, world, device)
+        extras = None
+    else:
+        import __graft_entry__
+        if rank == 0:
+            __graft_entry__.build()
+        if world > 1:
+            torch.distributed.barrier()
+        cache = WeightCache(device)
+        res = run_ours(args, wl, rank, world, device, cache=cache)
+        extras = None
+        if args.workload == "prefill32k" and not args.no_extras and args.layers is None and args.generator is None:
+            extras = run_default_extras(args, rank, world, device, cache)
+        del cache
     if rank == 0:
         extra = res.pop("config_extra", {})
         line = {**base, **res}
         line["config"] = {**line["config"], **extra}
+        if extras:
+            line["extras"] = extras
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(wl, args.seed)
         print(json.dumps(line))

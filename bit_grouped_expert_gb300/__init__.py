@@ -33,12 +33,15 @@ MOE_FLAG_SIMT_EXPERTS = 0x4
 MOE_FLAG_TILE_ROWS_64 = 0x8
 MOE_FLAG_PRENORM = 0x10
 MOE_FLAG_TRACE = 0x20
+MOE_FLAG_TEST_WITHHOLD = 0x40
 MOE_TRACE_CTAS = 256
 MOE_TRACE_SLOTS = 32
 
 EXPORTS = ("moe_plan", "moe_plan_destroy", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
-           "moe_route_from_logits", "moe_forward", "moe_route_view", "moe_rmsnorm", "moe_dequant",
-           "moe_device_status", "moe_last_launch_count", "moe_status_str", "moe_profile_events", "moe_last_cuda_error",
+           "moe_route_from_logits", "moe_route_from_ids", "moe_forward", "moe_prefill_stack", "moe_router_split_bytes",
+           "moe_router_split", "moe_route_view", "moe_rmsnorm", "moe_dequant",
+           "moe_device_status", "moe_last_launch_count", "moe_status_str", "moe_profile_events", "moe_profile_stride",
+           "moe_last_cuda_error",
            "moe_decode_static", "moe_decode_stack", "gdn_scan", "attn_decode_workspace_bytes", "attn_decode")
 
 MOE_DECODE_STATIC_SCRATCH_BYTES = 65536
@@ -71,7 +74,8 @@ class moe_config(ctypes.Structure):
 
 class moe_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("router_d", "gate_q_d", "up_q_d", "gate_s_d", "gate_b_d", "up_s_d",
-                                               "up_b_d", "down_q_d", "down_s_d", "down_b_d", "shared_gate_d")]
+                                               "up_b_d", "down_q_d", "down_s_d", "down_b_d", "shared_gate_d",
+                                               "router_split_d")]
 
 
 class moe_route_ptrs(ctypes.Structure):
@@ -105,8 +109,17 @@ def lib():
         L.moe_route.argtypes = [vp, vp, i32, vp, vp, vp, sz, vp]
         L.moe_route_from_logits.restype = i32
         L.moe_route_from_logits.argtypes = [vp, vp, i32, vp, sz, vp]
+        L.moe_route_from_ids.restype = i32
+        L.moe_route_from_ids.argtypes = [vp, vp, vp, i32, vp, sz, vp]
         L.moe_forward.restype = i32
         L.moe_forward.argtypes = [vp, vp, vp, i32, ctypes.POINTER(moe_weights), vp, vp, vp, sz, vp]
+        L.moe_prefill_stack.restype = i32
+        L.moe_prefill_stack.argtypes = [vp, vp, i32, i32, ctypes.POINTER(moe_weights), ctypes.POINTER(vp), vp, sz,
+                                        vp]
+        L.moe_router_split_bytes.restype = sz
+        L.moe_router_split_bytes.argtypes = [i32, i32]
+        L.moe_router_split.restype = i32
+        L.moe_router_split.argtypes = [vp, i32, i32, vp, sz, vp]
         L.moe_route_view.restype = i32
         L.moe_route_view.argtypes = [vp, vp, i32, ctypes.POINTER(moe_route_ptrs)]
         L.moe_rmsnorm.restype = i32
@@ -119,6 +132,8 @@ def lib():
         L.moe_last_launch_count.argtypes = []
         L.moe_profile_events.restype = i32
         L.moe_profile_events.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32]
+        L.moe_profile_stride.restype = i32
+        L.moe_profile_stride.argtypes = [i32, i32]
         L.moe_last_cuda_error.restype = ctypes.c_char_p
         L.moe_last_cuda_error.argtypes = []
         L.moe_status_str.restype = ctypes.c_char_p
@@ -204,7 +219,8 @@ def moe_workspace_init(plan: Plan, ws, stream=None):
 
 def make_weights(w: dict) -> moe_weights:
     """moe_weights from a dict of device tensors (keys: router, gate_q, ...;
-    shared_gate optional).  The caller keeps the tensors alive."""
+    shared_gate and router_split optional).  The caller keeps the tensors
+    alive."""
     return moe_weights(*[_ptr(w.get(n[:-2])) for n, _ in moe_weights._fields_])
 
 
@@ -218,6 +234,44 @@ def moe_route_from_logits(plan: Plan, keys, T: int, ws, stream=None):
                                                                 _nbytes(ws), _stream(stream)))
 
 
+def moe_route_from_ids(plan: Plan, ids, w, T: int, ws, stream=None):
+    _check("moe_route_from_ids", lib().moe_route_from_ids(plan.handle, _ptr(ids), _ptr(w), int(T), _ptr(ws),
+                                                          _nbytes(ws), _stream(stream)))
+
+
+def moe_router_split_bytes(E: int, H: int) -> int:
+    return int(lib().moe_router_split_bytes(int(E), int(H)))
+
+
+def moe_router_split(router, E: int, H: int, split, stream=None):
+    """The router's three bf16 parts into ``split`` (a device tensor of
+    moe_router_split_bytes(E, H) bytes), for the ``router_split`` weight."""
+    _check("moe_router_split", lib().moe_router_split(_ptr(router), int(E), int(H), _ptr(split), _nbytes(split),
+                                                      _stream(stream)))
+
+
+def _weights_array(weights):
+    n = len(weights)
+    return (moe_weights * max(n, 1))(*[w if isinstance(w, moe_weights) else make_weights(w) for w in weights])
+
+
+def _bias_array(logit_bias, n):
+    if logit_bias is None:
+        return None
+    if len(logit_bias) != n:
+        raise ValueError("one logit bias (or None) per layer")
+    return (ctypes.c_void_p * max(n, 1))(*[_ptr(b) for b in logit_bias])
+
+
+def moe_prefill_stack(plan: Plan, r, T: int, weights, logit_bias=None, ws=None, stream=None):
+    """T tokens of the residual stream ``r`` through len(weights) pre-norm
+    layers in chunks of the plan's max_tokens (chunk-major), in place."""
+    n = len(weights)
+    _check("moe_prefill_stack", lib().moe_prefill_stack(plan.handle, _ptr(r), int(T), n, _weights_array(weights),
+                                                        _bias_array(logit_bias, n), _ptr(ws), _nbytes(ws),
+                                                        _stream(stream)))
+
+
 def moe_forward(plan: Plan, x, residual, T: int, weights, logit_bias, out, ws, stream=None):
     cw = weights if isinstance(weights, moe_weights) else make_weights(weights)
     _check("moe_forward", lib().moe_forward(plan.handle, _ptr(x), _ptr(residual), int(T), ctypes.byref(cw),
@@ -229,13 +283,8 @@ def moe_decode_stack(plan: Plan, r, weights, logit_bias=None, ws=None, stream=No
     place.  ``weights``: list of weight dicts (or moe_weights); ``logit_bias``:
     None or a list of per-layer bias tensors (entries may be None)."""
     n = len(weights)
-    arr = (moe_weights * max(n, 1))(*[w if isinstance(w, moe_weights) else make_weights(w) for w in weights])
-    bias = None
-    if logit_bias is not None:
-        if len(logit_bias) != n:
-            raise ValueError("one logit bias (or None) per layer")
-        bias = (ctypes.c_void_p * max(n, 1))(*[_ptr(b) for b in logit_bias])
-    _check("moe_decode_stack", lib().moe_decode_stack(plan.handle, _ptr(r), n, arr, bias, _ptr(ws), _nbytes(ws),
+    _check("moe_decode_stack", lib().moe_decode_stack(plan.handle, _ptr(r), n, _weights_array(weights),
+                                                      _bias_array(logit_bias, n), _ptr(ws), _nbytes(ws),
                                                       _stream(stream)))
 
 
@@ -325,3 +374,8 @@ def moe_profile_events(kernel: int, start_events=(), stop_events=()):
     a = arr(*[e.cuda_event for e in start_events]) if n else None
     b = arr(*[e.cuda_event for e in stop_events]) if n else None
     _check("moe_profile_events", lib().moe_profile_events(int(kernel), a, b, n))
+
+
+def moe_profile_stride(kernel: int, stride: int):
+    """Bracket only every ``stride``-th launch of ``kernel`` from now on."""
+    _check("moe_profile_stride", lib().moe_profile_stride(int(kernel), int(stride)))

@@ -1,7 +1,7 @@
-// T == 1 decode path ("Decode" section of the Lily pages: at batch 1 there is
-// almost no weight reuse, so bandwidth sets the ceiling; only the bytes of the
-// selected experts are streamed, and the step's kernels overlap instead of
-// running as hundreds of sequential launches).
+// T == 1 decode path ("Decode" section of the Lily pages: a single token uses
+// each weight it reads once, so HBM bandwidth bounds the step; only the
+// selected experts' bytes are read, and the work of a step is overlapped
+// rather than issued as a long chain of small launches).
 //
 // One cooperative launch runs up to MAXL layers; for each layer every CTA
 // (one per SM) runs
@@ -55,7 +55,6 @@ constexpr int MAX_RU = 8;  // routed gate/up units (mbarriers) per CTA
 constexpr int MAXL = 7;    // layers per launch (the parameters stay under 4 KB)
 constexpr int DN_ITEMS = 4;  // down items (output unit, slot, K-chunk) per warp at most
 constexpr int XREG = 4;    // uint2 of r a thread holds in the RMSNorm: H <= 4 * XREG * DTHREADS
-constexpr unsigned long long DTIMEOUT_NS = 1000000000ull;
 
 struct DecMaps {
   CUtensorMap gate, up, down;  // packed codes, [rows][K/2] bytes, 128B-swizzled 8-row boxes
@@ -84,6 +83,8 @@ struct DecArgs {
   unsigned long long *epoch;  // epochs used so far (low 32 bits)
   int32_t *status;
   uint64_t *trace;  // [MOE_TRACE_CTAS][MOE_TRACE_SLOTS] phase timestamps or null
+  unsigned long long timeout_ns;  // limit of every bounded wait
+  int withhold;                   // test aid: expert 0's router key is never published
   int H, E, k, I, S, prenorm;
   float eps;
   int map3d;  // 1: one TMA op per matrix (3-D map over the K-chunks), 0: one per K-chunk
@@ -133,7 +134,7 @@ __device__ __forceinline__ bool has_tag(unsigned long long w, uint32_t ep) { ret
 // false, with the status set, when the wait times out.
 template <int N>
 __device__ bool poll_tagged(const unsigned long long *src, const int (&idx)[N], unsigned long long (&w)[N],
-                            uint32_t ep, int32_t *status) {
+                            uint32_t ep, int32_t *status, unsigned long long timeout_ns) {
   bool done = true;
 #pragma unroll
   for (int i = 0; i < N; ++i) w[i] = idx[i] >= 0 ? ld_relaxed64(src + idx[i]) : tagged(ep, 0u);
@@ -150,7 +151,7 @@ __device__ bool poll_tagged(const unsigned long long *src, const int (&idx)[N], 
         done = done && has_tag(w[i], ep);
       }
     if (done) return true;
-    if (ptx::globaltimer() - t0 > DTIMEOUT_NS) {
+    if (ptx::globaltimer() - t0 > timeout_ns) {
       set_status(status, MOE_ERR_DEVICE_TIMEOUT);
       return false;
     }
@@ -158,11 +159,11 @@ __device__ bool poll_tagged(const unsigned long long *src, const int (&idx)[N], 
 }
 
 // Bounded wait for the phase of an mbarrier with the given parity.
-__device__ bool wait_bar(uint64_t *bar, uint32_t parity, int32_t *status) {
+__device__ bool wait_bar(uint64_t *bar, uint32_t parity, int32_t *status, unsigned long long timeout_ns) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait_sleep(bar, parity, 20000)) {
-    if (ptx::globaltimer() - t0 > DTIMEOUT_NS) {
+    if (ptx::globaltimer() - t0 > timeout_ns) {
       set_status(status, MOE_ERR_DEVICE_TIMEOUT);
       return false;
     }
@@ -283,7 +284,9 @@ __device__ bool gu_compute(const DecArgs &a, const uint8_t *codes, const uint8_t
   for (int kc = kg; kc < nkc; kc += WK) {
     for (int rs = rg; rs < 2 * nu; rs += WR) {
       const int u = rs >> 1, mat = rs & 1;  // gate (0) or up (1) rows of unit u
-      if (bars && !(wait_bar(&bars[0], parity, a.status) && wait_bar(&bars[u], parity, a.status))) return false;
+      if (bars && !(wait_bar(&bars[0], parity, a.status, a.timeout_ns) &&
+                    wait_bar(&bars[u], parity, a.status, a.timeout_ns)))
+        return false;
       const uint16_t *sc = reinterpret_cast<const uint16_t *>(scales + (size_t)(2 * mat * ustride + u) * (H / 4));
       const uint16_t *bi = reinterpret_cast<const uint16_t *>(scales + (size_t)((2 * mat + 1) * ustride + u) * (H / 4));
       const float d = gemv_chunk(codes + (size_t)u * 8 * H + mat * 4 * H + kc * 1024, sc[g * gpr + 4 * kc + q],
@@ -616,7 +619,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
           idx[2 * j] = i < H / 4 ? 2 * i : -1;
           idx[2 * j + 1] = i < H / 4 ? 2 * i + 1 : -1;
         }
-        got = poll_tagged(a.tr + (size_t)pb * (H / 2), idx, w, ep, a.status);
+        got = poll_tagged(a.tr + (size_t)pb * (H / 2), idx, w, ep, a.status, a.timeout_ns);
 #pragma unroll
         for (int j = 0; j < XREG; ++j) rv[j] = make_uint2((uint32_t)w[2 * j], (uint32_t)w[2 * j + 1]);
       }
@@ -667,7 +670,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     trace(3, l);
 
     // -------------------------------------------------------------- P1: router rows, shared gate/up
-    ok = wait_bar(bar_p1, ph, a.status);
+    ok = wait_bar(bar_p1, ph, a.status, a.timeout_ns);
     trace(4, l);
     if (ok)
       for (int i = warp; i < nre_of(l); i += DWARPS) {  // one warp per router row, fp32 FMA
@@ -686,7 +689,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
         if (lane == 0) {
           const float key = (L.bias && e < E) ? acc + L.bias[e] : acc;
           if (e < E) a.keys[e] = key;
-          st_relaxed64(tk + e, tagged(ep, __float_as_uint(key)));
+          if (!(a.withhold && e == 0)) st_relaxed64(tk + e, tagged(ep, __float_as_uint(key)));
         }
       }
     trace(5, l);
@@ -715,7 +718,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
     {
       const int idx[2] = {tid < E ? tid : -1, tid + DTHREADS < E ? tid + DTHREADS : -1};
       unsigned long long w[2];
-      got = poll_tagged(tk, idx, w, ep, a.status);
+      got = poll_tagged(tk, idx, w, ep, a.status, a.timeout_ns);
       if (tid < E) keys[tid] = __uint_as_float((uint32_t)w[0]);
       if (tid + DTHREADS < E) keys[tid + DTHREADS] = __uint_as_float((uint32_t)w[1]);
     }
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
           const int v = u + DTHREADS < n8 ? 4 * (u + DTHREADS) : -4;
           const int idx[8] = {4 * u, 4 * u + 1, 4 * u + 2, 4 * u + 3, v, v + 1, v + 2, v + 3};
           unsigned long long w[8];
-          gotw = poll_tagged(thb, idx, w, ep, a.status);
+          gotw = poll_tagged(thb, idx, w, ep, a.status, a.timeout_ns);
           if (!gotw) break;
           *reinterpret_cast<uint4 *>(hs + (u >> 3) * XPAD + (u & 7) * 8) =
               perm8((uint32_t)w[0], (uint32_t)w[1], (uint32_t)w[2], (uint32_t)w[3]);
@@ -831,10 +834,10 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       if (GATE && S && L.w.shared_gate && tid == 0) {  // x . gate, published with the keys
         const int gi[1] = {E};
         unsigned long long gw[1];
-        gotw = gotw && poll_tagged(tk, gi, gw, ep, a.status);
+        gotw = gotw && poll_tagged(tk, gi, gw, ep, a.status, a.timeout_ns);
         s_gz = __uint_as_float((uint32_t)gw[0]);
       }
-      gotw = gotw && wait_bar(bar_drt, ph, a.status) && wait_bar(bar_dsh, ph, a.status);
+      gotw = gotw && wait_bar(bar_drt, ph, a.status, a.timeout_ns) && wait_bar(bar_dsh, ph, a.status, a.timeout_ns);
       gotw = __syncthreads_and(gotw) != 0;  // h is in shared memory
       trace(12, l);
 #pragma unroll
@@ -894,12 +897,15 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
   if (cta == 0 && tid == 0) st_relaxed64(a.epoch, (unsigned long long)(uint32_t)(ep0 + (uint32_t)a.nl));
   // never leave with copies in flight into this CTA's shared memory
   // (a phase that has completed passes at once)
+  // (the copies complete by themselves: these waits take the full second
+  // whatever limit the layer's waits had)
   if (tid == 0 && !ok) {
-    wait_bar(bar_p1, (n_p1 - 1) & 1u, a.status);
-    wait_bar(bar_dsh, (n_dsh - 1) & 1u, a.status);
+    constexpr unsigned long long DRAIN_NS = 1000000000ull;
+    wait_bar(bar_p1, (n_p1 - 1) & 1u, a.status, DRAIN_NS);
+    wait_bar(bar_dsh, (n_dsh - 1) & 1u, a.status, DRAIN_NS);
     if (n_drt > 0) {
-      wait_bar(bar_drt, (n_drt - 1) & 1u, a.status);
-      for (int i = 0; i < nru; ++i) wait_bar(&bar_ru[i], (n_drt - 1) & 1u, a.status);
+      wait_bar(bar_drt, (n_drt - 1) & 1u, a.status, DRAIN_NS);
+      for (int i = 0; i < nru; ++i) wait_bar(&bar_ru[i], (n_drt - 1) & 1u, a.status, DRAIN_NS);
     }
   }
   trace_at(a, MOE_TRACE_SLOTS - 1);
@@ -1068,6 +1074,8 @@ cudaError_t launch_layers(const uint16_t *x, const uint16_t *res, uint16_t *out,
   a.epoch = sc.epoch;
   a.status = sc.status;
   a.trace = trace ? sc.trace : nullptr;
+  a.timeout_ns = sc.timeout_ns;
+  a.withhold = sc.withhold;
   a.prenorm = prenorm;
   a.eps = eps;
   a.map3d = 1;

@@ -26,8 +26,14 @@ struct ExpertPtrs {
 // route.cu
 cudaError_t launch_router_logits(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
                                  float *keys, cudaStream_t s);
-cudaError_t launch_topk(const float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
-                        int32_t *status, cudaStream_t s);
+// part: null (keys given) or the router's KS K-slice partial sums [KS][T][E],
+// summed in slice order (+ bias) into keys before the selection.
+cudaError_t launch_topk(float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
+                        int32_t *status, const float *part, int KS, const float *bias, cudaStream_t s);
+// counts[e] += 1 for every given id (ids [T][k]); out-of-range ids (and, with
+// debug, an expert repeated within a token) set MOE_ERR_DEVICE_BOUNDS.
+cudaError_t launch_ids_histogram(const int32_t *ids, int T, int E, int k, int32_t *counts, int32_t *status, int debug,
+                                 cudaStream_t s);
 cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, int S, const int32_t *counts,
                            int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *blockmap, int32_t *n_tiles,
                            int max_tiles, int BN2, int32_t *blockmap2, int32_t *n_tiles2, int max_tiles2,
@@ -63,6 +69,8 @@ struct DecodeScratch {
   unsigned long long *tags;
   int32_t *status;
   uint64_t *trace;
+  unsigned long long timeout_ns = 1000000000ull;  // limit of every bounded wait
+  int withhold = 0;  // test aid (MOE_FLAG_TEST_WITHHOLD): expert 0's key is never published
 };
 size_t decode_tag_words(int H, int E, int k, int I, int S);
 bool decode_supported(int H, int E, int k, int I, int S, int num_sms);

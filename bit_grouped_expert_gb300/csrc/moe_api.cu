@@ -16,15 +16,18 @@ namespace {
 thread_local int32_t g_last_launches = 0;
 thread_local cudaError_t g_last_cuda = cudaSuccess;
 
+// Profiling hook state, per kernel id (moe_profile_events), per thread.
+constexpr int kProfKernels = 16;
 struct ProfState {
-  int kernel = 0;
   int n = 0;
+  int stride = 1;                   // bracket every stride-th launch
+  unsigned long long seen = 0;      // launches of the kernel since the hook was set
   unsigned long long next = 0;
   cudaEvent_t start[4096];
   cudaEvent_t stop[4096];
   bool open = false;
 };
-thread_local ProfState *g_prof = nullptr;
+thread_local ProfState *g_prof[kProfKernels] = {};
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -78,6 +81,10 @@ moe::DecodeScratch decode_scratch(const moe_plan_t *plan, void *ws_d) {
   sc.tags = moe::ws_ptr<unsigned long long>(ws_d, L.dtags);
   sc.status = moe::ws_ptr<int32_t>(ws_d, L.status);
   sc.trace = (plan->flags & MOE_FLAG_TRACE) ? moe::ws_ptr<uint64_t>(ws_d, L.trace) : nullptr;
+  if (plan->flags & MOE_FLAG_TEST_WITHHOLD) {  // one key is never published; waits give up after 1 ms
+    sc.timeout_ns = 1000000ull;
+    sc.withhold = 1;
+  }
   return sc;
 }
 
@@ -85,7 +92,8 @@ bool weights_aligned(const moe_weights *w) {
   using moe::aligned16;
   return aligned16(w->router_d) && aligned16(w->gate_q_d) && aligned16(w->up_q_d) && aligned16(w->gate_s_d) &&
          aligned16(w->gate_b_d) && aligned16(w->up_s_d) && aligned16(w->up_b_d) && aligned16(w->down_q_d) &&
-         aligned16(w->down_s_d) && aligned16(w->down_b_d) && aligned16(w->shared_gate_d);
+         aligned16(w->down_s_d) && aligned16(w->down_b_d) && aligned16(w->shared_gate_d) &&
+         aligned16(w->router_split_d);
 }
 
 bool weights_present(const moe_weights *w) {
@@ -112,9 +120,14 @@ moe_status cuda_status(cudaError_t e) {
   return MOE_ERR_CUDA;
 }
 
-// Routing kernels for T tokens; keys already in ws when from_keys.
-moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const float *router, const float *bias,
-                         void *ws, bool from_keys, cudaStream_t s, int *launches) {
+// How enqueue_route gets its selection: router keys from x, given keys
+// already in the workspace, or given ids and weights already in the
+// workspace's top-k buffers.
+enum class RouteFrom { kX, kKeys, kIds };
+
+// Routing kernels for T tokens.  split: the router's bf16 parts or null.
+moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const float *router, const uint16_t *split,
+                         const float *bias, void *ws, RouteFrom from, cudaStream_t s, int *launches) {
   const moe_config &c = p->cfg;
   const moe::Layout &L = p->lay;
   float *keys = moe::ws_ptr<float>(ws, L.keys);
@@ -122,21 +135,29 @@ moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const fl
   int32_t *counts = moe::ws_ptr<int32_t>(ws, L.counts);
   cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts, s);
   if (err != cudaSuccess) return cuda_status(err);
-  if (!from_keys) {
+  const float *part = nullptr;  // the tensor-core router's K-slice partial sums, when it splits K
+  int ks = 0;
+  if (from == RouteFrom::kX) {
     if (p->use_router_tc && T >= moe::ROUTER_TC_MIN_T) {
-      err = moe::launch_router_tc(x, T, c.hidden, router, c.n_experts, bias, moe::ws_ptr<uint16_t>(ws, L.rsplit),
-                                  moe::ws_ptr<float>(ws, L.rpart), keys, status, p->num_sms, s);
+      err = moe::launch_router_tc(x, T, c.hidden, router, c.n_experts, bias, split,
+                                  moe::ws_ptr<uint16_t>(ws, L.rsplit), moe::ws_ptr<float>(ws, L.rpart), keys, status,
+                                  p->num_sms, &ks, launches, s);
       if (err != cudaSuccess) return cuda_status(err);
-      *launches += moe::router_tc_slices(T, c.n_experts, c.hidden, p->num_sms) > 1 ? 3 : 2;
+      if (ks > 1) part = moe::ws_ptr<float>(ws, L.rpart);
     } else {
       if ((err = moe::launch_router_logits(x, T, c.hidden, router, c.n_experts, bias, keys, s)) != cudaSuccess)
         return cuda_status(err);
       ++*launches;
     }
   }
-  if ((err = moe::launch_topk(keys, T, c.n_experts, c.top_k, moe::ws_ptr<int32_t>(ws, L.topk_id),
-                              moe::ws_ptr<float>(ws, L.topk_w), counts, status, s)) != cudaSuccess)
-    return cuda_status(err);
+  if (from == RouteFrom::kIds) {
+    err = moe::launch_ids_histogram(moe::ws_ptr<int32_t>(ws, L.topk_id), T, c.n_experts, c.top_k, counts, status,
+                                    (p->flags & MOE_FLAG_DEBUG_CHECKS) ? 1 : 0, s);
+  } else {
+    err = moe::launch_topk(keys, T, c.n_experts, c.top_k, moe::ws_ptr<int32_t>(ws, L.topk_id),
+                           moe::ws_ptr<float>(ws, L.topk_w), counts, status, part, ks, part ? bias : nullptr, s);
+  }
+  if (err != cudaSuccess) return cuda_status(err);
   ++*launches;
   const int max_tiles = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, p->block_rows);
   const int max_tiles2 = p->block_rows2 ? tiles_bound(T, c.top_k, c.n_experts, c.n_shared, p->block_rows2) : 0;
@@ -183,14 +204,15 @@ static void prof_record(cudaEvent_t ev, cudaStream_t s) {
     cudaEventRecord(ev, s);
 }
 void prof_before(int kernel, cudaStream_t s) {
-  ProfState *p = g_prof;
-  if (!p || p->n == 0 || p->kernel != kernel) return;
+  ProfState *p = (kernel > 0 && kernel < kProfKernels) ? g_prof[kernel] : nullptr;
+  if (!p || p->n == 0) return;
+  if (p->seen++ % (unsigned long long)p->stride) return;
   prof_record(p->start[p->next % p->n], s);
   p->open = true;
 }
 void prof_after(int kernel, cudaStream_t s) {
-  ProfState *p = g_prof;
-  if (!p || p->n == 0 || p->kernel != kernel || !p->open) return;
+  ProfState *p = (kernel > 0 && kernel < kProfKernels) ? g_prof[kernel] : nullptr;
+  if (!p || p->n == 0 || !p->open) return;
   prof_record(p->stop[p->next % p->n], s);
   p->open = false;
   ++p->next;
@@ -204,21 +226,32 @@ moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *c
   if (n > 0 && (!start_events || !stop_events)) return MOE_ERR_INVALID_ARGUMENT;
   for (int i = 0; i < n; ++i)
     if (!start_events[i] || !stop_events[i]) return MOE_ERR_INVALID_ARGUMENT;
+  ProfState *&p = g_prof[kernel];
   if (n == 0) {
-    delete g_prof;
-    g_prof = nullptr;
+    delete p;
+    p = nullptr;
     return MOE_OK;
   }
-  if (!g_prof) g_prof = new (std::nothrow) ProfState;
-  if (!g_prof) return MOE_ERR_INVALID_ARGUMENT;
-  g_prof->kernel = kernel;
-  g_prof->n = n;
-  g_prof->next = 0;
-  g_prof->open = false;
+  if (!p) p = new (std::nothrow) ProfState;
+  if (!p) return MOE_ERR_INVALID_ARGUMENT;
+  p->n = n;
+  p->stride = 1;
+  p->seen = 0;
+  p->next = 0;
+  p->open = false;
   for (int i = 0; i < n; ++i) {
-    g_prof->start[i] = static_cast<cudaEvent_t>(start_events[i]);
-    g_prof->stop[i] = static_cast<cudaEvent_t>(stop_events[i]);
+    p->start[i] = static_cast<cudaEvent_t>(start_events[i]);
+    p->stop[i] = static_cast<cudaEvent_t>(stop_events[i]);
   }
+  return MOE_OK;
+}
+
+moe_status moe_profile_stride(int32_t kernel, int32_t stride) {
+  if (kernel < MOE_KERNEL_ROUTER || kernel > MOE_KERNEL_ATTN_DECODE || stride < 1) return MOE_ERR_INVALID_ARGUMENT;
+  ProfState *p = g_prof[kernel];
+  if (!p) return MOE_ERR_INVALID_ARGUMENT;
+  p->stride = stride;
+  p->seen = 0;
   return MOE_OK;
 }
 
@@ -242,7 +275,7 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
   if (!cfg || !out) return MOE_ERR_INVALID_ARGUMENT;
   *out = nullptr;
   const uint32_t known = MOE_FLAG_DEBUG_CHECKS | MOE_FLAG_FORCE_GROUPED | MOE_FLAG_SIMT_EXPERTS |
-                         MOE_FLAG_TILE_ROWS_64 | MOE_FLAG_PRENORM | MOE_FLAG_TRACE;
+                         MOE_FLAG_TILE_ROWS_64 | MOE_FLAG_PRENORM | MOE_FLAG_TRACE | MOE_FLAG_TEST_WITHHOLD;
   if (flags & ~known) return MOE_ERR_INVALID_ARGUMENT;
   if (max_tokens < 1 || max_tokens > 65536) return MOE_ERR_INVALID_ARGUMENT;
   const moe_config &c = *cfg;
@@ -322,8 +355,8 @@ moe_status moe_route(const moe_plan_t *plan, const void *x_d, int32_t T, const f
     return MOE_ERR_MISALIGNED;
   if ((st = device_ready(plan)) != MOE_OK) return st;
   int launches = 0;
-  st = enqueue_route(plan, static_cast<const uint16_t *>(x_d), T, router_d, logit_bias_d, ws_d, false,
-                     static_cast<cudaStream_t>(stream), &launches);
+  st = enqueue_route(plan, static_cast<const uint16_t *>(x_d), T, router_d, nullptr, logit_bias_d, ws_d,
+                     RouteFrom::kX, static_cast<cudaStream_t>(stream), &launches);
   g_last_launches = launches;
   return st;
 }
@@ -344,7 +377,29 @@ moe_status moe_route_from_logits(const moe_plan_t *plan, const float *keys_d, in
     if (err != cudaSuccess) return cuda_status(err);
   }
   int launches = 0;
-  st = enqueue_route(plan, nullptr, T, nullptr, nullptr, ws_d, true, s, &launches);
+  st = enqueue_route(plan, nullptr, T, nullptr, nullptr, nullptr, ws_d, RouteFrom::kKeys, s, &launches);
+  g_last_launches = launches;
+  return st;
+}
+
+moe_status moe_route_from_ids(const moe_plan_t *plan, const int32_t *ids_d, const float *w_d, int32_t T, void *ws_d,
+                              size_t ws_bytes, void *stream) {
+  g_last_launches = 0;
+  moe_status st = check_call(plan, T, ws_d, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!ids_d || !w_d) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(ids_d) || !moe::aligned16(w_d)) return MOE_ERR_MISALIGNED;
+  if ((st = device_ready(plan)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t n = (size_t)T * plan->cfg.top_k;
+  int32_t *ids = moe::ws_ptr<int32_t>(ws_d, plan->lay.topk_id);
+  float *w = moe::ws_ptr<float>(ws_d, plan->lay.topk_w);
+  cudaError_t err = cudaSuccess;
+  if (ids != ids_d) err = cudaMemcpyAsync(ids, ids_d, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+  if (err == cudaSuccess && w != w_d) err = cudaMemcpyAsync(w, w_d, n * sizeof(float), cudaMemcpyDeviceToDevice, s);
+  if (err != cudaSuccess) return cuda_status(err);
+  int launches = 0;
+  st = enqueue_route(plan, nullptr, T, nullptr, nullptr, nullptr, ws_d, RouteFrom::kIds, s, &launches);
   g_last_launches = launches;
   return st;
 }
@@ -388,7 +443,7 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
     ++launches;
     x = xn;
   }
-  st = enqueue_route(plan, x, T, w->router_d, logit_bias_d, ws_d, false, s, &launches);
+  st = enqueue_route(plan, x, T, w->router_d, w->router_split_d, logit_bias_d, ws_d, RouteFrom::kX, s, &launches);
   if (st != MOE_OK) return st;
   const int max_tiles = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, plan->block_rows);
   const int32_t *perm = moe::ws_ptr<int32_t>(ws_d, L.perm);
@@ -448,6 +503,56 @@ moe_status moe_decode_stack(const moe_plan_t *plan, void *r_d, int32_t n_layers,
       router.data(), logit_bias_d, ep.data(), decode_scratch(plan, ws_d), plan->num_sms, &launches,
       static_cast<cudaStream_t>(stream));
   g_last_launches = launches;
+  return cuda_status(err);
+}
+
+moe_status moe_prefill_stack(const moe_plan_t *plan, void *r_d, int32_t T, int32_t n_layers, const moe_weights *w,
+                             const float *const *logit_bias_d, void *ws_d, size_t ws_bytes, void *stream) {
+  g_last_launches = 0;
+  if (!plan || !r_d || !w || n_layers < 1 || T < 1) return MOE_ERR_INVALID_ARGUMENT;
+  if (!(plan->flags & MOE_FLAG_PRENORM)) return MOE_ERR_INVALID_ARGUMENT;
+  moe_status st = check_call(plan, 1, ws_d, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!moe::aligned16(r_d)) return MOE_ERR_MISALIGNED;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!weights_present(&w[l])) return MOE_ERR_INVALID_ARGUMENT;
+    if (!weights_aligned(&w[l]) || (logit_bias_d && !moe::aligned16(logit_bias_d[l]))) return MOE_ERR_MISALIGNED;
+  }
+  if ((st = device_ready(plan)) != MOE_OK) return st;
+  const size_t H = plan->cfg.hidden;
+  const int m = plan->max_tokens;
+  uint16_t *r = static_cast<uint16_t *>(r_d);
+  int launches = 0;
+  for (int c0 = 0; c0 < T; c0 += m) {  // chunk-major: each chunk through every layer
+    const int n = T - c0 < m ? T - c0 : m;
+    uint16_t *rc = r + (size_t)c0 * H;
+    for (int l = 0; l < n_layers; ++l) {
+      st = moe_forward(plan, rc, nullptr, n, &w[l], logit_bias_d ? logit_bias_d[l] : nullptr, rc, ws_d, ws_bytes,
+                       stream);
+      launches += g_last_launches;
+      if (st != MOE_OK) {
+        g_last_launches = launches;
+        return st;
+      }
+    }
+  }
+  g_last_launches = launches;
+  return MOE_OK;
+}
+
+size_t moe_router_split_bytes(int32_t E, int32_t H) {
+  return (E > 0 && H > 0) ? (size_t)3 * (size_t)E * (size_t)H * 2 : 0;
+}
+
+moe_status moe_router_split(const float *router_d, int32_t E, int32_t H, void *split_d, size_t split_bytes,
+                            void *stream) {
+  g_last_launches = 0;
+  if (!router_d || !split_d || E < 1 || H < 1 || ((size_t)E * H) % 4) return MOE_ERR_INVALID_ARGUMENT;
+  if (!moe::aligned16(router_d) || !moe::aligned16(split_d)) return MOE_ERR_MISALIGNED;
+  if (split_bytes < moe_router_split_bytes(E, H)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaError_t err = moe::launch_router_split(router_d, E, H, static_cast<uint16_t *>(split_d),
+                                             static_cast<cudaStream_t>(stream));
+  g_last_launches = 1;
   return cuda_status(err);
 }
 

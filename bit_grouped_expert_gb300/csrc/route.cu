@@ -69,14 +69,41 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t *__re
 
 // ---------------------------------------------------------------- top-k
 // (per-token selection: topk.cuh)
+// With part != null the keys are first summed from the router's KS K-slice
+// partial sums ([KS][T][E], in slice order, + bias) and stored to keys.
 template <int KPL>
-__global__ void __launch_bounds__(64) topk_kernel(const float *__restrict__ keys, int T, int E, int k,
+__global__ void __launch_bounds__(64) topk_kernel(float *__restrict__ keys, int T, int E, int k,
                                                    int32_t *__restrict__ topk_id, float *__restrict__ topk_w,
-                                                   int32_t *__restrict__ counts, int32_t *__restrict__ status) {
+                                                   int32_t *__restrict__ counts, int32_t *__restrict__ status,
+                                                   const float *__restrict__ part, int KS,
+                                                   const float *__restrict__ bias) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
   if (warp >= T) return;
+  const KeySrc src{part ? part + (size_t)warp * E : nullptr, (size_t)T * E, part ? KS : 0, bias};
   topk_token<KPL>(keys + (size_t)warp * E, E, k, lane, topk_id + (size_t)warp * k, topk_w + (size_t)warp * k,
-                  counts, status);
+                  counts, status, src);
+}
+
+// Histogram of given expert ids ([T][k]); ids outside [0, E) are not counted
+// and set MOE_ERR_DEVICE_BOUNDS; with debug, so does an expert named twice
+// by one token.
+__global__ void __launch_bounds__(256) ids_histogram_kernel(const int32_t *__restrict__ ids, int T, int E, int k,
+                                                            int32_t *__restrict__ counts, int32_t *__restrict__ status,
+                                                            int debug) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const int32_t *row = ids + (size_t)t * k;
+  for (int j = 0; j < k; ++j) {
+    const int e = row[j];
+    if (e < 0 || e >= E) {
+      set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    atomicAdd(&counts[e], 1);
+    if (debug)
+      for (int i = 0; i < j; ++i)
+        if (row[i] == e) set_status(status, MOE_ERR_DEVICE_BOUNDS);
+  }
 }
 
 // ---------------------------------------------------------------- scatter
@@ -235,25 +262,33 @@ cudaError_t launch_router_logits(const uint16_t *x, int T, int H, const float *r
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
-                        int32_t *status, cudaStream_t s) {
+cudaError_t launch_topk(float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
+                        int32_t *status, const float *part, int KS, const float *bias, cudaStream_t s) {
   // two tokens (warps) per block, so small T still spreads over many SMs
   const int blocks = (T + 1) / 2;
   const int kpl = (E + 31) / 32;
   prof_before(MOE_KERNEL_TOPK, s);
+#define MOE_TOPK(K) topk_kernel<K><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status, part, KS, bias)
   if (kpl <= 1)
-    topk_kernel<1><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    MOE_TOPK(1);
   else if (kpl <= 2)
-    topk_kernel<2><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    MOE_TOPK(2);
   else if (kpl <= 4)
-    topk_kernel<4><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    MOE_TOPK(4);
   else if (kpl <= 8)
-    topk_kernel<8><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    MOE_TOPK(8);
   else if (kpl <= 16)
-    topk_kernel<16><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    MOE_TOPK(16);
   else
-    topk_kernel<32><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status);
+    MOE_TOPK(32);
+#undef MOE_TOPK
   prof_after(MOE_KERNEL_TOPK, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ids_histogram(const int32_t *ids, int T, int E, int k, int32_t *counts, int32_t *status, int debug,
+                                 cudaStream_t s) {
+  ids_histogram_kernel<<<(T + 255) / 256, 256, 0, s>>>(ids, T, E, k, counts, status, debug);
   return cudaGetLastError();
 }
 

@@ -9,14 +9,16 @@
 // so key = sum_k x_k*hi_k + x_k*mid_k + x_k*lo_k accumulated in fp32 differs
 // from the fp32 dot product only by summation order.
 //
-//   router_split_kernel  fp32 [E][H] -> bf16 [3][E][H] (hi, mid, lo)
+//   router_split_kernel  fp32 [E][H] -> bf16 [3][E][H] (hi, mid, lo); run once
+//                        per set of weights (moe_router_split) or, when the
+//                        caller passes no split, inside the call
 //   router_tc_kernel     D[e][t] = sum over parts of A_p[e] . x[t] (tcgen05,
 //                        A and B from shared memory, fp32 accumulate in
 //                        tensor memory), keys[t][e] = D + bias[e]
 // One work item = 128 experts x N tokens (N = 32/64/128 by T) x one of KS
 // slices of K (KS chosen so that the items fill the SMs; with KS > 1 each
-// item writes fp32 partial sums and router_reduce_kernel adds the KS slices
-// in order, so the keys do not depend on timing); warp 0 issues
+// item writes fp32 partial sums and the top-k kernel adds the KS slices in
+// order before it selects, so the keys do not depend on timing); warp 0 issues
 // TMA (three 128x64 A boxes + one N x 64 B box per k-block, 128B swizzle),
 // warp 1 issues the MMAs, warps 4-7 drain the accumulator.  Waits are bounded
 // as in the expert kernels.
@@ -42,7 +44,7 @@ constexpr unsigned long long R_TIMEOUT_NS = 1000000000ull;
 
 struct RArgs {
   float *keys;     // [T][E] keys, or with KS > 1 the partial sums [KS][T][E]
-  const float *bias;  // added when KS == 1 (else by the reduction)
+  const float *bias;  // added when KS == 1 (else by the top-k kernel, after the slices)
   int32_t *status;
   int T, E, H, N, KS;
 };
@@ -235,30 +237,6 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   }
 }
 
-// keys = sum of the KS partial slices in slice order (+ bias), 4 keys a thread.
-__global__ void __launch_bounds__(256) router_reduce_kernel(const float4 *__restrict__ part, size_t n4, int KS,
-                                                            int E4, const float4 *__restrict__ bias,
-                                                            float4 *__restrict__ keys) {
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n4) return;
-  float4 acc = part[i];
-  for (int s = 1; s < KS; ++s) {
-    const float4 v = part[(size_t)s * n4 + i];
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
-  }
-  if (bias) {
-    const float4 b = bias[i % E4];
-    acc.x += b.x;
-    acc.y += b.y;
-    acc.z += b.z;
-    acc.w += b.w;
-  }
-  keys[i] = acc;
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
 
 // bf16 [rows][cols] tensor, boxes of box_rows x 64 elements, 128B swizzle.
@@ -303,16 +281,25 @@ cudaError_t router_tc_prepare() {
   return cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, R_SMEM);
 }
 
-cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
-                             uint16_t *split, float *partial, float *keys, int32_t *status, int num_sms,
-                             cudaStream_t s) {
+cudaError_t launch_router_split(const float *router, int E, int H, uint16_t *split, cudaStream_t s) {
   const size_t n = (size_t)E * H;
-  prof_before(MOE_KERNEL_ROUTER, s);
   router_split_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(
       reinterpret_cast<const float4 *>(router), n / 4, reinterpret_cast<uint2 *>(split),
       reinterpret_cast<uint2 *>(split + n), reinterpret_cast<uint2 *>(split + 2 * n));
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
+                             const uint16_t *split_given, uint16_t *split, float *partial, float *keys,
+                             int32_t *status, int num_sms, int *ks_out, int *launches, cudaStream_t s) {
+  prof_before(MOE_KERNEL_ROUTER, s);
+  cudaError_t e = cudaSuccess;
+  if (split_given) {
+    split = const_cast<uint16_t *>(split_given);
+  } else {
+    if ((e = launch_router_split(router, E, H, split, s)) != cudaSuccess) return e;
+    ++*launches;
+  }
   const int N = router_n(T), KS = router_tc_slices(T, E, H, num_sms);
   CUtensorMap ta, tb;
   if ((e = bf16_map(&ta, split, 3 * E, H, RM)) != cudaSuccess) return e;
@@ -320,13 +307,9 @@ cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *route
   RArgs a{KS > 1 ? partial : keys, bias, status, T, E, H, N, KS};
   const int items = ((T + N - 1) / N) * (E / RM) * KS;
   router_tc_kernel<<<items < num_sms ? items : num_sms, RTHREADS, R_SMEM, s>>>(ta, tb, a);
-  if (KS > 1 && (e = cudaGetLastError()) == cudaSuccess) {
-    const size_t n4 = (size_t)T * E / 4;
-    router_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
-        reinterpret_cast<const float4 *>(partial), n4, KS, E / 4, reinterpret_cast<const float4 *>(bias),
-        reinterpret_cast<float4 *>(keys));
-  }
   prof_after(MOE_KERNEL_ROUTER, s);
+  ++*launches;
+  *ks_out = KS;
   return cudaGetLastError();
 }
 

@@ -36,10 +36,17 @@ cudaError_t router_tc_prepare();
 // the SMs), and the fp32 partial-sum buffer a plan for up to Tmax tokens needs.
 int router_tc_slices(int T, int E, int H, int num_sms);
 size_t router_tc_partial_floats(int Tmax, int E, int H, int num_sms);
-// partial: workspace of router_tc_partial_floats floats (16-byte aligned).
+// The router's bf16 parts [3][E][H] (hi, mid, lo) from the fp32 router.
+cudaError_t launch_router_split(const float *router, int E, int H, uint16_t *split, cudaStream_t s);
+// Router keys for T tokens.  split_given: the parts from launch_router_split,
+// or null (then they are written into split first).  partial: workspace of
+// router_tc_partial_floats floats (16-byte aligned).  *ks_out = the K slices
+// used: with 1 the keys (bias added) are in keys; with more, partial holds
+// [KS][T][E] fp32 sums that the top-k kernel adds in slice order (+ bias).
+// *launches counts the kernels enqueued.
 cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
-                             uint16_t *split, float *partial, float *keys, int32_t *status, int num_sms,
-                             cudaStream_t s);
+                             const uint16_t *split_given, uint16_t *split, float *partial, float *keys,
+                             int32_t *status, int num_sms, int *ks_out, int *launches, cudaStream_t s);
 constexpr int ROUTER_TC_MIN_T = 32;  // below this the CUDA-core router is used
 
 }  // namespace moe

@@ -49,17 +49,41 @@ __device__ __forceinline__ void topk_finish(int lane, int k, int my_id, float my
   }
 }
 
+// The keys of one token come either from row (KS == 0) or, with the router's
+// K split into KS slices, as part[0][e] + part[1][e] + ... + part[KS-1][e]
+// (+ bias[e]), added in slice order; those sums are stored to row.
+// part points at the token's row of slice 0; slices are pstride floats apart.
+struct KeySrc {
+  const float *part;
+  size_t pstride;
+  int KS;
+  const float *bias;
+};
+
 // One warp selects a token's top k (k <= 32) from E <= 32*KPL keys.  Lane l
 // holds experts l, l+32, ...; each round takes the warp-wide largest code.
 template <int KPL>
-__device__ void topk_token(const float *__restrict__ row, int E, int k, int lane, int32_t *__restrict__ ids_out,
-                           float *__restrict__ w_out, int32_t *__restrict__ counts, int32_t *__restrict__ status) {
+__device__ void topk_token(float *__restrict__ row, int E, int k, int lane, int32_t *__restrict__ ids_out,
+                           float *__restrict__ w_out, int32_t *__restrict__ counts, int32_t *__restrict__ status,
+                           KeySrc src = KeySrc{nullptr, 0, 0, nullptr}) {
   unsigned long long c[KPL];
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const int e = lane + 32 * i;
-    c[i] = (e < E) ? topk_code(row[e], e) : 0ull;  // 0: below every real code
+    float key = 0.f;
+    if (e < E) {
+      if (src.KS > 0) {
+        key = src.part[e];
+        for (int s = 1; s < src.KS; ++s) key += src.part[(size_t)s * src.pstride + e];
+        if (src.bias) key += src.bias[e];
+        row[e] = key;
+      } else {
+        key = row[e];
+      }
+    }
+    c[i] = (e < E) ? topk_code(key, e) : 0ull;  // 0: below every real code
   }
+  if (src.KS > 0) __syncwarp();  // the stored keys are read back below
   int my_id = -1;
   float my_key = 0.f;
   for (int r = 0; r < k; ++r) {

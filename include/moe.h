@@ -9,8 +9,9 @@
  *     inside the grouped GEMM with FP32 accumulation, so no unpacked weight
  *     array reaches memory; routing (histogram, prefix scan, scatter, block
  *     map) stays on the GPU with no CPU sync inside the layer;
- *   - "Decode": at batch 1 there is almost no weight reuse, so bandwidth
- *     bounds the step; only the selected experts' bytes are streamed.
+ *   - "Decode": one token at a time reuses next to none of the weights it
+ *     reads, so HBM bandwidth sets the limit; only the selected experts'
+ *     bytes are streamed.
  *
  * Arithmetic (where the pages are silent, the plainest reading):
  *   w      = bf16_rne(scale * q + bias), q = (word[k/8] >> 4*(k%8)) & 15
@@ -79,7 +80,11 @@ typedef struct {
  * shared_gate (optional, a variant the pages do not print): the shared
  * expert's output is scaled by g = sigmoid(x . shared_gate) per token, x the
  * layer's expert input (after the pre-norm of stacked layers), the dot
- * product in fp32: out = bf16(res + g * y_shared + sum_j w_j y_j).  NULL: g = 1. */
+ * product in fp32: out = bf16(res + g * y_shared + sum_j w_j y_j).  NULL: g = 1.
+ * router_split_d (optional): the router as three bf16 parts, [3][E][H]
+ * (hi, mid, lo; moe_router_split writes them once per set of weights).  The
+ * tensor-core router (T >= 32) reads them instead of splitting router_d on
+ * every call; the keys are the same bit for bit.  NULL: split per call. */
 typedef struct {
   const float *router_d;
   const uint32_t *gate_q_d, *up_q_d;
@@ -87,6 +92,7 @@ typedef struct {
   const uint32_t *down_q_d;
   const uint16_t *down_s_d, *down_b_d;
   const float *shared_gate_d;
+  const uint16_t *router_split_d;
 } moe_weights;
 
 /* Device pointers into a workspace, for tests and tools (moe_route_view). */
@@ -130,6 +136,14 @@ typedef struct {
                                          computes x = RMSNorm(r) (unit gain, eps 1e-6) and
                                          out = r + MoE(x); residual_d must be NULL and out_d
                                          may alias x_d (in-place residual update) */
+#define MOE_FLAG_TEST_WITHHOLD  0x40u /* test aid for the failure path of the T == 1 decode kernel:
+                                         the CTA that computes expert 0's router key never
+                                         publishes it, and every wait of the decode kernel gives
+                                         up after 1 ms instead of 1 s, so the other CTAs' bounded
+                                         waits run out, MOE_ERR_DEVICE_TIMEOUT lands in the status
+                                         word and the kernel returns (its copies drained).  The
+                                         workspace then needs moe_workspace_init.  Other paths
+                                         are unaffected. */
 
 typedef struct moe_plan moe_plan_t;
 
@@ -164,6 +178,18 @@ moe_status moe_route(const moe_plan_t *plan, const void *x_d, int32_t T, const f
 moe_status moe_route_from_logits(const moe_plan_t *plan, const float *keys_d, int32_t T, void *ws_d,
                                  size_t ws_bytes, void *stream);
 
+/* Routing from given expert choices (test hook and teacher-forced routing):
+ * ids_d int32 [T][k] (distinct experts per token, in slot order) and w_d fp32
+ * [T][k] are copied into the workspace's top-k buffers, then the histogram,
+ * scan, scatter and block maps run as in moe_route (the key buffer is left
+ * as it was).  An id outside [0, E) is not counted and sets
+ * MOE_ERR_DEVICE_BOUNDS in the device status; with MOE_FLAG_DEBUG_CHECKS a
+ * token that names one expert twice does too (the scatter then finds fewer
+ * pairs than the histogram counted).  After such a status the routing
+ * buffers hold no valid routing. */
+moe_status moe_route_from_ids(const moe_plan_t *plan, const int32_t *ids_d, const float *w_d, int32_t T, void *ws_d,
+                              size_t ws_bytes, void *stream);
+
 /* The whole layer: routing, shared + routed SwiGLU experts over the packed
  * weights, and the weighted combine with the residual.
  *   x_d        bf16 [T][H] layer input (read only), or with MOE_FLAG_PRENORM
@@ -192,6 +218,38 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
  * moe_forward; MOE_ERR_UNSUPPORTED when the plan's shape has no decode path. */
 moe_status moe_decode_stack(const moe_plan_t *plan, void *r_d, int32_t n_layers, const moe_weights *w,
                             const float *const *logit_bias_d, void *ws_d, size_t ws_bytes, void *stream);
+
+/* A long prompt through a stack of n_layers pre-norm MoE layers in bounded
+ * chunks ("Prefill" section: long prompts are processed in chunks of bounded
+ * size, so temporary activations stay small next to the resident weights):
+ *   for c0 = 0, m, 2m, ... (m = the plan's max_tokens):
+ *     rows c0 .. c0 + n - 1 of r (n = min(m, T - c0)), for l = 0 .. n_layers-1:
+ *       r_c = r_c + MoE_l(RMSNorm(r_c))
+ * chunk-major (each chunk passes through every layer before the next chunk
+ * starts), every call on the one workspace.  The same arithmetic, call for
+ * call, as the moe_forward calls of that loop (a one-token tail chunk takes
+ * the decode path).  The plan must have MOE_FLAG_PRENORM.
+ *   r_d           bf16 [T][H] residual stream, updated in place (device)
+ *   T             1 <= T (no upper bound beyond the caller's buffer)
+ *   w             host array of n_layers moe_weights (device pointers)
+ *   logit_bias_d  host array of n_layers device pointers (entries may be
+ *                 NULL), or NULL
+ * Errors: as moe_forward (nothing is enqueued when an argument check fails;
+ * a launch failure part-way returns MOE_ERR_CUDA with the earlier calls
+ * enqueued). */
+moe_status moe_prefill_stack(const moe_plan_t *plan, void *r_d, int32_t T, int32_t n_layers, const moe_weights *w,
+                             const float *const *logit_bias_d, void *ws_d, size_t ws_bytes, void *stream);
+
+/* The router's three bf16 parts, for moe_weights.router_split_d (the
+ * tensor-core router's operand): split_d[p][e][h], p = 0, 1, 2, with
+ * hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid) (round to
+ * nearest even, each difference exact in fp32).  router_d fp32 [E][H];
+ * split_d bf16 [3][E][H] (moe_router_split_bytes(E, H) bytes, caller-owned).
+ * Enqueued on stream; run it once per set of router weights and pass split_d
+ * as moe_weights.router_split_d.  E * H must be a multiple of 4. */
+size_t moe_router_split_bytes(int32_t E, int32_t H);
+moe_status moe_router_split(const float *router_d, int32_t E, int32_t H, void *split_d, size_t split_bytes,
+                            void *stream);
 
 /* Device pointers of the workspace's routing buffers for T tokens (host-side
  * arithmetic only; nothing is read or enqueued). */
@@ -234,8 +292,8 @@ typedef enum {
   MOE_KERNEL_ATTN_DECODE = 13    /* decode attention, per-block pass (attn.h)  */
 } moe_kernel;
 
-/* Profiling hook.  From now on, on the calling thread, the i-th launch of
- * `kernel` is bracketed by cudaEventRecord(start_events[i % n]) and
+/* Profiling hook (one per kernel).  From now on, on the calling thread, the
+ * i-th launch of `kernel` is bracketed by cudaEventRecord(start_events[i % n]) and
  * cudaEventRecord(stop_events[i % n]) on that launch's stream (also inside a
  * stream capture, where the records become graph nodes).  start_events and
  * stop_events are host arrays of n cudaEvent_t handles, copied by the call;
@@ -243,6 +301,13 @@ typedef enum {
  * Errors: MOE_ERR_INVALID_ARGUMENT for an unknown kernel, n < 0, n > 4096,
  * null arrays with n > 0, or a null event handle. */
 moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *const *stop_events, int32_t n);
+
+/* Thin the hook of `kernel` out (after moe_profile_events turned it on):
+ * only launches 0, stride, 2*stride, ... of the kernel, counted from this
+ * call, are bracketed (the j-th of them by event j % n).  Errors:
+ * MOE_ERR_INVALID_ARGUMENT for an unknown kernel, stride < 1 or a kernel
+ * whose hook is off. */
+moe_status moe_profile_stride(int32_t kernel, int32_t stride);
 
 /* Allocation-free single-token layer.  The paper has no counterpart to this
  * entry point: it serves callers that cannot call cudaMalloc -- code running
@@ -276,9 +341,12 @@ moe_status moe_profile_events(int32_t kernel, void *const *start_events, void *c
  * array otherwise keeps the previous call's contents.  All calls on a device
  * share the one array: calls that can overlap on the GPU (other streams,
  * other threads) race and must be serialised by the caller.
- * Errors: MOE_ERR_WORKSPACE_TOO_SMALL when the layer's scratch (about
- * 16E + 8(k + n_shared)I + 8H + 4E + 8k bytes plus 256-byte alignment: 58,912
- * bytes for H=2048, E=256, k=8, n_shared=1, I=512) exceeds the array;
+ * Errors: MOE_ERR_WORKSPACE_TOO_SMALL when the layer's scratch exceeds the
+ * array.  The scratch is 256 bytes of status and counter, then
+ * 8 * (2 W + (k + n_shared) I + H) bytes of tagged words with
+ * W = round_up(E + 1, 16), then 4E bytes of keys, 4k of top-k ids and 4k of
+ * weights, each part starting on a 256-byte boundary: 59,168 bytes for
+ * H=2048, E=256, k=8, n_shared=1, I=512 (6,368 bytes below the limit);
  * MOE_ERR_UNSUPPORTED for dimensions the decode path does not take
  * (H and I powers of two, the kernel's shared memory within the device's
  * limit); MOE_ERR_INVALID_ARGUMENT / MOE_ERR_MISALIGNED as for moe_forward;
