@@ -96,10 +96,11 @@ def test_layer_dense_sizes_match_oracle(real, T, tiles):
 
 # ---------------------------------------------------------------- router parts given once
 
-@pytest.mark.parametrize("T", [256, 4096])
+@pytest.mark.parametrize("T", [256, 4096, 8192])
 def test_router_split_given_once_gives_the_same_keys(real, T):
-    # T = 256 splits K over several slices (summed by the top-k kernel),
-    # T = 4096 takes one slice: both must equal the per-call split bit for bit
+    # T = 256 and 4096 split K over 8 and 2 slices (summed by the top-k
+    # kernel), T = 8192 takes one slice: each must equal the per-call split
+    # bit for bit
     W, Wd = real
     x = dev(syn.activations(2000 + T, T, H))
     split = torch.empty(moe.moe_router_split_bytes(E, H), dtype=torch.uint8, device="cuda:0")
