@@ -442,15 +442,22 @@ def _stack_vs_layers(d, Ws, biases, r):
     return host_u16(rs), inputs, Ls, launches
 
 
-def test_decode_stack_real_dims_matches_layer_by_layer(real):
+def _centred_layers(seeds):
+    # centred weights: with the literal generator's mean weight a stack's
+    # residual stream runs away after its first layer (or the later layers'
+    # gates saturate and add exactly nothing), which a stack test would not see
+    Ws = []
+    for seed in seeds:
+        W = syn.experts(seed, 257, 2048, 512, layer=seed, centred=True)
+        W["router"] = syn.router(seed, 256, 2048, layer=seed)
+        Ws.append(W)
+    return Ws
+
+
+def test_decode_stack_real_dims_matches_layer_by_layer():
     # three distinct layers at the model's dims: one launch, bit-identical to
     # three single-layer calls; the last layer also against the oracle
-    W0, _ = real
-    Ws = [W0]
-    for seed in (1, 2):
-        W = syn.experts(seed, 257, 2048, 512)
-        W["router"] = syn.router(seed, 256, 2048)
-        Ws.append(W)
+    Ws = _centred_layers((0, 1, 2))
     biases = [None, syn.zipf_bias(5, 256), None]
     r = syn.activations(88, 1, 2048, tensor=syn.T_RESID)
     out, inputs, Ls, launches = _stack_vs_layers(dict(H=2048, E=256, k=8, I=512), Ws, biases, r)
@@ -493,16 +500,10 @@ def test_decode_stack_mixed_shared_gates():
     assert_outputs_close(out, ref, "gated stack layer 8", k=d["k"])
 
 
-def test_decode_stack_repeated_tokens_seven_layers(real):
+def test_decode_stack_repeated_tokens_seven_layers():
     # one full launch (7 layers) per token, several tokens in a row on one
     # workspace: the tagged exchange must hand every launch its own values
-    W0, _ = real
-    Ws = [W0]
-    for seed in range(1, 7):
-        W = syn.experts(seed, 257, 2048, 512)
-        W["router"] = syn.router(seed, 256, 2048)
-        Ws.append(W)
-    Wds = [dev_weights(W) for W in Ws]
+    Wds = [dev_weights(W) for W in _centred_layers(range(7))]
     L = Layer(max_tokens=1, flags=moe.MOE_FLAG_PRENORM)
     Ls = Layer(max_tokens=1)
     for t in range(6):

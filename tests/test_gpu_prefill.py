@@ -87,8 +87,8 @@ def test_layer_dense_sizes_match_oracle(real, T, tiles):
     assert L.status() == 0
     r = L.routing(T)
     _assert_routing_equal(r)
-    per_expert = r["counts"]
-    assert (per_expert > r["block_rows"]).any()  # some expert spans more than one tile
+    if 8 * T // 256 >= r["block_rows"]:  # some expert spans more than one tile
+        assert (r["counts"] > r["block_rows"]).any()
     rows = np.random.default_rng(T).choice(T, 64, replace=False)
     ref = orc.moe_layer(orc.Dims(), x[rows], W, keys=r["keys"][rows], intermediates=True)
     assert_outputs_close(host_u16(out)[rows], ref, f"T={T} {tiles} (64 sampled rows)")
