@@ -17,7 +17,7 @@ import pytest
 
 import oracle as orc
 import synthetic as syn
-from tests.tolerances import assert_outputs_close, output_errors
+from tests.tolerances import assert_outputs_close, bf16_value, output_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -117,8 +117,11 @@ def test_router_split_given_once_gives_the_same_keys(real, T):
     assert got["given"][0] == got["per call"][0] - 1  # no split kernel
     np.testing.assert_array_equal(got["given"][1], got["per call"][1])
     np.testing.assert_array_equal(got["given"][2], got["per call"][2])
-    ref = orc.logits(host_u16(x)[:64], W["router"])
-    assert np.allclose(got["given"][1][:64], ref, rtol=1e-5, atol=1e-5)
+    xs = host_u16(x)[:64]
+    ref = orc.logits(xs, W["router"]).astype(np.float64)
+    mag = np.abs(bf16_value(xs)) @ np.abs(W["router"].astype(np.float64)).T
+    bound = H * 2.0 ** -24 * mag + np.abs(ref) * 2.0 ** -23  # fp32 summation of H products
+    assert (np.abs(got["given"][1][:64] - ref) <= bound).all()
 
 
 # ---------------------------------------------------------------- chunked prompt through a stack
