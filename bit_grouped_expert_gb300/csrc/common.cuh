@@ -84,6 +84,27 @@ __device__ __forceinline__ void dequant_word(uint32_t word, __nv_bfloat162 s2, _
   }
 }
 
+// The rebuild through subnormal codes.  The bf16 pattern 0x000q is the
+// subnormal q * 2^-133 exactly, so with the scale taken times 2^133 (exact:
+// a power of two) one fused multiply-add of the masked code pair gives
+// bf16_rne(s*q + b) with a single rounding -- the same bits as the
+// 0x4300 | q route, without its OR and subtraction.  s * 2^133 stays finite
+// for |s| < 2^-5 (bf16 exponent field <= 121); larger scales take the other
+// route.
+__device__ __forceinline__ bool small_scale(__nv_bfloat162 s2) {
+  return (*reinterpret_cast<const uint32_t *>(&s2) & 0x7F80u) < (122u << 7);
+}
+__device__ __forceinline__ __nv_bfloat162 scale_for_subnormal_codes(__nv_bfloat162 s2) {
+  return __hmul2(__hmul2(s2, __floats2bfloat162_rn(0x1p127f, 0x1p127f)), __floats2bfloat162_rn(64.f, 64.f));
+}
+// Codes at bits 0..3 and 16..19 of t (other bits ignored) -> bf16x2 weights;
+// s2x from scale_for_subnormal_codes.
+__device__ __forceinline__ uint32_t dq_pair_subnormal(uint32_t t, __nv_bfloat162 s2x, __nv_bfloat162 b2) {
+  t &= 0x000F000Fu;
+  const __nv_bfloat162 r = __hfma2(s2x, *reinterpret_cast<const __nv_bfloat162 *>(&t), b2);
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 __device__ __forceinline__ __nv_bfloat162 bf16x2_splat(uint16_t v) {
   uint32_t u = static_cast<uint32_t>(v) | (static_cast<uint32_t>(v) << 16);
   return *reinterpret_cast<__nv_bfloat162 *>(&u);

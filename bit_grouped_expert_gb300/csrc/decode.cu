@@ -222,11 +222,22 @@ __device__ __forceinline__ float gemv_chunk(const uint8_t *chunk, uint16_t sv, u
   const uint2 *xp = reinterpret_cast<const uint2 *>(xg + q * XPAD) + (g & 1);
   // four accumulators: chains of two dependent MMAs
   float e[4][4] = {};
+  if (small_scale(s2)) {  // the usual case: subnormal codes (common.cuh)
+    const __nv_bfloat162 s2x = scale_for_subnormal_codes(s2);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {  // word i: codes 8i..8i+7 of the group
-    const uint32_t w = wv[i];
-    const uint2 xv = xp[2 * i];
-    mma16816(e[i & 3], dq(w, s2, b2), dq(w >> 8, s2, b2), dq(w >> 4, s2, b2), dq(w >> 12, s2, b2), xv.x, xv.y);
+    for (int i = 0; i < 8; ++i) {  // word i: codes 8i..8i+7 of the group
+      const uint32_t w = wv[i];
+      const uint2 xv = xp[2 * i];
+      mma16816(e[i & 3], dq_pair_subnormal(w, s2x, b2), dq_pair_subnormal(w >> 8, s2x, b2),
+               dq_pair_subnormal(w >> 4, s2x, b2), dq_pair_subnormal(w >> 12, s2x, b2), xv.x, xv.y);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w = wv[i];
+      const uint2 xv = xp[2 * i];
+      mma16816(e[i & 3], dq(w, s2, b2), dq(w >> 8, s2, b2), dq(w >> 4, s2, b2), dq(w >> 12, s2, b2), xv.x, xv.y);
+    }
   }
   return ((e[0][0] + e[1][0]) + (e[2][0] + e[3][0])) + ((e[0][3] + e[1][3]) + (e[2][3] + e[3][3]));
 }

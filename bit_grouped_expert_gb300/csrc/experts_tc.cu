@@ -510,12 +510,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           const __nv_bfloat162 s2 = pick_group(sg, j), b2 = pick_group(bg, j);
           uint32_t v[32];
           const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          if (small_scale(s2)) {  // the usual case: subnormal codes, one mask and one FMA a pair
+            const __nv_bfloat162 s2x = scale_for_subnormal_codes(s2);
 #pragma unroll
-          for (int wi = 0; wi < 8; ++wi) {
-            uint32_t p[4];
-            dequant_word_ilv(wv[wi], s2, b2, p);
+            for (int wi = 0; wi < 8; ++wi)
 #pragma unroll
-            for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = p[pi];
+              for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = dq_pair_subnormal(wv[wi] >> (4 * pi), s2x, b2);
+          } else {
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) {
+              uint32_t p[4];
+              dequant_word_ilv(wv[wi], s2, b2, p);
+#pragma unroll
+              for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = p[pi];
+            }
           }
           const int aslot = kbg % NSLOT;
           if (!__all_sync(0xffffffffu, timed(tr, w_free, [&] {

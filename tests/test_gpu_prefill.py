@@ -191,16 +191,23 @@ def test_prefill_stack_ragged_tail_and_errors(real):
 def test_prefill_32k_prompt_40_layers_end_to_end(centred):
     # the full long-prompt workload: 32768 tokens in 4096-token chunks through
     # 40 layers on one workspace; 8 sampled tokens through the oracle's own
-    # 40-layer stack (its own routing at every layer)
+    # 40-layer stack (its own routing at every layer).  The stack amplifies
+    # any rounding difference (a near-tie flips a token's routing, the next
+    # layers take a different input), so the GPU's end-to-end distance from
+    # the oracle is set against the oracle's distance from itself when one
+    # input element of each token moves by one bf16 step.
     T, chunk, n_layers = 32768, 4096, 40
     r0 = syn.activations(72, T, H, tensor=syn.T_RESID)
     sample = sorted(np.random.default_rng(6).choice(T, 8, replace=False).tolist())
     r_orc = r0[sample].copy()
+    r_pert = r_orc.copy()
+    r_pert[:, 100] += 1  # one bf16 step on one element
     Wds = []
     for l in range(n_layers):
         W = _layer_weights(11, l, centred)
         Wds.append(dev_weights(W))
         r_orc = orc.moe_layer(orc.Dims(), orc.rmsnorm(r_orc, 1e-6), W, res=r_orc)["out"]
+        r_pert = orc.moe_layer(orc.Dims(), orc.rmsnorm(r_pert, 1e-6), W, res=r_pert)["out"]
         del W
     L = Layer(max_tokens=chunk, flags=moe.MOE_FLAG_PRENORM)
     rd = dev(r0)
@@ -210,6 +217,8 @@ def test_prefill_32k_prompt_40_layers_end_to_end(centred):
     got = host_u16(rd)
     assert np.isfinite(orc.bf16_to_f64(got)).all()
     e = output_errors(got[sample], orc.bf16_to_f64(r_orc))
+    sens = output_errors(r_pert, orc.bf16_to_f64(r_orc))
     print(f"\n40-layer 32K prompt ({'centred' if centred else 'literal'} weights), 8 tokens vs the oracle's own "
-          f"stack: rel-L2 {e['rel_l2']:.3e}, max|err|/rms {e['max_abs'] / e['rms']:.3e}")
-    assert e["rel_l2"] < 0.1
+          f"stack: rel-L2 {e['rel_l2']:.3e}, max|err|/rms {e['max_abs'] / e['rms']:.3e}; the oracle against itself "
+          f"with one element one bf16 step off: rel-L2 {sens['rel_l2']:.3e}")
+    assert e["rel_l2"] <= 2 * sens["rel_l2"] + 0.02
