@@ -306,7 +306,7 @@ def run_ours(args, wl, rank, world, device, cache=None, steps=None, warmup=None,
     else:
         layers_per_launch = 1
         kerns = [moe.MOE_KERNEL_GATEUP, moe.MOE_KERNEL_DOWN]
-        n_ev = N_EV
+        n_ev = N_EV if L > 1 else 1  # a single layer launches each kernel once per step
     ev = {kn: ([torch.cuda.Event(enable_timing=True) for _ in range(n_ev)],
                [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]) for kn in kerns}
     profiling = [False]

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(&m->code_empty[i], NWG * 4);
     }
     for (int i = 0; i < NSLOT; ++i) {
-      ptx::mbar_init(&m->ready[i], 1 + C::NMAT * 128);  // token-row TMA + one warpgroup per matrix
+      ptx::mbar_init(&m->ready[i], 1 + 128);  // token-row TMA + the warpgroup that rebuilt the k-block
       ptx::mbar_init(&m->free[i], NISS);
     }
     ptx::mbar_init(&m->acc_full, NISS);
@@ -427,15 +427,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ dequant + epilogue
-    // Work unit u = kb * NMAT + mat (one k-block of one matrix) goes to
-    // warpgroup u % NWG; epilogue chunks of 16 columns are dealt the same way.
+    // Work unit = one k-block of every matrix (gate and up, or down): the
+    // CTA's running k-block kbg goes to warpgroup kbg % NWG, which rebuilds
+    // it into A slot kbg % NSLOT and arrives once on that slot's ready
+    // barrier; epilogue chunks of 16 columns are dealt round-robin.
     // A slot's free barrier is waited on by phase parity, which is exact only
     // while the waiter is at most one phase ahead of the slot.  That holds
-    // here: a warpgroup's consecutive units are at most 2 (gate/up) or 3
-    // (down) k-blocks apart, so its previous wait already saw the MMA past
-    // k-block kb - 8, and every warp meets the MMA at the end of each item
-    // (acc_full) before it starts the next.  A different unit order, or an
-    // epilogue moved past the next item's first units, must keep this.
+    // here: a warpgroup's consecutive k-blocks are NWG = 3 < NSLOT apart, so
+    // its previous wait already saw the MMA past k-block kbg - 7, and every
+    // warp meets the MMA at the end of each item (acc_full) before it starts
+    // the next.  A different unit order, or an epilogue moved past the next
+    // item's first units, must keep this.
     const int wg = (warp - 4) >> 2, q = warp & 3;
     const int row = q * 32 + lane;  // weight row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -496,44 +498,47 @@ __global__ void __launch_bounds__(THREADS, 1)
             bv[mt] = *reinterpret_cast<const uint2 *>(sb + mt * 2 * SBOX + SBOX);
           }
         }
-        const int u0 = kb0 * C::NMAT, u1 = (kb0 + nkb) * C::NMAT;
+        const uint8_t *stage = smem + cslot * C::STAGE_BYTES + row * 128;
+        const int r7 = row & 7;
 #pragma unroll 1
-        for (int u = u0 + ((wg - u0 % NWG) + NWG) % NWG; u < u1; u += NWG) {
-          const int j = u / C::NMAT - kb0, mat = u % C::NMAT;
+        for (int j = (int)((wg + NWG - kbc % NWG) % NWG); j < nkb; j += NWG) {
           const uint32_t kbg = kbc + j;
-          const uint8_t *rb = smem + cslot * C::STAGE_BYTES + mat * BOX + row * 128;
-          const int c0 = j * 2;
-          const uint4 w0 = *reinterpret_cast<const uint4 *>(rb + ((c0 ^ (row & 7)) << 4));
-          const uint4 w1 = *reinterpret_cast<const uint4 *>(rb + (((c0 + 1) ^ (row & 7)) << 4));
-          const uint2 sg = mat ? sv[C::NMAT - 1] : sv[0];
-          const uint2 bg = mat ? bv[C::NMAT - 1] : bv[0];
-          const __nv_bfloat162 s2 = pick_group(sg, j), b2 = pick_group(bg, j);
-          uint32_t v[32];
-          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-          if (small_scale(s2)) {  // the usual case: subnormal codes, one mask and one FMA a pair
-            const __nv_bfloat162 s2x = scale_for_subnormal_codes(s2);
+          const uint32_t aslot = kbg % NSLOT;
 #pragma unroll
-            for (int wi = 0; wi < 8; ++wi)
+          for (int mat = 0; mat < C::NMAT; ++mat) {
+            const uint8_t *rb = stage + mat * BOX;
+            const uint4 w0 = *reinterpret_cast<const uint4 *>(rb + (((2 * j) ^ r7) << 4));
+            const uint4 w1 = *reinterpret_cast<const uint4 *>(rb + (((2 * j + 1) ^ r7) << 4));
+            const __nv_bfloat162 s2 = pick_group(sv[mat], j), b2 = pick_group(bv[mat], j);
+            uint32_t v[32];
+            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            if (small_scale(s2)) {  // the usual case: subnormal codes, one mask and one FMA a pair
+              const __nv_bfloat162 s2x = scale_for_subnormal_codes(s2);
 #pragma unroll
-              for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = dq_pair_subnormal(wv[wi] >> (4 * pi), s2x, b2);
-          } else {
+              for (int wi = 0; wi < 8; ++wi)
 #pragma unroll
-            for (int wi = 0; wi < 8; ++wi) {
-              uint32_t p[4];
-              dequant_word_ilv(wv[wi], s2, b2, p);
+                for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = dq_pair_subnormal(wv[wi] >> (4 * pi), s2x, b2);
+            } else {
 #pragma unroll
-              for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = p[pi];
+              for (int wi = 0; wi < 8; ++wi) {
+                uint32_t p[4];
+                dequant_word_ilv(wv[wi], s2, b2, p);
+#pragma unroll
+                for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = p[pi];
+              }
             }
+            if (mat == 0) {  // the slot's previous k-block has left the MMA
+              if (!__all_sync(0xffffffffu, timed(tr, w_free, [&] {
+                    return wait_bar(&m->free[aslot], ((kbg / NSLOT) & 1u) ^ 1u, m, a.status);
+                  }))) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+            }
+            ptx::tmem_st_x32(tmem + lane_base + A_COL + aslot * 64 + mat * 32, v);
           }
-          const int aslot = kbg % NSLOT;
-          if (!__all_sync(0xffffffffu, timed(tr, w_free, [&] {
-                return wait_bar(&m->free[aslot], ((kbg / NSLOT) & 1u) ^ 1u, m, a.status);
-              }))) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          ptx::tmem_st_x32(tmem + lane_base + A_COL + aslot * 64 + mat * 32, v);
+          if (!ok) break;
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
           ptx::mbar_arrive(&m->ready[aslot]);
