@@ -22,10 +22,12 @@
 //               of a row -> 32 bf16x2, w = bf16_rne(scale*q + bias)) straight
 //               into tensor memory with tcgen05.st, then run the epilogue:
 //               gate/up: h = bf16(silu(g) * u); down: y = bf16(acc)
-// Tensor memory (512 columns): D_gate [0,128), D_up [128,256) (down: D
-// [0,256)), four A slots of 64 columns at 256 (gate at +0, up at +32; 32
-// columns = 64 bf16 of K).  A k-block's token rows and its A slot form one
-// slot of a four-slot ring.
+// Tensor memory (512 columns), gate/up: D_gate [0,128), D_up [128,256), four
+// A slots of 64 columns at 256 (gate at +0, up at +32; 32 columns = 64 bf16
+// of K).  Down: two accumulators D0 [0,192) and D1 [192,384), so that the MMA
+// runs the next item while the epilogue drains the last one, and four A slots
+// of 32 columns at 384.  A k-block's token rows and its A slot form one slot
+// of a four-slot ring.
 // Every wait is bounded: after one second the kernel records
 // MOE_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees tensor memory
 // and exits.
@@ -49,7 +51,6 @@ constexpr int NWG = 3;                    // dequant/epilogue warpgroups
 constexpr int THREADS = 128 + NWG * 128;  // 4 role warps + the warpgroups
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int D_UP_COL = 128;
-constexpr int A_COL = 256;
 constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
 
 constexpr int SBOX = BM * 16;  // one scale (or bias) box: 128 rows x 8 groups of bf16
@@ -59,8 +60,13 @@ struct Cfg {
   static constexpr int NMAT = GATEUP ? 2 : 1;
   // Token rows per work item (the MMA's N).  Gate and up keep two fp32
   // accumulators of N columns next to the A slots in tensor memory, so N <=
-  // 128; the down GEMM has one accumulator and takes N <= 256.
-  static constexpr int MAXN = GATEUP ? 128 : 256;
+  // 128; the down GEMM keeps two accumulators of up to 192 columns.
+  static constexpr int MAXN = GATEUP ? 128 : TC_DOWN_ROWS;
+  static constexpr int NBUF = GATEUP ? 1 : 2;         // accumulators (items in flight)
+  static constexpr int D_BUF = GATEUP ? 0 : MAXN;     // columns from one accumulator to the next
+  static constexpr int A_COL = GATEUP ? 256 : 2 * MAXN;  // first A slot
+  static constexpr int A_SLOT = GATEUP ? 64 : 32;     // columns per A slot
+  static_assert(A_COL + NSLOT * A_SLOT <= (int)TMEM_COLS, "tensor memory");
   static constexpr int B_SLOT = MAXN * 128;  // one k-block of MAXN token rows
   // Code stages (4 k-blocks each, from HBM) and the k-block ring (token rows
   // in shared memory + dequantised weights in tensor memory) share the
@@ -125,7 +131,7 @@ __device__ __forceinline__ bool timed(bool on, unsigned long long &acc, F f) {
 struct Misc {
   uint64_t code_full[8], code_empty[8];
   uint64_t ready[NSLOT], free[NSLOT];
-  uint64_t acc_full, acc_empty, final_bar;
+  uint64_t acc_full[2], acc_empty[2], final_bar;  // per accumulator
   uint32_t tmem;
   int abort_flag;
 };
@@ -243,8 +249,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(&m->ready[i], 1 + 128);  // token-row TMA + the warpgroup that rebuilt the k-block
       ptx::mbar_init(&m->free[i], NISS);
     }
-    ptx::mbar_init(&m->acc_full, NISS);
-    ptx::mbar_init(&m->acc_empty, NWG * 128);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&m->acc_full[b], NISS);
+      ptx::mbar_init(&m->acc_empty[b], NWG * 128);
+    }
     ptx::mbar_init(&m->final_bar, NISS);
     m->abort_flag = 0;
     ptx::fence_mbar_init();
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t bdesc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + C::OFF_B));
       const uint32_t b_lo0 = (uint32_t)bdesc0, b_hi = (uint32_t)(bdesc0 >> 32);
       const int mat = GATEUP ? iss : 0;
-      const uint32_t a_col = tmem + A_COL + (uint32_t)(mat * 32);
+      const uint32_t a_col = tmem + C::A_COL + (uint32_t)(mat * 32);
       uint32_t kbc = 0, itc = 0;
       bool ok = true;
       Item nit = blockIdx.x < n_items ? get_item<C::MAXN>(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
@@ -343,9 +351,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           nc = iss ? it.n_mma - half : half;
         }
         const uint32_t idesc = ptx::idesc_bf16_f32((uint32_t)(nc > 0 ? nc : 16));
-        const uint32_t d = tmem + (uint32_t)(mat * D_UP_COL + c0);
+        // accumulator itc % NBUF; its previous item's epilogue must have read it
+        const uint32_t buf = itc % C::NBUF, use = itc / C::NBUF;
+        const uint32_t d = tmem + buf * C::D_BUF + (uint32_t)(mat * D_UP_COL + c0);
         const uint32_t b_lo = b_lo0 + (uint32_t)c0 * 8u;  // c0 rows of 128 B, in 16-byte units
-        if (!timed(tr, w_acc, [&] { return wait_bar(&m->acc_empty, (itc & 1u) ^ 1u, m, a.status); })) break;
+        if (!timed(tr, w_acc, [&] { return wait_bar(&m->acc_empty[buf], (use & 1u) ^ 1u, m, a.status); })) break;
         ptx::tc_fence_after();
         for (int kb = 0; kb < KB && ok; kb += NSLOT, kbc += NSLOT) {
           const uint32_t ph = (kbc / NSLOT) & 1u;
@@ -357,13 +367,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             ptx::tc_fence_after();
             if (nc > 0)
-              ptx::mma_ts_kblock(d, a_col + j * 64, b_lo + (uint32_t)(j * (C::B_SLOT >> 4)), b_hi, idesc,
+              ptx::mma_ts_kblock(d, a_col + j * C::A_SLOT, b_lo + (uint32_t)(j * (C::B_SLOT >> 4)), b_hi, idesc,
                                  (uint32_t)(kb + j));
             ptx::mma_commit(&m->free[j]);
           }
         }
         if (!ok) break;
-        ptx::mma_commit(&m->acc_full);
+        ptx::mma_commit(&m->acc_full[buf]);
         ++itc;
       }
       // every MMA this thread issued has completed before tensor memory is freed
@@ -465,6 +475,39 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     };
     if (nitem < n_items && !a.tma_scales) prefetch(nit, 0);
+    // The epilogue of item number ic (this CTA's count): chunks of 16 token
+    // columns dealt round-robin to the warpgroups, out of accumulator ic % NBUF.
+    auto epilogue = [&](const Item &ei, uint32_t ic) -> bool {
+      const uint32_t buf = ic % C::NBUF, use = ic / C::NBUF;
+      if (!__all_sync(0xffffffffu,
+                      timed(tr, w_acc, [&] { return wait_bar(&m->acc_full[buf], use & 1u, m, a.status); }))) {
+        ok = false;
+        return false;
+      }
+      ptx::tc_fence_after();
+      const uint32_t dcol = tmem + lane_base + buf * C::D_BUF;
+      // gate/up writes h in the interleaved K order of the down GEMM
+      uint16_t *orow = a.out + (size_t)ei.row0 * a.NOUT + (size_t)ei.mt * BM + (GATEUP ? ilv_pos(row) : row);
+      for (int ch = wg; ch < ei.n_mma / 16; ch += NWG) {
+        uint32_t g[16], u[16];
+        ptx::tmem_ld_x16(dcol + ch * 16, g);
+        if (GATEUP) ptx::tmem_ld_x16(dcol + D_UP_COL + ch * 16, u);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int n = ch * 16 + i;
+          if (n < ei.nrows) {
+            const float val = GATEUP ? silu(__uint_as_float(g[i])) * __uint_as_float(u[i]) : __uint_as_float(g[i]);
+            orow[(size_t)n * a.NOUT] = f32_to_bf16(val);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&m->acc_empty[buf]);
+      return true;
+    };
+    Item prev{0, 0, 0, 16, 0};
+    bool has_prev = false;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const Item it = nit;
       for (int st = 0; st < NST; ++st, ++cs) {
@@ -536,7 +579,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
               ptx::tc_fence_after();
             }
-            ptx::tmem_st_x32(tmem + lane_base + A_COL + aslot * 64 + mat * 32, v);
+            ptx::tmem_st_x32(tmem + lane_base + C::A_COL + aslot * C::A_SLOT + mat * 32, v);
           }
           if (!ok) break;
           ptx::tmem_wait_st();
@@ -549,31 +592,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
       }
       if (!ok) break;
-      // epilogue: chunks of 16 token columns dealt round-robin to the warpgroups
-      if (!__all_sync(0xffffffffu,
-                      timed(tr, w_acc, [&] { return wait_bar(&m->acc_full, itc & 1u, m, a.status); })))
-        break;
-      ptx::tc_fence_after();
-      // gate/up writes h in the interleaved K order of the down GEMM
-      uint16_t *orow = a.out + (size_t)it.row0 * a.NOUT + (size_t)it.mt * BM + (GATEUP ? ilv_pos(row) : row);
-      for (int ch = wg; ch < it.n_mma / 16; ch += NWG) {
-        uint32_t g[16], u[16];
-        ptx::tmem_ld_x16(tmem + lane_base + ch * 16, g);
-        if (GATEUP) ptx::tmem_ld_x16(tmem + lane_base + D_UP_COL + ch * 16, u);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int n = ch * 16 + i;
-          if (n < it.nrows) {
-            const float val = GATEUP ? silu(__uint_as_float(g[i])) * __uint_as_float(u[i]) : __uint_as_float(g[i]);
-            orow[(size_t)n * a.NOUT] = f32_to_bf16(val);
-          }
-        }
+      // With two accumulators the epilogue of an item runs after the next
+      // item's k-blocks have been rebuilt (the MMA has long finished it by
+      // then); with one, right away (the next item's MMAs need the
+      // accumulator back).
+      if (C::NBUF == 1) {
+        if (!epilogue(it, itc)) break;
+      } else {
+        if (has_prev && !epilogue(prev, itc - 1)) break;
+        prev = it;
+        has_prev = true;
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&m->acc_empty);
       ++itc;
     }
+    if (C::NBUF == 2 && ok && has_prev) epilogue(prev, itc - 1);
     if (tr) {
       trace_put(a, TW_DQ_CODE, w_code);
       trace_put(a, TW_DQ_FREE, w_free);

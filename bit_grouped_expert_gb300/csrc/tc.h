@@ -11,7 +11,7 @@
 namespace moe {
 
 constexpr int TC_ROWS = 128;       // default token rows per block-map tile (gate/up GEMM)
-constexpr int TC_DOWN_ROWS = 256;  // token rows per tile of the down GEMM's block map
+constexpr int TC_DOWN_ROWS = 192;  // token rows per tile of the down GEMM's block map (two accumulators fit)
 
 // The driver's cuTensorMapEncodeTiled (null when the driver lacks it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

@@ -180,7 +180,7 @@ def test_routing_is_deterministic(real):
 
 def test_default_plan_uses_tensor_core_path():
     v = Layer(max_tokens=8).view(1)
-    assert (v.block_rows, v.block_rows2) == (128, 256)
+    assert (v.block_rows, v.block_rows2) == (128, 192)
     v = Layer(max_tokens=8, flags=moe.MOE_FLAG_TILE_ROWS_64).view(1)
     assert (v.block_rows, v.block_rows2) == (64, 64)
     v = Layer(max_tokens=8, flags=moe.MOE_FLAG_SIMT_EXPERTS).view(1)
