@@ -14,7 +14,7 @@ struct Layout {
   // status, counter (the decode epoch) and dtags (the decode kernel's tagged
   // exchange words) lie below keys: moe_workspace_init zeroes [0, keys)
   size_t status, counter, dtags, keys, topk_id, topk_w, counts, offsets, perm, inv, blockmap, n_tiles, blockmap2,
-      n_tiles2, h, y, xg, rsplit, rpart, xn, trace, total;
+      n_tiles2, qctr, h, y, xg, rsplit, rpart, xn, trace, total;
 };
 
 }  // namespace moe

@@ -6,8 +6,11 @@
 // a device-built block map (one tile = up to 128 (gate/up) or 256 (down)
 // rows of one expert).
 //
-// One persistent CTA per SM walks work items (block-map tile, 128 output
-// features).  The packed weights are the MMA's A operand (M = 128 rows of
+// One persistent CTA per SM takes work items (block-map tile, 128 output
+// features) from a queue: the code producer draws the next item number from
+// a global counter (zeroed by the scatter kernel before every layer) and
+// hands its block-map entry to the CTA's other roles through a ring in shared
+// memory, so the SMs stay busy to the end whatever the tiles' sizes.  The packed weights are the MMA's A operand (M = 128 rows of
 // output features) and the tile's token rows are B (N = rows rounded up to
 // 16), so a weight tile is rebuilt once for all of an expert's tokens:
 //   warp 0      TMA: packed 4-bit codes, 128 rows x 256 codes per box, 128B
@@ -95,6 +98,7 @@ struct TcMaps {
 
 struct TcArgs {
   const int32_t *blockmap, *n_tiles;
+  int32_t *item_counter;          // next item number, zero at launch
   const uint16_t *sc[2], *bi[2];  // scale / bias arrays of the matrices
   uint16_t *out;                  // h [rows][NOUT] or y [rows][NOUT]
   int32_t *status;
@@ -128,7 +132,15 @@ __device__ __forceinline__ bool timed(bool on, unsigned long long &acc, F f) {
 // landed (the TMA bytes plus one arrival per dequant thread of each matrix);
 // free[s] when every MMA that read the slot has completed (one commit per
 // issuer).
+// Items in flight between the code producer and the other roles.
+constexpr int IRING = 8;
+// Consumers of an item-ring slot: the token loader, the MMA issuers and every
+// dequant warp.
+constexpr int ITEM_READERS = 1 + NISS + NWG * 4;
+
 struct Misc {
+  int4 item[IRING];  // (expert, first row, rows, m-tile); expert < 0: no more items
+  uint64_t item_full[IRING], item_empty[IRING];
   uint64_t code_full[8], code_empty[8];
   uint64_t ready[NSLOT], free[NSLOT];
   uint64_t acc_full[2], acc_empty[2], final_bar;  // per accumulator
@@ -140,15 +152,20 @@ struct Item {
   int e, row0, nrows, n_mma, mt;
 };
 
+// Block-map entry of item number `item` as a ring entry.
 template <int MAXN>
-__device__ __forceinline__ Item get_item(const TcArgs &a, int item, int MT) {
+__device__ __forceinline__ int4 item_entry(const TcArgs &a, int item, int MT) {
   const int tile = item / MT;
-  Item it;
-  it.mt = item - tile * MT;
   const int4 ent = reinterpret_cast<const int4 *>(a.blockmap)[tile];
+  return make_int4(ent.x, ent.y, min(ent.z, MAXN), item - tile * MT);
+}
+
+__device__ __forceinline__ Item as_item(int4 ent) {
+  Item it;
   it.e = ent.x;
   it.row0 = ent.y;
-  it.nrows = min(ent.z, MAXN);
+  it.nrows = ent.z;
+  it.mt = ent.w;
   it.n_mma = max(16, (it.nrows + 15) & ~15);
   return it;
 }
@@ -177,6 +194,19 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait(bar, parity))
     if (ptx::globaltimer() - t0 > TIMEOUT_NS) return;
+}
+
+// The n-th item of this CTA from the ring (all lanes of the calling warp, or
+// one thread with warp_wide false); false on a failed wait.
+__device__ __forceinline__ bool read_item(Misc *m, uint32_t n, int4 &ent, int32_t *status, bool warp_wide) {
+  const int s = n % IRING;
+  const bool got = wait_bar(&m->item_full[s], (n / IRING) & 1u, m, status);
+  if (warp_wide ? !__all_sync(0xffffffffu, got) : !got) return false;
+  const volatile int *src = reinterpret_cast<volatile int *>(&m->item[s]);
+  ent = make_int4(src[0], src[1], src[2], src[3]);
+  if (warp_wide) __syncwarp();
+  if (!warp_wide || (threadIdx.x & 31) == 0) ptx::mbar_arrive(&m->item_empty[s]);
+  return true;
 }
 
 // K order inside the tensor-core GEMMs.  Within every run of 8 values along
@@ -241,6 +271,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::tmem_relinquish();
   }
   if (threadIdx.x == 0) {
+    for (int i = 0; i < IRING; ++i) {
+      ptx::mbar_init(&m->item_full[i], 1);
+      ptx::mbar_init(&m->item_empty[i], ITEM_READERS);
+    }
     for (int i = 0; i < C::CSTAGES; ++i) {
       ptx::mbar_init(&m->code_full[i], 1);
       ptx::mbar_init(&m->code_empty[i], NWG * 4);
@@ -282,10 +316,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       uint32_t cs = 0;
       bool ok = true;
-      Item nit = blockIdx.x < n_items ? get_item<C::MAXN>(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const Item it = nit;  // the next item's block-map entry is loaded one item ahead
-        if (item + (int)gridDim.x < n_items) nit = get_item<C::MAXN>(a, item + gridDim.x, MT);
+      for (uint32_t n = 0; ok; ++n) {
+        // the next item from the queue, posted to the ring before its codes
+        const int s = n % IRING;
+        if (!wait_bar(&m->item_empty[s], ((n / IRING) & 1u) ^ 1u, m, a.status)) break;
+        const int idx = atomicAdd(a.item_counter, 1);
+        const int4 ent = idx < n_items ? item_entry<C::MAXN>(a, idx, MT) : make_int4(-1, 0, 0, 0);
+        m->item[s] = ent;
+        ptx::mbar_arrive(&m->item_full[s]);
+        if (ent.x < 0) break;
+        const Item it = as_item(ent);
         const int row_base = it.e * a.NOUT + it.mt * BM;
         for (int st = 0; st < NST; ++st, ++cs) {
           const int slot = cs % C::CSTAGES;
@@ -339,10 +379,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t a_col = tmem + C::A_COL + (uint32_t)(mat * 32);
       uint32_t kbc = 0, itc = 0;
       bool ok = true;
-      Item nit = blockIdx.x < n_items ? get_item<C::MAXN>(a, blockIdx.x, MT) : Item{0, 0, 0, 16, 0};
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const Item it = nit;
-        if (item + (int)gridDim.x < n_items) nit = get_item<C::MAXN>(a, item + gridDim.x, MT);
+      for (;;) {
+        int4 ent;
+        if (!read_item(m, itc, ent, a.status, false)) break;
+        if (ent.x < 0) break;
+        const Item it = as_item(ent);
         // this issuer's token columns [c0, c0 + nc)
         int c0 = 0, nc = it.n_mma;
         if (!GATEUP) {
@@ -400,8 +441,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < 4; ++i) ptx::prefetch_tmap(&maps.act[i]);
       uint32_t kbc = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const Item it = get_item<C::MAXN>(a, item, MT);
+      for (uint32_t n = 0; ok; ++n) {
+        int4 ent;
+        if (!read_item(m, n, ent, a.status, false) || ent.x < 0) break;
+        const Item it = as_item(ent);
         const CUtensorMap *mp = maps.act;
         const int rb = it.row0;
         for (int kb = 0; kb < KB; ++kb, ++kbc) {
@@ -458,12 +501,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     unsigned long long w_code = 0, w_free = 0, w_acc = 0;
     uint32_t cs = 0, kbc = 0, itc = 0;
     bool ok = true;
-    // scales/biases of the next stage are loaded one stage ahead; block-map
-    // entries two items ahead
-    int nitem = blockIdx.x;
-    Item nit = nitem < n_items ? get_item<C::MAXN>(a, nitem, MT) : Item{0, 0, 0, 16, 0};
-    Item nit2 = nitem + (int)gridDim.x < n_items ? get_item<C::MAXN>(a, nitem + gridDim.x, MT) : Item{0, 0, 0, 16, 0};
-    int nst = 0;
+    // (without scale boxes) the scales and biases of the next stage of the
+    // item are loaded one stage ahead
     uint2 nsv[C::NMAT], nbv[C::NMAT];
     auto prefetch = [&](const Item &pi, int pst) {
       const size_t grow = (size_t)pi.e * a.NOUT + (size_t)pi.mt * BM + row;
@@ -474,7 +513,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         nbv[mt] = load_groups(a.bi[mt] + grow * groups + kb0, nkb, vec);
       }
     };
-    if (nitem < n_items && !a.tma_scales) prefetch(nit, 0);
     // The epilogue of item number ic (this CTA's count): chunks of 16 token
     // columns dealt round-robin to the warpgroups, out of accumulator ic % NBUF.
     auto epilogue = [&](const Item &ei, uint32_t ic) -> bool {
@@ -508,8 +546,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     Item prev{0, 0, 0, 16, 0};
     bool has_prev = false;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const Item it = nit;
+    for (;;) {
+      int4 ent;
+      if (!read_item(m, itc, ent, a.status, true)) {
+        ok = false;
+        break;
+      }
+      if (ent.x < 0) break;
+      const Item it = as_item(ent);
+      if (!a.tma_scales) prefetch(it, 0);
       for (int st = 0; st < NST; ++st, ++cs) {
         const int kb0 = st * STAGE_KB, nkb = min(STAGE_KB, KB - kb0);
         uint2 sv[C::NMAT], bv[C::NMAT];
@@ -518,14 +563,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           sv[mt] = nsv[mt];
           bv[mt] = nbv[mt];
         }
-        // advance the prefetch cursor (next stage of this item, or stage 0 of the next item)
-        if (++nst == NST) {
-          nst = 0;
-          nitem += gridDim.x;
-          nit = nit2;
-          if (nitem + (int)gridDim.x < n_items) nit2 = get_item<C::MAXN>(a, nitem + gridDim.x, MT);
-        }
-        if (nitem < n_items && !a.tma_scales) prefetch(nit, nst);
+        if (!a.tma_scales && st + 1 < NST) prefetch(it, st + 1);
         const int cslot = cs % C::CSTAGES;
         if (!__all_sync(0xffffffffu, timed(tr, w_code, [&] {
               return wait_bar(&m->code_full[cslot], (cs / C::CSTAGES) & 1u, m, a.status);
@@ -719,8 +757,8 @@ cudaError_t tc_prepare() {
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
                               const int32_t *blockmap, const int32_t *n_tiles, int max_tiles,
                               const int32_t *blockmap2, const int32_t *n_tiles2, int max_tiles2, ExpertPtrs w,
-                              uint16_t *h, uint16_t *y, uint16_t *xg, int32_t *status, uint64_t *trace,
-                              int *launches, cudaStream_t s) {
+                              uint16_t *h, uint16_t *y, uint16_t *xg, int32_t *qctr, int32_t *status,
+                              uint64_t *trace, int *launches, cudaStream_t s) {
   const moe_config &c = plan->cfg;
   const int rows_gu = (c.n_experts + c.n_shared) * c.inter;
   const int rows_dn = (c.n_experts + c.n_shared) * c.hidden;
@@ -757,6 +795,7 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   TcArgs a{};
   a.blockmap = blockmap;
   a.n_tiles = n_tiles;
+  a.item_counter = qctr;  // gate/up's queue (the scatter kernel zeroed both)
   a.status = status;
   a.T = T;
   a.k = c.top_k;
@@ -784,6 +823,7 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.trace_base = 16;
   a.blockmap = blockmap2;
   a.n_tiles = n_tiles2;
+  a.item_counter = qctr + 1;
   a.sc[0] = w.down_s;
   a.bi[0] = w.down_b;
   a.sc[1] = w.down_s;

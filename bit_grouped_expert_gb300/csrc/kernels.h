@@ -37,7 +37,7 @@ cudaError_t launch_ids_histogram(const int32_t *ids, int T, int E, int k, int32_
 cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, int S, const int32_t *counts,
                            int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *blockmap, int32_t *n_tiles,
                            int max_tiles, int BN2, int32_t *blockmap2, int32_t *n_tiles2, int max_tiles2,
-                           int32_t *status, int debug, cudaStream_t s);
+                           int32_t *status, int debug, int32_t *qctr, cudaStream_t s);
 
 // experts_simt.cu (CUDA-core grouped GEMMs, tiles of SIMT_ROWS rows)
 constexpr int SIMT_ROWS = 32;

@@ -60,6 +60,7 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_ti
   L.n_tiles = take(16);
   L.blockmap2 = take((size_t)max_tiles2 * 16);
   L.n_tiles2 = take(16);
+  L.qctr = take(16);  // the grouped GEMMs' work-queue counters
   L.h = take((k + S) * T * I * 2);
   L.y = take((k + S) * T * H * 2);
   L.xg = take(tc ? (k + S) * T * H * 2 : 0);  // x rows gathered in block-map row order (tensor-core gate/up)
@@ -167,7 +168,8 @@ moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const fl
                                  moe::ws_ptr<int32_t>(ws, L.blockmap), moe::ws_ptr<int32_t>(ws, L.n_tiles), max_tiles,
                                  p->block_rows2, p->block_rows2 ? moe::ws_ptr<int32_t>(ws, L.blockmap2) : nullptr,
                                  moe::ws_ptr<int32_t>(ws, L.n_tiles2), max_tiles2, status,
-                                 (p->flags & MOE_FLAG_DEBUG_CHECKS) ? 1 : 0, s)) != cudaSuccess)
+                                 (p->flags & MOE_FLAG_DEBUG_CHECKS) ? 1 : 0, moe::ws_ptr<int32_t>(ws, L.qctr),
+                                 s)) != cudaSuccess)
     return cuda_status(err);
   ++*launches;
   return MOE_OK;
@@ -462,7 +464,7 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
     const int max_tiles2 = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, plan->block_rows2);
     err = moe::launch_experts_tc(plan, x, T, perm, bm, nt, max_tiles, moe::ws_ptr<int32_t>(ws_d, L.blockmap2),
                                  moe::ws_ptr<int32_t>(ws_d, L.n_tiles2), max_tiles2, ep, h, y,
-                                 moe::ws_ptr<uint16_t>(ws_d, L.xg),
+                                 moe::ws_ptr<uint16_t>(ws_d, L.xg), moe::ws_ptr<int32_t>(ws_d, L.qctr),
                                  status,
                                  (plan->flags & MOE_FLAG_TRACE) ? moe::ws_ptr<uint64_t>(ws_d, L.trace) : nullptr,
                                  &launches, s);

@@ -116,11 +116,16 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t *__restrict_
                                                       int32_t *__restrict__ inv, int32_t *__restrict__ blockmap,
                                                       int32_t *__restrict__ n_tiles, int max_tiles, int BN2,
                                                       int32_t *__restrict__ blockmap2, int32_t *__restrict__ n_tiles2,
-                                                      int max_tiles2, int32_t *__restrict__ status, int debug) {
+                                                      int max_tiles2, int32_t *__restrict__ status, int debug,
+                                                      int32_t *__restrict__ qctr) {
   __shared__ int s_a[32], s_b[32], s_c[32];
   __shared__ int s_warp[8];
   __shared__ int s_off, s_tb, s_tb2;
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (qctr && e == 0 && tid == 0) {  // the grouped GEMMs' work-queue counters start the layer at zero
+    qctr[0] = 0;
+    qctr[1] = 0;
+  }
   int off = 0, tb = 0, tb2 = 0;
   for (int i = tid; i < e; i += blockDim.x) {
     int c = counts[i];
@@ -295,11 +300,11 @@ cudaError_t launch_ids_histogram(const int32_t *ids, int T, int E, int k, int32_
 cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, int S, const int32_t *counts,
                            int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *blockmap, int32_t *n_tiles,
                            int max_tiles, int BN2, int32_t *blockmap2, int32_t *n_tiles2, int max_tiles2,
-                           int32_t *status, int debug, cudaStream_t s) {
+                           int32_t *status, int debug, int32_t *qctr, cudaStream_t s) {
   if (!blockmap2) BN2 = BN;
   prof_before(MOE_KERNEL_SCATTER, s);
   scatter_kernel<<<E, 256, 0, s>>>(topk_id, T, E, k, BN, S, counts, offsets, perm, inv, blockmap, n_tiles, max_tiles,
-                                   BN2, blockmap2, n_tiles2, max_tiles2, status, debug);
+                                   BN2, blockmap2, n_tiles2, max_tiles2, status, debug, qctr);
   prof_after(MOE_KERNEL_SCATTER, s);
   return cudaGetLastError();
 }

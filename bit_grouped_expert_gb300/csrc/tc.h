@@ -22,11 +22,13 @@ bool tc_supported(const moe_config &c);
 // One-time kernel attributes (dynamic shared memory size); needs a device.
 cudaError_t tc_prepare();
 
+// qctr: two work-queue counters (gate/up, down), zero at the launch (the
+// scatter kernel of the layer's routing zeroes them).
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
                               const int32_t *blockmap, const int32_t *n_tiles, int max_tiles,
                               const int32_t *blockmap2, const int32_t *n_tiles2, int max_tiles2, ExpertPtrs w,
-                              uint16_t *h, uint16_t *y, uint16_t *xg, int32_t *status, uint64_t *trace,
-                              int *launches, cudaStream_t s);
+                              uint16_t *h, uint16_t *y, uint16_t *xg, int32_t *qctr, int32_t *status,
+                              uint64_t *trace, int *launches, cudaStream_t s);
 
 // Router keys on tensor cores (E % 128 == 0, H % 64 == 0).
 bool router_tc_supported(int E, int H);
