@@ -119,9 +119,9 @@ __global__ void dequant_kernel(const uint32_t *__restrict__ q, const uint16_t *_
   if (i >= words) return;
   const size_t n = i / (K / 8), kw = i % (K / 8);
   const size_t g = n * (K / G) + (kw * 8) / G;
-  __nv_bfloat162 p[4];
-  dequant_word(q[i], bf16x2_splat(sc[g]), bf16x2_splat(b[g]), p);
-  *reinterpret_cast<uint4 *>(w + n * K + kw * 8) = *reinterpret_cast<uint4 *>(p);
+  uint32_t p[4];
+  dequant_word(q[i], group_scale(bf16x2_splat(sc[g]), bf16x2_splat(b[g])), p);
+  *reinterpret_cast<uint4 *>(w + n * K + kw * 8) = make_uint4(p[0], p[1], p[2], p[3]);
 }
 
 cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w,

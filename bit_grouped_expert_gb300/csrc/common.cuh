@@ -64,45 +64,74 @@ __device__ __forceinline__ bool precedes(float ka, int ia, float kb, int ib) {
 // fast reciprocal division: within 2 ulp of fp32, far below the bf16 rounding of h
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// Dequantise the 8 codes of one packed word into 4 bf16x2 pairs, each
-// w = bf16_rne(s * q + b) with one rounding (fma.rn.bf16x2 rounds the exact
-// s*q+b once).  s2/b2 hold the group's scale/bias in both halves.
-__device__ __forceinline__ void dequant_word(uint32_t word, __nv_bfloat162 s2, __nv_bfloat162 b2,
-                                             __nv_bfloat162 out[4]) {
-  // q as bf16: 0x4300 | q is 128 + q exactly; subtracting 128 is exact.
-  const uint32_t hi4 = word >> 4;
+// The rebuild of the code pairs (j, j+4), j = 0..3, of a packed word (code i
+// at bits 4i): out[j] holds w = bf16_rne(s*q + b) of code j in its low half
+// and of code j+4 in its high half.
+//
+// Usual route, for |s| < 2^-5: the bf16 bit patterns 0 .. 0x00FF are the
+// values 0 .. 255 times 2^-133 exactly (subnormals up to 0x007F, then the
+// first binade, whose step is the same), so a code masked in place -- at
+// bits 0..3 of a half (q * 2^-133) or at bits 4..7 (q * 2^-129) -- is an exact
+// bf16 operand, and with the scale taken times 2^133 or 2^129 (powers of two:
+// exact while the product stays finite, i.e. |s| < 2^-5) one fused
+// multiply-add rounds the exact s*q + b once.  A word costs one shift and four
+// ANDs for its four pairs.
+// Other scales: 0x4300 | q is the bf16 value 128 + q; subtracting 128 is
+// exact and the fused multiply-add rounds once.
+struct GroupScale {
+  __nv_bfloat162 s133, s129;  // s * 2^133, s * 2^129 (usual route)
+  __nv_bfloat162 s, b;
+  bool small;                 // |s| < 2^-5 (bf16 exponent field <= 121)
+};
+
+__device__ __forceinline__ GroupScale group_scale(__nv_bfloat162 s2, __nv_bfloat162 b2) {
+  GroupScale g;
+  g.s = s2;
+  g.b = b2;
+  g.small = (*reinterpret_cast<const uint32_t *>(&s2) & 0x7F80u) < (122u << 7);
+  g.s129 = __hmul2(__hmul2(s2, __floats2bfloat162_rn(0x1p127f, 0x1p127f)), __floats2bfloat162_rn(4.f, 4.f));
+  g.s133 = __hmul2(g.s129, __floats2bfloat162_rn(16.f, 16.f));
+  return g;
+}
+
+__device__ __forceinline__ uint32_t fma_pair(__nv_bfloat162 s2, uint32_t codes, __nv_bfloat162 b2) {
+  const __nv_bfloat162 r = __hfma2(s2, *reinterpret_cast<const __nv_bfloat162 *>(&codes), b2);
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// Usual route (g.small).
+__device__ __forceinline__ void dq_word_small(uint32_t w, const GroupScale &g, uint32_t out[4]) {
+  const uint32_t w8 = w >> 8;
+  out[0] = fma_pair(g.s133, w & 0x000F000Fu, g.b);   // codes 0, 4
+  out[1] = fma_pair(g.s129, w & 0x00F000F0u, g.b);   // codes 1, 5
+  out[2] = fma_pair(g.s133, w8 & 0x000F000Fu, g.b);  // codes 2, 6
+  out[3] = fma_pair(g.s129, w8 & 0x00F000F0u, g.b);  // codes 3, 7
+}
+
+// Any scale.
+__device__ __forceinline__ void dq_word_general(uint32_t w, const GroupScale &g, uint32_t out[4]) {
   const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    // result bytes [word.byte i, -, hi4.byte i, -]: the low nibble of byte 0 is
-    // code 2i, the low nibble of byte 2 is code 2i+1 (element 2i in the low half)
-    uint32_t t = __byte_perm(word, hi4, static_cast<uint32_t>(i | ((4 + i) << 8)));
-    t = (t & 0x000F000Fu) | 0x43004300u;
-    __nv_bfloat162 m = *reinterpret_cast<__nv_bfloat162 *>(&t);
-    __nv_bfloat162 q = __hsub2(m, k128);
-    out[i] = __hfma2(s2, q, b2);
+  for (int j = 0; j < 4; ++j) {
+    uint32_t t = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+    const __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&t), k128);
+    const __nv_bfloat162 r = __hfma2(g.s, q, g.b);
+    out[j] = *reinterpret_cast<const uint32_t *>(&r);
   }
 }
 
-// The rebuild through subnormal codes.  The bf16 pattern 0x000q is the
-// subnormal q * 2^-133 exactly, so with the scale taken times 2^133 (exact:
-// a power of two) one fused multiply-add of the masked code pair gives
-// bf16_rne(s*q + b) with a single rounding -- the same bits as the
-// 0x4300 | q route, without its OR and subtraction.  s * 2^133 stays finite
-// for |s| < 2^-5 (bf16 exponent field <= 121); larger scales take the other
-// route.
-__device__ __forceinline__ bool small_scale(__nv_bfloat162 s2) {
-  return (*reinterpret_cast<const uint32_t *>(&s2) & 0x7F80u) < (122u << 7);
-}
-__device__ __forceinline__ __nv_bfloat162 scale_for_subnormal_codes(__nv_bfloat162 s2) {
-  return __hmul2(__hmul2(s2, __floats2bfloat162_rn(0x1p127f, 0x1p127f)), __floats2bfloat162_rn(64.f, 64.f));
-}
-// Codes at bits 0..3 and 16..19 of t (other bits ignored) -> bf16x2 weights;
-// s2x from scale_for_subnormal_codes.
-__device__ __forceinline__ uint32_t dq_pair_subnormal(uint32_t t, __nv_bfloat162 s2x, __nv_bfloat162 b2) {
-  t &= 0x000F000Fu;
-  const __nv_bfloat162 r = __hfma2(s2x, *reinterpret_cast<const __nv_bfloat162 *>(&t), b2);
-  return *reinterpret_cast<const uint32_t *>(&r);
+// The 8 weights of a packed word in natural order (bf16, two per 32-bit
+// word: out[i] holds codes 2i and 2i+1), through the pair rebuild above.
+__device__ __forceinline__ void dequant_word(uint32_t w, const GroupScale &g, uint32_t out[4]) {
+  uint32_t p[4];
+  if (g.small)
+    dq_word_small(w, g, p);
+  else
+    dq_word_general(w, g, p);
+  out[0] = __byte_perm(p[0], p[1], 0x5410);
+  out[1] = __byte_perm(p[2], p[3], 0x5410);
+  out[2] = __byte_perm(p[0], p[1], 0x7632);
+  out[3] = __byte_perm(p[2], p[3], 0x7632);
 }
 
 __device__ __forceinline__ __nv_bfloat162 bf16x2_splat(uint16_t v) {

@@ -185,19 +185,10 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Codes j and j+4 of a word (nibbles j and j+4, after a shift of 4j bits) as
-// bf16_rne(s*q + bias), packed.  0x4300 | q is the bf16 value 128 + q, so one
-// subtraction and one fused multiply-add (a single rounding) rebuild the weight.
-__device__ __forceinline__ uint32_t dq(uint32_t t, __nv_bfloat162 s2, __nv_bfloat162 b2) {
-  t = (t & 0x000F000Fu) | 0x43004300u;
-  const __nv_bfloat162 m = *reinterpret_cast<__nv_bfloat162 *>(&t);
-  const __nv_bfloat162 r = __hfma2(s2, __hsub2(m, __floats2bfloat162_rn(128.f, 128.f)), b2);
-  return *reinterpret_cast<const uint32_t *>(&r);
-}
-
 // Vectors the GEMV reads (x, h) sit in shared memory in groups of 64 values,
 // XPAD slots apart, each 8-value run (one code word) stored in the order
-// p0 p4 p1 p5 | p2 p6 p3 p7: the pairs dq() yields.  perm8 takes a run in
+// p0 p4 p1 p5 | p2 p6 p3 p7: the code pairs (0,4) (2,6) (1,5) (3,7) of the
+// word's rebuild (common.cuh), as the GEMV feeds them to the MMA.  perm8 takes a run in
 // natural order (v0 = p0 p1, v1 = p2 p3, v2 = p4 p5, v3 = p6 p7) to that order.
 __device__ __forceinline__ uint4 perm8(uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
   return make_uint4(__byte_perm(v0, v2, 0x5410), __byte_perm(v0, v2, 0x7632), __byte_perm(v1, v3, 0x5410),
@@ -222,21 +213,22 @@ __device__ __forceinline__ float gemv_chunk(const uint8_t *chunk, uint16_t sv, u
   const uint2 *xp = reinterpret_cast<const uint2 *>(xg + q * XPAD) + (g & 1);
   // four accumulators: chains of two dependent MMAs
   float e[4][4] = {};
-  if (small_scale(s2)) {  // the usual case: subnormal codes (common.cuh)
-    const __nv_bfloat162 s2x = scale_for_subnormal_codes(s2);
+  const GroupScale gs = group_scale(s2, b2);
+  if (gs.small) {  // the usual route (common.cuh)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {  // word i: codes 8i..8i+7 of the group
-      const uint32_t w = wv[i];
+      uint32_t p[4];  // pairs (0,4) (1,5) (2,6) (3,7)
+      dq_word_small(wv[i], gs, p);
       const uint2 xv = xp[2 * i];
-      mma16816(e[i & 3], dq_pair_subnormal(w, s2x, b2), dq_pair_subnormal(w >> 8, s2x, b2),
-               dq_pair_subnormal(w >> 4, s2x, b2), dq_pair_subnormal(w >> 12, s2x, b2), xv.x, xv.y);
+      mma16816(e[i & 3], p[0], p[2], p[1], p[3], xv.x, xv.y);
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t w = wv[i];
+      uint32_t p[4];
+      dq_word_general(wv[i], gs, p);
       const uint2 xv = xp[2 * i];
-      mma16816(e[i & 3], dq(w, s2, b2), dq(w >> 8, s2, b2), dq(w >> 4, s2, b2), dq(w >> 12, s2, b2), xv.x, xv.y);
+      mma16816(e[i & 3], p[0], p[2], p[1], p[3], xv.x, xv.y);
     }
   }
   return ((e[0][0] + e[1][0]) + (e[2][0] + e[3][0])) + ((e[0][3] + e[1][3]) + (e[2][3] + e[3][3]));

@@ -16,15 +16,15 @@ constexpr int SB_K = 64;  // K step (one quantisation group)
 
 // Dequantise 4 consecutive words (32 codes) of one row into floats.
 __device__ __forceinline__ void dequant4_to_float(uint4 words, uint16_t s, uint16_t b, float out[32]) {
-  const __nv_bfloat162 s2 = bf16x2_splat(s), b2 = bf16x2_splat(b);
+  const GroupScale gs = group_scale(bf16x2_splat(s), bf16x2_splat(b));
   const uint32_t wv[4] = {words.x, words.y, words.z, words.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 p[4];
-    dequant_word(wv[i], s2, b2, p);
+    uint32_t p[4];
+    dequant_word(wv[i], gs, p);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float2 f = __bfloat1622float2(p[j]);
+      float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&p[j]));
       out[8 * i + 2 * j] = f.x;
       out[8 * i + 2 * j + 1] = f.y;
     }

@@ -218,21 +218,6 @@ __device__ __forceinline__ bool read_item(Misc *m, uint32_t n, int4 &ent, int32_
 //   ilv_pos(f): storage position of value f of a run.
 __device__ __forceinline__ int ilv_pos(int f) { return (f & ~7) | ((f & 3) << 1) | ((f >> 2) & 1); }
 
-// Codes (j, j+4), j = 0..3, of a word as bf16_rne(scale * q + bias) pairs
-// (one rounding: 0x4300 | q is 128 + q exactly, the subtraction is exact and
-// the fused multiply-add rounds once).
-__device__ __forceinline__ void dequant_word_ilv(uint32_t word, __nv_bfloat162 s2, __nv_bfloat162 b2,
-                                                 uint32_t out[4]) {
-  const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t t = ((word >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
-    const __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&t), k128);
-    const __nv_bfloat162 r = __hfma2(s2, q, b2);
-    out[j] = *reinterpret_cast<const uint32_t *>(&r);
-  }
-}
-
 // The bf16 values of groups g0 .. g0+n-1 of one row (n <= 4), packed two
 // per 32-bit word (group g0 in the low half of .x).
 __device__ __forceinline__ uint2 load_groups(const uint16_t *p, int n, bool vec) {
@@ -590,23 +575,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint8_t *rb = stage + mat * BOX;
             const uint4 w0 = *reinterpret_cast<const uint4 *>(rb + (((2 * j) ^ r7) << 4));
             const uint4 w1 = *reinterpret_cast<const uint4 *>(rb + (((2 * j + 1) ^ r7) << 4));
-            const __nv_bfloat162 s2 = pick_group(sv[mat], j), b2 = pick_group(bv[mat], j);
+            const GroupScale gs = group_scale(pick_group(sv[mat], j), pick_group(bv[mat], j));
             uint32_t v[32];
             const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            if (small_scale(s2)) {  // the usual case: subnormal codes, one mask and one FMA a pair
-              const __nv_bfloat162 s2x = scale_for_subnormal_codes(s2);
+            if (gs.small) {  // the usual route (common.cuh)
 #pragma unroll
-              for (int wi = 0; wi < 8; ++wi)
-#pragma unroll
-                for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = dq_pair_subnormal(wv[wi] >> (4 * pi), s2x, b2);
+              for (int wi = 0; wi < 8; ++wi) dq_word_small(wv[wi], gs, v + wi * 4);
             } else {
 #pragma unroll
-              for (int wi = 0; wi < 8; ++wi) {
-                uint32_t p[4];
-                dequant_word_ilv(wv[wi], s2, b2, p);
-#pragma unroll
-                for (int pi = 0; pi < 4; ++pi) v[wi * 4 + pi] = p[pi];
-              }
+              for (int wi = 0; wi < 8; ++wi) dq_word_general(wv[wi], gs, v + wi * 4);
             }
             if (mat == 0) {  // the slot's previous k-block has left the MMA
               if (!__all_sync(0xffffffffu, timed(tr, w_free, [&] {

@@ -94,6 +94,17 @@ def test_dequant_bit_exact():
     s[2, :] = 0x3F81
     b[2, :] = 0
     b[3, :] = 0x0001  # subnormal bias
+    # both rebuild routes and their boundary: scales below 2^-5 take the
+    # masked-code route, 2^-5 and above the 0x4300 | q route
+    s[4, :] = 0x3CFF   # largest scale of the masked-code route
+    s[5, :] = 0x3D00   # 2^-5: the other route
+    s[6, :] = 0xBCFF   # negative scale
+    s[7, :] = 0x0001   # subnormal scale
+    b[7, :] = 0x8001
+    s[8, :] = 0x3A80
+    b[8, :] = 0xBC40   # bias cancelling s*q for some codes
+    s[9, :] = 0x3C00
+    b[9, :] = 0x4B80   # bias far above s*q
     wd = torch.empty((rows, K), dtype=torch.int16, device="cuda:0")
     moe.moe_dequant(dev(q), dev(s), dev(b), rows, K, 64, wd)
     torch.cuda.synchronize()
