@@ -301,15 +301,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       uint32_t cs = 0;
       bool ok = true;
+      // Items are drawn from the queue two ahead of the one being loaded, so
+      // the counter's and the block map's round trips overlap earlier work:
+      // nxt = the next item's entry, idx2 = the number after it.
+      int idx2 = atomicAdd(a.item_counter, 1);
+      int4 nxt = idx2 < n_items ? item_entry<C::MAXN>(a, idx2, MT) : make_int4(-1, 0, 0, 0);
+      idx2 = nxt.x < 0 ? n_items : atomicAdd(a.item_counter, 1);
       for (uint32_t n = 0; ok; ++n) {
-        // the next item from the queue, posted to the ring before its codes
+        // the next item, posted to the ring before its codes
         const int s = n % IRING;
         if (!wait_bar(&m->item_empty[s], ((n / IRING) & 1u) ^ 1u, m, a.status)) break;
-        const int idx = atomicAdd(a.item_counter, 1);
-        const int4 ent = idx < n_items ? item_entry<C::MAXN>(a, idx, MT) : make_int4(-1, 0, 0, 0);
+        const int4 ent = nxt;
         m->item[s] = ent;
         ptx::mbar_arrive(&m->item_full[s]);
         if (ent.x < 0) break;
+        nxt = idx2 < n_items ? item_entry<C::MAXN>(a, idx2, MT) : make_int4(-1, 0, 0, 0);
+        if (nxt.x >= 0) idx2 = atomicAdd(a.item_counter, 1);
         const Item it = as_item(ent);
         const int row_base = it.e * a.NOUT + it.mt * BM;
         for (int st = 0; st < NST; ++st, ++cs) {
