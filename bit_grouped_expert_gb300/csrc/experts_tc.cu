@@ -7,10 +7,11 @@
 // rows of one expert).
 //
 // One persistent CTA per SM takes work items (block-map tile, 128 output
-// features) from a queue: the code producer draws the next item number from
-// a global counter (zeroed by the scatter kernel before every layer) and
-// hands its block-map entry to the CTA's other roles through a ring in shared
-// memory, so the SMs stay busy to the end whatever the tiles' sizes.  The packed weights are the MMA's A operand (M = 128 rows of
+// features): the code producer draws the next item number -- gate/up: from a
+// queue, a global counter zeroed by the scatter kernel before every layer, so
+// the SMs stay busy to the end whatever the tiles' sizes; down: round-robin --
+// and hands its block-map entry to the CTA's other roles through a ring in
+// shared memory.  The packed weights are the MMA's A operand (M = 128 rows of
 // output features) and the tile's token rows are B (N = rows rounded up to
 // 16), so a weight tile is rebuilt once for all of an expert's tokens:
 //   warp 0      TMA: packed 4-bit codes, 128 rows x 256 codes per box, 128B
@@ -21,10 +22,10 @@
 //   warp 2      TMA: the tile's token rows, contiguous in the source (x rows
 //               gathered in perm order for the routed experts, x itself for
 //               the shared expert, h for the down GEMM), 128B-swizzled
-//   warps 4-15  three warpgroups: dequantise a k-block of one matrix (64 codes
-//               of a row -> 32 bf16x2, w = bf16_rne(scale*q + bias)) straight
-//               into tensor memory with tcgen05.st, then run the epilogue:
-//               gate/up: h = bf16(silu(g) * u); down: y = bf16(acc)
+//   warps 4-19  four warpgroups: dequantise a k-block of every matrix (64
+//               codes of a row -> 32 bf16x2, w = bf16_rne(scale*q + bias))
+//               straight into tensor memory with tcgen05.st, then run the
+//               epilogue: gate/up: h = bf16(silu(g) * u); down: y = bf16(acc)
 // Tensor memory (512 columns), gate/up: D_gate [0,128), D_up [128,256), four
 // A slots of 64 columns at 256 (gate at +0, up at +32; 32 columns = 64 bf16
 // of K).  Down: two accumulators D0 [0,192) and D1 [192,384), so that the MMA
@@ -50,7 +51,7 @@ constexpr int STAGE_KB = 4;     // k-blocks per code stage (one TMA box per matr
 constexpr int BOX = BM * 128;   // one TMA box: 128 rows x 128 bytes (256 codes)
 constexpr int NSLOT = 4;        // k-block ring: A slots in tensor memory (64 columns each) + token-row slots
 constexpr int NISS = 2;         // MMA-issuing threads (warps 1 and 3)
-constexpr int NWG = 3;                    // dequant/epilogue warpgroups
+constexpr int NWG = 4;                    // dequant/epilogue warpgroups (one warp per scheduler each)
 constexpr int THREADS = 128 + NWG * 128;  // 4 role warps + the warpgroups
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int D_UP_COL = 128;
@@ -98,7 +99,7 @@ struct TcMaps {
 
 struct TcArgs {
   const int32_t *blockmap, *n_tiles;
-  int32_t *item_counter;          // next item number, zero at launch
+  int32_t *item_counter;          // next item number, zero at launch; null: items round-robin
   const uint16_t *sc[2], *bi[2];  // scale / bias arrays of the matrices
   uint16_t *out;                  // h [rows][NOUT] or y [rows][NOUT]
   int32_t *status;
@@ -304,9 +305,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Items are drawn from the queue two ahead of the one being loaded, so
       // the counter's and the block map's round trips overlap earlier work:
       // nxt = the next item's entry, idx2 = the number after it.
-      int idx2 = atomicAdd(a.item_counter, 1);
+      // With a.item_counter null the items go round-robin instead (item
+      // number blockIdx.x + n * gridDim.x), which served the down GEMM's
+      // short items better than the queue in measurements.
+      int stat = blockIdx.x;
+      auto draw = [&]() {
+        if (a.item_counter) return atomicAdd(a.item_counter, 1);
+        const int i = stat;
+        stat += gridDim.x;
+        return i;
+      };
+      int idx2 = draw();
       int4 nxt = idx2 < n_items ? item_entry<C::MAXN>(a, idx2, MT) : make_int4(-1, 0, 0, 0);
-      idx2 = nxt.x < 0 ? n_items : atomicAdd(a.item_counter, 1);
+      idx2 = nxt.x < 0 ? n_items : draw();
       for (uint32_t n = 0; ok; ++n) {
         // the next item, posted to the ring before its codes
         const int s = n % IRING;
@@ -316,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         ptx::mbar_arrive(&m->item_full[s]);
         if (ent.x < 0) break;
         nxt = idx2 < n_items ? item_entry<C::MAXN>(a, idx2, MT) : make_int4(-1, 0, 0, 0);
-        if (nxt.x >= 0) idx2 = atomicAdd(a.item_counter, 1);
+        if (nxt.x >= 0) idx2 = draw();
         const Item it = as_item(ent);
         const int row_base = it.e * a.NOUT + it.mt * BM;
         for (int st = 0; st < NST; ++st, ++cs) {
@@ -478,8 +489,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // barrier; epilogue chunks of 16 columns are dealt round-robin.
     // A slot's free barrier is waited on by phase parity, which is exact only
     // while the waiter is at most one phase ahead of the slot.  That holds
-    // here: a warpgroup's consecutive k-blocks are NWG = 3 < NSLOT apart, so
-    // its previous wait already saw the MMA past k-block kbg - 7, and every
+    // here: a warpgroup's consecutive k-blocks are NWG <= NSLOT apart, so its
+    // previous wait already saw the MMA past k-block kbg - 2 NSLOT, and every
     // warp meets the MMA at the end of each item (acc_full) before it starts
     // the next.  A different unit order, or an epilogue moved past the next
     // item's first units, must keep this.
@@ -807,7 +818,7 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.trace_base = 16;
   a.blockmap = blockmap2;
   a.n_tiles = n_tiles2;
-  a.item_counter = qctr + 1;
+  a.item_counter = nullptr;  // round-robin (qctr[1] stays unused)
   a.sc[0] = w.down_s;
   a.bi[0] = w.down_b;
   a.sc[1] = w.down_s;
