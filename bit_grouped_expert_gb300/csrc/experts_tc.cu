@@ -22,7 +22,7 @@
 //   warp 2      TMA: the tile's token rows, contiguous in the source (x rows
 //               gathered in perm order for the routed experts, x itself for
 //               the shared expert, h for the down GEMM), 128B-swizzled
-//   warps 4-19  four warpgroups: dequantise a k-block of every matrix (64
+//   warps 4-15  three warpgroups: dequantise a k-block of every matrix (64
 //               codes of a row -> 32 bf16x2, w = bf16_rne(scale*q + bias))
 //               straight into tensor memory with tcgen05.st, then run the
 //               epilogue: gate/up: h = bf16(silu(g) * u); down: y = bf16(acc)
@@ -51,7 +51,7 @@ constexpr int STAGE_KB = 4;     // k-blocks per code stage (one TMA box per matr
 constexpr int BOX = BM * 128;   // one TMA box: 128 rows x 128 bytes (256 codes)
 constexpr int NSLOT = 4;        // k-block ring: A slots in tensor memory (64 columns each) + token-row slots
 constexpr int NISS = 2;         // MMA-issuing threads (warps 1 and 3)
-constexpr int NWG = 4;                    // dequant/epilogue warpgroups (one warp per scheduler each)
+constexpr int NWG = 3;                    // dequant/epilogue warpgroups
 constexpr int THREADS = 128 + NWG * 128;  // 4 role warps + the warpgroups
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int D_UP_COL = 128;
@@ -72,18 +72,16 @@ struct Cfg {
   static constexpr int A_SLOT = GATEUP ? 64 : 32;     // columns per A slot
   static_assert(A_COL + NSLOT * A_SLOT <= (int)TMEM_COLS, "tensor memory");
   static constexpr int B_SLOT = MAXN * 128;  // one k-block of MAXN token rows
-  // Code stages (4 k-blocks each, from HBM) and the token-row ring (one
-  // k-block of the tile's rows per slot, loaded from L2 NB k-blocks ahead of
-  // the MMA -- deeper than the A ring, whose depth tensor memory bounds)
-  // share the shared memory.
-  static constexpr int CSTAGES = GATEUP ? 3 : 4;
-  static constexpr int NB = 6;
+  // Code stages (4 k-blocks each, from HBM) and the k-block ring (token rows
+  // in shared memory + dequantised weights in tensor memory) share the
+  // shared memory.
+  static constexpr int CSTAGES = 4;
   // per stage: codes of each matrix, then (scale, bias) boxes of each matrix
   static constexpr int STAGE_BYTES = NMAT * BOX + NMAT * 2 * SBOX;
   static constexpr int OFF_B = CSTAGES * STAGE_BYTES;
-  static constexpr int OFF_MISC = OFF_B + NB * B_SLOT;
+  static constexpr int OFF_MISC = OFF_B + NSLOT * B_SLOT;
   static constexpr int SMEM = OFF_MISC + 1024 /* misc */ + 1024 /* alignment slack */;
-  static_assert(CSTAGES <= 8 && NB <= 8, "barrier arrays");
+  static_assert(CSTAGES <= 8, "code_full / code_empty arrays");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -129,12 +127,12 @@ __device__ __forceinline__ bool timed(bool on, unsigned long long &acc, F f) {
   return r;
 }
 
-// Two k-block rings, indexed by the CTA's running k-block count kbg: the A
-// ring (slot kbg % NSLOT: the dequantised weights in tensor memory; ready[s]
-// completes with one arrival per thread of the warpgroup that rebuilt them,
-// free[s] when every MMA that read the slot has completed, one commit per
-// issuer) and the token-row ring (slot kbg % NB in shared memory; bready[s]
-// completes on the TMA bytes, bfree[s] like free).
+// The k-block ring: slot s holds k-block kb (s = kb % NSLOT of the CTA's
+// running k-block count) -- its token rows in shared memory and its
+// dequantised weights in tensor memory.  ready[s] completes when both have
+// landed (the TMA bytes plus one arrival per dequant thread of each matrix);
+// free[s] when every MMA that read the slot has completed (one commit per
+// issuer).
 // Items in flight between the code producer and the other roles.
 constexpr int IRING = 8;
 // Consumers of an item-ring slot: the token loader, the MMA issuers and every
@@ -146,7 +144,6 @@ struct Misc {
   uint64_t item_full[IRING], item_empty[IRING];
   uint64_t code_full[8], code_empty[8];
   uint64_t ready[NSLOT], free[NSLOT];
-  uint64_t bready[8], bfree[8];
   uint64_t acc_full[2], acc_empty[2], final_bar;  // per accumulator
   uint32_t tmem;
   int abort_flag;
@@ -269,12 +266,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(&m->code_empty[i], NWG * 4);
     }
     for (int i = 0; i < NSLOT; ++i) {
-      ptx::mbar_init(&m->ready[i], 128);  // the warpgroup that rebuilt the k-block
+      ptx::mbar_init(&m->ready[i], 1 + 128);  // token-row TMA + the warpgroup that rebuilt the k-block
       ptx::mbar_init(&m->free[i], NISS);
-    }
-    for (int i = 0; i < C::NB; ++i) {
-      ptx::mbar_init(&m->bready[i], 1);  // the token-row TMA (arrive + bytes)
-      ptx::mbar_init(&m->bfree[i], NISS);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&m->acc_full[b], NISS);
@@ -412,20 +405,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t ph = (kbc / NSLOT) & 1u;
 #pragma unroll
           for (int j = 0; j < NSLOT; ++j) {
-            const uint32_t kbg = kbc + j, bs = kbg % C::NB;
-            if (!timed(tr, w_ready, [&] {
-                  return wait_bar(&m->bready[bs], (kbg / C::NB) & 1u, m, a.status) &&
-                         wait_bar(&m->ready[j], ph, m, a.status);
-                })) {
+            if (!timed(tr, w_ready, [&] { return wait_bar(&m->ready[j], ph, m, a.status); })) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
             if (nc > 0)
-              ptx::mma_ts_kblock(d, a_col + j * C::A_SLOT, b_lo + bs * (uint32_t)(C::B_SLOT >> 4), b_hi, idesc,
+              ptx::mma_ts_kblock(d, a_col + j * C::A_SLOT, b_lo + (uint32_t)(j * (C::B_SLOT >> 4)), b_hi, idesc,
                                  (uint32_t)(kb + j));
             ptx::mma_commit(&m->free[j]);
-            ptx::mma_commit(&m->bfree[bs]);
           }
         }
         if (!ok) break;
@@ -463,31 +451,31 @@ __global__ void __launch_bounds__(THREADS, 1)
         const CUtensorMap *mp = maps.act;
         const int rb = it.row0;
         for (int kb = 0; kb < KB; ++kb, ++kbc) {
-          const int slot = kbc % C::NB;
-          if (!timed(tr, w_free, [&] { return wait_bar(&m->bfree[slot], ((kbc / C::NB) & 1u) ^ 1u, m, a.status); })) {
+          const int slot = kbc % NSLOT;
+          if (!timed(tr, w_free, [&] { return wait_bar(&m->free[slot], ((kbc / NSLOT) & 1u) ^ 1u, m, a.status); })) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&m->bready[slot], (uint32_t)it.n_mma * 128u);
+          ptx::mbar_arrive_expect_tx(&m->ready[slot], (uint32_t)it.n_mma * 128u);
           uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT;
           int r = 0;
           for (; it.n_mma - r >= 128; r += 128)
-            ptx::tma_load_2d(bs + r * 128, &mp[0], &m->bready[slot], kb * KBLK, rb + r);
+            ptx::tma_load_2d(bs + r * 128, &mp[0], &m->ready[slot], kb * KBLK, rb + r);
 #pragma unroll
           for (int i = 1; i < 4; ++i) {
             const int h = 128 >> i;
             if (it.n_mma - r >= h) {
-              ptx::tma_load_2d(bs + r * 128, &mp[i], &m->bready[slot], kb * KBLK, rb + r);
+              ptx::tma_load_2d(bs + r * 128, &mp[i], &m->ready[slot], kb * KBLK, rb + r);
               r += h;
             }
           }
         }
       }
       if (!ok) {  // the last slots' loads may still be in flight
-        const uint32_t n = kbc < (uint32_t)C::NB ? kbc : (uint32_t)C::NB;
+        const uint32_t n = kbc < (uint32_t)NSLOT ? kbc : (uint32_t)NSLOT;
         for (uint32_t i = 1; i <= n; ++i) {
           const uint32_t c = kbc - i;
-          drain_wait(&m->bready[c % C::NB], (c / C::NB) & 1u);
+          drain_wait(&m->ready[c % NSLOT], (c / NSLOT) & 1u);
         }
       }
       trace_put(a, TW_LOAD_FREE, w_free);
