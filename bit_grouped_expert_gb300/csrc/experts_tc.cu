@@ -75,11 +75,14 @@ struct Cfg {
   // Code stages (4 k-blocks each, from HBM) and the k-block ring (token rows
   // in shared memory + dequantised weights in tensor memory) share the
   // shared memory.
-  static constexpr int CSTAGES = 4;
+  static constexpr int CSTAGES = GATEUP ? 3 : 4;
   // per stage: codes of each matrix, then (scale, bias) boxes of each matrix
   static constexpr int STAGE_BYTES = NMAT * BOX + NMAT * 2 * SBOX;
   static constexpr int OFF_B = CSTAGES * STAGE_BYTES;
-  static constexpr int OFF_MISC = OFF_B + NSLOT * B_SLOT;
+  // epilogue staging: per dequant warp two buffers of 16 rows x 32 features
+  static constexpr int EPI_BUF = 16 * 32 * 2;
+  static constexpr int OFF_EPI = OFF_B + NSLOT * B_SLOT;
+  static constexpr int OFF_MISC = OFF_EPI + NWG * 4 * 2 * EPI_BUF;
   static constexpr int SMEM = OFF_MISC + 1024 /* misc */ + 1024 /* alignment slack */;
   static_assert(CSTAGES <= 8, "code_full / code_empty arrays");
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -95,6 +98,9 @@ struct TcMaps {
   // k-block (64 values) x 128 / 64 / 32 / 16 rows: h (down) or the x rows
   // gathered in block-map row order (gate/up), both in the interleaved K order
   CUtensorMap act[4];
+  // the output (h or y) as bf16 [rows][NOUT], boxes of 32 features x 16
+  // rows, for the epilogue's TMA stores (one per warp and chunk)
+  CUtensorMap out;
 };
 
 struct TcArgs {
@@ -518,6 +524,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     // The epilogue of item number ic (this CTA's count): chunks of 16 token
     // columns dealt round-robin to the warpgroups, out of accumulator ic % NBUF.
+    uint32_t epi_n = 0;  // whole chunks this warpgroup has stored by TMA
     auto epilogue = [&](const Item &ei, uint32_t ic) -> bool {
       const uint32_t buf = ic % C::NBUF, use = ic / C::NBUF;
       if (!__all_sync(0xffffffffu,
@@ -527,20 +534,39 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       ptx::tc_fence_after();
       const uint32_t dcol = tmem + lane_base + buf * C::D_BUF;
-      // gate/up writes h in the interleaved K order of the down GEMM
-      uint16_t *orow = a.out + (size_t)ei.row0 * a.NOUT + (size_t)ei.mt * BM + (GATEUP ? ilv_pos(row) : row);
+      // gate/up writes h in the interleaved K order of the down GEMM (a
+      // permutation within runs of 8, so within this warp's 32 features)
+      const int pos = GATEUP ? ilv_pos(row) : row;
       for (int ch = wg; ch < ei.n_mma / 16; ch += NWG) {
         uint32_t g[16], u[16];
         ptx::tmem_ld_x16(dcol + ch * 16, g);
         if (GATEUP) ptx::tmem_ld_x16(dcol + D_UP_COL + ch * 16, u);
         ptx::tmem_wait_ld();
+        uint16_t o[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int n = ch * 16 + i;
-          if (n < ei.nrows) {
-            const float val = GATEUP ? silu(__uint_as_float(g[i])) * __uint_as_float(u[i]) : __uint_as_float(g[i]);
-            orow[(size_t)n * a.NOUT] = f32_to_bf16(val);
+        for (int i = 0; i < 16; ++i)
+          o[i] = f32_to_bf16(GATEUP ? silu(__uint_as_float(g[i])) * __uint_as_float(u[i]) : __uint_as_float(g[i]));
+        if (ch * 16 + 16 <= ei.nrows) {
+          // a whole chunk: through this warp's staging buffer and one TMA
+          // store of 16 rows x its 32 features (the buffer used two chunks
+          // ago must have been read by its store first)
+          uint16_t *sb = reinterpret_cast<uint16_t *>(smem + C::OFF_EPI + ((warp - 4) * 2 + (epi_n & 1)) * C::EPI_BUF);
+          if (lane == 0) ptx::bulk_wait_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sb[i * 32 + (pos & 31)] = o[i];
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&maps.out, sb, ei.mt * BM + q * 32, ei.row0 + ch * 16);
+            ptx::bulk_commit();
           }
+          ++epi_n;
+        } else {  // the tile's ragged last chunk: rows past it belong to the next tile
+          uint16_t *orow = a.out + (size_t)ei.row0 * a.NOUT + (size_t)ei.mt * BM + pos;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (ch * 16 + i < ei.nrows) orow[(size_t)(ch * 16 + i) * a.NOUT] = o[i];
         }
       }
       ptx::tc_fence_before();
@@ -639,6 +665,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       ++itc;
     }
     if (C::NBUF == 2 && ok && has_prev) epilogue(prev, itc - 1);
+    if (lane == 0) ptx::bulk_wait_all();  // the epilogue's stores have landed
     if (tr) {
       trace_put(a, TW_DQ_CODE, w_code);
       trace_put(a, TW_DQ_FREE, w_free);
@@ -704,6 +731,21 @@ cudaError_t code_map(CUtensorMap *map, const uint32_t *codes, int rows_total, in
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(codes), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Output rows (h or y) as a 2D bf16 tensor [rows_total][NOUT], boxes of 32
+// features x 16 rows, no swizzle (the epilogue's staging layout).
+cudaError_t out_map(CUtensorMap *map, const uint16_t *p, int rows_total, int NOUT) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorInitializationError;
+  cuuint64_t dims[2] = {(cuuint64_t)NOUT, (cuuint64_t)rows_total};
+  cuuint64_t strides[1] = {(cuuint64_t)NOUT * 2};
+  cuuint32_t box[2] = {32, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(p), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -777,6 +819,8 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   const int rows_h = (c.top_k + c.n_shared) * T;
   for (int i = 0; i < 4; ++i)
     if ((e = act_map(&md.act[i], h, rows_h, c.inter, BM >> i)) != cudaSuccess) return e;
+  if ((e = out_map(&mg.out, h, rows_h, c.inter)) != cudaSuccess) return e;
+  if ((e = out_map(&md.out, y, rows_h, c.hidden)) != cudaSuccess) return e;
   {  // gate/up token rows by TMA from a gathered, interleaved copy of x
     for (int i = 0; i < 4; ++i)
       if ((e = act_map(&mg.act[i], xg, rows_h, c.hidden, BM >> i)) != cudaSuccess) return e;
