@@ -67,23 +67,39 @@ __device__ void topk_token(float *__restrict__ row, int E, int k, int lane, int3
                            float *__restrict__ w_out, int32_t *__restrict__ counts, int32_t *__restrict__ status,
                            KeySrc src = KeySrc{nullptr, 0, 0, nullptr}) {
   unsigned long long c[KPL];
+  float key[KPL];
+  if (src.KS > 0) {
+    // every slice's loads issued before the first sum (the sums stay in
+    // slice order; the router splits K into at most 8 slices)
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) key[i] = lane + 32 * i < E ? src.part[lane + 32 * i] : 0.f;
+#pragma unroll
+    for (int s = 1; s < 8; ++s) {
+      if (s >= src.KS) break;
+      float v[KPL];
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) v[i] = lane + 32 * i < E ? src.part[(size_t)s * src.pstride + lane + 32 * i] : 0.f;
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) key[i] += v[i];
+    }
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        if (src.bias) key[i] += src.bias[e];
+        row[e] = key[i];
+      }
+    }
+    __syncwarp();  // the stored keys are read back below
+  } else {
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) key[i] = lane + 32 * i < E ? row[lane + 32 * i] : 0.f;
+  }
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const int e = lane + 32 * i;
-    float key = 0.f;
-    if (e < E) {
-      if (src.KS > 0) {
-        key = src.part[e];
-        for (int s = 1; s < src.KS; ++s) key += src.part[(size_t)s * src.pstride + e];
-        if (src.bias) key += src.bias[e];
-        row[e] = key;
-      } else {
-        key = row[e];
-      }
-    }
-    c[i] = (e < E) ? topk_code(key, e) : 0ull;  // 0: below every real code
+    c[i] = (e < E) ? topk_code(key[i], e) : 0ull;  // 0: below every real code
   }
-  if (src.KS > 0) __syncwarp();  // the stored keys are read back below
   int my_id = -1;
   float my_key = 0.f;
   for (int r = 0; r < k; ++r) {
