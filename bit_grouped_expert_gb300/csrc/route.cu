@@ -110,7 +110,9 @@ __global__ void __launch_bounds__(256) ids_histogram_kernel(const int32_t *__res
 // One block per expert e.  offsets[e] and the first tile index of e are
 // sums over counts[0..e-1] (each block recomputes them: E values).  The
 // scatter walks tokens in ascending order, so perm is stable.
-__global__ void __launch_bounds__(256) scatter_kernel(const int32_t *__restrict__ topk_id, int T, int E, int k,
+constexpr int SCATTER_THREADS = 1024;  // 4 tokens a thread: one round covers 4096 tokens
+
+__global__ void __launch_bounds__(SCATTER_THREADS) scatter_kernel(const int32_t *__restrict__ topk_id, int T, int E, int k,
                                                       int BN, int S, const int32_t *__restrict__ counts,
                                                       int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
                                                       int32_t *__restrict__ inv, int32_t *__restrict__ blockmap,
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t *__restrict_
                                                       int max_tiles2, int32_t *__restrict__ status, int debug,
                                                       int32_t *__restrict__ qctr) {
   __shared__ int s_a[32], s_b[32], s_c[32];
-  __shared__ int s_warp[8];
+  __shared__ int s_warp[SCATTER_THREADS / 32];
   __shared__ int s_off, s_tb, s_tb2;
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   if (qctr && e == 0 && tid == 0) {  // the grouped GEMMs' work-queue counters start the layer at zero
@@ -231,8 +233,8 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t *__restrict_
     if (lane == 31) s_warp[wid] = incl;
     __syncthreads();
     int before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
+#pragma unroll 8
+    for (int w = 0; w < SCATTER_THREADS / 32; ++w) {
       const int cw = s_warp[w];
       before += (w < wid) ? cw : 0;
       total += cw;
@@ -303,7 +305,7 @@ cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, 
                            int32_t *status, int debug, int32_t *qctr, cudaStream_t s) {
   if (!blockmap2) BN2 = BN;
   prof_before(MOE_KERNEL_SCATTER, s);
-  scatter_kernel<<<E, 256, 0, s>>>(topk_id, T, E, k, BN, S, counts, offsets, perm, inv, blockmap, n_tiles, max_tiles,
+  scatter_kernel<<<E, SCATTER_THREADS, 0, s>>>(topk_id, T, E, k, BN, S, counts, offsets, perm, inv, blockmap, n_tiles, max_tiles,
                                    BN2, blockmap2, n_tiles2, max_tiles2, status, debug, qctr);
   prof_after(MOE_KERNEL_SCATTER, s);
   return cudaGetLastError();
