@@ -28,7 +28,9 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
   return make_uint4(u[0], u[1], u[2], u[3]);
 }
 
-// One block per token; each thread owns 8 consecutive columns.
+// One block per token; each thread owns 8 consecutive columns.  KMAX >= k:
+// the rows' loads are all in flight before the sums.
+template <int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ res, const uint16_t *__restrict__ y,
                                                       const int32_t *__restrict__ inv,
                                                       const float *__restrict__ topk_w, const uint16_t *__restrict__ x,
@@ -68,15 +70,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
   }
   __syncthreads();
   for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    // every row's 16 bytes are requested before the first sum; the sums then
+    // run in the fixed order
+    uint4 yv[KMAX];
+    const uint4 rv = *reinterpret_cast<const uint4 *>(res + (size_t)t * H + c);
+    const uint4 sv = S ? *reinterpret_cast<const uint4 *>(y + ((size_t)k * T + t) * H + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) yv[j] = *reinterpret_cast<const uint4 *>(y + (size_t)s_row[j] * H + c);
     float acc[8], v[8];
-    unpack8(*reinterpret_cast<const uint4 *>(res + (size_t)t * H + c), acc);
+    unpack8(rv, acc);
     if (S) {
-      unpack8(*reinterpret_cast<const uint4 *>(y + ((size_t)k * T + t) * H + c), v);
+      unpack8(sv, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(gsh, v[i], acc[i]);
     }
-    for (int j = 0; j < k; ++j) {
-      unpack8(*reinterpret_cast<const uint4 *>(y + (size_t)s_row[j] * H + c), v);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j >= k) break;
+      unpack8(yv[j], v);
       const float wj = s_w[j];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
@@ -128,7 +140,10 @@ cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t
                            const uint16_t *x, const float *shared_gate, int T, int H, int k, int S, uint16_t *out,
                            cudaStream_t s) {
   prof_before(MOE_KERNEL_COMBINE, s);
-  combine_kernel<<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out);
+  if (k <= 8)
+    combine_kernel<8><<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out);
+  else
+    combine_kernel<16><<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out);
   prof_after(MOE_KERNEL_COMBINE, s);
   return cudaGetLastError();
 }
