@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t *__re
 // With part != null the keys are first summed from the router's KS K-slice
 // partial sums ([KS][T][E], in slice order, + bias) and stored to keys.
 template <int KPL>
-__global__ void __launch_bounds__(64) topk_kernel(float *__restrict__ keys, int T, int E, int k,
+__global__ void __launch_bounds__(256) topk_kernel(float *__restrict__ keys, int T, int E, int k,
                                                    int32_t *__restrict__ topk_id, float *__restrict__ topk_w,
                                                    int32_t *__restrict__ counts, int32_t *__restrict__ status,
                                                    const float *__restrict__ part, int KS,
@@ -271,11 +271,13 @@ cudaError_t launch_router_logits(const uint16_t *x, int T, int H, const float *r
 
 cudaError_t launch_topk(float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
                         int32_t *status, const float *part, int KS, const float *bias, cudaStream_t s) {
-  // two tokens (warps) per block, so small T still spreads over many SMs
-  const int blocks = (T + 1) / 2;
+  // a warp per token: eight tokens per block, or two when T is small (so
+  // that small T still spreads over many SMs)
+  const int tpb = T >= 1024 ? 8 : 2;
+  const int blocks = (T + tpb - 1) / tpb;
   const int kpl = (E + 31) / 32;
   prof_before(MOE_KERNEL_TOPK, s);
-#define MOE_TOPK(K) topk_kernel<K><<<blocks, 64, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status, part, KS, bias)
+#define MOE_TOPK(K) topk_kernel<K><<<blocks, 32 * tpb, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status, part, KS, bias)
   if (kpl <= 1)
     MOE_TOPK(1);
   else if (kpl <= 2)
