@@ -77,11 +77,13 @@ __global__ void __launch_bounds__(256) topk_kernel(float *__restrict__ keys, int
                                                    int32_t *__restrict__ counts, int32_t *__restrict__ status,
                                                    const float *__restrict__ part, int KS,
                                                    const float *__restrict__ bias) {
+  // per warp: the candidates (up to 256 codes) and the k picked ones
+  __shared__ unsigned long long s_cand[KPL <= 8 ? 8 : 1][KPL <= 8 ? 256 + 16 : 1];
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
   if (warp >= T) return;
   const KeySrc src{part ? part + (size_t)warp * E : nullptr, (size_t)T * E, part ? KS : 0, bias};
   topk_token<KPL>(keys + (size_t)warp * E, E, k, lane, topk_id + (size_t)warp * k, topk_w + (size_t)warp * k,
-                  counts, status, src);
+                  counts, status, src, KPL <= 8 ? s_cand[threadIdx.x / 32] : nullptr);
 }
 
 // Histogram of given expert ids ([T][k]); ids outside [0, E) are not counted

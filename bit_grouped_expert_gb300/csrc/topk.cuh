@@ -60,12 +60,14 @@ struct KeySrc {
   const float *bias;
 };
 
-// One warp selects a token's top k (k <= 32) from E <= 32*KPL keys.  Lane l
-// holds experts l, l+32, ...; each round takes the warp-wide largest code.
+// One warp selects a token's top k (k <= 16) from E <= 32*KPL keys.  Lane l
+// holds experts l, l+32, ...
+// cand (KPL <= 8): a warp-private shared buffer of 256 + 16 codes; null: k
+// rounds of a warp-wide maximum instead.
 template <int KPL>
 __device__ void topk_token(float *__restrict__ row, int E, int k, int lane, int32_t *__restrict__ ids_out,
                            float *__restrict__ w_out, int32_t *__restrict__ counts, int32_t *__restrict__ status,
-                           KeySrc src = KeySrc{nullptr, 0, 0, nullptr}) {
+                           KeySrc src = KeySrc{nullptr, 0, 0, nullptr}, unsigned long long *cand = nullptr) {
   unsigned long long c[KPL];
   float key[KPL];
   if (src.KS > 0) {
@@ -102,18 +104,55 @@ __device__ void topk_token(float *__restrict__ row, int E, int k, int lane, int3
   }
   int my_id = -1;
   float my_key = 0.f;
-  for (int r = 0; r < k; ++r) {
-    unsigned long long best = c[0];
+  if (KPL <= 8 && cand != nullptr) {
+    // Threshold, then rank.  tau = the k-th largest of the 32 lane maxima's
+    // key bits (k rounds of a warp maximum, each dropping the lanes that hold
+    // it): k distinct keys reach it, so every selected key is at or above it.
+    // The codes at or above it -- k of them, a few more when lanes hold
+    // several large keys, all E when every key is equal -- are ranked against
+    // one another; rank r < k is slot r.
+    unsigned long long m = c[0];
 #pragma unroll
-    for (int i = 1; i < KPL; ++i) best = c[i] > best ? c[i] : best;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = shfl_xor_u64(best, o);
-      best = other > best ? other : best;
+    for (int i = 1; i < KPL; ++i) m = c[i] > m ? c[i] : m;
+    uint32_t v = (uint32_t)(m >> 32), t = 0u;
+    for (int r = 0; r < k; ++r) {
+      t = __reduce_max_sync(0xffffffffu, v);
+      if (v == t) v = 0u;
     }
+    const unsigned long long tau = (unsigned long long)t << 32;
+    int n = 0;
+    const unsigned below = (1u << lane) - 1u;
 #pragma unroll
-    for (int i = 0; i < KPL; ++i) c[i] = (c[i] == best) ? 0ull : c[i];  // the owner drops it
-    if (r == lane) my_id = topk_code_expert(best);
+    for (int i = 0; i < KPL; ++i) {
+      const bool take = c[i] != 0ull && c[i] >= tau;
+      const unsigned b = __ballot_sync(0xffffffffu, take);
+      if (take) cand[n + __popc(b & below)] = c[i];
+      n += __popc(b);
+    }
+    __syncwarp();
+    for (int q = lane; q < n; q += 32) {
+      const unsigned long long cq = cand[q];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += cand[j] > cq;
+      if (rank < k) cand[256 + rank] = cq;  // slot order
+    }
+    __syncwarp();
+    if (lane < k) my_id = topk_code_expert(cand[256 + lane]);
+    __syncwarp();
+  } else {
+    for (int r = 0; r < k; ++r) {
+      unsigned long long best = c[0];
+#pragma unroll
+      for (int i = 1; i < KPL; ++i) best = c[i] > best ? c[i] : best;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = shfl_xor_u64(best, o);
+        best = other > best ? other : best;
+      }
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) c[i] = (c[i] == best) ? 0ull : c[i];  // the owner drops it
+      if (r == lane) my_id = topk_code_expert(best);
+    }
   }
   if (lane < k) my_key = row[my_id];
   topk_finish(lane, k, my_id, my_key, ids_out, w_out, counts, status);
