@@ -105,9 +105,6 @@ def parse():
                     help="token rows per grouped-GEMM tile (64: MOE_FLAG_TILE_ROWS_64)")
     ap.add_argument("--generator", default=None, choices=["centred", "literal"],
                     help="weight generator of a prefill workload (default: the workload's own)")
-    ap.add_argument("--codes", default="paired", choices=["paired", "pages"],
-                    help="code order of the packed weights: paired (moe_pair_codes once per weight set, the "
-                         "grouped GEMM reads token rows straight from x) or the pages' packing (gathered copy of x)")
     ap.add_argument("--no-extras", action="store_true",
                     help="prefill32k: leave out the literal-generator, decode and single-layer lines")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -219,13 +216,10 @@ def gpu_id(device):
 class WeightCache:
     """Packed weights of the stack's layers on the device, generated on the
     host once per (seed, layer, generator) and shared by the workloads of one
-    run; each layer is prepared once as a loader would: the router's bf16
-    parts (moe_router_split) and, with paired codes, the code words rewritten
-    in place (moe_pair_codes)."""
+    run; each layer also gets the router's bf16 parts (moe_router_split) once."""
 
-    def __init__(self, device, paired=True):
+    def __init__(self, device):
         self.device = device
-        self.paired = paired
         self.layers = {}
 
     def get(self, seed, layer, centred):
@@ -246,8 +240,6 @@ class WeightCache:
                 out[n] = torch.from_numpy(a).to(self.device)
             out["router_split"] = torch.empty(moe.moe_router_split_bytes(E, H), dtype=torch.uint8, device=self.device)
             moe.moe_router_split(out["router"], E, H, out["router_split"])
-            if self.paired:
-                out = moe.pair_weights(out)
             self.layers[key] = out
         return self.layers[key]
 
@@ -277,7 +269,7 @@ def run_ours(args, wl, rank, world, device, cache=None, steps=None, warmup=None,
     steps = args.steps if steps is None else steps
     warmup = args.warmup if warmup is None else warmup
     name = args.workload if name is None else name
-    cache = cache or WeightCache(device, paired=args.codes == "paired")
+    cache = cache or WeightCache(device)
     T, L, chunk = wl["T"], wl["layers"], wl["chunk"]
     flags = moe.MOE_FLAG_SIMT_EXPERTS if args.experts == "simt" else 0
     if args.tile_rows == 64:
@@ -893,8 +885,7 @@ def main():
                        "l2": (f"{GDN_SETS} distinct input sets cycled (~50 MB each, larger than L2 together)"
                               if "Hv" in wl else f"{wl.get('sets')} distinct KV caches cycled" if "Hkv" in wl
                               else "inputs larger than L2 (packed weights >= 455 MB per layer)"),
-                       "experts": args.experts,
-                       "codes": (args.codes if "Hv" not in wl and "Hkv" not in wl else None)}}
+                       "experts": args.experts}}
     if args.impl == "reference":
         if rank != 0:
             return
@@ -916,7 +907,7 @@ def main():
             __graft_entry__.build()
         if world > 1:
             torch.distributed.barrier()
-        cache = WeightCache(device, paired=args.codes == "paired")
+        cache = WeightCache(device)
         res = run_ours(args, wl, rank, world, device, cache=cache)
         extras = None
         if args.workload == "prefill32k" and not args.no_extras and args.layers is None and args.generator is None:

@@ -34,14 +34,12 @@ MOE_FLAG_TILE_ROWS_64 = 0x8
 MOE_FLAG_PRENORM = 0x10
 MOE_FLAG_TRACE = 0x20
 MOE_FLAG_TEST_WITHHOLD = 0x40
-MOE_CODES_PAGES = 0
-MOE_CODES_PAIRED = 1
 MOE_TRACE_CTAS = 256
 MOE_TRACE_SLOTS = 32
 
 EXPORTS = ("moe_plan", "moe_plan_destroy", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_route_from_logits", "moe_route_from_ids", "moe_forward", "moe_prefill_stack", "moe_router_split_bytes",
-           "moe_router_split", "moe_pair_codes", "moe_route_view", "moe_rmsnorm", "moe_dequant",
+           "moe_router_split", "moe_route_view", "moe_rmsnorm", "moe_dequant",
            "moe_device_status", "moe_last_launch_count", "moe_status_str", "moe_profile_events", "moe_profile_stride",
            "moe_last_cuda_error",
            "moe_decode_static", "moe_decode_stack", "gdn_scan", "attn_decode_workspace_bytes", "attn_decode")
@@ -77,7 +75,7 @@ class moe_config(ctypes.Structure):
 class moe_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("router_d", "gate_q_d", "up_q_d", "gate_s_d", "gate_b_d", "up_s_d",
                                                "up_b_d", "down_q_d", "down_s_d", "down_b_d", "shared_gate_d",
-                                               "router_split_d")] + [("code_order", ctypes.c_int32)]
+                                               "router_split_d")]
 
 
 class moe_route_ptrs(ctypes.Structure):
@@ -127,9 +125,7 @@ def lib():
         L.moe_rmsnorm.restype = i32
         L.moe_rmsnorm.argtypes = [vp, i32, i32, f32, vp, vp]
         L.moe_dequant.restype = i32
-        L.moe_dequant.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
-        L.moe_pair_codes.restype = i32
-        L.moe_pair_codes.argtypes = [vp, vp, sz, vp]
+        L.moe_dequant.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
         L.moe_device_status.restype = i32
         L.moe_device_status.argtypes = [vp, vp, vp, ctypes.POINTER(i32), i32]
         L.moe_last_launch_count.restype = i32
@@ -223,10 +219,9 @@ def moe_workspace_init(plan: Plan, ws, stream=None):
 
 def make_weights(w: dict) -> moe_weights:
     """moe_weights from a dict of device tensors (keys: router, gate_q, ...;
-    shared_gate and router_split optional; code_order an int, default
-    MOE_CODES_PAGES).  The caller keeps the tensors alive."""
-    ptrs = [_ptr(w.get(n[:-2])) for n, _ in moe_weights._fields_[:-1]]
-    return moe_weights(*ptrs, int(w.get("code_order", MOE_CODES_PAGES)))
+    shared_gate and router_split optional).  The caller keeps the tensors
+    alive."""
+    return moe_weights(*[_ptr(w.get(n[:-2])) for n, _ in moe_weights._fields_])
 
 
 def moe_route(plan: Plan, x, T: int, router, logit_bias, ws, stream=None):
@@ -253,24 +248,6 @@ def moe_router_split(router, E: int, H: int, split, stream=None):
     moe_router_split_bytes(E, H) bytes), for the ``router_split`` weight."""
     _check("moe_router_split", lib().moe_router_split(_ptr(router), int(E), int(H), _ptr(split), _nbytes(split),
                                                       _stream(stream)))
-
-
-def moe_pair_codes(src, dst, n_words: int, stream=None):
-    """Rewrite packed code words into the paired order (moe_weights.code_order
-    = MOE_CODES_PAIRED); dst may be src (in place)."""
-    _check("moe_pair_codes", lib().moe_pair_codes(_ptr(src), _ptr(dst), int(n_words), _stream(stream)))
-
-
-def pair_weights(w: dict, stream=None) -> dict:
-    """The weights dict with its three code arrays rewritten in place into the
-    paired order and code_order set (the tensors of w are modified)."""
-    if int(w.get("code_order", MOE_CODES_PAGES)) == MOE_CODES_PAIRED:
-        return w
-    for n in ("gate_q", "up_q", "down_q"):
-        moe_pair_codes(w[n], w[n], w[n].numel(), stream)
-    out = dict(w)
-    out["code_order"] = MOE_CODES_PAIRED
-    return out
 
 
 def _weights_array(weights):
@@ -367,9 +344,9 @@ def moe_rmsnorm(r, T: int, H: int, eps: float, x, stream=None):
     _check("moe_rmsnorm", lib().moe_rmsnorm(_ptr(r), int(T), int(H), float(eps), _ptr(x), _stream(stream)))
 
 
-def moe_dequant(q, s, b, rows: int, K: int, G: int, w, stream=None, code_order: int = MOE_CODES_PAGES):
-    _check("moe_dequant", lib().moe_dequant(_ptr(q), _ptr(s), _ptr(b), int(rows), int(K), int(G), int(code_order),
-                                            _ptr(w), _stream(stream)))
+def moe_dequant(q, s, b, rows: int, K: int, G: int, w, stream=None):
+    _check("moe_dequant", lib().moe_dequant(_ptr(q), _ptr(s), _ptr(b), int(rows), int(K), int(G), _ptr(w),
+                                            _stream(stream)))
 
 
 def moe_device_status(plan: Plan, ws, stream=None, reset: bool = True) -> int:

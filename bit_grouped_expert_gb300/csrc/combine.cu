@@ -125,15 +125,14 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t *__restrict
 
 // One thread per packed word (8 weights).
 __global__ void dequant_kernel(const uint32_t *__restrict__ q, const uint16_t *__restrict__ sc,
-                               const uint16_t *__restrict__ b, int rows, int K, int G, int paired,
-                               uint16_t *__restrict__ w) {
+                               const uint16_t *__restrict__ b, int rows, int K, int G, uint16_t *__restrict__ w) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t words = (size_t)rows * (K / 8);
   if (i >= words) return;
   const size_t n = i / (K / 8), kw = i % (K / 8);
   const size_t g = n * (K / G) + (kw * 8) / G;
   uint32_t p[4];
-  dequant_word(q[i], group_scale(bf16x2_splat(sc[g]), bf16x2_splat(b[g])), p, paired != 0);
+  dequant_word(q[i], group_scale(bf16x2_splat(sc[g]), bf16x2_splat(b[g])), p);
   *reinterpret_cast<uint4 *>(w + n * K + kw * 8) = make_uint4(p[0], p[1], p[2], p[3]);
 }
 
@@ -157,35 +156,10 @@ cudaError_t launch_rmsnorm(const uint16_t *r, int T, int H, float eps, uint16_t 
 }
 
 cudaError_t launch_dequant(const uint32_t *q, const uint16_t *sc, const uint16_t *b, int rows, int K, int G,
-                           int paired, uint16_t *w, cudaStream_t s) {
+                           uint16_t *w, cudaStream_t s) {
   const size_t words = (size_t)rows * (K / 8);
   const unsigned blocks = (unsigned)((words + 255) / 256);
-  dequant_kernel<<<blocks, 256, 0, s>>>(q, sc, b, rows, K, G, paired, w);
-  return cudaGetLastError();
-}
-
-// The paired order (moe_pair_codes): codes 2m and 2m+1 of a word move to bits
-// 4m and 4m+16, so that the pair rebuild (common.cuh) gives consecutive
-// weights; src may equal dst (each thread rewrites its own words).
-__global__ void pair_codes_kernel(const uint32_t *src, uint32_t *dst, size_t n) {
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const uint32_t w = src[i];
-    uint32_t o = 0;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      o |= ((w >> (8 * m)) & 0xFu) << (4 * m);            // code 2m
-      o |= ((w >> (8 * m + 4)) & 0xFu) << (4 * m + 16);   // code 2m + 1
-    }
-    dst[i] = o;
-  }
-}
-
-cudaError_t launch_pair_codes(const uint32_t *src, uint32_t *dst, size_t n, int num_sms, cudaStream_t s) {
-  if (n == 0) return cudaSuccess;
-  size_t blocks = (n + 255) / 256;
-  const size_t cap = (size_t)num_sms * 8;
-  if (blocks > cap) blocks = cap;
-  pair_codes_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, n);
+  dequant_kernel<<<blocks, 256, 0, s>>>(q, sc, b, rows, K, G, w);
   return cudaGetLastError();
 }
 

@@ -64,11 +64,9 @@ __device__ __forceinline__ bool precedes(float ka, int ia, float kb, int ib) {
 // fast reciprocal division: within 2 ulp of fp32, far below the bf16 rounding of h
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// The rebuild of the code pairs at bits (4j, 4j+16), j = 0..3, of a packed
-// word: out[j] holds w = bf16_rne(s*q + b) of the code at bits 4j in its low
-// half and of the code at bits 4j+16 in its high half.  In the pages' packing
-// (code i at bits 4i) these are the pairs (j, j+4); in the paired order
-// (moe_pair_codes: codes 2m, 2m+1 at bits 4m, 4m+16) they are (2j, 2j+1).
+// The rebuild of the code pairs (j, j+4), j = 0..3, of a packed word (code i
+// at bits 4i): out[j] holds w = bf16_rne(s*q + b) of code j in its low half
+// and of code j+4 in its high half.
 //
 // Usual route, for |s| < 2^-5: the bf16 bit patterns 0 .. 0x00FF are the
 // values 0 .. 255 times 2^-133 exactly (subnormals up to 0x007F, then the
@@ -123,19 +121,13 @@ __device__ __forceinline__ void dq_word_general(uint32_t w, const GroupScale &g,
 }
 
 // The 8 weights of a packed word in natural order (bf16, two per 32-bit
-// word: out[i] holds codes 2i and 2i+1), through the pair rebuild above;
-// paired: the word is in the paired order, whose pairs come out in order.
-__device__ __forceinline__ void dequant_word(uint32_t w, const GroupScale &g, uint32_t out[4], bool paired) {
+// word: out[i] holds codes 2i and 2i+1), through the pair rebuild above.
+__device__ __forceinline__ void dequant_word(uint32_t w, const GroupScale &g, uint32_t out[4]) {
   uint32_t p[4];
   if (g.small)
     dq_word_small(w, g, p);
   else
     dq_word_general(w, g, p);
-  if (paired) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) out[i] = p[i];
-    return;
-  }
   out[0] = __byte_perm(p[0], p[1], 0x5410);
   out[1] = __byte_perm(p[2], p[3], 0x5410);
   out[2] = __byte_perm(p[0], p[1], 0x7632);

@@ -186,14 +186,11 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // Vectors the GEMV reads (x, h) sit in shared memory in groups of 64 values,
-// XPAD slots apart, each 8-value run (one code word) stored in the order of
-// the word's four rebuilt pairs (common.cuh) -- the pairs at bits (0,16),
-// (4,20) | (8,24), (12,28) -- as the GEMV feeds them to the MMA.  With the
-// pages' packing those are values p0 p4 p1 p5 | p2 p6 p3 p7; with paired
-// codes p0 p1 p2 p3 | p4 p5 p6 p7, the natural order.  perm8 takes a run in
+// XPAD slots apart, each 8-value run (one code word) stored in the order
+// p0 p4 p1 p5 | p2 p6 p3 p7: the code pairs (0,4) (2,6) (1,5) (3,7) of the
+// word's rebuild (common.cuh), as the GEMV feeds them to the MMA.  perm8 takes a run in
 // natural order (v0 = p0 p1, v1 = p2 p3, v2 = p4 p5, v3 = p6 p7) to that order.
-__device__ __forceinline__ uint4 perm8(uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3, bool paired) {
-  if (paired) return make_uint4(v0, v1, v2, v3);
+__device__ __forceinline__ uint4 perm8(uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
   return make_uint4(__byte_perm(v0, v2, 0x5410), __byte_perm(v0, v2, 0x7632), __byte_perm(v1, v3, 0x5410),
                     __byte_perm(v1, v3, 0x7632));
 }
@@ -202,9 +199,8 @@ __device__ __forceinline__ uint4 perm8(uint32_t v0, uint32_t v1, uint32_t v2, ui
 // image of the chunk; sv, bv: the scale and bias of this lane's group (row g,
 // group q of the chunk); xg: the chunk's first group of the permuted vector.  Lane (g, q) takes
 // group q of the chunk in row g; the weights are the A operand: rows g and
-// g+8 of A are the rebuilt pairs 0, 1 and 2, 3 of a word of row g (codes
-// {j, j+4 : j = 0, 1} and {j, j+4 : j = 2, 3} in the pages' packing, codes
-// 0..3 and 4..7 when paired), and B columns 0 and 1 (lanes g = 0 and 1) carry the matching x
+// g+8 of A are codes {j, j+4 : j = 0, 1} and {j, j+4 : j = 2, 3} of a word of
+// row g, and B columns 0 and 1 (lanes g = 0 and 1) carry the matching x
 // values, so D[g][0] + D[g+8][1] sums row g over the 32 values of the word
 // and its three quad partners.  Returns row g's sum in the lanes with q == 0.
 __device__ __forceinline__ float gemv_chunk(const uint8_t *chunk, uint16_t sv, uint16_t bv, const uint16_t *xg, int g,
@@ -221,7 +217,7 @@ __device__ __forceinline__ float gemv_chunk(const uint8_t *chunk, uint16_t sv, u
   if (gs.small) {  // the usual route (common.cuh)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {  // word i: codes 8i..8i+7 of the group
-      uint32_t p[4];  // the word's four rebuilt pairs
+      uint32_t p[4];  // pairs (0,4) (1,5) (2,6) (3,7)
       dq_word_small(wv[i], gs, p);
       const uint2 xv = xp[2 * i];
       mma16816(e[i & 3], p[0], p[2], p[1], p[3], xv.x, xv.y);
@@ -661,7 +657,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
           // lanes 2c and 2c+1 hold the halves of word c: swap one register
           const bool odd = (lane & 1) != 0;
           const uint32_t got2 = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
-          const uint4 pw = odd ? perm8(got2, got2, lo, hi, L.w.paired) : perm8(lo, hi, got2, got2, L.w.paired);
+          const uint4 pw = odd ? perm8(got2, got2, lo, hi) : perm8(lo, hi, got2, got2);
           *reinterpret_cast<uint2 *>(xs + (i >> 4) * XPAD + (i & 15) * 4) =
               odd ? make_uint2(pw.z, pw.w) : make_uint2(pw.x, pw.y);
         }
@@ -670,7 +666,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
       for (int i = tid; i < H / 8; i += DTHREADS) {
         const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.xin) + i);
         reinterpret_cast<uint4 *>(xn)[i] = v;
-        *reinterpret_cast<uint4 *>(xs + (i >> 3) * XPAD + (i & 7) * 8) = perm8(v.x, v.y, v.z, v.w, L.w.paired);
+        *reinterpret_cast<uint4 *>(xs + (i >> 3) * XPAD + (i & 7) * 8) = perm8(v.x, v.y, v.z, v.w);
       }
     }
     __syncthreads();
@@ -829,11 +825,11 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_layer_kernel(const __grid_
           gotw = poll_tagged(thb, idx, w, ep, a.status, a.timeout_ns);
           if (!gotw) break;
           *reinterpret_cast<uint4 *>(hs + (u >> 3) * XPAD + (u & 7) * 8) =
-              perm8((uint32_t)w[0], (uint32_t)w[1], (uint32_t)w[2], (uint32_t)w[3], L.w.paired);
+              perm8((uint32_t)w[0], (uint32_t)w[1], (uint32_t)w[2], (uint32_t)w[3]);
           if (v >= 0) {
             const int u2 = u + DTHREADS;
             *reinterpret_cast<uint4 *>(hs + (u2 >> 3) * XPAD + (u2 & 7) * 8) =
-                perm8((uint32_t)w[4], (uint32_t)w[5], (uint32_t)w[6], (uint32_t)w[7], L.w.paired);
+                perm8((uint32_t)w[4], (uint32_t)w[5], (uint32_t)w[6], (uint32_t)w[7]);
           }
         }
       }

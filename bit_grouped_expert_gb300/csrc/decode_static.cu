@@ -73,8 +73,7 @@ moe_status device_setup(DeviceState **out) {
 
 bool present(const moe_weights *w) {
   return w->router_d && w->gate_q_d && w->up_q_d && w->gate_s_d && w->gate_b_d && w->up_s_d && w->up_b_d &&
-         w->down_q_d && w->down_s_d && w->down_b_d &&
-         (w->code_order == MOE_CODES_PAGES || w->code_order == MOE_CODES_PAIRED);
+         w->down_q_d && w->down_s_d && w->down_b_d;
 }
 
 bool aligned(const moe_weights *w) {
@@ -139,7 +138,6 @@ extern "C" moe_status moe_decode_static(const moe_config *cfg, const void *x_d, 
   ep.down_s = w->down_s_d;
   ep.down_b = w->down_b_d;
   ep.shared_gate = w->shared_gate_d;
-  ep.paired = w->code_order == MOE_CODES_PAIRED ? 1 : 0;
   const uint16_t *x = static_cast<const uint16_t *>(x_d);
   const uint16_t *res = residual_d ? static_cast<const uint16_t *>(residual_d) : x;
   uint8_t *sc = d->scratch;

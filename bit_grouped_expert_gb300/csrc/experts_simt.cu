@@ -15,13 +15,13 @@ constexpr int SB_N = 64;  // output features per block
 constexpr int SB_K = 64;  // K step (one quantisation group)
 
 // Dequantise 4 consecutive words (32 codes) of one row into floats.
-__device__ __forceinline__ void dequant4_to_float(uint4 words, uint16_t s, uint16_t b, float out[32], bool paired) {
+__device__ __forceinline__ void dequant4_to_float(uint4 words, uint16_t s, uint16_t b, float out[32]) {
   const GroupScale gs = group_scale(bf16x2_splat(s), bf16x2_splat(b));
   const uint32_t wv[4] = {words.x, words.y, words.z, words.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t p[4];
-    dequant_word(wv[i], gs, p, paired);
+    dequant_word(wv[i], gs, p);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&p[j]));
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256) grouped_simt_kernel(const uint16_t *__res
       const size_t gi = (size_t)(n0 + f) * (K / 64) + k0 / 64;
       const uint16_t s = (m ? sb : sa)[gi], b = (m ? bb : ba)[gi];
       float vals[32];
-      dequant4_to_float(*reinterpret_cast<const uint4 *>(q), s, b, vals, w.paired != 0);
+      dequant4_to_float(*reinterpret_cast<const uint4 *>(q), s, b, vals);
       float(*dst)[SB_N + 4] = m ? wb : wa;
 #pragma unroll
       for (int i = 0; i < 32; ++i) dst[32 * half + i][f] = vals[i];

@@ -19,10 +19,9 @@
 //   warps 1, 3  one thread each issues tcgen05.mma (A from tensor memory, B
 //               from shared memory, D fp32 in tensor memory) and commits;
 //               warp 3 also allocates and frees the tensor memory
-//   warp 2      the tile's token rows, 128B-swizzled: down: h rows by TMA
-//               (contiguous); gate/up with paired codes: x rows straight from
-//               x by row index (cp.async, 16 bytes a lane); gate/up with the
-//               pages' packing: a gathered copy of x by TMA
+//   warp 2      TMA: the tile's token rows, contiguous in the source (x rows
+//               gathered in perm order for the routed experts, x itself for
+//               the shared expert, h for the down GEMM), 128B-swizzled
 //   warps 4-15  three warpgroups: dequantise a k-block of every matrix (64
 //               codes of a row -> 32 bf16x2, w = bf16_rne(scale*q + bias))
 //               straight into tensor memory with tcgen05.st, then run the
@@ -84,7 +83,7 @@ struct Cfg {
   static constexpr int EPI_BUF = 16 * 32 * 2;
   static constexpr int OFF_EPI = OFF_B + NSLOT * B_SLOT;
   static constexpr int OFF_MISC = OFF_EPI + NWG * 4 * 2 * EPI_BUF;
-  static constexpr int SMEM = OFF_MISC + 2048 /* misc */ + 1024 /* alignment slack */;
+  static constexpr int SMEM = OFF_MISC + 1024 /* misc */ + 1024 /* alignment slack */;
   static_assert(CSTAGES <= 8, "code_full / code_empty arrays");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -96,9 +95,8 @@ struct TcMaps {
   CUtensorMap sc[2];
   CUtensorMap bi[2];
   // token rows: a bf16 tensor [rows][K] with 128B-swizzled boxes of one
-  // k-block (64 values) x 128 / 64 / 32 / 16 rows: h (down) or, for codes in
-  // the pages' packing, the x rows gathered in block-map row order (gate/up)
-  // in the interleaved K order (unused when gate/up reads x directly)
+  // k-block (64 values) x 128 / 64 / 32 / 16 rows: h (down) or the x rows
+  // gathered in block-map row order (gate/up), both in the interleaved K order
   CUtensorMap act[4];
   // the output (h or y) as bf16 [rows][NOUT], boxes of 32 features x 16
   // rows, for the epilogue's TMA stores (one per warp and chunk)
@@ -113,12 +111,6 @@ struct TcArgs {
   int32_t *status;
   int T, k, E, K, NOUT;           // K: reduction length; NOUT: output features per expert
   int tma_scales;                 // scales/biases staged by TMA (K % 512 == 0)
-  // gate/up with paired codes: the token rows come straight from x [T][K]
-  // (row p of the block map is token perm[p] / k, or p - k*T for the shared
-  // expert), in natural K order; h is written in natural order too.
-  const uint16_t *x;
-  const int32_t *perm;
-  int direct;
   // Optional wait accounting (tracing aid): per CTA, cycles each role spent
   // in its barrier waits and in total, at trace[cta * 32 + trace_base + i].
   uint64_t *trace;
@@ -161,10 +153,7 @@ struct Misc {
   uint64_t acc_full[2], acc_empty[2], final_bar;  // per accumulator
   uint32_t tmem;
   int abort_flag;
-  uint32_t row_off[128];  // direct token rows: offset of each tile row's token in x, 16-byte units
 };
-
-static_assert(sizeof(Misc) <= 2048, "the misc block of shared memory");
 
 struct Item {
   int e, row0, nrows, n_mma, mt;
@@ -227,14 +216,13 @@ __device__ __forceinline__ bool read_item(Misc *m, uint32_t n, int4 &ent, int32_
   return true;
 }
 
-// K order inside the tensor-core GEMMs.  The rebuild (common.cuh) turns the
-// codes at bits (4j, 4j+16) of a word into one bf16 pair.  With the pages'
-// packing (code i at bits 4i) that is the pair (j, j+4), so within every run
-// of 8 values along K the operands are stored as (0,4), (1,5), (2,6), (3,7)
-// pairs and the token rows (x gathered, h written by the gate/up epilogue)
-// are stored in the same order, so the MMA sums exactly the same products.
-// With paired codes the pairs are (2j, 2j+1): natural order throughout.
-//   ilv_pos(f): storage position of value f of a run (pages' packing).
+// K order inside the tensor-core GEMMs.  Within every run of 8 values along
+// K the operands are stored as (0,4), (1,5), (2,6), (3,7) pairs: a packed code
+// word holds code i at bits 4i, so the pair (j, j+4) sits at bits 4j and
+// 4j+16 and comes out with one shift and one and-or, and the token rows (x
+// gathered, h written by the gate/up epilogue) are stored in the same order,
+// so the MMA sums exactly the same products.
+//   ilv_pos(f): storage position of value f of a run.
 __device__ __forceinline__ int ilv_pos(int f) { return (f & ~7) | ((f & 3) << 1) | ((f >> 2) & 1); }
 
 // The bf16 values of groups g0 .. g0+n-1 of one row (n <= 4), packed two
@@ -284,9 +272,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(&m->code_empty[i], NWG * 4);
     }
     for (int i = 0; i < NSLOT; ++i) {
-      // the token rows (one TMA arrival, or one cp.async arrival per lane of
-      // the loader warp) + the warpgroup that rebuilt the k-block
-      ptx::mbar_init(&m->ready[i], (a.direct ? 32 : 1) + 128);
+      ptx::mbar_init(&m->ready[i], 1 + 128);  // token-row TMA + the warpgroup that rebuilt the k-block
       ptx::mbar_init(&m->free[i], NISS);
     }
     for (int b = 0; b < 2; ++b) {
@@ -430,8 +416,6 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             ptx::tc_fence_after();
-            // rows written by cp.async (generic proxy) before the MMA reads them (async proxy)
-            if (GATEUP && a.direct) ptx::fence_proxy_async_smem();
             if (nc > 0)
               ptx::mma_ts_kblock(d, a_col + j * C::A_SLOT, b_lo + (uint32_t)(j * (C::B_SLOT >> 4)), b_hi, idesc,
                                  (uint32_t)(kb + j));
@@ -449,60 +433,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       trace_put(a, TW_MMA_READY, w_ready);
       trace_put(a, TW_MMA_TOTAL, (unsigned long long)(clock64() - t_start));
       trace_put(a, TW_ITEMS, itc);
-    }
-  } else if (warp == 2 && GATEUP && a.direct) {
-    // ------------------------------------------------------------ token rows straight from x
-    // Paired codes: x's natural K order is the MMA's, so the tile's rows come
-    // from x by row index, 16 bytes a lane (cp.async), into the 128B-swizzled
-    // K-major layout: chunk c of row r lands at r * 128 + ((c ^ (r & 7)) << 4).
-    // Lane l takes chunk l & 7 of rows l / 8 + 4 i.  Rows past the tile (up
-    // to the MMA's N) repeat its first row: they feed columns the epilogue
-    // never stores.  Each lane's arrival on ready[] fires once its copies of
-    // the k-block have landed.
-    const bool tr = a.trace != nullptr && lane == 0;
-    const long long t_start = clock64();
-    unsigned long long w_free = 0;
-    const int c = lane & 7, r0 = lane >> 3;
-    const char *xb = reinterpret_cast<const char *>(a.x);
-    uint32_t kbc = 0;
-    bool ok = true;
-    for (uint32_t n = 0; ok; ++n) {
-      int4 ent;
-      if (!read_item(m, n, ent, a.status, true) || ent.x < 0) break;
-      const Item it = as_item(ent);
-      for (int r = lane; r < it.n_mma; r += 32) {
-        const int p = it.row0 + (r < it.nrows ? r : 0);
-        const int t = it.e < a.E ? __ldg(a.perm + p) / a.k : p - a.k * a.T;
-        m->row_off[r] = (uint32_t)t * (uint32_t)(a.K / 8);
-      }
-      __syncwarp();
-      const int rows4 = it.n_mma >> 2;  // rows per lane
-      for (int kb = 0; kb < KB; ++kb, ++kbc) {
-        const int slot = kbc % NSLOT;
-        if (!__all_sync(0xffffffffu, timed(tr, w_free, [&] {
-              return wait_bar(&m->free[slot], ((kbc / NSLOT) & 1u) ^ 1u, m, a.status);
-            }))) {
-          ok = false;
-          break;
-        }
-        const uint32_t bs = ptx::smem_u32(smem + C::OFF_B + slot * C::B_SLOT);
-        const char *src = xb + kb * 128 + c * 16;
-        // row r = r0 + 4 i: (r & 7) alternates between r0 and r0 + 4
-        const uint32_t d0 = bs + r0 * 128 + ((c ^ r0) << 4), d1 = bs + (r0 + 4) * 128 + ((c ^ (r0 + 4)) << 4);
-#pragma unroll 4
-        for (int i = 0; i < rows4; i += 2) {
-          const int r = r0 + 4 * i;
-          ptx::cp_async_16_full(d0 + i * 512, src + ((size_t)m->row_off[r] << 4));
-          ptx::cp_async_16_full(d1 + i * 512, src + ((size_t)m->row_off[r + 4] << 4));
-        }
-        ptx::cp_async_arrive_noinc(&m->ready[slot]);
-      }
-      __syncwarp();  // every lane is past its reads of row_off before the next item rewrites it
-    }
-    ptx::cp_async_wait_all();  // nothing of this warp is still landing when the CTA winds down
-    if (tr) {
-      trace_put(a, TW_LOAD_FREE, w_free);
-      trace_put(a, TW_LOAD_TOTAL, (unsigned long long)(clock64() - t_start));
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ token-row TMA
@@ -604,10 +534,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       ptx::tc_fence_after();
       const uint32_t dcol = tmem + lane_base + buf * C::D_BUF;
-      // gate/up writes h in the down GEMM's K order: with the pages' packing
-      // the interleaved order (a permutation within runs of 8, so within this
-      // warp's 32 features), with paired codes the natural one
-      const int pos = (GATEUP && !a.direct) ? ilv_pos(row) : row;
+      // gate/up writes h in the interleaved K order of the down GEMM (a
+      // permutation within runs of 8, so within this warp's 32 features)
+      const int pos = GATEUP ? ilv_pos(row) : row;
       for (int ch = wg; ch < ei.n_mma / 16; ch += NWG) {
         uint32_t g[16], u[16];
         ptx::tmem_ld_x16(dcol + ch * 16, g);
@@ -892,7 +821,7 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
     if ((e = act_map(&md.act[i], h, rows_h, c.inter, BM >> i)) != cudaSuccess) return e;
   if ((e = out_map(&mg.out, h, rows_h, c.inter)) != cudaSuccess) return e;
   if ((e = out_map(&md.out, y, rows_h, c.hidden)) != cudaSuccess) return e;
-  if (!w.paired) {  // gate/up token rows by TMA from a gathered, interleaved copy of x
+  {  // gate/up token rows by TMA from a gathered, interleaved copy of x
     for (int i = 0; i < 4; ++i)
       if ((e = act_map(&mg.act[i], xg, rows_h, c.hidden, BM >> i)) != cudaSuccess) return e;
     prof_before(MOE_KERNEL_GATHER, s);
@@ -922,9 +851,6 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.K = c.hidden;
   a.NOUT = c.inter;
   a.tma_scales = ts_gu;
-  a.x = x;
-  a.perm = perm;
-  a.direct = w.paired ? 1 : 0;  // paired codes: token rows straight from x
   int items = max_tiles * (c.inter / BM);
   int grid = items < plan->num_sms ? items : plan->num_sms;
   prof_before(MOE_KERNEL_GATEUP, s);
@@ -945,7 +871,6 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.K = c.inter;
   a.NOUT = c.hidden;
   a.tma_scales = ts_dn;
-  a.direct = 0;
   items = max_tiles2 * (c.hidden / BM);
   grid = items < plan->num_sms ? items : plan->num_sms;
   prof_before(MOE_KERNEL_DOWN, s);

@@ -21,7 +21,6 @@ struct ExpertPtrs {
   const uint16_t *gate_s = nullptr, *gate_b = nullptr, *up_s = nullptr, *up_b = nullptr, *down_s = nullptr,
                  *down_b = nullptr;
   const float *shared_gate = nullptr;  // [H] fp32 or null: the shared expert's output is scaled by sigmoid(x . gate)
-  int paired = 0;  // 1: the codes are in the paired order (MOE_CODES_PAIRED), 0: the pages' packing
 };
 
 // route.cu
@@ -55,8 +54,7 @@ cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t
                            cudaStream_t s);
 cudaError_t launch_rmsnorm(const uint16_t *r, int T, int H, float eps, uint16_t *x, cudaStream_t s);
 cudaError_t launch_dequant(const uint32_t *q, const uint16_t *sc, const uint16_t *b, int rows, int K, int G,
-                           int paired, uint16_t *w, cudaStream_t s);
-cudaError_t launch_pair_codes(const uint32_t *src, uint32_t *dst, size_t n, int num_sms, cudaStream_t s);
+                           uint16_t *w, cudaStream_t s);
 
 // decode.cu (T == 1: one cooperative launch runs whole layers)
 // The decode kernel's scratch: the fp32 router keys and the top-k of the last

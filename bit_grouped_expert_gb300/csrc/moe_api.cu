@@ -99,8 +99,7 @@ bool weights_aligned(const moe_weights *w) {
 
 bool weights_present(const moe_weights *w) {
   return w->router_d && w->gate_q_d && w->up_q_d && w->gate_s_d && w->gate_b_d && w->up_s_d && w->up_b_d &&
-         w->down_q_d && w->down_s_d && w->down_b_d &&
-         (w->code_order == MOE_CODES_PAGES || w->code_order == MOE_CODES_PAIRED);
+         w->down_q_d && w->down_s_d && w->down_b_d;
 }
 
 moe_status check_call(const moe_plan_t *p, int32_t T, const void *ws, size_t ws_bytes) {
@@ -188,7 +187,6 @@ moe::ExpertPtrs expert_ptrs(const moe_weights *w) {
   e.down_s = w->down_s_d;
   e.down_b = w->down_b_d;
   e.shared_gate = w->shared_gate_d;
-  e.paired = w->code_order == MOE_CODES_PAIRED ? 1 : 0;
   return e;
 }
 
@@ -560,21 +558,6 @@ moe_status moe_router_split(const float *router_d, int32_t E, int32_t H, void *s
   return cuda_status(err);
 }
 
-moe_status moe_pair_codes(const uint32_t *src_d, uint32_t *dst_d, size_t n_words, void *stream) {
-  g_last_launches = 0;
-  if (!src_d || !dst_d) return MOE_ERR_INVALID_ARGUMENT;
-  if (!moe::aligned16(src_d) || !moe::aligned16(dst_d)) return MOE_ERR_MISALIGNED;
-  const uintptr_t a = reinterpret_cast<uintptr_t>(src_d), b = reinterpret_cast<uintptr_t>(dst_d);
-  const uintptr_t len = (uintptr_t)n_words * 4u;
-  if (a != b && a < b + len && b < a + len) return MOE_ERR_INVALID_ARGUMENT;  // partial overlap
-  int dev = 0, sms = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (err == cudaSuccess) err = moe::launch_pair_codes(src_d, dst_d, n_words, sms > 0 ? sms : 1, static_cast<cudaStream_t>(stream));
-  g_last_launches = n_words ? 1 : 0;
-  return cuda_status(err);
-}
-
 moe_status moe_route_view(const moe_plan_t *plan, void *ws_d, int32_t T, moe_route_ptrs *out) {
   if (!plan || !ws_d || !out) return MOE_ERR_INVALID_ARGUMENT;
   if (T < 1) return MOE_ERR_INVALID_ARGUMENT;
@@ -616,13 +599,12 @@ moe_status moe_rmsnorm(const void *r_d, int32_t T, int32_t H, float eps, void *x
 }
 
 moe_status moe_dequant(const uint32_t *q_d, const uint16_t *s_d, const uint16_t *b_d, int32_t rows, int32_t K,
-                       int32_t G, int32_t code_order, void *w_d, void *stream) {
+                       int32_t G, void *w_d, void *stream) {
   g_last_launches = 0;
   if (!q_d || !s_d || !b_d || !w_d || rows < 1 || K < 8) return MOE_ERR_INVALID_ARGUMENT;
-  if (code_order != MOE_CODES_PAGES && code_order != MOE_CODES_PAIRED) return MOE_ERR_INVALID_ARGUMENT;
   if (G != 64 || K % G) return MOE_ERR_UNSUPPORTED;
   if (!moe::aligned16(q_d) || !moe::aligned16(w_d)) return MOE_ERR_MISALIGNED;
-  cudaError_t err = moe::launch_dequant(q_d, s_d, b_d, rows, K, G, code_order, static_cast<uint16_t *>(w_d),
+  cudaError_t err = moe::launch_dequant(q_d, s_d, b_d, rows, K, G, static_cast<uint16_t *>(w_d),
                                         static_cast<cudaStream_t>(stream));
   g_last_launches = 1;
   return cuda_status(err);

@@ -124,9 +124,6 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_16_full(uint32_t dst_smem, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Arrive on an mbarrier once every prior cp.async of this thread has landed
 // (the arrival counts against the barrier's expected count).

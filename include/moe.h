@@ -70,7 +70,6 @@ typedef struct {
 
 /* Packed expert weights, device pointers, experts stacked 0..E+S-1:
  *   gate_q, up_q   uint32 [E+S][I][H/8]   8 codes per word, code k at bits 4*(k%8)
- *                  (code_order MOE_CODES_PAGES; see code_order below)
  *   gate_s, gate_b, up_s, up_b  bf16 [E+S][I][H/G]  scale and bias per group
  *   down_q         uint32 [E+S][H][I/8]
  *   down_s, down_b bf16   [E+S][H][I/G]
@@ -85,14 +84,7 @@ typedef struct {
  * router_split_d (optional): the router as three bf16 parts, [3][E][H]
  * (hi, mid, lo; moe_router_split writes them once per set of weights).  The
  * tensor-core router (T >= 32) reads them instead of splitting router_d on
- * every call; the keys are the same bit for bit.  NULL: split per call.
- * code_order: the order of the 8 codes inside every packed word of gate_q,
- * up_q and down_q -- MOE_CODES_PAGES (0, the pages' packing above) or
- * MOE_CODES_PAIRED (1, written once per set of weights by moe_pair_codes).
- * Both give the same results bit for bit.  With paired codes the grouped
- * tensor-core GEMM reads the token rows straight from x by row index; with
- * the pages' packing it first gathers a (k+1)T x H copy of x in the order its
- * weight rebuild produces.  Any other value: MOE_ERR_INVALID_ARGUMENT. */
+ * every call; the keys are the same bit for bit.  NULL: split per call. */
 typedef struct {
   const float *router_d;
   const uint32_t *gate_q_d, *up_q_d;
@@ -101,11 +93,7 @@ typedef struct {
   const uint16_t *down_s_d, *down_b_d;
   const float *shared_gate_d;
   const uint16_t *router_split_d;
-  int32_t code_order;
 } moe_weights;
-
-#define MOE_CODES_PAGES  0  /* code k of a word at bits 4*(k%8) */
-#define MOE_CODES_PAIRED 1  /* codes 2m and 2m+1 of a word at bits 4m and 4m+16, m = 0..3 */
 
 /* Device pointers into a workspace, for tests and tools (moe_route_view). */
 typedef struct {
@@ -263,17 +251,6 @@ size_t moe_router_split_bytes(int32_t E, int32_t H);
 moe_status moe_router_split(const float *router_d, int32_t E, int32_t H, void *split_d, size_t split_bytes,
                             void *stream);
 
-/* Rewrite packed code words from the pages' packing (code k of a word at
- * bits 4*(k%8)) to the paired order (codes 2m and 2m+1 at bits 4m and 4m+16),
- * for moe_weights.code_order = MOE_CODES_PAIRED.  The rebuild of the
- * "Prefill" section then turns one masked pair of a word into two
- * consecutive weights, so activations need no reordering.  src_d, dst_d:
- * uint32 [n_words] device arrays, 16-byte aligned; dst_d may equal src_d (in
- * place) but may not otherwise overlap it.  Enqueued on stream; run once per
- * code array (gate_q, up_q, down_q).  The map is a permutation of the
- * nibbles; applying it to paired words does not undo it. */
-moe_status moe_pair_codes(const uint32_t *src_d, uint32_t *dst_d, size_t n_words, void *stream);
-
 /* Device pointers of the workspace's routing buffers for T tokens (host-side
  * arithmetic only; nothing is read or enqueued). */
 moe_status moe_route_view(const moe_plan_t *plan, void *ws_d, int32_t T, moe_route_ptrs *out);
@@ -286,10 +263,9 @@ moe_status moe_rmsnorm(const void *r_d, int32_t T, int32_t H, float eps, void *x
 
 /* Dequantise one packed matrix to bf16 (test hook for the rebuild step of
  * "Prefill"):  w_d[n][k] = bf16_rne(s[n][k/G] * q + b[n][k/G]).
- * q_d: uint32 [rows][K/8] in code_order (MOE_CODES_PAGES or
- * MOE_CODES_PAIRED); s_d, b_d: bf16 [rows][K/G]; w_d: bf16 [rows][K]. */
+ * q_d: uint32 [rows][K/8]; s_d, b_d: bf16 [rows][K/G]; w_d: bf16 [rows][K]. */
 moe_status moe_dequant(const uint32_t *q_d, const uint16_t *s_d, const uint16_t *b_d, int32_t rows,
-                       int32_t K, int32_t G, int32_t code_order, void *w_d, void *stream);
+                       int32_t K, int32_t G, void *w_d, void *stream);
 
 /* Synchronises the stream, reads the workspace's sticky status word into
  * *host_status, and (if reset != 0) zeroes it.  The only entry point that

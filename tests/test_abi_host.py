@@ -121,8 +121,6 @@ def test_forward_argument_errors_enqueue_nothing(lib):
     assert status_of(weights={**W, "down_q": None}) == moe.MOE_ERR_INVALID_ARGUMENT
     assert status_of(weights={**W, "up_s": W["up_s"] + 2}) == moe.MOE_ERR_MISALIGNED
     assert status_of(logit_bias=0x50000004) == moe.MOE_ERR_MISALIGNED
-    assert status_of(weights={**W, "code_order": 2}) == moe.MOE_ERR_INVALID_ARGUMENT
-    assert status_of(weights={**W, "code_order": -1}) == moe.MOE_ERR_INVALID_ARGUMENT
     assert moe.moe_last_launch_count() == 0
 
 
@@ -147,7 +145,6 @@ def test_decode_stack_argument_errors(lib):
     assert status_of(Ws=({**W, "down_s": W["down_s"] + 4}, W)) == moe.MOE_ERR_MISALIGNED
     assert status_of(bias=[None, 0x50000004]) == moe.MOE_ERR_MISALIGNED
     assert status_of(w=_FakeTensor(0x10000000, need - 1)) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
-    assert status_of(Ws=(W, {**W, "code_order": 3})) == moe.MOE_ERR_INVALID_ARGUMENT
     with pytest.raises(ValueError):
         moe.moe_decode_stack(plan, 0x20000000, [W, W], [None], ws, stream=0)
     assert moe.moe_last_launch_count() == 0
@@ -189,17 +186,6 @@ def test_other_entry_point_errors(lib):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_dequant(0x1004, 0x2000, 0x3000, 4, 128, 64, 0x4000, stream=0)
     assert ei.value.status == moe.MOE_ERR_MISALIGNED
-    with pytest.raises(moe.MoeError) as ei:
-        moe.moe_dequant(0x1000, 0x2000, 0x3000, 4, 128, 64, 0x4000, stream=0, code_order=2)
-    assert ei.value.status == moe.MOE_ERR_INVALID_ARGUMENT
-    # moe_pair_codes: null, misaligned and partly overlapping arrays
-    for args, want in (((None, 0x2000, 64), moe.MOE_ERR_INVALID_ARGUMENT),
-                       ((0x1000, 0x2004, 64), moe.MOE_ERR_MISALIGNED),
-                       ((0x1000, 0x1010, 64), moe.MOE_ERR_INVALID_ARGUMENT),
-                       ((0x1010, 0x1000, 64), moe.MOE_ERR_INVALID_ARGUMENT)):
-        with pytest.raises(moe.MoeError) as ei:
-            moe.moe_pair_codes(*args, stream=0)
-        assert ei.value.status == want, args
     assert moe.status_str(moe.MOE_ERR_NONFINITE) == "non-finite router key"
 
 
