@@ -8,6 +8,10 @@
 
 namespace moe {
 
+// (token, slot) pairs per block of the scatter kernel; the top-k and the
+// given-ids histogram count the pairs of every such chunk per expert.
+constexpr int SCATTER_ENT = 2048;
+
 // ----------------------------------------------------------------- plan
 
 struct Layout {

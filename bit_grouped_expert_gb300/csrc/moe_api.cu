@@ -52,7 +52,8 @@ moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_ti
   L.keys = take(T * E * 4);
   L.topk_id = take(T * k * 4);
   L.topk_w = take(T * k * 4);
-  L.counts = take(E * 4);
+  // the histogram, then one per chunk of SCATTER_ENT (token, slot) pairs (the scatter kernel's blocks)
+  L.counts = take((1 + (k * T + moe::SCATTER_ENT - 1) / moe::SCATTER_ENT) * E * 4);
   L.offsets = take((E + 1) * 4);
   L.perm = take(k * T * 4);
   L.inv = take(k * T * 4);
@@ -134,7 +135,8 @@ moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const fl
   float *keys = moe::ws_ptr<float>(ws, L.keys);
   int32_t *status = moe::ws_ptr<int32_t>(ws, L.status);
   int32_t *counts = moe::ws_ptr<int32_t>(ws, L.counts);
-  cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts, s);
+  const size_t chunks = ((size_t)T * c.top_k + moe::SCATTER_ENT - 1) / moe::SCATTER_ENT;
+  cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts * (1 + chunks), s);
   if (err != cudaSuccess) return cuda_status(err);
   const float *part = nullptr;  // the tensor-core router's K-slice partial sums, when it splits K
   int ks = 0;

@@ -5,10 +5,12 @@
 //
 //   router_logits_kernel   keys[t][e] = fp32(x[t] . router[e]) (+ bias[e])
 //   topk_kernel            per token: k best keys, softmax weights, histogram
-//   scatter_kernel         per expert: offset (scan of the histogram), stable
-//                          scatter of its pairs (perm / inv) and its block-map
-//                          tiles; the last expert's block also appends the
-//                          shared expert's tiles.
+//                          (over all pairs and per chunk of SCATTER_ENT pairs)
+//   scatter_kernel         per chunk of pairs: the experts' offsets (scan of the
+//                          histogram), stable ranks of the chunk's pairs and
+//                          their scatter (perm / inv); the blocks share the
+//                          block-map tiles out by expert, the shared expert's
+//                          tiles last.
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
@@ -77,16 +79,19 @@ __global__ void __launch_bounds__(256) topk_kernel(float *__restrict__ keys, int
                                                    int32_t *__restrict__ counts, int32_t *__restrict__ status,
                                                    const float *__restrict__ part, int KS,
                                                    const float *__restrict__ bias) {
+  // counts[0 .. E) is the histogram, then one histogram per chunk of pairs
   // per warp: the candidates (up to 256 codes) and the k picked ones
   __shared__ unsigned long long s_cand[KPL <= 8 ? 8 : 1][KPL <= 8 ? 256 + 16 : 1];
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
   if (warp >= T) return;
   const KeySrc src{part ? part + (size_t)warp * E : nullptr, (size_t)T * E, part ? KS : 0, bias};
   topk_token<KPL>(keys + (size_t)warp * E, E, k, lane, topk_id + (size_t)warp * k, topk_w + (size_t)warp * k,
-                  counts, status, src, KPL <= 8 ? s_cand[threadIdx.x / 32] : nullptr);
+                  counts, status, src, KPL <= 8 ? s_cand[threadIdx.x / 32] : nullptr, counts + E,
+                  (size_t)warp * k);
 }
 
-// Histogram of given expert ids ([T][k]); ids outside [0, E) are not counted
+// Histogram of given expert ids ([T][k]), over all pairs and per chunk of
+// SCATTER_ENT pairs (as the top-k kernel); ids outside [0, E) are not counted
 // and set MOE_ERR_DEVICE_BOUNDS; with debug, so does an expert named twice
 // by one token.
 __global__ void __launch_bounds__(256) ids_histogram_kernel(const int32_t *__restrict__ ids, int T, int E, int k,
@@ -102,6 +107,7 @@ __global__ void __launch_bounds__(256) ids_histogram_kernel(const int32_t *__res
       continue;
     }
     atomicAdd(&counts[e], 1);
+    atomicAdd(&counts[(size_t)E + (((size_t)t * k + j) / SCATTER_ENT) * E + e], 1);  // the pair's chunk
     if (debug)
       for (int i = 0; i < j; ++i)
         if (row[i] == e) set_status(status, MOE_ERR_DEVICE_BOUNDS);
@@ -109,155 +115,174 @@ __global__ void __launch_bounds__(256) ids_histogram_kernel(const int32_t *__res
 }
 
 // ---------------------------------------------------------------- scatter
-// One block per expert e.  offsets[e] and the first tile index of e are
-// sums over counts[0..e-1] (each block recomputes them: E values).  The
-// scatter walks tokens in ascending order, so perm is stable.
-constexpr int SCATTER_THREADS = 1024;  // 4 tokens a thread: one round covers 4096 tokens
+// One block per chunk of SCATTER_ENT consecutive (token, slot) pairs.  Every
+// block scans the histogram (E values) for the experts' offsets and first
+// tiles; the pairs of expert e in earlier chunks (the per-chunk histograms)
+// put the chunk's first pair of e at base[e].  Within the chunk each warp
+// takes SCATTER_ENT / 8 consecutive pairs in rounds of 32: a match over the
+// warp counts each expert's pairs (per warp), a scan over the warps turns the
+// counts into starts, and a second pass hands out the ranks in pair order.
+// The scatter is therefore stable: perm lists each expert's pairs in
+// ascending pair index.  The blocks share the block-map entries out by
+// expert (e = block, block + gridDim.x, ...); the last block also writes the
+// shared expert's tiles, n_tiles and offsets[E].
+constexpr int SCATTER_THREADS = 256;
+constexpr int SCATTER_WARPS = SCATTER_THREADS / 32;
 
-__global__ void __launch_bounds__(SCATTER_THREADS) scatter_kernel(const int32_t *__restrict__ topk_id, int T, int E, int k,
-                                                      int BN, int S, const int32_t *__restrict__ counts,
-                                                      int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
-                                                      int32_t *__restrict__ inv, int32_t *__restrict__ blockmap,
-                                                      int32_t *__restrict__ n_tiles, int max_tiles, int BN2,
-                                                      int32_t *__restrict__ blockmap2, int32_t *__restrict__ n_tiles2,
-                                                      int max_tiles2, int32_t *__restrict__ status, int debug,
-                                                      int32_t *__restrict__ qctr) {
-  __shared__ int s_a[32], s_b[32], s_c[32];
-  __shared__ int s_warp[SCATTER_THREADS / 32];
-  __shared__ int s_off, s_tb, s_tb2;
-  const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (qctr && e == 0 && tid == 0) {  // the grouped GEMMs' work-queue counters start the layer at zero
+// Exclusive scan over the block of one value per expert (E <= 4 * 256 = 1024:
+// thread i holds experts 4i .. 4i+3); returns the total.
+__device__ __forceinline__ int block_exscan4(int v[4], int *s_warp) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int tsum = v[0] + v[1] + v[2] + v[3];
+  int incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_warp[wid] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < SCATTER_WARPS; ++w) {
+    const int cw = s_warp[w];
+    before += (w < wid) ? cw : 0;
+    total += cw;
+  }
+  __syncthreads();  // s_warp is reused by the next scan
+  int run = before + incl - tsum;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int x = v[i];
+    v[i] = run;
+    run += x;
+  }
+  return total;
+}
+
+__global__ void __launch_bounds__(SCATTER_THREADS) scatter_kernel(
+    const int32_t *__restrict__ topk_id, int T, int E, int k, int BN, int S, const int32_t *__restrict__ counts,
+    int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+    int32_t *__restrict__ blockmap, int32_t *__restrict__ n_tiles, int max_tiles, int BN2,
+    int32_t *__restrict__ blockmap2, int32_t *__restrict__ n_tiles2, int max_tiles2, int32_t *__restrict__ status,
+    int debug, int32_t *__restrict__ qctr) {
+  // shared: start of each expert in the chunk, per warp ([warp][E]); the
+  // experts' offsets and first tiles ([3][E])
+  extern __shared__ int s_dyn[];
+  int *s_hist = s_dyn;
+  int *s_off = s_dyn + SCATTER_WARPS * E, *s_tb = s_off + E, *s_tb2 = s_tb + E;
+  __shared__ int s_warp[SCATTER_WARPS];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, b = blockIdx.x;
+  const int n_pairs = T * k;
+  // this warp's pairs of the chunk: ids loaded first, so that their latency
+  // overlaps the scans below
+  constexpr int PER_WARP = SCATTER_ENT / SCATTER_WARPS, ROUNDS = PER_WARP / 32;
+  const int p0 = b * SCATTER_ENT + wid * PER_WARP;
+  int ev[ROUNDS];
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int p = p0 + r * 32 + lane;
+    const int e = p < n_pairs ? __ldg(topk_id + p) : -1;
+    ev[r] = (e >= 0 && e < E) ? e : -1;  // out-of-range ids were flagged when they were counted
+  }
+  if (qctr && b == 0 && tid == 0) {  // the grouped GEMMs' work-queue counters start the layer at zero
     qctr[0] = 0;
     qctr[1] = 0;
   }
-  int off = 0, tb = 0, tb2 = 0;
-  for (int i = tid; i < e; i += blockDim.x) {
-    int c = counts[i];
-    off += c;
-    tb += (c + BN - 1) / BN;
-    tb2 += (c + BN2 - 1) / BN2;
-  }
+  // the experts' offsets and first tiles: scans of the histogram
+  int vo[4], vt[4], vt2[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    off += __shfl_xor_sync(0xffffffffu, off, o);
-    tb += __shfl_xor_sync(0xffffffffu, tb, o);
-    tb2 += __shfl_xor_sync(0xffffffffu, tb2, o);
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * tid + i;
+    const int c = e < E ? counts[e] : 0;
+    vo[i] = c;
+    vt[i] = (c + BN - 1) / BN;
+    vt2[i] = (c + BN2 - 1) / BN2;
   }
-  if (lane == 0) {
-    s_a[wid] = off;
-    s_b[wid] = tb;
-    s_c[wid] = tb2;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int a = 0, b = 0, c = 0;
-    for (int w = 0; w < (int)(blockDim.x / 32); ++w) {
-      a += s_a[w];
-      b += s_b[w];
-      c += s_c[w];
+  const int total = block_exscan4(vo, s_warp);
+  const int routed_tiles = block_exscan4(vt, s_warp);
+  const int routed_tiles2 = block_exscan4(vt2, s_warp);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * tid + i;
+    if (e < E) {
+      s_off[e] = vo[i];
+      s_tb[e] = vt[i];
+      s_tb2[e] = vt2[i];
     }
-    s_off = a;
-    s_tb = b;
-    s_tb2 = c;
   }
+  for (int i = tid; i < SCATTER_WARPS * E; i += SCATTER_THREADS) s_hist[i] = 0;
   __syncthreads();
-  off = s_off;
-  tb = s_tb;
-  tb2 = s_tb2;
-  const int ce = counts[e];
-  // one block map per tile height: rows of BN (and, when blockmap2 is given, of BN2)
-  auto write_map = [&](int32_t *map, int32_t *nt, int mt, int bn, int tbase) {
-    const int ntile_e = (ce + bn - 1) / bn;
-    if (e == E - 1) {
-      const int routed_tiles = tbase + ntile_e;
-      const int shared_tiles = S ? (T + bn - 1) / bn : 0;
-      if (tid == 0) {
-        *nt = routed_tiles + shared_tiles;
-        if (debug && (off + ce != k * T || routed_tiles + shared_tiles > mt)) set_status(status, MOE_ERR_DEVICE_BOUNDS);
-      }
-      for (int s = tid; s < shared_tiles; s += blockDim.x) {
-        int idx = routed_tiles + s;
-        if (idx < mt) {
-          int4 ent = make_int4(E, k * T + s * bn, min(bn, T - s * bn), 0);
-          reinterpret_cast<int4 *>(map)[idx] = ent;
-        }
-      }
-    }
-    for (int r = tid; r < ntile_e; r += blockDim.x) {
-      int idx = tbase + r;
-      if (idx < mt) {
-        int4 ent = make_int4(e, off + r * bn, min(bn, ce - r * bn), 0);
-        reinterpret_cast<int4 *>(map)[idx] = ent;
+  auto end_of = [&](int e) { return e + 1 < E ? s_off[e + 1] : total; };
+
+  // block-map entries: expert e = b + i * gridDim.x goes to thread i
+  auto write_map = [&](int32_t *map, int mt, int bn, const int *tbase) {
+    for (int e = b + tid * gridDim.x; e < E; e += SCATTER_THREADS * gridDim.x) {
+      const int o = s_off[e], ce = end_of(e) - o;
+      for (int r = 0; r * bn < ce; ++r) {
+        const int idx = tbase[e] + r;
+        if (idx < mt) reinterpret_cast<int4 *>(map)[idx] = make_int4(e, o + r * bn, min(bn, ce - r * bn), 0);
       }
     }
   };
-  if (tid == 0) offsets[e] = off;
-  if (e == E - 1 && tid == 0) offsets[E] = off + ce;
-  write_map(blockmap, n_tiles, max_tiles, BN, tb);
-  if (blockmap2) write_map(blockmap2, n_tiles2, max_tiles2, BN2, tb2);
-  if (ce == 0) return;
-  // Tokens in rounds of blockDim.x * TPT: thread tid takes TPT consecutive
-  // tokens, so (thread, token) order is token order and a block-wide scan of
-  // the per-thread match counts gives every match its rank.
-  constexpr int TPT = 4;
-  const bool vec = (k % 4) == 0;  // a token's k ids as int4 loads (rows are 16-byte aligned)
-  int running = 0;
-  for (int t0 = 0; t0 < T; t0 += blockDim.x * TPT) {
-    int jf[TPT];
-    int c = 0;
-#pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-      const int t = t0 + tid * TPT + i;
-      jf[i] = -1;
-      if (t < T) {
-        const int32_t *row = topk_id + (size_t)t * k;
-        if (vec) {
-          for (int j4 = 0; j4 < k; j4 += 4) {
-            const int4 v = *reinterpret_cast<const int4 *>(row + j4);
-            if (v.x == e) jf[i] = j4;
-            if (v.y == e) jf[i] = j4 + 1;
-            if (v.z == e) jf[i] = j4 + 2;
-            if (v.w == e) jf[i] = j4 + 3;
-          }
-        } else {
-          for (int j = 0; j < k; ++j)
-            if (row[j] == e) jf[i] = j;
-        }
-      }
-      c += jf[i] >= 0;
+  auto write_shared = [&](int32_t *map, int32_t *nt, int mt, int bn, int rtiles) {
+    const int shared_tiles = S ? (T + bn - 1) / bn : 0;
+    if (tid == 0) {
+      *nt = rtiles + shared_tiles;
+      if (debug && (total != k * T || rtiles + shared_tiles > mt)) set_status(status, MOE_ERR_DEVICE_BOUNDS);
     }
-    int incl = c;  // inclusive scan of the counts over the warp
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
+    for (int s = tid; s < shared_tiles; s += SCATTER_THREADS) {
+      const int idx = rtiles + s;
+      if (idx < mt) reinterpret_cast<int4 *>(map)[idx] = make_int4(E, k * T + s * bn, min(bn, T - s * bn), 0);
     }
-    if (lane == 31) s_warp[wid] = incl;
-    __syncthreads();
-    int before = 0, total = 0;
-#pragma unroll 8
-    for (int w = 0; w < SCATTER_THREADS / 32; ++w) {
-      const int cw = s_warp[w];
-      before += (w < wid) ? cw : 0;
-      total += cw;
-    }
-    int pos = off + running + before + incl - c;
+  };
+  write_map(blockmap, max_tiles, BN, s_tb);
+  if (blockmap2) write_map(blockmap2, max_tiles2, BN2, s_tb2);
+  if (b == gridDim.x - 1) {
+    write_shared(blockmap, n_tiles, max_tiles, BN, routed_tiles);
+    if (blockmap2) write_shared(blockmap2, n_tiles2, max_tiles2, BN2, routed_tiles2);
+  }
+  if (b == 0)
+    for (int e = tid; e <= E; e += SCATTER_THREADS) offsets[e] = e < E ? s_off[e] : total;
+
+  int *hw = s_hist + wid * E;
+  unsigned peers[ROUNDS];
 #pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-      if (jf[i] < 0) continue;
-      const int p = (t0 + tid * TPT + i) * k + jf[i];
-      if (pos < off + ce) {  // always checked: a stale histogram must not write out of bounds
+  for (int r = 0; r < ROUNDS; ++r) {  // pass 1: pairs per expert and warp
+    peers[r] = __match_any_sync(0xffffffffu, ev[r]);
+    if (ev[r] >= 0 && lane == __ffs(peers[r]) - 1) hw[ev[r]] += __popc(peers[r]);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += SCATTER_THREADS) {  // starts: the experts' pairs in earlier chunks and warps
+    int run = s_off[e];
+    for (int c = 0; c < b; ++c) run += counts[(size_t)E + (size_t)c * E + e];
+#pragma unroll
+    for (int w = 0; w < SCATTER_WARPS; ++w) {
+      const int x = s_hist[w * E + e];
+      s_hist[w * E + e] = run;
+      run += x;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {  // pass 2: ranks in pair order
+    const int e = ev[r];
+    const int pos = e >= 0 ? hw[e] + __popc(peers[r] & lt) : 0;
+    __syncwarp();
+    if (e >= 0) {
+      if (lane == __ffs(peers[r]) - 1) hw[e] += __popc(peers[r]);
+      const int p = p0 + r * 32 + lane;
+      if (pos < end_of(e)) {  // always checked: a stale histogram must not write out of bounds
         perm[pos] = p;
         inv[p] = pos;
       } else {
         set_status(status, MOE_ERR_DEVICE_BOUNDS);
       }
-      ++pos;
     }
-    running += total;
-    __syncthreads();
+    __syncwarp();
   }
-  if (debug && tid == 0 && running != ce) set_status(status, MOE_ERR_DEVICE_BOUNDS);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -308,9 +333,13 @@ cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, 
                            int max_tiles, int BN2, int32_t *blockmap2, int32_t *n_tiles2, int max_tiles2,
                            int32_t *status, int debug, int32_t *qctr, cudaStream_t s) {
   if (!blockmap2) BN2 = BN;
+  if (E > 4 * SCATTER_THREADS) return cudaErrorInvalidValue;
+  const int blocks = (T * k + SCATTER_ENT - 1) / SCATTER_ENT;
+  const size_t smem = (size_t)(SCATTER_WARPS + 3) * E * sizeof(int);
   prof_before(MOE_KERNEL_SCATTER, s);
-  scatter_kernel<<<E, SCATTER_THREADS, 0, s>>>(topk_id, T, E, k, BN, S, counts, offsets, perm, inv, blockmap, n_tiles, max_tiles,
-                                   BN2, blockmap2, n_tiles2, max_tiles2, status, debug, qctr);
+  scatter_kernel<<<blocks, SCATTER_THREADS, smem, s>>>(topk_id, T, E, k, BN, S, counts, offsets, perm, inv, blockmap,
+                                                        n_tiles, max_tiles, BN2, blockmap2, n_tiles2, max_tiles2,
+                                                        status, debug, qctr);
   prof_after(MOE_KERNEL_SCATTER, s);
   return cudaGetLastError();
 }

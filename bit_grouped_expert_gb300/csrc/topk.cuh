@@ -34,9 +34,13 @@ __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v,
 
 // Weights of the picked keys: softmax over the k picked keys (max = slot 0),
 // written with the ids; lane j < k owns slot j.  NaN/Inf keys set the status.
+// counts (or null): the histogram over experts; ccounts (or null): the same
+// per chunk of SCATTER_ENT consecutive (token, slot) pairs, [chunk][E], the
+// token's first pair being number p0.
 __device__ __forceinline__ void topk_finish(int lane, int k, int my_id, float my_key, int32_t *__restrict__ ids_out,
                                             float *__restrict__ w_out, int32_t *__restrict__ counts,
-                                            int32_t *__restrict__ status) {
+                                            int32_t *__restrict__ status, int32_t *__restrict__ ccounts = nullptr,
+                                            int E = 0, size_t p0 = 0) {
   const float l0 = __shfl_sync(0xffffffffu, my_key, 0);
   const float ex = (lane < k) ? expf(my_key - l0) : 0.f;
   const float den = warp_sum(ex);
@@ -46,6 +50,7 @@ __device__ __forceinline__ void topk_finish(int lane, int k, int my_id, float my
     ids_out[lane] = my_id;
     w_out[lane] = ex / den;
     if (counts) atomicAdd(&counts[my_id], 1);
+    if (ccounts) atomicAdd(&ccounts[((p0 + lane) / SCATTER_ENT) * E + my_id], 1);
   }
 }
 
@@ -67,7 +72,8 @@ struct KeySrc {
 template <int KPL>
 __device__ void topk_token(float *__restrict__ row, int E, int k, int lane, int32_t *__restrict__ ids_out,
                            float *__restrict__ w_out, int32_t *__restrict__ counts, int32_t *__restrict__ status,
-                           KeySrc src = KeySrc{nullptr, 0, 0, nullptr}, unsigned long long *cand = nullptr) {
+                           KeySrc src = KeySrc{nullptr, 0, 0, nullptr}, unsigned long long *cand = nullptr,
+                           int32_t *__restrict__ ccounts = nullptr, size_t p0 = 0) {
   unsigned long long c[KPL];
   float key[KPL];
   if (src.KS > 0) {
@@ -155,7 +161,7 @@ __device__ void topk_token(float *__restrict__ row, int E, int k, int lane, int3
     }
   }
   if (lane < k) my_key = row[my_id];
-  topk_finish(lane, k, my_id, my_key, ids_out, w_out, counts, status);
+  topk_finish(lane, k, my_id, my_key, ids_out, w_out, counts, status, ccounts, E, p0);
 }
 
 }  // namespace moe

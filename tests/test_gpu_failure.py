@@ -84,8 +84,9 @@ def _ids_inputs(T, E, k, seed):
     return ids, w / w.sum(axis=1, keepdims=True)
 
 
-def test_route_from_ids_matches_the_oracle_maps():
-    E, k, T = 16, 4, 300
+@pytest.mark.parametrize("E,k,T", [(16, 4, 300), (40, 3, 1500)])
+def test_route_from_ids_matches_the_oracle_maps(E, k, T):
+    # (40, 3, 1500): 4500 pairs, three blocks of the scatter kernel
     L = Layer(H=256, E=E, k=k, I=256, max_tokens=T)
     ids, w = _ids_inputs(T, E, k, 1)
     moe.moe_route_from_ids(L.plan, dev(ids), dev(w), T, L.ws)

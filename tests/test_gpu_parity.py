@@ -173,6 +173,24 @@ def test_routing_edge_cases_from_keys(path):
     assert L.status() == 0
 
 
+@pytest.mark.parametrize("E,k,T", [(40, 3, 1500), (1024, 16, 300), (256, 8, 4096)])
+def test_routing_spans_scatter_chunks(E, k, T):
+    # the scatter kernel takes 2048 (token, slot) pairs a block: several
+    # blocks here, tokens whose pairs straddle two blocks (k = 3), the most
+    # experts a plan takes (E = 1024), and three hot experts whose pairs run
+    # through every block
+    L = Layer(H=256, E=E, k=k, I=256, max_tokens=T)
+    rng = np.random.default_rng(E + k)
+    keys = rng.normal(size=(T, E)).astype(np.float32)
+    keys[:, :3] += 2.0
+    moe.moe_route_from_logits(L.plan, dev(keys), T, L.ws)
+    torch.cuda.synchronize()
+    got = L.routing(T)
+    assert T * k > 2 * 2048
+    _assert_routing_equal(got, keys, k, E, 1)
+    assert L.status() == 0
+
+
 def test_routing_is_deterministic(real):
     W, Wd = real
     T = 512
