@@ -4,7 +4,10 @@
 //           fp32, summed in that order (the layer's bf16 weighted gather-combine
 //           with the shared expert's output and a residual add); g[t] = 1, or
 //           with a shared-expert gate vector, sigmoid(x[t] . gate) in fp32.
-// rmsnorm:  x = bf16(r / sqrt(mean(r^2) + eps)), fp32 (between stacked layers).
+// rmsnorm:  x = bf16(r / sqrt(mean(r^2) + eps)), fp32 (between stacked layers);
+//           the combine can also write it for its own output rows (the next
+//           layer's input in a stack), with the same arithmetic in the same
+//           order as the separate kernel, so the two agree bit for bit.
 // dequant:  w = bf16_rne(scale * q + bias) ("Prefill": 64 weights share one bf16
 //           scale and bias; weights are rebuilt to bf16).
 #include "common.cuh"
@@ -28,14 +31,43 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
   return make_uint4(u[0], u[1], u[2], u[3]);
 }
 
+// RMSNorm of row r (bf16, H values) into xo, by the whole block (256
+// threads, thread t owning columns 8t, 8t + 2048, ...): the sum of squares
+// per thread in column order, warp sums, the warps' partials in warp order.
+// Every thread of the block calls it; s_part holds 8 floats.
+__device__ __forceinline__ void rmsnorm_row(const uint16_t *r, int H, float eps, uint16_t *xo, float *s_part) {
+  float ss = 0.f;
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    float v[8];
+    unpack8(*reinterpret_cast<const uint4 *>(r + c), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_part[w];
+  const float scale = rsqrtf(tot / (float)H + eps);
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    float v[8];
+    unpack8(*reinterpret_cast<const uint4 *>(r + c), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] *= scale;
+    *reinterpret_cast<uint4 *>(xo + c) = pack8(v);
+  }
+}
+
 // One block per token; each thread owns 8 consecutive columns.  KMAX >= k:
-// the rows' loads are all in flight before the sums.
+// the rows' loads are all in flight before the sums.  xnorm (or null): also
+// the RMSNorm of the output row, for the next layer of a stack (x may alias
+// it: this block reads row t of x before it writes row t of xnorm).
 template <int KMAX>
-__global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ res, const uint16_t *__restrict__ y,
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t *res, const uint16_t *__restrict__ y,
                                                       const int32_t *__restrict__ inv,
-                                                      const float *__restrict__ topk_w, const uint16_t *__restrict__ x,
+                                                      const float *__restrict__ topk_w, const uint16_t *x,
                                                       const float *__restrict__ sh_gate, int T, int H, int k, int S,
-                                                      uint16_t *__restrict__ out) {
+                                                      uint16_t *out, uint16_t *xnorm, float eps) {
   const int t = blockIdx.x;
   __shared__ int s_row[16];
   __shared__ float s_w[16];
@@ -95,32 +127,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     }
     *reinterpret_cast<uint4 *>(out + (size_t)t * H + c) = pack8(acc);
   }
+  if (xnorm) {  // the block's writes of the row are visible to it after the barrier
+    __syncthreads();
+    rmsnorm_row(out + (size_t)t * H, H, eps, xnorm + (size_t)t * H, s_part);
+  }
 }
 
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t *__restrict__ r, int H, float eps,
                                                       uint16_t *__restrict__ x) {
-  const int t = blockIdx.x;
   __shared__ float s_part[8];
-  float ss = 0.f;
-  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
-    float v[8];
-    unpack8(*reinterpret_cast<const uint4 *>(r + (size_t)t * H + c), v);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
-  }
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_part[w];
-  const float scale = rsqrtf(tot / (float)H + eps);
-  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
-    float v[8];
-    unpack8(*reinterpret_cast<const uint4 *>(r + (size_t)t * H + c), v);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] *= scale;
-    *reinterpret_cast<uint4 *>(x + (size_t)t * H + c) = pack8(v);
-  }
+  const int t = blockIdx.x;
+  rmsnorm_row(r + (size_t)t * H, H, eps, x + (size_t)t * H, s_part);
 }
 
 // One thread per packed word (8 weights).
@@ -138,12 +155,12 @@ __global__ void dequant_kernel(const uint32_t *__restrict__ q, const uint16_t *_
 
 cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w,
                            const uint16_t *x, const float *shared_gate, int T, int H, int k, int S, uint16_t *out,
-                           cudaStream_t s) {
+                           uint16_t *xnorm, float eps, cudaStream_t s) {
   prof_before(MOE_KERNEL_COMBINE, s);
   if (k <= 8)
-    combine_kernel<8><<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out);
+    combine_kernel<8><<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out, xnorm, eps);
   else
-    combine_kernel<16><<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out);
+    combine_kernel<16><<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out, xnorm, eps);
   prof_after(MOE_KERNEL_COMBINE, s);
   return cudaGetLastError();
 }

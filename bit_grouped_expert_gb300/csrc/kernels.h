@@ -49,9 +49,10 @@ cudaError_t launch_down_simt(const uint16_t *h, int T, int H, int I, int E, int 
 
 // combine.cu
 // shared_gate: [H] fp32 or null; x: the layer's expert input (read only with a gate)
+// xnorm (or null): also RMSNorm(out) with eps, bit for bit as launch_rmsnorm
 cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w,
                            const uint16_t *x, const float *shared_gate, int T, int H, int k, int S, uint16_t *out,
-                           cudaStream_t s);
+                           uint16_t *xnorm, float eps, cudaStream_t s);
 cudaError_t launch_rmsnorm(const uint16_t *r, int T, int H, float eps, uint16_t *x, cudaStream_t s);
 cudaError_t launch_dequant(const uint32_t *q, const uint16_t *sc, const uint16_t *b, int rows, int K, int G,
                            uint16_t *w, cudaStream_t s);

@@ -408,9 +408,13 @@ moe_status moe_route_from_ids(const moe_plan_t *plan, const int32_t *ids_d, cons
   return st;
 }
 
-moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *residual_d, int32_t T,
-                       const moe_weights *w, const float *logit_bias_d, void *out_d, void *ws_d, size_t ws_bytes,
-                       void *stream) {
+// One layer.  For the chunk loop of pre-norm stacks (grouped path only):
+// norm_in -- the workspace's normalised x already holds RMSNorm(x_d) (the
+// previous layer's combine wrote it), so the norm kernel is skipped;
+// norm_out -- the combine also writes RMSNorm(out) there for the next layer.
+static moe_status forward_impl(const moe_plan_t *plan, const void *x_d, const void *residual_d, int32_t T,
+                               const moe_weights *w, const float *logit_bias_d, void *out_d, void *ws_d,
+                               size_t ws_bytes, void *stream, bool norm_in, bool norm_out) {
   g_last_launches = 0;
   moe_status st = check_call(plan, T, ws_d, ws_bytes);
   if (st != MOE_OK) return st;
@@ -440,12 +444,16 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
     return cuda_status(err);
   }
 
+  uint16_t *xnorm_next = nullptr;
   if (prenorm) {  // x = RMSNorm(r) into the workspace; the residual is r
     uint16_t *xn = moe::ws_ptr<uint16_t>(ws_d, L.xn);
-    cudaError_t err = moe::launch_rmsnorm(x, T, c.hidden, 1e-6f, xn, s);
-    if (err != cudaSuccess) return cuda_status(err);
-    ++launches;
+    if (!norm_in) {
+      cudaError_t err = moe::launch_rmsnorm(x, T, c.hidden, 1e-6f, xn, s);
+      if (err != cudaSuccess) return cuda_status(err);
+      ++launches;
+    }
     x = xn;
+    if (norm_out) xnorm_next = xn;
   }
   st = enqueue_route(plan, x, T, w->router_d, w->router_split_d, logit_bias_d, ws_d, RouteFrom::kX, s, &launches);
   if (st != MOE_OK) return st;
@@ -473,11 +481,17 @@ moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *resi
     if (err != cudaSuccess) return cuda_status(err);
   }
   err = moe::launch_combine(res, y, moe::ws_ptr<int32_t>(ws_d, L.inv), moe::ws_ptr<float>(ws_d, L.topk_w), x,
-                            ep.shared_gate, T, c.hidden, c.top_k, c.n_shared, out, s);
+                            ep.shared_gate, T, c.hidden, c.top_k, c.n_shared, out, xnorm_next, 1e-6f, s);
   if (err != cudaSuccess) return cuda_status(err);
   ++launches;
   g_last_launches = launches;
   return MOE_OK;
+}
+
+moe_status moe_forward(const moe_plan_t *plan, const void *x_d, const void *residual_d, int32_t T,
+                       const moe_weights *w, const float *logit_bias_d, void *out_d, void *ws_d, size_t ws_bytes,
+                       void *stream) {
+  return forward_impl(plan, x_d, residual_d, T, w, logit_bias_d, out_d, ws_d, ws_bytes, stream, false, false);
 }
 
 moe_status moe_decode_stack(const moe_plan_t *plan, void *r_d, int32_t n_layers, const moe_weights *w,
@@ -530,9 +544,12 @@ moe_status moe_prefill_stack(const moe_plan_t *plan, void *r_d, int32_t T, int32
   for (int c0 = 0; c0 < T; c0 += m) {  // chunk-major: each chunk through every layer
     const int n = T - c0 < m ? T - c0 : m;
     uint16_t *rc = r + (size_t)c0 * H;
+    // on the grouped path each layer's combine also normalises its output
+    // for the next layer (bit for bit the norm kernel's result)
+    const bool grouped = !(n == 1 && plan->use_decode && !(plan->flags & MOE_FLAG_FORCE_GROUPED));
     for (int l = 0; l < n_layers; ++l) {
-      st = moe_forward(plan, rc, nullptr, n, &w[l], logit_bias_d ? logit_bias_d[l] : nullptr, rc, ws_d, ws_bytes,
-                       stream);
+      st = forward_impl(plan, rc, nullptr, n, &w[l], logit_bias_d ? logit_bias_d[l] : nullptr, rc, ws_d, ws_bytes,
+                        stream, grouped && l > 0, grouped && l + 1 < n_layers);
       launches += g_last_launches;
       if (st != MOE_OK) {
         g_last_launches = launches;

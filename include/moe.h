@@ -226,9 +226,11 @@ moe_status moe_decode_stack(const moe_plan_t *plan, void *r_d, int32_t n_layers,
  *     rows c0 .. c0 + n - 1 of r (n = min(m, T - c0)), for l = 0 .. n_layers-1:
  *       r_c = r_c + MoE_l(RMSNorm(r_c))
  * chunk-major (each chunk passes through every layer before the next chunk
- * starts), every call on the one workspace.  The same arithmetic, call for
- * call, as the moe_forward calls of that loop (a one-token tail chunk takes
- * the decode path).  The plan must have MOE_FLAG_PRENORM.
+ * starts), every call on the one workspace.  The same results, bit for bit,
+ * as the moe_forward calls of that loop (a one-token tail chunk takes the
+ * decode path); on the grouped path each layer's combine also writes the
+ * next layer's RMSNorm, with the norm step's arithmetic, so that step is not
+ * launched again.  The plan must have MOE_FLAG_PRENORM.
  *   r_d           bf16 [T][H] residual stream, updated in place (device)
  *   T             1 <= T (no upper bound beyond the caller's buffer)
  *   w             host array of n_layers moe_weights (device pointers)
