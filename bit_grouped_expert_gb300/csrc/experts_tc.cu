@@ -28,10 +28,13 @@
 //               epilogue: gate/up: h = bf16(silu(g) * u); down: y = bf16(acc)
 // Tensor memory (512 columns), gate/up: D_gate [0,128), D_up [128,256), four
 // A slots of 64 columns at 256 (gate at +0, up at +32; 32 columns = 64 bf16
-// of K).  Down: two accumulators D0 [0,192) and D1 [192,384), so that the MMA
-// runs the next item while the epilogue drains the last one, and four A slots
-// of 32 columns at 384.  A k-block's token rows and its A slot form one slot
-// of a four-slot ring.
+// of K).  Down, one output tile per item (tiles of up to 192 rows): two
+// accumulators D0 [0,192) and D1 [192,384), so that the MMA runs the next
+// item while the epilogue drains the last one, and four A slots of 32
+// columns at 384.  Down, two output tiles per item (tiles of up to 128 rows,
+// the layout of gate/up): the two tiles share the item's token rows, which
+// halves their reads where the tiles are short.  A k-block's token rows and
+// its A slot form one slot of a four-slot ring.
 // Every wait is bounded: after one second the kernel records
 // MOE_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees tensor memory
 // and exits.
@@ -59,23 +62,33 @@ constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
 
 constexpr int SBOX = BM * 16;  // one scale (or bias) box: 128 rows x 8 groups of bf16
 
-template <bool GATEUP>
+// Kernel modes: the gate/up GEMM (+ SwiGLU); the down GEMM with one
+// 128-feature output tile per item; the down GEMM with two output tiles per
+// item (features 256 m .. 256 m + 255), which share the item's token rows
+// exactly as gate and up do.
+enum { MODE_DOWN = 0, MODE_GATEUP = 1, MODE_DOWN2 = 2 };
+
+template <int MODE>
 struct Cfg {
-  static constexpr int NMAT = GATEUP ? 2 : 1;
-  // Token rows per work item (the MMA's N).  Gate and up keep two fp32
-  // accumulators of N columns next to the A slots in tensor memory, so N <=
-  // 128; the down GEMM keeps two accumulators of up to 192 columns.
-  static constexpr int MAXN = GATEUP ? 128 : TC_DOWN_ROWS;
-  static constexpr int NBUF = GATEUP ? 1 : 2;         // accumulators (items in flight)
-  static constexpr int D_BUF = GATEUP ? 0 : MAXN;     // columns from one accumulator to the next
-  static constexpr int A_COL = GATEUP ? 256 : 2 * MAXN;  // first A slot
-  static constexpr int A_SLOT = GATEUP ? 64 : 32;     // columns per A slot
+  // two weight tiles per k-block against the same token rows (gate and up,
+  // or two output tiles of down), each with its own accumulator
+  static constexpr bool TWO = MODE != MODE_DOWN;
+  static constexpr int NMAT = TWO ? 2 : 1;
+  // Token rows per work item (the MMA's N).  Two accumulators of N columns
+  // sit next to the A slots in tensor memory, so N <= 128 with two weight
+  // tiles; the one-tile down GEMM keeps two accumulators (items) of up to
+  // 192 columns.
+  static constexpr int MAXN = TWO ? 128 : TC_DOWN_ROWS;
+  static constexpr int NBUF = TWO ? 1 : 2;         // accumulators (items in flight)
+  static constexpr int D_BUF = TWO ? 0 : MAXN;     // columns from one accumulator to the next
+  static constexpr int A_COL = TWO ? 256 : 2 * MAXN;  // first A slot
+  static constexpr int A_SLOT = TWO ? 64 : 32;     // columns per A slot
   static_assert(A_COL + NSLOT * A_SLOT <= (int)TMEM_COLS, "tensor memory");
   static constexpr int B_SLOT = MAXN * 128;  // one k-block of MAXN token rows
   // Code stages (4 k-blocks each, from HBM) and the k-block ring (token rows
   // in shared memory + dequantised weights in tensor memory) share the
   // shared memory.
-  static constexpr int CSTAGES = GATEUP ? 3 : 4;
+  static constexpr int CSTAGES = TWO ? 3 : 4;
   // per stage: codes of each matrix, then (scale, bias) boxes of each matrix
   static constexpr int STAGE_BYTES = NMAT * BOX + NMAT * 2 * SBOX;
   static constexpr int OFF_B = CSTAGES * STAGE_BYTES;
@@ -247,10 +260,16 @@ __device__ __forceinline__ void trace_put(const TcArgs &a, int slot, unsigned lo
   if (a.trace && blockIdx.x < MOE_TRACE_CTAS) a.trace[blockIdx.x * MOE_TRACE_SLOTS + a.trace_base + slot] = v;
 }
 
-template <bool GATEUP>
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     experts_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
-  using C = Cfg<GATEUP>;
+  using C = Cfg<MODE>;
+  constexpr bool GATEUP = MODE == MODE_GATEUP, PAIR = MODE == MODE_DOWN2;
+  // first weight row of matrix mat of an item: its output tile (two per item
+  // when PAIR)
+  auto w_row = [&](const Item &it, int mat) {
+    return it.e * a.NOUT + (PAIR ? (2 * it.mt + mat) : it.mt) * BM;
+  };
   extern __shared__ uint8_t smem_raw[];
   // offset the shared pointer itself (not an integer cast), so accesses stay
   // shared-memory loads rather than generic ones
@@ -288,7 +307,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = m->tmem;
 
-  const int MT = a.NOUT / BM;
+  const int MT = a.NOUT / (PAIR ? 2 * BM : BM);  // items per block-map tile
   const int KB = a.K / KBLK;  // a multiple of NSLOT (K % 256 == 0)
   const int NST = (KB + STAGE_KB - 1) / STAGE_KB;
   const int n_items = (*a.n_tiles) * MT;
@@ -335,7 +354,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         nxt = idx2 < n_items ? item_entry<C::MAXN>(a, idx2, MT) : make_int4(-1, 0, 0, 0);
         if (nxt.x >= 0) idx2 = draw();
         const Item it = as_item(ent);
-        const int row_base = it.e * a.NOUT + it.mt * BM;
         for (int st = 0; st < NST; ++st, ++cs) {
           const int slot = cs % C::CSTAGES;
           const uint32_t ph = (cs / C::CSTAGES) & 1u;
@@ -348,6 +366,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::mbar_arrive_expect_tx(&m->code_full[slot], bytes);
           uint8_t *stage = smem + slot * C::STAGE_BYTES;
           for (int mat = 0; mat < C::NMAT; ++mat) {
+            const int row_base = w_row(it, mat);
             ptx::tma_load_2d(stage + mat * BOX, &maps.code[mat], &m->code_full[slot], kb0 * (KBLK / 2), row_base);
             if (a.tma_scales) {  // the 8 groups around this stage's 4 (16-byte aligned boxes)
               uint8_t *sb = stage + C::NMAT * BOX + mat * 2 * SBOX;
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // steps only move the address field in its low word
       const uint64_t bdesc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + C::OFF_B));
       const uint32_t b_lo0 = (uint32_t)bdesc0, b_hi = (uint32_t)(bdesc0 >> 32);
-      const int mat = GATEUP ? iss : 0;
+      const int mat = C::TWO ? iss : 0;
       const uint32_t a_col = tmem + C::A_COL + (uint32_t)(mat * 32);
       uint32_t kbc = 0, itc = 0;
       bool ok = true;
@@ -395,7 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const Item it = as_item(ent);
         // this issuer's token columns [c0, c0 + nc)
         int c0 = 0, nc = it.n_mma;
-        if (!GATEUP) {
+        if (!C::TWO) {
           const int half = ((it.n_mma >> 1) + 15) & ~15;
           c0 = iss ? half : 0;
           nc = iss ? it.n_mma - half : half;
@@ -514,10 +533,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // item are loaded one stage ahead
     uint2 nsv[C::NMAT], nbv[C::NMAT];
     auto prefetch = [&](const Item &pi, int pst) {
-      const size_t grow = (size_t)pi.e * a.NOUT + (size_t)pi.mt * BM + row;
       const int kb0 = pst * STAGE_KB, nkb = min(STAGE_KB, KB - kb0);
 #pragma unroll
       for (int mt = 0; mt < C::NMAT; ++mt) {
+        const size_t grow = (size_t)w_row(pi, mt) + row;
         nsv[mt] = load_groups(a.sc[mt] + grow * groups + kb0, nkb, vec);
         nbv[mt] = load_groups(a.bi[mt] + grow * groups + kb0, nkb, vec);
       }
@@ -537,18 +556,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       // gate/up writes h in the interleaved K order of the down GEMM (a
       // permutation within runs of 8, so within this warp's 32 features)
       const int pos = GATEUP ? ilv_pos(row) : row;
-      for (int ch = wg; ch < ei.n_mma / 16; ch += NWG) {
-        uint32_t g[16], u[16];
-        ptx::tmem_ld_x16(dcol + ch * 16, g);
-        if (GATEUP) ptx::tmem_ld_x16(dcol + D_UP_COL + ch * 16, u);
-        ptx::tmem_wait_ld();
-        uint16_t o[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          o[i] = f32_to_bf16(GATEUP ? silu(__uint_as_float(g[i])) * __uint_as_float(u[i]) : __uint_as_float(g[i]));
+      // 16 token rows x this warp's 32 features of output tile `tile`
+      auto put = [&](const uint16_t (&o)[16], int ch, int tile) {
         if (ch * 16 + 16 <= ei.nrows) {
           // a whole chunk: through this warp's staging buffer and one TMA
-          // store of 16 rows x its 32 features (the buffer used two chunks
+          // store of 16 rows x its 32 features (the buffer used two stores
           // ago must have been read by its store first)
           uint16_t *sb = reinterpret_cast<uint16_t *>(smem + C::OFF_EPI + ((warp - 4) * 2 + (epi_n & 1)) * C::EPI_BUF);
           if (lane == 0) ptx::bulk_wait_read<1>();
@@ -558,15 +570,31 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_2d(&maps.out, sb, ei.mt * BM + q * 32, ei.row0 + ch * 16);
+            ptx::tma_store_2d(&maps.out, sb, tile * BM + q * 32, ei.row0 + ch * 16);
             ptx::bulk_commit();
           }
           ++epi_n;
         } else {  // the tile's ragged last chunk: rows past it belong to the next tile
-          uint16_t *orow = a.out + (size_t)ei.row0 * a.NOUT + (size_t)ei.mt * BM + pos;
+          uint16_t *orow = a.out + (size_t)ei.row0 * a.NOUT + (size_t)tile * BM + pos;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (ch * 16 + i < ei.nrows) orow[(size_t)(ch * 16 + i) * a.NOUT] = o[i];
+        }
+      };
+      for (int ch = wg; ch < ei.n_mma / 16; ch += NWG) {
+        uint32_t g[16], u[16];
+        ptx::tmem_ld_x16(dcol + ch * 16, g);
+        if (C::TWO) ptx::tmem_ld_x16(dcol + D_UP_COL + ch * 16, u);
+        ptx::tmem_wait_ld();
+        uint16_t o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          o[i] = f32_to_bf16(GATEUP ? silu(__uint_as_float(g[i])) * __uint_as_float(u[i]) : __uint_as_float(g[i]));
+        put(o, ch, PAIR ? 2 * ei.mt : ei.mt);
+        if (PAIR) {  // the item's second output tile
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = f32_to_bf16(__uint_as_float(u[i]));
+          put(o, ch, 2 * ei.mt + 1);
         }
       }
       ptx::tc_fence_before();
@@ -783,11 +811,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 bool tc_supported(const moe_config &c) { return c.hidden % 256 == 0 && c.inter % 256 == 0; }
 
 cudaError_t tc_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(experts_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<true>::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(experts_tc_kernel<MODE_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<MODE_GATEUP>::SMEM);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(experts_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<false>::SMEM);
+    e = cudaFuncSetAttribute(experts_tc_kernel<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<MODE_DOWN>::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(experts_tc_kernel<MODE_DOWN2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<MODE_DOWN2>::SMEM);
   return e;
 }
 
@@ -815,6 +846,10 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
     if ((e = group_map(&md.sc[0], w.down_s, rows_dn, c.inter)) != cudaSuccess) return e;
     if ((e = group_map(&md.bi[0], w.down_b, rows_dn, c.inter)) != cudaSuccess) return e;
   }
+  // two output tiles per down item: both "matrices" are the down weights
+  md.code[1] = md.code[0];
+  md.sc[1] = md.sc[0];
+  md.bi[1] = md.bi[0];
   // h: the routed rows (k per token) then the shared expert's (n_shared per token)
   const int rows_h = (c.top_k + c.n_shared) * T;
   for (int i = 0; i < 4; ++i)
@@ -854,14 +889,16 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   int items = max_tiles * (c.inter / BM);
   int grid = items < plan->num_sms ? items : plan->num_sms;
   prof_before(MOE_KERNEL_GATEUP, s);
-  experts_tc_kernel<true><<<grid, THREADS, Cfg<true>::SMEM, s>>>(mg, a);
+  experts_tc_kernel<MODE_GATEUP><<<grid, THREADS, Cfg<MODE_GATEUP>::SMEM, s>>>(mg, a);
   prof_after(MOE_KERNEL_GATEUP, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  // down: h rows -> y, over the block map of taller tiles
+  // down: h rows -> y; with a second block map (taller tiles) one output
+  // tile per item, else two output tiles per item over the first map
+  const bool pair = blockmap2 == nullptr;
   a.trace_base = 16;
-  a.blockmap = blockmap2;
-  a.n_tiles = n_tiles2;
+  a.blockmap = pair ? blockmap : blockmap2;
+  a.n_tiles = pair ? n_tiles : n_tiles2;
   a.item_counter = nullptr;  // round-robin (qctr[1] stays unused)
   a.sc[0] = w.down_s;
   a.bi[0] = w.down_b;
@@ -871,10 +908,13 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.K = c.inter;
   a.NOUT = c.hidden;
   a.tma_scales = ts_dn;
-  items = max_tiles2 * (c.hidden / BM);
+  items = pair ? max_tiles * (c.hidden / (2 * BM)) : max_tiles2 * (c.hidden / BM);
   grid = items < plan->num_sms ? items : plan->num_sms;
   prof_before(MOE_KERNEL_DOWN, s);
-  experts_tc_kernel<false><<<grid, THREADS, Cfg<false>::SMEM, s>>>(md, a);
+  if (pair)
+    experts_tc_kernel<MODE_DOWN2><<<grid, THREADS, Cfg<MODE_DOWN2>::SMEM, s>>>(md, a);
+  else
+    experts_tc_kernel<MODE_DOWN><<<grid, THREADS, Cfg<MODE_DOWN>::SMEM, s>>>(md, a);
   prof_after(MOE_KERNEL_DOWN, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   *launches += 2;

@@ -471,8 +471,15 @@ static moe_status forward_impl(const moe_plan_t *plan, const void *x_d, const vo
     if (err != cudaSuccess) return cuda_status(err);
     launches += 2;
   } else {
-    const int max_tiles2 = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, plan->block_rows2);
-    err = moe::launch_experts_tc(plan, x, T, perm, bm, nt, max_tiles, moe::ws_ptr<int32_t>(ws_d, L.blockmap2),
+    const int max_tiles2 = plan->block_rows2 ? tiles_bound(T, c.top_k, c.n_experts, c.n_shared, plan->block_rows2) : 0;
+    // The down GEMM: with few rows per expert (k T / E < 96) two output tiles
+    // per item over the first block map, whose items share their token rows
+    // (measured: T = 256 86 -> 66 us, T = 2048 94 -> 82 us); with more, one
+    // output tile per item over the taller tiles of the second map, whose two
+    // accumulators hide the epilogue (T = 4096: 105 us against 125).
+    const bool down_pair = !plan->block_rows2 || (int64_t)c.top_k * T < (int64_t)96 * c.n_experts;
+    err = moe::launch_experts_tc(plan, x, T, perm, bm, nt, max_tiles,
+                                 down_pair ? nullptr : moe::ws_ptr<int32_t>(ws_d, L.blockmap2),
                                  moe::ws_ptr<int32_t>(ws_d, L.n_tiles2), max_tiles2, ep, h, y,
                                  moe::ws_ptr<uint16_t>(ws_d, L.xg), moe::ws_ptr<int32_t>(ws_d, L.qctr),
                                  status,

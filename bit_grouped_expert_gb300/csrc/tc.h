@@ -23,7 +23,9 @@ bool tc_supported(const moe_config &c);
 cudaError_t tc_prepare();
 
 // qctr: two work-queue counters (gate/up, down), zero at the launch (the
-// scatter kernel of the layer's routing zeroes them).
+// scatter kernel of the layer's routing zeroes them).  blockmap2 null: the
+// down GEMM takes two 128-feature output tiles per item over blockmap;
+// otherwise one output tile per item over blockmap2's taller tiles.
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
                               const int32_t *blockmap, const int32_t *n_tiles, int max_tiles,
                               const int32_t *blockmap2, const int32_t *n_tiles2, int max_tiles2, ExpertPtrs w,

@@ -239,10 +239,28 @@ def test_layer_tiny_dims(path, T):
     out = _forward(L, x, Wd, res=res, bias=bias)
     r = L.routing(T)
     keys = r["keys"]
-    if T == 300 and path != "simt":  # the skew puts > 128 rows in one down tile (N up to 256)
-        assert (r["blockmap2"][:, 2] > 128).any()
     ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, res=res, keys=keys, intermediates=True)
     assert_outputs_close(out, ref, f"tiny T={T} {path}", k=d["k"])
+    assert L.status() == 0
+
+
+@pytest.mark.parametrize("T", [300, 700])
+def test_layer_tiny_dims_both_down_modes(T):
+    # k T / E < 96 (T = 300): the down GEMM takes two output tiles per item
+    # over the 128-row map; T = 700: one output tile per item over the
+    # 192-row map, where the skew puts more than 128 rows in a tile
+    d, W, Wd = _tiny(500 + T)
+    x = syn.activations(500 + T, T, d["H"])
+    bias = syn.zipf_bias(500 + T, d["E"])
+    L = Layer(H=d["H"], E=d["E"], k=d["k"], I=d["I"], max_tokens=T)
+    out = _forward(L, x, Wd, bias=bias)
+    r = L.routing(T)
+    if T == 700:
+        assert d["k"] * T >= 96 * d["E"] and (r["blockmap2"][:, 2] > 128).any()
+    else:
+        assert d["k"] * T < 96 * d["E"] and (r["blockmap"][:, 2] > 64).any()
+    ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, bias=bias, keys=r["keys"], intermediates=True)
+    assert_outputs_close(out, ref, f"tiny T={T} down modes", k=d["k"])
     assert L.status() == 0
 
 
