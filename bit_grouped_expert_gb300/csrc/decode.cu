@@ -347,17 +347,19 @@ __device__ void topk_warp(const float *keys, int E, int k, unsigned long long *c
     c[i] = lane + 32 * i < E ? topk_code(kv[i], lane + 32 * i) : 0ull;
     m = c[i] > m ? c[i] : m;
   }
-  // A lower bound on the k-th largest key: k rounds of a warp maximum over
-  // the key bits (upper word) of the lane maxima, each round dropping the
-  // lanes that hold it.  Every round drops at least one of the largest
-  // lanes, so the k-th round's maximum is at most the k-th largest lane
-  // maximum, itself at most the k-th largest key (k lanes hold distinct keys
-  // that reach it); tied lanes dropping together only lower the bound.
-  uint32_t v = (uint32_t)(m >> 32), tau_hi = 0u;
-  for (int i = 0; i < k; ++i) {
-    tau_hi = __reduce_max_sync(0xffffffffu, v);
-    if (v == tau_hi) v = 0u;
-  }
+  // A lower bound on the k-th largest key: the k-th largest of the key bits
+  // (upper word) of the 32 lane maxima -- k lanes hold distinct keys that
+  // reach it.  Each lane counts the maxima at or above its own (all 32 read
+  // from shared memory at once, no dependent chain), and the largest value
+  // that at least k maxima reach is the k-th largest.
+  __shared__ uint32_t s_lmax[32];
+  const uint32_t v = (uint32_t)(m >> 32);
+  s_lmax[lane] = v;
+  __syncwarp();
+  int ge = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) ge += s_lmax[j] >= v;
+  const uint32_t tau_hi = __reduce_max_sync(0xffffffffu, ge >= k ? v : 0u);
   const unsigned long long tau = (unsigned long long)tau_hi << 32;  // 0: every key is a candidate
   mark(19);
   int n = 0;
@@ -373,7 +375,10 @@ __device__ void topk_warp(const float *keys, int E, int k, unsigned long long *c
   for (int t = lane; t < n; t += 32) {
     const unsigned long long ct = cand[t];
     int rank = 0;
-    for (int j = 0; j < n; ++j) rank += cand[j] > ct;
+    int j = 0;
+    for (; j + 4 <= n; j += 4)  // four independent loads a step
+      rank += (cand[j] > ct) + (cand[j + 1] > ct) + (cand[j + 2] > ct) + (cand[j + 3] > ct);
+    for (; j < n; ++j) rank += cand[j] > ct;
     if (rank < k) {
       ids[rank] = topk_code_expert(ct);
       // the key back from its code (a NaN stays a NaN, -0 becomes +0: same weights)
