@@ -109,7 +109,8 @@ def test_debug_checks_reach_the_bounds_status():
     oob[9, 1] = E  # an id past the last expert
     dbg = Layer(H=256, E=E, k=k, I=256, max_tokens=T, flags=moe.MOE_FLAG_DEBUG_CHECKS)
     plain = Layer(H=256, E=E, k=k, I=256, max_tokens=T)
-    # a repeated expert: the histogram counts one pair the scatter never finds
+    # a repeated expert: the histogram kernel's debug check compares each id
+    # with the token's earlier ones
     moe.moe_route_from_ids(dbg.plan, dev(dup), dev(w), T, dbg.ws)
     assert dbg.status() == moe.MOE_ERR_DEVICE_BOUNDS
     moe.moe_route_from_ids(plain.plan, dev(dup), dev(w), T, plain.ws)
