@@ -455,6 +455,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ token-row TMA
+    // (Launched as a programmatic dependent, the kernel may start while the
+    // kernel before it -- the gather of x, or gate/up for down -- still runs:
+    // the weights' copies and every other role go ahead, and only the token
+    // rows, that kernel's output, wait for it to finish.)
     // The rows of a tile are contiguous (down: routed rows of h in perm order,
     // then the shared expert's; gate/up: the x rows gathered in the same
     // order), so each k-block of the
@@ -467,6 +471,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const long long t_start = clock64();
       unsigned long long w_free = 0;
       for (int i = 0; i < 4; ++i) ptx::prefetch_tmap(&maps.act[i]);
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       uint32_t kbc = 0;
       bool ok = true;
       for (uint32_t n = 0; ok; ++n) {
@@ -718,6 +723,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *__restrict__ x,
                                                           const int32_t *__restrict__ perm, int routed, int rows,
                                                           int k, int K, uint16_t *__restrict__ xg) {
+  // the gate/up kernel that follows may be scheduled from here on (it waits
+  // for this grid's rows before it reads them)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= rows) return;
   const int t = r < routed ? perm[r] / k : r - routed;
@@ -793,6 +801,29 @@ cudaError_t act_map(CUtensorMap *map, const uint16_t *p, int rows_total, int K, 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// One launch of the grouped kernel; with pdl, as a programmatic dependent of
+// the kernel before it in the stream (a plain launch where that is refused).
+template <int MODE>
+cudaError_t launch_tc(const TcMaps &m, const TcArgs &a, int grid, bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = Cfg<MODE>::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, experts_tc_kernel<MODE>, m, a);
+  if (e != cudaSuccess && pdl) {
+    cudaGetLastError();
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, experts_tc_kernel<MODE>, m, a);
+  }
+  return e;
+}
+
 }  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -832,6 +863,9 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   const int rows_dn = (c.n_experts + c.n_shared) * c.hidden;
   TcMaps mg{}, md{};
   cudaError_t e;
+  // Each grouped kernel starts as a programmatic dependent of the kernel
+  // before it (the gather, then gate/up) unless a timing event sits between.
+  bool gather_quiet = true;
   const bool ts_gu = c.hidden % 512 == 0, ts_dn = c.inter % 512 == 0;
   if ((e = code_map(&mg.code[0], w.gate_q, rows_gu, c.hidden)) != cudaSuccess) return e;
   if ((e = code_map(&mg.code[1], w.up_q, rows_gu, c.hidden)) != cudaSuccess) return e;
@@ -859,6 +893,7 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   {  // gate/up token rows by TMA from a gathered, interleaved copy of x
     for (int i = 0; i < 4; ++i)
       if ((e = act_map(&mg.act[i], xg, rows_h, c.hidden, BM >> i)) != cudaSuccess) return e;
+    gather_quiet = prof_quiet(MOE_KERNEL_GATHER);
     prof_before(MOE_KERNEL_GATHER, s);
     gather_rows_kernel<<<(rows_h + 7) / 8, 256, 0, s>>>(x, perm, c.top_k * T, rows_h, c.top_k, c.hidden, xg);
     prof_after(MOE_KERNEL_GATHER, s);
@@ -888,9 +923,11 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.tma_scales = ts_gu;
   int items = max_tiles * (c.inter / BM);
   int grid = items < plan->num_sms ? items : plan->num_sms;
+  const bool gu_quiet = prof_quiet(MOE_KERNEL_GATEUP);
   prof_before(MOE_KERNEL_GATEUP, s);
-  experts_tc_kernel<MODE_GATEUP><<<grid, THREADS, Cfg<MODE_GATEUP>::SMEM, s>>>(mg, a);
+  e = launch_tc<MODE_GATEUP>(mg, a, grid, gather_quiet && gu_quiet, s);
   prof_after(MOE_KERNEL_GATEUP, s);
+  if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // down: h rows -> y; with a second block map (taller tiles) one output
@@ -910,12 +947,11 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.tma_scales = ts_dn;
   items = pair ? max_tiles * (c.hidden / (2 * BM)) : max_tiles2 * (c.hidden / BM);
   grid = items < plan->num_sms ? items : plan->num_sms;
+  const bool dn_pdl = gu_quiet && prof_quiet(MOE_KERNEL_DOWN);
   prof_before(MOE_KERNEL_DOWN, s);
-  if (pair)
-    experts_tc_kernel<MODE_DOWN2><<<grid, THREADS, Cfg<MODE_DOWN2>::SMEM, s>>>(md, a);
-  else
-    experts_tc_kernel<MODE_DOWN><<<grid, THREADS, Cfg<MODE_DOWN>::SMEM, s>>>(md, a);
+  e = pair ? launch_tc<MODE_DOWN2>(md, a, grid, dn_pdl, s) : launch_tc<MODE_DOWN>(md, a, grid, dn_pdl, s);
   prof_after(MOE_KERNEL_DOWN, s);
+  if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   *launches += 2;
   return cudaSuccess;

@@ -14,6 +14,9 @@ moe_status note_cuda_error(cudaError_t e);
 // Profiling hook (moe_profile_events): record events around a kernel launch.
 void prof_before(int kernel, cudaStream_t s);
 void prof_after(int kernel, cudaStream_t s);
+// true when the kernel's next launch records no timing event (a launch that
+// follows another kernel directly may then start as its programmatic dependent)
+bool prof_quiet(int kernel);
 
 // Every member starts null: a pointer a caller leaves unset reads as absent.
 struct ExpertPtrs {

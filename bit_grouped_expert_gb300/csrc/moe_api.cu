@@ -214,6 +214,10 @@ void prof_before(int kernel, cudaStream_t s) {
   prof_record(p->start[p->next % p->n], s);
   p->open = true;
 }
+bool prof_quiet(int kernel) {
+  const ProfState *p = (kernel > 0 && kernel < kProfKernels) ? g_prof[kernel] : nullptr;
+  return !p || p->n == 0 || (p->seen % (unsigned long long)p->stride) != 0;
+}
 void prof_after(int kernel, cudaStream_t s) {
   ProfState *p = (kernel > 0 && kernel < kProfKernels) ? g_prof[kernel] : nullptr;
   if (!p || p->n == 0 || !p->open) return;
