@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *res, const
   __shared__ int s_row[16];
   __shared__ float s_w[16];
   __shared__ float s_part[8];
+  // launched as a programmatic dependent of the down GEMM: its y first
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x < k) {
     s_row[threadIdx.x] = inv[(size_t)t * k + threadIdx.x];
     s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
@@ -156,13 +158,15 @@ __global__ void dequant_kernel(const uint32_t *__restrict__ q, const uint16_t *_
 cudaError_t launch_combine(const uint16_t *res, const uint16_t *y, const int32_t *inv, const float *topk_w,
                            const uint16_t *x, const float *shared_gate, int T, int H, int k, int S, uint16_t *out,
                            uint16_t *xnorm, float eps, cudaStream_t s) {
+  const bool pdl = prof_chain(MOE_KERNEL_COMBINE);  // a dependent of the down GEMM
   prof_before(MOE_KERNEL_COMBINE, s);
-  if (k <= 8)
-    combine_kernel<8><<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out, xnorm, eps);
-  else
-    combine_kernel<16><<<T, 256, 0, s>>>(res, y, inv, topk_w, x, shared_gate, T, H, k, S, out, xnorm, eps);
+  const cudaError_t e =
+      k <= 8 ? launch_dep(pdl, combine_kernel<8>, dim3(T), dim3(256), 0, s, res, y, inv, topk_w, x, shared_gate, T, H,
+                          k, S, out, xnorm, eps)
+             : launch_dep(pdl, combine_kernel<16>, dim3(T), dim3(256), 0, s, res, y, inv, topk_w, x, shared_gate, T,
+                          H, k, S, out, xnorm, eps);
   prof_after(MOE_KERNEL_COMBINE, s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(const uint16_t *r, int T, int H, float eps, uint16_t *x, cudaStream_t s) {

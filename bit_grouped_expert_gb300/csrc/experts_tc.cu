@@ -723,8 +723,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *__restrict__ x,
                                                           const int32_t *__restrict__ perm, int routed, int rows,
                                                           int k, int K, uint16_t *__restrict__ xg) {
-  // the gate/up kernel that follows may be scheduled from here on (it waits
-  // for this grid's rows before it reads them)
+  // launched as a programmatic dependent of the scatter: its perm first; the
+  // gate/up kernel that follows may be scheduled from here on (it waits for
+  // this grid's rows before it reads them)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -894,9 +896,12 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
     for (int i = 0; i < 4; ++i)
       if ((e = act_map(&mg.act[i], xg, rows_h, c.hidden, BM >> i)) != cudaSuccess) return e;
     gather_quiet = prof_quiet(MOE_KERNEL_GATHER);
+    const bool pdl = prof_chain(MOE_KERNEL_GATHER);  // a dependent of the scatter
     prof_before(MOE_KERNEL_GATHER, s);
-    gather_rows_kernel<<<(rows_h + 7) / 8, 256, 0, s>>>(x, perm, c.top_k * T, rows_h, c.top_k, c.hidden, xg);
+    e = launch_dep(pdl, gather_rows_kernel, dim3((rows_h + 7) / 8), dim3(256), 0, s, x, perm, c.top_k * T, rows_h,
+                   c.top_k, c.hidden, xg);
     prof_after(MOE_KERNEL_GATHER, s);
+    if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     *launches += 1;
   }

@@ -17,6 +17,36 @@ void prof_after(int kernel, cudaStream_t s);
 // true when the kernel's next launch records no timing event (a launch that
 // follows another kernel directly may then start as its programmatic dependent)
 bool prof_quiet(int kernel);
+// true when no timing event was recorded after the last kernel and none will
+// be recorded before this one: the launch may start as a programmatic
+// dependent of the kernel before it
+bool prof_chain(int kernel);
+
+// Launch of kernel(args...); with pdl, as a programmatic dependent of the
+// previous kernel in the stream (the kernel waits for it with
+// griddepcontrol.wait before touching its outputs); a plain launch where the
+// attribute is refused.
+template <typename... P, typename... A>
+cudaError_t launch_dep(bool pdl, void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess && pdl) {
+    cudaGetLastError();
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  }
+  return e;
+}
 
 // Every member starts null: a pointer a caller leaves unset reads as absent.
 struct ExpertPtrs {
@@ -31,8 +61,11 @@ cudaError_t launch_router_logits(const uint16_t *x, int T, int H, const float *r
                                  float *keys, cudaStream_t s);
 // part: null (keys given) or the router's KS K-slice partial sums [KS][T][E],
 // summed in slice order (+ bias) into keys before the selection.
+// after_kernel: the launch directly follows the router kernel in the stream
+// (it may then start as that kernel's programmatic dependent).
 cudaError_t launch_topk(float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
-                        int32_t *status, const float *part, int KS, const float *bias, cudaStream_t s);
+                        int32_t *status, const float *part, int KS, const float *bias, bool after_kernel,
+                        cudaStream_t s);
 // counts[e] += 1 for every given id (ids [T][k]); out-of-range ids (and, with
 // debug, an expert repeated within a token) set MOE_ERR_DEVICE_BOUNDS.
 cudaError_t launch_ids_histogram(const int32_t *ids, int T, int E, int k, int32_t *counts, int32_t *status, int debug,

@@ -158,7 +158,8 @@ moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const fl
                                     (p->flags & MOE_FLAG_DEBUG_CHECKS) ? 1 : 0, s);
   } else {
     err = moe::launch_topk(keys, T, c.n_experts, c.top_k, moe::ws_ptr<int32_t>(ws, L.topk_id),
-                           moe::ws_ptr<float>(ws, L.topk_w), counts, status, part, ks, part ? bias : nullptr, s);
+                           moe::ws_ptr<float>(ws, L.topk_w), counts, status, part, ks, part ? bias : nullptr,
+                           from == RouteFrom::kX, s);
   }
   if (err != cudaSuccess) return cuda_status(err);
   ++*launches;
@@ -218,10 +219,14 @@ bool prof_quiet(int kernel) {
   const ProfState *p = (kernel > 0 && kernel < kProfKernels) ? g_prof[kernel] : nullptr;
   return !p || p->n == 0 || (p->seen % (unsigned long long)p->stride) != 0;
 }
+thread_local bool g_after_recorded = false;  // the last prof_after recorded an event
+bool prof_chain(int kernel) { return !g_after_recorded && prof_quiet(kernel); }
 void prof_after(int kernel, cudaStream_t s) {
   ProfState *p = (kernel > 0 && kernel < kProfKernels) ? g_prof[kernel] : nullptr;
+  g_after_recorded = false;
   if (!p || p->n == 0 || !p->open) return;
   prof_record(p->stop[p->next % p->n], s);
+  g_after_recorded = true;
   p->open = false;
   ++p->next;
 }

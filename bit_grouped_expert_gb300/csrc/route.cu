@@ -82,6 +82,9 @@ __global__ void __launch_bounds__(256) topk_kernel(float *__restrict__ keys, int
   // counts[0 .. E) is the histogram, then one histogram per chunk of pairs
   // per warp: the candidates (up to 256 codes) and the k picked ones
   __shared__ unsigned long long s_cand[KPL <= 8 ? 8 : 1][KPL <= 8 ? 256 + 16 : 1];
+  // launched as a programmatic dependent of the router: its keys first
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
   if (warp >= T) return;
   const KeySrc src{part ? part + (size_t)warp * E : nullptr, (size_t)T * E, part ? KS : 0, bias};
@@ -172,6 +175,9 @@ __global__ void __launch_bounds__(SCATTER_THREADS) scatter_kernel(
   int *s_hist = s_dyn;
   int *s_off = s_dyn + SCATTER_WARPS * E, *s_tb = s_off + E, *s_tb2 = s_tb + E;
   __shared__ int s_warp[SCATTER_WARPS];
+  // launched as a programmatic dependent of the top-k: its ids and counts first
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, b = blockIdx.x;
   const int n_pairs = T * k;
   // this warp's pairs of the chunk: ids loaded first, so that their latency
@@ -297,14 +303,20 @@ cudaError_t launch_router_logits(const uint16_t *x, int T, int H, const float *r
 }
 
 cudaError_t launch_topk(float *keys, int T, int E, int k, int32_t *topk_id, float *topk_w, int32_t *counts,
-                        int32_t *status, const float *part, int KS, const float *bias, cudaStream_t s) {
+                        int32_t *status, const float *part, int KS, const float *bias, bool after_kernel,
+                        cudaStream_t s) {
   // a warp per token: eight tokens per block, or two when T is small (so
   // that small T still spreads over many SMs)
   const int tpb = T >= 1024 ? 8 : 2;
   const int blocks = (T + tpb - 1) / tpb;
   const int kpl = (E + 31) / 32;
+  // a programmatic dependent of the router kernel (not of a memset)
+  const bool pdl = after_kernel && prof_chain(MOE_KERNEL_TOPK);
   prof_before(MOE_KERNEL_TOPK, s);
-#define MOE_TOPK(K) topk_kernel<K><<<blocks, 32 * tpb, 0, s>>>(keys, T, E, k, topk_id, topk_w, counts, status, part, KS, bias)
+  cudaError_t e = cudaSuccess;
+#define MOE_TOPK(K)                                                                                               \
+  e = launch_dep(pdl, topk_kernel<K>, dim3(blocks), dim3(32 * tpb), 0, s, keys, T, E, k, topk_id, topk_w, counts, \
+                 status, part, KS, bias)
   if (kpl <= 1)
     MOE_TOPK(1);
   else if (kpl <= 2)
@@ -319,7 +331,7 @@ cudaError_t launch_topk(float *keys, int T, int E, int k, int32_t *topk_id, floa
     MOE_TOPK(32);
 #undef MOE_TOPK
   prof_after(MOE_KERNEL_TOPK, s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_ids_histogram(const int32_t *ids, int T, int E, int k, int32_t *counts, int32_t *status, int debug,
@@ -336,12 +348,13 @@ cudaError_t launch_scatter(const int32_t *topk_id, int T, int E, int k, int BN, 
   if (E > 4 * SCATTER_THREADS) return cudaErrorInvalidValue;
   const int blocks = (T * k + SCATTER_ENT - 1) / SCATTER_ENT;
   const size_t smem = (size_t)(SCATTER_WARPS + 3) * E * sizeof(int);
+  const bool pdl = prof_chain(MOE_KERNEL_SCATTER);  // a dependent of the top-k or the ids histogram
   prof_before(MOE_KERNEL_SCATTER, s);
-  scatter_kernel<<<blocks, SCATTER_THREADS, smem, s>>>(topk_id, T, E, k, BN, S, counts, offsets, perm, inv, blockmap,
-                                                        n_tiles, max_tiles, BN2, blockmap2, n_tiles2, max_tiles2,
-                                                        status, debug, qctr);
+  const cudaError_t e = launch_dep(pdl, scatter_kernel, dim3(blocks), dim3(SCATTER_THREADS), smem, s, topk_id, T, E,
+                                   k, BN, S, counts, offsets, perm, inv, blockmap, n_tiles, max_tiles, BN2, blockmap2,
+                                   n_tiles2, max_tiles2, status, debug, qctr);
   prof_after(MOE_KERNEL_SCATTER, s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace moe
