@@ -804,26 +804,10 @@ cudaError_t act_map(CUtensorMap *map, const uint16_t *p, int rows_total, int K, 
 }
 
 // One launch of the grouped kernel; with pdl, as a programmatic dependent of
-// the kernel before it in the stream (a plain launch where that is refused).
+// the kernel before it in the stream.
 template <int MODE>
 cudaError_t launch_tc(const TcMaps &m, const TcArgs &a, int grid, bool pdl, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = Cfg<MODE>::SMEM;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, experts_tc_kernel<MODE>, m, a);
-  if (e != cudaSuccess && pdl) {
-    cudaGetLastError();
-    cfg.numAttrs = 0;
-    e = cudaLaunchKernelEx(&cfg, experts_tc_kernel<MODE>, m, a);
-  }
-  return e;
+  return launch_dep(pdl, experts_tc_kernel<MODE>, dim3(grid), dim3(THREADS), Cfg<MODE>::SMEM, s, m, a);
 }
 
 }  // namespace
