@@ -57,7 +57,6 @@ constexpr int NISS = 2;         // MMA-issuing threads (warps 1 and 3)
 constexpr int NWG = 3;                    // dequant/epilogue warpgroups
 constexpr int THREADS = 128 + NWG * 128;  // 4 role warps + the warpgroups
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int D_UP_COL = 128;
 constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
 
 constexpr int SBOX = BM * 16;  // one scale (or bias) box: 128 rows x 8 groups of bf16
@@ -65,8 +64,10 @@ constexpr int SBOX = BM * 16;  // one scale (or bias) box: 128 rows x 8 groups o
 // Kernel modes: the gate/up GEMM (+ SwiGLU); the down GEMM with one
 // 128-feature output tile per item; the down GEMM with two output tiles per
 // item (features 256 m .. 256 m + 255), which share the item's token rows
-// exactly as gate and up do.
-enum { MODE_DOWN = 0, MODE_GATEUP = 1, MODE_DOWN2 = 2 };
+// exactly as gate and up do; and the same with short tiles (at most
+// TC_SHORT_ROWS rows), whose accumulators are small enough to keep two items
+// in flight.
+enum { MODE_DOWN = 0, MODE_GATEUP = 1, MODE_DOWN2 = 2, MODE_DOWN2_SHORT = 3 };
 
 template <int MODE>
 struct Cfg {
@@ -74,14 +75,15 @@ struct Cfg {
   // or two output tiles of down), each with its own accumulator
   static constexpr bool TWO = MODE != MODE_DOWN;
   static constexpr int NMAT = TWO ? 2 : 1;
-  // Token rows per work item (the MMA's N).  Two accumulators of N columns
-  // sit next to the A slots in tensor memory, so N <= 128 with two weight
-  // tiles; the one-tile down GEMM keeps two accumulators (items) of up to
-  // 192 columns.
-  static constexpr int MAXN = TWO ? 128 : TC_DOWN_ROWS;
-  static constexpr int NBUF = TWO ? 1 : 2;         // accumulators (items in flight)
-  static constexpr int D_BUF = TWO ? 0 : MAXN;     // columns from one accumulator to the next
-  static constexpr int A_COL = TWO ? 256 : 2 * MAXN;  // first A slot
+  // Token rows per work item (the MMA's N).  The accumulators (NMAT tiles x
+  // NBUF items in flight, N columns each) sit next to the A slots in tensor
+  // memory: N <= 128 with two tiles and one item, N <= 192 with one tile and
+  // two items, N <= 64 with two tiles and two items.
+  static constexpr int MAXN = MODE == MODE_DOWN2_SHORT ? TC_SHORT_ROWS : TWO ? 128 : TC_DOWN_ROWS;
+  static constexpr int NBUF = (TWO && MODE != MODE_DOWN2_SHORT) ? 1 : 2;  // accumulators (items in flight)
+  static constexpr int D_UP = MAXN;                      // second tile's accumulator, after the first
+  static constexpr int D_BUF = NBUF == 2 ? NMAT * MAXN : 0;  // columns from one item's accumulators to the next
+  static constexpr int A_COL = NBUF * NMAT * MAXN;       // first A slot
   static constexpr int A_SLOT = TWO ? 64 : 32;     // columns per A slot
   static_assert(A_COL + NSLOT * A_SLOT <= (int)TMEM_COLS, "tensor memory");
   static constexpr int B_SLOT = MAXN * 128;  // one k-block of MAXN token rows
@@ -264,7 +266,7 @@ template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     experts_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   using C = Cfg<MODE>;
-  constexpr bool GATEUP = MODE == MODE_GATEUP, PAIR = MODE == MODE_DOWN2;
+  constexpr bool GATEUP = MODE == MODE_GATEUP, PAIR = MODE == MODE_DOWN2 || MODE == MODE_DOWN2_SHORT;
   // first weight row of matrix mat of an item: its output tile (two per item
   // when PAIR)
   auto w_row = [&](const Item &it, int mat) {
@@ -422,7 +424,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t idesc = ptx::idesc_bf16_f32((uint32_t)(nc > 0 ? nc : 16));
         // accumulator itc % NBUF; its previous item's epilogue must have read it
         const uint32_t buf = itc % C::NBUF, use = itc / C::NBUF;
-        const uint32_t d = tmem + buf * C::D_BUF + (uint32_t)(mat * D_UP_COL + c0);
+        const uint32_t d = tmem + buf * C::D_BUF + (uint32_t)(mat * C::D_UP + c0);
         const uint32_t b_lo = b_lo0 + (uint32_t)c0 * 8u;  // c0 rows of 128 B, in 16-byte units
         if (!timed(tr, w_acc, [&] { return wait_bar(&m->acc_empty[buf], (use & 1u) ^ 1u, m, a.status); })) break;
         ptx::tc_fence_after();
@@ -589,7 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int ch = wg; ch < ei.n_mma / 16; ch += NWG) {
         uint32_t g[16], u[16];
         ptx::tmem_ld_x16(dcol + ch * 16, g);
-        if (C::TWO) ptx::tmem_ld_x16(dcol + D_UP_COL + ch * 16, u);
+        if (C::TWO) ptx::tmem_ld_x16(dcol + C::D_UP + ch * 16, u);
         ptx::tmem_wait_ld();
         uint16_t o[16];
 #pragma unroll
@@ -836,11 +838,14 @@ cudaError_t tc_prepare() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(experts_tc_kernel<MODE_DOWN2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<MODE_DOWN2>::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(experts_tc_kernel<MODE_DOWN2_SHORT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<MODE_DOWN2_SHORT>::SMEM);
   return e;
 }
 
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
-                              const int32_t *blockmap, const int32_t *n_tiles, int max_tiles,
+                              const int32_t *blockmap, const int32_t *n_tiles, int max_tiles, int down_mode,
                               const int32_t *blockmap2, const int32_t *n_tiles2, int max_tiles2, ExpertPtrs w,
                               uint16_t *h, uint16_t *y, uint16_t *xg, int32_t *qctr, int32_t *status,
                               uint64_t *trace, int *launches, cudaStream_t s) {
@@ -919,12 +924,12 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  // down: h rows -> y; with a second block map (taller tiles) one output
-  // tile per item, else two output tiles per item over the first map
-  const bool pair = blockmap2 == nullptr;
+  // down: h rows -> y, in the mode the caller chose (tc.h)
+  const bool first_map = down_mode == TC_DOWN_PAIR;
+  const bool pair = down_mode != TC_DOWN_ONE;
   a.trace_base = 16;
-  a.blockmap = pair ? blockmap : blockmap2;
-  a.n_tiles = pair ? n_tiles : n_tiles2;
+  a.blockmap = first_map ? blockmap : blockmap2;
+  a.n_tiles = first_map ? n_tiles : n_tiles2;
   a.item_counter = nullptr;  // round-robin (qctr[1] stays unused)
   a.sc[0] = w.down_s;
   a.bi[0] = w.down_b;
@@ -934,11 +939,13 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.K = c.inter;
   a.NOUT = c.hidden;
   a.tma_scales = ts_dn;
-  items = pair ? max_tiles * (c.hidden / (2 * BM)) : max_tiles2 * (c.hidden / BM);
+  items = (first_map ? max_tiles : max_tiles2) * (c.hidden / ((pair ? 2 : 1) * BM));
   grid = items < plan->num_sms ? items : plan->num_sms;
   const bool dn_pdl = gu_quiet && prof_quiet(MOE_KERNEL_DOWN);
   prof_before(MOE_KERNEL_DOWN, s);
-  e = pair ? launch_tc<MODE_DOWN2>(md, a, grid, dn_pdl, s) : launch_tc<MODE_DOWN>(md, a, grid, dn_pdl, s);
+  e = down_mode == TC_DOWN_PAIR         ? launch_tc<MODE_DOWN2>(md, a, grid, dn_pdl, s)
+      : down_mode == TC_DOWN_PAIR_SHORT ? launch_tc<MODE_DOWN2_SHORT>(md, a, grid, dn_pdl, s)
+                                        : launch_tc<MODE_DOWN>(md, a, grid, dn_pdl, s);
   prof_after(MOE_KERNEL_DOWN, s);
   if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <new>
+#include <algorithm>
 #include <vector>
 
 #include "common.cuh"
@@ -34,6 +35,40 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int tiles_bound(int T, int k, int E, int S, int BN) {
   // sum_e ceil(c_e / BN) <= k*T/BN + E, plus the shared expert's tiles
   return (k * T + BN - 1) / BN + E + (S ? (T + BN - 1) / BN : 0);
+}
+
+// The down GEMM's mode for T tokens (tensor-core plans), from the average
+// rows per expert k T / E:
+//   < 12: two output tiles per item, two items in flight, over the second
+//         block map cut into short tiles (TC_SHORT_ROWS; T = 256: 66 -> 61
+//         us; at T = 512 with skewed routing, 16 rows on average, the busiest
+//         experts' many short tiles made it slower: 37 -> 39 us);
+//   < 96: two output tiles per item over the first map, whose items share
+//         their token rows (measured: T = 256 86 -> 66 us, T = 2048 94 -> 82
+//         us against one tile per item);
+//   else: one output tile per item over the second map's taller tiles, whose
+//         two accumulators hide the epilogue (T = 4096: 105 us against 125).
+int down_mode(const moe_plan_t *p, int T) {
+  const int64_t kt = (int64_t)p->cfg.top_k * T, e = p->cfg.n_experts;
+  if (!p->block_rows2) return moe::TC_DOWN_PAIR;
+  if (kt < 12 * e) return moe::TC_DOWN_PAIR_SHORT;
+  if (kt < 96 * e) return moe::TC_DOWN_PAIR;
+  return moe::TC_DOWN_ONE;
+}
+
+// Tile height of the second block map for T tokens (0: no second map).
+int block_rows2_at(const moe_plan_t *p, int T) {
+  if (!p->block_rows2) return 0;
+  return down_mode(p, T) == moe::TC_DOWN_PAIR_SHORT ? moe::TC_SHORT_ROWS : p->block_rows2;
+}
+
+// Tiles of the second block map a plan's workspace holds: enough for either height.
+int max_tiles2_of(const moe_plan_t *p, int Tmax) {
+  if (!p->block_rows2) return 0;
+  const moe_config &c = p->cfg;
+  int m = tiles_bound(Tmax, c.top_k, c.n_experts, c.n_shared, p->block_rows2);
+  const int t_short = (int)std::min<int64_t>(Tmax, (12 * (int64_t)c.n_experts + c.top_k - 1) / c.top_k);
+  return std::max(m, tiles_bound(t_short, c.top_k, c.n_experts, c.n_shared, moe::TC_SHORT_ROWS));
 }
 
 moe::Layout make_layout(const moe_config &c, int Tmax, int max_tiles, int max_tiles2, bool tc,
@@ -164,12 +199,13 @@ moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const fl
   if (err != cudaSuccess) return cuda_status(err);
   ++*launches;
   const int max_tiles = tiles_bound(T, c.top_k, c.n_experts, c.n_shared, p->block_rows);
-  const int max_tiles2 = p->block_rows2 ? tiles_bound(T, c.top_k, c.n_experts, c.n_shared, p->block_rows2) : 0;
+  const int bn2 = block_rows2_at(p, T);
+  const int max_tiles2 = bn2 ? tiles_bound(T, c.top_k, c.n_experts, c.n_shared, bn2) : 0;
   if ((err = moe::launch_scatter(moe::ws_ptr<int32_t>(ws, L.topk_id), T, c.n_experts, c.top_k, p->block_rows,
                                  c.n_shared, counts, moe::ws_ptr<int32_t>(ws, L.offsets),
                                  moe::ws_ptr<int32_t>(ws, L.perm), moe::ws_ptr<int32_t>(ws, L.inv),
                                  moe::ws_ptr<int32_t>(ws, L.blockmap), moe::ws_ptr<int32_t>(ws, L.n_tiles), max_tiles,
-                                 p->block_rows2, p->block_rows2 ? moe::ws_ptr<int32_t>(ws, L.blockmap2) : nullptr,
+                                 bn2, bn2 ? moe::ws_ptr<int32_t>(ws, L.blockmap2) : nullptr,
                                  moe::ws_ptr<int32_t>(ws, L.n_tiles2), max_tiles2, status,
                                  (p->flags & MOE_FLAG_DEBUG_CHECKS) ? 1 : 0, moe::ws_ptr<int32_t>(ws, L.qctr),
                                  s)) != cudaSuccess)
@@ -307,7 +343,7 @@ moe_status moe_plan(const moe_config *cfg, int32_t max_tokens, uint32_t flags, m
   p->max_tiles = tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows);
   // the tensor-core down GEMM takes tiles of up to TC_DOWN_ROWS rows
   p->block_rows2 = simt ? 0 : ((flags & MOE_FLAG_TILE_ROWS_64) ? 64 : moe::TC_DOWN_ROWS);
-  p->max_tiles2 = p->block_rows2 ? tiles_bound(max_tokens, c.top_k, c.n_experts, c.n_shared, p->block_rows2) : 0;
+  p->max_tiles2 = max_tiles2_of(p, max_tokens);
   p->lay = make_layout(c, max_tokens, p->max_tiles, p->max_tiles2, !simt);
   p->num_sms = 0;
   p->use_router_tc = false;
@@ -480,16 +516,11 @@ static moe_status forward_impl(const moe_plan_t *plan, const void *x_d, const vo
     if (err != cudaSuccess) return cuda_status(err);
     launches += 2;
   } else {
-    const int max_tiles2 = plan->block_rows2 ? tiles_bound(T, c.top_k, c.n_experts, c.n_shared, plan->block_rows2) : 0;
-    // The down GEMM: with few rows per expert (k T / E < 96) two output tiles
-    // per item over the first block map, whose items share their token rows
-    // (measured: T = 256 86 -> 66 us, T = 2048 94 -> 82 us); with more, one
-    // output tile per item over the taller tiles of the second map, whose two
-    // accumulators hide the epilogue (T = 4096: 105 us against 125).
-    const bool down_pair = !plan->block_rows2 || (int64_t)c.top_k * T < (int64_t)96 * c.n_experts;
-    err = moe::launch_experts_tc(plan, x, T, perm, bm, nt, max_tiles,
-                                 down_pair ? nullptr : moe::ws_ptr<int32_t>(ws_d, L.blockmap2),
-                                 moe::ws_ptr<int32_t>(ws_d, L.n_tiles2), max_tiles2, ep, h, y,
+    const int bn2 = block_rows2_at(plan, T);
+    const int max_tiles2 = bn2 ? tiles_bound(T, c.top_k, c.n_experts, c.n_shared, bn2) : 0;
+    err = moe::launch_experts_tc(plan, x, T, perm, bm, nt, max_tiles, down_mode(plan, T),
+                                 moe::ws_ptr<int32_t>(ws_d, L.blockmap2), moe::ws_ptr<int32_t>(ws_d, L.n_tiles2),
+                                 max_tiles2, ep, h, y,
                                  moe::ws_ptr<uint16_t>(ws_d, L.xg), moe::ws_ptr<int32_t>(ws_d, L.qctr),
                                  status,
                                  (plan->flags & MOE_FLAG_TRACE) ? moe::ws_ptr<uint64_t>(ws_d, L.trace) : nullptr,
@@ -615,10 +646,9 @@ moe_status moe_route_view(const moe_plan_t *plan, void *ws_d, int32_t T, moe_rou
   out->block_rows = plan->block_rows;
   out->blockmap2_d = moe::ws_ptr<int32_t>(ws_d, L.blockmap2);
   out->n_tiles2_d = moe::ws_ptr<int32_t>(ws_d, L.n_tiles2);
-  out->max_tiles2 =
-      plan->block_rows2 ? tiles_bound(T, plan->cfg.top_k, plan->cfg.n_experts, plan->cfg.n_shared, plan->block_rows2)
-                        : 0;
-  out->block_rows2 = plan->block_rows2;
+  const int bn2 = block_rows2_at(plan, T);
+  out->max_tiles2 = bn2 ? tiles_bound(T, plan->cfg.top_k, plan->cfg.n_experts, plan->cfg.n_shared, bn2) : 0;
+  out->block_rows2 = bn2;
   return MOE_OK;
 }
 

@@ -12,6 +12,7 @@ namespace moe {
 
 constexpr int TC_ROWS = 128;       // default token rows per block-map tile (gate/up GEMM)
 constexpr int TC_DOWN_ROWS = 192;  // token rows per tile of the down GEMM's block map (two accumulators fit)
+constexpr int TC_SHORT_ROWS = 64;  // the same map's tile height when experts average few rows
 
 // The driver's cuTensorMapEncodeTiled (null when the driver lacks it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
@@ -22,12 +23,15 @@ bool tc_supported(const moe_config &c);
 // One-time kernel attributes (dynamic shared memory size); needs a device.
 cudaError_t tc_prepare();
 
+// The down GEMM's modes (down_mode): one 128-feature output tile per item
+// over blockmap2's taller tiles; two output tiles per item over blockmap;
+// two output tiles per item, two items in flight, over blockmap2's short tiles.
+enum { TC_DOWN_ONE = 0, TC_DOWN_PAIR = 1, TC_DOWN_PAIR_SHORT = 2 };
+
 // qctr: two work-queue counters (gate/up, down), zero at the launch (the
-// scatter kernel of the layer's routing zeroes them).  blockmap2 null: the
-// down GEMM takes two 128-feature output tiles per item over blockmap;
-// otherwise one output tile per item over blockmap2's taller tiles.
+// scatter kernel of the layer's routing zeroes them).
 cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, const int32_t *perm,
-                              const int32_t *blockmap, const int32_t *n_tiles, int max_tiles,
+                              const int32_t *blockmap, const int32_t *n_tiles, int max_tiles, int down_mode,
                               const int32_t *blockmap2, const int32_t *n_tiles2, int max_tiles2, ExpertPtrs w,
                               uint16_t *h, uint16_t *y, uint16_t *xg, int32_t *qctr, int32_t *status,
                               uint64_t *trace, int *launches, cudaStream_t s);

@@ -208,8 +208,11 @@ def test_routing_is_deterministic(real):
 # ---------------------------------------------------------------- layer, tiny dims
 
 def test_default_plan_uses_tensor_core_path():
-    v = Layer(max_tokens=8).view(1)
-    assert (v.block_rows, v.block_rows2) == (128, 192)
+    # the second map's tile height follows the down GEMM's mode for T tokens:
+    # taller tiles from k T / E >= 96, short tiles below 12
+    L = Layer(max_tokens=4096)
+    assert (L.view(4096).block_rows, L.view(4096).block_rows2) == (128, 192)
+    assert L.view(8).block_rows2 == 64
     v = Layer(max_tokens=8, flags=moe.MOE_FLAG_TILE_ROWS_64).view(1)
     assert (v.block_rows, v.block_rows2) == (64, 64)
     v = Layer(max_tokens=8, flags=moe.MOE_FLAG_SIMT_EXPERTS).view(1)
@@ -244,11 +247,15 @@ def test_layer_tiny_dims(path, T):
     assert L.status() == 0
 
 
-@pytest.mark.parametrize("T", [300, 700])
+@pytest.mark.parametrize("T", [40, 300, 700])
 def test_layer_tiny_dims_both_down_modes(T):
-    # k T / E < 96 (T = 300): the down GEMM takes two output tiles per item
-    # over the 128-row map; T = 700: one output tile per item over the
-    # 192-row map, where the skew puts more than 128 rows in a tile
+    # k T / E < 12 (T = 40): the down GEMM takes two output tiles per item,
+    # two items in flight, over the second map cut into 64-row tiles (as do
+    # the tiny-dims tests below T = 48 and the real-dims T = 256 tests, whose
+    # shared expert spans four such tiles); k T / E < 96 (T = 300):
+    # two output tiles per item over the 128-row map; T = 700: one output
+    # tile per item over the 192-row map, where the skew puts more than 128
+    # rows in a tile
     d, W, Wd = _tiny(500 + T)
     x = syn.activations(500 + T, T, d["H"])
     bias = syn.zipf_bias(500 + T, d["E"])
@@ -257,8 +264,10 @@ def test_layer_tiny_dims_both_down_modes(T):
     r = L.routing(T)
     if T == 700:
         assert d["k"] * T >= 96 * d["E"] and (r["blockmap2"][:, 2] > 128).any()
-    else:
+    elif T == 300:
         assert d["k"] * T < 96 * d["E"] and (r["blockmap"][:, 2] > 64).any()
+    else:
+        assert d["k"] * T < 12 * d["E"] and r["block_rows2"] == 64 and (r["blockmap2"][:, 2] <= 64).all()
     ref = orc.moe_layer(orc.Dims(**d, n_shared=1), x, W, bias=bias, keys=r["keys"], intermediates=True)
     assert_outputs_close(out, ref, f"tiny T={T} down modes", k=d["k"])
     assert L.status() == 0
