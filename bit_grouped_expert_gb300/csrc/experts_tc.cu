@@ -126,6 +126,10 @@ struct TcArgs {
   int32_t *status;
   int T, k, E, K, NOUT;           // K: reduction length; NOUT: output features per expert
   int tma_scales;                 // scales/biases staged by TMA (K % 512 == 0)
+  // The block map's last `first` tiles (the shared expert's: with few tokens
+  // per routed expert, the largest) are handed out before the others, so the
+  // items that finish last are short ones.
+  int first;
   // Optional wait accounting (tracing aid): per CTA, cycles each role spent
   // in its barrier waits and in total, at trace[cta * 32 + trace_base + i].
   uint64_t *trace;
@@ -174,12 +178,15 @@ struct Item {
   int e, row0, nrows, n_mma, mt;
 };
 
-// Block-map entry of item number `item` as a ring entry.
+// Block-map entry of item number `item` (of n_tiles * MT) as a ring entry;
+// items count from the map's last a.first tiles, then from its start.
 template <int MAXN>
-__device__ __forceinline__ int4 item_entry(const TcArgs &a, int item, int MT) {
-  const int tile = item / MT;
+__device__ __forceinline__ int4 item_entry(const TcArgs &a, int item, int MT, int n_tiles) {
+  const int t = item / MT;
+  const int first = a.first < n_tiles ? a.first : n_tiles;
+  const int tile = t < first ? n_tiles - first + t : t - first;
   const int4 ent = reinterpret_cast<const int4 *>(a.blockmap)[tile];
-  return make_int4(ent.x, ent.y, min(ent.z, MAXN), item - tile * MT);
+  return make_int4(ent.x, ent.y, min(ent.z, MAXN), item - t * MT);
 }
 
 __device__ __forceinline__ Item as_item(int4 ent) {
@@ -312,7 +319,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int MT = a.NOUT / (PAIR ? 2 * BM : BM);  // items per block-map tile
   const int KB = a.K / KBLK;  // a multiple of NSLOT (K % 256 == 0)
   const int NST = (KB + STAGE_KB - 1) / STAGE_KB;
-  const int n_items = (*a.n_tiles) * MT;
+  const int n_tiles = *a.n_tiles;
+  const int n_items = n_tiles * MT;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (codes, scales)
@@ -343,7 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         return i;
       };
       int idx2 = draw();
-      int4 nxt = idx2 < n_items ? item_entry<C::MAXN>(a, idx2, MT) : make_int4(-1, 0, 0, 0);
+      int4 nxt = idx2 < n_items ? item_entry<C::MAXN>(a, idx2, MT, n_tiles) : make_int4(-1, 0, 0, 0);
       idx2 = nxt.x < 0 ? n_items : draw();
       for (uint32_t n = 0; ok; ++n) {
         // the next item, posted to the ring before its codes
@@ -353,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         m->item[s] = ent;
         ptx::mbar_arrive(&m->item_full[s]);
         if (ent.x < 0) break;
-        nxt = idx2 < n_items ? item_entry<C::MAXN>(a, idx2, MT) : make_int4(-1, 0, 0, 0);
+        nxt = idx2 < n_items ? item_entry<C::MAXN>(a, idx2, MT, n_tiles) : make_int4(-1, 0, 0, 0);
         if (nxt.x >= 0) idx2 = draw();
         const Item it = as_item(ent);
         for (int st = 0; st < NST; ++st, ++cs) {
@@ -915,6 +923,7 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.K = c.hidden;
   a.NOUT = c.inter;
   a.tma_scales = ts_gu;
+  a.first = c.n_shared ? (T + plan->block_rows - 1) / plan->block_rows : 0;
   int items = max_tiles * (c.inter / BM);
   int grid = items < plan->num_sms ? items : plan->num_sms;
   const bool gu_quiet = prof_quiet(MOE_KERNEL_GATEUP);
@@ -939,6 +948,10 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.K = c.inter;
   a.NOUT = c.hidden;
   a.tma_scales = ts_dn;
+  {
+    const int bn = first_map ? plan->block_rows : down_mode == TC_DOWN_PAIR_SHORT ? TC_SHORT_ROWS : plan->block_rows2;
+    a.first = c.n_shared ? (T + bn - 1) / bn : 0;
+  }
   items = (first_map ? max_tiles : max_tiles2) * (c.hidden / ((pair ? 2 : 1) * BM));
   grid = items < plan->num_sms ? items : plan->num_sms;
   const bool dn_pdl = gu_quiet && prof_quiet(MOE_KERNEL_DOWN);
