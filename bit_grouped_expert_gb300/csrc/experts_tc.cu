@@ -7,11 +7,10 @@
 // rows of one expert).
 //
 // One persistent CTA per SM takes work items (block-map tile, 128 output
-// features): the code producer draws the next item number -- gate/up: from a
-// queue, a global counter zeroed by the scatter kernel before every layer, so
-// the SMs stay busy to the end whatever the tiles' sizes; down: round-robin --
-// and hands its block-map entry to the CTA's other roles through a ring in
-// shared memory.  The packed weights are the MMA's A operand (M = 128 rows of
+// features): the code producer draws the next item number from a queue (a
+// global counter per GEMM, zeroed by the scatter kernel before every layer),
+// so the SMs stay busy to the end whatever the tiles' sizes, and hands its
+// block-map entry to the CTA's other roles through a ring in shared memory.  The packed weights are the MMA's A operand (M = 128 rows of
 // output features) and the tile's token rows are B (N = rows rounded up to
 // 16), so a weight tile is rebuilt once for all of an expert's tokens:
 //   warp 0      TMA: packed 4-bit codes, 128 rows x 256 codes per box, 128B
@@ -341,8 +340,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // the counter's and the block map's round trips overlap earlier work:
       // nxt = the next item's entry, idx2 = the number after it.
       // With a.item_counter null the items go round-robin instead (item
-      // number blockIdx.x + n * gridDim.x), which served the down GEMM's
-      // short items better than the queue in measurements.
+      // number blockIdx.x + n * gridDim.x).
       int stat = blockIdx.x;
       auto draw = [&]() {
         if (a.item_counter) return atomicAdd(a.item_counter, 1);
@@ -939,7 +937,7 @@ cudaError_t launch_experts_tc(const moe_plan_t *plan, const uint16_t *x, int T, 
   a.trace_base = 16;
   a.blockmap = first_map ? blockmap : blockmap2;
   a.n_tiles = first_map ? n_tiles : n_tiles2;
-  a.item_counter = nullptr;  // round-robin (qctr[1] stays unused)
+  a.item_counter = qctr + 1;  // down's queue (the scatter kernel zeroed it)
   a.sc[0] = w.down_s;
   a.bi[0] = w.down_b;
   a.sc[1] = w.down_s;
