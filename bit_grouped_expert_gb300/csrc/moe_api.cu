@@ -171,15 +171,20 @@ moe_status enqueue_route(const moe_plan_t *p, const uint16_t *x, int T, const fl
   int32_t *status = moe::ws_ptr<int32_t>(ws, L.status);
   int32_t *counts = moe::ws_ptr<int32_t>(ws, L.counts);
   const size_t chunks = ((size_t)T * c.top_k + moe::SCATTER_ENT - 1) / moe::SCATTER_ENT;
-  cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts * (1 + chunks), s);
-  if (err != cudaSuccess) return cuda_status(err);
+  const int n_counts = (int)(c.n_experts * (1 + chunks));
+  // the tensor-core router zeroes the histograms itself (no memset between
+  // the kernels); every other path clears them here
+  const bool tc_router = from == RouteFrom::kX && p->use_router_tc && T >= moe::ROUTER_TC_MIN_T;
+  cudaError_t err = cudaSuccess;
+  if (!tc_router && (err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * n_counts, s)) != cudaSuccess)
+    return cuda_status(err);
   const float *part = nullptr;  // the tensor-core router's K-slice partial sums, when it splits K
   int ks = 0;
   if (from == RouteFrom::kX) {
-    if (p->use_router_tc && T >= moe::ROUTER_TC_MIN_T) {
+    if (tc_router) {
       err = moe::launch_router_tc(x, T, c.hidden, router, c.n_experts, bias, split,
                                   moe::ws_ptr<uint16_t>(ws, L.rsplit), moe::ws_ptr<float>(ws, L.rpart), keys, status,
-                                  p->num_sms, &ks, launches, s);
+                                  counts, n_counts, p->num_sms, &ks, launches, s);
       if (err != cudaSuccess) return cuda_status(err);
       if (ks > 1) part = moe::ws_ptr<float>(ws, L.rpart);
     } else {

@@ -262,7 +262,13 @@ __global__ void __launch_bounds__(SCATTER_THREADS) scatter_kernel(
   __syncthreads();
   for (int e = tid; e < E; e += SCATTER_THREADS) {  // starts: the experts' pairs in earlier chunks and warps
     int run = s_off[e];
-    for (int c = 0; c < b; ++c) run += counts[(size_t)E + (size_t)c * E + e];
+    for (int c0 = 0; c0 < b; c0 += 16) {  // earlier chunks' counts, sixteen loads in flight at a time
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = c0 + i < b ? counts[(size_t)E + (size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) run += v[i];
+    }
 #pragma unroll
     for (int w = 0; w < SCATTER_WARPS; ++w) {
       const int x = s_hist[w * E + e];

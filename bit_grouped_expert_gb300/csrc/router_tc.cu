@@ -47,6 +47,8 @@ struct RArgs {
   const float *bias;  // added when KS == 1 (else by the top-k kernel, after the slices)
   int32_t *status;
   int T, E, H, N, KS;
+  int32_t *zero;  // nzero ints set to 0 (the top-k's histograms), or null
+  int nzero;
 };
 
 struct RMisc {
@@ -138,6 +140,11 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // launched as a programmatic dependent of the kernel before it (which may
+  // write x): everything above overlapped its tail, nothing below does
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = blockIdx.x * RTHREADS + threadIdx.x; i < a.nzero; i += gridDim.x * RTHREADS) a.zero[i] = 0;
   const uint32_t tmem = m->tmem;
   const int MT = a.E / RM;
   const int n_items = ((a.T + a.N - 1) / a.N) * MT * a.KS;
@@ -291,7 +298,9 @@ cudaError_t launch_router_split(const float *router, int E, int H, uint16_t *spl
 
 cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
                              const uint16_t *split_given, uint16_t *split, float *partial, float *keys,
-                             int32_t *status, int num_sms, int *ks_out, int *launches, cudaStream_t s) {
+                             int32_t *status, int32_t *zero, int nzero, int num_sms, int *ks_out, int *launches,
+                             cudaStream_t s) {
+  const bool pdl = prof_chain(MOE_KERNEL_ROUTER);  // a dependent of the kernel before it (not of the split)
   prof_before(MOE_KERNEL_ROUTER, s);
   cudaError_t e = cudaSuccess;
   if (split_given) {
@@ -304,10 +313,12 @@ cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *route
   CUtensorMap ta, tb;
   if ((e = bf16_map(&ta, split, 3 * E, H, RM)) != cudaSuccess) return e;
   if ((e = bf16_map(&tb, x, T, H, N)) != cudaSuccess) return e;
-  RArgs a{KS > 1 ? partial : keys, bias, status, T, E, H, N, KS};
+  RArgs a{KS > 1 ? partial : keys, bias, status, T, E, H, N, KS, zero, zero ? nzero : 0};
   const int items = ((T + N - 1) / N) * (E / RM) * KS;
-  router_tc_kernel<<<items < num_sms ? items : num_sms, RTHREADS, R_SMEM, s>>>(ta, tb, a);
+  e = launch_dep(pdl && split_given != nullptr, router_tc_kernel, dim3(items < num_sms ? items : num_sms),
+                 dim3(RTHREADS), R_SMEM, s, ta, tb, a);
   prof_after(MOE_KERNEL_ROUTER, s);
+  if (e != cudaSuccess) return e;
   ++*launches;
   *ks_out = KS;
   return cudaGetLastError();

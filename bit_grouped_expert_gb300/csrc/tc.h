@@ -51,10 +51,15 @@ cudaError_t launch_router_split(const float *router, int E, int H, uint16_t *spl
 // router_tc_partial_floats floats (16-byte aligned).  *ks_out = the K slices
 // used: with 1 the keys (bias added) are in keys; with more, partial holds
 // [KS][T][E] fp32 sums that the top-k kernel adds in slice order (+ bias).
+// zero (or null): nzero ints the kernel sets to 0 before any of its own work
+// (the top-k's histograms, so that no memset sits between the kernels).  The
+// kernel starts as a programmatic dependent of the kernel before it in the
+// stream and waits for it before touching memory.
 // *launches counts the kernels enqueued.
 cudaError_t launch_router_tc(const uint16_t *x, int T, int H, const float *router, int E, const float *bias,
                              const uint16_t *split_given, uint16_t *split, float *partial, float *keys,
-                             int32_t *status, int num_sms, int *ks_out, int *launches, cudaStream_t s);
+                             int32_t *status, int32_t *zero, int nzero, int num_sms, int *ks_out, int *launches,
+                             cudaStream_t s);
 constexpr int ROUTER_TC_MIN_T = 32;  // below this the CUDA-core router is used
 
 }  // namespace moe
