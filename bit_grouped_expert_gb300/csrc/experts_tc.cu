@@ -52,6 +52,7 @@ constexpr int KBLK = 64;        // k-block = one quantisation group
 constexpr int STAGE_KB = 4;     // k-blocks per code stage (one TMA box per matrix)
 constexpr int BOX = BM * 128;   // one TMA box: 128 rows x 128 bytes (256 codes)
 constexpr int NSLOT = 4;        // k-block ring: A slots in tensor memory (64 columns each) + token-row slots
+static_assert(STAGE_KB <= NSLOT, "an item's first code stage must fit the k-block ring (deferred epilogue)");
 constexpr int NISS = 2;         // MMA-issuing threads (warps 1 and 3)
 constexpr int NWG = 3;                    // dequant/epilogue warpgroups
 constexpr int THREADS = 128 + NWG * 128;  // 4 role warps + the warpgroups
@@ -690,22 +691,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&m->code_empty[cslot]);
         if (!ok) break;
+        // With one accumulator the previous item's epilogue runs once this
+        // item's first stage is rebuilt: those k-blocks' ring slots were
+        // freed by the previous item's MMAs (a stage fits the ring), so the
+        // MMA finds them ready the moment the accumulator comes back.
+        if (C::NBUF == 1 && st == 0 && has_prev) {
+          if (!epilogue(prev, itc - 1)) break;
+          has_prev = false;
+        }
       }
       if (!ok) break;
       // With two accumulators the epilogue of an item runs after the next
       // item's k-blocks have been rebuilt (the MMA has long finished it by
-      // then); with one, right away (the next item's MMAs need the
-      // accumulator back).
-      if (C::NBUF == 1) {
-        if (!epilogue(it, itc)) break;
-      } else {
-        if (has_prev && !epilogue(prev, itc - 1)) break;
-        prev = it;
-        has_prev = true;
-      }
+      // then).
+      if (C::NBUF == 2 && has_prev && !epilogue(prev, itc - 1)) break;
+      prev = it;
+      has_prev = true;
       ++itc;
     }
-    if (C::NBUF == 2 && ok && has_prev) epilogue(prev, itc - 1);
+    if (ok && has_prev) epilogue(prev, itc - 1);
     if (lane == 0) ptx::bulk_wait_all();  // the epilogue's stores have landed
     if (tr) {
       trace_put(a, TW_DQ_CODE, w_code);
