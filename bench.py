@@ -51,9 +51,9 @@ ROUTER_BYTES = E * H * 4                                              # 2,097,15
 # where no capture of that workload exists.  Update with every kernel change.
 TRAFFIC = {
     # gate/up + down, one launch each (the roofline kernel pair of the prefill lines)
-    "layer256": 475_129_600,      # profiles/grouped_experts_tc_layer256.md
-    "layer4096": 783_452_160,     # profiles/grouped_experts_tc_layer4096.md
-    "prefill32k": 783_452_160,    # every 4096-token chunk-layer is the layer4096 launch pair
+    "layer256": 475_237_376,      # profiles/grouped_experts_tc_layer256.md
+    "layer4096": 784_453_120,     # profiles/grouped_experts_tc_layer4096.md
+    "prefill32k": 784_453_120,    # every 4096-token chunk-layer is the layer4096 launch pair
     "decode40": 127_976_576,      # decode_layer_kernel, 7 layers; profiles/decode_layer_decode40.md
     "gdn2k": 36_231_706,          # gdn_scan_kernel, profiles/gdn_scan_gdn2k.md
     "attn32k": 67_307_776,        # attn_block_kernel, profiles/attn_block_attn128k.md
