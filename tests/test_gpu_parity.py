@@ -191,6 +191,24 @@ def test_routing_spans_scatter_chunks(E, k, T):
     assert L.status() == 0
 
 
+@pytest.mark.parametrize("T", [16, 300, 4096])
+def test_routing_resets_between_calls(real, T):
+    # a second call on the same workspace routes only its own tokens: the
+    # histograms start from zero each call (cleared by a memset below 32
+    # tokens, by the tensor-core router itself above), so the counts, the
+    # offsets and the maps match the oracle for the second input alone
+    W, Wd = real
+    L = Layer(max_tokens=T)
+    for seed in (21, 22):
+        x = syn.activations(seed, T, 2048)
+        moe.moe_route(L.plan, dev(x), T, Wd["router"], None, L.ws)
+        torch.cuda.synchronize()
+    got = L.routing(T)
+    _assert_routing_equal(got, got["keys"], 8, 256, 1)
+    assert int(got["counts"].sum()) == 8 * T
+    assert L.status() == 0
+
+
 def test_routing_is_deterministic(real):
     W, Wd = real
     T = 512
