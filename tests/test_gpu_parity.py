@@ -393,6 +393,27 @@ def test_layer_t512_zipf_sampled(real):
     assert_outputs_close(out[rows], ref, "T=512 zipf sample")
 
 
+@pytest.mark.parametrize("T", [512, 4096])
+def test_layer_all_tokens_to_eight_experts(real, T):
+    # the degenerate routing: a bias that puts experts 0..7 first for every
+    # token, so eight experts take all T rows each (several full tiles, over
+    # the down GEMM's taller tiles at T = 4096) and the other 248 none
+    W, Wd = real
+    x = syn.activations(5, T, 2048)
+    bias = np.zeros(256, np.float32)
+    bias[:8] = 50.0
+    L = Layer(max_tokens=T)
+    out = _forward(L, x, Wd, bias=bias)
+    r = L.routing(T)
+    np.testing.assert_array_equal(r["counts"][:8], np.full(8, T))
+    assert int(r["counts"][8:].sum()) == 0
+    _assert_routing_equal(r, r["keys"], 8, 256, 1)
+    rows = np.random.default_rng(1).choice(T, 40, replace=False)
+    ref = orc.moe_layer(orc.Dims(), x[rows], W, keys=r["keys"][rows], intermediates=True)
+    assert_outputs_close(out[rows], ref, f"T={T}, every token to experts 0..7")
+    assert L.status() == 0
+
+
 # ---------------------------------------------------------------- decode path
 
 def test_decode_t1_matches_oracle_and_grouped(real):
