@@ -619,21 +619,37 @@ def run_gdn(args, wl, rank, world, device):
                 "kernel_ms": round(dom_ms, 5),
                 "peak_src": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2070 MHz"}
     # end to end: each step copies its inputs from pinned host memory, scans,
-    # and copies the outputs back
+    # and copies the outputs back.  Two buffer sets alternate, so a step's
+    # copies (on their own streams) overlap the neighbouring steps' scans.
     pinned = [{n: torch.from_numpy(np.ascontiguousarray(a).view(np.int16 if a.dtype == np.uint16 else a.dtype))
                .pin_memory() for n, a in h.items() if n != "state"} for h in host[:2]]
-    host_o = torch.empty((T, Hv, dv), dtype=torch.int16).pin_memory()
+    host_o = [torch.empty((T, Hv, dv), dtype=torch.int16).pin_memory() for _ in range(2)]
     h2d = sum(a.numel() * a.element_size() for a in pinned[0].values())
-    e2e_steps = min(args.steps, 10)
+    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    out_read = [torch.cuda.Event() for _ in range(2)]
+    e2e_steps = min(args.steps, 50)
     torch.cuda.synchronize()
     te = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(e2e_steps):
-            b = i % 2
+    for i in range(e2e_steps):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(done[b])  # step i-2's scan has read this input set
             for n, a in pinned[b].items():
                 sets[b][n].copy_(a, non_blocking=True)
+            in_ready[b].record(s_in)
+        stream.wait_event(in_ready[b])
+        if i >= 2:
+            stream.wait_event(out_read[b])  # step i-2's output has been copied out
+        with torch.cuda.stream(stream):
             graphs[b].replay()
-            host_o.copy_(outs[b], non_blocking=True)
+            done[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[b])
+            host_o[b].copy_(outs[b], non_blocking=True)
+            out_read[b].record(s_out)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - te
     e2e = {"value": T * e2e_steps / e2e_s * world, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -722,18 +738,26 @@ def run_attn(args, wl, rank, world, device):
                 "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": TRAFFIC.get(args.workload),
                 "kernel": "attn_block_kernel (one block of positions per SM, 8 query heads per KV row read)",
                 "kernel_ms": round(dom_ms, 5), "peak_src": pk["src"]}
-    # end to end: the query in from pinned host memory, the output back
+    # end to end: every step copies the query in from pinned host memory and
+    # the output back, both captured with the attention call into one graph
+    # per buffer set (the copies are 8 KB; a step is tens of microseconds, so
+    # per-step stream bookkeeping on the host would cost more than the step)
     host_q = torch.from_numpy(np.ascontiguousarray(host[0]["q"]).view(np.int16)).pin_memory()
-    host_o = torch.empty((Hq, D), dtype=torch.int16).pin_memory()
-    e2e_steps = min(args.steps, 100)
+    host_o = [torch.empty((Hq, D), dtype=torch.int16).pin_memory() for _ in range(2)]
+    e2e_graphs = []
+    for b in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            sets[b]["q"].copy_(host_q, non_blocking=True)
+            body(b)
+            host_o[b].copy_(outs[b], non_blocking=True)
+        e2e_graphs.append(g)
+    e2e_steps = min(args.steps, 2000)
     torch.cuda.synchronize()
     te = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(e2e_steps):
-            b = i % n_sets
-            sets[b]["q"].copy_(host_q, non_blocking=True)
-            graphs[b].replay()
-            host_o.copy_(outs[b], non_blocking=True)
+            e2e_graphs[i & 1].replay()
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - te
     e2e = {"value": kv_bytes * e2e_steps / e2e_s / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": Hq * D * 2,
